@@ -1,0 +1,91 @@
+"""Seeded synthetic inputs for D = A * B^T (fp16 A: M x K, fp16 B: N x K).
+
+This module draws inputs and nothing else: it holds none of the GEMM's
+arithmetic, so both the CUDA path's tests and the CPU oracle can be fed from it.
+
+Each workload fixes a shape, a value distribution and a seed.  Values are drawn
+in float32 from one ``torch.Generator`` on the CPU, A first and then B, and are
+rounded to fp16 by the ordinary float32 -> fp16 conversion:
+
+* ``uniform``: i.i.d. uniform on [-1, 1]  (``rand * 2 - 1``)
+* ``normal``:  i.i.d. normal(0, 1) times ``scale``  (``randn * scale``)
+
+The shapes are the ones the GEMM pages use (a single 128 x 128 x 64 tile, as in
+Step 1 of "TIRx 与高性能GEMM (上)") plus square, ragged and MLP-projection
+shapes of the size a linear layer has.  torch's CPU generator may produce
+different streams on different CPU architectures, so expected values are
+always computed on the machine that runs the comparison, never stored.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+    a_dist: str
+    a_scale: float
+    b_dist: str
+    b_scale: float
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def min_bytes(self) -> int:
+        """Bytes that must cross HBM at least once: read A and B, write D (fp16)."""
+        return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
+
+
+def _normal_over_sqrt_k(name, M, N, K, seed):
+    s = 1.0 / math.sqrt(K)
+    return Workload(name, M, N, K, seed, "normal", s, "normal", s)
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("single_tile_128x128x64", 128, 128, 64, 0, "uniform", 1.0, "uniform", 1.0),
+        _normal_over_sqrt_k("square_2048", 2048, 2048, 2048, 1),
+        Workload("ragged_3000x5000x1000", 3000, 5000, 1000, 2, "uniform", 1.0, "uniform", 1.0),
+        _normal_over_sqrt_k("square_8192", 8192, 8192, 8192, 3),
+        # MLP up-projection: 16384 tokens, hidden 4096 -> 14336; weights normal(0, 1/sqrt(4096)).
+        Workload("mlp_up_16384x14336x4096", 16384, 14336, 4096, 4, "normal", 1.0, "normal",
+                 1.0 / 64.0),
+    ]
+}
+
+ORDER = list(WORKLOADS)
+
+
+def _draw(gen: torch.Generator, shape, dist: str, scale: float) -> torch.Tensor:
+    if dist == "uniform":
+        x = torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    elif dist == "normal":
+        x = torch.randn(shape, generator=gen, dtype=torch.float32) * scale
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    return x.to(torch.float16)
+
+
+def make_inputs(M: int, N: int, K: int, seed: int, a_dist: str = "uniform",
+                a_scale: float = 1.0, b_dist: str = "uniform", b_scale: float = 1.0):
+    """(A, B) as contiguous CPU fp16 tensors of shapes (M, K) and (N, K)."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    A = _draw(gen, (M, K), a_dist, a_scale)
+    B = _draw(gen, (N, K), b_dist, b_scale)
+    return A.contiguous(), B.contiguous()
+
+
+def workload_inputs(w: Workload):
+    return make_inputs(w.M, w.N, w.K, w.seed, w.a_dist, w.a_scale, w.b_dist, w.b_scale)

@@ -1,0 +1,149 @@
+"""The CPU oracle for D = A * B^T (fp16 in, binary64 sum).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product package imports, loads or
+runs this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may.  The library path fails loudly when its CUDA
+extension is missing; it never falls back to this code.
+
+The arithmetic lives in ``gemm_ref.c`` (plain C, binary64, OpenMP over output
+rows), written from the definition D[i][j] = sum_k A[i][k] * B[j][k] on the
+page "TIRx 与高性能GEMM (上)" (section "从 GEMM 公式到数据路径") and from the
+IEEE 754 binary16 format.  This file only builds that C file with gcc and
+marshals numpy arrays through ctypes.
+
+Pins: ``tests/test_oracle.py`` checks every function here against values fixed
+by the pages and by mathematics (all-ones, identity, permutation, rank-one
+probes, exact rational brute force, exhaustive binary16 round trips, library
+conversions).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_ref.c")
+_LIB = os.path.join(_HERE, "liboracle_gemm.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gemm_ref.c`` into ``liboracle_gemm.so`` next to it (gcc, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-Wall", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, u16p, f64p, i64p = (ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p)
+            lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_f16_to_f64.restype = ctypes.c_double
+            lib.oracle_f64_to_f16.argtypes = [ctypes.c_double]
+            lib.oracle_f64_to_f16.restype = ctypes.c_uint16
+            lib.oracle_decode_f16.argtypes = [u16p, f64p, i64]
+            lib.oracle_decode_f16.restype = None
+            lib.oracle_round_f16.argtypes = [f64p, u16p, i64]
+            lib.oracle_round_f16.restype = None
+            lib.oracle_gemm_f64.argtypes = [u16p, u16p, f64p, i64, i64, i64]
+            lib.oracle_gemm_f64.restype = ctypes.c_int
+            lib.oracle_gemm_f64_sampled.argtypes = [u16p, u16p, i64, i64, i64, i64p, i64p,
+                                                    i64, f64p]
+            lib.oracle_gemm_f64_sampled.restype = None
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _as_u16(x) -> np.ndarray:
+    """fp16 array (numpy float16/uint16 or a CPU torch tensor) -> contiguous uint16 view."""
+    if hasattr(x, "detach"):  # a torch tensor: reinterpret its bits without arithmetic
+        x = x.detach().cpu().contiguous().view(dtype=__import__("torch").int16).numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16 or x.dtype == np.int16:
+        x = x.view(np.uint16)
+    if x.dtype != np.uint16:
+        raise TypeError(f"expected fp16 bits, got {x.dtype}")
+    return x
+
+
+def f16_bits_to_f64(bits) -> np.ndarray:
+    """binary16 bit patterns -> binary64 values (exact widening)."""
+    b = _as_u16(bits)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_decode_f16(b.ctypes.data, out.ctypes.data, b.size)
+    return out
+
+
+def f64_to_f16_bits(x) -> np.ndarray:
+    """binary64 values -> binary16 bit patterns, round to nearest, ties to even."""
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_round_f16(v.ctypes.data, out.ctypes.data, v.size)
+    return out
+
+
+def gemm_f64(A, B) -> np.ndarray:
+    """D64 = A * B^T summed in binary64.  A: (M, K) fp16, B: (N, K) fp16."""
+    a, b = _as_u16(A), _as_u16(B)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError(f"shapes {a.shape} and {b.shape} do not contract")
+    M, K = a.shape
+    N = b.shape[0]
+    out = np.empty((M, N), dtype=np.float64)
+    if _load().oracle_gemm_f64(a.ctypes.data, b.ctypes.data, out.ctypes.data, M, N, K) != 0:
+        raise MemoryError("oracle could not allocate its binary64 copies")
+    return out
+
+
+def gemm_f16(A, B) -> np.ndarray:
+    """The fp16 output value: RNE(A * B^T), as binary16 bit patterns (uint16)."""
+    return f64_to_f16_bits(gemm_f64(A, B))
+
+
+def gemm_f64_sampled(A, B, rows, cols) -> np.ndarray:
+    """D64[rows[t], cols[t]] for each t, each an independent binary64 dot product."""
+    a, b = _as_u16(A), _as_u16(B)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError(f"shapes {a.shape} and {b.shape} do not contract")
+    M, K = a.shape
+    N = b.shape[0]
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.shape != c.shape:
+        raise ValueError("rows and cols differ in length")
+    if r.size and (r.min() < 0 or r.max() >= M or c.min() < 0 or c.max() >= N):
+        raise IndexError("sample index out of range")
+    out = np.empty(r.shape, dtype=np.float64)
+    _load().oracle_gemm_f64_sampled(a.ctypes.data, b.ctypes.data, M, N, K, r.ctypes.data,
+                                    c.ctypes.data, r.size, out.ctypes.data)
+    return out
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(_load().oracle_num_threads())
+
+
+def tolerance(d_ref: np.ndarray, K: int) -> np.ndarray:
+    """Per-element bound |D_gpu - D_ref| <= 1e-3 * sqrt(K) + 2^-10 * |D_ref|.
+
+    D_ref is the binary64 sum (unrounded).  The bound's absolute term covers the
+    fp32 accumulation of K terms of size O(1/sqrt(K)) to O(1); its relative term
+    covers the final fp16 rounding (at most 2^-11 relative) with a factor of two
+    to spare.
+    """
+    return 1e-3 * np.sqrt(float(K)) + np.abs(d_ref) * 2.0 ** -10
