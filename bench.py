@@ -1,0 +1,418 @@
+#!/usr/bin/env python
+"""Throughput of the fp16 GEMM D = A * B^T on GB300.
+
+One step = one pass of the hot path over one batch of synthetic input: the 8192^3 GEMM and the
+MLP up-projection GEMM (M 16384, N 14336, K 4096), inputs resident in HBM.  The line reports
+fp16 GEMM TFLOP/s over both (total algorithmic FLOPs 2*M*N*K / total time) with a breakdown per
+shape, the dominant kernel's roofline, an end-to-end figure with host copies, clocks sampled
+during the timed region, and the CPU oracle's throughput on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun), every rank runs its own replica of the step on its own GPU (the GEMM
+here has no exchange step), the timed region is bracketed by barriers and the maximum time over
+ranks is used: value = FLOPs of all ranks / that time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fp16 GEMM TFLOP/s at 8192³ and MLP shape; % of GB300 dense fp16 peak"
+WORKLOADS = ("square_8192", "mlp_up_16384x14336x4096")
+FALLBACK_PEAK_TFLOPS = 1900.0
+L2_BYTES = 129e6
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--variant", type=int, default=0, help="kernel variant (0 = auto)")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "blackwell_tensor_core_fp16_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0) or 0), "measured"
+    except Exception:
+        return FALLBACK_PEAK_TFLOPS, 1700.0, "fallback"
+
+
+def recorded_traffic(variant_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_src_sha256") != kernel_source_hash():
+        return None
+    return d.get("per_launch_dram_bytes", {}).get(variant_name)
+
+
+# ---- clocks --------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid: str | None):
+        self.proc = None
+        self.uuid = device_uuid
+        self.out_path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.fh = open(self.out_path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.out_path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 8:
+                rows.append(parts)
+        os.unlink(self.out_path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---- CPU oracle sample ----------------------------------------------------------------------
+
+def oracle_sample(inputs, seconds_target, rng_seed=0):
+    """Time the oracle on random output elements of each GEMM, sized to ~seconds_target.
+    Returns (flops, seconds, description)."""
+    import numpy as np
+    import oracle
+
+    rng = np.random.default_rng(rng_seed)
+    total_flops = 0.0
+    total_s = 0.0
+    desc = []
+    per = seconds_target / len(inputs)
+    for name, (A, B) in inputs.items():
+        M, K = A.shape
+        N = B.shape[0]
+        # calibrate on a small batch, then size the timed sample
+        n0 = 256
+        r = rng.integers(0, M, n0)
+        c = rng.integers(0, N, n0)
+        t = time.perf_counter()
+        oracle.gemm_f64_sampled(A, B, r, c)
+        dt = max(time.perf_counter() - t, 1e-6)
+        count = max(64, int(n0 * per / dt))
+        r = rng.integers(0, M, count)
+        c = rng.integers(0, N, count)
+        t = time.perf_counter()
+        oracle.gemm_f64_sampled(A, B, r, c)
+        dt = time.perf_counter() - t
+        total_flops += 2.0 * K * count
+        total_s += dt
+        desc.append(f"{count} random output elements of {name} ({M}x{N}x{K})")
+    return total_flops, total_s, "; ".join(desc)
+
+
+def host_inputs():
+    from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS as W, workload_inputs
+    return {n: workload_inputs(W[n]) for n in WORKLOADS}
+
+
+# ---- reference arm: the oracle, timed on host cores -------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS as W
+
+    oracle.build()
+    inputs = host_inputs()
+    per_step = min(0.25, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(inputs, per_step, rng_seed=1)
+    flops = secs = 0.0
+    desc = ""
+    for s in range(args.steps):
+        f, t, desc = oracle_sample(inputs, per_step, rng_seed=100 + s)
+        flops += f
+        secs += t
+    value = flops / secs / 1e12
+    cfg = {"workload": "+".join(WORKLOADS),
+           "shapes": [[W[n].M, W[n].N, W[n].K] for n in WORKLOADS]}
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"per step, {desc} (binary64 dot products)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- our arm ---------------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import blackwell_tensor_core_fp16_gb300 as g
+    from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS as W
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    g.build()
+    g.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    props = torch.cuda.get_device_properties(dev)
+    num_sms = props.multi_processor_count
+
+    inputs = host_inputs()
+    work = []
+    for n in WORKLOADS:
+        w = W[n]
+        A, B = inputs[n]
+        Ad, Bd = A.to(dev), B.to(dev)
+        D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+        variant = args.variant or g.gemm_f16_choose_variant(w.M, w.N, w.K, num_sms)
+        work.append((w, Ad, Bd, D, variant))
+    torch.cuda.synchronize()
+
+    def launch(item):
+        w, Ad, Bd, D, variant = item
+        rc = g.gemm_f16_nt_variant(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), w.M, w.N, w.K, sh,
+                                   variant)
+        if rc != g.OK:
+            raise g.GemmError(rc, g.gemm_f16_last_error())
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for item in work:
+                launch(item)
+    torch.cuda.synchronize()
+    g.check_status(stream)
+
+    # timed region: events between launches on the launching stream
+    K = args.steps
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(len(work) * K + 1)]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        events[0].record(stream)
+        e = 1
+        for _ in range(K):
+            for item in work:
+                launch(item)
+                events[e].record(stream)
+                e += 1
+    torch.cuda.synchronize()
+    barrier()
+    wall_s = time.perf_counter() - t_wall
+    clock_info = clocks.stop()
+    g.check_status(stream)
+
+    durs = [events[i].elapsed_time(events[i + 1]) for i in range(len(events) - 1)]
+    total_ms = events[0].elapsed_time(events[-1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops_step = sum(2.0 * w.M * w.N * w.K for (w, *_rest) in work)
+    value = world * K * flops_step / (total_ms * 1e-3) / 1e12
+
+    per = {}
+    kernel_ms_total = 0.0
+    for j, (w, _, _, _, variant) in enumerate(work):
+        ds = durs[j::len(work)]
+        mean_ms = sum(ds) / len(ds)
+        kernel_ms_total += sum(ds)
+        per[w.name] = {"M": w.M, "N": w.N, "K": w.K, "variant": variant,
+                       "ms_per_launch": mean_ms,
+                       "tflops": 2.0 * w.M * w.N * w.K / (mean_ms * 1e-3) / 1e12}
+    peak, peak_sus, peak_src = measured_peaks()
+    achieved = K * flops_step / (kernel_ms_total * 1e-3) / 1e12
+    for v in per.values():
+        v["frac_of_peak"] = v["tflops"] / peak
+
+    variant_names = {val: key for key, val in g.VARIANTS.items()}
+    dom = max(work, key=lambda it: 2.0 * it[0].M * it[0].N * it[0].K)
+    traffic = recorded_traffic(variant_names.get(dom[4], str(dom[4])))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops (burst; fp16 and bf16 share the "
+                               f"kind::f16 tensor path at the same nominal rate)",
+                "peak_sustained": peak_sus,
+                "frac_of_sustained": achieved / peak_sus if peak_sus else None,
+                "kernel": "gemm_ws_kernel",
+                "achieved_def": "algorithmic 2*M*N*K over both launches of a step / summed "
+                                "CUDA-event launch durations"}
+
+    # end to end through the public API: pinned host inputs -> device, GEMM, result -> host
+    e2e_steps = max(3, min(args.e2e_steps, K))
+    pinned = []
+    h2d = d2h = 0
+    for (w, Ad, Bd, D, variant) in work:
+        A, B = inputs[w.name]
+        Ah, Bh = A.pin_memory(), B.pin_memory()
+        Dh = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+        pinned.append((w, Ah, Bh, Dh, Ad, Bd, D, variant))
+        h2d += Ah.numel() * 2 + Bh.numel() * 2
+        d2h += Dh.numel() * 2
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(e2e_steps):
+            for (w, Ah, Bh, Dh, Ad, Bd, D, variant) in pinned:
+                Ad.copy_(Ah, non_blocking=True)
+                Bd.copy_(Bh, non_blocking=True)
+                g.gemm(Ad, Bd, out=D, variant=variant, stream=stream)
+                Dh.copy_(D, non_blocking=True)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    g.check_status(stream)
+    e2e_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        f, s, desc = oracle_sample(inputs, args.cpu_seconds)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": desc + " (binary64 dot products, OpenMP)",
+               "seconds": s}
+
+    in_bytes = [2 * (w.M * w.K + w.N * w.K) for (w, *_r) in work]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {
+            "workload": "+".join(WORKLOADS),
+            "shapes": [[w.M, w.N, w.K] for (w, *_r) in work],
+            "accumulate": "f32", "variant": [it[4] for it in work],
+            "parallelism": f"replicas x{world}",
+            "l2": f"no flush: every step's inputs ({', '.join(f'{b / 2**20:.0f} MiB' for b in in_bytes)}) "
+                  f"exceed the {L2_BYTES / 1e6:.0f} MB L2",
+            "device": props.name, "sms": num_sms,
+        },
+        "per_workload": per,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "path": "pinned host A,B -> device copy, gemm() public API, D -> pinned host"},
+        "gpu_launches": K * len(work),
+        "clocks": clock_info,
+        "wall_s_timed_region": wall_s,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

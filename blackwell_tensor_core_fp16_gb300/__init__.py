@@ -1,0 +1,207 @@
+"""GB300-native fp16 GEMM: D = A * B^T (A: M x K, B: N x K, fp16 row-major; fp32 accumulation;
+D: M x N fp16), computed by the hand-written sm_103a kernels of ``libgemm_f16.so``.
+
+This module is a thin ctypes binding over the C ABI in ``include/gemm_f16.h``: the functions
+named ``gemm_f16_*`` take plain integers (device pointers, sizes, a stream handle) exactly as
+the C functions do, and ``gemm()`` marshals torch tensors into them.  Every step of the
+computation runs in the CUDA library; there is no other code path.  If the library has not
+been built, every call raises ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+import threading
+
+from . import _build
+
+__all__ = [
+    "GemmError", "build", "load", "gemm", "check_status",
+    "gemm_f16_nt", "gemm_f16_nt_variant", "gemm_f16_choose_variant", "gemm_f16_check_status",
+    "gemm_f16_last_error", "gemm_f16_version", "gemm_f16_get_variant_info", "gemm_f16_idesc",
+    "gemm_f16_smem_desc_sw128", "gemm_f16_sw128", "gemm_f16_tile_coord", "gemm_f16_ring_pos",
+    "exported_symbols", "VARIANTS", "STATUS",
+]
+
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA_ERROR", 4: "TIMEOUT"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+VARIANTS = {"auto": 0, "tile": 1, "ws_128x256": 2, "ws_pair": 3, "ws_128x128": 4}
+
+build = _build.build
+LIB_PATH = _build.LIB_PATH
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"gemm_f16 status {code} ({STATUS.get(code, '?')}): {message}")
+        self.code = code
+
+
+class VariantInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "cta_group", "block_m", "block_n", "block_k", "stages", "threads", "smem_bytes",
+        "tmem_cols", "stage_tx_bytes", "persistent")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+def load():
+    """Load libgemm_f16.so (raises RuntimeError if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        import os
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build the CUDA library first "
+                "(blackwell_tensor_core_fp16_gb300.build()); there is no fallback path")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, u32, u64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32,
+                                  ctypes.c_uint64)
+        u32p = ctypes.POINTER(ctypes.c_uint32)
+        lib.gemm_f16_nt.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        lib.gemm_f16_nt.restype = i32
+        lib.gemm_f16_nt_variant.argtypes = [vp, vp, vp, i64, i64, i64, vp, i32]
+        lib.gemm_f16_nt_variant.restype = i32
+        lib.gemm_f16_choose_variant.argtypes = [i64, i64, i64, i32]
+        lib.gemm_f16_choose_variant.restype = i32
+        lib.gemm_f16_check_status.argtypes = [vp, u32p]
+        lib.gemm_f16_check_status.restype = i32
+        lib.gemm_f16_last_error.argtypes = []
+        lib.gemm_f16_last_error.restype = ctypes.c_char_p
+        lib.gemm_f16_version.argtypes = []
+        lib.gemm_f16_version.restype = i32
+        lib.gemm_f16_get_variant_info.argtypes = [i32, ctypes.POINTER(VariantInfo)]
+        lib.gemm_f16_get_variant_info.restype = i32
+        lib.gemm_f16_idesc.argtypes = [u32, u32, u32]
+        lib.gemm_f16_idesc.restype = u32
+        lib.gemm_f16_smem_desc_sw128.argtypes = [u32, u32]
+        lib.gemm_f16_smem_desc_sw128.restype = u64
+        lib.gemm_f16_sw128.argtypes = [u32]
+        lib.gemm_f16_sw128.restype = u32
+        lib.gemm_f16_tile_coord.argtypes = [u32, u32, u32, u32, u32p, u32p]
+        lib.gemm_f16_tile_coord.restype = None
+        lib.gemm_f16_ring_pos.argtypes = [u32, u32, u32p, u32p]
+        lib.gemm_f16_ring_pos.restype = None
+        _lib = lib
+        return lib
+
+
+# ---- the C ABI, one Python function per C function -------------------------------------------
+
+def gemm_f16_nt(A: int, B: int, D: int, M: int, N: int, K: int, stream: int = 0) -> int:
+    return load().gemm_f16_nt(A, B, D, M, N, K, stream)
+
+
+def gemm_f16_nt_variant(A: int, B: int, D: int, M: int, N: int, K: int, stream: int,
+                        variant: int) -> int:
+    return load().gemm_f16_nt_variant(A, B, D, M, N, K, stream, variant)
+
+
+def gemm_f16_choose_variant(M: int, N: int, K: int, num_sms: int) -> int:
+    return load().gemm_f16_choose_variant(M, N, K, num_sms)
+
+
+def gemm_f16_check_status(stream: int = 0):
+    """Returns (status, bits)."""
+    bits = ctypes.c_uint32(0)
+    rc = load().gemm_f16_check_status(stream, ctypes.byref(bits))
+    return rc, bits.value
+
+
+def gemm_f16_last_error() -> str:
+    return load().gemm_f16_last_error().decode()
+
+
+def gemm_f16_version() -> int:
+    return load().gemm_f16_version()
+
+
+def gemm_f16_get_variant_info(variant: int) -> dict:
+    info = VariantInfo()
+    rc = load().gemm_f16_get_variant_info(variant, ctypes.byref(info))
+    if rc != OK:
+        raise GemmError(rc, f"unknown variant {variant}")
+    return info.as_dict()
+
+
+def gemm_f16_idesc(M: int, N: int, ab_bf16: int = 0) -> int:
+    return load().gemm_f16_idesc(M, N, ab_bf16)
+
+
+def gemm_f16_smem_desc_sw128(smem_addr: int, sbo_bytes: int) -> int:
+    return load().gemm_f16_smem_desc_sw128(smem_addr, sbo_bytes)
+
+
+def gemm_f16_sw128(off: int) -> int:
+    return load().gemm_f16_sw128(off)
+
+
+def gemm_f16_tile_coord(t: int, num_m: int, num_n: int, group: int):
+    m, n = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    load().gemm_f16_tile_coord(t, num_m, num_n, group, ctypes.byref(m), ctypes.byref(n))
+    return m.value, n.value
+
+
+def gemm_f16_ring_pos(it: int, stages: int):
+    s, p = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    load().gemm_f16_ring_pos(it, stages, ctypes.byref(s), ctypes.byref(p))
+    return s.value, p.value
+
+
+def exported_symbols(header_path: str | None = None):
+    """Names of the functions the public header declares."""
+    import os
+    path = header_path or os.path.join(_build.ROOT, "include", "gemm_f16.h")
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_f16_\w+)\s*\(", text)))
+
+
+# ---- torch convenience ----------------------------------------------------------------------
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def gemm(A, B, out=None, variant: int | str = 0, stream=None):
+    """D = A @ B.T for CUDA fp16 tensors A (M, K) and B (N, K); returns D (M, N) fp16.
+
+    ``out`` may be a preallocated contiguous (M, N) fp16 CUDA tensor.  The call is asynchronous
+    on ``stream`` (default: torch's current stream).  Raises GemmError on a non-zero status.
+    """
+    import torch
+    if isinstance(variant, str):
+        variant = VARIANTS[variant]
+    for name, t in (("A", A), ("B", B)):
+        if t.dtype != torch.float16 or not t.is_cuda or t.dim() != 2 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 2-D CUDA float16 tensor")
+    M, K = A.shape
+    N, K2 = B.shape
+    if K2 != K:
+        raise ValueError(f"A is {tuple(A.shape)} and B is {tuple(B.shape)}: K differs")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    elif (out.dtype != torch.float16 or not out.is_cuda or tuple(out.shape) != (M, N)
+          or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous (M, N) CUDA float16 tensor")
+    rc = gemm_f16_nt_variant(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                             _stream_handle(stream), int(variant))
+    if rc != OK:
+        raise GemmError(rc, gemm_f16_last_error())
+    return out
+
+
+def check_status(stream=None) -> None:
+    """Synchronise ``stream`` and raise GemmError if a kernel gave up a bounded wait."""
+    rc, bits = gemm_f16_check_status(_stream_handle(stream))
+    if rc != OK:
+        raise GemmError(rc, f"{gemm_f16_last_error()} (bits 0x{bits:x})")

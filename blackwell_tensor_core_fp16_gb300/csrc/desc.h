@@ -1,0 +1,112 @@
+// Encoders shared by the host (unit tests, launch set-up) and the device (the kernels):
+// the tcgen05 instruction descriptor, the shared-memory matrix descriptor, the 128-byte
+// swizzle, the mbarrier ring's stage/phase sequence and the persistent tile order.
+#pragma once
+
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define GF16_HD __host__ __device__ __forceinline__ constexpr
+#else
+#define GF16_HD inline constexpr
+#endif
+
+namespace gf16 {
+
+// ---------------------------------------------------------------------------------------------
+// Instruction descriptor of tcgen05.mma .kind::f16 (dense), a 32-bit word:
+//   bits  5:4   accumulator format       (1 = f32)
+//   bits  9:7   A format                 (0 = f16, 1 = bf16)
+//   bits 12:10  B format                 (0 = f16, 1 = bf16)
+//   bit  15/16  A / B major              (0 = K-major)
+//   bits 22:17  N >> 3
+//   bits 28:24  M >> 4
+// Everything else (sparsity, saturation, negation, shift) is zero.  For f16 x f16 -> f32 with
+// M = N = 128 and both operands K-major this gives 0x08200010, the constant the page
+// "TIRx Compiler Foundation" (section "Example: A GEMM Kernel") uses for its 128x128 tile.
+// ---------------------------------------------------------------------------------------------
+GF16_HD uint32_t make_idesc_f16(uint32_t M, uint32_t N, uint32_t ab_bf16)
+{
+    return (1u << 4) | ((ab_bf16 & 7u) << 7) | ((ab_bf16 & 7u) << 10) | (((N >> 3) & 0x3Fu) << 17) |
+           (((M >> 4) & 0x1Fu) << 24);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Shared-memory matrix descriptor (64-bit) for a K-major operand tile stored with the 128-byte
+// swizzle: rows of 64 fp16 (128 bytes), grouped in atoms of 8 rows = 1024 bytes.
+//   bits 13:0   start address >> 4
+//   bits 29:16  leading-dimension byte offset >> 4 (not used by swizzled K-major tiles; 1)
+//   bits 45:32  stride-dimension byte offset >> 4  (distance between 8-row atoms: 1024 B)
+//   bits 48:46  fixed 0b001 (the tcgen05 descriptor version)
+//   bits 51:49  base offset (0: every tile starts on a 1024-byte boundary)
+//   bit  52     leading-dimension mode (0: relative)
+//   bits 63:61  swizzle mode (2 = 128-byte swizzle)
+// Stepping along K inside the 128-byte row (16 fp16 = 32 bytes per MMA) adds 32 bytes to the
+// start address, i.e. 2 to the low field: the swizzle is a function of the final address bits,
+// so the same XOR pattern the TMA wrote is applied to the shifted address.
+// ---------------------------------------------------------------------------------------------
+GF16_HD uint64_t make_smem_desc_sw128(uint32_t smem_addr, uint32_t sbo_bytes)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// ---------------------------------------------------------------------------------------------
+// 128-byte swizzle of a byte offset inside a 1024-byte-aligned tile whose rows are 128 bytes:
+// the 16-byte chunk index (bits 6:4) is XORed with the row index modulo 8 (bits 9:7).  For an
+// (8, 64) fp16 tile this is the element map addr = 64*i + 8*(q xor i) + r with q = j / 8 and
+// r = j mod 8, the worked example of the page "chapter_tirx_layout_api" (section "示例：对
+// (8, 64) float16 Tile 应用 128B Swizzle"), there derived from per_element = 3,
+// swizzle_len = 3, atom_len = 3.
+// ---------------------------------------------------------------------------------------------
+GF16_HD uint32_t sw128(uint32_t byte_offset)
+{
+    return byte_offset ^ ((byte_offset >> 3) & 0x70u);
+}
+
+// ---------------------------------------------------------------------------------------------
+// The mbarrier ring.  Iteration `it` (counted across all tiles a CTA processes, never reset)
+// uses stage it % S and waits for the phase of parity (it / S) & 1 on that stage's "full"
+// barrier; the producer waits on the stage's "empty" barrier with the opposite parity, so its
+// first pass over the ring proceeds at once.  Carrying `it` across tiles removes the
+// requirement that a tile's K-iteration count be a multiple of 2*S.
+// ---------------------------------------------------------------------------------------------
+struct RingPos {
+    uint32_t stage;
+    uint32_t parity;
+};
+
+GF16_HD RingPos ring_pos(uint32_t it, uint32_t stages)
+{
+    return RingPos{it % stages, (it / stages) & 1u};
+}
+
+// ---------------------------------------------------------------------------------------------
+// Persistent tile order with grouped rasterisation: tiles are numbered so that consecutive
+// numbers walk down a group of `group` tile-rows inside one tile-column, then move to the next
+// column; groups follow each other down the M dimension.  A wave of CTAs therefore shares a
+// few B column bands and a few A row bands, which keeps both in L2 (the l2_group_size idea of
+// the page "TIRx 与高性能GEMM (上)", section "Step 6").
+// ---------------------------------------------------------------------------------------------
+struct TileCoord {
+    uint32_t m_blk;
+    uint32_t n_blk;
+};
+
+GF16_HD TileCoord tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_t group)
+{
+    const uint32_t per_group = group * num_n;
+    const uint32_t g = t / per_group;
+    const uint32_t first_m = g * group;
+    const uint32_t left = num_m - first_m;
+    const uint32_t gsize = left < group ? left : group;
+    const uint32_t r = t - g * per_group;
+    return TileCoord{first_m + r % gsize, r / gsize};
+}
+
+}  // namespace gf16

@@ -1,0 +1,453 @@
+// Host side of libgemm_f16.so: argument checks, TMA descriptors, variant choice and launch.
+// The C ABI is declared (and documented) in include/gemm_f16.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/gemm_f16.h"
+#include "desc.h"
+#include "gemm_kernels.cuh"
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kMaxDevices = 64;
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(GEMM_F16_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+// ---- configuration read once from the environment --------------------------------------------
+uint64_t wait_timeout_ns()
+{
+    static const uint64_t v = [] {
+        const char* s = std::getenv("GEMM_F16_WAIT_TIMEOUT_MS");
+        long long ms = s ? std::atoll(s) : 4000;
+        if (ms < 1) ms = 1;
+        return static_cast<uint64_t>(ms) * 1000000ull;
+    }();
+    return v;
+}
+
+uint32_t group_m_setting()
+{
+    static const uint32_t v = [] {
+        const char* s = std::getenv("GEMM_F16_GROUP");
+        long g = s ? std::atol(s) : 8;
+        if (g < 1) g = 1;
+        if (g > 64) g = 64;
+        return static_cast<uint32_t>(g);
+    }();
+    return v;
+}
+
+// ---- the variants ----------------------------------------------------------------------------
+using Ws128x256 = gf16::WsCfg<1, 256, 4>;
+using WsPair = gf16::WsCfg<2, 256, 6>;
+using Ws128x128 = gf16::WsCfg<1, 128, 6>;
+
+bool variant_info(int v, gemm_f16_variant_info* o)
+{
+    switch (v) {
+    case GEMM_F16_VARIANT_TILE:
+        *o = {1, 128, 128, 64, 1, (int)gf16::TileCfg::THREADS, (int)gf16::TileCfg::SMEM_ALLOC,
+              (int)gf16::TileCfg::TMEM_COLS, (int)gf16::TileCfg::STAGE_TX, 0};
+        return true;
+    case GEMM_F16_VARIANT_WS_128x256:
+        *o = {1, 128, 256, 64, 4, (int)Ws128x256::THREADS, (int)Ws128x256::SMEM_ALLOC,
+              (int)Ws128x256::TMEM_COLS, (int)Ws128x256::STAGE_TX, 1};
+        return true;
+    case GEMM_F16_VARIANT_WS_PAIR:
+        *o = {2, 256, 256, 64, 6, (int)WsPair::THREADS, (int)WsPair::SMEM_ALLOC,
+              (int)WsPair::TMEM_COLS, (int)WsPair::STAGE_TX, 1};
+        return true;
+    case GEMM_F16_VARIANT_WS_128x128:
+        *o = {1, 128, 128, 64, 6, (int)Ws128x128::THREADS, (int)Ws128x128::SMEM_ALLOC,
+              (int)Ws128x128::TMEM_COLS, (int)Ws128x128::STAGE_TX, 1};
+        return true;
+    default:
+        return false;
+    }
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int choose_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
+{
+    if (num_sms < 2) num_sms = 2;
+    const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 256);
+    const int64_t tiles_128x256 = cdiv(M, 128) * cdiv(N, 256);
+    if (M > 128 && pair_tiles >= num_sms / 2) return GEMM_F16_VARIANT_WS_PAIR;
+    if (tiles_128x256 >= num_sms) return GEMM_F16_VARIANT_WS_128x256;
+    return GEMM_F16_VARIANT_WS_128x128;
+}
+
+// ---- per-device state ------------------------------------------------------------------------
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    bool smem_set[GEMM_F16_NUM_VARIANTS] = {};
+    int pair_clusters = 0;  // co-resident CTA pairs of the pair variant
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+int device_state(DeviceState** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GEMM_F16_ERR_CUDA, "device %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (major != 10 || minor != 3)
+            return fail(GEMM_F16_ERR_UNSUPPORTED,
+                        "device %d is sm_%d%d; this library is built for sm_103a only", dev, major,
+                        minor);
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_F16_OK;
+}
+
+template <typename Kernel>
+int ensure_smem(DeviceState& d, int variant, Kernel kernel, uint32_t bytes)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (d.smem_set[variant]) return GEMM_F16_OK;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    d.smem_set[variant] = true;
+    return GEMM_F16_OK;
+}
+
+// ---- TMA descriptors -------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// A row-major fp16 matrix of `rows` x `cols` (cols contiguous) read or written in boxes of
+// box_rows x box_cols elements with the 128-byte swizzle (box_cols * 2 == 128 bytes).
+int make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+             uint32_t box_cols)
+{
+    auto fn = encode_fn();
+    if (!fn) return fail(GEMM_F16_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_F16_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for %llux%llu",
+                    (int)r, (unsigned long long)rows, (unsigned long long)cols);
+    return GEMM_F16_OK;
+}
+
+// Small per-thread cache of encoded descriptors, keyed by everything they encode.
+struct MapKey {
+    const void* a;
+    const void* b;
+    const void* d;
+    int64_t M, N, K;
+    int variant;
+    int device;
+    bool operator==(const MapKey& o) const
+    {
+        return a == o.a && b == o.b && d == o.d && M == o.M && N == o.N && K == o.K &&
+               variant == o.variant && device == o.device;
+    }
+};
+
+struct MapEntry {
+    MapKey key;
+    CUtensorMap ma, mb, md;
+    bool valid;
+};
+
+constexpr int kCacheSize = 8;
+thread_local MapEntry t_cache[kCacheSize];
+thread_local int t_cache_next = 0;
+
+int get_maps(const MapKey& k, uint32_t a_box_rows, uint32_t b_box_rows, bool need_d,
+             const CUtensorMap** ma, const CUtensorMap** mb, const CUtensorMap** md)
+{
+    for (auto& e : t_cache) {
+        if (e.valid && e.key == k) {
+            *ma = &e.ma;
+            *mb = &e.mb;
+            *md = &e.md;
+            return GEMM_F16_OK;
+        }
+    }
+    MapEntry& e = t_cache[t_cache_next];
+    t_cache_next = (t_cache_next + 1) % kCacheSize;
+    e.valid = false;
+    int rc;
+    if ((rc = make_map(&e.ma, k.a, k.M, k.K, a_box_rows, 64)) != GEMM_F16_OK) return rc;
+    if ((rc = make_map(&e.mb, k.b, k.N, k.K, b_box_rows, 64)) != GEMM_F16_OK) return rc;
+    if (need_d) {
+        if ((rc = make_map(&e.md, k.d, k.M, k.N, 128, 64)) != GEMM_F16_OK) return rc;
+    } else {
+        std::memset(&e.md, 0, sizeof(e.md));
+    }
+    e.key = k;
+    e.valid = true;
+    *ma = &e.ma;
+    *mb = &e.mb;
+    *md = &e.md;
+    return GEMM_F16_OK;
+}
+
+// ---- launches --------------------------------------------------------------------------------
+int launch_tile(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                cudaStream_t stream, DeviceState& d, int dev)
+{
+    using C = gf16::TileCfg;
+    int rc = ensure_smem(d, GEMM_F16_VARIANT_TILE, gf16::gemm_tile_kernel, C::SMEM_ALLOC);
+    if (rc != GEMM_F16_OK) return rc;
+    const CUtensorMap *ma, *mb, *md;
+    MapKey key{A, B, D, M, N, K, GEMM_F16_VARIANT_TILE, dev};
+    if ((rc = get_maps(key, 128, 128, false, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
+    const dim3 grid(static_cast<uint32_t>(cdiv(N, 128)), static_cast<uint32_t>(cdiv(M, 128)));
+    if (grid.y > 65535u) return fail(GEMM_F16_ERR_UNSUPPORTED, "M too large for the tile variant");
+    gf16::gemm_tile_kernel<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(
+        *ma, *mb, static_cast<uint16_t*>(D), (uint32_t)M, (uint32_t)N, (uint32_t)cdiv(K, 64),
+        wait_timeout_ns());
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch of gemm_tile_kernel");
+    return GEMM_F16_OK;
+}
+
+template <int kCtaGroup, int kBlockN, int kStages>
+int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+              cudaStream_t stream, DeviceState& d, int dev)
+{
+    using C = gf16::WsCfg<kCtaGroup, kBlockN, kStages>;
+    auto kernel = gf16::gemm_ws_kernel<kCtaGroup, kBlockN, kStages>;
+    int rc = ensure_smem(d, variant, kernel, C::SMEM_ALLOC);
+    if (rc != GEMM_F16_OK) return rc;
+    const CUtensorMap *ma, *mb, *md;
+    MapKey key{A, B, D, M, N, K, variant, dev};
+    if ((rc = get_maps(key, 128, C::B_ROWS, true, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
+
+    const int64_t num_m = cdiv(M, C::MMA_M);
+    const int64_t num_n = cdiv(N, C::BN);
+    const int64_t tiles = num_m * num_n;
+    if (tiles > 0x7FFFFFFFll) return fail(GEMM_F16_ERR_UNSUPPORTED, "too many tiles");
+
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = stream;
+    int64_t units = d.sms;
+    if constexpr (kCtaGroup == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        {
+            std::lock_guard<std::mutex> lk(g_mu);
+            if (d.pair_clusters == 0) {
+                cfg.gridDim = dim3(2 * (d.sms / 2));
+                int n = 0;
+                cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+                if (n < 1) return fail(GEMM_F16_ERR_CUDA, "no CTA pair fits on this device");
+                d.pair_clusters = n;
+            }
+            units = d.pair_clusters;
+        }
+        const int64_t clusters = tiles < units ? tiles : units;
+        cfg.gridDim = dim3(static_cast<uint32_t>(2 * clusters));
+    } else {
+        cfg.attrs = nullptr;
+        cfg.numAttrs = 0;
+        const int64_t ctas = tiles < units ? tiles : units;
+        cfg.gridDim = dim3(static_cast<uint32_t>(ctas));
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *ma, *mb, *md, (uint32_t)M, (uint32_t)N,
+                                       (uint32_t)num_m, (uint32_t)num_n, (uint32_t)cdiv(K, 64),
+                                       group_m_setting(), wait_timeout_ns());
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_ws_kernel)");
+    return GEMM_F16_OK;
+}
+
+int check_args(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K)
+{
+    const int64_t lim = 0x7FFFFFFFll;
+    if (M < 0 || N < 0 || K < 0)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "negative size (M=%lld N=%lld K=%lld)", (long long)M,
+                    (long long)N, (long long)K);
+    if (M > lim || N > lim || K > lim)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "size above 2^31-1 (M=%lld N=%lld K=%lld)",
+                    (long long)M, (long long)N, (long long)K);
+    if (M == 0 || N == 0) return GEMM_F16_OK;
+    if (D == nullptr) return fail(GEMM_F16_ERR_INVALID_ARG, "D is null");
+    if (K > 0 && (A == nullptr || B == nullptr))
+        return fail(GEMM_F16_ERR_INVALID_ARG, "A or B is null");
+    if (K % 8 != 0)
+        return fail(GEMM_F16_ERR_UNSUPPORTED, "K=%lld is not a multiple of 8", (long long)K);
+    if (N % 8 != 0)
+        return fail(GEMM_F16_ERR_UNSUPPORTED, "N=%lld is not a multiple of 8", (long long)N);
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (misaligned(D) || (K > 0 && (misaligned(A) || misaligned(B))))
+        return fail(GEMM_F16_ERR_UNSUPPORTED, "A, B and D must be 16-byte aligned");
+    return GEMM_F16_OK;
+}
+
+int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+        cudaStream_t stream, int variant)
+{
+    t_last_error.clear();
+    if (variant < 0 || variant >= GEMM_F16_NUM_VARIANTS)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "unknown variant %d", variant);
+    int rc = check_args(A, B, D, M, N, K);
+    if (rc != GEMM_F16_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_F16_OK;
+    if (K == 0) {
+        cudaError_t e = cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream);
+        return e == cudaSuccess ? GEMM_F16_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != GEMM_F16_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (variant == GEMM_F16_VARIANT_AUTO) variant = choose_variant(M, N, K, d->sms);
+    switch (variant) {
+    case GEMM_F16_VARIANT_TILE:
+        return launch_tile(A, B, D, M, N, K, stream, *d, dev);
+    case GEMM_F16_VARIANT_WS_128x256:
+        return launch_ws<1, 256, 4>(variant, A, B, D, M, N, K, stream, *d, dev);
+    case GEMM_F16_VARIANT_WS_PAIR:
+        return launch_ws<2, 256, 6>(variant, A, B, D, M, N, K, stream, *d, dev);
+    case GEMM_F16_VARIANT_WS_128x128:
+        return launch_ws<1, 128, 6>(variant, A, B, D, M, N, K, stream, *d, dev);
+    default:
+        return fail(GEMM_F16_ERR_INVALID_ARG, "unknown variant %d", variant);
+    }
+}
+
+}  // namespace
+
+// ================================ C ABI ======================================================
+extern "C" {
+
+int gemm_f16_nt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                cudaStream_t stream)
+{
+    return run(A, B, D, M, N, K, stream, GEMM_F16_VARIANT_AUTO);
+}
+
+int gemm_f16_nt_variant(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream, int variant)
+{
+    return run(A, B, D, M, N, K, stream, variant);
+}
+
+int gemm_f16_choose_variant(int64_t M, int64_t N, int64_t K, int num_sms)
+{
+    return choose_variant(M, N, K, num_sms);
+}
+
+int gemm_f16_check_status(cudaStream_t stream, uint32_t* bits)
+{
+    t_last_error.clear();
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t v = 0;
+    e = cudaMemcpyFromSymbol(&v, gf16::gemm_f16_status_word, sizeof(v));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol(status)");
+    if (bits) *bits = v;
+    if (v != 0) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(gf16::gemm_f16_status_word, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol(status)");
+        return fail(GEMM_F16_ERR_TIMEOUT, "a kernel gave up a bounded wait (status bits 0x%x)", v);
+    }
+    return GEMM_F16_OK;
+}
+
+const char* gemm_f16_last_error(void) { return t_last_error.c_str(); }
+
+int gemm_f16_version(void) { return kVersion; }
+
+int gemm_f16_get_variant_info(int variant, gemm_f16_variant_info* out)
+{
+    if (!out) return GEMM_F16_ERR_INVALID_ARG;
+    return variant_info(variant, out) ? GEMM_F16_OK : GEMM_F16_ERR_INVALID_ARG;
+}
+
+uint32_t gemm_f16_idesc(uint32_t M, uint32_t N, uint32_t ab_bf16)
+{
+    return gf16::make_idesc_f16(M, N, ab_bf16);
+}
+
+uint64_t gemm_f16_smem_desc_sw128(uint32_t smem_addr, uint32_t sbo_bytes)
+{
+    return gf16::make_smem_desc_sw128(smem_addr, sbo_bytes);
+}
+
+uint32_t gemm_f16_sw128(uint32_t off) { return gf16::sw128(off); }
+
+void gemm_f16_tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_t group,
+                         uint32_t* m_blk, uint32_t* n_blk)
+{
+    const gf16::TileCoord c = gf16::tile_coord(t, num_m, num_n, group);
+    if (m_blk) *m_blk = c.m_blk;
+    if (n_blk) *n_blk = c.n_blk;
+}
+
+void gemm_f16_ring_pos(uint32_t it, uint32_t stages, uint32_t* stage, uint32_t* parity)
+{
+    const gf16::RingPos p = gf16::ring_pos(it, stages);
+    if (stage) *stage = p.stage;
+    if (parity) *parity = p.parity;
+}
+
+}  // extern "C"

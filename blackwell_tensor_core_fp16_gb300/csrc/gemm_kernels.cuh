@@ -1,0 +1,478 @@
+// GEMM kernels for sm_103a: D = A * B^T with A (M x K) and B (N x K) fp16 row-major,
+// fp32 accumulation in Tensor Memory, D (M x N) fp16 row-major.
+//
+// Two kernels:
+//
+//  * gemm_tile_kernel: one 128x128 output tile per CTA on a 2-D grid, 4 warps, a single
+//    shared-memory stage.  Thread 0 issues the TMA loads of a 64-wide K chunk, waits for them,
+//    issues four K=16 tcgen05.mma and waits for their commit before loading the next chunk;
+//    then every warp reads its 32 TMEM lanes, converts and stores its rows directly.  This is
+//    the synchronous protocol of Steps 2-4 on the page "TIRx 与高性能GEMM (上)": a K loop whose
+//    first MMA overwrites the accumulator, an mbarrier phase flipped on every use, TMA loads
+//    completing on a transaction-count barrier.  It is the cross-check for the fast kernel.
+//
+//  * gemm_ws_kernel<CtaGroup, BlockN, Stages>: the persistent, warp-specialised kernel.
+//      warp 0      TMA producer: fills a ring of `Stages` shared-memory stages (A 128x64 and
+//                  B (BlockN/CtaGroup)x64 per CTA, 128-byte swizzle), one "full" barrier per
+//                  stage with an expected byte count, waiting on the stage's "empty" barrier.
+//      warp 1      MMA issuer (one thread; in a CTA pair only the even CTA issues): four
+//                  tcgen05.mma per stage into one of two TMEM accumulators, tcgen05.commit to
+//                  the stage's "empty" barrier, and after the tile's last K chunk to the
+//                  accumulator's "tmem_full" barrier.  Also allocates and frees TMEM.
+//      warps 2-5   epilogue warpgroup: waits on "tmem_full", reads its TMEM lanes with
+//                  tcgen05.ld 32x32b, frees the accumulator for the next tile ("tmem_empty"),
+//                  converts fp32 -> fp16 with round-to-nearest-even, writes 128x64 swizzled
+//                  sub-tiles to shared memory and stores them with TMA (double-buffered).
+//    Tiles come from a static persistent schedule (tile = cluster id + i * clusters) in the
+//    grouped order of tile_coord().  Ring and accumulator positions are counted across tiles,
+//    so any K works.  Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+//    With CtaGroup == 2, a cluster of two CTAs computes a 256 x BlockN tile with
+//    tcgen05.mma.cta_group::2 (M = 256): each CTA loads its own 128 rows of A and its own half
+//    of the BlockN rows of B, both CTAs' loads complete on the even CTA's "full" barrier, and
+//    the MMA commit signals both CTAs.  No operand is shared, so no load is multicast.
+//
+// Tails: TMA loads fill elements outside [0,M)x[0,K) and [0,N)x[0,K) with zeros, so partial K
+// chunks add nothing and partial M/N tiles compute zeros in the padding; TMA stores and the
+// direct stores of gemm_tile_kernel never write outside [0,M)x[0,N).
+//
+// Every wait is bounded.  A wait that runs out sets a bit in gemm_f16_status_word and the
+// CTA's abort flag (so the CTA's other roles stop waiting too), the role waits (bounded) for the
+// asynchronous work it issued, and the CTA frees its TMEM and exits.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "desc.h"
+#include "ptx.cuh"
+
+namespace gf16 {
+
+// Bits reported through gemm_f16_status_word (read and cleared by the host).
+constexpr uint32_t kStatusProducerTimeout = 1u;
+constexpr uint32_t kStatusMmaTimeout = 2u;
+constexpr uint32_t kStatusEpilogueTimeout = 4u;
+constexpr uint32_t kStatusDrainTimeout = 8u;
+
+__device__ uint32_t gemm_f16_status_word;
+
+__device__ __forceinline__ void report(uint32_t bits, volatile uint32_t* abort_flag)
+{
+    *abort_flag = 1u;
+    atomicOr(&gemm_f16_status_word, bits);
+}
+
+constexpr uint32_t kBlockM = 128;  // rows of A (and D) per CTA
+constexpr uint32_t kBlockK = 64;   // one 128-byte swizzle row of fp16
+constexpr uint32_t kUmmaK = 16;    // K per tcgen05.mma of kind::f16
+
+// ==============================================================================================
+// gemm_tile_kernel: one 128 x 128 tile per CTA, single stage, synchronous K loop.
+// ==============================================================================================
+struct TileCfg {
+    static constexpr uint32_t BN = 128;
+    static constexpr uint32_t A_BYTES = kBlockM * kBlockK * 2;  // 16384
+    static constexpr uint32_t B_BYTES = BN * kBlockK * 2;       // 16384
+    static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;     // 32768
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = A_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_B + B_BYTES;        // tma, mma, drain
+    static constexpr uint32_t OFF_SLOT = OFF_BAR + 3 * 8;
+    static constexpr uint32_t OFF_ABORT = OFF_SLOT + 4;
+    static constexpr uint32_t SMEM_ALLOC = OFF_ABORT + 4 + 1024;
+    static constexpr uint32_t TMEM_COLS = 128;
+    static constexpr uint32_t THREADS = 128;
+};
+
+__global__ void __launch_bounds__(128, 1)
+    gemm_tile_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                     const __grid_constant__ CUtensorMap tmap_b, uint16_t* __restrict__ D,
+                     uint32_t M, uint32_t N, uint32_t num_k_blocks, uint64_t timeout_ns)
+{
+    using C = TileCfg;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const uint32_t sA = base + C::OFF_A;
+    const uint32_t sB = base + C::OFF_B;
+    const uint32_t tma_bar = base + C::OFF_BAR;
+    const uint32_t mma_bar = tma_bar + 8;
+    const uint32_t drain_bar = tma_bar + 16;
+    volatile uint32_t* slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_SLOT);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31u;
+    const int32_t m0 = static_cast<int32_t>(blockIdx.y * kBlockM);
+    const int32_t n0 = static_cast<int32_t>(blockIdx.x * C::BN);
+    constexpr uint32_t idesc = make_idesc_f16(kBlockM, C::BN, 0);
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_b);
+        mbar_init(tma_bar, 1);
+        mbar_init(mma_bar, 1);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        fence_mbarrier_init();
+    }
+    if (warp == 0) tmem_alloc<1>(smem_u32(const_cast<uint32_t*>(slot_ptr)), C::TMEM_COLS);
+    tcgen05_fence_before();
+    __syncthreads();
+    tcgen05_fence_after();
+    const uint32_t tmem_base = *slot_ptr;
+
+    if (threadIdx.x == 0) {
+        uint32_t phase = 0;
+        bool ok = true;
+        bool issued_mma = false;
+        for (uint32_t kb = 0; kb < num_k_blocks; ++kb) {
+            const int32_t k0 = static_cast<int32_t>(kb * kBlockK);
+            mbar_arrive_expect_tx(tma_bar, C::STAGE_TX);
+            tma_load_2d(sA, &tmap_a, tma_bar, k0, m0);
+            tma_load_2d(sB, &tmap_b, tma_bar, k0, n0);
+            if (!mbar_wait(tma_bar, phase, abort_flag, timeout_ns)) {
+                report(kStatusProducerTimeout, abort_flag);
+                ok = false;
+                break;
+            }
+            tcgen05_fence_after();
+            const uint64_t ad = make_smem_desc_sw128(sA, 1024);
+            const uint64_t bd = make_smem_desc_sw128(sB, 1024);
+#pragma unroll
+            for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
+                mma_f16<1>(tmem_base, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0u);
+            mma_commit(mma_bar);
+            issued_mma = true;
+            if (!mbar_wait(mma_bar, phase, abort_flag, timeout_ns)) {
+                report(kStatusMmaTimeout, abort_flag);
+                ok = false;
+                break;
+            }
+            phase ^= 1u;
+        }
+        if (!ok && issued_mma) {
+            // Let every MMA this thread issued finish before TMEM is freed.
+            mma_commit(drain_bar);
+            if (!mbar_wait(drain_bar, 0, nullptr, timeout_ns))
+                atomicOr(&gemm_f16_status_word, kStatusDrainTimeout);
+        }
+    }
+    __syncwarp();
+    tcgen05_fence_before();
+    __syncthreads();
+    tcgen05_fence_after();
+
+    if (*abort_flag == 0u) {
+        // TMEM lane = row of the tile; warp w may read lanes 32w .. 32w + 31.
+        const uint32_t row = warp * 32u + lane;
+        const uint32_t grow = static_cast<uint32_t>(m0) + row;
+#pragma unroll 1
+        for (uint32_t c = 0; c < C::BN / 32u; ++c) {
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tmem_base + ((warp * 32u) << 16), v, static_cast<int>(c * 32u));
+            tmem_ld_wait();
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) p[i] = pack_f16x2_rn(v[2 * i], v[2 * i + 1]);
+            if (grow < M) {
+#pragma unroll
+                for (uint32_t q = 0; q < 4; ++q) {
+                    const uint32_t col = static_cast<uint32_t>(n0) + c * 32u + q * 8u;
+                    if (col < N)  // N is a multiple of 8: a vector is all in or all out
+                        st_global_v4(D + static_cast<uint64_t>(grow) * N + col, p[4 * q],
+                                     p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+                }
+            }
+        }
+    }
+    tcgen05_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tcgen05_fence_after();
+        tmem_dealloc<1>(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ==============================================================================================
+// gemm_ws_kernel: persistent, warp-specialised, TMEM double-buffered.
+// ==============================================================================================
+template <int kCtaGroup, int kBlockN, int kStages>
+struct WsCfg {
+    static_assert(kCtaGroup == 1 || kCtaGroup == 2, "a CTA or a CTA pair");
+    static_assert(kBlockN % 64 == 0 && kBlockN >= 64 && kBlockN <= 256, "N tile");
+    static constexpr uint32_t BN = kBlockN;
+    static constexpr uint32_t MMA_M = kBlockM * kCtaGroup;
+    static constexpr uint32_t B_ROWS = kBlockN / kCtaGroup;  // rows of B each CTA loads
+    static constexpr uint32_t A_BYTES = kBlockM * kBlockK * 2;
+    static constexpr uint32_t B_BYTES = B_ROWS * kBlockK * 2;
+    // Bytes that complete on the issuing CTA's "full" barrier per stage (both CTAs' loads).
+    static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES) * kCtaGroup;
+    static constexpr uint32_t D_COLS = 64;                   // one 128-byte swizzle row of fp16
+    static constexpr uint32_t D_BYTES = kBlockM * D_COLS * 2;
+    static constexpr uint32_t TMEM_COLS = 2 * kBlockN;       // two accumulators
+    static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM columns");
+    static constexpr uint32_t OFF_A = 0;
+    static constexpr uint32_t OFF_B = OFF_A + kStages * A_BYTES;
+    static constexpr uint32_t OFF_D = OFF_B + kStages * B_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_D + 2 * D_BYTES;
+    static constexpr uint32_t NUM_BARS = 2 * kStages + 5;    // full, empty, tfull x2, tempty x2, drain
+    static constexpr uint32_t OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+    static constexpr uint32_t OFF_ABORT = OFF_SLOT + 4;
+    static constexpr uint32_t SMEM_ALLOC = OFF_ABORT + 4 + 1024;  // + slack to align the base
+    static_assert(SMEM_ALLOC <= 232448, "shared memory per CTA");
+    static constexpr uint32_t THREADS = 192;
+    static constexpr uint32_t EPI_THREADS = 128;
+};
+
+template <int kCtaGroup, int kBlockN, int kStages>
+__global__ void __launch_bounds__(192, 1)
+    gemm_ws_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b,
+                   const __grid_constant__ CUtensorMap tmap_d, uint32_t M, uint32_t N,
+                   uint32_t num_m_blocks, uint32_t num_n_blocks, uint32_t num_k_blocks,
+                   uint32_t group_m, uint64_t timeout_ns)
+{
+    using C = WsCfg<kCtaGroup, kBlockN, kStages>;
+    constexpr bool kPair = (kCtaGroup == 2);
+    constexpr uint32_t idesc = make_idesc_f16(C::MMA_M, C::BN, 0);
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const uint32_t sA = base + C::OFF_A;
+    const uint32_t sB = base + C::OFF_B;
+    const uint32_t sD = base + C::OFF_D;
+    const uint32_t bar0 = base + C::OFF_BAR;
+    const auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+    const auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (kStages + s); };
+    const auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2u * kStages + b); };
+    const auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2u * kStages + 2u + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2u * kStages + 4u);
+    volatile uint32_t* slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_SLOT);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+    const uint32_t cid = kPair ? cluster_id_x() : blockIdx.x;
+    const uint32_t ncl = kPair ? num_clusters_x() : gridDim.x;
+    const uint32_t num_tiles = num_m_blocks * num_n_blocks;
+
+    // ---- set-up: barriers, TMEM ----------------------------------------------------------
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_b);
+        prefetch_tensormap(&tmap_d);
+        for (uint32_t s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), 4u * kCtaGroup);  // one arrival per epilogue warp per CTA
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<kCtaGroup>(smem_u32(const_cast<uint32_t*>(slot_ptr)), C::TMEM_COLS);
+        tmem_relinquish<kCtaGroup>();
+    }
+    tcgen05_fence_before();
+    if constexpr (kPair) cluster_sync(); else __syncthreads();
+    tcgen05_fence_after();
+    const uint32_t tmem_base = *slot_ptr;
+
+    if (warp == 0) {
+        // ---- TMA producer ------------------------------------------------------------------
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (uint32_t t = cid; ok && t < num_tiles; t += ncl) {
+                const TileCoord tc = tile_coord(t, num_m_blocks, num_n_blocks, group_m);
+                const int32_t m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
+                const int32_t n0 = static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS);
+                for (uint32_t kb = 0; kb < num_k_blocks; ++kb, ++it) {
+                    const RingPos p = ring_pos(it, kStages);
+                    if (!mbar_wait<kPair>(empty_bar(p.stage), p.parity ^ 1u, abort_flag,
+                                          timeout_ns)) {
+                        report(kStatusProducerTimeout, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    const int32_t k0 = static_cast<int32_t>(kb * kBlockK);
+                    const uint32_t dA = sA + p.stage * C::A_BYTES;
+                    const uint32_t dB = sB + p.stage * C::B_BYTES;
+                    if constexpr (!kPair) {
+                        mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
+                        tma_load_2d(dA, &tmap_a, full_bar(p.stage), k0, m0);
+                        tma_load_2d(dB, &tmap_b, full_bar(p.stage), k0, n0);
+                    } else {
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
+                        const uint32_t fb = mapa_shared(full_bar(p.stage), 0);
+                        tma_load_2d_pair(dA, &tmap_a, fb, k0, m0);
+                        tma_load_2d_pair(dB, &tmap_b, fb, k0, n0);
+                    }
+                }
+            }
+            // Every stage must be released by the MMAs before this CTA may exit: the last
+            // commits still arrive on the "empty" barriers (in a pair, from the other CTA).
+            // Iteration j is released when phase j / Stages of its stage's barrier completes.
+            const uint32_t first = it > kStages ? it - kStages : 0u;
+            if (ok) {
+                for (uint32_t j = first; j < it; ++j) {
+                    const RingPos p = ring_pos(j, kStages);
+                    if (!mbar_wait<kPair>(empty_bar(p.stage), p.parity, abort_flag, timeout_ns)) {
+                        report(kStatusDrainTimeout, abort_flag);
+                        break;
+                    }
+                }
+            } else if (rank == 0) {
+                // After an abort: wait (bounded, ignoring the abort flag) for loads still in
+                // flight into the ring, so none lands after this CTA has exited.
+                for (uint32_t j = first; j < it; ++j) {
+                    const RingPos p = ring_pos(j, kStages);
+                    if (!mbar_wait<kPair>(full_bar(p.stage), p.parity, nullptr, timeout_ns / 8))
+                        break;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---- MMA issuer (the even CTA of a pair issues for both) ----------------------------
+        if (rank == 0 && lane == 0) {
+            uint32_t it = 0;
+            uint32_t acc = 0;
+            bool ok = true;
+            bool issued = false;
+            for (uint32_t t = cid; ok && t < num_tiles; t += ncl, ++acc) {
+                const uint32_t b = acc & 1u;
+                const uint32_t aph = (acc >> 1) & 1u;
+                if (!mbar_wait<kPair>(tempty_bar(b), aph ^ 1u, abort_flag, timeout_ns)) {
+                    report(kStatusMmaTimeout, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tcgen05_fence_after();
+                const uint32_t d_tmem = tmem_base + b * C::BN;
+                for (uint32_t kb = 0; kb < num_k_blocks; ++kb, ++it) {
+                    const RingPos p = ring_pos(it, kStages);
+                    if (!mbar_wait<kPair>(full_bar(p.stage), p.parity, abort_flag, timeout_ns)) {
+                        report(kStatusMmaTimeout, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tcgen05_fence_after();
+                    const uint64_t ad = make_smem_desc_sw128(sA + p.stage * C::A_BYTES, 1024);
+                    const uint64_t bd = make_smem_desc_sw128(sB + p.stage * C::B_BYTES, 1024);
+#pragma unroll
+                    for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
+                        mma_f16<kCtaGroup>(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc,
+                                           (kb | k) != 0u);
+                    issued = true;
+                    if constexpr (kPair) mma_commit_pair(empty_bar(p.stage), 0x3);
+                    else mma_commit(empty_bar(p.stage));
+                }
+                if (!ok) break;
+                if constexpr (kPair) mma_commit_pair(tfull_bar(b), 0x3);
+                else mma_commit(tfull_bar(b));
+            }
+            if (!ok && issued) {
+                // Let every MMA issued so far finish before TMEM is freed.
+                if constexpr (kPair) mma_commit_pair(drain_bar, 0x1);
+                else mma_commit(drain_bar);
+                if (!mbar_wait<false>(drain_bar, 0, nullptr, timeout_ns))
+                    atomicOr(&gemm_f16_status_word, kStatusDrainTimeout);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue warpgroup ------------------------------------------------------------
+        const uint32_t quad = warp & 3u;             // TMEM lanes 32*quad .. 32*quad + 31
+        const uint32_t row = quad * 32u + lane;      // row of this CTA's 128-row slab
+        const uint32_t et = threadIdx.x - 64u;       // 0 .. 127
+        const uint32_t lane_off = (quad * 32u) << 16;
+        uint32_t acc = 0;
+        uint32_t sbuf = 0;
+        bool ok = true;
+        for (uint32_t t = cid; t < num_tiles; t += ncl, ++acc) {
+            const TileCoord tc = tile_coord(t, num_m_blocks, num_n_blocks, group_m);
+            const int32_t m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
+            const int32_t n0 = static_cast<int32_t>(tc.n_blk * C::BN);
+            const uint32_t b = acc & 1u;
+            const uint32_t aph = (acc >> 1) & 1u;
+            // One thread polls; the barrier-AND gives all 128 threads the same answer, so the
+            // group never splits between leaving and waiting at a named barrier.
+            uint32_t waited = 1u;
+            if (et == 0) waited = mbar_wait<kPair>(tfull_bar(b), aph, abort_flag, timeout_ns);
+            waited = named_barrier_and(2, C::EPI_THREADS, waited);
+            if (!waited) {
+                if (et == 0) report(kStatusEpilogueTimeout, abort_flag);
+                ok = false;
+                break;
+            }
+            tcgen05_fence_after();
+#pragma unroll 1
+            for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr = tmem_base + lane_off + b * C::BN + c * C::D_COLS;
+                tmem_ld_32x32b_x32(taddr, v0, 0);
+                tmem_ld_32x32b_x32(taddr, v1, 32);
+                tmem_ld_wait();
+                if (c == C::BN / C::D_COLS - 1) {
+                    // This warp is done with accumulator b: hand it back to the MMA issuer.
+                    tcgen05_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(b), 0));
+                        else mbar_arrive_local(tempty_bar(b));
+                    }
+                    __syncwarp();
+                }
+                const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
+                if (col0 < static_cast<int32_t>(N) && m0 < static_cast<int32_t>(M)) {
+                    uint32_t p[32];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) p[i] = pack_f16x2_rn(v0[2 * i], v0[2 * i + 1]);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        p[16 + i] = pack_f16x2_rn(v1[2 * i], v1[2 * i + 1]);
+                    // The store issued two sub-tiles ago read this buffer; wait until it has.
+                    if (et == 0) bulk_wait_group_read<1>();
+                    __syncwarp();
+                    named_barrier_sync(1, C::EPI_THREADS);
+                    const uint32_t dbuf = sD + sbuf * C::D_BYTES;
+#pragma unroll
+                    for (uint32_t j = 0; j < 8; ++j)
+                        st_shared_v4(dbuf + sw128(row * 128u + j * 16u), p[4 * j], p[4 * j + 1],
+                                     p[4 * j + 2], p[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    named_barrier_sync(1, C::EPI_THREADS);
+                    if (et == 0) {
+                        tma_store_2d(&tmap_d, dbuf, col0, m0);
+                        bulk_commit_group();
+                    }
+                    __syncwarp();
+                    sbuf ^= 1u;
+                }
+            }
+        }
+        (void)ok;
+        if (et == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    // ---- teardown ------------------------------------------------------------------------
+    tcgen05_fence_before();
+    if constexpr (kPair) cluster_sync(); else __syncthreads();
+    if (warp == 1) {
+        tcgen05_fence_after();
+        tmem_dealloc<kCtaGroup>(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace gf16

@@ -1,0 +1,134 @@
+/*
+ * gemm_f16.h -- C ABI of the GB300 (sm_103a) fp16 GEMM library libgemm_f16.so.
+ *
+ * The operation (page "TIRx 与高性能GEMM (上)", section "从 GEMM 公式到数据路径"):
+ *
+ *     D = A * B^T,   D[i][j] = sum_{k < K} A[i][k] * B[j][k]
+ *
+ * A is M x K, B is N x K (the weight layout: each row of B is one output feature, K
+ * contiguous, so the transpose is a property of the storage and no data is moved), D is M x N.
+ * All three are IEEE binary16, row-major and dense (leading dimensions K, K and N).  Products
+ * are accumulated in fp32 in Tensor Memory; each output is rounded to fp16 with
+ * round-to-nearest-even (page "TIRx Compiler Foundation", section "Example: A GEMM Kernel":
+ * the accumulator is converted to FP16 with cvt.rn before the store).
+ *
+ * Memory: the caller owns A, B and D, which must be device memory of the current CUDA device.
+ * The library allocates no device memory, keeps no pointer beyond a call, and only caches
+ * host-side objects (TMA descriptors, device properties).  D is overwritten, never read.
+ *
+ * Asynchrony: every compute entry point enqueues work on `stream` and returns; it does not
+ * synchronise.  Errors that need the GPU to detect (a bounded wait that ran out) are reported
+ * by gemm_f16_check_status().
+ *
+ * Thread safety: entry points may be called from several host threads at once.
+ */
+#ifndef GEMM_F16_H
+#define GEMM_F16_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point that can fail. */
+#define GEMM_F16_OK 0
+/* A null pointer with a non-empty operand, a negative size, or a size above 2^31 - 1. */
+#define GEMM_F16_ERR_INVALID_ARG 1
+/* A shape or pointer the tensor-memory-access path cannot address: K or N not a multiple of 8
+ * (row strides must be multiples of 16 bytes), or A, B or D not 16-byte aligned.  There is no
+ * fallback path; the call does nothing. */
+#define GEMM_F16_ERR_UNSUPPORTED 2
+/* A CUDA runtime or driver call failed; gemm_f16_last_error() describes it. */
+#define GEMM_F16_ERR_CUDA 3
+/* A kernel gave up a bounded wait (its pipeline did not make progress within the limit);
+ * D is unspecified.  Returned by gemm_f16_check_status() only. */
+#define GEMM_F16_ERR_TIMEOUT 4
+
+/* Kernel variants (gemm_f16_nt_variant).  All compute the same D. */
+#define GEMM_F16_VARIANT_AUTO 0       /* choose by shape and device */
+#define GEMM_F16_VARIANT_TILE 1       /* one 128x128 tile per CTA, synchronous K loop */
+#define GEMM_F16_VARIANT_WS_128x256 2 /* persistent, warp-specialised, 1 CTA per 128x256 tile */
+#define GEMM_F16_VARIANT_WS_PAIR 3    /* persistent, warp-specialised, CTA pair per 256x256 */
+#define GEMM_F16_VARIANT_WS_128x128 4 /* persistent, warp-specialised, 1 CTA per 128x128 tile */
+#define GEMM_F16_NUM_VARIANTS 5
+
+/*
+ * D = A * B^T for fp16 A (M x K), B (N x K), D (M x N), fp32 accumulation, on `stream`.
+ *
+ * A, B, D: device pointers (binary16 elements), 16-byte aligned.
+ * M, N, K: sizes, 0 <= each <= 2^31 - 1; K % 8 == 0 and N % 8 == 0.
+ * stream:  the CUDA stream to enqueue on (0 is the legacy default stream).
+ *
+ * M == 0 or N == 0: nothing to compute; returns GEMM_F16_OK without touching any pointer.
+ * K == 0: D is the empty sum, all zeros (filled with cudaMemsetAsync).
+ * Returns a GEMM_F16_* status; on any status other than GEMM_F16_OK nothing was enqueued.
+ */
+int gemm_f16_nt(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                cudaStream_t stream);
+
+/* Same operation with an explicit kernel variant (GEMM_F16_VARIANT_*), for benchmarking and
+ * cross-checking; GEMM_F16_VARIANT_AUTO is what gemm_f16_nt uses.  An unknown variant is
+ * GEMM_F16_ERR_INVALID_ARG. */
+int gemm_f16_nt_variant(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream, int variant);
+
+/* The variant GEMM_F16_VARIANT_AUTO picks for this shape on a device with `num_sms`
+ * multiprocessors.  Host-only; needs no GPU. */
+int gemm_f16_choose_variant(int64_t M, int64_t N, int64_t K, int num_sms);
+
+/* Synchronise `stream`, then read and clear the device status word of the current device.
+ * Returns GEMM_F16_OK, GEMM_F16_ERR_TIMEOUT (a kernel gave up a bounded wait; *bits, if not
+ * null, receives which roles did) or GEMM_F16_ERR_CUDA. */
+int gemm_f16_check_status(cudaStream_t stream, uint32_t* bits);
+
+/* Description of the last error on the calling thread ("" if none).  The string stays valid
+ * until the thread's next call into the library. */
+const char* gemm_f16_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int gemm_f16_version(void);
+
+/* ---- host-side encoders (no GPU needed; used by the unit tests) -------------------------- */
+
+/* Static description of a variant's tiling.  Returns GEMM_F16_OK or GEMM_F16_ERR_INVALID_ARG. */
+typedef struct gemm_f16_variant_info {
+    int32_t cta_group;      /* CTAs per tile (1, or 2 for a CTA pair) */
+    int32_t block_m;        /* output rows per tile */
+    int32_t block_n;        /* output columns per tile */
+    int32_t block_k;        /* K per pipeline stage */
+    int32_t stages;         /* shared-memory pipeline stages */
+    int32_t threads;        /* threads per CTA */
+    int32_t smem_bytes;     /* dynamic shared memory per CTA */
+    int32_t tmem_cols;      /* Tensor Memory columns per CTA */
+    int32_t stage_tx_bytes; /* bytes a stage's "full" barrier expects (both CTAs of a pair) */
+    int32_t persistent;     /* 1 if CTAs loop over tiles */
+} gemm_f16_variant_info;
+
+int gemm_f16_get_variant_info(int variant, gemm_f16_variant_info* out);
+
+/* tcgen05.mma .kind::f16 instruction descriptor: fp32 accumulator, A and B both fp16
+ * (ab_bf16 = 0) or both bf16 (1), K-major, M x N.  For M = N = 128, fp16: 0x08200010. */
+uint32_t gemm_f16_idesc(uint32_t M, uint32_t N, uint32_t ab_bf16);
+
+/* Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand tile at shared
+ * address `smem_addr` whose 8-row atoms are `sbo_bytes` apart. */
+uint64_t gemm_f16_smem_desc_sw128(uint32_t smem_addr, uint32_t sbo_bytes);
+
+/* Byte offset after the 128-byte swizzle of byte offset `off` inside a 1024-byte-aligned tile
+ * with 128-byte rows. */
+uint32_t gemm_f16_sw128(uint32_t off);
+
+/* Tile number t -> (m_blk, n_blk) in the persistent schedule's grouped order. */
+void gemm_f16_tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_t group,
+                         uint32_t* m_blk, uint32_t* n_blk);
+
+/* Pipeline iteration `it` -> ring stage and the parity of the "full" phase it waits for. */
+void gemm_f16_ring_pos(uint32_t it, uint32_t stages, uint32_t* stage, uint32_t* parity);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_H */

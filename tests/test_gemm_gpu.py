@@ -1,0 +1,224 @@
+"""Parity of the CUDA path with the CPU oracle (needs a GB300).
+
+Every case calls the C ABI (gemm_f16_nt / gemm_f16_nt_variant) on seeded inputs and compares
+each output element with the oracle's binary64 sum D_ref:
+
+    |D_gpu - D_ref| <= 1e-3 * sqrt(K) + 2^-10 * |D_ref|
+
+Outputs are written into a buffer prefilled with a NaN pattern and flanked by guard bands, so
+an element the kernel failed to write, or a write outside D, fails the test.  Sizes the oracle
+finishes in seconds are compared in full; the two largest workloads are compared on sampled
+elements (corners, tile boundaries, random picks) plus properties that hold at any size.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import blackwell_tensor_core_fp16_gb300 as g
+import oracle
+from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS, make_inputs, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 4096          # fp16 elements on each side of D (8 KiB: keeps D 16-byte aligned)
+FILL = 0x7E5A         # a NaN bit pattern
+WS_VARIANTS = [g.VARIANTS["ws_128x256"], g.VARIANTS["ws_pair"], g.VARIANTS["ws_128x128"]]
+ALL_VARIANTS = [g.VARIANTS["tile"], g.VARIANTS["auto"]] + WS_VARIANTS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_library():
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    g.build()
+    g.load()
+    torch.cuda.init()
+    yield
+    rc, bits = g.gemm_f16_check_status(0)
+    assert rc == g.OK, f"a kernel gave up a bounded wait: bits 0x{bits:x}"
+
+
+def run(A_cpu, B_cpu, variant=0, stream=None):
+    """Run D = A B^T through the C ABI into a guarded, NaN-prefilled buffer; returns D (CPU)."""
+    A = A_cpu.cuda()
+    B = B_cpu.cuda()
+    M, K = A.shape
+    N = B.shape[0]
+    buf = torch.full((2 * GUARD + M * N,), FILL, dtype=torch.int16, device="cuda")
+    D = buf[GUARD:GUARD + M * N].view(torch.float16).view(M, N)
+    s = torch.cuda.current_stream() if stream is None else stream
+    rc = g.gemm_f16_nt_variant(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, s.cuda_stream,
+                               variant)
+    assert rc == g.OK, g.gemm_f16_last_error()
+    rc, bits = g.gemm_f16_check_status(s.cuda_stream)
+    assert rc == g.OK, f"status bits 0x{bits:x}"
+    head = buf[:GUARD]
+    tail = buf[GUARD + M * N:]
+    assert bool((head == FILL).all()) and bool((tail == FILL).all()), "write outside D"
+    return D.cpu()
+
+
+def assert_parity(D_gpu, d_ref, K, where=""):
+    d = D_gpu.double().numpy()
+    assert np.isfinite(d).all(), f"{where}: non-finite output (unwritten element?)"
+    err = np.abs(d - d_ref)
+    tol = oracle.tolerance(d_ref, K)
+    bad = err > tol
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        worst = float((err / tol).max())
+        pytest.fail(f"{where}: {int(bad.sum())} elements out of tolerance, worst err/tol "
+                    f"{worst:.3f}, first at {idx.tolist()}")
+
+
+def full_parity(A, B, variant, where):
+    D = run(A, B, variant)
+    assert_parity(D, oracle.gemm_f64(A, B), A.shape[1], where)
+    return D
+
+
+# ---- the single-tile workload, every variant ---------------------------------------------------
+
+@pytest.mark.parametrize("variant", ALL_VARIANTS)
+def test_single_tile_workload(variant):
+    A, B = workload_inputs(WORKLOADS["single_tile_128x128x64"])
+    full_parity(A, B, variant, f"128x128x64 variant {variant}")
+
+
+# ---- several tiles and ragged tails, compared in full ------------------------------------------
+
+SHAPES = [
+    (300, 264, 200),    # ragged M, N and K
+    (129, 136, 72),     # one past a tile in M; K tail of 8
+    (1, 8, 8),          # smallest legal problem
+    (7, 24, 1000),      # K tail of 40 (like the ragged workload)
+    (255, 520, 64),     # one short of a 256-row pair tile
+    (257, 256, 8),      # one past a pair tile; K far below one chunk
+    (520, 776, 1000),   # several tiles each way, every tail at once
+    (64, 64, 16384),    # one tile, a long K loop (many ring wraps)
+]
+
+
+@pytest.mark.parametrize("variant", ALL_VARIANTS)
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_ragged_shapes(shape, variant):
+    M, N, K = shape
+    A, B = make_inputs(M, N, K, seed=100 + M + N + K)
+    full_parity(A, B, variant, f"{shape} variant {variant}")
+
+
+@pytest.mark.parametrize("variant", [0] + WS_VARIANTS)
+def test_square_2048_workload(variant):
+    A, B = workload_inputs(WORKLOADS["square_2048"])
+    full_parity(A, B, variant, f"2048^3 variant {variant}")
+
+
+@pytest.mark.parametrize("variant", [0, g.VARIANTS["tile"]] + WS_VARIANTS)
+def test_ragged_3000x5000x1000_workload(variant):
+    A, B = workload_inputs(WORKLOADS["ragged_3000x5000x1000"])
+    full_parity(A, B, variant, f"3000x5000x1000 variant {variant}")
+
+
+# ---- the two largest workloads: sampled elements and whole-output properties -------------------
+
+def sample_indices(M, N, rng, count=3000):
+    """Every pair of edge rows x edge columns (corners and tile boundaries) plus random picks."""
+    edges_m = sorted({r for r in (0, 1, 127, 128, 255, 256, M // 2, M - 129, M - 128, M - 2,
+                                  M - 1) if 0 <= r < M})
+    edges_n = sorted({c for c in (0, 1, 63, 64, 127, 128, 255, 256, N // 2, N - 257, N - 256,
+                                  N - 2, N - 1) if 0 <= c < N})
+    er, ec = np.meshgrid(edges_m, edges_n, indexing="ij")
+    rows = np.concatenate([er.ravel(), rng.integers(0, M, count)])
+    cols = np.concatenate([ec.ravel(), rng.integers(0, N, count)])
+    return rows.astype(np.int64), cols.astype(np.int64)
+
+
+@pytest.mark.parametrize("name", ["square_8192", "mlp_up_16384x14336x4096"])
+@pytest.mark.parametrize("variant", [0] + WS_VARIANTS)
+def test_large_workloads_sampled(name, variant):
+    w = WORKLOADS[name]
+    A, B = workload_inputs(w)
+    D = run(A, B, variant)
+    assert not torch.isnan(D).any(), "unwritten output elements"
+    rows, cols = sample_indices(w.M, w.N, np.random.default_rng(w.seed))
+    ref = oracle.gemm_f64_sampled(A, B, rows, cols)
+    got = D[torch.from_numpy(rows), torch.from_numpy(cols)]
+    assert_parity(got, ref, w.K, f"{name} variant {variant} (sampled)")
+
+
+@pytest.mark.parametrize("name", ["square_8192", "mlp_up_16384x14336x4096"])
+def test_large_workloads_all_ones_exact(name):
+    """A = B = 1 gives exactly K in every element at full size (K <= 8192 is exact in fp32
+    accumulation and in fp16)."""
+    w = WORKLOADS[name]
+    A = torch.ones((w.M, w.K), dtype=torch.float16)
+    B = torch.ones((w.N, w.K), dtype=torch.float16)
+    D = run(A, B, 0)
+    assert bool((D == float(w.K)).all())
+
+
+# ---- edge cases --------------------------------------------------------------------------------
+
+def test_k_zero_gives_zeros():
+    A = torch.zeros((5, 0), dtype=torch.float16)
+    B = torch.zeros((8, 0), dtype=torch.float16)
+    D = run(A, B, 0)
+    assert bool((D == 0).all())
+
+
+def test_empty_outputs_touch_nothing():
+    A = torch.zeros((0, 16), dtype=torch.float16, device="cuda")
+    B = torch.zeros((8, 16), dtype=torch.float16, device="cuda")
+    assert g.gemm_f16_nt(A.data_ptr(), B.data_ptr(), 0, 0, 8, 16, 0) == g.OK
+    assert g.gemm_f16_nt(B.data_ptr(), A.data_ptr(), 0, 8, 0, 16, 0) == g.OK
+
+
+def test_misaligned_device_pointer_rejected():
+    A = torch.zeros((16, 16), dtype=torch.float16, device="cuda")
+    D = torch.zeros((16, 16), dtype=torch.float16, device="cuda")
+    rc = g.gemm_f16_nt(A.data_ptr() + 2, A.data_ptr(), D.data_ptr(), 8, 8, 8, 0)
+    assert rc == g.ERR_UNSUPPORTED
+
+
+def test_deterministic_and_variants_agree():
+    A, B = make_inputs(1000, 1032, 1536, seed=7)
+    outs = [run(A, B, v) for v in WS_VARIANTS + [g.VARIANTS["tile"]]]
+    again = run(A, B, WS_VARIANTS[0])
+    assert torch.equal(outs[0].view(torch.int16), again.view(torch.int16)), "not deterministic"
+    ref = oracle.gemm_f64(A, B)
+    for o in outs:
+        assert_parity(o, ref, 1536, "variant agreement")
+
+
+def test_back_to_back_shapes_on_one_stream():
+    """Several launches in flight on one stream with different shapes (descriptor cache reuse
+    and invalidation), checked after a single synchronisation."""
+    s = torch.cuda.Stream()
+    cases = [(130, 264, 72), (384, 512, 128), (130, 264, 72), (1024, 1024, 256)]
+    outs, refs = [], []
+    with torch.cuda.stream(s):
+        for i, (M, N, K) in enumerate(cases):
+            A, B = make_inputs(M, N, K, seed=50 + i)
+            Ad, Bd = A.cuda(), B.cuda()
+            D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+            assert g.gemm_f16_nt(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K,
+                                 s.cuda_stream) == g.OK
+            outs.append((D, Ad, Bd))
+            refs.append((oracle.gemm_f64(A, B), K))
+    rc, _ = g.gemm_f16_check_status(s.cuda_stream)
+    assert rc == g.OK
+    for (D, _, _), (ref, K) in zip(outs, refs):
+        assert_parity(D.cpu(), ref, K, "back-to-back")
+
+
+def test_torch_binding():
+    A, B = make_inputs(200, 96, 64, seed=9)
+    D = g.gemm(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    assert_parity(D.cpu(), oracle.gemm_f64(A, B), 64, "torch binding")
+    with pytest.raises(ValueError):
+        g.gemm(A.cuda().float(), B.cuda())
+    with pytest.raises(g.GemmError):
+        g.gemm(A[:, :60].contiguous().cuda(), B[:, :60].contiguous().cuda())  # K % 8 != 0

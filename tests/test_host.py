@@ -1,0 +1,282 @@
+"""Host-side tests of the CUDA library (no GPU): the C ABI loads and exports every declared
+symbol, the encoders reproduce the values the pages print, the ring and scheduler logic
+holds its invariants, and argument checks reject bad calls before any CUDA call is made."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import pytest
+
+import blackwell_tensor_core_fp16_gb300 as g
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden_rows(name):
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line.split())
+    return rows
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    g.build()
+    return g.load()
+
+
+def test_library_exports_every_declared_symbol(built_library):
+    names = g.exported_symbols()
+    assert "gemm_f16_nt" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(built_library, n), f"{n} declared in include/gemm_f16.h but not exported"
+
+
+def test_version():
+    assert g.gemm_f16_version() >= 10000
+
+
+# ---- encoders against the pages ---------------------------------------------------------------
+
+def test_idesc_matches_page_constant():
+    for M, N, bf16, want in golden_rows("idesc_f16.txt"):
+        assert g.gemm_f16_idesc(int(M), int(N), int(bf16)) == int(want, 16)
+
+
+def test_idesc_fields():
+    d = g.gemm_f16_idesc(256, 256, 0)
+    assert (d >> 4) & 3 == 1            # f32 accumulator
+    assert (d >> 7) & 7 == 0 and (d >> 10) & 7 == 0  # f16 A and B
+    assert (d >> 15) & 1 == 0 and (d >> 16) & 1 == 0  # both K-major
+    assert (d >> 17) & 0x3F == 256 >> 3
+    assert (d >> 24) & 0x1F == 256 >> 4
+    assert d & 0xF == 0 and (d >> 13) & 3 == 0 and (d >> 29) == 0
+    b = g.gemm_f16_idesc(128, 256, 1)
+    assert (b >> 7) & 7 == 1 and (b >> 10) & 7 == 1
+
+
+def test_swizzle_bank_map_matches_page():
+    for i, bank_sw, bank_plain in golden_rows("sw128_f16_8x64_column0_banks.txt"):
+        i = int(i)
+        byte = g.gemm_f16_sw128(128 * i + 0)      # element (i, 0) of a 128-byte-row tile
+        assert (byte // 4) % 32 == int(bank_sw)
+        assert ((128 * i) // 4) % 32 == int(bank_plain)
+
+
+def test_swizzle_element_formula_whole_tile():
+    """addr = 64*i + 8*(q xor i) + r elements for every (i, j) of an (8, 64) fp16 tile, and the
+    pattern repeats every 8 rows (rows 8..127 of a 128-row operand tile)."""
+    for i in range(128):
+        for j in range(64):
+            q, r = divmod(j, 8)
+            want_elem = 64 * i + 8 * (q ^ (i % 8)) + r
+            assert g.gemm_f16_sw128(2 * (64 * i + j)) == 2 * want_elem
+
+
+def test_swizzle_is_a_permutation_of_each_atom():
+    for base in (0, 1024, 8192):
+        outs = {g.gemm_f16_sw128(base + o) for o in range(0, 1024, 16)}
+        assert outs == set(range(base, base + 1024, 16))
+
+
+def test_smem_descriptor_fields():
+    addr = 0x12400  # 1024-byte aligned shared address
+    d = g.gemm_f16_smem_desc_sw128(addr, 1024)
+    assert d & 0x3FFF == addr >> 4
+    assert (d >> 16) & 0x3FFF == 1
+    assert (d >> 32) & 0x3FFF == 1024 >> 4
+    assert (d >> 46) & 7 == 1
+    assert (d >> 49) & 7 == 0 and (d >> 52) & 1 == 0
+    assert (d >> 61) & 7 == 2
+    # advancing K by 16 fp16 (32 bytes) inside the swizzle row adds 2 to the address field
+    assert g.gemm_f16_smem_desc_sw128(addr + 32, 1024) == d + 2
+
+
+def test_expect_tx_bytes_match_page():
+    (bm, bn, bk, want), = golden_rows("expect_tx_bytes.txt")
+    info = g.gemm_f16_get_variant_info(g.VARIANTS["tile"])
+    assert (info["block_m"], info["block_n"], info["block_k"]) == (int(bm), int(bn), int(bk))
+    assert info["stage_tx_bytes"] == int(want)
+    # the same formula for the other variants (a pair counts both CTAs' loads)
+    for name in ("ws_128x256", "ws_128x128", "ws_pair"):
+        v = g.gemm_f16_get_variant_info(g.VARIANTS[name])
+        assert v["stage_tx_bytes"] == (v["block_m"] * v["block_k"] + v["block_n"] * v["block_k"]) * 2
+
+
+def test_variant_info_resources():
+    for name, v in g.VARIANTS.items():
+        if v == 0:
+            continue
+        info = g.gemm_f16_get_variant_info(v)
+        assert info["smem_bytes"] <= 232448          # 227 KB per CTA
+        assert info["tmem_cols"] in (32, 64, 128, 256, 512)
+        if info["persistent"]:
+            assert info["tmem_cols"] == 2 * info["block_n"]  # two accumulators
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_get_variant_info(99)
+
+
+# ---- pipeline phase bookkeeping ----------------------------------------------------------------
+
+def test_single_barrier_phase_table_matches_page():
+    """With one stage the ring position's parity is the page's phase before the wait, and the
+    next iteration's parity is the phase after it."""
+    for k, before, after in golden_rows("mbarrier_phase_table.txt"):
+        k = int(k)
+        assert g.gemm_f16_ring_pos(k, 1) == (0, int(before))
+        assert g.gemm_f16_ring_pos(k + 1, 1)[1] == int(after)
+
+
+def test_step6_parity_returns_after_even_uses():
+    (K, bk, depth, mma_uses, stage_uses), = golden_rows("ring_parity_step6.txt")
+    iters = int(K) // int(bk)
+    assert iters == int(mma_uses)
+    uses = [0] * int(depth)
+    for it in range(iters):
+        s, _ = g.gemm_f16_ring_pos(it, int(depth))
+        uses[s] += 1
+    assert uses == [int(stage_uses)] * int(depth)
+    assert g.gemm_f16_ring_pos(iters, int(depth)) == (0, 0)  # parity back to the start
+
+
+class _BarrierModel:
+    """A host model of an mbarrier's phase: completes a phase per `complete()`;
+    try_wait(parity) is true iff the phase with that parity has completed and no newer one."""
+
+    def __init__(self):
+        self.phase = 0
+
+    def complete(self):
+        self.phase += 1
+
+    def try_wait(self, parity):
+        # the current (incomplete) phase has parity phase & 1; the previous one is complete
+        return (self.phase & 1) != parity
+
+
+@pytest.mark.parametrize("stages", [1, 2, 4, 6])
+@pytest.mark.parametrize("k_iters", [1, 3, 16, 17, 64])
+def test_ring_protocol_model_across_tiles(stages, k_iters):
+    """Simulate producer and consumer on per-stage full/empty barriers over several tiles whose
+    K-iteration count is not a multiple of 2*stages: with positions carried across tiles, every
+    wait returns exactly when its data is ready and never early."""
+    full = [_BarrierModel() for _ in range(stages)]
+    empty = [_BarrierModel() for _ in range(stages)]
+    total = 3 * k_iters
+    produced = consumed = 0
+    stage_content = [None] * stages
+    steps = 0
+    while consumed < total:
+        steps += 1
+        assert steps < 100 * total
+        # producer tries to fill iteration `produced`
+        if produced < total:
+            s, par = g.gemm_f16_ring_pos(produced, stages)
+            if empty[s].try_wait(par ^ 1):
+                assert stage_content[s] is None, "producer overwrote an unconsumed stage"
+                stage_content[s] = produced
+                full[s].complete()
+                produced += 1
+        # consumer tries iteration `consumed`
+        s, par = g.gemm_f16_ring_pos(consumed, stages)
+        if full[s].try_wait(par):
+            assert stage_content[s] == consumed, "consumer saw the wrong iteration"
+            stage_content[s] = None
+            empty[s].complete()
+            consumed += 1
+
+
+# ---- persistent scheduler ----------------------------------------------------------------------
+
+@pytest.mark.parametrize("num_m,num_n,group", [(1, 1, 8), (64, 32, 8), (24, 20, 8), (7, 5, 3),
+                                               (13, 1, 8), (1, 13, 8), (128, 56, 16)])
+def test_tile_order_is_a_bijection(num_m, num_n, group):
+    seen = set()
+    for t in range(num_m * num_n):
+        m, n = g.gemm_f16_tile_coord(t, num_m, num_n, group)
+        assert 0 <= m < num_m and 0 <= n < num_n
+        seen.add((m, n))
+    assert len(seen) == num_m * num_n
+
+
+def test_tile_order_groups_walk_m_within_a_column():
+    num_m, num_n, group = 64, 32, 8
+    coords = [g.gemm_f16_tile_coord(t, num_m, num_n, group) for t in range(num_m * num_n)]
+    for t in range(0, len(coords), group):
+        block = coords[t:t + group]
+        assert len({n for _, n in block}) == 1                 # one N column ...
+        assert [m for m, _ in block] == list(range(block[0][0], block[0][0] + group))  # ... 8 M rows
+
+
+def test_persistent_schedule_covers_every_tile_once():
+    """Static persistent schedule: unit c takes tiles c, c + units, ...; every tile exactly once."""
+    num_m, num_n, units = 24, 20, 152
+    tiles = num_m * num_n
+    hits = [0] * tiles
+    for c in range(units):
+        for t in range(c, tiles, units):
+            hits[t] += 1
+    assert hits == [1] * tiles
+
+
+def test_choose_variant_returns_a_variant():
+    for (M, N, K) in [(128, 128, 64), (2048, 2048, 2048), (3000, 5000, 1000), (8192, 8192, 8192),
+                      (16384, 14336, 4096), (1, 8, 8), (100000, 8, 8)]:
+        v = g.gemm_f16_choose_variant(M, N, K, 152)
+        assert v in (1, 2, 3, 4)
+
+
+# ---- argument checks (return before any CUDA call) ---------------------------------------------
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced: every case below fails validation
+
+
+@pytest.mark.parametrize("args,code", [
+    ((FAKE, FAKE, FAKE, -1, 8, 8), g.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 8, -8, 8), g.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 8, 8, -8), g.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 1 << 31, 8, 8), g.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 0, 8, 8, 8), g.ERR_INVALID_ARG),
+    ((0, FAKE, FAKE, 8, 8, 8), g.ERR_INVALID_ARG),
+    ((FAKE, 0, FAKE, 8, 8, 8), g.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, 8, 8, 12), g.ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, 8, 12, 8), g.ERR_UNSUPPORTED),
+    ((FAKE + 2, FAKE, FAKE, 8, 8, 8), g.ERR_UNSUPPORTED),
+    ((FAKE, FAKE + 8, FAKE, 8, 8, 8), g.ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE + 4, 8, 8, 8), g.ERR_UNSUPPORTED),
+])
+def test_argument_checks(args, code):
+    assert g.gemm_f16_nt(*args, 0) == code
+    assert g.gemm_f16_last_error() != ""
+
+
+def test_empty_output_is_a_no_op():
+    # M == 0 or N == 0: nothing to do, no pointer is touched, no CUDA call is made
+    assert g.gemm_f16_nt(0, 0, 0, 0, 8, 8, 0) == g.OK
+    assert g.gemm_f16_nt(0, 0, 0, 8, 0, 8, 0) == g.OK
+
+
+def test_unknown_variant_rejected():
+    assert g.gemm_f16_nt_variant(FAKE, FAKE, FAKE, 8, 8, 8, 0, 17) == g.ERR_INVALID_ARG
+    assert g.gemm_f16_nt_variant(FAKE, FAKE, FAKE, 8, 8, 8, 0, -1) == g.ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    """With the extension absent the binding raises; it never computes another way."""
+    monkeypatch.setattr(g, "_lib", None)
+    monkeypatch.setattr(g, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        g.load()
+
+
+def test_product_package_does_not_reference_the_oracle():
+    pkg = os.path.dirname(g.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(root, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "gemm_ref" not in text, f
