@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(128, 1)
         *abort_flag = 0u;
         fence_mbarrier_init();
     }
+    __syncwarp();
     if (warp == 0) tmem_alloc<1>(smem_u32(const_cast<uint32_t*>(slot_ptr)), C::TMEM_COLS);
     tcgen05_fence_before();
     __syncthreads();
@@ -278,6 +279,7 @@ __global__ void __launch_bounds__(192, 1)
         *abort_flag = 0u;
         fence_mbarrier_init();
     }
+    __syncwarp();
     if (warp == 1) {
         tmem_alloc<kCtaGroup>(smem_u32(const_cast<uint32_t*>(slot_ptr)), C::TMEM_COLS);
         tmem_relinquish<kCtaGroup>();
