@@ -37,15 +37,29 @@ L2_BYTES = 129e6
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--steps", type=int, default=800)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--variant", type=int, default=0, help="kernel variant (0 = auto)")
-    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--only", default="", help="comma-separated subset of the step's workloads")
+    p.add_argument("--skip-e2e", action="store_true")
+    p.add_argument("--cublas-steps", type=int, default=20,
+                   help="launches of torch.matmul on the same shapes, for context (0: skip)")
     return p.parse_args()
+
+
+def step_workloads(args):
+    if not args.only:
+        return WORKLOADS
+    names = tuple(n.strip() for n in args.only.split(",") if n.strip())
+    for n in names:
+        if n not in WORKLOADS:
+            raise SystemExit(f"--only: unknown workload {n!r}; choose from {WORKLOADS}")
+    return names
 
 
 def dist_env():
@@ -172,9 +186,9 @@ def oracle_sample(inputs, seconds_target, rng_seed=0):
     return total_flops, total_s, "; ".join(desc)
 
 
-def host_inputs():
+def host_inputs(names=WORKLOADS):
     from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS as W, workload_inputs
-    return {n: workload_inputs(W[n]) for n in WORKLOADS}
+    return {n: workload_inputs(W[n]) for n in names}
 
 
 # ---- reference arm: the oracle, timed on host cores -------------------------------------------
@@ -187,7 +201,8 @@ def run_reference(args):
     from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS as W
 
     oracle.build()
-    inputs = host_inputs()
+    names = step_workloads(args)
+    inputs = host_inputs(names)
     per_step = min(0.25, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(inputs, per_step, rng_seed=1)
@@ -198,8 +213,8 @@ def run_reference(args):
         flops += f
         secs += t
     value = flops / secs / 1e12
-    cfg = {"workload": "+".join(WORKLOADS),
-           "shapes": [[W[n].M, W[n].N, W[n].K] for n in WORKLOADS]}
+    cfg = {"workload": "+".join(names),
+           "shapes": [[W[n].M, W[n].N, W[n].K] for n in names]}
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -239,9 +254,10 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(dev)
     num_sms = props.multi_processor_count
 
-    inputs = host_inputs()
+    names = step_workloads(args)
+    inputs = host_inputs(names)
     work = []
-    for n in WORKLOADS:
+    for n in names:
         w = W[n]
         A, B = inputs[n]
         Ad, Bd = A.to(dev), B.to(dev)
@@ -333,39 +349,91 @@ def run_ours(args):
                 "achieved_def": "algorithmic 2*M*N*K over both launches of a step / summed "
                                 "CUDA-event launch durations"}
 
-    # end to end through the public API: pinned host inputs -> device, GEMM, result -> host
-    e2e_steps = max(3, min(args.e2e_steps, K))
-    pinned = []
+    # cuBLAS (torch.matmul) on the same resident inputs, for context only
+    cublas = None
+    if args.cublas_steps > 0:
+        cublas = {}
+        for (w, Ad, Bd, D, variant) in work:
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    torch.mm(Ad, Bd.t(), out=D)
+                c0 = torch.cuda.Event(enable_timing=True)
+                c1 = torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                for _ in range(args.cublas_steps):
+                    torch.mm(Ad, Bd.t(), out=D)
+                c1.record(stream)
+            torch.cuda.synchronize()
+            ms = c0.elapsed_time(c1) / args.cublas_steps
+            cublas[w.name] = {"ms_per_launch": ms,
+                              "tflops": 2.0 * w.M * w.N * w.K / (ms * 1e-3) / 1e12}
+
+    # End to end through the public API: every step copies its inputs from pinned host memory
+    # to the device, runs the GEMMs with gemm(), and copies each result back to pinned host
+    # memory.  Copies run on their own streams with two buffer slots, so the upload of step
+    # i + 1 and the download of step i - 1 overlap the GEMMs of step i; the timed region runs
+    # from before the first upload to after the last download.
+    e2e_steps = 0 if args.skip_e2e else max(3, min(args.e2e_steps, K))
+    e2e_value = None
     h2d = d2h = 0
-    for (w, Ad, Bd, D, variant) in work:
-        A, B = inputs[w.name]
-        Ah, Bh = A.pin_memory(), B.pin_memory()
-        Dh = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
-        pinned.append((w, Ah, Bh, Dh, Ad, Bd, D, variant))
-        h2d += Ah.numel() * 2 + Bh.numel() * 2
-        d2h += Dh.numel() * 2
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
+    if e2e_steps:
+        s_up = torch.cuda.Stream(device=dev)
+        s_down = torch.cuda.Stream(device=dev)
+        slots = []
+        for slot in range(2):
+            items = []
+            for (w, Ad, Bd, D, variant) in work:
+                A, B = inputs[w.name]
+                if slot == 0:
+                    Ah, Bh = A.pin_memory(), B.pin_memory()
+                else:
+                    Ah, Bh = slots[0][len(items)][1], slots[0][len(items)][2]
+                Dh = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+                Ad2 = Ad if slot == 0 else torch.empty_like(Ad)
+                Bd2 = Bd if slot == 0 else torch.empty_like(Bd)
+                D2 = D if slot == 0 else torch.empty_like(D)
+                ev = {k: torch.cuda.Event() for k in ("up", "mm", "down")}
+                items.append((w, Ah, Bh, Dh, Ad2, Bd2, D2, variant, ev))
+            slots.append(items)
+        for (w, *_r) in work:
+            h2d += 2 * (w.M * w.K + w.N * w.K)
+            d2h += 2 * w.M * w.N
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
         ev0.record(stream)
-        for _ in range(e2e_steps):
-            for (w, Ah, Bh, Dh, Ad, Bd, D, variant) in pinned:
-                Ad.copy_(Ah, non_blocking=True)
-                Bd.copy_(Bh, non_blocking=True)
-                g.gemm(Ad, Bd, out=D, variant=variant, stream=stream)
-                Dh.copy_(D, non_blocking=True)
+        s_up.wait_event(ev0)
+        s_down.wait_event(ev0)
+        for i in range(e2e_steps):
+            for (w, Ah, Bh, Dh, Ad2, Bd2, D2, variant, ev) in slots[i % 2]:
+                if i >= 2:
+                    s_up.wait_event(ev["mm"])       # step i-2 finished reading this slot
+                with torch.cuda.stream(s_up):
+                    Ad2.copy_(Ah, non_blocking=True)
+                    Bd2.copy_(Bh, non_blocking=True)
+                    ev["up"].record(s_up)
+                stream.wait_event(ev["up"])
+                if i >= 2:
+                    stream.wait_event(ev["down"])   # step i-2's result has left this slot
+                g.gemm(Ad2, Bd2, out=D2, variant=variant, stream=stream)
+                ev["mm"].record(stream)
+                s_down.wait_event(ev["mm"])
+                with torch.cuda.stream(s_down):
+                    Dh.copy_(D2, non_blocking=True)
+                    ev["down"].record(s_down)
+        stream.wait_stream(s_up)
+        stream.wait_stream(s_down)
         ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    g.check_status(stream)
-    e2e_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+        torch.cuda.synchronize()
+        barrier()
+        g.check_status(stream)
+        e2e_ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e_value = world * e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -382,7 +450,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {
-            "workload": "+".join(WORKLOADS),
+            "workload": "+".join(names),
             "shapes": [[w.M, w.N, w.K] for (w, *_r) in work],
             "accumulate": "f32", "variant": [it[4] for it in work],
             "parallelism": f"replicas x{world}",
@@ -391,11 +459,14 @@ def run_ours(args):
             "device": props.name, "sms": num_sms,
         },
         "per_workload": per,
+        "cublas_fp16_same_shapes": cublas,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "path": "pinned host A,B -> device copy, gemm() public API, D -> pinned host"},
+                "path": "pinned host A,B -> device (copy stream), gemm() public API, "
+                        "D -> pinned host (copy stream); two buffer slots, copies of "
+                        "neighbouring steps overlap the GEMMs"},
         "gpu_launches": K * len(work),
         "clocks": clock_info,
         "wall_s_timed_region": wall_s,

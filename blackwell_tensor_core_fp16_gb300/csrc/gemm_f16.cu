@@ -64,9 +64,10 @@ uint32_t group_m_setting()
 }
 
 // ---- the variants ----------------------------------------------------------------------------
-using Ws128x256 = gf16::WsCfg<1, 256, 4>;
-using WsPair = gf16::WsCfg<2, 256, 6>;
-using Ws128x128 = gf16::WsCfg<1, 128, 6>;
+using Ws128x256 = gf16::WsCfg<1, 256, 4, true>;
+using WsPair = gf16::WsCfg<2, 256, 6, true>;
+using Ws128x128 = gf16::WsCfg<1, 128, 6, true>;
+using WsPairDirect = gf16::WsCfg<2, 256, 7, false>;
 
 bool variant_info(int v, gemm_f16_variant_info* o)
 {
@@ -86,6 +87,10 @@ bool variant_info(int v, gemm_f16_variant_info* o)
     case GEMM_F16_VARIANT_WS_128x128:
         *o = {1, 128, 128, 64, 6, (int)Ws128x128::THREADS, (int)Ws128x128::SMEM_ALLOC,
               (int)Ws128x128::TMEM_COLS, (int)Ws128x128::STAGE_TX, 1};
+        return true;
+    case GEMM_F16_VARIANT_WS_PAIR_DIRECT:
+        *o = {2, 256, 256, 64, 7, (int)WsPairDirect::THREADS, (int)WsPairDirect::SMEM_ALLOC,
+              (int)WsPairDirect::TMEM_COLS, (int)WsPairDirect::STAGE_TX, 1};
         return true;
     default:
         return false;
@@ -109,7 +114,7 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     bool smem_set[GEMM_F16_NUM_VARIANTS] = {};
-    int pair_clusters = 0;  // co-resident CTA pairs of the pair variant
+    int pair_clusters[GEMM_F16_NUM_VARIANTS] = {};  // co-resident CTA pairs per variant
 };
 
 std::mutex g_mu;
@@ -261,17 +266,17 @@ int launch_tile(const void* A, const void* B, void* D, int64_t M, int64_t N, int
     return GEMM_F16_OK;
 }
 
-template <int kCtaGroup, int kBlockN, int kStages>
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore>
 int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
               cudaStream_t stream, DeviceState& d, int dev)
 {
-    using C = gf16::WsCfg<kCtaGroup, kBlockN, kStages>;
-    auto kernel = gf16::gemm_ws_kernel<kCtaGroup, kBlockN, kStages>;
+    using C = gf16::WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
+    auto kernel = gf16::gemm_ws_kernel<kCtaGroup, kBlockN, kStages, kTmaStore>;
     int rc = ensure_smem(d, variant, kernel, C::SMEM_ALLOC);
     if (rc != GEMM_F16_OK) return rc;
     const CUtensorMap *ma, *mb, *md;
     MapKey key{A, B, D, M, N, K, variant, dev};
-    if ((rc = get_maps(key, 128, C::B_ROWS, true, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
+    if ((rc = get_maps(key, 128, C::B_ROWS, kTmaStore, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
 
     const int64_t num_m = cdiv(M, C::MMA_M);
     const int64_t num_n = cdiv(N, C::BN);
@@ -293,15 +298,15 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
         cfg.numAttrs = 1;
         {
             std::lock_guard<std::mutex> lk(g_mu);
-            if (d.pair_clusters == 0) {
+            if (d.pair_clusters[variant] == 0) {
                 cfg.gridDim = dim3(2 * (d.sms / 2));
                 int n = 0;
                 cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
                 if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
                 if (n < 1) return fail(GEMM_F16_ERR_CUDA, "no CTA pair fits on this device");
-                d.pair_clusters = n;
+                d.pair_clusters[variant] = n;
             }
-            units = d.pair_clusters;
+            units = d.pair_clusters[variant];
         }
         const int64_t clusters = tiles < units ? tiles : units;
         cfg.gridDim = dim3(static_cast<uint32_t>(2 * clusters));
@@ -311,7 +316,13 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
         const int64_t ctas = tiles < units ? tiles : units;
         cfg.gridDim = dim3(static_cast<uint32_t>(ctas));
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *ma, *mb, *md, (uint32_t)M, (uint32_t)N,
+    // Pipeline positions are 32-bit counters over a CTA's (tile, k-block) iterations.
+    const int64_t units_used = cfg.gridDim.x / kCtaGroup;
+    if (cdiv(tiles, units_used) * cdiv(K, 64) >= (int64_t(1) << 31))
+        return fail(GEMM_F16_ERR_UNSUPPORTED, "problem too large for one launch (M=%lld N=%lld "
+                    "K=%lld)", (long long)M, (long long)N, (long long)K);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *ma, *mb, *md, static_cast<uint16_t*>(D),
+                                       (uint32_t)M, (uint32_t)N,
                                        (uint32_t)num_m, (uint32_t)num_n, (uint32_t)cdiv(K, 64),
                                        group_m_setting(), wait_timeout_ns());
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_ws_kernel)");
@@ -363,11 +374,13 @@ int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
     case GEMM_F16_VARIANT_TILE:
         return launch_tile(A, B, D, M, N, K, stream, *d, dev);
     case GEMM_F16_VARIANT_WS_128x256:
-        return launch_ws<1, 256, 4>(variant, A, B, D, M, N, K, stream, *d, dev);
+        return launch_ws<1, 256, 4, true>(variant, A, B, D, M, N, K, stream, *d, dev);
     case GEMM_F16_VARIANT_WS_PAIR:
-        return launch_ws<2, 256, 6>(variant, A, B, D, M, N, K, stream, *d, dev);
+        return launch_ws<2, 256, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev);
     case GEMM_F16_VARIANT_WS_128x128:
-        return launch_ws<1, 128, 6>(variant, A, B, D, M, N, K, stream, *d, dev);
+        return launch_ws<1, 128, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev);
+    case GEMM_F16_VARIANT_WS_PAIR_DIRECT:
+        return launch_ws<2, 256, 7, false>(variant, A, B, D, M, N, K, stream, *d, dev);
     default:
         return fail(GEMM_F16_ERR_INVALID_ARG, "unknown variant %d", variant);
     }

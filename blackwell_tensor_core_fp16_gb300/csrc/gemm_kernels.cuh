@@ -62,6 +62,12 @@ __device__ __forceinline__ void report(uint32_t bits, volatile uint32_t* abort_f
     atomicOr(&gemm_f16_status_word, bits);
 }
 
+// Tiles a persistent unit (CTA or CTA pair) `c` of `units` processes: c, c + units, ...
+__device__ __forceinline__ uint32_t tiles_of(uint32_t c, uint32_t units, uint32_t num_tiles)
+{
+    return c < num_tiles ? (num_tiles - c + units - 1u) / units : 0u;
+}
+
 constexpr uint32_t kBlockM = 128;  // rows of A (and D) per CTA
 constexpr uint32_t kBlockK = 64;   // one 128-byte swizzle row of fp16
 constexpr uint32_t kUmmaK = 16;    // K per tcgen05.mma of kind::f16
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(128, 1)
 // ==============================================================================================
 // gemm_ws_kernel: persistent, warp-specialised, TMEM double-buffered.
 // ==============================================================================================
-template <int kCtaGroup, int kBlockN, int kStages>
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore = true>
 struct WsCfg {
     static_assert(kCtaGroup == 1 || kCtaGroup == 2, "a CTA or a CTA pair");
     static_assert(kBlockN % 64 == 0 && kBlockN >= 64 && kBlockN <= 256, "N tile");
@@ -217,7 +223,8 @@ struct WsCfg {
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + kStages * A_BYTES;
     static constexpr uint32_t OFF_D = OFF_B + kStages * B_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_D + 2 * D_BYTES;
+    // Two staging buffers for the TMA-store epilogue; none when the epilogue stores directly.
+    static constexpr uint32_t OFF_BAR = OFF_D + (kTmaStore ? 2 * D_BYTES : 0);
     static constexpr uint32_t NUM_BARS = 2 * kStages + 5;    // full, empty, tfull x2, tempty x2, drain
     static constexpr uint32_t OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ABORT = OFF_SLOT + 4;
@@ -227,15 +234,16 @@ struct WsCfg {
     static constexpr uint32_t EPI_THREADS = 128;
 };
 
-template <int kCtaGroup, int kBlockN, int kStages>
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore>
 __global__ void __launch_bounds__(192, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
-                   const __grid_constant__ CUtensorMap tmap_d, uint32_t M, uint32_t N,
+                   const __grid_constant__ CUtensorMap tmap_d, uint16_t* __restrict__ Dptr,
+                   uint32_t M, uint32_t N,
                    uint32_t num_m_blocks, uint32_t num_n_blocks, uint32_t num_k_blocks,
                    uint32_t group_m, uint64_t timeout_ns)
 {
-    using C = WsCfg<kCtaGroup, kBlockN, kStages>;
+    using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
     constexpr bool kPair = (kCtaGroup == 2);
     constexpr uint32_t idesc = make_idesc_f16(C::MMA_M, C::BN, 0);
 
@@ -291,99 +299,134 @@ __global__ void __launch_bounds__(192, 1)
 
     if (warp == 0) {
         // ---- TMA producer ------------------------------------------------------------------
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (uint32_t t = cid; ok && t < num_tiles; t += ncl) {
+        // The whole warp runs the loop, so every value it computes is warp-uniform; the waits'
+        // outcome is agreed by a vote, and one elected lane issues the copies.
+        const bool leader = elect_one_sync();
+        const uint32_t total = tiles_of(cid, ncl, num_tiles) * num_k_blocks;
+        uint32_t it = 0;
+        bool ok = true;
+        uint32_t t = cid;
+        uint32_t kb = 0;
+        int32_t m0 = 0, n0 = 0;
+        for (; it < total; ++it) {
+            if (kb == 0) {
                 const TileCoord tc = tile_coord(t, num_m_blocks, num_n_blocks, group_m);
-                const int32_t m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
-                const int32_t n0 = static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS);
-                for (uint32_t kb = 0; kb < num_k_blocks; ++kb, ++it) {
-                    const RingPos p = ring_pos(it, kStages);
-                    if (!mbar_wait<kPair>(empty_bar(p.stage), p.parity ^ 1u, abort_flag,
-                                          timeout_ns)) {
-                        report(kStatusProducerTimeout, abort_flag);
-                        ok = false;
-                        break;
-                    }
-                    const int32_t k0 = static_cast<int32_t>(kb * kBlockK);
-                    const uint32_t dA = sA + p.stage * C::A_BYTES;
-                    const uint32_t dB = sB + p.stage * C::B_BYTES;
-                    if constexpr (!kPair) {
-                        mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
-                        tma_load_2d(dA, &tmap_a, full_bar(p.stage), k0, m0);
-                        tma_load_2d(dB, &tmap_b, full_bar(p.stage), k0, n0);
-                    } else {
-                        if (rank == 0) mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
-                        const uint32_t fb = mapa_shared(full_bar(p.stage), 0);
-                        tma_load_2d_pair(dA, &tmap_a, fb, k0, m0);
-                        tma_load_2d_pair(dB, &tmap_b, fb, k0, n0);
-                    }
+                m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
+                n0 = static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS);
+            }
+            const RingPos p = ring_pos(it, kStages);
+            const bool w = mbar_wait<kPair>(empty_bar(p.stage), p.parity ^ 1u, abort_flag,
+                                            timeout_ns);
+            if (!__all_sync(0xffffffffu, w)) {
+                if (leader) report(kStatusProducerTimeout, abort_flag);
+                ok = false;
+                break;
+            }
+            if (leader) {
+                const int32_t k0 = static_cast<int32_t>(kb * kBlockK);
+                const uint32_t dA = sA + p.stage * C::A_BYTES;
+                const uint32_t dB = sB + p.stage * C::B_BYTES;
+                if constexpr (!kPair) {
+                    mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
+                    tma_load_2d(dA, &tmap_a, full_bar(p.stage), k0, m0);
+                    tma_load_2d(dB, &tmap_b, full_bar(p.stage), k0, n0);
+                } else {
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
+                    const uint32_t fb = mapa_shared(full_bar(p.stage), 0);
+                    tma_load_2d_pair(dA, &tmap_a, fb, k0, m0);
+                    tma_load_2d_pair(dB, &tmap_b, fb, k0, n0);
                 }
             }
-            // Every stage must be released by the MMAs before this CTA may exit: the last
-            // commits still arrive on the "empty" barriers (in a pair, from the other CTA).
-            // Iteration j is released when phase j / Stages of its stage's barrier completes.
-            const uint32_t first = it > kStages ? it - kStages : 0u;
-            if (ok) {
-                for (uint32_t j = first; j < it; ++j) {
-                    const RingPos p = ring_pos(j, kStages);
-                    if (!mbar_wait<kPair>(empty_bar(p.stage), p.parity, abort_flag, timeout_ns)) {
-                        report(kStatusDrainTimeout, abort_flag);
-                        break;
-                    }
+            __syncwarp();
+            if (++kb == num_k_blocks) {
+                kb = 0;
+                t += ncl;
+            }
+        }
+        // Every stage must be released by the MMAs before this CTA may exit: the last commits
+        // still arrive on the "empty" barriers (in a pair, from the other CTA).  Iteration j is
+        // released when phase j / Stages of its stage's barrier completes.
+        const uint32_t first = it > kStages ? it - kStages : 0u;
+        if (ok) {
+            for (uint32_t j = first; j < it; ++j) {
+                const RingPos p = ring_pos(j, kStages);
+                const bool w = mbar_wait<kPair>(empty_bar(p.stage), p.parity, abort_flag,
+                                                timeout_ns);
+                if (!__all_sync(0xffffffffu, w)) {
+                    if (leader) report(kStatusDrainTimeout, abort_flag);
+                    break;
                 }
-            } else if (rank == 0) {
-                // After an abort: wait (bounded, ignoring the abort flag) for loads still in
-                // flight into the ring, so none lands after this CTA has exited.
-                for (uint32_t j = first; j < it; ++j) {
-                    const RingPos p = ring_pos(j, kStages);
-                    if (!mbar_wait<kPair>(full_bar(p.stage), p.parity, nullptr, timeout_ns / 8))
-                        break;
-                }
+            }
+        } else if (rank == 0) {
+            // After an abort: wait (bounded, ignoring the abort flag) for loads still in flight
+            // into the ring, so none lands after this CTA has exited.
+            for (uint32_t j = first; j < it; ++j) {
+                const RingPos p = ring_pos(j, kStages);
+                const bool w = mbar_wait<kPair>(full_bar(p.stage), p.parity, nullptr,
+                                                timeout_ns / 8);
+                if (!__all_sync(0xffffffffu, w)) break;
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ---- MMA issuer (the even CTA of a pair issues for both) ----------------------------
-        if (rank == 0 && lane == 0) {
-            uint32_t it = 0;
+        // Warp-uniform loop as in the producer; one elected lane issues the MMAs and commits
+        // (a commit tracks the MMAs its own thread issued, so it is always the same lane).
+        if (rank == 0) {
+            const bool leader = elect_one_sync();
+            const uint32_t total = tiles_of(cid, ncl, num_tiles) * num_k_blocks;
+            uint32_t kb = 0;
             uint32_t acc = 0;
+            uint32_t d_tmem = tmem_base;
             bool ok = true;
             bool issued = false;
-            for (uint32_t t = cid; ok && t < num_tiles; t += ncl, ++acc) {
-                const uint32_t b = acc & 1u;
-                const uint32_t aph = (acc >> 1) & 1u;
-                if (!mbar_wait<kPair>(tempty_bar(b), aph ^ 1u, abort_flag, timeout_ns)) {
-                    report(kStatusMmaTimeout, abort_flag);
-                    ok = false;
-                    break;
-                }
-                tcgen05_fence_after();
-                const uint32_t d_tmem = tmem_base + b * C::BN;
-                for (uint32_t kb = 0; kb < num_k_blocks; ++kb, ++it) {
-                    const RingPos p = ring_pos(it, kStages);
-                    if (!mbar_wait<kPair>(full_bar(p.stage), p.parity, abort_flag, timeout_ns)) {
-                        report(kStatusMmaTimeout, abort_flag);
+            for (uint32_t it = 0; it < total; ++it) {
+                if (kb == 0) {
+                    // A new tile: wait until the epilogue has drained accumulator acc % 2.
+                    const uint32_t b = acc & 1u;
+                    const bool w = mbar_wait<kPair>(tempty_bar(b), ((acc >> 1) & 1u) ^ 1u,
+                                                    abort_flag, timeout_ns);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        if (leader) report(kStatusMmaTimeout, abort_flag);
                         ok = false;
                         break;
                     }
                     tcgen05_fence_after();
-                    const uint64_t ad = make_smem_desc_sw128(sA + p.stage * C::A_BYTES, 1024);
-                    const uint64_t bd = make_smem_desc_sw128(sB + p.stage * C::B_BYTES, 1024);
+                    d_tmem = tmem_base + b * C::BN;
+                }
+                const RingPos p = ring_pos(it, kStages);
+                const bool w = mbar_wait<kPair>(full_bar(p.stage), p.parity, abort_flag,
+                                                timeout_ns);
+                if (!__all_sync(0xffffffffu, w)) {
+                    if (leader) report(kStatusMmaTimeout, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tcgen05_fence_after();
+                const uint64_t ad = make_smem_desc_sw128(sA + p.stage * C::A_BYTES, 1024);
+                const uint64_t bd = make_smem_desc_sw128(sB + p.stage * C::B_BYTES, 1024);
+                if (leader) {
 #pragma unroll
                     for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
                         mma_f16<kCtaGroup>(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc,
                                            (kb | k) != 0u);
-                    issued = true;
                     if constexpr (kPair) mma_commit_pair(empty_bar(p.stage), 0x3);
                     else mma_commit(empty_bar(p.stage));
                 }
-                if (!ok) break;
-                if constexpr (kPair) mma_commit_pair(tfull_bar(b), 0x3);
-                else mma_commit(tfull_bar(b));
+                __syncwarp();
+                issued = true;
+                if (++kb == num_k_blocks) {
+                    // Tile done: the accumulator is ready for the epilogue once these MMAs are.
+                    if (leader) {
+                        if constexpr (kPair) mma_commit_pair(tfull_bar(acc & 1u), 0x3);
+                        else mma_commit(tfull_bar(acc & 1u));
+                    }
+                    __syncwarp();
+                    kb = 0;
+                    ++acc;
+                }
             }
-            if (!ok && issued) {
+            if (!ok && issued && leader) {
                 // Let every MMA issued so far finish before TMEM is freed.
                 if constexpr (kPair) mma_commit_pair(drain_bar, 0x1);
                 else mma_commit(drain_bar);
@@ -443,28 +486,46 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         p[16 + i] = pack_f16x2_rn(v1[2 * i], v1[2 * i + 1]);
-                    // The store issued two sub-tiles ago read this buffer; wait until it has.
-                    if (et == 0) bulk_wait_group_read<1>();
-                    __syncwarp();
-                    named_barrier_sync(1, C::EPI_THREADS);
-                    const uint32_t dbuf = sD + sbuf * C::D_BYTES;
+                    if constexpr (kTmaStore) {
+                        // The store issued two sub-tiles ago read this buffer; wait until it has.
+                        if (et == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                        named_barrier_sync(1, C::EPI_THREADS);
+                        const uint32_t dbuf = sD + sbuf * C::D_BYTES;
 #pragma unroll
-                    for (uint32_t j = 0; j < 8; ++j)
-                        st_shared_v4(dbuf + sw128(row * 128u + j * 16u), p[4 * j], p[4 * j + 1],
-                                     p[4 * j + 2], p[4 * j + 3]);
-                    fence_proxy_async_smem();
-                    named_barrier_sync(1, C::EPI_THREADS);
-                    if (et == 0) {
-                        tma_store_2d(&tmap_d, dbuf, col0, m0);
-                        bulk_commit_group();
+                        for (uint32_t j = 0; j < 8; ++j)
+                            st_shared_v4(dbuf + sw128(row * 128u + j * 16u), p[4 * j],
+                                         p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        named_barrier_sync(1, C::EPI_THREADS);
+                        if (et == 0) {
+                            tma_store_2d(&tmap_d, dbuf, col0, m0);
+                            bulk_commit_group();
+                        }
+                        __syncwarp();
+                        sbuf ^= 1u;
+                    } else {
+                        // Each thread writes its own row: 64 fp16 as 8 16-byte vectors; the
+                        // L2 merges the warp's 32 partial lines into full lines.
+                        const int32_t grow = m0 + static_cast<int32_t>(row);
+                        if (grow < static_cast<int32_t>(M)) {
+                            uint16_t* drow = Dptr + static_cast<uint64_t>(grow) * N;
+#pragma unroll
+                            for (uint32_t j = 0; j < 8; ++j) {
+                                const int32_t col = col0 + static_cast<int32_t>(8u * j);
+                                if (col < static_cast<int32_t>(N))  // N % 8 == 0
+                                    st_global_v4(drow + col, p[4 * j], p[4 * j + 1],
+                                                 p[4 * j + 2], p[4 * j + 3]);
+                            }
+                        }
                     }
-                    __syncwarp();
-                    sbuf ^= 1u;
                 }
             }
         }
         (void)ok;
-        if (et == 0) bulk_wait_group_all();
+        if constexpr (kTmaStore) {
+            if (et == 0) bulk_wait_group_all();
+        }
         __syncwarp();
     }
 

@@ -64,6 +64,17 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// True in exactly one lane of the (converged) warp: the lowest active lane.
+__device__ __forceinline__ bool elect_one_sync()
+{
+    uint32_t pred = 0;
+    asm volatile("{\n\t.reg .pred P;\n\t"
+                 "elect.sync _|P, 0xffffffff;\n\t"
+                 "selp.u32 %0, 1, 0, P;\n\t}"
+                 : "=r"(pred));
+    return pred != 0;
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32); id 0 is __syncthreads' barrier.
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads)
 {

@@ -52,7 +52,8 @@ extern "C" {
 #define GEMM_F16_VARIANT_WS_128x256 2 /* persistent, warp-specialised, 1 CTA per 128x256 tile */
 #define GEMM_F16_VARIANT_WS_PAIR 3    /* persistent, warp-specialised, CTA pair per 256x256 */
 #define GEMM_F16_VARIANT_WS_128x128 4 /* persistent, warp-specialised, 1 CTA per 128x128 tile */
-#define GEMM_F16_NUM_VARIANTS 5
+#define GEMM_F16_VARIANT_WS_PAIR_DIRECT 5 /* as WS_PAIR, 7 stages, epilogue stores from registers */
+#define GEMM_F16_NUM_VARIANTS 6
 
 /*
  * D = A * B^T for fp16 A (M x K), B (N x K), D (M x N), fp32 accumulation, on `stream`.
