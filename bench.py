@@ -47,8 +47,9 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--only", default="", help="comma-separated subset of the step's workloads")
     p.add_argument("--skip-e2e", action="store_true")
-    p.add_argument("--cublas-steps", type=int, default=20,
-                   help="launches of torch.matmul on the same shapes, for context (0: skip)")
+    p.add_argument("--cublas-steps", type=int, default=-1,
+                   help="steps of torch.mm on the same shapes, for context (-1: as many as "
+                        "--steps, 0: skip)")
     return p.parse_args()
 
 
@@ -349,24 +350,40 @@ def run_ours(args):
                 "achieved_def": "algorithmic 2*M*N*K over both launches of a step / summed "
                                 "CUDA-event launch durations"}
 
-    # cuBLAS (torch.matmul) on the same resident inputs, for context only
+    # cuBLAS (torch.mm) on the same resident inputs and the same step, run back to back for the
+    # same number of steps right after ours so both see the same power-capped clocks.  Context
+    # only: it is a library kernel, not part of this path.
     cublas = None
-    if args.cublas_steps > 0:
-        cublas = {}
-        for (w, Ad, Bd, D, variant) in work:
-            with torch.cuda.stream(stream):
-                for _ in range(3):
+    if args.cublas_steps != 0:
+        csteps = K if args.cublas_steps < 0 else args.cublas_steps
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                for (w, Ad, Bd, D, variant) in work:
                     torch.mm(Ad, Bd.t(), out=D)
-                c0 = torch.cuda.Event(enable_timing=True)
-                c1 = torch.cuda.Event(enable_timing=True)
-                c0.record(stream)
-                for _ in range(args.cublas_steps):
+        torch.cuda.synchronize()
+        cev = [torch.cuda.Event(enable_timing=True) for _ in range(len(work) * csteps + 1)]
+        csampler = ClockSampler(uuid)
+        csampler.start()
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            cev[0].record(stream)
+            e = 1
+            for _ in range(csteps):
+                for (w, Ad, Bd, D, variant) in work:
                     torch.mm(Ad, Bd.t(), out=D)
-                c1.record(stream)
-            torch.cuda.synchronize()
-            ms = c0.elapsed_time(c1) / args.cublas_steps
-            cublas[w.name] = {"ms_per_launch": ms,
-                              "tflops": 2.0 * w.M * w.N * w.K / (ms * 1e-3) / 1e12}
+                    cev[e].record(stream)
+                    e += 1
+        torch.cuda.synchronize()
+        cclk = csampler.stop()
+        cd = [cev[i].elapsed_time(cev[i + 1]) for i in range(len(cev) - 1)]
+        ctot = cev[0].elapsed_time(cev[-1])
+        cublas = {"value": csteps * flops_step / (ctot * 1e-3) / 1e12, "unit": "TFLOP/s",
+                  "steps": csteps, "clocks": cclk, "per_workload": {}}
+        for j, (w, *_r) in enumerate(work):
+            ms = sum(cd[j::len(work)]) / csteps
+            cublas["per_workload"][w.name] = {"ms_per_launch": ms,
+                                              "tflops": 2.0 * w.M * w.N * w.K / (ms * 1e-3) / 1e12}
+        cublas["ours_over_cublas"] = value / world / cublas["value"]
 
     # End to end through the public API: every step copies its inputs from pinned host memory
     # to the device, runs the GEMMs with gemm(), and copies each result back to pinned host
@@ -459,7 +476,7 @@ def run_ours(args):
             "device": props.name, "sms": num_sms,
         },
         "per_workload": per,
-        "cublas_fp16_same_shapes": cublas,
+        "cublas_fp16_same_step": cublas,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
