@@ -51,6 +51,25 @@ uint64_t wait_timeout_ns()
     return v;
 }
 
+// L2 priorities for the A and B loads: bits 1:0 A, bits 3:2 B (0 normal, 1 evict_first,
+// 2 evict_last).  Default: A evict_last (a band of A rows is reused by every tile of its group
+// of tile-rows across several waves), B normal; measured 0.5-1.5% faster under the power cap
+// than no hint.  GEMM_F16_L2_A / GEMM_F16_L2_B = normal | first | last override.
+uint32_t l2_hint_setting()
+{
+    static const uint32_t v = [] {
+        auto parse = [](const char* s, uint32_t dflt) -> uint32_t {
+            if (!s) return dflt;
+            if (!std::strcmp(s, "first")) return 1u;
+            if (!std::strcmp(s, "last")) return 2u;
+            return 0u;
+        };
+        return parse(std::getenv("GEMM_F16_L2_A"), 2u) |
+               (parse(std::getenv("GEMM_F16_L2_B"), 0u) << 2);
+    }();
+    return v;
+}
+
 uint32_t group_m_setting()
 {
     static const uint32_t v = [] {
@@ -324,7 +343,7 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *ma, *mb, *md, static_cast<uint16_t*>(D),
                                        (uint32_t)M, (uint32_t)N,
                                        (uint32_t)num_m, (uint32_t)num_n, (uint32_t)cdiv(K, 64),
-                                       group_m_setting(), wait_timeout_ns());
+                                       group_m_setting(), wait_timeout_ns(), l2_hint_setting());
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_ws_kernel)");
     return GEMM_F16_OK;
 }

@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(192, 1)
                    const __grid_constant__ CUtensorMap tmap_d, uint16_t* __restrict__ Dptr,
                    uint32_t M, uint32_t N,
                    uint32_t num_m_blocks, uint32_t num_n_blocks, uint32_t num_k_blocks,
-                   uint32_t group_m, uint64_t timeout_ns)
+                   uint32_t group_m, uint64_t timeout_ns, uint32_t l2_hints)
 {
     using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
     constexpr bool kPair = (kCtaGroup == 2);
@@ -302,6 +302,9 @@ __global__ void __launch_bounds__(192, 1)
         // The whole warp runs the loop, so every value it computes is warp-uniform; the waits'
         // outcome is agreed by a vote, and one elected lane issues the copies.
         const bool leader = elect_one_sync();
+        // L2 priorities of A and B loads (bits 1:0 and 3:2 of l2_hints; 0 = normal).
+        const uint64_t pol_a = make_l2_policy(l2_hints & 3u);
+        const uint64_t pol_b = make_l2_policy((l2_hints >> 2) & 3u);
         const uint32_t total = tiles_of(cid, ncl, num_tiles) * num_k_blocks;
         uint32_t it = 0;
         bool ok = true;
@@ -328,13 +331,13 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t dB = sB + p.stage * C::B_BYTES;
                 if constexpr (!kPair) {
                     mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
-                    tma_load_2d(dA, &tmap_a, full_bar(p.stage), k0, m0);
-                    tma_load_2d(dB, &tmap_b, full_bar(p.stage), k0, n0);
+                    tma_load_2d_hint(dA, &tmap_a, full_bar(p.stage), k0, m0, pol_a);
+                    tma_load_2d_hint(dB, &tmap_b, full_bar(p.stage), k0, n0, pol_b);
                 } else {
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
                     const uint32_t fb = mapa_shared(full_bar(p.stage), 0);
-                    tma_load_2d_pair(dA, &tmap_a, fb, k0, m0);
-                    tma_load_2d_pair(dB, &tmap_b, fb, k0, n0);
+                    tma_load_2d_pair_hint(dA, &tmap_a, fb, k0, m0, pol_a);
+                    tma_load_2d_pair_hint(dB, &tmap_b, fb, k0, n0, pol_b);
                 }
             }
             __syncwarp();

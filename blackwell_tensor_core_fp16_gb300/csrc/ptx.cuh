@@ -211,6 +211,43 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
                  : "memory");
 }
 
+// L2 eviction-priority policy for TMA loads (createpolicy, fraction 1.0).
+// priority: 0 = evict_normal, 1 = evict_first, 2 = evict_last.
+__device__ __forceinline__ uint64_t make_l2_policy(uint32_t priority)
+{
+    uint64_t pol;
+    if (priority == 1)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else if (priority == 2)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 2-D tiled load with an L2 eviction-priority hint.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+                 : "memory");
+}
+
+// CTA-pair form of tma_load_2d_hint (see tma_load_2d_pair).
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t bar_cluster, int32_t x, int32_t y,
+                                                      uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+                 ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(
+                     dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y),
+                 "l"(policy)
+                 : "memory");
+}
+
 // Same, for a CTA pair: the destination is this CTA's shared memory, and the completion
 // barrier may be the peer CTA's (a shared::cluster address from mapa_shared).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
