@@ -20,6 +20,8 @@ __all__ = [
     "gemm_f16_nt", "gemm_f16_nt_variant", "gemm_f16_choose_variant", "gemm_f16_check_status",
     "gemm_f16_last_error", "gemm_f16_version", "gemm_f16_get_variant_info", "gemm_f16_idesc",
     "gemm_f16_smem_desc_sw128", "gemm_f16_sw128", "gemm_f16_tile_coord", "gemm_f16_ring_pos",
+    "gemm_f16_nt_ws", "gemm_f16_nt_ex", "gemm_f16_workspace_bytes", "gemm_f16_sk_tail_tiles",
+    "gemm_f16_sk_items", "gemm_f16_sk_item", "gemm_f16_sk_unit_of",
     "exported_symbols", "VARIANTS", "STATUS",
 ]
 
@@ -89,6 +91,21 @@ def load():
         lib.gemm_f16_tile_coord.restype = None
         lib.gemm_f16_ring_pos.argtypes = [u32, u32, u32p, u32p]
         lib.gemm_f16_ring_pos.restype = None
+        sz = ctypes.c_size_t
+        lib.gemm_f16_nt_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+        lib.gemm_f16_nt_ws.restype = i32
+        lib.gemm_f16_nt_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
+        lib.gemm_f16_nt_ex.restype = i32
+        lib.gemm_f16_workspace_bytes.argtypes = [i64, i64, i64, i32, ctypes.POINTER(sz)]
+        lib.gemm_f16_workspace_bytes.restype = i32
+        lib.gemm_f16_sk_tail_tiles.argtypes = [i64, i64, i64]
+        lib.gemm_f16_sk_tail_tiles.restype = i64
+        lib.gemm_f16_sk_items.argtypes = [u32, u32, u32, u32, u32]
+        lib.gemm_f16_sk_items.restype = u32
+        lib.gemm_f16_sk_item.argtypes = [u32, u32, u32, u32, u32, u32, u32p]
+        lib.gemm_f16_sk_item.restype = None
+        lib.gemm_f16_sk_unit_of.argtypes = [u32, u32, u32, u32, u32]
+        lib.gemm_f16_sk_unit_of.restype = u32
         _lib = lib
         return lib
 
@@ -102,6 +119,42 @@ def gemm_f16_nt(A: int, B: int, D: int, M: int, N: int, K: int, stream: int = 0)
 def gemm_f16_nt_variant(A: int, B: int, D: int, M: int, N: int, K: int, stream: int,
                         variant: int) -> int:
     return load().gemm_f16_nt_variant(A, B, D, M, N, K, stream, variant)
+
+
+def gemm_f16_nt_ws(A: int, B: int, D: int, M: int, N: int, K: int, workspace: int,
+                   workspace_bytes: int, stream: int = 0) -> int:
+    return load().gemm_f16_nt_ws(A, B, D, M, N, K, workspace, workspace_bytes, stream)
+
+
+def gemm_f16_nt_ex(A: int, B: int, D: int, M: int, N: int, K: int, variant: int,
+                   workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    return load().gemm_f16_nt_ex(A, B, D, M, N, K, variant, workspace, workspace_bytes, stream)
+
+
+def gemm_f16_workspace_bytes(M: int, N: int, K: int, variant: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    rc = load().gemm_f16_workspace_bytes(M, N, K, variant, ctypes.byref(out))
+    if rc != OK:
+        raise GemmError(rc, gemm_f16_last_error())
+    return out.value
+
+
+def gemm_f16_sk_tail_tiles(tiles: int, units: int, k_blocks: int) -> int:
+    return load().gemm_f16_sk_tail_tiles(tiles, units, k_blocks)
+
+
+def gemm_f16_sk_items(tiles: int, units: int, k_blocks: int, tail: int, unit: int) -> int:
+    return load().gemm_f16_sk_items(tiles, units, k_blocks, tail, unit)
+
+
+def gemm_f16_sk_item(tiles: int, units: int, k_blocks: int, tail: int, unit: int, idx: int):
+    out = (ctypes.c_uint32 * 5)()
+    load().gemm_f16_sk_item(tiles, units, k_blocks, tail, unit, idx, out)
+    return tuple(out)
+
+
+def gemm_f16_sk_unit_of(tiles: int, units: int, k_blocks: int, tail: int, x: int) -> int:
+    return load().gemm_f16_sk_unit_of(tiles, units, k_blocks, tail, x)
 
 
 def gemm_f16_choose_variant(M: int, N: int, K: int, num_sms: int) -> int:
@@ -173,11 +226,14 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def gemm(A, B, out=None, variant: int | str = 0, stream=None):
+def gemm(A, B, out=None, variant: int | str = 0, stream=None, workspace=True):
     """D = A @ B.T for CUDA fp16 tensors A (M, K) and B (N, K); returns D (M, N) fp16.
 
     ``out`` may be a preallocated contiguous (M, N) fp16 CUDA tensor.  The call is asynchronous
-    on ``stream`` (default: torch's current stream).  Raises GemmError on a non-zero status.
+    on ``stream`` (default: torch's current stream).  ``workspace``: True (default) takes a
+    stream-K workspace from torch's caching allocator when the shape benefits from one; a CUDA
+    uint8 tensor supplies one; False or None runs without.  Raises GemmError on a non-zero
+    status.
     """
     import torch
     if isinstance(variant, str):
@@ -194,11 +250,28 @@ def gemm(A, B, out=None, variant: int | str = 0, stream=None):
     elif (out.dtype != torch.float16 or not out.is_cuda or tuple(out.shape) != (M, N)
           or not out.is_contiguous()):
         raise ValueError("out must be a contiguous (M, N) CUDA float16 tensor")
-    rc = gemm_f16_nt_variant(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
-                             _stream_handle(stream), int(variant))
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is True and M and N and K:
+        need = gemm_f16_workspace_bytes(M, N, K, int(variant))
+        if need:
+            s = stream if stream is not None else torch.cuda.current_stream()
+            with torch.cuda.stream(s) if hasattr(s, "cuda_stream") else _nullctx():
+                workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+    if workspace is not None and workspace is not True and workspace is not False:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = gemm_f16_nt_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, int(variant),
+                        ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != OK:
         raise GemmError(rc, gemm_f16_last_error())
     return out
+
+
+class _nullctx:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
 
 
 def check_status(stream=None) -> None:

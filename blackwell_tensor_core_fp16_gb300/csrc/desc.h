@@ -109,4 +109,81 @@ GF16_HD TileCoord tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_
     return TileCoord{first_m + r % gsize, r / gsize};
 }
 
+// ---------------------------------------------------------------------------------------------
+// Work split of the persistent kernel with a stream-K tail.  T tiles, U persistent units (CTAs
+// or CTA pairs), KB k-blocks per tile, and R tail tiles (R = 0: pure data-parallel).
+//   * data-parallel part: tiles [0, T - R); unit c takes c, c + U, ... (T - R is a multiple of U
+//     when R > 0, so every unit gets W = (T - R) / U of them);
+//   * stream-K part: the R tail tiles' k-blocks, numbered x = r * KB + kb over [0, R * KB), are
+//     cut into S contiguous ranges [lo_c, hi_c) with lo_c = floor(c * R * KB / S), one for each
+//     of units 0 .. S-1 (S <= U); each range is split at tile boundaries into pieces.  With
+//     R <= S a range is at most KB long, so a unit has at most two pieces, and a tail tile has
+//     at most ceil(S / R) + 1 contributors.
+// A piece that does not cover its whole tile is "partial": its fp32 accumulator is summed with
+// the other pieces of that tile by whichever contributor finishes last.
+// ---------------------------------------------------------------------------------------------
+struct WorkSplit {
+    uint32_t T, U, KB, R;
+    uint32_t S;  // units sharing the stream-K k-blocks (units S .. U-1 get none); S <= U
+};
+
+struct WorkItem {
+    uint32_t tile;     // tile number in the grouped order
+    uint32_t kb0;      // first k-block
+    uint32_t kb1;      // one past the last k-block
+    uint32_t piece;    // 0 or 1 for stream-K pieces (workspace slot), unused otherwise
+    uint32_t partial;  // 1 if the piece's accumulator must be combined with others
+};
+
+GF16_HD uint32_t sk_lo(const WorkSplit& w, uint32_t c)
+{
+    const uint32_t cc = c < w.S ? c : w.S;
+    return static_cast<uint32_t>((static_cast<uint64_t>(cc) * w.R * w.KB) / w.S);
+}
+
+GF16_HD uint32_t dp_tiles_of(const WorkSplit& w, uint32_t c)
+{
+    const uint32_t dp = w.T - w.R;
+    if (w.R > 0) return dp / w.U;
+    return c < dp ? (dp - c + w.U - 1) / w.U : 0u;
+}
+
+GF16_HD uint32_t sk_pieces_of(const WorkSplit& w, uint32_t c)
+{
+    if (w.R == 0) return 0u;
+    const uint32_t lo = sk_lo(w, c), hi = sk_lo(w, c + 1);
+    return hi > lo ? (hi - 1) / w.KB - lo / w.KB + 1 : 0u;
+}
+
+GF16_HD uint32_t items_of(const WorkSplit& w, uint32_t c)
+{
+    return dp_tiles_of(w, c) + sk_pieces_of(w, c);
+}
+
+// Total k-block iterations of unit c (the pipeline counters run over these).
+GF16_HD uint32_t iterations_of(const WorkSplit& w, uint32_t c)
+{
+    return dp_tiles_of(w, c) * w.KB + (w.R ? sk_lo(w, c + 1) - sk_lo(w, c) : 0u);
+}
+
+GF16_HD WorkItem work_item(const WorkSplit& w, uint32_t c, uint32_t idx)
+{
+    const uint32_t ndp = dp_tiles_of(w, c);
+    if (idx < ndp) return WorkItem{c + idx * w.U, 0u, w.KB, 0u, 0u};
+    const uint32_t j = idx - ndp;
+    const uint32_t lo = sk_lo(w, c), hi = sk_lo(w, c + 1);
+    const uint32_t r = lo / w.KB + j;
+    const uint32_t start = (j == 0 ? lo : r * w.KB) - r * w.KB;
+    const uint32_t end = (hi < (r + 1) * w.KB ? hi : (r + 1) * w.KB) - r * w.KB;
+    const uint32_t partial = (start != 0u || end != w.KB) ? 1u : 0u;
+    return WorkItem{w.T - w.R + r, start, end, j, partial};
+}
+
+// The unit whose stream-K range holds tail k-block x.
+GF16_HD uint32_t sk_unit_of(const WorkSplit& w, uint32_t x)
+{
+    return static_cast<uint32_t>(((static_cast<uint64_t>(x) + 1u) * w.S - 1u) /
+                                 (static_cast<uint64_t>(w.R) * w.KB));
+}
+
 }  // namespace gf16

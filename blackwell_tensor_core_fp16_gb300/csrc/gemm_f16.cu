@@ -285,17 +285,45 @@ int launch_tile(const void* A, const void* B, void* D, int64_t M, int64_t N, int
     return GEMM_F16_OK;
 }
 
+// Units that share the stream-K tail of R tiles: at most 3 per tile, so a tile has at most
+// 4 contributors (the kernel's fix-up keeps up to 4 partial loads in flight per slice).
+int64_t sk_units_for(int64_t R, int64_t U)
+{
+    return R * 3 < U ? R * 3 : U;
+}
+
+// Stream-K tail size for T tiles of KB k-blocks on U units: the tiles of the last, partial
+// wave (all tiles when T < U), or 0 when the tail is nearly a full wave or the per-unit pieces
+// would be tiny.
+int64_t sk_tail_tiles(int64_t T, int64_t U, int64_t KB)
+{
+    if (T <= 0 || U <= 0) return 0;
+    const int64_t R = T < U ? T : T % U;
+    if (R == 0) return 0;
+    if (R * 10 > U * 9) return 0;   // the last wave is at least 90% full already
+    if (R * KB < 4 * sk_units_for(R, U)) return 0;   // under 4 k-blocks per unit
+    return R;
+}
+
+// Workspace layout: [counters, kWsCountBytes][partials: units x 2 pieces x cta_group x
+// 128 x BN fp32].  Counters must be zero when a launch starts; the host clears the ones a
+// launch uses with cudaMemsetAsync on the launch's stream.
+constexpr size_t kWsCountBytes = 4096;
+
+size_t ws_bytes_for(int64_t units, int cta_group, int block_n)
+{
+    return kWsCountBytes + static_cast<size_t>(units) * 2u * cta_group * 128u * block_n * 4u;
+}
+
 template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore>
 int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
-              cudaStream_t stream, DeviceState& d, int dev)
+              cudaStream_t stream, DeviceState& d, int dev, void* workspace = nullptr,
+              size_t workspace_bytes = 0, size_t* bytes_needed = nullptr)
 {
     using C = gf16::WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
     auto kernel = gf16::gemm_ws_kernel<kCtaGroup, kBlockN, kStages, kTmaStore>;
     int rc = ensure_smem(d, variant, kernel, C::SMEM_ALLOC);
     if (rc != GEMM_F16_OK) return rc;
-    const CUtensorMap *ma, *mb, *md;
-    MapKey key{A, B, D, M, N, K, variant, dev};
-    if ((rc = get_maps(key, 128, C::B_ROWS, kTmaStore, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
 
     const int64_t num_m = cdiv(M, C::MMA_M);
     const int64_t num_n = cdiv(N, C::BN);
@@ -327,23 +355,45 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
             }
             units = d.pair_clusters[variant];
         }
-        const int64_t clusters = tiles < units ? tiles : units;
-        cfg.gridDim = dim3(static_cast<uint32_t>(2 * clusters));
     } else {
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
-        const int64_t ctas = tiles < units ? tiles : units;
-        cfg.gridDim = dim3(static_cast<uint32_t>(ctas));
     }
-    // Pipeline positions are 32-bit counters over a CTA's (tile, k-block) iterations.
-    const int64_t units_used = cfg.gridDim.x / kCtaGroup;
-    if (cdiv(tiles, units_used) * cdiv(K, 64) >= (int64_t(1) << 31))
+    const int64_t KB = cdiv(K, 64);
+    // Stream-K tail: all units take part; otherwise no more units than tiles.
+    int64_t R = sk_tail_tiles(tiles, units, KB);
+    const size_t need = R ? ws_bytes_for(units, kCtaGroup, kBlockN) : 0;
+    if (bytes_needed) {
+        *bytes_needed = need;
+        return GEMM_F16_OK;
+    }
+    const CUtensorMap *ma, *mb, *md;
+    MapKey key{A, B, D, M, N, K, variant, dev};
+    if ((rc = get_maps(key, 128, C::B_ROWS, kTmaStore, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
+    if (R && (workspace == nullptr || workspace_bytes < need ||
+              (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        R = 0;  // no usable workspace: plain data-parallel schedule
+    const int64_t units_used = R ? units : (tiles < units ? tiles : units);
+    cfg.gridDim = dim3(static_cast<uint32_t>(kCtaGroup * units_used));
+    // Pipeline positions are 32-bit counters over a unit's k-block iterations.
+    if ((cdiv(tiles - R, units_used) + 1) * KB >= (int64_t(1) << 31))
         return fail(GEMM_F16_ERR_UNSUPPORTED, "problem too large for one launch (M=%lld N=%lld "
                     "K=%lld)", (long long)M, (long long)N, (long long)K);
+    uint32_t* ws_count = nullptr;
+    float* ws_part = nullptr;
+    if (R) {
+        ws_count = static_cast<uint32_t*>(workspace);
+        ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsCountBytes);
+        cudaError_t e = cudaMemsetAsync(ws_count, 0, static_cast<size_t>(R) * kCtaGroup * 4u,
+                                        stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(stream-K counters)");
+    }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *ma, *mb, *md, static_cast<uint16_t*>(D),
                                        (uint32_t)M, (uint32_t)N,
-                                       (uint32_t)num_m, (uint32_t)num_n, (uint32_t)cdiv(K, 64),
-                                       group_m_setting(), wait_timeout_ns(), l2_hint_setting());
+                                       (uint32_t)num_m, (uint32_t)num_n, (uint32_t)KB,
+                                       group_m_setting(), wait_timeout_ns(), l2_hint_setting(),
+                                       ws_part, ws_count, (uint32_t)R,
+                                       (uint32_t)(R ? sk_units_for(R, units_used) : units_used));
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_ws_kernel)");
     return GEMM_F16_OK;
 }
@@ -372,14 +422,18 @@ int check_args(const void* A, const void* B, void* D, int64_t M, int64_t N, int6
 }
 
 int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
-        cudaStream_t stream, int variant)
+        cudaStream_t stream, int variant, void* ws = nullptr, size_t ws_bytes = 0,
+        size_t* bytes_needed = nullptr)
 {
     t_last_error.clear();
+    if (bytes_needed) *bytes_needed = 0;
     if (variant < 0 || variant >= GEMM_F16_NUM_VARIANTS)
         return fail(GEMM_F16_ERR_INVALID_ARG, "unknown variant %d", variant);
-    int rc = check_args(A, B, D, M, N, K);
+    int rc = bytes_needed ? GEMM_F16_OK : check_args(A, B, D, M, N, K);
     if (rc != GEMM_F16_OK) return rc;
+    if (M < 0 || N < 0 || K < 0) return fail(GEMM_F16_ERR_INVALID_ARG, "negative size");
     if (M == 0 || N == 0) return GEMM_F16_OK;
+    if (bytes_needed && K == 0) return GEMM_F16_OK;
     if (K == 0) {
         cudaError_t e = cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream);
         return e == cudaSuccess ? GEMM_F16_OK : cuda_fail(e, "cudaMemsetAsync");
@@ -391,15 +445,20 @@ int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
     if (variant == GEMM_F16_VARIANT_AUTO) variant = choose_variant(M, N, K, d->sms);
     switch (variant) {
     case GEMM_F16_VARIANT_TILE:
+        if (bytes_needed) return GEMM_F16_OK;
         return launch_tile(A, B, D, M, N, K, stream, *d, dev);
     case GEMM_F16_VARIANT_WS_128x256:
-        return launch_ws<1, 256, 4, true>(variant, A, B, D, M, N, K, stream, *d, dev);
+        return launch_ws<1, 256, 4, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                          ws_bytes, bytes_needed);
     case GEMM_F16_VARIANT_WS_PAIR:
-        return launch_ws<2, 256, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev);
+        return launch_ws<2, 256, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                          ws_bytes, bytes_needed);
     case GEMM_F16_VARIANT_WS_128x128:
-        return launch_ws<1, 128, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev);
+        return launch_ws<1, 128, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                          ws_bytes, bytes_needed);
     case GEMM_F16_VARIANT_WS_PAIR_DIRECT:
-        return launch_ws<2, 256, 7, false>(variant, A, B, D, M, N, K, stream, *d, dev);
+        return launch_ws<2, 256, 7, false>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                           ws_bytes, bytes_needed);
     default:
         return fail(GEMM_F16_ERR_INVALID_ARG, "unknown variant %d", variant);
     }
@@ -420,6 +479,24 @@ int gemm_f16_nt_variant(const void* A, const void* B, void* D, int64_t M, int64_
                         cudaStream_t stream, int variant)
 {
     return run(A, B, D, M, N, K, stream, variant);
+}
+
+int gemm_f16_nt_ws(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return run(A, B, D, M, N, K, stream, GEMM_F16_VARIANT_AUTO, workspace, workspace_bytes);
+}
+
+int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                   int variant, void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return run(A, B, D, M, N, K, stream, variant, workspace, workspace_bytes);
+}
+
+int gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, size_t* bytes)
+{
+    if (!bytes) return fail(GEMM_F16_ERR_INVALID_ARG, "bytes is null");
+    return run(nullptr, nullptr, nullptr, M, N, K, nullptr, variant, nullptr, 0, bytes);
 }
 
 int gemm_f16_choose_variant(int64_t M, int64_t N, int64_t K, int num_sms)
@@ -473,6 +550,41 @@ void gemm_f16_tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_t gr
     const gf16::TileCoord c = gf16::tile_coord(t, num_m, num_n, group);
     if (m_blk) *m_blk = c.m_blk;
     if (n_blk) *n_blk = c.n_blk;
+}
+
+int64_t gemm_f16_sk_tail_tiles(int64_t tiles, int64_t units, int64_t k_blocks)
+{
+    return sk_tail_tiles(tiles, units, k_blocks);
+}
+
+static gf16::WorkSplit host_split(uint32_t tiles, uint32_t units, uint32_t k_blocks,
+                                  uint32_t tail)
+{
+    const uint32_t S = tail ? static_cast<uint32_t>(sk_units_for(tail, units)) : units;
+    return gf16::WorkSplit{tiles, units, k_blocks, tail, S};
+}
+
+uint32_t gemm_f16_sk_items(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t tail,
+                           uint32_t unit)
+{
+    return gf16::items_of(host_split(tiles, units, k_blocks, tail), unit);
+}
+
+void gemm_f16_sk_item(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t tail,
+                      uint32_t unit, uint32_t idx, uint32_t out[5])
+{
+    const gf16::WorkItem w = gf16::work_item(host_split(tiles, units, k_blocks, tail), unit, idx);
+    out[0] = w.tile;
+    out[1] = w.kb0;
+    out[2] = w.kb1;
+    out[3] = w.piece;
+    out[4] = w.partial;
+}
+
+uint32_t gemm_f16_sk_unit_of(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t tail,
+                             uint32_t x)
+{
+    return gf16::sk_unit_of(host_split(tiles, units, k_blocks, tail), x);
 }
 
 void gemm_f16_ring_pos(uint32_t it, uint32_t stages, uint32_t* stage, uint32_t* parity)

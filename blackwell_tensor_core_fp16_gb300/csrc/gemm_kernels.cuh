@@ -69,6 +69,7 @@ __device__ __forceinline__ uint32_t tiles_of(uint32_t c, uint32_t units, uint32_
 }
 
 constexpr uint32_t kBlockM = 128;  // rows of A (and D) per CTA
+constexpr uint32_t kMaxContrib = 4;  // most stream-K pieces one tile is split into
 constexpr uint32_t kBlockK = 64;   // one 128-byte swizzle row of fp16
 constexpr uint32_t kUmmaK = 16;    // K per tcgen05.mma of kind::f16
 
@@ -228,7 +229,10 @@ struct WsCfg {
     static constexpr uint32_t NUM_BARS = 2 * kStages + 5;    // full, empty, tfull x2, tempty x2, drain
     static constexpr uint32_t OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ABORT = OFF_SLOT + 4;
-    static constexpr uint32_t SMEM_ALLOC = OFF_ABORT + 4 + 1024;  // + slack to align the base
+    static constexpr uint32_t OFF_EPI_WORD = OFF_ABORT + 4;      // epilogue broadcast word
+    static constexpr uint32_t SMEM_ALLOC = OFF_EPI_WORD + 4 + 1024;  // + slack to align the base
+    // Stream-K workspace: one fp32 partial accumulator per (unit, piece, CTA of the pair).
+    static constexpr uint32_t PART_FLOATS = kBlockM * kBlockN;
     static_assert(SMEM_ALLOC <= 232448, "shared memory per CTA");
     static constexpr uint32_t THREADS = 192;
     static constexpr uint32_t EPI_THREADS = 128;
@@ -241,7 +245,9 @@ __global__ void __launch_bounds__(192, 1)
                    const __grid_constant__ CUtensorMap tmap_d, uint16_t* __restrict__ Dptr,
                    uint32_t M, uint32_t N,
                    uint32_t num_m_blocks, uint32_t num_n_blocks, uint32_t num_k_blocks,
-                   uint32_t group_m, uint64_t timeout_ns, uint32_t l2_hints)
+                   uint32_t group_m, uint64_t timeout_ns, uint32_t l2_hints,
+                   float* __restrict__ ws_part, uint32_t* __restrict__ ws_count,
+                   uint32_t sk_tiles, uint32_t sk_units)
 {
     using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
     constexpr bool kPair = (kCtaGroup == 2);
@@ -269,6 +275,10 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t cid = kPair ? cluster_id_x() : blockIdx.x;
     const uint32_t ncl = kPair ? num_clusters_x() : gridDim.x;
     const uint32_t num_tiles = num_m_blocks * num_n_blocks;
+    // Work of this unit: its data-parallel tiles, then (sk_tiles > 0) its stream-K pieces.
+    const WorkSplit split{num_tiles, ncl, num_k_blocks, sk_tiles, sk_units};
+    const uint32_t n_items = items_of(split, cid);
+    const uint32_t total = iterations_of(split, cid);
 
     // ---- set-up: barriers, TMEM ----------------------------------------------------------
     if (threadIdx.x == 0) {
@@ -305,15 +315,15 @@ __global__ void __launch_bounds__(192, 1)
         // L2 priorities of A and B loads (bits 1:0 and 3:2 of l2_hints; 0 = normal).
         const uint64_t pol_a = make_l2_policy(l2_hints & 3u);
         const uint64_t pol_b = make_l2_policy((l2_hints >> 2) & 3u);
-        const uint32_t total = tiles_of(cid, ncl, num_tiles) * num_k_blocks;
         uint32_t it = 0;
         bool ok = true;
-        uint32_t t = cid;
-        uint32_t kb = 0;
+        uint32_t item = 0;
+        WorkItem wi = work_item(split, cid, 0);
+        uint32_t kb = wi.kb0;
         int32_t m0 = 0, n0 = 0;
         for (; it < total; ++it) {
-            if (kb == 0) {
-                const TileCoord tc = tile_coord(t, num_m_blocks, num_n_blocks, group_m);
+            if (kb == wi.kb0) {
+                const TileCoord tc = tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
                 m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
                 n0 = static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS);
             }
@@ -341,9 +351,9 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
             __syncwarp();
-            if (++kb == num_k_blocks) {
-                kb = 0;
-                t += ncl;
+            if (++kb == wi.kb1 && ++item < n_items) {
+                wi = work_item(split, cid, item);
+                kb = wi.kb0;
             }
         }
         // Every stage must be released by the MMAs before this CTA may exit: the last commits
@@ -377,14 +387,15 @@ __global__ void __launch_bounds__(192, 1)
         // (a commit tracks the MMAs its own thread issued, so it is always the same lane).
         if (rank == 0) {
             const bool leader = elect_one_sync();
-            const uint32_t total = tiles_of(cid, ncl, num_tiles) * num_k_blocks;
-            uint32_t kb = 0;
+            uint32_t item = 0;
+            WorkItem wi = work_item(split, cid, 0);
+            uint32_t kb = wi.kb0;
             uint32_t acc = 0;
             uint32_t d_tmem = tmem_base;
             bool ok = true;
             bool issued = false;
             for (uint32_t it = 0; it < total; ++it) {
-                if (kb == 0) {
+                if (kb == wi.kb0) {
                     // A new tile: wait until the epilogue has drained accumulator acc % 2.
                     const uint32_t b = acc & 1u;
                     const bool w = mbar_wait<kPair>(tempty_bar(b), ((acc >> 1) & 1u) ^ 1u,
@@ -412,21 +423,24 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                     for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
                         mma_f16<kCtaGroup>(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc,
-                                           (kb | k) != 0u);
+                                           ((kb - wi.kb0) | k) != 0u);
                     if constexpr (kPair) mma_commit_pair(empty_bar(p.stage), 0x3);
                     else mma_commit(empty_bar(p.stage));
                 }
                 __syncwarp();
                 issued = true;
-                if (++kb == num_k_blocks) {
-                    // Tile done: the accumulator is ready for the epilogue once these MMAs are.
+                if (++kb == wi.kb1) {
+                    // Item done: the accumulator is ready for the epilogue once these MMAs are.
                     if (leader) {
                         if constexpr (kPair) mma_commit_pair(tfull_bar(acc & 1u), 0x3);
                         else mma_commit(tfull_bar(acc & 1u));
                     }
                     __syncwarp();
-                    kb = 0;
                     ++acc;
+                    if (++item < n_items) {
+                        wi = work_item(split, cid, item);
+                        kb = wi.kb0;
+                    }
                 }
             }
             if (!ok && issued && leader) {
@@ -444,13 +458,63 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t row = quad * 32u + lane;      // row of this CTA's 128-row slab
         const uint32_t et = threadIdx.x - 64u;       // 0 .. 127
         const uint32_t lane_off = (quad * 32u) << 16;
-        uint32_t acc = 0;
+        volatile uint32_t* epi_word =
+            reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_EPI_WORD);
         uint32_t sbuf = 0;
+
+        // Store 64 columns (32 packed f16x2 words) of this thread's row at column col0.
+        const auto store_chunk = [&](const uint32_t (&p)[32], int32_t m0, int32_t col0) {
+            if constexpr (kTmaStore) {
+                // The store issued two sub-tiles ago read this buffer; wait until it has.
+                if (et == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                named_barrier_sync(1, C::EPI_THREADS);
+                const uint32_t dbuf = sD + sbuf * C::D_BYTES;
+#pragma unroll
+                for (uint32_t j = 0; j < 8; ++j)
+                    st_shared_v4(dbuf + sw128(row * 128u + j * 16u), p[4 * j], p[4 * j + 1],
+                                 p[4 * j + 2], p[4 * j + 3]);
+                fence_proxy_async_smem();
+                named_barrier_sync(1, C::EPI_THREADS);
+                if (et == 0) {
+                    tma_store_2d(&tmap_d, dbuf, col0, m0);
+                    bulk_commit_group();
+                }
+                __syncwarp();
+                sbuf ^= 1u;
+            } else {
+                // Each thread writes its own row: 64 fp16 as 8 16-byte vectors; the L2 merges
+                // the warp's 32 partial lines into full lines.
+                const int32_t grow = m0 + static_cast<int32_t>(row);
+                if (grow < static_cast<int32_t>(M)) {
+                    uint16_t* drow = Dptr + static_cast<uint64_t>(grow) * N;
+#pragma unroll
+                    for (uint32_t j = 0; j < 8; ++j) {
+                        const int32_t col = col0 + static_cast<int32_t>(8u * j);
+                        if (col < static_cast<int32_t>(N))  // N % 8 == 0
+                            st_global_v4(drow + col, p[4 * j], p[4 * j + 1], p[4 * j + 2],
+                                         p[4 * j + 3]);
+                    }
+                }
+            }
+        };
+
+        // Partial accumulators live in the workspace in a layout where a warp's 32 rows of one
+        // 16-byte column group are contiguous: float4 index ((chunk * 16 + j) * 128 + row).
+        const auto part_of = [&](uint32_t unit, uint32_t piece) {
+            return reinterpret_cast<float4*>(
+                ws_part + (static_cast<uint64_t>(unit * 2u + piece) * kCtaGroup + rank) *
+                              C::PART_FLOATS);
+        };
+
+        uint32_t acc = 0;
         bool ok = true;
-        for (uint32_t t = cid; t < num_tiles; t += ncl, ++acc) {
-            const TileCoord tc = tile_coord(t, num_m_blocks, num_n_blocks, group_m);
+        for (uint32_t item = 0; item < n_items; ++item, ++acc) {
+            const WorkItem wi = work_item(split, cid, item);
+            const TileCoord tc = tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
             const int32_t m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
             const int32_t n0 = static_cast<int32_t>(tc.n_blk * C::BN);
+            const bool rows_in = m0 < static_cast<int32_t>(M);
             const uint32_t b = acc & 1u;
             const uint32_t aph = (acc >> 1) & 1u;
             // One thread polls; the barrier-AND gives all 128 threads the same answer, so the
@@ -464,6 +528,7 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tcgen05_fence_after();
+            float4* my_part = wi.partial ? part_of(cid, wi.piece) : nullptr;
 #pragma unroll 1
             for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
                 uint32_t v0[32], v1[32];
@@ -481,49 +546,91 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     __syncwarp();
                 }
+                if (wi.partial) {
+                    // Stream-K piece: park the fp32 partial sums in the workspace.
+                    float4* dst = my_part + c * 16u * 128u + row;
+#pragma unroll
+                    for (uint32_t j = 0; j < 8; ++j)
+                        dst[j * 128u] = make_float4(
+                            __uint_as_float(v0[4 * j]), __uint_as_float(v0[4 * j + 1]),
+                            __uint_as_float(v0[4 * j + 2]), __uint_as_float(v0[4 * j + 3]));
+#pragma unroll
+                    for (uint32_t j = 0; j < 8; ++j)
+                        dst[(8 + j) * 128u] = make_float4(
+                            __uint_as_float(v1[4 * j]), __uint_as_float(v1[4 * j + 1]),
+                            __uint_as_float(v1[4 * j + 2]), __uint_as_float(v1[4 * j + 3]));
+                    continue;
+                }
                 const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
-                if (col0 < static_cast<int32_t>(N) && m0 < static_cast<int32_t>(M)) {
+                if (col0 < static_cast<int32_t>(N) && rows_in) {
                     uint32_t p[32];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) p[i] = pack_f16x2_rn(v0[2 * i], v0[2 * i + 1]);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         p[16 + i] = pack_f16x2_rn(v1[2 * i], v1[2 * i + 1]);
-                    if constexpr (kTmaStore) {
-                        // The store issued two sub-tiles ago read this buffer; wait until it has.
-                        if (et == 0) bulk_wait_group_read<1>();
-                        __syncwarp();
-                        named_barrier_sync(1, C::EPI_THREADS);
-                        const uint32_t dbuf = sD + sbuf * C::D_BYTES;
-#pragma unroll
-                        for (uint32_t j = 0; j < 8; ++j)
-                            st_shared_v4(dbuf + sw128(row * 128u + j * 16u), p[4 * j],
-                                         p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-                        fence_proxy_async_smem();
-                        named_barrier_sync(1, C::EPI_THREADS);
-                        if (et == 0) {
-                            tma_store_2d(&tmap_d, dbuf, col0, m0);
-                            bulk_commit_group();
-                        }
-                        __syncwarp();
-                        sbuf ^= 1u;
-                    } else {
-                        // Each thread writes its own row: 64 fp16 as 8 16-byte vectors; the
-                        // L2 merges the warp's 32 partial lines into full lines.
-                        const int32_t grow = m0 + static_cast<int32_t>(row);
-                        if (grow < static_cast<int32_t>(M)) {
-                            uint16_t* drow = Dptr + static_cast<uint64_t>(grow) * N;
-#pragma unroll
-                            for (uint32_t j = 0; j < 8; ++j) {
-                                const int32_t col = col0 + static_cast<int32_t>(8u * j);
-                                if (col < static_cast<int32_t>(N))  // N % 8 == 0
-                                    st_global_v4(drow + col, p[4 * j], p[4 * j + 1],
-                                                 p[4 * j + 2], p[4 * j + 3]);
-                            }
-                        }
-                    }
+                    store_chunk(p, m0, col0);
                 }
             }
+            if (!wi.partial) continue;
+
+            // Count this CTA's contribution to the tile; the contributor that arrives last sums
+            // every piece (in unit order, so the result does not depend on arrival order),
+            // stores the tile and resets the counter for the next launch.
+            const uint32_t r = wi.tile - (num_tiles - sk_tiles);
+            const uint32_t u0 = sk_unit_of(split, r * num_k_blocks);
+            const uint32_t u1 = sk_unit_of(split, r * num_k_blocks + num_k_blocks - 1u);
+            __threadfence();
+            named_barrier_sync(1, C::EPI_THREADS);
+            if (et == 0) {
+                __threadfence();
+                *epi_word = atomicAdd(&ws_count[r * kCtaGroup + rank], 1u);
+            }
+            named_barrier_sync(1, C::EPI_THREADS);
+            const uint32_t arrived = *epi_word;
+            if (arrived != u1 - u0) continue;
+            __threadfence();
+            // Up to kMaxContrib pieces per tile (the host bounds it); all their loads for a
+            // 32-column slice are issued before any is summed.
+            const float4* srcs[kMaxContrib];
+#pragma unroll
+            for (uint32_t q = 0; q < kMaxContrib; ++q) {
+                const uint32_t u = u0 + q <= u1 ? u0 + q : u1;
+                srcs[q] = part_of(u, r - sk_lo(split, u) / num_k_blocks) + row;
+            }
+            const uint32_t ncontrib = u1 - u0 + 1u;
+#pragma unroll 1
+            for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
+                uint32_t p[32];
+#pragma unroll
+                for (uint32_t h = 0; h < 2; ++h) {
+                    float4 x[kMaxContrib][8];
+#pragma unroll
+                    for (uint32_t q = 0; q < kMaxContrib; ++q)
+#pragma unroll
+                        for (uint32_t j = 0; j < 8; ++j)
+                            x[q][j] = q < ncontrib
+                                          ? __ldcg(srcs[q] + (c * 16u + h * 8u + j) * 128u)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (uint32_t j = 0; j < 8; ++j) {
+                        float4 t = x[0][j];
+#pragma unroll
+                        for (uint32_t q = 1; q < kMaxContrib; ++q) {
+                            t.x += x[q][j].x;
+                            t.y += x[q][j].y;
+                            t.z += x[q][j].z;
+                            t.w += x[q][j].w;
+                        }
+                        p[h * 16 + 2 * j] = pack_f16x2_rn(__float_as_uint(t.x), __float_as_uint(t.y));
+                        p[h * 16 + 2 * j + 1] =
+                            pack_f16x2_rn(__float_as_uint(t.z), __float_as_uint(t.w));
+                    }
+                }
+                const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
+                if (col0 < static_cast<int32_t>(N) && rows_in) store_chunk(p, m0, col0);
+            }
+            if (et == 0) ws_count[r * kCtaGroup + rank] = 0u;
         }
         (void)ok;
         if constexpr (kTmaStore) {

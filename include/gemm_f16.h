@@ -12,9 +12,10 @@
  * round-to-nearest-even (page "TIRx Compiler Foundation", section "Example: A GEMM Kernel":
  * the accumulator is converted to FP16 with cvt.rn before the store).
  *
- * Memory: the caller owns A, B and D, which must be device memory of the current CUDA device.
- * The library allocates no device memory, keeps no pointer beyond a call, and only caches
- * host-side objects (TMA descriptors, device properties).  D is overwritten, never read.
+ * Memory: the caller owns A, B and D (and the optional workspace of gemm_f16_nt_ws), which must
+ * be device memory of the current CUDA device.  The library allocates no device memory, keeps no
+ * pointer beyond a call, and only caches host-side objects (TMA descriptors, device
+ * properties).  D is overwritten, never read.
  *
  * Asynchrony: every compute entry point enqueues work on `stream` and returns; it does not
  * synchronise.  Errors that need the GPU to detect (a bounded wait that ran out) are reported
@@ -25,6 +26,7 @@
 #ifndef GEMM_F16_H
 #define GEMM_F16_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -74,6 +76,32 @@ int gemm_f16_nt(const void* A, const void* B, void* D, int64_t M, int64_t N, int
  * GEMM_F16_ERR_INVALID_ARG. */
 int gemm_f16_nt_variant(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                         cudaStream_t stream, int variant);
+
+/*
+ * D = A * B^T with a caller-provided workspace, which lets the persistent kernels run the tiles
+ * of the last, partial wave "stream-K": their k-blocks are split evenly over all CTAs, each CTA
+ * parks its fp32 partial sums in the workspace, and the last contributor to a tile adds the
+ * pieces and stores the tile.  This keeps every SM busy to the end of the launch.
+ *
+ * workspace:       device memory, 256-byte aligned, at least gemm_f16_workspace_bytes(...) bytes
+ *                  (or null / too small: the call runs without the stream-K tail).  The library
+ *                  clears the counters it uses with cudaMemsetAsync on `stream` before each launch
+ *                  and overwrites the rest; nothing needs initialising.  Launches that share a
+ *                  workspace must not overlap on the GPU (use one workspace per stream).
+ * Everything else is as gemm_f16_nt.  The result differs from gemm_f16_nt's only in the order of
+ * the fp32 additions of the tail tiles (both within the tolerance of an fp32 accumulation).
+ */
+int gemm_f16_nt_ws(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* gemm_f16_nt_ws with an explicit variant (GEMM_F16_VARIANT_*). */
+int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                   int variant, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes gemm_f16_nt_ws / gemm_f16_nt_ex need for this shape and variant on the current
+ * device (0: the shape gets no stream-K tail).  At most 4 KiB + 2 x units x 128 x 256 x 4 bytes
+ * (about 38 MiB on a 152-SM GPU).  Queries the device; launches nothing. */
+int gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, size_t* bytes);
 
 /* The variant GEMM_F16_VARIANT_AUTO picks for this shape on a device with `num_sms`
  * multiprocessors.  Host-only; needs no GPU. */
@@ -127,6 +155,20 @@ void gemm_f16_tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_t gr
 
 /* Pipeline iteration `it` -> ring stage and the parity of the "full" phase it waits for. */
 void gemm_f16_ring_pos(uint32_t it, uint32_t stages, uint32_t* stage, uint32_t* parity);
+
+/* The persistent kernels' work split (host copies of the device arithmetic).  `tiles` output
+ * tiles of `k_blocks` k-blocks each on `units` CTAs (or CTA pairs), of which the last `tail` run
+ * stream-K (0: none).  gemm_f16_sk_tail_tiles: the tail the library chooses.
+ * gemm_f16_sk_items: work items of one unit.  gemm_f16_sk_item: item `idx` of `unit` as
+ * {tile, first k-block, end k-block, piece 0/1, partial 0/1}.  gemm_f16_sk_unit_of: the unit
+ * whose stream-K range holds tail k-block x (x counts k-blocks over the tail tiles). */
+int64_t gemm_f16_sk_tail_tiles(int64_t tiles, int64_t units, int64_t k_blocks);
+uint32_t gemm_f16_sk_items(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t tail,
+                           uint32_t unit);
+void gemm_f16_sk_item(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t tail,
+                      uint32_t unit, uint32_t idx, uint32_t out[5]);
+uint32_t gemm_f16_sk_unit_of(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t tail,
+                             uint32_t x);
 
 #ifdef __cplusplus
 }

@@ -280,3 +280,64 @@ def test_product_package_does_not_reference_the_oracle():
                 text = open(os.path.join(root, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "gemm_ref" not in text, f
+
+
+# ---- stream-K tail: the work split covers every k-block of every tile exactly once ----------
+
+SPLITS = [  # (tiles, units, k_blocks): 8192^3 pairs, MLP pairs, 2048^3 pairs, odd cases
+    (1024, 76, 128), (3584, 76, 64), (64, 76, 32), (20, 76, 24), (24, 76, 63), (480, 152, 16),
+    (7, 5, 9), (13, 4, 40), (100, 7, 3),
+]
+
+
+@pytest.mark.parametrize("T,U,KB", SPLITS)
+def test_stream_k_split_covers_each_k_block_once(T, U, KB):
+    R = g.gemm_f16_sk_tail_tiles(T, U, KB)
+    for tail in sorted({R, 0}):
+        S = min(3 * tail, U)  # units sharing the tail: at most 3 per tail tile
+        if tail:
+            assert 0 < tail <= U and tail <= T and (T - tail) % U == 0 and tail * KB >= 4 * S
+        cover = {}
+        per_unit = []
+        for c in range(U):
+            n = g.gemm_f16_sk_items(T, U, KB, tail, c)
+            assert n <= (T - tail) // U + (T - tail) % U + 2 if tail else True
+            work = 0
+            pieces = 0
+            for i in range(n):
+                tile, kb0, kb1, piece, partial = g.gemm_f16_sk_item(T, U, KB, tail, c, i)
+                assert 0 <= tile < T and 0 <= kb0 < kb1 <= KB
+                if tile < T - tail:
+                    assert (kb0, kb1, partial) == (0, KB, 0)
+                else:
+                    assert piece == pieces and piece <= 1
+                    pieces += 1
+                    assert partial == int(not (kb0 == 0 and kb1 == KB))
+                    r = tile - (T - tail)
+                    # every k-block of this piece is in unit c's range
+                    for kb in (kb0, kb1 - 1):
+                        assert g.gemm_f16_sk_unit_of(T, U, KB, tail, r * KB + kb) == c
+                for kb in range(kb0, kb1):
+                    cover[(tile, kb)] = cover.get((tile, kb), 0) + 1
+                work += kb1 - kb0
+            per_unit.append(work)
+        assert len(cover) == T * KB and set(cover.values()) == {1}
+        if tail:
+            assert max(per_unit[:S]) - min(per_unit[:S]) <= 1   # balanced to one k-block
+            assert max(per_unit[S:], default=0) <= min(per_unit[:S])
+            for r in range(tail):  # at most 4 contributors per tail tile
+                u0 = g.gemm_f16_sk_unit_of(T, U, KB, tail, r * KB)
+                u1 = g.gemm_f16_sk_unit_of(T, U, KB, tail, r * KB + KB - 1)
+                assert 0 <= u0 <= u1 < S and u1 - u0 + 1 <= 4
+        else:
+            assert max(per_unit) - min(per_unit) <= KB  # at most one tile apart
+
+
+def test_stream_k_tail_choice():
+    assert g.gemm_f16_sk_tail_tiles(1024, 76, 128) == 36      # 8192^3: 13.47 waves of pairs
+    assert g.gemm_f16_sk_tail_tiles(3584, 76, 64) == 12       # MLP: 47.16 waves
+    assert g.gemm_f16_sk_tail_tiles(64, 76, 32) == 64         # 2048^3: under one wave
+    assert g.gemm_f16_sk_tail_tiles(76 * 5, 76, 64) == 0      # whole waves
+    assert g.gemm_f16_sk_tail_tiles(76 * 5 + 75, 76, 64) == 0  # last wave 99% full
+    assert g.gemm_f16_sk_tail_tiles(240, 76, 16) == 12        # 12 tiles over 36 units
+    assert g.gemm_f16_sk_tail_tiles(240, 76, 3) == 0          # pieces under 4 k-blocks
