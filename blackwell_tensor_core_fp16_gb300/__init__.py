@@ -20,7 +20,8 @@ __all__ = [
     "gemm_f16_nt", "gemm_f16_nt_variant", "gemm_f16_choose_variant", "gemm_f16_check_status",
     "gemm_f16_last_error", "gemm_f16_version", "gemm_f16_get_variant_info", "gemm_f16_idesc",
     "gemm_f16_smem_desc_sw128", "gemm_f16_sw128", "gemm_f16_tile_coord", "gemm_f16_ring_pos",
-    "gemm_f16_nt_ws", "gemm_f16_nt_ex", "gemm_f16_workspace_bytes", "gemm_f16_sk_tail_tiles",
+    "gemm_f16_nt_ws", "gemm_f16_nt_ex", "gemm_f16_nt_noalloc", "gemm_f16_workspace_bytes",
+    "gemm_f16_sk_tail_tiles",
     "gemm_f16_sk_items", "gemm_f16_sk_item", "gemm_f16_sk_unit_of",
     "exported_symbols", "VARIANTS", "STATUS",
 ]
@@ -96,6 +97,8 @@ def load():
         lib.gemm_f16_nt_ws.restype = i32
         lib.gemm_f16_nt_ex.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, sz, vp]
         lib.gemm_f16_nt_ex.restype = i32
+        lib.gemm_f16_nt_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        lib.gemm_f16_nt_noalloc.restype = i32
         lib.gemm_f16_workspace_bytes.argtypes = [i64, i64, i64, i32, ctypes.POINTER(sz)]
         lib.gemm_f16_workspace_bytes.restype = i32
         lib.gemm_f16_sk_tail_tiles.argtypes = [i64, i64, i64]
@@ -129,6 +132,12 @@ def gemm_f16_nt_ws(A: int, B: int, D: int, M: int, N: int, K: int, workspace: in
 def gemm_f16_nt_ex(A: int, B: int, D: int, M: int, N: int, K: int, variant: int,
                    workspace: int, workspace_bytes: int, stream: int = 0) -> int:
     return load().gemm_f16_nt_ex(A, B, D, M, N, K, variant, workspace, workspace_bytes, stream)
+
+
+def gemm_f16_nt_noalloc(A: int, B: int, D: int, M: int, N: int, K: int, stream: int = 0) -> int:
+    """D = A * B^T using the library's fixed device scratch instead of any allocation (for
+    callers that cannot allocate, e.g. while recording a CUDA graph); see include/gemm_f16.h."""
+    return load().gemm_f16_nt_noalloc(A, B, D, M, N, K, stream)
 
 
 def gemm_f16_workspace_bytes(M: int, N: int, K: int, variant: int = 0) -> int:

@@ -464,6 +464,36 @@ int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
     }
 }
 
+// ---- scratch for callers that cannot allocate -------------------------------------------------
+// gemm_f16_nt_noalloc runs the stream-K schedule with its workspace in this fixed array instead
+// of caller memory.  The array exists on every device that loads the library, for the life of
+// the process.  Host code must not use its name as a device address (on the host it is only a
+// stand-in); the device address is looked up once per device with cudaGetSymbolAddress.
+constexpr size_t kNoAllocScratchBytes = size_t(40) << 20;   // 40 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on first use).
+int noalloc_scratch(void** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(GEMM_F16_ERR_CUDA, "device %d out of range", dev);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+        if (p == nullptr) return fail(GEMM_F16_ERR_CUDA, "no device address for the scratch array");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return GEMM_F16_OK;
+}
+
 }  // namespace
 
 // ================================ C ABI ======================================================
@@ -491,6 +521,29 @@ int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, 
                    int variant, void* workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     return run(A, B, D, M, N, K, stream, variant, workspace, workspace_bytes);
+}
+
+int gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream)
+{
+    t_last_error.clear();
+    int rc = check_args(A, B, D, M, N, K);
+    if (rc != GEMM_F16_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_F16_OK;
+    size_t need = 0;
+    if (K > 0) {
+        rc = run(nullptr, nullptr, nullptr, M, N, K, nullptr, GEMM_F16_VARIANT_AUTO, nullptr, 0,
+                 &need);
+        if (rc != GEMM_F16_OK) return rc;
+    }
+    if (need > kNoAllocScratchBytes)
+        return fail(GEMM_F16_ERR_UNSUPPORTED,
+                    "this shape needs %zu bytes of scratch; the fixed scratch holds %zu", need,
+                    kNoAllocScratchBytes);
+    void* scratch = nullptr;
+    if (need > 0 && (rc = noalloc_scratch(&scratch)) != GEMM_F16_OK) return rc;
+    return run(A, B, D, M, N, K, stream, GEMM_F16_VARIANT_AUTO, scratch,
+               need > 0 ? kNoAllocScratchBytes : 0);
 }
 
 int gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, size_t* bytes)

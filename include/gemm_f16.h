@@ -98,6 +98,29 @@ int gemm_f16_nt_ws(const void* A, const void* B, void* D, int64_t M, int64_t N, 
 int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                    int variant, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * D = A * B^T without allocating anything, for callers that cannot allocate device memory: code
+ * recording a CUDA graph (cudaMalloc cannot be captured and would end the capture), servers that
+ * hand all device memory to their own pool at start-up and forbid other allocations, and
+ * latency-bound loops that cannot afford cudaMalloc's implicit synchronisation.  The GEMM pages
+ * have no counterpart to this entry point; it is a deployment convenience.
+ *
+ * It computes what gemm_f16_nt_ws computes, with the stream-K workspace taken from a fixed 40 MiB
+ * array of device memory that the library reserves on every device that loads it, for the life
+ * of the process.  The caller passes A, B and D as for gemm_f16_nt.  Nothing else is allocated:
+ * no cudaMalloc, cudaFree or allocating library routine is called.
+ *
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture that uses this entry
+ * point.  Every call shares the one array and finds the previous call's contents in it; the
+ * counters that must start at zero are cleared on `stream` before each launch.  Calls that
+ * overlap on the GPU (on different streams) race on the array and give wrong results: serialise
+ * them.  A shape whose stream-K workspace would exceed 40 MiB (not possible on a 152-SM GB300,
+ * whose largest request is about 38 MiB) returns GEMM_F16_ERR_UNSUPPORTED and does nothing.
+ */
+int gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                        cudaStream_t stream);
+
 /* Workspace bytes gemm_f16_nt_ws / gemm_f16_nt_ex need for this shape and variant on the current
  * device (0: the shape gets no stream-K tail).  At most 4 KiB + 2 x units x 128 x 256 x 4 bytes
  * (about 38 MiB on a 152-SM GPU).  Queries the device; launches nothing. */
