@@ -62,14 +62,34 @@ def _load():
             lib.oracle_gemm_f64_sampled.argtypes = [u16p, u16p, i64, i64, i64, i64p, i64p,
                                                     i64, f64p]
             lib.oracle_gemm_f64_sampled.restype = None
+            lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_f64.restype = ctypes.c_double
+            lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_decode_bf16.argtypes = [u16p, f64p, i64]
+            lib.oracle_decode_bf16.restype = None
+            lib.oracle_round_bf16.argtypes = [f64p, u16p, i64]
+            lib.oracle_round_bf16.restype = None
+            lib.oracle_gemm_f64_dt.argtypes = [u16p, u16p, f64p, i64, i64, i64, ctypes.c_int]
+            lib.oracle_gemm_f64_dt.restype = ctypes.c_int
+            lib.oracle_gemm_f64_sampled_dt.argtypes = [u16p, u16p, i64, i64, i64, i64p, i64p,
+                                                       i64, f64p, ctypes.c_int]
+            lib.oracle_gemm_f64_sampled_dt.restype = None
+            lib.oracle_epilogue_f64.argtypes = [f64p, i64, i64, u16p, ctypes.c_int, ctypes.c_int]
+            lib.oracle_epilogue_f64.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
 
 
+DTYPES = {"f16": 0, "bf16": 1}
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
+
+
 def _as_u16(x) -> np.ndarray:
-    """fp16 array (numpy float16/uint16 or a CPU torch tensor) -> contiguous uint16 view."""
+    """16-bit array (numpy float16/uint16, or a CPU torch fp16/bf16 tensor) -> contiguous uint16
+    view of its bits."""
     if hasattr(x, "detach"):  # a torch tensor: reinterpret its bits without arithmetic
         x = x.detach().cpu().contiguous().view(dtype=__import__("torch").int16).numpy()
     x = np.ascontiguousarray(x)
@@ -131,6 +151,80 @@ def gemm_f64_sampled(A, B, rows, cols) -> np.ndarray:
     _load().oracle_gemm_f64_sampled(a.ctypes.data, b.ctypes.data, M, N, K, r.ctypes.data,
                                     c.ctypes.data, r.size, out.ctypes.data)
     return out
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """bfloat16 bit patterns -> binary64 values (exact widening)."""
+    b = _as_u16(bits)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().oracle_decode_bf16(b.ctypes.data, out.ctypes.data, b.size)
+    return out
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """binary64 values -> bfloat16 bit patterns, round to nearest, ties to even."""
+    v = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_round_bf16(v.ctypes.data, out.ctypes.data, v.size)
+    return out
+
+
+def gemm_f64_dt(A, B, dtype: str = "f16") -> np.ndarray:
+    """D64 = A * B^T in binary64 for fp16 ("f16") or bfloat16 ("bf16") inputs."""
+    a, b = _as_u16(A), _as_u16(B)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError(f"shapes {a.shape} and {b.shape} do not contract")
+    M, K = a.shape
+    N = b.shape[0]
+    out = np.empty((M, N), dtype=np.float64)
+    if _load().oracle_gemm_f64_dt(a.ctypes.data, b.ctypes.data, out.ctypes.data, M, N, K,
+                                  DTYPES[dtype]) != 0:
+        raise MemoryError("oracle could not allocate its binary64 copies")
+    return out
+
+
+def gemm_f64_sampled_dt(A, B, rows, cols, dtype: str = "f16") -> np.ndarray:
+    a, b = _as_u16(A), _as_u16(B)
+    M, K = a.shape
+    N = b.shape[0]
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.size and (r.min() < 0 or r.max() >= M or c.min() < 0 or c.max() >= N):
+        raise IndexError("sample index out of range")
+    out = np.empty(r.shape, dtype=np.float64)
+    _load().oracle_gemm_f64_sampled_dt(a.ctypes.data, b.ctypes.data, M, N, K, r.ctypes.data,
+                                       c.ctypes.data, r.size, out.ctypes.data, DTYPES[dtype])
+    return out
+
+
+def epilogue(X, bias=None, activation: str = "none", dtype: str = "f16", cols=None) -> np.ndarray:
+    """act(X + bias[j]) in binary64 (a new array).  X: (M, N) binary64 sums, or a 1-D array of
+    sampled elements whose column indices are `cols`.  bias: N elements of the given 16-bit type
+    (bits or a torch tensor) or None."""
+    x = np.array(X, dtype=np.float64, copy=True)
+    b = None if bias is None else _as_u16(bias)
+    if x.ndim == 1:  # sampled elements: gather the bias columns into a 1 x count problem
+        bb = None if b is None else np.ascontiguousarray(b[np.asarray(cols)])
+        x2 = np.ascontiguousarray(x.reshape(1, -1))
+        _load().oracle_epilogue_f64(x2.ctypes.data, 1, x2.shape[1],
+                                    None if bb is None else bb.ctypes.data, DTYPES[dtype],
+                                    ACTIVATIONS[activation])
+        return x2.reshape(-1)
+    x = np.ascontiguousarray(x)
+    M, N = x.shape
+    if b is not None and b.size != N:
+        raise ValueError("bias must have N elements")
+    _load().oracle_epilogue_f64(x.ctypes.data, M, N, None if b is None else b.ctypes.data,
+                                DTYPES[dtype], ACTIVATIONS[activation])
+    return x
+
+
+def tolerance_dt(d_ref: np.ndarray, K: int, dtype: str = "f16") -> np.ndarray:
+    """The parity bound for an output of the given type: 1e-3 * sqrt(K) + rel * |D_ref| with
+    rel = 2^-10 for fp16 (the stated bound: twice fp16's half-ulp 2^-11) and 2^-7 for bfloat16
+    (twice bfloat16's half-ulp 2^-8, by the same derivation)."""
+    rel = 2.0 ** -10 if dtype == "f16" else 2.0 ** -7
+    return 1e-3 * np.sqrt(float(K)) + np.abs(d_ref) * rel
 
 
 def num_threads() -> int:

@@ -386,3 +386,205 @@ def test_unmutated_reference_copy_passes_pins():
     pin_permutation(gemm)
     pin_rank_one(gemm)
     pin_bruteforce(gemm, oracle.f64_to_f16_bits)
+
+
+# ---------------------------------------------------------------------------
+# bfloat16 conversions and the bfloat16 GEMM.
+# ---------------------------------------------------------------------------
+
+def _torch_bf16_bits_to_f64(bits):
+    import torch
+    t = torch.from_numpy(np.asarray(bits, dtype=np.uint16).view(np.int16).copy())
+    return t.view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def test_bf16_decode_exhaustive_vs_torch():
+    got = oracle.bf16_bits_to_f64(ALL16)
+    want = _torch_bf16_bits_to_f64(ALL16)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_bf16_encode_round_trip_exhaustive():
+    vals = oracle.bf16_bits_to_f64(ALL16)
+    got = oracle.f64_to_bf16_bits(vals)
+    ok = ~np.isnan(vals)
+    assert np.array_equal(got[ok], ALL16[ok])
+
+
+def test_bf16_encode_midpoints_ties_to_even():
+    lo = np.arange(0, 0x7F7F, dtype=np.uint16)  # positive finite, up to the second-largest
+    a = oracle.bf16_bits_to_f64(lo)
+    b = oracle.bf16_bits_to_f64(lo + 1)
+    mid = (a + b) / 2  # exact in binary64
+    got = oracle.f64_to_bf16_bits(mid)
+    even = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint16)
+    assert np.array_equal(got, even)
+    assert np.array_equal(oracle.f64_to_bf16_bits(np.nextafter(mid, np.inf)), lo + 1)
+    assert np.array_equal(oracle.f64_to_bf16_bits(np.nextafter(mid, -np.inf)), lo)
+
+
+def test_bf16_encode_vs_torch_on_binary32_values():
+    """For values that are exactly binary32, torch's float32 -> bfloat16 conversion (round to
+    nearest even) is a reference with no double rounding."""
+    import torch
+    rng = np.random.default_rng(21)
+    x32 = np.concatenate([
+        (rng.standard_normal(200000) * 10.0 ** rng.uniform(-30, 30, 200000)).astype(np.float32),
+        rng.integers(0, 2 ** 32, 50000, dtype=np.uint64).astype(np.uint32).view(np.float32),
+    ])
+    x32 = x32[np.isfinite(x32)]
+    want = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.f64_to_bf16_bits(x32.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_bf16_encode_special_values():
+    e = oracle.f64_to_bf16_bits
+    top = float(oracle.bf16_bits_to_f64(np.array([0x7F7F], np.uint16))[0])  # largest finite
+    assert e([top])[0] == 0x7F7F
+    assert e([top * (1 + 2.0 ** -9)])[0] == 0x7F7F           # below the halfway point
+    assert e([2.0 ** 128 * (1 - 2.0 ** -9)])[0] == 0x7F80     # the tie above the top: to even (inf)
+    assert e([2.0 ** -133])[0] == 0x0001 and e([2.0 ** -134])[0] == 0x0000
+    assert e([-0.0])[0] == 0x8000 and e([1.0])[0] == 0x3F80
+    assert e([np.inf])[0] == 0x7F80 and e([-np.inf])[0] == 0xFF80
+
+
+def _bf16_bits(x):
+    import torch
+    t = torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_gemm_pins():
+    # all ones
+    for (M, N, K) in [(3, 5, 7), (17, 9, 1000)]:
+        A = np.full((M, K), 0x3F80, np.uint16)
+        B = np.full((N, K), 0x3F80, np.uint16)
+        assert np.all(oracle.gemm_f64_dt(A, B, "bf16") == float(K))
+    # permutation probe
+    rng = np.random.default_rng(22)
+    K = 16
+    pi = rng.permutation(K)
+    P = np.zeros((K, K), np.float32)
+    P[np.arange(K), pi] = 1.0
+    A = _bf16_bits(rng.uniform(-1, 1, (5, K)))
+    D = oracle.gemm_f64_dt(A, _bf16_bits(P), "bf16")
+    assert np.array_equal(D, oracle.bf16_bits_to_f64(A)[:, pi])
+    # exact rational brute force, bfloat16 inputs
+    for (M, N, K) in [(2, 3, 5), (4, 4, 16)]:
+        A = _bf16_bits(rng.uniform(-2, 2, (M, K)))
+        B = _bf16_bits(rng.uniform(-2, 2, (N, K)))
+        D = oracle.gemm_f64_dt(A, B, "bf16")
+        a, b = oracle.bf16_bits_to_f64(A), oracle.bf16_bits_to_f64(B)
+        for i in range(M):
+            for j in range(N):
+                ex = sum(Fraction(a[i, k]) * Fraction(b[j, k]) for k in range(K))
+                assert abs(Fraction(float(D[i, j])) - ex) <= Fraction(1, 2 ** 45)
+    # the dtype-generic entry agrees with the binary16 one on binary16 data
+    A = rand_f16(rng, (9, 33))
+    B = rand_f16(rng, (7, 33))
+    assert np.array_equal(oracle.gemm_f64_dt(A, B, "f16"), oracle.gemm_f64(A, B))
+
+
+# ---------------------------------------------------------------------------
+# The fused epilogue act(x + bias[j]).
+# ---------------------------------------------------------------------------
+
+def test_epilogue_bias_lands_on_columns():
+    """A = 0 gives D = bias[j] in every row: pins that bias is indexed by output column."""
+    M = N = 6
+    bias = bits(np.arange(N, dtype=np.float64) * 0.5 - 1.0)
+    X = np.zeros((M, N))
+    Y = oracle.epilogue(X, bias, "none")
+    assert np.array_equal(Y, np.tile(oracle.f16_bits_to_f64(bias), (M, 1)))
+    assert np.array_equal(oracle.epilogue(X, None, "none"), X)
+
+
+def test_epilogue_relu_closed_form():
+    x = np.array([[-3.0, -0.0, 0.0, 2.5, 1e-30, -1e-30]])
+    y = oracle.epilogue(x, None, "relu")
+    assert np.array_equal(y, np.array([[0.0, 0.0, 0.0, 2.5, 1e-30, 0.0]]))
+    bias = bits([1.0, -1.0, 0.5, -4.0, 0.0, 0.0])
+    y = oracle.epilogue(np.array([[-0.5, 0.5, 0.25, 3.0, 0.0, -1.0]]), bias, "relu")
+    assert np.array_equal(y, np.array([[0.5, 0.0, 0.75, 0.0, 0.0, 0.0]]))
+
+
+def test_epilogue_gelu_pins():
+    """GELU(x) = x * Phi(x): against scipy's normal CDF (a library routine), the odd-part
+    identity GELU(x) - GELU(-x) = x, and the limits."""
+    scipy_special = pytest.importorskip("scipy.special")
+    x = np.linspace(-8, 8, 4001).reshape(1, -1)
+    y = oracle.epilogue(x, None, "gelu")
+    want = x * scipy_special.ndtr(x)
+    assert np.allclose(y, want, rtol=1e-13, atol=1e-15)
+    ym = oracle.epilogue(-x, None, "gelu")
+    assert np.allclose(y - ym, x, rtol=0, atol=1e-14)
+    assert oracle.epilogue(np.array([[0.0]]), None, "gelu")[0, 0] == 0.0
+    assert abs(oracle.epilogue(np.array([[1.0]]), None, "gelu")[0, 0] - 0.8413447460685429) < 1e-15
+    big = oracle.epilogue(np.array([[40.0, -40.0]]), None, "gelu")
+    assert big[0, 0] == 40.0 and big[0, 1] == 0.0
+
+
+def test_epilogue_sampled_matches_full():
+    rng = np.random.default_rng(23)
+    X = rng.standard_normal((7, 11))
+    bias = bits(rng.uniform(-1, 1, 11))
+    full = oracle.epilogue(X, bias, "gelu")
+    rows = rng.integers(0, 7, 50)
+    cols = rng.integers(0, 11, 50)
+    samp = oracle.epilogue(X[rows, cols], bias, "gelu", cols=cols)
+    assert np.array_equal(samp, full[rows, cols])
+
+
+@pytest.mark.parametrize("mutant", ["bias_by_row", "bias_after_act", "gelu_sign"])
+def test_epilogue_pins_catch_planted_mistakes(mutant):
+    """Broken copies of the epilogue (planted here, on the CPU) fail the pins above."""
+    scipy_special = pytest.importorskip("scipy.special")
+
+    def broken(X, bias, act):
+        X = np.array(X, dtype=np.float64)
+        b = None if bias is None else oracle.f16_bits_to_f64(bias)
+        if mutant == "bias_by_row" and b is not None:
+            X = X + b[: X.shape[0], None]
+        elif mutant != "bias_after_act" and b is not None:
+            X = X + b[None, :]
+        if act == "relu":
+            X = np.maximum(X, 0)
+        elif act == "gelu":
+            s = -1.0 if mutant == "gelu_sign" else 1.0
+            X = X * scipy_special.ndtr(s * X)
+        if mutant == "bias_after_act" and b is not None:
+            X = X + b[None, :]
+        return X
+
+    failures = 0
+    M = N = 6
+    bias = bits(np.arange(N, dtype=np.float64) * 0.5 - 1.0)
+    try:  # bias on columns
+        assert np.array_equal(broken(np.zeros((M, N)), bias, "none"),
+                              np.tile(oracle.f16_bits_to_f64(bias), (M, 1)))
+    except AssertionError:
+        failures += 1
+    try:  # relu with bias, closed form
+        b2 = bits([1.0, -1.0, 0.5, -4.0, 0.0, 0.0])
+        assert np.array_equal(broken(np.array([[-0.5, 0.5, 0.25, 3.0, 0.0, -1.0]]), b2, "relu"),
+                              np.array([[0.5, 0.0, 0.75, 0.0, 0.0, 0.0]]))
+    except AssertionError:
+        failures += 1
+    try:  # gelu odd-part identity, value at 1 and the large-x limit
+        x = np.linspace(-4, 4, 81).reshape(1, -1)
+        assert np.allclose(broken(x, None, "gelu") - broken(-x, None, "gelu"), x, atol=1e-12)
+        assert abs(broken(np.array([[1.0]]), None, "gelu")[0, 0] - 0.8413447460685429) < 1e-15
+        assert broken(np.array([[40.0]]), None, "gelu")[0, 0] == 40.0
+    except AssertionError:
+        failures += 1
+    assert failures >= 1, mutant
+
+
+def test_tolerance_by_dtype():
+    d = np.array([0.0, 1.0, -1024.0])
+    assert np.allclose(oracle.tolerance_dt(d, 4096, "f16"), oracle.tolerance(d, 4096))
+    assert np.allclose(oracle.tolerance_dt(d, 4096, "bf16"), [0.064, 0.064 + 2.0 ** -7,
+                                                              0.064 + 8.0])
