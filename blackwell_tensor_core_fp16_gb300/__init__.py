@@ -21,6 +21,7 @@ __all__ = [
     "gemm_f16_last_error", "gemm_f16_version", "gemm_f16_get_variant_info", "gemm_f16_idesc",
     "gemm_f16_smem_desc_sw128", "gemm_f16_sw128", "gemm_f16_tile_coord", "gemm_f16_ring_pos",
     "gemm_f16_nt_ws", "gemm_f16_nt_ex", "gemm_f16_nt_noalloc", "gemm_f16_workspace_bytes",
+    "gemm_f16_nt_fused", "linear", "DTYPES", "ACTIVATIONS",
     "gemm_f16_sk_tail_tiles",
     "gemm_f16_sk_items", "gemm_f16_sk_item", "gemm_f16_sk_unit_of",
     "exported_symbols", "VARIANTS", "STATUS",
@@ -99,6 +100,9 @@ def load():
         lib.gemm_f16_nt_ex.restype = i32
         lib.gemm_f16_nt_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         lib.gemm_f16_nt_noalloc.restype = i32
+        lib.gemm_f16_nt_fused.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, i32, vp, sz,
+                                          vp]
+        lib.gemm_f16_nt_fused.restype = i32
         lib.gemm_f16_workspace_bytes.argtypes = [i64, i64, i64, i32, ctypes.POINTER(sz)]
         lib.gemm_f16_workspace_bytes.restype = i32
         lib.gemm_f16_sk_tail_tiles.argtypes = [i64, i64, i64]
@@ -132,6 +136,44 @@ def gemm_f16_nt_ws(A: int, B: int, D: int, M: int, N: int, K: int, workspace: in
 def gemm_f16_nt_ex(A: int, B: int, D: int, M: int, N: int, K: int, variant: int,
                    workspace: int, workspace_bytes: int, stream: int = 0) -> int:
     return load().gemm_f16_nt_ex(A, B, D, M, N, K, variant, workspace, workspace_bytes, stream)
+
+
+DTYPES = {"f16": 0, "bf16": 1}
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2}
+
+
+def gemm_f16_nt_fused(A: int, B: int, D: int, M: int, N: int, K: int, dtype: int, bias: int,
+                      activation: int, variant: int, workspace: int, workspace_bytes: int,
+                      stream: int = 0) -> int:
+    return load().gemm_f16_nt_fused(A, B, D, M, N, K, dtype, bias, activation, variant,
+                                    workspace, workspace_bytes, stream)
+
+
+def linear(A, W, bias=None, activation: str = "none", out=None, variant: int = 0, stream=None):
+    """act(A @ W.T + bias) for CUDA fp16 or bfloat16 tensors A (M, K), W (N, K), bias (N,);
+    returns (M, N) in the same type.  The bias add and the activation run in the GEMM's epilogue
+    on the fp32 sums.  Asynchronous on ``stream``; raises GemmError on a non-zero status."""
+    import torch
+    dt = {torch.float16: "f16", torch.bfloat16: "bf16"}.get(A.dtype)
+    if dt is None or W.dtype != A.dtype or (bias is not None and bias.dtype != A.dtype):
+        raise ValueError("A, W and bias must all be float16 or all bfloat16")
+    for name, t in (("A", A), ("W", W)):
+        if not t.is_cuda or t.dim() != 2 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 2-D CUDA tensor")
+    M, K = A.shape
+    N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("K differs")
+    if bias is not None and (bias.numel() != N or not bias.is_cuda or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous CUDA vector of N elements")
+    if out is None:
+        out = torch.empty((M, N), dtype=A.dtype, device=A.device)
+    rc = gemm_f16_nt_fused(A.data_ptr(), W.data_ptr(), out.data_ptr(), M, N, K, DTYPES[dt],
+                           0 if bias is None else bias.data_ptr(), ACTIVATIONS[activation],
+                           int(variant), 0, 0, _stream_handle(stream))
+    if rc != OK:
+        raise GemmError(rc, gemm_f16_last_error())
+    return out
 
 
 def gemm_f16_nt_noalloc(A: int, B: int, D: int, M: int, N: int, K: int, stream: int = 0) -> int:

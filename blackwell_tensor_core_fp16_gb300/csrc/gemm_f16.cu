@@ -132,7 +132,7 @@ int choose_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
 struct DeviceState {
     bool ready = false;
     int sms = 0;
-    bool smem_set[GEMM_F16_NUM_VARIANTS] = {};
+    bool smem_set[2 * GEMM_F16_NUM_VARIANTS] = {};  // per variant, fp16 then bf16
     int pair_clusters[GEMM_F16_NUM_VARIANTS] = {};  // co-resident CTA pairs per variant
 };
 
@@ -193,7 +193,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 // A row-major fp16 matrix of `rows` x `cols` (cols contiguous) read or written in boxes of
 // box_rows x box_cols elements with the 128-byte swizzle (box_cols * 2 == 128 bytes).
 int make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
-             uint32_t box_cols)
+             uint32_t box_cols, bool bf16 = false)
 {
     auto fn = encode_fn();
     if (!fn) return fail(GEMM_F16_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
@@ -201,7 +201,8 @@ int make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, ui
     const cuuint64_t strides[1] = {cols * 2};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    2, const_cast<void*>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
@@ -218,10 +219,11 @@ struct MapKey {
     int64_t M, N, K;
     int variant;
     int device;
+    int dtype = 0;
     bool operator==(const MapKey& o) const
     {
         return a == o.a && b == o.b && d == o.d && M == o.M && N == o.N && K == o.K &&
-               variant == o.variant && device == o.device;
+               variant == o.variant && device == o.device && dtype == o.dtype;
     }
 };
 
@@ -250,10 +252,11 @@ int get_maps(const MapKey& k, uint32_t a_box_rows, uint32_t b_box_rows, bool nee
     t_cache_next = (t_cache_next + 1) % kCacheSize;
     e.valid = false;
     int rc;
-    if ((rc = make_map(&e.ma, k.a, k.M, k.K, a_box_rows, 64)) != GEMM_F16_OK) return rc;
-    if ((rc = make_map(&e.mb, k.b, k.N, k.K, b_box_rows, 64)) != GEMM_F16_OK) return rc;
+    const bool bf = k.dtype == GEMM_F16_DTYPE_BF16;
+    if ((rc = make_map(&e.ma, k.a, k.M, k.K, a_box_rows, 64, bf)) != GEMM_F16_OK) return rc;
+    if ((rc = make_map(&e.mb, k.b, k.N, k.K, b_box_rows, 64, bf)) != GEMM_F16_OK) return rc;
     if (need_d) {
-        if ((rc = make_map(&e.md, k.d, k.M, k.N, 128, 64)) != GEMM_F16_OK) return rc;
+        if ((rc = make_map(&e.md, k.d, k.M, k.N, 128, 64, bf)) != GEMM_F16_OK) return rc;
     } else {
         std::memset(&e.md, 0, sizeof(e.md));
     }
@@ -315,14 +318,23 @@ size_t ws_bytes_for(int64_t units, int cta_group, int block_n)
     return kWsCountBytes + static_cast<size_t>(units) * 2u * cta_group * 128u * block_n * 4u;
 }
 
-template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore>
+// Epilogue options of a launch: element type, bias (N elements of that type, or null) and
+// activation.
+struct EpiOpts {
+    int dtype = GEMM_F16_DTYPE_F16;
+    const void* bias = nullptr;
+    int act = GEMM_F16_ACT_NONE;
+};
+
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore, bool kBf16 = false>
 int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
               cudaStream_t stream, DeviceState& d, int dev, void* workspace = nullptr,
-              size_t workspace_bytes = 0, size_t* bytes_needed = nullptr)
+              size_t workspace_bytes = 0, size_t* bytes_needed = nullptr,
+              const EpiOpts& epi = EpiOpts{})
 {
     using C = gf16::WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
-    auto kernel = gf16::gemm_ws_kernel<kCtaGroup, kBlockN, kStages, kTmaStore>;
-    int rc = ensure_smem(d, variant, kernel, C::SMEM_ALLOC);
+    auto kernel = gf16::gemm_ws_kernel<kCtaGroup, kBlockN, kStages, kTmaStore, kBf16>;
+    int rc = ensure_smem(d, variant + (kBf16 ? GEMM_F16_NUM_VARIANTS : 0), kernel, C::SMEM_ALLOC);
     if (rc != GEMM_F16_OK) return rc;
 
     const int64_t num_m = cdiv(M, C::MMA_M);
@@ -368,7 +380,7 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
         return GEMM_F16_OK;
     }
     const CUtensorMap *ma, *mb, *md;
-    MapKey key{A, B, D, M, N, K, variant, dev};
+    MapKey key{A, B, D, M, N, K, variant, dev, kBf16 ? GEMM_F16_DTYPE_BF16 : GEMM_F16_DTYPE_F16};
     if ((rc = get_maps(key, 128, C::B_ROWS, kTmaStore, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
     if (R && (workspace == nullptr || workspace_bytes < need ||
               (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
@@ -393,7 +405,9 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
                                        (uint32_t)num_m, (uint32_t)num_n, (uint32_t)KB,
                                        group_m_setting(), wait_timeout_ns(), l2_hint_setting(),
                                        ws_part, ws_count, (uint32_t)R,
-                                       (uint32_t)(R ? sk_units_for(R, units_used) : units_used));
+                                       (uint32_t)(R ? sk_units_for(R, units_used) : units_used),
+                                       static_cast<const uint16_t*>(epi.bias),
+                                       static_cast<uint32_t>(epi.act));
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_ws_kernel)");
     return GEMM_F16_OK;
 }
@@ -423,7 +437,7 @@ int check_args(const void* A, const void* B, void* D, int64_t M, int64_t N, int6
 
 int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
         cudaStream_t stream, int variant, void* ws = nullptr, size_t ws_bytes = 0,
-        size_t* bytes_needed = nullptr)
+        size_t* bytes_needed = nullptr, const EpiOpts& epi = EpiOpts{})
 {
     t_last_error.clear();
     if (bytes_needed) *bytes_needed = 0;
@@ -443,6 +457,39 @@ int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
     int dev = 0;
     cudaGetDevice(&dev);
     if (variant == GEMM_F16_VARIANT_AUTO) variant = choose_variant(M, N, K, d->sms);
+    const bool plain = epi.dtype == GEMM_F16_DTYPE_F16 && epi.bias == nullptr &&
+                       epi.act == GEMM_F16_ACT_NONE;
+    if (!plain) {
+        if (epi.dtype != GEMM_F16_DTYPE_F16 && epi.dtype != GEMM_F16_DTYPE_BF16)
+            return fail(GEMM_F16_ERR_INVALID_ARG, "unknown dtype %d", epi.dtype);
+        if (epi.act < GEMM_F16_ACT_NONE || epi.act > GEMM_F16_ACT_GELU)
+            return fail(GEMM_F16_ERR_INVALID_ARG, "unknown activation %d", epi.act);
+        if (epi.bias != nullptr && (reinterpret_cast<uintptr_t>(epi.bias) & 15u) != 0)
+            return fail(GEMM_F16_ERR_UNSUPPORTED, "bias must be 16-byte aligned");
+        if (K == 0)
+            return fail(GEMM_F16_ERR_UNSUPPORTED, "K == 0 with a fused epilogue is not supported");
+        const bool bf = epi.dtype == GEMM_F16_DTYPE_BF16;
+        switch (variant) {
+        case GEMM_F16_VARIANT_WS_128x256:
+            return bf ? launch_ws<1, 256, 4, true, true>(variant, A, B, D, M, N, K, stream, *d, dev,
+                                                         ws, ws_bytes, bytes_needed, epi)
+                      : launch_ws<1, 256, 4, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                                   ws_bytes, bytes_needed, epi);
+        case GEMM_F16_VARIANT_WS_PAIR:
+            return bf ? launch_ws<2, 256, 6, true, true>(variant, A, B, D, M, N, K, stream, *d, dev,
+                                                         ws, ws_bytes, bytes_needed, epi)
+                      : launch_ws<2, 256, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                                   ws_bytes, bytes_needed, epi);
+        case GEMM_F16_VARIANT_WS_128x128:
+            return bf ? launch_ws<1, 128, 6, true, true>(variant, A, B, D, M, N, K, stream, *d, dev,
+                                                         ws, ws_bytes, bytes_needed, epi)
+                      : launch_ws<1, 128, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                                   ws_bytes, bytes_needed, epi);
+        default:
+            return fail(GEMM_F16_ERR_UNSUPPORTED,
+                        "variant %d has no bf16 / fused-epilogue form (use 0, 2, 3 or 4)", variant);
+        }
+    }
     switch (variant) {
     case GEMM_F16_VARIANT_TILE:
         if (bytes_needed) return GEMM_F16_OK;
@@ -521,6 +568,17 @@ int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, 
                    int variant, void* workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     return run(A, B, D, M, N, K, stream, variant, workspace, workspace_bytes);
+}
+
+int gemm_f16_nt_fused(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                      int dtype, const void* bias, int activation, int variant, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream)
+{
+    EpiOpts epi;
+    epi.dtype = dtype;
+    epi.bias = bias;
+    epi.act = activation;
+    return run(A, B, D, M, N, K, stream, variant, workspace, workspace_bytes, nullptr, epi);
 }
 
 int gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,

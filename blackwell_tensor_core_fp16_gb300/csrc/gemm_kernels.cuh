@@ -42,6 +42,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "desc.h"
 #include "ptx.cuh"
@@ -204,6 +205,56 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ==============================================================================================
+// The fused epilogue of a linear layer: y = act(x + bias[column]) on the fp32 accumulator,
+// before the single rounding to the output type.  act: 0 none, 1 ReLU, 2 GELU (exact form,
+// x * Phi(x) = x/2 * (1 + erf(x / sqrt 2)), with CUDA's erff).
+// ==============================================================================================
+constexpr uint32_t kActNone = 0, kActRelu = 1, kActGelu = 2;
+
+__device__ __forceinline__ float apply_act(float v, uint32_t act)
+{
+    if (act == kActRelu) return fmaxf(v, 0.f);
+    if (act == kActGelu) return 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+    return v;
+}
+
+// Widen a 16-bit element of the given type (fp16 or bf16) to fp32.
+template <bool kBf16>
+__device__ __forceinline__ float widen16(uint32_t h)
+{
+    if constexpr (kBf16) return __uint_as_float(h << 16);
+    else return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+// 8 consecutive fp32 accumulators of columns col .. col+7 -> act(acc + bias).  `col` is a
+// multiple of 8 and N % 8 == 0, so the 16-byte bias vector is all in or all out.
+template <bool kBf16>
+__device__ __forceinline__ void epilogue8(float (&v)[8], const uint16_t* bias, int32_t col,
+                                          uint32_t N, uint32_t act)
+{
+    if (bias != nullptr && col < static_cast<int32_t>(N)) {
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + col));
+        const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] += widen16<kBf16>(w[i] & 0xFFFFu);
+            v[2 * i + 1] += widen16<kBf16>(w[i] >> 16);
+        }
+    }
+    if (act != kActNone) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = apply_act(v[i], act);
+    }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits)
+{
+    if constexpr (kBf16) return pack_bf16x2_rn(lo_bits, hi_bits);
+    else return pack_f16x2_rn(lo_bits, hi_bits);
+}
+
+// ==============================================================================================
 // gemm_ws_kernel: persistent, warp-specialised, TMEM double-buffered.
 // ==============================================================================================
 template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore = true>
@@ -238,7 +289,7 @@ struct WsCfg {
     static constexpr uint32_t EPI_THREADS = 128;
 };
 
-template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore>
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore, bool kBf16 = false>
 __global__ void __launch_bounds__(192, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
@@ -247,11 +298,13 @@ __global__ void __launch_bounds__(192, 1)
                    uint32_t num_m_blocks, uint32_t num_n_blocks, uint32_t num_k_blocks,
                    uint32_t group_m, uint64_t timeout_ns, uint32_t l2_hints,
                    float* __restrict__ ws_part, uint32_t* __restrict__ ws_count,
-                   uint32_t sk_tiles, uint32_t sk_units)
+                   uint32_t sk_tiles, uint32_t sk_units, const uint16_t* __restrict__ bias,
+                   uint32_t act)
 {
     using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
     constexpr bool kPair = (kCtaGroup == 2);
-    constexpr uint32_t idesc = make_idesc_f16(C::MMA_M, C::BN, 0);
+    constexpr uint32_t idesc = make_idesc_f16(C::MMA_M, C::BN, kBf16 ? 1u : 0u);
+    const bool fused = bias != nullptr || act != kActNone;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -563,12 +616,32 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
                 if (col0 < static_cast<int32_t>(N) && rows_in) {
+                    if (fused) {
+#pragma unroll
+                        for (int g8 = 0; g8 < 4; ++g8) {
+                            float f[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v0[8 * g8 + i]);
+                            epilogue8<kBf16>(f, bias, col0 + 8 * g8, N, act);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v0[8 * g8 + i] = __float_as_uint(f[i]);
+                        }
+#pragma unroll
+                        for (int g8 = 0; g8 < 4; ++g8) {
+                            float f[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v1[8 * g8 + i]);
+                            epilogue8<kBf16>(f, bias, col0 + 32 + 8 * g8, N, act);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) v1[8 * g8 + i] = __float_as_uint(f[i]);
+                        }
+                    }
                     uint32_t p[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) p[i] = pack_f16x2_rn(v0[2 * i], v0[2 * i + 1]);
+                    for (int i = 0; i < 16; ++i) p[i] = pack2<kBf16>(v0[2 * i], v0[2 * i + 1]);
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        p[16 + i] = pack_f16x2_rn(v1[2 * i], v1[2 * i + 1]);
+                        p[16 + i] = pack2<kBf16>(v1[2 * i], v1[2 * i + 1]);
                     store_chunk(p, m0, col0);
                 }
             }
@@ -601,19 +674,21 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t ncontrib = u1 - u0 + 1u;
 #pragma unroll 1
             for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
+                const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
                 uint32_t p[32];
 #pragma unroll
-                for (uint32_t h = 0; h < 2; ++h) {
-                    float4 x[kMaxContrib][8];
+                for (uint32_t h = 0; h < 4; ++h) {   // 16 columns per step
+                    float4 x[kMaxContrib][4];
 #pragma unroll
                     for (uint32_t q = 0; q < kMaxContrib; ++q)
 #pragma unroll
-                        for (uint32_t j = 0; j < 8; ++j)
+                        for (uint32_t j = 0; j < 4; ++j)
                             x[q][j] = q < ncontrib
-                                          ? __ldcg(srcs[q] + (c * 16u + h * 8u + j) * 128u)
+                                          ? __ldcg(srcs[q] + (c * 16u + h * 4u + j) * 128u)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float f[16];
 #pragma unroll
-                    for (uint32_t j = 0; j < 8; ++j) {
+                    for (uint32_t j = 0; j < 4; ++j) {
                         float4 t = x[0][j];
 #pragma unroll
                         for (uint32_t q = 1; q < kMaxContrib; ++q) {
@@ -622,12 +697,28 @@ __global__ void __launch_bounds__(192, 1)
                             t.z += x[q][j].z;
                             t.w += x[q][j].w;
                         }
-                        p[h * 16 + 2 * j] = pack_f16x2_rn(__float_as_uint(t.x), __float_as_uint(t.y));
-                        p[h * 16 + 2 * j + 1] =
-                            pack_f16x2_rn(__float_as_uint(t.z), __float_as_uint(t.w));
+                        f[4 * j] = t.x;
+                        f[4 * j + 1] = t.y;
+                        f[4 * j + 2] = t.z;
+                        f[4 * j + 3] = t.w;
                     }
+                    if (fused) {
+#pragma unroll
+                        for (int g8 = 0; g8 < 2; ++g8) {
+                            float e[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) e[i] = f[8 * g8 + i];
+                            epilogue8<kBf16>(e, bias, col0 + static_cast<int32_t>(h * 16u) + 8 * g8,
+                                             N, act);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) f[8 * g8 + i] = e[i];
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        p[h * 8 + i] = pack2<kBf16>(__float_as_uint(f[2 * i]),
+                                                    __float_as_uint(f[2 * i + 1]));
                 }
-                const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
                 if (col0 < static_cast<int32_t>(N) && rows_in) store_chunk(p, m0, col0);
             }
             if (et == 0) ws_count[r * kCtaGroup + rank] = 0u;

@@ -408,6 +408,16 @@ __device__ __forceinline__ uint32_t pack_f16x2_rn(uint32_t lo_bits, uint32_t hi_
     return out;
 }
 
+// Two fp32 values -> one bf16x2 word, each rounded to nearest even; `lo` lands in bits 15:0.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(uint32_t lo_bits, uint32_t hi_bits)
+{
+    uint32_t out;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+        : "=r"(out)
+        : "f"(__uint_as_float(hi_bits)), "f"(__uint_as_float(lo_bits)));
+    return out;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)
 {

@@ -67,24 +67,34 @@ WORKLOADS = {
 ORDER = list(WORKLOADS)
 
 
-def _draw(gen: torch.Generator, shape, dist: str, scale: float) -> torch.Tensor:
+def _draw(gen: torch.Generator, shape, dist: str, scale: float,
+          dtype=torch.float16) -> torch.Tensor:
     if dist == "uniform":
         x = torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
     elif dist == "normal":
         x = torch.randn(shape, generator=gen, dtype=torch.float32) * scale
     else:
         raise ValueError(f"unknown distribution {dist!r}")
-    return x.to(torch.float16)
+    return x.to(dtype)
 
 
 def make_inputs(M: int, N: int, K: int, seed: int, a_dist: str = "uniform",
-                a_scale: float = 1.0, b_dist: str = "uniform", b_scale: float = 1.0):
-    """(A, B) as contiguous CPU fp16 tensors of shapes (M, K) and (N, K)."""
+                a_scale: float = 1.0, b_dist: str = "uniform", b_scale: float = 1.0,
+                dtype=torch.float16):
+    """(A, B) as contiguous CPU tensors of shapes (M, K) and (N, K), fp16 unless `dtype` says
+    bfloat16 (drawn in float32, then rounded to the 16-bit type)."""
     gen = torch.Generator(device="cpu")
     gen.manual_seed(int(seed))
-    A = _draw(gen, (M, K), a_dist, a_scale)
-    B = _draw(gen, (N, K), b_dist, b_scale)
+    A = _draw(gen, (M, K), a_dist, a_scale, dtype)
+    B = _draw(gen, (N, K), b_dist, b_scale, dtype)
     return A.contiguous(), B.contiguous()
+
+
+def make_bias(N: int, seed: int, scale: float = 1.0, dtype=torch.float16) -> torch.Tensor:
+    """A bias vector of N elements, uniform on [-scale, scale]."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed) + 7919)
+    return ((torch.rand(N, generator=gen, dtype=torch.float32) * 2.0 - 1.0) * scale).to(dtype)
 
 
 def workload_inputs(w: Workload):

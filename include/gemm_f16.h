@@ -77,6 +77,32 @@ int gemm_f16_nt(const void* A, const void* B, void* D, int64_t M, int64_t N, int
 int gemm_f16_nt_variant(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                         cudaStream_t stream, int variant);
 
+/* Element types and activations of gemm_f16_nt_fused. */
+#define GEMM_F16_DTYPE_F16 0  /* IEEE binary16 */
+#define GEMM_F16_DTYPE_BF16 1 /* bfloat16 */
+#define GEMM_F16_ACT_NONE 0
+#define GEMM_F16_ACT_RELU 1   /* max(y, 0) */
+#define GEMM_F16_ACT_GELU 2   /* y * Phi(y) = y/2 * (1 + erf(y / sqrt 2)), the exact form */
+
+/*
+ * A linear layer: D = act(A * B^T + bias), for fp16 or bf16 data.  bf16 inputs use the same
+ * tensor-core path as fp16 (tcgen05.mma .kind::f16 with the instruction descriptor's A/B format
+ * set to bf16); the page "TIRx" (section "SM90a 支持具体补了什么") names FP16 and BF16 inputs with
+ * FP32 accumulation, and the page "TIRx 与高性能GEMM (上)" motivates the GEMM by linear layers.
+ *
+ * dtype:      GEMM_F16_DTYPE_F16 or GEMM_F16_DTYPE_BF16, for A, B, D and bias alike.
+ * bias:       N elements (one per output column), 16-byte aligned, or null for none.
+ * activation: GEMM_F16_ACT_*.
+ * variant:    GEMM_F16_VARIANT_AUTO or one of the persistent variants (2, 3, 4).
+ * workspace:  as gemm_f16_nt_ws (may be null).
+ * The bias and the activation are applied in fp32 to the fp32 sum; the result is then rounded
+ * once (round to nearest even) to the output type.  K must be at least 1.  Other rules and
+ * return codes as gemm_f16_nt.
+ */
+int gemm_f16_nt_fused(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
+                      int dtype, const void* bias, int activation, int variant, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream);
+
 /*
  * D = A * B^T with a caller-provided workspace, which lets the persistent kernels run the tiles
  * of the last, partial wave "stream-K": their k-blocks are split evenly over all CTAs, each CTA
