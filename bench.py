@@ -392,6 +392,7 @@ def run_ours(args):
     # from before the first upload to after the last download.
     e2e_steps = 0 if args.skip_e2e else max(3, min(args.e2e_steps, K))
     e2e_value = None
+    link_gbs = copy_roof = None
     h2d = d2h = 0
     if e2e_steps:
         s_up = torch.cuda.Stream(device=dev)
@@ -451,6 +452,25 @@ def run_ours(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e_ms = float(t.item())
         e2e_value = world * e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+        # The copy roofline of this leg: the measured rate of concurrent pinned-host copies in
+        # both directions (256 MiB each way, the same streams), and the TFLOP/s a step could
+        # reach if its copies ran at that rate and the GEMMs hid under them.
+        nb = 256 << 20
+        hsrc = torch.empty(nb, dtype=torch.uint8).pin_memory()
+        hdst = torch.empty(nb, dtype=torch.uint8).pin_memory()
+        dsrc = torch.empty(nb, dtype=torch.uint8, device=dev)
+        ddst = torch.empty(nb, dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        c0 = time.perf_counter()
+        for _ in range(8):
+            with torch.cuda.stream(s_up):
+                ddst.copy_(hsrc, non_blocking=True)
+            with torch.cuda.stream(s_down):
+                hdst.copy_(dsrc, non_blocking=True)
+        torch.cuda.synchronize()
+        link_gbs = 8 * 2 * nb / (time.perf_counter() - c0) / 1e9
+        copy_roof = flops_step / ((h2d + d2h) / (link_gbs * 1e9)) / 1e12
+        del hsrc, hdst, dsrc, ddst
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -481,6 +501,9 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "copy_link_gbs_measured": link_gbs,
+                "copy_roofline_tflops": copy_roof,
+                "frac_of_copy_roofline": (e2e_value / world / copy_roof) if copy_roof else None,
                 "path": "pinned host A,B -> device (copy stream), gemm() public API, "
                         "D -> pinned host (copy stream); two buffer slots, copies of "
                         "neighbouring steps overlap the GEMMs"},

@@ -21,7 +21,8 @@ __all__ = [
     "gemm_f16_last_error", "gemm_f16_version", "gemm_f16_get_variant_info", "gemm_f16_idesc",
     "gemm_f16_smem_desc_sw128", "gemm_f16_sw128", "gemm_f16_tile_coord", "gemm_f16_ring_pos",
     "gemm_f16_nt_ws", "gemm_f16_nt_ex", "gemm_f16_nt_noalloc", "gemm_f16_workspace_bytes",
-    "gemm_f16_nt_fused", "linear", "DTYPES", "ACTIVATIONS",
+    "gemm_f16_nt_fused", "linear", "DTYPES", "ACTIVATIONS", "gemm_f16_set_wait_timeout_ms",
+    "gemm_f16_set_fault_injection",
     "gemm_f16_sk_tail_tiles",
     "gemm_f16_sk_items", "gemm_f16_sk_item", "gemm_f16_sk_unit_of",
     "exported_symbols", "VARIANTS", "STATUS",
@@ -103,6 +104,10 @@ def load():
         lib.gemm_f16_nt_fused.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, i32, vp, sz,
                                           vp]
         lib.gemm_f16_nt_fused.restype = i32
+        lib.gemm_f16_set_wait_timeout_ms.argtypes = [u32]
+        lib.gemm_f16_set_wait_timeout_ms.restype = i32
+        lib.gemm_f16_set_fault_injection.argtypes = [i32]
+        lib.gemm_f16_set_fault_injection.restype = i32
         lib.gemm_f16_workspace_bytes.argtypes = [i64, i64, i64, i32, ctypes.POINTER(sz)]
         lib.gemm_f16_workspace_bytes.restype = i32
         lib.gemm_f16_sk_tail_tiles.argtypes = [i64, i64, i64]
@@ -217,6 +222,14 @@ def gemm_f16_check_status(stream: int = 0):
     bits = ctypes.c_uint32(0)
     rc = load().gemm_f16_check_status(stream, ctypes.byref(bits))
     return rc, bits.value
+
+
+def gemm_f16_set_wait_timeout_ms(ms: int) -> int:
+    return load().gemm_f16_set_wait_timeout_ms(ms)
+
+
+def gemm_f16_set_fault_injection(mode: int) -> int:
+    return load().gemm_f16_set_fault_injection(mode)
 
 
 def gemm_f16_last_error() -> str:

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -40,16 +41,27 @@ int cuda_fail(cudaError_t e, const char* what)
 }
 
 // ---- configuration read once from the environment --------------------------------------------
+// Wall-clock limit of one bounded wait inside a kernel: GEMM_F16_WAIT_TIMEOUT_MS at first use
+// (default 4000 ms), changeable with gemm_f16_set_wait_timeout_ms.
+std::atomic<uint64_t> g_timeout_ns{0};
+std::atomic<uint32_t> g_debug_flags{0};
+
 uint64_t wait_timeout_ns()
 {
-    static const uint64_t v = [] {
+    uint64_t v = g_timeout_ns.load(std::memory_order_relaxed);
+    if (v == 0) {
         const char* s = std::getenv("GEMM_F16_WAIT_TIMEOUT_MS");
         long long ms = s ? std::atoll(s) : 4000;
         if (ms < 1) ms = 1;
-        return static_cast<uint64_t>(ms) * 1000000ull;
-    }();
+        v = static_cast<uint64_t>(ms) * 1000000ull;
+        uint64_t expected = 0;
+        g_timeout_ns.compare_exchange_strong(expected, v);
+        v = g_timeout_ns.load(std::memory_order_relaxed);
+    }
     return v;
 }
+
+uint32_t debug_flags() { return g_debug_flags.load(std::memory_order_relaxed); }
 
 // L2 priorities for the A and B loads: bits 1:0 A, bits 3:2 B (0 normal, 1 evict_first,
 // 2 evict_last).  Default: A evict_last (a band of A rows is reused by every tile of its group
@@ -282,7 +294,7 @@ int launch_tile(const void* A, const void* B, void* D, int64_t M, int64_t N, int
     if (grid.y > 65535u) return fail(GEMM_F16_ERR_UNSUPPORTED, "M too large for the tile variant");
     gf16::gemm_tile_kernel<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(
         *ma, *mb, static_cast<uint16_t*>(D), (uint32_t)M, (uint32_t)N, (uint32_t)cdiv(K, 64),
-        wait_timeout_ns());
+        wait_timeout_ns(), debug_flags());
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch of gemm_tile_kernel");
     return GEMM_F16_OK;
@@ -407,7 +419,7 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
                                        ws_part, ws_count, (uint32_t)R,
                                        (uint32_t)(R ? sk_units_for(R, units_used) : units_used),
                                        static_cast<const uint16_t*>(epi.bias),
-                                       static_cast<uint32_t>(epi.act));
+                                       static_cast<uint32_t>(epi.act), debug_flags());
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_ws_kernel)");
     return GEMM_F16_OK;
 }
@@ -634,6 +646,20 @@ int gemm_f16_check_status(cudaStream_t stream, uint32_t* bits)
 }
 
 const char* gemm_f16_last_error(void) { return t_last_error.c_str(); }
+
+int gemm_f16_set_wait_timeout_ms(uint32_t ms)
+{
+    if (ms == 0) return fail(GEMM_F16_ERR_INVALID_ARG, "timeout must be at least 1 ms");
+    g_timeout_ns.store(static_cast<uint64_t>(ms) * 1000000ull);
+    return GEMM_F16_OK;
+}
+
+int gemm_f16_set_fault_injection(int mode)
+{
+    if (mode < 0 || mode > 1) return fail(GEMM_F16_ERR_INVALID_ARG, "unknown injection %d", mode);
+    g_debug_flags.store(mode == 1 ? gf16::kDebugNoLoads : 0u);
+    return GEMM_F16_OK;
+}
 
 int gemm_f16_version(void) { return kVersion; }
 

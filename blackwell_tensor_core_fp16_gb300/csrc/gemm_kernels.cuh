@@ -49,6 +49,11 @@
 
 namespace gf16 {
 
+// Debug flags of a launch (testing the failure path without faulting anything).
+// kDebugNoLoads: the producer issues no copies and arms no barrier, so the first wait on a
+// "full" barrier can only run out; nothing asynchronous is ever in flight.
+constexpr uint32_t kDebugNoLoads = 1u;
+
 // Bits reported through gemm_f16_status_word (read and cleared by the host).
 constexpr uint32_t kStatusProducerTimeout = 1u;
 constexpr uint32_t kStatusMmaTimeout = 2u;
@@ -95,7 +100,8 @@ struct TileCfg {
 __global__ void __launch_bounds__(128, 1)
     gemm_tile_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b, uint16_t* __restrict__ D,
-                     uint32_t M, uint32_t N, uint32_t num_k_blocks, uint64_t timeout_ns)
+                     uint32_t M, uint32_t N, uint32_t num_k_blocks, uint64_t timeout_ns,
+                     uint32_t debug_flags)
 {
     using C = TileCfg;
     extern __shared__ uint8_t smem_raw[];
@@ -138,9 +144,11 @@ __global__ void __launch_bounds__(128, 1)
         bool issued_mma = false;
         for (uint32_t kb = 0; kb < num_k_blocks; ++kb) {
             const int32_t k0 = static_cast<int32_t>(kb * kBlockK);
-            mbar_arrive_expect_tx(tma_bar, C::STAGE_TX);
-            tma_load_2d(sA, &tmap_a, tma_bar, k0, m0);
-            tma_load_2d(sB, &tmap_b, tma_bar, k0, n0);
+            if (!(debug_flags & kDebugNoLoads)) {
+                mbar_arrive_expect_tx(tma_bar, C::STAGE_TX);
+                tma_load_2d(sA, &tmap_a, tma_bar, k0, m0);
+                tma_load_2d(sB, &tmap_b, tma_bar, k0, n0);
+            }
             if (!mbar_wait(tma_bar, phase, abort_flag, timeout_ns)) {
                 report(kStatusProducerTimeout, abort_flag);
                 ok = false;
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(192, 1)
                    uint32_t group_m, uint64_t timeout_ns, uint32_t l2_hints,
                    float* __restrict__ ws_part, uint32_t* __restrict__ ws_count,
                    uint32_t sk_tiles, uint32_t sk_units, const uint16_t* __restrict__ bias,
-                   uint32_t act)
+                   uint32_t act, uint32_t debug_flags)
 {
     using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
     constexpr bool kPair = (kCtaGroup == 2);
@@ -374,7 +382,8 @@ __global__ void __launch_bounds__(192, 1)
         WorkItem wi = work_item(split, cid, 0);
         uint32_t kb = wi.kb0;
         int32_t m0 = 0, n0 = 0;
-        for (; it < total; ++it) {
+        const uint32_t produce = (debug_flags & kDebugNoLoads) ? 0u : total;
+        for (; it < produce; ++it) {
             if (kb == wi.kb0) {
                 const TileCoord tc = tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
                 m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);

@@ -161,6 +161,17 @@ int gemm_f16_choose_variant(int64_t M, int64_t N, int64_t K, int num_sms);
  * null, receives which roles did) or GEMM_F16_ERR_CUDA. */
 int gemm_f16_check_status(cudaStream_t stream, uint32_t* bits);
 
+/* Wall-clock limit of each bounded wait inside the kernels, for launches made after the call
+ * (default: GEMM_F16_WAIT_TIMEOUT_MS, else 4000 ms).  A wait that runs out makes the kernel stop
+ * cleanly and report GEMM_F16_ERR_TIMEOUT through gemm_f16_check_status. */
+int gemm_f16_set_wait_timeout_ms(uint32_t ms);
+
+/* Testing hook for the failure path, process-wide, for launches made after the call.  mode 1:
+ * the kernels' load producer issues no copies, so the first wait for operand data can only run
+ * out (nothing asynchronous is left in flight; the kernel reports TIMEOUT and exits cleanly);
+ * mode 0: normal operation.  Never set it outside tests. */
+int gemm_f16_set_fault_injection(int mode);
+
 /* Description of the last error on the calling thread ("" if none).  The string stays valid
  * until the thread's next call into the library. */
 const char* gemm_f16_last_error(void);

@@ -1,0 +1,65 @@
+"""Failure detection on the GPU without faulting it (needs a GB300).
+
+Every wait inside the kernels is bounded.  With the testing hook gemm_f16_set_fault_injection(1)
+the load producer issues nothing, so the first wait for operand data waits on a barrier that
+nothing will complete; with a 200 ms limit the wait runs out, the kernel stops cleanly (no copy
+or MMA is ever in flight), and the host reads GEMM_F16_ERR_TIMEOUT with the roles that gave up.
+The context must stay usable: a normal GEMM right after still matches the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import blackwell_tensor_core_fp16_gb300 as g
+import oracle
+from blackwell_tensor_core_fp16_gb300.workloads import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def restore_settings():
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    g.build()
+    g.load()
+    yield
+    g.gemm_f16_set_fault_injection(0)
+    g.gemm_f16_set_wait_timeout_ms(4000)
+    torch.cuda.synchronize()
+    g.gemm_f16_check_status(0)
+
+
+@pytest.mark.parametrize("variant,expect_bits", [
+    (g.VARIANTS["tile"], 1),         # the single-tile kernel's load wait
+    (g.VARIANTS["ws_128x128"], 2),   # the MMA issuer's wait for operand data
+    (g.VARIANTS["ws_pair"], 2),      # same, in a CTA pair (the other CTA's epilogue also gives up)
+])
+def test_wait_runs_out_and_context_survives(variant, expect_bits):
+    M, N, K = 520, 776, 1000
+    A, B = make_inputs(M, N, K, seed=700)
+    Ad, Bd = A.cuda(), B.cuda()
+    D = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert g.gemm_f16_set_wait_timeout_ms(200) == g.OK
+    assert g.gemm_f16_set_fault_injection(1) == g.OK
+    assert g.gemm_f16_nt_variant(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, s,
+                                 variant) == g.OK
+    rc, bits = g.gemm_f16_check_status(s)
+    assert rc == g.ERR_TIMEOUT, (rc, bits)
+    assert bits & expect_bits, f"bits 0x{bits:x}"
+    assert "bounded wait" in g.gemm_f16_last_error()
+    # the status word was cleared by the read
+    assert g.gemm_f16_check_status(s) == (g.OK, 0)
+
+    # back to normal: the same context computes correctly
+    assert g.gemm_f16_set_fault_injection(0) == g.OK
+    assert g.gemm_f16_set_wait_timeout_ms(4000) == g.OK
+    assert g.gemm_f16_nt_variant(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), M, N, K, s,
+                                 variant) == g.OK
+    assert g.gemm_f16_check_status(s) == (g.OK, 0)
+    d = D.cpu().double().numpy()
+    ref = oracle.gemm_f64(A, B)
+    assert (np.abs(d - ref) <= oracle.tolerance(ref, K)).all()

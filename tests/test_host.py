@@ -341,3 +341,11 @@ def test_stream_k_tail_choice():
     assert g.gemm_f16_sk_tail_tiles(76 * 5 + 75, 76, 64) == 0  # last wave 99% full
     assert g.gemm_f16_sk_tail_tiles(240, 76, 16) == 12        # 12 tiles over 36 units
     assert g.gemm_f16_sk_tail_tiles(240, 76, 3) == 0          # pieces under 4 k-blocks
+
+
+def test_failure_hooks_validate_arguments():
+    assert g.gemm_f16_set_wait_timeout_ms(0) == g.ERR_INVALID_ARG
+    assert g.gemm_f16_set_fault_injection(2) == g.ERR_INVALID_ARG
+    assert g.gemm_f16_set_fault_injection(-1) == g.ERR_INVALID_ARG
+    assert g.gemm_f16_set_fault_injection(0) == g.OK
+    assert g.gemm_f16_set_wait_timeout_ms(4000) == g.OK
