@@ -47,6 +47,17 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--only", default="", help="comma-separated subset of the step's workloads")
     p.add_argument("--skip-e2e", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="time every workload under every kernel variant (with and without a "
+                        "stream-K workspace) and print one JSON line per case instead of the "
+                        "bench line")
+    p.add_argument("--sweep-workloads", default="",
+                   help="comma-separated subset of workloads for --sweep (default: all five)")
+    p.add_argument("--sweep-variants", default="1,2,3,4,5",
+                   help="variants for --sweep; 'auto' = the automatic choice only")
+    p.add_argument("--sweep-reps", type=int, default=0,
+                   help="timed launches per case in --sweep (0: about 0.3 s of work)")
+    p.add_argument("--sweep-no-stream-k", action="store_true")
     p.add_argument("--cublas-steps", type=int, default=-1,
                    help="steps of torch.mm on the same shapes, for context (-1: as many as "
                         "--steps, 0: skip)")
@@ -518,10 +529,75 @@ def run_ours(args):
     return 0
 
 
+def run_sweep(args):
+    """Per workload and variant: TFLOP/s and algorithmic HBM GB/s of back-to-back launches."""
+    import torch
+
+    import blackwell_tensor_core_fp16_gb300 as g
+    from blackwell_tensor_core_fp16_gb300.workloads import ORDER, WORKLOADS as W, workload_inputs
+
+    g.build()
+    g.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    names = [n.strip() for n in args.sweep_workloads.split(",") if n.strip()] or ORDER
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    for name in names:
+        w = W[name]
+        A, B = workload_inputs(w)
+        Ad, Bd = A.to(dev), B.to(dev)
+        D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+        auto = g.gemm_f16_choose_variant(w.M, w.N, w.K, sms)
+        variants = ([auto] if args.sweep_variants == "auto"
+                    else [int(v) for v in args.sweep_variants.split(",")])
+        for variant in variants:
+            for use_ws in ((False,) if args.sweep_no_stream_k else (False, True)):
+                need = g.gemm_f16_workspace_bytes(w.M, w.N, w.K, variant) if use_ws else 0
+                if use_ws and need == 0:
+                    continue
+                ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+                def launch():
+                    rc = g.gemm_f16_nt_ex(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), w.M, w.N,
+                                          w.K, variant, ws.data_ptr(), need, stream.cuda_stream)
+                    if rc != g.OK:
+                        raise g.GemmError(rc, g.gemm_f16_last_error())
+
+                with torch.cuda.stream(stream):
+                    for _ in range(5):
+                        launch()
+                torch.cuda.synchronize()
+                # enough launches for ~0.3 s of work
+                t0 = time.perf_counter()
+                with torch.cuda.stream(stream):
+                    launch()
+                torch.cuda.synchronize()
+                reps = args.sweep_reps or max(10, min(5000, int(0.3 / max(time.perf_counter() - t0,
+                                                                           1e-6))))
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    for _ in range(reps):
+                        launch()
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                g.check_status(stream)
+                ms = e0.elapsed_time(e1) / reps
+                print(json.dumps({
+                    "workload": name, "M": w.M, "N": w.N, "K": w.K, "variant": variant,
+                    "auto_variant": auto, "stream_k": bool(need), "launches": reps,
+                    "ms_per_launch": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
+                    "hbm_gbs_algorithmic": w.min_bytes / (ms * 1e-3) / 1e9}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

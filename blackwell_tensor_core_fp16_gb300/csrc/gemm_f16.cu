@@ -130,11 +130,17 @@ bool variant_info(int v, gemm_f16_variant_info* o)
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Automatic variant.  Measured on GB300 (bench.py --sweep): the CTA pair is fastest once its
+// tiles fill the GPU (3000x5000x1000, 8192^3, MLP shape); when every 128x256 tile fits in one
+// wave that keeps at least half the SMs busy, the single-CTA 128x256 kernel wins (2048^3: 16.8 us
+// against 18.9 us for the pair); below that, 128x128 tiles keep more SMs busy.
 int choose_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
 {
     if (num_sms < 2) num_sms = 2;
     const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 256);
     const int64_t tiles_128x256 = cdiv(M, 128) * cdiv(N, 256);
+    if (tiles_128x256 <= num_sms && 2 * tiles_128x256 >= num_sms)
+        return GEMM_F16_VARIANT_WS_128x256;
     if (M > 128 && pair_tiles >= num_sms / 2) return GEMM_F16_VARIANT_WS_PAIR;
     if (tiles_128x256 >= num_sms) return GEMM_F16_VARIANT_WS_128x256;
     return GEMM_F16_VARIANT_WS_128x128;
