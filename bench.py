@@ -32,6 +32,7 @@ METRIC = "fp16 GEMM TFLOP/s at 8192³ and MLP shape; % of GB300 dense fp16 peak"
 WORKLOADS = ("square_8192", "mlp_up_16384x14336x4096")
 FALLBACK_PEAK_TFLOPS = 1900.0
 L2_BYTES = 129e6
+FLOP_PER_CLK_PER_SM = 8192
 
 
 def parse_args():
@@ -58,6 +59,12 @@ def parse_args():
     p.add_argument("--sweep-reps", type=int, default=0,
                    help="timed launches per case in --sweep (0: about 0.3 s of work)")
     p.add_argument("--sweep-no-stream-k", action="store_true")
+    p.add_argument("--sweep-cold-l2", action="store_true",
+                   help="in --sweep, write a 512 MiB scratch buffer before every launch and time "
+                        "each launch alone (events around the launch only)")
+    p.add_argument("--sweep-processes", type=int, default=1,
+                   help="run --sweep in this many fresh processes and report, per case, the "
+                        "median of the per-process means")
     p.add_argument("--cublas-steps", type=int, default=-1,
                    help="steps of torch.mm on the same shapes, for context (-1: as many as "
                         "--steps, 0: skip)")
@@ -361,6 +368,14 @@ def run_ours(args):
                 "achieved_def": "algorithmic 2*M*N*K over both launches of a step / summed "
                                 "CUDA-event launch durations"}
 
+    # The peak implied by the clock seen during the timed region: 8192 dense fp16 FLOP per
+    # clock per SM (one 256x256x16 cta_group::2 MMA per 128 cycles per CTA pair, measured with a
+    # bare MMA stream) times the SMs times the median sampled SM clock.
+    if clock_info and clock_info.get("sm_mhz"):
+        cpk = num_sms * FLOP_PER_CLK_PER_SM * clock_info["sm_mhz"] * 1e6 / 1e12
+        roofline["clock_peak_tflops"] = cpk
+        roofline["frac_of_clock_peak"] = achieved / cpk
+
     # cuBLAS (torch.mm) on the same resident inputs and the same step, run back to back for the
     # same number of steps right after ours so both see the same power-capped clocks.  Context
     # only: it is a library kernel, not part of this path.
@@ -542,6 +557,8 @@ def run_sweep(args):
     stream = torch.cuda.Stream(device=dev)
     names = [n.strip() for n in args.sweep_workloads.split(",") if n.strip()] or ORDER
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    scratch = (torch.empty(512 << 20, dtype=torch.uint8, device=dev) if args.sweep_cold_l2
+               else None)
     for name in names:
         w = W[name]
         A, B = workload_inputs(w)
@@ -567,6 +584,26 @@ def run_sweep(args):
                     for _ in range(5):
                         launch()
                 torch.cuda.synchronize()
+                if args.sweep_cold_l2:
+                    reps = args.sweep_reps or 100
+                    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                          for _ in range(reps)]
+                    with torch.cuda.stream(stream):
+                        for i in range(reps):
+                            scratch.fill_(i & 0xFF)
+                            ev[i][0].record(stream)
+                            launch()
+                            ev[i][1].record(stream)
+                    torch.cuda.synchronize()
+                    g.check_status(stream)
+                    ms = sum(a.elapsed_time(b) for a, b in ev) / reps
+                    print(json.dumps({
+                        "workload": name, "M": w.M, "N": w.N, "K": w.K, "variant": variant,
+                        "auto_variant": auto, "stream_k": bool(need), "launches": reps,
+                        "l2": "cold (512 MiB written before each launch)",
+                        "ms_per_launch": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
+                        "hbm_gbs_algorithmic": w.min_bytes / (ms * 1e-3) / 1e9}), flush=True)
+                    continue
                 # enough launches for ~0.3 s of work
                 t0 = time.perf_counter()
                 with torch.cuda.stream(stream):
@@ -587,8 +624,36 @@ def run_sweep(args):
                 print(json.dumps({
                     "workload": name, "M": w.M, "N": w.N, "K": w.K, "variant": variant,
                     "auto_variant": auto, "stream_k": bool(need), "launches": reps,
-                    "ms_per_launch": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
+                    "l2": "warm (back-to-back launches)", "ms_per_launch": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
                     "hbm_gbs_algorithmic": w.min_bytes / (ms * 1e-3) / 1e9}), flush=True)
+    return 0
+
+
+def run_sweep_processes(args):
+    """--sweep in several fresh processes; per case, the median of the per-process means."""
+    argv = [a for a in sys.argv[1:]]
+    i = argv.index("--sweep-processes")
+    del argv[i:i + 2]
+    cases = {}
+    for _ in range(args.sweep_processes):
+        out = subprocess.run([sys.executable, os.path.abspath(__file__)] + argv, check=True,
+                             capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if not line.startswith("{"):
+                continue
+            d = json.loads(line)
+            key = (d["workload"], d["variant"], d["stream_k"], d["l2"])
+            cases.setdefault(key, []).append(d)
+    for key, runs in cases.items():
+        d = dict(runs[0])
+        means = [r["ms_per_launch"] for r in runs]
+        ms = statistics.median(means)
+        w_flops = 2.0 * d["M"] * d["N"] * d["K"]
+        w_bytes = 2.0 * (d["M"] * d["K"] + d["N"] * d["K"] + d["M"] * d["N"])
+        d.update({"processes": len(runs), "ms_per_launch": ms, "ms_per_process": means,
+                  "tflops": w_flops / (ms * 1e-3) / 1e12,
+                  "hbm_gbs_algorithmic": w_bytes / (ms * 1e-3) / 1e9})
+        print(json.dumps(d), flush=True)
     return 0
 
 
@@ -596,6 +661,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep and args.sweep_processes > 1:
+        return run_sweep_processes(args)
     if args.sweep:
         return run_sweep(args)
     return run_ours(args)

@@ -99,3 +99,85 @@ def make_bias(N: int, seed: int, scale: float = 1.0, dtype=torch.float16) -> tor
 
 def workload_inputs(w: Workload):
     return make_inputs(w.M, w.N, w.K, w.seed, w.a_dist, w.a_scale, w.b_dist, w.b_scale)
+
+
+# ---- block-scaled FP8 (MX) inputs ----------------------------------------------------------------
+#
+# Elements: i.i.d. normal(0, 1) in float32, clamped to the format's largest finite value and
+# rounded to FP8 (E4M3 or E5M2) by torch's float32 -> float8 conversion.  Scales: one E8M0 code
+# per row and per block of 32 K elements, 127 - s + r with s = round(log2(K) / 4) and r uniform
+# on {-2, ..., 2}, so that sums of K terms stay of order one in fp16 and bf16 whatever K is.
+# Drawn from one torch.Generator in the order A, B, SA, SB.
+
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+FP8_TORCH = {"e4m3": "float8_e4m3fn", "e5m2": "float8_e5m2"}
+
+
+@dataclass(frozen=True)
+class MxWorkload:
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+    fmt_a: str = "e4m3"
+    fmt_b: str = "e4m3"
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def min_bytes(self) -> int:
+        """Bytes that must cross HBM at least once: FP8 A and B, their scales, fp16 D."""
+        return self.M * self.K + self.N * self.K + (self.M + self.N) * (self.K // 32) \
+            + 2 * self.M * self.N
+
+
+MX_WORKLOADS = {
+    w.name: w
+    for w in [
+        MxWorkload("mx_single_tile_128x128x128", 128, 128, 128, 10),
+        MxWorkload("mx_square_2048", 2048, 2048, 2048, 11),
+        # ragged in M and N; K = 8 * 128 + 32 ends in a partial group of four scale blocks
+        MxWorkload("mx_ragged_3000x5000x1056", 3000, 5000, 1056, 12),
+        MxWorkload("mx_square_8192", 8192, 8192, 8192, 13),
+        MxWorkload("mx_mlp_up_16384x14336x4096", 16384, 14336, 4096, 14),
+    ]
+}
+
+MX_ORDER = list(MX_WORKLOADS)
+
+
+def _draw_fp8(gen: torch.Generator, shape, fmt: str) -> torch.Tensor:
+    x = torch.randn(shape, generator=gen, dtype=torch.float32)
+    x = x.clamp_(-FP8_MAX[fmt], FP8_MAX[fmt])
+    return x.to(getattr(torch, FP8_TORCH[fmt])).view(torch.uint8).contiguous()
+
+
+def mx_scale_shift(K: int) -> int:
+    return int(round(math.log2(max(K, 1)) / 4.0))
+
+
+def _draw_scales(gen: torch.Generator, rows: int, K: int) -> torch.Tensor:
+    r = torch.randint(-2, 3, (rows, K // 32), generator=gen, dtype=torch.int32)
+    return (127 - mx_scale_shift(K) + r).to(torch.uint8).contiguous()
+
+
+def make_mx_inputs(M: int, N: int, K: int, seed: int, fmt_a: str = "e4m3",
+                   fmt_b: str = "e4m3"):
+    """(A, B, SA, SB) as contiguous CPU uint8 tensors: FP8 codes of shapes (M, K) and (N, K),
+    E8M0 scale codes of shapes (M, K/32) and (N, K/32), row-major."""
+    if K % 32 != 0:
+        raise ValueError("K must be a multiple of 32 (the scale block)")
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    A = _draw_fp8(gen, (M, K), fmt_a)
+    B = _draw_fp8(gen, (N, K), fmt_b)
+    SA = _draw_scales(gen, M, K)
+    SB = _draw_scales(gen, N, K)
+    return A, B, SA, SB
+
+
+def mx_workload_inputs(w: MxWorkload):
+    return make_mx_inputs(w.M, w.N, w.K, w.seed, w.fmt_a, w.fmt_b)

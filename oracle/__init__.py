@@ -27,16 +27,20 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_ref.c")
+_SRCS = [_SRC, os.path.join(_HERE, "mx_ref.c")]
 _LIB = os.path.join(_HERE, "liboracle_gemm.so")
 _lock = threading.Lock()
 _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile ``gemm_ref.c`` into ``liboracle_gemm.so`` next to it (gcc, OpenMP)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    """Compile ``gemm_ref.c`` and ``mx_ref.c`` into ``liboracle_gemm.so`` next to them (gcc,
+    OpenMP)."""
+    stale = not os.path.exists(_LIB) or any(os.path.getmtime(_LIB) < os.path.getmtime(f)
+                                            for f in _SRCS)
+    if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-Wall", _SRC, "-o", tmp, "-lm"]
+        cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-Wall"] + _SRCS + ["-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -77,6 +81,22 @@ def _load():
             lib.oracle_gemm_f64_sampled_dt.restype = None
             lib.oracle_epilogue_f64.argtypes = [f64p, i64, i64, u16p, ctypes.c_int, ctypes.c_int]
             lib.oracle_epilogue_f64.restype = None
+            u8p = ctypes.c_void_p
+            lib.oracle_fp8_to_f64.argtypes = [ctypes.c_uint8, ctypes.c_int]
+            lib.oracle_fp8_to_f64.restype = ctypes.c_double
+            lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+            lib.oracle_e8m0_to_f64.restype = ctypes.c_double
+            lib.oracle_decode_fp8.argtypes = [u8p, f64p, i64, ctypes.c_int]
+            lib.oracle_decode_fp8.restype = None
+            lib.oracle_decode_e8m0.argtypes = [u8p, f64p, i64]
+            lib.oracle_decode_e8m0.restype = None
+            lib.oracle_gemm_mx_f64.argtypes = [u8p, u8p, u8p, u8p, f64p, f64p, i64, i64, i64,
+                                               ctypes.c_int, ctypes.c_int]
+            lib.oracle_gemm_mx_f64.restype = ctypes.c_int
+            lib.oracle_gemm_mx_f64_sampled.argtypes = [u8p, u8p, u8p, u8p, i64, i64, i64,
+                                                       ctypes.c_int, ctypes.c_int, i64p, i64p,
+                                                       i64, f64p, f64p]
+            lib.oracle_gemm_mx_f64_sampled.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -241,3 +261,97 @@ def tolerance(d_ref: np.ndarray, K: int) -> np.ndarray:
     to spare.
     """
     return 1e-3 * np.sqrt(float(K)) + np.abs(d_ref) * 2.0 ** -10
+
+
+# ---- block-scaled FP8 (MX) ----------------------------------------------------------------------
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+
+
+def _as_u8(x) -> np.ndarray:
+    """8-bit codes (numpy uint8/int8, or a CPU torch uint8/int8/float8 tensor) -> contiguous
+    uint8 view of their bits."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().cpu().contiguous().view(dtype=torch.uint8).numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.int8:
+        x = x.view(np.uint8)
+    if x.dtype != np.uint8:
+        raise TypeError(f"expected 8-bit codes, got {x.dtype}")
+    return x
+
+
+def fp8_bits_to_f64(codes, fmt: str = "e4m3") -> np.ndarray:
+    """FP8 codes -> binary64 values (exact)."""
+    c = _as_u8(codes)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_decode_fp8(c.ctypes.data, out.ctypes.data, c.size, FP8_FORMATS[fmt])
+    return out
+
+
+def e8m0_to_f64(codes) -> np.ndarray:
+    """E8M0 scale codes -> 2^(e - 127) (255: NaN)."""
+    c = _as_u8(codes)
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().oracle_decode_e8m0(c.ctypes.data, out.ctypes.data, c.size)
+    return out
+
+
+def _mx_args(A, B, SA, SB):
+    a, b, sa, sb = _as_u8(A), _as_u8(B), _as_u8(SA), _as_u8(SB)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError(f"shapes {a.shape} and {b.shape} do not contract")
+    M, K = a.shape
+    N = b.shape[0]
+    if K % 32 != 0:
+        raise ValueError("K must be a multiple of the 32-element scale block")
+    if sa.shape != (M, K // 32) or sb.shape != (N, K // 32):
+        raise ValueError(f"scale shapes {sa.shape}, {sb.shape}; want {(M, K // 32)}, "
+                         f"{(N, K // 32)}")
+    return a, b, sa, sb, M, N, K
+
+
+def gemm_mx_f64(A, B, SA, SB, fmt_a: str = "e4m3", fmt_b: str = "e4m3"):
+    """(D, Dabs): D = sum_k (a*sa) * (b*sb) in binary64 and Dabs = sum_k |(a*sa) * (b*sb)|.
+    A: (M, K) FP8 codes, B: (N, K), SA: (M, K/32) E8M0 codes, SB: (N, K/32)."""
+    a, b, sa, sb, M, N, K = _mx_args(A, B, SA, SB)
+    D = np.empty((M, N), dtype=np.float64)
+    Dabs = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_mx_f64(a.ctypes.data, b.ctypes.data, sa.ctypes.data, sb.ctypes.data,
+                                    D.ctypes.data, Dabs.ctypes.data, M, N, K,
+                                    FP8_FORMATS[fmt_a], FP8_FORMATS[fmt_b])
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its binary64 copies")
+    return D, Dabs
+
+
+def gemm_mx_f64_sampled(A, B, SA, SB, rows, cols, fmt_a: str = "e4m3", fmt_b: str = "e4m3"):
+    """(D, Dabs) at the output elements (rows[t], cols[t])."""
+    a, b, sa, sb, M, N, K = _mx_args(A, B, SA, SB)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.shape != c.shape or r.ndim != 1:
+        raise ValueError("rows and cols must be 1-D and of equal length")
+    if r.size and (r.min() < 0 or r.max() >= M or c.min() < 0 or c.max() >= N):
+        raise IndexError("sampled index out of range")
+    out = np.empty(r.size, dtype=np.float64)
+    out_abs = np.empty(r.size, dtype=np.float64)
+    _load().oracle_gemm_mx_f64_sampled(a.ctypes.data, b.ctypes.data, sa.ctypes.data,
+                                       sb.ctypes.data, M, N, K, FP8_FORMATS[fmt_a],
+                                       FP8_FORMATS[fmt_b], r.ctypes.data, c.ctypes.data, r.size,
+                                       out.ctypes.data, out_abs.ctypes.data)
+    return out, out_abs
+
+
+def tolerance_mx(d_ref: np.ndarray, d_abs: np.ndarray, K: int, out_dtype: str = "f16"):
+    """Parity bound for the block-scaled GEMM: rel * |D| + 4 * (K/32 + 1) * 2^-24 * Dabs.
+
+    Every product of two scaled FP8 values is exact in fp32's 24-bit significand (8 significant
+    bits), so the only accumulation error is the rounding of partial sums, one per 32-element
+    block and one per accumulate into the fp32 accumulator: at most (K/32 + 1) roundings of
+    2^-24 relative to the sum of |terms|, with a factor of 4 to spare for the order of the
+    tensor core's internal adds.  rel covers the final rounding as for the 16-bit GEMM: 2^-10
+    for fp16 output and 2^-7 for bfloat16."""
+    rel = 2.0 ** -10 if out_dtype == "f16" else 2.0 ** -7
+    return np.abs(d_ref) * rel + 4.0 * (K / 32.0 + 1.0) * 2.0 ** -24 * np.asarray(d_abs)
