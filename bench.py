@@ -65,6 +65,11 @@ def parse_args():
     p.add_argument("--sweep-processes", type=int, default=1,
                    help="run --sweep in this many fresh processes and report, per case, the "
                         "median of the per-process means")
+    p.add_argument("--mx-steps", type=int, default=200,
+                   help="steps of the block-scaled FP8 leg (8192^3 and MLP shapes; 0: skip)")
+    p.add_argument("--mx-variant", type=int, default=0, help="block-scaled variant (0 = auto)")
+    p.add_argument("--sweep-mx", action="store_true",
+                   help="in --sweep, time the block-scaled FP8 workloads instead")
     p.add_argument("--cublas-steps", type=int, default=-1,
                    help="steps of torch.mm on the same shapes, for context (-1: as many as "
                         "--steps, 0: skip)")
@@ -248,6 +253,85 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ---- block-scaled FP8 leg ---------------------------------------------------------------------
+
+MX_STEP = ("mx_square_8192", "mx_mlp_up_16384x14336x4096")
+FP8_OVER_16BIT = 2.0   # nominal dense rate ratio of the FP8 and 16-bit tensor paths (4.5 / 2.25 PF)
+
+
+def mx_inputs_on_device(g, w, dev):
+    import torch
+    from blackwell_tensor_core_fp16_gb300.workloads import mx_workload_inputs
+    A, B, SA, SB = mx_workload_inputs(w)
+    Ad, Bd = A.to(dev), B.to(dev)
+    sfa = g.pack_scales(SA.to(dev))
+    sfb = g.pack_scales(SB.to(dev))
+    D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    return Ad, Bd, sfa, sfb, D
+
+
+def mx_launch(g, w, t, variant, stream):
+    Ad, Bd, sfa, sfb, D = t
+    rc = g.gemm_mxf8_nt(Ad.data_ptr(), Bd.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
+                        D.data_ptr(), w.M, w.N, w.K, g.FP8_FORMATS[w.fmt_a],
+                        g.FP8_FORMATS[w.fmt_b], g.DTYPES["f16"], 0, 0, variant, 0, 0,
+                        stream.cuda_stream)
+    if rc != g.OK:
+        raise g.GemmError(rc, g.gemm_f16_last_error())
+
+
+def run_mx_leg(args, g, dev, stream, num_sms, peak16, uuid):
+    """The block-scaled FP8 GEMM (E4M3 x E4M3, E8M0 scales per 32 K elements, fp16 out) on the
+    same two shapes, inputs resident, back-to-back launches timed with CUDA events."""
+    import torch
+    from blackwell_tensor_core_fp16_gb300.workloads import MX_WORKLOADS
+    work = []
+    for n in MX_STEP:
+        w = MX_WORKLOADS[n]
+        v = args.mx_variant or g.gemm_mxf8_choose_variant(w.M, w.N, w.K, num_sms)
+        work.append((w, mx_inputs_on_device(g, w, dev), v))
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            for w, t, v in work:
+                mx_launch(g, w, t, v, stream)
+    torch.cuda.synchronize()
+    K = args.mx_steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(work) * K + 1)]
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        e = 1
+        for _ in range(K):
+            for w, t, v in work:
+                mx_launch(g, w, t, v, stream)
+                ev[e].record(stream)
+                e += 1
+    torch.cuda.synchronize()
+    clk = sampler.stop()
+    g.check_status(stream)
+    durs = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
+    total = ev[0].elapsed_time(ev[-1])
+    flops = sum(w.flops for w, _, _ in work)
+    per = {}
+    for j, (w, _, v) in enumerate(work):
+        ms = sum(durs[j::len(work)]) / K
+        per[w.name] = {"M": w.M, "N": w.N, "K": w.K, "variant": v, "ms_per_launch": ms,
+                       "tflops": w.flops / (ms * 1e-3) / 1e12}
+    achieved = K * flops / (sum(durs) * 1e-3) / 1e12
+    peak8 = peak16 * FP8_OVER_16BIT
+    return {"metric": "block-scaled FP8 (MX E4M3, E8M0 per 32) GEMM TFLOP/s, fp16 out",
+            "value": K * flops / (total * 1e-3) / 1e12, "unit": "TFLOP/s", "steps": K,
+            "per_workload": per, "clocks": clk,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak8,
+                         "unit": "TFLOP/s", "frac": achieved / peak8, "traffic": None,
+                         "peak_source": "measured bf16_tflops x 2 (nominal FP8 / 16-bit dense "
+                                        "rate ratio, 4.5 / 2.25 PFLOP/s)"},
+            "gpu_launches": K * len(work)}
 
 
 # ---- our arm ---------------------------------------------------------------------------------
@@ -498,6 +582,10 @@ def run_ours(args):
         copy_roof = flops_step / ((h2d + d2h) / (link_gbs * 1e9)) / 1e12
         del hsrc, hdst, dsrc, ddst
 
+    mx_leg = None
+    if args.mx_steps > 0:
+        mx_leg = run_mx_leg(args, g, dev, stream, num_sms, peak, uuid)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -534,6 +622,7 @@ def run_ours(args):
                         "D -> pinned host (copy stream); two buffer slots, copies of "
                         "neighbouring steps overlap the GEMMs"},
         "gpu_launches": K * len(work),
+        "mx_fp8": mx_leg,
         "clocks": clock_info,
         "wall_s_timed_region": wall_s,
     }
@@ -555,8 +644,10 @@ def run_sweep(args):
     g.load()
     dev = torch.device("cuda", 0)
     stream = torch.cuda.Stream(device=dev)
-    names = [n.strip() for n in args.sweep_workloads.split(",") if n.strip()] or ORDER
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if args.sweep_mx:
+        return run_sweep_mx(args, g, dev, stream, sms)
+    names = [n.strip() for n in args.sweep_workloads.split(",") if n.strip()] or ORDER
     scratch = (torch.empty(512 << 20, dtype=torch.uint8, device=dev) if args.sweep_cold_l2
                else None)
     for name in names:
@@ -626,6 +717,47 @@ def run_sweep(args):
                     "auto_variant": auto, "stream_k": bool(need), "launches": reps,
                     "l2": "warm (back-to-back launches)", "ms_per_launch": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
                     "hbm_gbs_algorithmic": w.min_bytes / (ms * 1e-3) / 1e9}), flush=True)
+    return 0
+
+
+def run_sweep_mx(args, g, dev, stream, sms):
+    """--sweep over the block-scaled FP8 workloads and variants."""
+    import torch
+    from blackwell_tensor_core_fp16_gb300.workloads import MX_ORDER, MX_WORKLOADS
+    names = [n.strip() for n in args.sweep_workloads.split(",") if n.strip()] or MX_ORDER
+    for name in names:
+        w = MX_WORKLOADS[name]
+        t = mx_inputs_on_device(g, w, dev)
+        auto = g.gemm_mxf8_choose_variant(w.M, w.N, w.K, sms)
+        variants = [auto] if args.sweep_variants == "auto" else [1, 2]
+        for v in variants:
+            with torch.cuda.stream(stream):
+                for _ in range(5):
+                    mx_launch(g, w, t, v, stream)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            with torch.cuda.stream(stream):
+                mx_launch(g, w, t, v, stream)
+            torch.cuda.synchronize()
+            reps = args.sweep_reps or max(10, min(5000, int(0.3 / max(time.perf_counter() - t0,
+                                                                       1e-6))))
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(reps):
+                    mx_launch(g, w, t, v, stream)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            g.check_status(stream)
+            ms = e0.elapsed_time(e1) / reps
+            print(json.dumps({
+                "workload": name, "M": w.M, "N": w.N, "K": w.K, "variant": v,
+                "auto_variant": auto, "stream_k": False, "launches": reps,
+                "l2": "warm (back-to-back launches)", "ms_per_launch": ms,
+                "tflops": w.flops / (ms * 1e-3) / 1e12,
+                "hbm_gbs_algorithmic": w.min_bytes / (ms * 1e-3) / 1e9}), flush=True)
+        del t
     return 0
 
 

@@ -118,6 +118,25 @@ def load():
         lib.gemm_f16_sk_item.restype = None
         lib.gemm_f16_sk_unit_of.argtypes = [u32, u32, u32, u32, u32]
         lib.gemm_f16_sk_unit_of.restype = u32
+        lib.gemm_mxf8_nt.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, vp, i32,
+                                     i32, vp, sz, vp]
+        lib.gemm_mxf8_nt.restype = i32
+        lib.gemm_mxf8_workspace_bytes.argtypes = [i64, i64, i64, i32, ctypes.POINTER(sz)]
+        lib.gemm_mxf8_workspace_bytes.restype = i32
+        lib.gemm_mxf8_choose_variant.argtypes = [i64, i64, i64, i32]
+        lib.gemm_mxf8_choose_variant.restype = i32
+        lib.gemm_mxf8_scale_bytes.argtypes = [i64, i64]
+        lib.gemm_mxf8_scale_bytes.restype = i64
+        lib.gemm_mxf8_pack_scales.argtypes = [vp, vp, i64, i64, vp]
+        lib.gemm_mxf8_pack_scales.restype = i32
+        lib.gemm_mxf8_idesc.argtypes = [u32, u32, u32, u32]
+        lib.gemm_mxf8_idesc.restype = u32
+        lib.gemm_mxf8_sf_offset.argtypes = [i64, i64, i64]
+        lib.gemm_mxf8_sf_offset.restype = i64
+        lib.gemm_mxf8_sf_desc.argtypes = [u32]
+        lib.gemm_mxf8_sf_desc.restype = ctypes.c_uint64
+        lib.gemm_mxf8_get_variant_info.argtypes = [i32, ctypes.POINTER(VariantInfo)]
+        lib.gemm_mxf8_get_variant_info.restype = i32
         _lib = lib
         return lib
 
@@ -278,7 +297,136 @@ def exported_symbols(header_path: str | None = None):
     path = header_path or os.path.join(_build.ROOT, "include", "gemm_f16.h")
     text = open(path).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_f16_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(gemm_(?:f16|mxf8)_\w+)\s*\(", text)))
+
+
+# ---- block-scaled FP8 (MX) ---------------------------------------------------------------------
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+MX_VARIANTS = {"auto": 0, "mx_128x128": 1, "mx_pair_256x128": 2}
+
+
+def gemm_mxf8_nt(A: int, B: int, SFA: int, SFB: int, D: int, M: int, N: int, K: int,
+                 fmt_a: int, fmt_b: int, out_dtype: int, bias: int, activation: int,
+                 variant: int, workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    return load().gemm_mxf8_nt(A, B, SFA, SFB, D, M, N, K, fmt_a, fmt_b, out_dtype, bias,
+                               activation, variant, workspace, workspace_bytes, stream)
+
+
+def gemm_mxf8_workspace_bytes(M: int, N: int, K: int, variant: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    rc = load().gemm_mxf8_workspace_bytes(M, N, K, variant, ctypes.byref(out))
+    if rc != OK:
+        raise GemmError(rc, gemm_f16_last_error())
+    return out.value
+
+
+def gemm_mxf8_choose_variant(M: int, N: int, K: int, num_sms: int) -> int:
+    return load().gemm_mxf8_choose_variant(M, N, K, num_sms)
+
+
+def gemm_mxf8_scale_bytes(rows: int, K: int) -> int:
+    return load().gemm_mxf8_scale_bytes(rows, K)
+
+
+def gemm_mxf8_pack_scales(src: int, dst: int, rows: int, K: int, stream: int = 0) -> int:
+    return load().gemm_mxf8_pack_scales(src, dst, rows, K, stream)
+
+
+def gemm_mxf8_idesc(M: int, N: int, fmt_a: int = 0, fmt_b: int = 0) -> int:
+    return load().gemm_mxf8_idesc(M, N, fmt_a, fmt_b)
+
+
+def gemm_mxf8_sf_offset(row: int, k_block: int, K: int) -> int:
+    return load().gemm_mxf8_sf_offset(row, k_block, K)
+
+
+def gemm_mxf8_sf_desc(smem_addr: int) -> int:
+    return load().gemm_mxf8_sf_desc(smem_addr)
+
+
+def gemm_mxf8_get_variant_info(variant: int) -> dict:
+    info = VariantInfo()
+    rc = load().gemm_mxf8_get_variant_info(variant, ctypes.byref(info))
+    if rc != OK:
+        raise GemmError(rc, f"unknown block-scaled variant {variant}")
+    return info.as_dict()
+
+
+def pack_scales(S, K: int | None = None, stream=None):
+    """Row-major block scales (a contiguous CUDA uint8 tensor of rows x K/32 E8M0 codes) -> a new
+    CUDA uint8 tensor in the tiled layout the block-scaled GEMM reads."""
+    import torch
+    if S.dtype != torch.uint8 or not S.is_cuda or S.dim() != 2 or not S.is_contiguous():
+        raise ValueError("S must be a contiguous 2-D CUDA uint8 tensor")
+    rows, kb = S.shape
+    K = 32 * kb if K is None else K
+    if K != 32 * kb:
+        raise ValueError("S must have K/32 columns")
+    out = torch.empty(max(gemm_mxf8_scale_bytes(rows, K), 0), dtype=torch.uint8,
+                      device=S.device)
+    rc = gemm_mxf8_pack_scales(S.data_ptr(), out.data_ptr(), rows, K, _stream_handle(stream))
+    if rc != OK:
+        raise GemmError(rc, gemm_f16_last_error())
+    return out
+
+
+def _u8(t, name):
+    import torch
+    if t.dtype in (getattr(torch, "float8_e4m3fn", None), getattr(torch, "float8_e5m2", None)):
+        t = t.view(torch.uint8)
+    if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA uint8 (or float8) tensor")
+    return t
+
+
+def gemm_mx(A, B, SFA, SFB, out=None, fmt_a: str = "e4m3", fmt_b: str = "e4m3",
+            out_dtype: str = "f16", bias=None, activation: str = "none",
+            variant: int | str = 0, stream=None, workspace=True):
+    """Block-scaled FP8 GEMM: D = act((A * 2^(SA-127)) @ (B * 2^(SB-127)).T + bias).
+
+    A (M, K) and B (N, K): FP8 codes (uint8 or float8 CUDA tensors); SFA, SFB: their E8M0 scales
+    in the tiled layout (``pack_scales`` of the row-major (rows, K/32) codes).  Returns D (M, N)
+    in float16 or bfloat16.  Asynchronous on ``stream``; raises GemmError on a non-zero status.
+    """
+    import torch
+    if isinstance(variant, str):
+        variant = MX_VARIANTS[variant]
+    A, B = _u8(A, "A"), _u8(B, "B")
+    SFA, SFB = _u8(SFA, "SFA"), _u8(SFB, "SFB")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError(f"A is {tuple(A.shape)} and B is {tuple(B.shape)}: K differs")
+    M, K = A.shape
+    N = B.shape[0]
+    for name, t, rows in (("SFA", SFA, M), ("SFB", SFB, N)):
+        need = gemm_mxf8_scale_bytes(rows, K)
+        if need < 0 or t.numel() < need:
+            raise ValueError(f"{name} must hold {need} bytes of tiled scales")
+    tdt = torch.float16 if out_dtype == "f16" else torch.bfloat16
+    if out is None:
+        out = torch.empty((M, N), dtype=tdt, device=A.device)
+    elif out.dtype != tdt or not out.is_cuda or tuple(out.shape) != (M, N) or \
+            not out.is_contiguous():
+        raise ValueError("out must be a contiguous (M, N) CUDA tensor of the output dtype")
+    if bias is not None and (bias.dtype != tdt or bias.numel() != N or not bias.is_cuda
+                             or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous CUDA vector of N elements of the output dtype")
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is True and M and N and K:
+        need = gemm_mxf8_workspace_bytes(M, N, K, int(variant))
+        if need:
+            s = stream if stream is not None else torch.cuda.current_stream()
+            with torch.cuda.stream(s) if hasattr(s, "cuda_stream") else _nullctx():
+                workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
+    if workspace is not None and workspace is not True and workspace is not False:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    rc = gemm_mxf8_nt(A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(), out.data_ptr(),
+                      M, N, K, FP8_FORMATS[fmt_a], FP8_FORMATS[fmt_b], DTYPES[out_dtype],
+                      0 if bias is None else bias.data_ptr(), ACTIVATIONS[activation],
+                      int(variant), ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != OK:
+        raise GemmError(rc, gemm_f16_last_error())
+    return out
 
 
 # ---- torch convenience ----------------------------------------------------------------------

@@ -32,6 +32,60 @@ GF16_HD uint32_t make_idesc_f16(uint32_t M, uint32_t N, uint32_t ab_bf16)
 }
 
 // ---------------------------------------------------------------------------------------------
+// Instruction descriptor of tcgen05.mma .kind::mxf8f6f4 with block scaling (E8M0 scales, one per
+// 32 K elements), a 32-bit word:
+//   bits  5:4   B scale-factor ID: the byte of each 32-bit scale column this MMA reads
+//   bits  9:7   A format                 (0 = E4M3, 1 = E5M2)
+//   bits 12:10  B format
+//   bit  15/16  A / B major              (0 = K-major)
+//   bits 22:17  N >> 3
+//   bit  23     scale format             (1 = E8M0)
+//   bits 28:24  M >> 4
+//   bits 30:29  A scale-factor ID
+// The IDs are left 0 here; the MMA issuer ORs in the K block (0-3) of each MMA.
+// ---------------------------------------------------------------------------------------------
+GF16_HD uint32_t make_idesc_mx(uint32_t M, uint32_t N, uint32_t fmt_a, uint32_t fmt_b)
+{
+    return ((fmt_a & 7u) << 7) | ((fmt_b & 7u) << 10) | (((N >> 3) & 0x3Fu) << 17) | (1u << 23) |
+           (((M >> 4) & 0x1Fu) << 24);
+}
+
+GF16_HD uint32_t idesc_mx_with_sf_id(uint32_t idesc, uint32_t k_block)
+{
+    return idesc | ((k_block & 3u) << 4) | ((k_block & 3u) << 29);
+}
+
+// ---------------------------------------------------------------------------------------------
+// The tiled layout of block scales (one E8M0 byte per row and per 32-element K block) that the
+// kernels read.  Rows are grouped by 128 and K blocks by 4; each (row group, K-block group)
+// pair is one contiguous 512-byte chunk, chunks ordered row-group-major.  Inside a chunk,
+// row r = 32 q + l (l < 32, q < 4) and K block b (b < 4) sit at byte 16 l + 4 q + b: the 16
+// bytes at 16 l are the 128-bit row l of a 32 x 128-bit block that tcgen05.cp .32x128b.warpx4
+// copies into lane l of every 32-lane window of tensor memory, so tensor-memory column q holds
+// rows 32 q .. 32 q + 31 and its byte b holds K block b.
+// ---------------------------------------------------------------------------------------------
+GF16_HD uint32_t mx_k_groups(uint32_t k_blocks) { return (k_blocks + 3u) / 4u; }
+
+GF16_HD uint64_t mx_sf_offset(uint64_t row, uint32_t k_block, uint32_t k_groups)
+{
+    return ((row / 128u) * k_groups + k_block / 4u) * 512u + (row % 32u) * 16u +
+           ((row % 128u) / 32u) * 4u + (k_block % 4u);
+}
+
+// Shared-memory descriptor of one 512-byte scale chunk as the source of tcgen05.cp .32x128b:
+// 32 rows of 16 bytes, no swizzle, 8-row core matrices 128 bytes apart (both offset fields
+// carry that stride; the copy is one core matrix wide).
+GF16_HD uint64_t make_sf_desc(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(128u >> 4) << 16;
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
+// ---------------------------------------------------------------------------------------------
 // Shared-memory matrix descriptor (64-bit) for a K-major operand tile stored with the 128-byte
 // swizzle: rows of 64 fp16 (128 bytes), grouped in atoms of 8 rows = 1024 bytes.
 //   bits 13:0   start address >> 4

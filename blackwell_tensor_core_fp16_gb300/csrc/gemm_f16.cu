@@ -147,11 +147,17 @@ int choose_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
 }
 
 // ---- per-device state ------------------------------------------------------------------------
+// Kernel slots (one per compiled kernel instance) for the per-device caches below:
+// 16-bit path: variant + (bf16 ? GEMM_F16_NUM_VARIANTS : 0); block-scaled path: kMxSlot0 +
+// 2 * variant + (bf16 output ? 1 : 0).
+constexpr int kMxSlot0 = 32;
+constexpr int kNumSlots = 64;
+
 struct DeviceState {
     bool ready = false;
     int sms = 0;
-    bool smem_set[2 * GEMM_F16_NUM_VARIANTS] = {};  // per variant, fp16 then bf16
-    int pair_clusters[GEMM_F16_NUM_VARIANTS] = {};  // co-resident CTA pairs per variant
+    bool smem_set[kNumSlots] = {};    // max dynamic shared memory raised, per kernel slot
+    int pair_clusters[kNumSlots] = {};  // co-resident CTA pairs, per kernel slot
 };
 
 std::mutex g_mu;
@@ -182,14 +188,14 @@ int device_state(DeviceState** out)
 }
 
 template <typename Kernel>
-int ensure_smem(DeviceState& d, int variant, Kernel kernel, uint32_t bytes)
+int ensure_smem(DeviceState& d, int slot, Kernel kernel, uint32_t bytes)
 {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (d.smem_set[variant]) return GEMM_F16_OK;
+    if (d.smem_set[slot]) return GEMM_F16_OK;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(bytes));
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-    d.smem_set[variant] = true;
+    d.smem_set[slot] = true;
     return GEMM_F16_OK;
 }
 
@@ -208,24 +214,49 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// A row-major fp16 matrix of `rows` x `cols` (cols contiguous) read or written in boxes of
-// box_rows x box_cols elements with the 128-byte swizzle (box_cols * 2 == 128 bytes).
+// A row-major matrix of `rows` x `cols` (cols contiguous) of 16-bit elements (fp16, or bf16),
+// or of 8-bit codes (fp8: FP8 operands of the block-scaled path), read or written in boxes of
+// box_rows x box_cols elements with the 128-byte swizzle (box_cols * element size == 128 bytes).
 int make_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
-             uint32_t box_cols, bool bf16 = false)
+             uint32_t box_cols, bool bf16 = false, bool fp8 = false)
 {
     auto fn = encode_fn();
     if (!fn) return fail(GEMM_F16_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint64_t strides[1] = {cols * (fp8 ? 1 : 2)};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                    2, const_cast<void*>(ptr), dims, strides,
+    const CUtensorMapDataType dt = fp8    ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(GEMM_F16_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for %llux%llu",
                     (int)r, (unsigned long long)rows, (unsigned long long)cols);
+    return GEMM_F16_OK;
+}
+
+// Block scales in the tiled layout (mx_sf_offset) of a `rows` x K operand, viewed as a 3-D
+// tensor of 32-bit words {128 words = one 512-byte chunk, K-block groups, 128-row groups}; a box
+// is `chunks` consecutive row groups of one K-block group.  Row groups past the end read as zero.
+int make_sf_map(CUtensorMap* map, const void* ptr, uint64_t rows, uint64_t K, uint32_t chunks)
+{
+    auto fn = encode_fn();
+    if (!fn) return fail(GEMM_F16_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const uint64_t kgroups = gf16::mx_k_groups(static_cast<uint32_t>(K / 32));
+    const cuuint64_t dims[3] = {128, kgroups, (rows + 127) / 128};
+    const cuuint64_t strides[2] = {512, kgroups * 512};
+    const cuuint32_t box[3] = {128, 1, chunks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(GEMM_F16_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for the "
+                    "scales of %llu rows, K=%llu", (int)r, (unsigned long long)rows,
+                    (unsigned long long)K);
     return GEMM_F16_OK;
 }
 
@@ -237,17 +268,20 @@ struct MapKey {
     int64_t M, N, K;
     int variant;
     int device;
-    int dtype = 0;
+    int dtype = 0;           // GEMM_F16_DTYPE_* of the 16-bit operands / output
+    const void* sfa = nullptr;  // block-scaled path: scale buffers (else null)
+    const void* sfb = nullptr;
     bool operator==(const MapKey& o) const
     {
         return a == o.a && b == o.b && d == o.d && M == o.M && N == o.N && K == o.K &&
-               variant == o.variant && device == o.device && dtype == o.dtype;
+               variant == o.variant && device == o.device && dtype == o.dtype && sfa == o.sfa &&
+               sfb == o.sfb;
     }
 };
 
 struct MapEntry {
     MapKey key;
-    CUtensorMap ma, mb, md;
+    CUtensorMap ma, mb, md, msfa, msfb;
     bool valid;
 };
 
@@ -255,14 +289,14 @@ constexpr int kCacheSize = 8;
 thread_local MapEntry t_cache[kCacheSize];
 thread_local int t_cache_next = 0;
 
+// Descriptors of one launch.  mx: FP8 operands (8-bit codes, 128-element boxes) plus the two
+// scale maps, B's boxes holding sfb_chunks row groups.
 int get_maps(const MapKey& k, uint32_t a_box_rows, uint32_t b_box_rows, bool need_d,
-             const CUtensorMap** ma, const CUtensorMap** mb, const CUtensorMap** md)
+             const MapEntry** out, bool mx = false, uint32_t sfb_chunks = 0)
 {
     for (auto& e : t_cache) {
         if (e.valid && e.key == k) {
-            *ma = &e.ma;
-            *mb = &e.mb;
-            *md = &e.md;
+            *out = &e;
             return GEMM_F16_OK;
         }
     }
@@ -271,18 +305,26 @@ int get_maps(const MapKey& k, uint32_t a_box_rows, uint32_t b_box_rows, bool nee
     e.valid = false;
     int rc;
     const bool bf = k.dtype == GEMM_F16_DTYPE_BF16;
-    if ((rc = make_map(&e.ma, k.a, k.M, k.K, a_box_rows, 64, bf)) != GEMM_F16_OK) return rc;
-    if ((rc = make_map(&e.mb, k.b, k.N, k.K, b_box_rows, 64, bf)) != GEMM_F16_OK) return rc;
+    const uint32_t box_k = mx ? 128 : 64;
+    if ((rc = make_map(&e.ma, k.a, k.M, k.K, a_box_rows, box_k, !mx && bf, mx)) != GEMM_F16_OK)
+        return rc;
+    if ((rc = make_map(&e.mb, k.b, k.N, k.K, b_box_rows, box_k, !mx && bf, mx)) != GEMM_F16_OK)
+        return rc;
     if (need_d) {
         if ((rc = make_map(&e.md, k.d, k.M, k.N, 128, 64, bf)) != GEMM_F16_OK) return rc;
     } else {
         std::memset(&e.md, 0, sizeof(e.md));
     }
+    if (mx) {
+        if ((rc = make_sf_map(&e.msfa, k.sfa, k.M, k.K, 1)) != GEMM_F16_OK) return rc;
+        if ((rc = make_sf_map(&e.msfb, k.sfb, k.N, k.K, sfb_chunks)) != GEMM_F16_OK) return rc;
+    } else {
+        std::memset(&e.msfa, 0, sizeof(e.msfa));
+        std::memset(&e.msfb, 0, sizeof(e.msfb));
+    }
     e.key = k;
     e.valid = true;
-    *ma = &e.ma;
-    *mb = &e.mb;
-    *md = &e.md;
+    *out = &e;
     return GEMM_F16_OK;
 }
 
@@ -293,13 +335,13 @@ int launch_tile(const void* A, const void* B, void* D, int64_t M, int64_t N, int
     using C = gf16::TileCfg;
     int rc = ensure_smem(d, GEMM_F16_VARIANT_TILE, gf16::gemm_tile_kernel, C::SMEM_ALLOC);
     if (rc != GEMM_F16_OK) return rc;
-    const CUtensorMap *ma, *mb, *md;
+    const MapEntry* maps = nullptr;
     MapKey key{A, B, D, M, N, K, GEMM_F16_VARIANT_TILE, dev};
-    if ((rc = get_maps(key, 128, 128, false, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
+    if ((rc = get_maps(key, 128, 128, false, &maps)) != GEMM_F16_OK) return rc;
     const dim3 grid(static_cast<uint32_t>(cdiv(N, 128)), static_cast<uint32_t>(cdiv(M, 128)));
     if (grid.y > 65535u) return fail(GEMM_F16_ERR_UNSUPPORTED, "M too large for the tile variant");
     gf16::gemm_tile_kernel<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(
-        *ma, *mb, static_cast<uint16_t*>(D), (uint32_t)M, (uint32_t)N, (uint32_t)cdiv(K, 64),
+        maps->ma, maps->mb, static_cast<uint16_t*>(D), (uint32_t)M, (uint32_t)N, (uint32_t)cdiv(K, 64),
         wait_timeout_ns(), debug_flags());
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch of gemm_tile_kernel");
@@ -344,15 +386,26 @@ struct EpiOpts {
     int act = GEMM_F16_ACT_NONE;
 };
 
-template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore, bool kBf16 = false>
+// Block-scaled operands of a launch: the two tiled scale buffers and the element formats.
+struct MxOpts {
+    const void* sfa = nullptr;
+    const void* sfb = nullptr;
+    int fmt_a = GEMM_MXF8_E4M3;
+    int fmt_b = GEMM_MXF8_E4M3;
+};
+
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore, bool kBf16 = false,
+          bool kMx = false>
 int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
               cudaStream_t stream, DeviceState& d, int dev, void* workspace = nullptr,
               size_t workspace_bytes = 0, size_t* bytes_needed = nullptr,
-              const EpiOpts& epi = EpiOpts{})
+              const EpiOpts& epi = EpiOpts{}, const MxOpts& mx = MxOpts{})
 {
-    using C = gf16::WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
-    auto kernel = gf16::gemm_ws_kernel<kCtaGroup, kBlockN, kStages, kTmaStore, kBf16>;
-    int rc = ensure_smem(d, variant + (kBf16 ? GEMM_F16_NUM_VARIANTS : 0), kernel, C::SMEM_ALLOC);
+    using C = gf16::WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore, kMx>;
+    auto kernel = gf16::gemm_ws_kernel<kCtaGroup, kBlockN, kStages, kTmaStore, kBf16, kMx>;
+    const int slot = kMx ? kMxSlot0 + 2 * variant + (kBf16 ? 1 : 0)
+                         : variant + (kBf16 ? GEMM_F16_NUM_VARIANTS : 0);
+    int rc = ensure_smem(d, slot, kernel, C::SMEM_ALLOC);
     if (rc != GEMM_F16_OK) return rc;
 
     const int64_t num_m = cdiv(M, C::MMA_M);
@@ -375,21 +428,21 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
         cfg.numAttrs = 1;
         {
             std::lock_guard<std::mutex> lk(g_mu);
-            if (d.pair_clusters[variant] == 0) {
+            if (d.pair_clusters[slot] == 0) {
                 cfg.gridDim = dim3(2 * (d.sms / 2));
                 int n = 0;
                 cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
                 if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
                 if (n < 1) return fail(GEMM_F16_ERR_CUDA, "no CTA pair fits on this device");
-                d.pair_clusters[variant] = n;
+                d.pair_clusters[slot] = n;
             }
-            units = d.pair_clusters[variant];
+            units = d.pair_clusters[slot];
         }
     } else {
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
     }
-    const int64_t KB = cdiv(K, 64);
+    const int64_t KB = cdiv(K, C::BLOCK_K);
     // Stream-K tail: all units take part; otherwise no more units than tiles.
     int64_t R = sk_tail_tiles(tiles, units, KB);
     const size_t need = R ? ws_bytes_for(units, kCtaGroup, kBlockN) : 0;
@@ -397,9 +450,15 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
         *bytes_needed = need;
         return GEMM_F16_OK;
     }
-    const CUtensorMap *ma, *mb, *md;
-    MapKey key{A, B, D, M, N, K, variant, dev, kBf16 ? GEMM_F16_DTYPE_BF16 : GEMM_F16_DTYPE_F16};
-    if ((rc = get_maps(key, 128, C::B_ROWS, kTmaStore, &ma, &mb, &md)) != GEMM_F16_OK) return rc;
+    const MapEntry* maps = nullptr;
+    MapKey key{A, B, D, M, N, K, kMx ? -1 - variant : variant, dev,
+               kBf16 ? GEMM_F16_DTYPE_BF16 : GEMM_F16_DTYPE_F16, mx.sfa, mx.sfb};
+    if ((rc = get_maps(key, 128, C::B_ROWS, kTmaStore, &maps, kMx, C::SFB_CHUNKS)) != GEMM_F16_OK)
+        return rc;
+    const uint32_t mx_idesc =
+        kMx ? gf16::make_idesc_mx(C::MMA_M, C::BN, static_cast<uint32_t>(mx.fmt_a),
+                                  static_cast<uint32_t>(mx.fmt_b))
+            : 0u;
     if (R && (workspace == nullptr || workspace_bytes < need ||
               (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         R = 0;  // no usable workspace: plain data-parallel schedule
@@ -418,14 +477,16 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
                                         stream);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(stream-K counters)");
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, *ma, *mb, *md, static_cast<uint16_t*>(D),
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, maps->ma, maps->mb, maps->md,
+                                       static_cast<uint16_t*>(D),
                                        (uint32_t)M, (uint32_t)N,
                                        (uint32_t)num_m, (uint32_t)num_n, (uint32_t)KB,
                                        group_m_setting(), wait_timeout_ns(), l2_hint_setting(),
                                        ws_part, ws_count, (uint32_t)R,
                                        (uint32_t)(R ? sk_units_for(R, units_used) : units_used),
                                        static_cast<const uint16_t*>(epi.bias),
-                                       static_cast<uint32_t>(epi.act), debug_flags());
+                                       static_cast<uint32_t>(epi.act), debug_flags(),
+                                       maps->msfa, maps->msfb, mx_idesc);
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_ws_kernel)");
     return GEMM_F16_OK;
 }
@@ -557,6 +618,98 @@ int noalloc_scratch(void** out)
     }
     *out = g_noalloc_ptr[dev];
     return GEMM_F16_OK;
+}
+
+// ---- block-scaled FP8 (MX) ---------------------------------------------------------------------
+// 128x128 tiles on one CTA (5-stage ring) and 256x128 tiles on a CTA pair (7 stages).  Both keep
+// two 128-column accumulators, so the scale-factor ring fits beside them in tensor memory.
+using MxCta = gf16::WsCfg<1, 128, 5, true, true>;
+using MxPair = gf16::WsCfg<2, 128, 7, true, true>;
+
+int choose_mx_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
+{
+    if (num_sms < 2) num_sms = 2;
+    const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 128);
+    if (M > 128 && pair_tiles >= num_sms / 2) return GEMM_MXF8_VARIANT_PAIR_256x128;
+    return GEMM_MXF8_VARIANT_128x128;
+}
+
+int64_t mx_scale_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 0 || K < 0 || K % 32 != 0) return -1;
+    return cdiv(rows, 128) * static_cast<int64_t>(gf16::mx_k_groups(static_cast<uint32_t>(K / 32))) *
+           512;
+}
+
+int check_mx_args(const void* A, const void* B, const void* SFA, const void* SFB, void* D,
+                  int64_t M, int64_t N, int64_t K, int fmt_a, int fmt_b, const EpiOpts& epi)
+{
+    int rc = check_args(A, B, D, M, N, K);
+    if (rc != GEMM_F16_OK) return rc;
+    if (fmt_a < GEMM_MXF8_E4M3 || fmt_a > GEMM_MXF8_E5M2 || fmt_b < GEMM_MXF8_E4M3 ||
+        fmt_b > GEMM_MXF8_E5M2)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "unknown FP8 format (A %d, B %d)", fmt_a, fmt_b);
+    if (epi.dtype != GEMM_F16_DTYPE_F16 && epi.dtype != GEMM_F16_DTYPE_BF16)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "unknown output dtype %d", epi.dtype);
+    if (epi.act < GEMM_F16_ACT_NONE || epi.act > GEMM_F16_ACT_GELU)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "unknown activation %d", epi.act);
+    if (M == 0 || N == 0) return GEMM_F16_OK;
+    if (K % 32 != 0)
+        return fail(GEMM_F16_ERR_UNSUPPORTED, "K=%lld is not a multiple of the 32-element scale "
+                    "block", (long long)K);
+    auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (K > 0 && (SFA == nullptr || SFB == nullptr))
+        return fail(GEMM_F16_ERR_INVALID_ARG, "SFA or SFB is null");
+    if (K > 0 && (misaligned(SFA) || misaligned(SFB)))
+        return fail(GEMM_F16_ERR_UNSUPPORTED, "SFA and SFB must be 16-byte aligned");
+    if (epi.bias != nullptr && misaligned(epi.bias))
+        return fail(GEMM_F16_ERR_UNSUPPORTED, "bias must be 16-byte aligned");
+    return GEMM_F16_OK;
+}
+
+int run_mx(const void* A, const void* B, const void* SFA, const void* SFB, void* D, int64_t M,
+           int64_t N, int64_t K, int fmt_a, int fmt_b, const EpiOpts& epi, int variant, void* ws,
+           size_t ws_bytes, size_t* bytes_needed, cudaStream_t stream)
+{
+    t_last_error.clear();
+    if (bytes_needed) *bytes_needed = 0;
+    if (variant < 0 || variant >= GEMM_MXF8_NUM_VARIANTS)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "unknown block-scaled variant %d", variant);
+    if (M < 0 || N < 0 || K < 0) return fail(GEMM_F16_ERR_INVALID_ARG, "negative size");
+    int rc = bytes_needed ? GEMM_F16_OK
+                          : check_mx_args(A, B, SFA, SFB, D, M, N, K, fmt_a, fmt_b, epi);
+    if (rc != GEMM_F16_OK) return rc;
+    if (M == 0 || N == 0) return GEMM_F16_OK;
+    if (K == 0) {
+        if (bytes_needed) return GEMM_F16_OK;
+        if (epi.bias != nullptr || epi.act != GEMM_F16_ACT_NONE)
+            return fail(GEMM_F16_ERR_UNSUPPORTED, "K == 0 with a fused epilogue is not supported");
+        cudaError_t e = cudaMemsetAsync(D, 0, static_cast<size_t>(M) * N * 2, stream);
+        return e == cudaSuccess ? GEMM_F16_OK : cuda_fail(e, "cudaMemsetAsync");
+    }
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != GEMM_F16_OK) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (variant == GEMM_MXF8_VARIANT_AUTO) variant = choose_mx_variant(M, N, K, d->sms);
+    const MxOpts mx{SFA, SFB, fmt_a, fmt_b};
+    const bool bf = epi.dtype == GEMM_F16_DTYPE_BF16;
+    switch (variant) {
+    case GEMM_MXF8_VARIANT_128x128:
+        return bf ? launch_ws<1, 128, 5, true, true, true>(variant, A, B, D, M, N, K, stream, *d,
+                                                           dev, ws, ws_bytes, bytes_needed, epi, mx)
+                  : launch_ws<1, 128, 5, true, false, true>(variant, A, B, D, M, N, K, stream, *d,
+                                                            dev, ws, ws_bytes, bytes_needed, epi,
+                                                            mx);
+    case GEMM_MXF8_VARIANT_PAIR_256x128:
+        return bf ? launch_ws<2, 128, 7, true, true, true>(variant, A, B, D, M, N, K, stream, *d,
+                                                           dev, ws, ws_bytes, bytes_needed, epi, mx)
+                  : launch_ws<2, 128, 7, true, false, true>(variant, A, B, D, M, N, K, stream, *d,
+                                                            dev, ws, ws_bytes, bytes_needed, epi,
+                                                            mx);
+    default:
+        return fail(GEMM_F16_ERR_INVALID_ARG, "unknown block-scaled variant %d", variant);
+    }
 }
 
 }  // namespace
@@ -728,6 +881,93 @@ uint32_t gemm_f16_sk_unit_of(uint32_t tiles, uint32_t units, uint32_t k_blocks, 
                              uint32_t x)
 {
     return gf16::sk_unit_of(host_split(tiles, units, k_blocks, tail), x);
+}
+
+int gemm_mxf8_nt(const void* A, const void* B, const void* SFA, const void* SFB, void* D,
+                 int64_t M, int64_t N, int64_t K, int fmt_a, int fmt_b, int out_dtype,
+                 const void* bias, int activation, int variant, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream)
+{
+    EpiOpts epi;
+    epi.dtype = out_dtype;
+    epi.bias = bias;
+    epi.act = activation;
+    return run_mx(A, B, SFA, SFB, D, M, N, K, fmt_a, fmt_b, epi, variant, workspace,
+                  workspace_bytes, nullptr, stream);
+}
+
+int gemm_mxf8_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, size_t* bytes)
+{
+    if (!bytes) return fail(GEMM_F16_ERR_INVALID_ARG, "bytes is null");
+    if (K % 32 != 0) return fail(GEMM_F16_ERR_UNSUPPORTED, "K is not a multiple of 32");
+    return run_mx(nullptr, nullptr, nullptr, nullptr, nullptr, M, N, K, GEMM_MXF8_E4M3,
+                  GEMM_MXF8_E4M3, EpiOpts{}, variant, nullptr, 0, bytes, nullptr);
+}
+
+int gemm_mxf8_choose_variant(int64_t M, int64_t N, int64_t K, int num_sms)
+{
+    return choose_mx_variant(M, N, K, num_sms);
+}
+
+int64_t gemm_mxf8_scale_bytes(int64_t rows, int64_t K) { return mx_scale_bytes(rows, K); }
+
+int gemm_mxf8_pack_scales(const void* src, void* dst, int64_t rows, int64_t K,
+                          cudaStream_t stream)
+{
+    t_last_error.clear();
+    const int64_t total = mx_scale_bytes(rows, K);
+    if (total < 0)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "rows=%lld, K=%lld: need rows >= 0 and K a "
+                    "non-negative multiple of 32", (long long)rows, (long long)K);
+    if (rows > 0x7FFFFFFFll || K > 0x7FFFFFFFll)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "size above 2^31-1");
+    if (total == 0) return GEMM_F16_OK;
+    if (src == nullptr || dst == nullptr) return fail(GEMM_F16_ERR_INVALID_ARG, "null pointer");
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != GEMM_F16_OK) return rc;
+    const int64_t blocks_needed = cdiv(total, 256);
+    const int64_t cap = static_cast<int64_t>(d->sms) * 8;
+    const uint32_t grid = static_cast<uint32_t>(blocks_needed < cap ? blocks_needed : cap);
+    const uint32_t kb = static_cast<uint32_t>(K / 32);
+    gf16::mx_pack_scales_kernel<<<grid, 256, 0, stream>>>(
+        static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), static_cast<uint64_t>(rows),
+        kb, gf16::mx_k_groups(kb), static_cast<uint64_t>(total));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch of mx_pack_scales_kernel");
+    return GEMM_F16_OK;
+}
+
+uint32_t gemm_mxf8_idesc(uint32_t M, uint32_t N, uint32_t fmt_a, uint32_t fmt_b)
+{
+    return gf16::make_idesc_mx(M, N, fmt_a, fmt_b);
+}
+
+int64_t gemm_mxf8_sf_offset(int64_t row, int64_t k_block, int64_t K)
+{
+    if (row < 0 || k_block < 0 || K < 0 || K % 32 != 0 || k_block >= K / 32) return -1;
+    return static_cast<int64_t>(gf16::mx_sf_offset(static_cast<uint64_t>(row),
+                                                   static_cast<uint32_t>(k_block),
+                                                   gf16::mx_k_groups(static_cast<uint32_t>(K / 32))));
+}
+
+uint64_t gemm_mxf8_sf_desc(uint32_t smem_addr) { return gf16::make_sf_desc(smem_addr); }
+
+int gemm_mxf8_get_variant_info(int variant, gemm_f16_variant_info* o)
+{
+    if (!o) return GEMM_F16_ERR_INVALID_ARG;
+    switch (variant) {
+    case GEMM_MXF8_VARIANT_128x128:
+        *o = {1, 128, 128, 128, 5, (int)MxCta::THREADS, (int)MxCta::SMEM_ALLOC,
+              (int)MxCta::TMEM_COLS, (int)MxCta::STAGE_TX, 1};
+        return GEMM_F16_OK;
+    case GEMM_MXF8_VARIANT_PAIR_256x128:
+        *o = {2, 256, 128, 128, 7, (int)MxPair::THREADS, (int)MxPair::SMEM_ALLOC,
+              (int)MxPair::TMEM_COLS, (int)MxPair::STAGE_TX, 1};
+        return GEMM_F16_OK;
+    default:
+        return GEMM_F16_ERR_INVALID_ARG;
+    }
 }
 
 void gemm_f16_ring_pos(uint32_t it, uint32_t stages, uint32_t* stage, uint32_t* parity)

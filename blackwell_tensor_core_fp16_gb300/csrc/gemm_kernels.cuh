@@ -265,24 +265,38 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits)
 // ==============================================================================================
 // gemm_ws_kernel: persistent, warp-specialised, TMEM double-buffered.
 // ==============================================================================================
-template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore = true>
+// kMx: block-scaled FP8 operands (E4M3/E5M2 with one E8M0 scale per 32 K elements) instead of
+// fp16/bf16.  A stage still holds 128-byte rows (128 FP8 elements instead of 64 fp16), plus the
+// stage's scale chunks (see mx_sf_offset): one for this CTA's 128 rows of A and SFB_CHUNKS for
+// the tile's rows of B, which every CTA of a pair loads whole.  The MMA issuer copies them into
+// a ring of tensor-memory columns after the two accumulators, one slot per stage.
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore = true, bool kMx = false>
 struct WsCfg {
     static_assert(kCtaGroup == 1 || kCtaGroup == 2, "a CTA or a CTA pair");
     static_assert(kBlockN % 64 == 0 && kBlockN >= 64 && kBlockN <= 256, "N tile");
     static constexpr uint32_t BN = kBlockN;
     static constexpr uint32_t MMA_M = kBlockM * kCtaGroup;
     static constexpr uint32_t B_ROWS = kBlockN / kCtaGroup;  // rows of B each CTA loads
-    static constexpr uint32_t A_BYTES = kBlockM * kBlockK * 2;
-    static constexpr uint32_t B_BYTES = B_ROWS * kBlockK * 2;
+    static constexpr uint32_t ELEM_BYTES = kMx ? 1u : 2u;
+    static constexpr uint32_t BLOCK_K = 128u / ELEM_BYTES;   // elements in a 128-byte row
+    static constexpr uint32_t A_BYTES = kBlockM * 128u;
+    static constexpr uint32_t B_BYTES = B_ROWS * 128u;
+    static constexpr uint32_t SFB_CHUNKS = kMx ? (kBlockN % 128 == 0 ? kBlockN / 128 : kBlockN / 128 + 1) : 0u;
+    static constexpr uint32_t SF_BYTES = kMx ? 512u * (1u + SFB_CHUNKS) : 0u;
+    static constexpr uint32_t SF_COLS = kMx ? 4u * (1u + SFB_CHUNKS) : 0u;  // TMEM cols per stage
+    static constexpr uint32_t TMEM_SF = 2u * kBlockN;          // first scale-factor column
     // Bytes that complete on the issuing CTA's "full" barrier per stage (both CTAs' loads).
-    static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES) * kCtaGroup;
+    static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES + SF_BYTES) * kCtaGroup;
     static constexpr uint32_t D_COLS = 64;                   // one 128-byte swizzle row of fp16
     static constexpr uint32_t D_BYTES = kBlockM * D_COLS * 2;
-    static constexpr uint32_t TMEM_COLS = 2 * kBlockN;       // two accumulators
+    static constexpr uint32_t TMEM_COLS = kMx ? 512u : 2u * kBlockN;  // two accumulators (+ scales)
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM columns");
+    static_assert(!kMx || TMEM_SF + kStages * SF_COLS <= TMEM_COLS, "TMEM scale-factor ring");
     static constexpr uint32_t OFF_A = 0;
     static constexpr uint32_t OFF_B = OFF_A + kStages * A_BYTES;
-    static constexpr uint32_t OFF_D = OFF_B + kStages * B_BYTES;
+    static constexpr uint32_t OFF_SF = OFF_B + kStages * B_BYTES;
+    // the swizzled D staging buffers start on a 1024-byte boundary
+    static constexpr uint32_t OFF_D = (OFF_SF + kStages * SF_BYTES + 1023u) & ~1023u;
     // Two staging buffers for the TMA-store epilogue; none when the epilogue stores directly.
     static constexpr uint32_t OFF_BAR = OFF_D + (kTmaStore ? 2 * D_BYTES : 0);
     static constexpr uint32_t NUM_BARS = 2 * kStages + 5;    // full, empty, tfull x2, tempty x2, drain
@@ -297,7 +311,9 @@ struct WsCfg {
     static constexpr uint32_t EPI_THREADS = 128;
 };
 
-template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore, bool kBf16 = false>
+// kBf16: bf16 operands and output (fp16 otherwise); with kMx it selects the output type only.
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore, bool kBf16 = false,
+          bool kMx = false>
 __global__ void __launch_bounds__(192, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
@@ -307,9 +323,11 @@ __global__ void __launch_bounds__(192, 1)
                    uint32_t group_m, uint64_t timeout_ns, uint32_t l2_hints,
                    float* __restrict__ ws_part, uint32_t* __restrict__ ws_count,
                    uint32_t sk_tiles, uint32_t sk_units, const uint16_t* __restrict__ bias,
-                   uint32_t act, uint32_t debug_flags)
+                   uint32_t act, uint32_t debug_flags,
+                   const __grid_constant__ CUtensorMap tmap_sfa,
+                   const __grid_constant__ CUtensorMap tmap_sfb, uint32_t mx_idesc)
 {
-    using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore>;
+    using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore, kMx>;
     constexpr bool kPair = (kCtaGroup == 2);
     constexpr uint32_t idesc = make_idesc_f16(C::MMA_M, C::BN, kBf16 ? 1u : 0u);
     const bool fused = bias != nullptr || act != kActNone;
@@ -320,6 +338,7 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t sA = base + C::OFF_A;
     const uint32_t sB = base + C::OFF_B;
+    const uint32_t sSF = base + C::OFF_SF;
     const uint32_t sD = base + C::OFF_D;
     const uint32_t bar0 = base + C::OFF_BAR;
     const auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
@@ -346,6 +365,10 @@ __global__ void __launch_bounds__(192, 1)
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
         prefetch_tensormap(&tmap_d);
+        if constexpr (kMx) {
+            prefetch_tensormap(&tmap_sfa);
+            prefetch_tensormap(&tmap_sfb);
+        }
         for (uint32_t s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
@@ -381,13 +404,15 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t item = 0;
         WorkItem wi = work_item(split, cid, 0);
         uint32_t kb = wi.kb0;
-        int32_t m0 = 0, n0 = 0;
+        int32_t m0 = 0, n0 = 0, sf_rb_b = 0;
         const uint32_t produce = (debug_flags & kDebugNoLoads) ? 0u : total;
         for (; it < produce; ++it) {
             if (kb == wi.kb0) {
                 const TileCoord tc = tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
                 m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
                 n0 = static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS);
+                // the 128-row group of B's scales that holds the tile's first row
+                sf_rb_b = static_cast<int32_t>(tc.n_blk * C::BN / 128u);
             }
             const RingPos p = ring_pos(it, kStages);
             const bool w = mbar_wait<kPair>(empty_bar(p.stage), p.parity ^ 1u, abort_flag,
@@ -398,18 +423,31 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             if (leader) {
-                const int32_t k0 = static_cast<int32_t>(kb * kBlockK);
+                const int32_t k0 = static_cast<int32_t>(kb * C::BLOCK_K);
                 const uint32_t dA = sA + p.stage * C::A_BYTES;
                 const uint32_t dB = sB + p.stage * C::B_BYTES;
+                const uint32_t dS = sSF + p.stage * C::SF_BYTES;
                 if constexpr (!kPair) {
                     mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
                     tma_load_2d_hint(dA, &tmap_a, full_bar(p.stage), k0, m0, pol_a);
                     tma_load_2d_hint(dB, &tmap_b, full_bar(p.stage), k0, n0, pol_b);
+                    if constexpr (kMx) {
+                        // scale chunks (K-block group kb): A's row group, then B's groups
+                        tma_load_3d(dS, &tmap_sfa, full_bar(p.stage), 0, static_cast<int32_t>(kb),
+                                    m0 / 128);
+                        tma_load_3d(dS + 512u, &tmap_sfb, full_bar(p.stage), 0,
+                                    static_cast<int32_t>(kb), sf_rb_b);
+                    }
                 } else {
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
                     const uint32_t fb = mapa_shared(full_bar(p.stage), 0);
                     tma_load_2d_pair_hint(dA, &tmap_a, fb, k0, m0, pol_a);
                     tma_load_2d_pair_hint(dB, &tmap_b, fb, k0, n0, pol_b);
+                    if constexpr (kMx) {
+                        tma_load_3d_pair(dS, &tmap_sfa, fb, 0, static_cast<int32_t>(kb), m0 / 128);
+                        tma_load_3d_pair(dS + 512u, &tmap_sfb, fb, 0, static_cast<int32_t>(kb),
+                                         sf_rb_b);
+                    }
                 }
             }
             __syncwarp();
@@ -454,6 +492,7 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t kb = wi.kb0;
             uint32_t acc = 0;
             uint32_t d_tmem = tmem_base;
+            uint32_t sfb_shift = 0;
             bool ok = true;
             bool issued = false;
             for (uint32_t it = 0; it < total; ++it) {
@@ -469,6 +508,12 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     tcgen05_fence_after();
                     d_tmem = tmem_base + b * C::BN;
+                    if constexpr (kMx) {
+                        // B's scales start at the tile's first row inside its first chunk.
+                        const TileCoord tc =
+                            tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
+                        sfb_shift = ((tc.n_blk * C::BN) % 128u) / 32u;
+                    }
                 }
                 const RingPos p = ring_pos(it, kStages);
                 const bool w = mbar_wait<kPair>(full_bar(p.stage), p.parity, abort_flag,
@@ -482,10 +527,27 @@ __global__ void __launch_bounds__(192, 1)
                 const uint64_t ad = make_smem_desc_sw128(sA + p.stage * C::A_BYTES, 1024);
                 const uint64_t bd = make_smem_desc_sw128(sB + p.stage * C::B_BYTES, 1024);
                 if (leader) {
+                    if constexpr (kMx) {
+                        // This stage's scales -> its tensor-memory slot, then 4 MMAs of K = 32
+                        // (one scale block each; the scale-factor ID picks the block's byte).
+                        const uint32_t sf_col = tmem_base + C::TMEM_SF + p.stage * C::SF_COLS;
+                        const uint32_t sS = sSF + p.stage * C::SF_BYTES;
 #pragma unroll
-                    for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
-                        mma_f16<kCtaGroup>(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc,
-                                           ((kb - wi.kb0) | k) != 0u);
+                        for (uint32_t c = 0; c <= C::SFB_CHUNKS; ++c)
+                            tmem_cp_32x128b_warpx4<kCtaGroup>(sf_col + 4u * c,
+                                                              make_sf_desc(sS + 512u * c));
+#pragma unroll
+                        for (uint32_t k = 0; k < 4; ++k)
+                            mma_mx<kCtaGroup>(d_tmem, ad + 2ull * k, bd + 2ull * k,
+                                              idesc_mx_with_sf_id(mx_idesc, k), sf_col,
+                                              sf_col + 4u + sfb_shift,
+                                              ((kb - wi.kb0) | k) != 0u);
+                    } else {
+#pragma unroll
+                        for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
+                            mma_f16<kCtaGroup>(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc,
+                                               ((kb - wi.kb0) | k) != 0u);
+                    }
                     if constexpr (kPair) mma_commit_pair(empty_bar(p.stage), 0x3);
                     else mma_commit(empty_bar(p.stage));
                 }
@@ -745,6 +807,28 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 1) {
         tcgen05_fence_after();
         tmem_dealloc<kCtaGroup>(tmem_base, C::TMEM_COLS);
+    }
+}
+
+
+// ==============================================================================================
+// Block scales, row-major (rows x k_blocks bytes, one E8M0 code per row and 32-element K block)
+// -> the tiled layout the block-scaled kernels read (mx_sf_offset).  One thread per byte of the
+// tiled buffer; bytes that no (row, block) maps to (rows past the last 128-row group, K blocks
+// past the last group of 4) get 127, a scale of 1.0, so a zero-filled K tail stays zero.
+// ==============================================================================================
+__global__ void mx_pack_scales_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                      uint64_t rows, uint32_t k_blocks, uint32_t k_groups,
+                                      uint64_t total)
+{
+    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+    for (uint64_t t = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+         t += stride) {
+        const uint64_t chunk = t / 512u;
+        const uint32_t w = static_cast<uint32_t>(t % 512u);
+        const uint64_t row = (chunk / k_groups) * 128u + ((w % 16u) / 4u) * 32u + w / 16u;
+        const uint32_t kb = static_cast<uint32_t>(chunk % k_groups) * 4u + w % 4u;
+        dst[t] = (row < rows && kb < k_blocks) ? src[row * k_blocks + kb] : uint8_t{127};
     }
 }
 

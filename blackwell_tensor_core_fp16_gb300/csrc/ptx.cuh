@@ -259,6 +259,28 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
                  : "memory");
 }
 
+// 3-D tiled load into this CTA's shared memory (the block-scale chunks); x is the inner
+// coordinate in elements.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// CTA-pair form of tma_load_3d: completes on a barrier that may be the peer CTA's.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y,
+                                                 int32_t z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+                 ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // 2-D tiled store from this CTA's shared memory; elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x,
                                              int32_t y)
@@ -353,6 +375,48 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
                      "setp.ne.b32 p, %4, 0;\n\t"
                      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+}
+
+// Block-scaled FP8 MMA (kind::mxf8f6f4, one E8M0 scale per 32 K elements):
+// D[tmem] (+)= (A * sA) * (B * sB)^T.  sfa_tmem / sfb_tmem are the tensor-memory addresses of the
+// scale-factor columns; the idesc's scale-factor IDs pick the byte of each 32-bit column that
+// holds this MMA's K block.
+template <int kCtaGroup>
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                       uint32_t accumulate)
+{
+    if constexpr (kCtaGroup == 1)
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+                     "[%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+                     "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem),
+                     "r"(sfb_tmem)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+                     "[%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+                     "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem),
+                     "r"(sfb_tmem)
+                     : "memory");
+}
+
+// Copy 32 rows x 128 bits from shared memory (described by `sdesc`) into tensor memory at
+// `taddr`, replicated into all four 32-lane windows (lanes r, 32 + r, 64 + r, 96 + r get row r):
+// the scale-factor layout of the page "TIRx Layout API", section "Scale Factor 布局".  Runs in
+// issue order with the MMAs of the same thread.
+template <int kCtaGroup>
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
+{
+    if constexpr (kCtaGroup == 1)
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                     : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                      : "memory");
 }
 

@@ -230,6 +230,86 @@ void gemm_f16_sk_item(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_
 uint32_t gemm_f16_sk_unit_of(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t tail,
                              uint32_t x);
 
+/* ---- block-scaled FP8 GEMM (MX formats) ------------------------------------------------------
+ *
+ * The operation (page "TIRx Layout API", sections "示例：Blackwell Tensor Memory" and
+ * "Scale Factor 布局": a block-scaled FP8 GEMM whose MMA reads 8-bit scale factors kept in
+ * tensor memory next to two accumulator stages, replicated into every 32-lane window).  The
+ * pages fix neither the element formats nor the block length; this library implements the
+ * OCP Microscaling reading that the tensor cores' mxf8f6f4 kind computes:
+ *
+ *     D[i][j] = sum_{k < K} (A[i][k] * 2^(SA[i][k/32] - 127)) * (B[j][k] * 2^(SB[j][k/32] - 127))
+ *
+ * A (M x K) and B (N x K) hold FP8 codes, row-major and dense (leading dimension K bytes), each
+ * in E4M3 or E5M2 (chosen per operand).  SA and SB hold one E8M0 code (a biased exponent; 255
+ * is NaN) per row and per block of 32 consecutive K elements, so K must be a multiple of 32.
+ * The sums are accumulated in fp32 in tensor memory, then optionally act(sum + bias[j]) as in
+ * gemm_f16_nt_fused, and rounded to fp16 or bf16 (round to nearest even) into D (M x N,
+ * row-major, leading dimension N).
+ *
+ * Scale layout.  The kernels read SA and SB in a tiled layout, not row-major: rows in groups of
+ * 128 and K blocks in groups of 4 form 512-byte chunks, ordered row-group-major; scale (r, b)
+ * lives at byte
+ *     ((r / 128) * ceil(K/128) + b / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + b % 4
+ * (gemm_mxf8_sf_offset computes it).  A buffer holds gemm_mxf8_scale_bytes(rows, K) bytes;
+ * gemm_mxf8_pack_scales converts a row-major rows x K/32 array into it.  Padding bytes (rows
+ * past the last full group, K blocks past K/32) are read: those of padded rows only reach
+ * outputs that are never written, but those of padded K blocks multiply the zeros the K tail is
+ * filled with, so they must not hold 255 (NaN); the pack routine writes 127 (1.0) there.
+ *
+ * Ownership, asynchrony and errors as for gemm_f16_nt; D is overwritten, never read.
+ */
+#define GEMM_MXF8_E4M3 0 /* 1 sign, 4 exponent (bias 7), 3 fraction bits; no infinities */
+#define GEMM_MXF8_E5M2 1 /* 1 sign, 5 exponent (bias 15), 2 fraction bits; IEEE-like */
+
+#define GEMM_MXF8_VARIANT_AUTO 0
+#define GEMM_MXF8_VARIANT_128x128 1      /* persistent, warp-specialised, 1 CTA per 128x128 tile */
+#define GEMM_MXF8_VARIANT_PAIR_256x128 2 /* persistent, warp-specialised, CTA pair per 256x128 */
+#define GEMM_MXF8_NUM_VARIANTS 3
+
+/* D = act(A * B^T with block scales + bias), as above.
+ *   A, B:        FP8 codes, M x K and N x K, 16-byte aligned (device memory).
+ *   SFA, SFB:    tiled scales of A and B (gemm_mxf8_scale_bytes(M, K), (N, K) bytes),
+ *                16-byte aligned.
+ *   D:           M x N of out_dtype (GEMM_F16_DTYPE_F16 or _BF16), 16-byte aligned.
+ *   fmt_a/fmt_b: GEMM_MXF8_E4M3 or GEMM_MXF8_E5M2.
+ *   bias:        N elements of out_dtype, 16-byte aligned, or NULL; activation GEMM_F16_ACT_*.
+ *   variant:     GEMM_MXF8_VARIANT_*; workspace/workspace_bytes as for gemm_f16_nt_ex (NULL/0:
+ *                data-parallel schedule).
+ * Errors: GEMM_F16_ERR_INVALID_ARG for a null pointer, a negative or too large size or an
+ * unknown format, dtype, activation or variant; GEMM_F16_ERR_UNSUPPORTED when K is not a
+ * multiple of 32, N not a multiple of 8, or a pointer is misaligned.  M == 0 or N == 0 does
+ * nothing; K == 0 writes zeros (not with a bias or activation). */
+int gemm_mxf8_nt(const void* A, const void* B, const void* SFA, const void* SFB, void* D,
+                 int64_t M, int64_t N, int64_t K, int fmt_a, int fmt_b, int out_dtype,
+                 const void* bias, int activation, int variant, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes for the stream-K tail of gemm_mxf8_nt with this shape and variant (0 when
+ * the shape gets no tail). */
+int gemm_mxf8_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, size_t* bytes);
+
+/* The variant GEMM_MXF8_VARIANT_AUTO picks for this shape on a device with num_sms SMs. */
+int gemm_mxf8_choose_variant(int64_t M, int64_t N, int64_t K, int num_sms);
+
+/* Bytes of a tiled scale buffer for a rows x K operand; -1 if rows < 0 or K is not a
+ * non-negative multiple of 32. */
+int64_t gemm_mxf8_scale_bytes(int64_t rows, int64_t K);
+
+/* Row-major scales (rows x K/32 bytes at src, device memory) -> the tiled layout at dst
+ * (gemm_mxf8_scale_bytes(rows, K) bytes, device memory, not overlapping src), padding bytes set
+ * to 127.  Asynchronous on `stream`. */
+int gemm_mxf8_pack_scales(const void* src, void* dst, int64_t rows, int64_t K,
+                          cudaStream_t stream);
+
+/* Host-side encoders (no GPU needed): the instruction descriptor of the block-scaled MMA with
+ * scale-factor IDs 0, the tiled-layout byte offset of scale (row, k_block) for a given K (-1 if
+ * out of range), and the shared-memory descriptor of a 512-byte scale chunk. */
+uint32_t gemm_mxf8_idesc(uint32_t M, uint32_t N, uint32_t fmt_a, uint32_t fmt_b);
+int64_t gemm_mxf8_sf_offset(int64_t row, int64_t k_block, int64_t K);
+uint64_t gemm_mxf8_sf_desc(uint32_t smem_addr);
+int gemm_mxf8_get_variant_info(int variant, gemm_f16_variant_info* out);
+
 #ifdef __cplusplus
 }
 #endif
