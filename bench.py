@@ -729,7 +729,9 @@ def run_sweep_mx(args, g, dev, stream, sms):
         w = MX_WORKLOADS[name]
         t = mx_inputs_on_device(g, w, dev)
         auto = g.gemm_mxf8_choose_variant(w.M, w.N, w.K, sms)
-        variants = [auto] if args.sweep_variants == "auto" else [1, 2]
+        variants = ([auto] if args.sweep_variants == "auto"
+                    else [int(v) for v in args.sweep_variants.split(",")]
+                    if args.sweep_variants != "1,2,3,4,5" else [1, 2, 3, 4])
         for v in variants:
             with torch.cuda.stream(stream):
                 for _ in range(5):

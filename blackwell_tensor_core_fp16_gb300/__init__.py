@@ -303,7 +303,8 @@ def exported_symbols(header_path: str | None = None):
 # ---- block-scaled FP8 (MX) ---------------------------------------------------------------------
 
 FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
-MX_VARIANTS = {"auto": 0, "mx_128x128": 1, "mx_pair_256x128": 2}
+MX_VARIANTS = {"auto": 0, "mx_128x128": 1, "mx_pair_256x128": 2, "mx_pair_256x192": 3,
+               "mx_pair_256x256": 4}
 
 
 def gemm_mxf8_nt(A: int, B: int, SFA: int, SFB: int, D: int, M: int, N: int, K: int,

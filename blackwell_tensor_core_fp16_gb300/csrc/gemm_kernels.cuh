@@ -270,8 +270,14 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits)
 // stage's scale chunks (see mx_sf_offset): one for this CTA's 128 rows of A and SFB_CHUNKS for
 // the tile's rows of B, which every CTA of a pair loads whole.  The MMA issuer copies them into
 // a ring of tensor-memory columns after the two accumulators, one slot per stage.
-template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore = true, bool kMx = false>
+// kAccBufs: tensor-memory accumulators (2: the epilogue of tile i overlaps the MMAs of tile
+// i + 1; 1: a 256-column accumulator leaves room for the block scales, and the epilogue reads it
+// out into registers before it stores, so the MMAs wait only for that read).
+template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore = true, bool kMx = false,
+          int kAccBufs = 2>
 struct WsCfg {
+    static_assert(kAccBufs == 1 || kAccBufs == 2, "one or two accumulators");
+    static constexpr uint32_t ACC_BUFS = kAccBufs;
     static_assert(kCtaGroup == 1 || kCtaGroup == 2, "a CTA or a CTA pair");
     static_assert(kBlockN % 64 == 0 && kBlockN >= 64 && kBlockN <= 256, "N tile");
     static constexpr uint32_t BN = kBlockN;
@@ -284,12 +290,12 @@ struct WsCfg {
     static constexpr uint32_t SFB_CHUNKS = kMx ? (kBlockN % 128 == 0 ? kBlockN / 128 : kBlockN / 128 + 1) : 0u;
     static constexpr uint32_t SF_BYTES = kMx ? 512u * (1u + SFB_CHUNKS) : 0u;
     static constexpr uint32_t SF_COLS = kMx ? 4u * (1u + SFB_CHUNKS) : 0u;  // TMEM cols per stage
-    static constexpr uint32_t TMEM_SF = 2u * kBlockN;          // first scale-factor column
+    static constexpr uint32_t TMEM_SF = kAccBufs * kBlockN;    // first scale-factor column
     // Bytes that complete on the issuing CTA's "full" barrier per stage (both CTAs' loads).
     static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES + SF_BYTES) * kCtaGroup;
     static constexpr uint32_t D_COLS = 64;                   // one 128-byte swizzle row of fp16
     static constexpr uint32_t D_BYTES = kBlockM * D_COLS * 2;
-    static constexpr uint32_t TMEM_COLS = kMx ? 512u : 2u * kBlockN;  // two accumulators (+ scales)
+    static constexpr uint32_t TMEM_COLS = kMx ? 512u : kAccBufs * kBlockN;  // accumulators (+ scales)
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM columns");
     static_assert(!kMx || TMEM_SF + kStages * SF_COLS <= TMEM_COLS, "TMEM scale-factor ring");
     static constexpr uint32_t OFF_A = 0;
@@ -313,7 +319,7 @@ struct WsCfg {
 
 // kBf16: bf16 operands and output (fp16 otherwise); with kMx it selects the output type only.
 template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore, bool kBf16 = false,
-          bool kMx = false>
+          bool kMx = false, int kAccBufs = 2>
 __global__ void __launch_bounds__(192, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
@@ -327,7 +333,7 @@ __global__ void __launch_bounds__(192, 1)
                    const __grid_constant__ CUtensorMap tmap_sfa,
                    const __grid_constant__ CUtensorMap tmap_sfb, uint32_t mx_idesc)
 {
-    using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore, kMx>;
+    using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore, kMx, kAccBufs>;
     constexpr bool kPair = (kCtaGroup == 2);
     constexpr uint32_t idesc = make_idesc_f16(C::MMA_M, C::BN, kBf16 ? 1u : 0u);
     const bool fused = bias != nullptr || act != kActNone;
@@ -498,8 +504,8 @@ __global__ void __launch_bounds__(192, 1)
             for (uint32_t it = 0; it < total; ++it) {
                 if (kb == wi.kb0) {
                     // A new tile: wait until the epilogue has drained accumulator acc % 2.
-                    const uint32_t b = acc & 1u;
-                    const bool w = mbar_wait<kPair>(tempty_bar(b), ((acc >> 1) & 1u) ^ 1u,
+                    const uint32_t b = acc % C::ACC_BUFS;
+                    const bool w = mbar_wait<kPair>(tempty_bar(b), ((acc / C::ACC_BUFS) & 1u) ^ 1u,
                                                     abort_flag, timeout_ns);
                     if (!__all_sync(0xffffffffu, w)) {
                         if (leader) report(kStatusMmaTimeout, abort_flag);
@@ -556,8 +562,8 @@ __global__ void __launch_bounds__(192, 1)
                 if (++kb == wi.kb1) {
                     // Item done: the accumulator is ready for the epilogue once these MMAs are.
                     if (leader) {
-                        if constexpr (kPair) mma_commit_pair(tfull_bar(acc & 1u), 0x3);
-                        else mma_commit(tfull_bar(acc & 1u));
+                        if constexpr (kPair) mma_commit_pair(tfull_bar(acc % C::ACC_BUFS), 0x3);
+                        else mma_commit(tfull_bar(acc % C::ACC_BUFS));
                     }
                     __syncwarp();
                     ++acc;
@@ -639,8 +645,8 @@ __global__ void __launch_bounds__(192, 1)
             const int32_t m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
             const int32_t n0 = static_cast<int32_t>(tc.n_blk * C::BN);
             const bool rows_in = m0 < static_cast<int32_t>(M);
-            const uint32_t b = acc & 1u;
-            const uint32_t aph = (acc >> 1) & 1u;
+            const uint32_t b = acc % C::ACC_BUFS;
+            const uint32_t aph = (acc / C::ACC_BUFS) & 1u;
             // One thread polls; the barrier-AND gives all 128 threads the same answer, so the
             // group never splits between leaving and waiting at a named barrier.
             uint32_t waited = 1u;
@@ -652,6 +658,56 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tcgen05_fence_after();
+            if constexpr (C::ACC_BUFS == 1) {
+                if (!wi.partial) {
+                    // One accumulator: read all of it out (as packed 16-bit values, after the
+                    // fused epilogue), hand it back to the MMA issuer, then store.
+                    uint32_t pk[C::BN / C::D_COLS][32];
+#pragma unroll
+                    for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
+                        uint32_t v0[32], v1[32];
+                        const uint32_t taddr = tmem_base + lane_off + c * C::D_COLS;
+                        tmem_ld_32x32b_x32(taddr, v0, 0);
+                        tmem_ld_32x32b_x32(taddr, v1, 32);
+                        tmem_ld_wait();
+                        const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
+                        if (fused) {
+#pragma unroll
+                            for (int g8 = 0; g8 < 8; ++g8) {
+                                float f[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    f[i] = __uint_as_float(g8 < 4 ? v0[8 * g8 + i]
+                                                                  : v1[8 * (g8 - 4) + i]);
+                                epilogue8<kBf16>(f, bias, col0 + 8 * g8, N, act);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    if (g8 < 4) v0[8 * g8 + i] = __float_as_uint(f[i]);
+                                    else v1[8 * (g8 - 4) + i] = __float_as_uint(f[i]);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[c][i] = pack2<kBf16>(v0[2 * i], v0[2 * i + 1]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            pk[c][16 + i] = pack2<kBf16>(v1[2 * i], v1[2 * i + 1]);
+                    }
+                    tcgen05_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(0), 0));
+                        else mbar_arrive_local(tempty_bar(0));
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
+                        const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
+                        if (col0 < static_cast<int32_t>(N) && rows_in) store_chunk(pk[c], m0, col0);
+                    }
+                    continue;
+                }
+            }
             float4* my_part = wi.partial ? part_of(cid, wi.piece) : nullptr;
 #pragma unroll 1
             for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {

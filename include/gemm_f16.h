@@ -265,7 +265,9 @@ uint32_t gemm_f16_sk_unit_of(uint32_t tiles, uint32_t units, uint32_t k_blocks, 
 #define GEMM_MXF8_VARIANT_AUTO 0
 #define GEMM_MXF8_VARIANT_128x128 1      /* persistent, warp-specialised, 1 CTA per 128x128 tile */
 #define GEMM_MXF8_VARIANT_PAIR_256x128 2 /* persistent, warp-specialised, CTA pair per 256x128 */
-#define GEMM_MXF8_NUM_VARIANTS 3
+#define GEMM_MXF8_VARIANT_PAIR_256x192 3 /* persistent, warp-specialised, CTA pair per 256x192 */
+#define GEMM_MXF8_VARIANT_PAIR_256x256 4 /* as the pair, 256x256 tiles, one TMEM accumulator */
+#define GEMM_MXF8_NUM_VARIANTS 5
 
 /* D = act(A * B^T with block scales + bias), as above.
  *   A, B:        FP8 codes, M x K and N x K, 16-byte aligned (device memory).

@@ -26,7 +26,8 @@ pytestmark = pytest.mark.gpu
 
 GUARD = 4096
 FILL = 0x7E5A                     # a NaN in fp16 and in bf16
-VARIANTS = [g.MX_VARIANTS["mx_128x128"], g.MX_VARIANTS["mx_pair_256x128"]]
+VARIANTS = [g.MX_VARIANTS["mx_128x128"], g.MX_VARIANTS["mx_pair_256x128"],
+            g.MX_VARIANTS["mx_pair_256x192"], g.MX_VARIANTS["mx_pair_256x256"]]
 TDT = {"f16": torch.float16, "bf16": torch.bfloat16}
 
 
