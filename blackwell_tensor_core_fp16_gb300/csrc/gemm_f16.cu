@@ -633,12 +633,13 @@ using MxPair192 = gf16::WsCfg<2, 192, 6, true, true>;
 // 5-slot scale ring: the epilogue frees the accumulator before it stores.
 using MxPair256 = gf16::WsCfg<2, 256, 5, true, true, 1>;
 
-int choose_mx_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
+// Measured on GB300 (bench.py --sweep --sweep-mx): the single-accumulator 256x256 pair is the
+// fastest at 2048^3 (13.2 us against 15.2 us for 128x128), 8192^3 and the MLP shape, and within
+// 1% of 256x192 on 3000x5000x1056; one 128x128 tile is faster on a single CTA.
+int choose_mx_variant(int64_t M, int64_t N, int64_t /*K*/, int /*num_sms*/)
 {
-    if (num_sms < 2) num_sms = 2;
-    const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 128);
-    if (M > 128 && pair_tiles >= num_sms / 2) return GEMM_MXF8_VARIANT_PAIR_256x128;
-    return GEMM_MXF8_VARIANT_128x128;
+    if (M <= 128 || N <= 128) return GEMM_MXF8_VARIANT_128x128;
+    return GEMM_MXF8_VARIANT_PAIR_256x256;
 }
 
 int64_t mx_scale_bytes(int64_t rows, int64_t K)

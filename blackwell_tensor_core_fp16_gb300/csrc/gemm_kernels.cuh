@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(192, 1)
                     tcgen05_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(0), 0));
+                        if constexpr (kPair) mbar_arrive_remote(mapa_shared(tempty_bar(0), 0));
                         else mbar_arrive_local(tempty_bar(0));
                     }
                     __syncwarp();
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(192, 1)
                     tcgen05_fence_before();
                     __syncwarp();
                     if (lane == 0) {
-                        if constexpr (kPair) mbar_arrive_cluster(mapa_shared(tempty_bar(b), 0));
+                        if constexpr (kPair) mbar_arrive_remote(mapa_shared(tempty_bar(b), 0));
                         else mbar_arrive_local(tempty_bar(b));
                     }
                     __syncwarp();

@@ -130,11 +130,15 @@ __device__ __forceinline__ void mbar_arrive_local(uint32_t bar)
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Arrival on a barrier named by a shared::cluster address (possibly another CTA's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster)
+// Arrival on a barrier named by a shared::cluster address (possibly another CTA's), with the
+// default CTA-scope release.  The epilogue's "accumulator drained" signal needs no cluster-scope
+// ordering of memory: its tensor-memory reads are complete (tcgen05.wait::ld) and fenced with
+// tcgen05.fence::before_thread_sync, and the waiting MMA issuer fences after the wait.  Measured
+// on GB300 (per-tile timeline probe of the CTA-pair kernel), a .release.cluster arrival on the
+// peer's barrier took about 550 ns longer to reach the waiter than this form.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // True once the phase of parity `parity` has completed.  A fresh barrier is in phase 0, and

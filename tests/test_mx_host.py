@@ -100,8 +100,9 @@ def test_variant_budgets(variant):
 
 def test_choose_variant():
     assert g.gemm_mxf8_choose_variant(128, 128, 128, 152) == 1
-    assert g.gemm_mxf8_choose_variant(8192, 8192, 8192, 152) == 2
-    assert g.gemm_mxf8_choose_variant(16384, 14336, 4096, 152) == 2
+    assert g.gemm_mxf8_choose_variant(2048, 2048, 2048, 152) == 4
+    assert g.gemm_mxf8_choose_variant(8192, 8192, 8192, 152) == 4
+    assert g.gemm_mxf8_choose_variant(16384, 14336, 4096, 152) == 4
 
 
 def test_rejects_before_touching_the_gpu():
