@@ -324,9 +324,41 @@ def run_mx_leg(args, g, dev, stream, num_sms, peak16, uuid):
                        "tflops": w.flops / (ms * 1e-3) / 1e12}
     achieved = K * flops / (sum(durs) * 1e-3) / 1e12
     peak8 = peak16 * FP8_OVER_16BIT
+
+    # cuBLAS's MXFP8 GEMM (torch._scaled_mm) on the same packed inputs, for the same number of
+    # steps right after ours: context only.  The tiled scale layout is the one cuBLAS reads, so
+    # the same buffers serve both.
+    cublas = None
+    try:
+        e4, e8 = torch.float8_e4m3fn, torch.float8_e8m0fnu
+        ops = [(w, t[0].view(e4), t[1].view(e4).t(), t[2].view(e8), t[3].view(e8), t[4])
+               for w, t, _ in work]
+
+        def cublas_step():
+            for w, a8, b8t, sa, sb, D in ops:
+                torch._scaled_mm(a8, b8t, scale_a=sa, scale_b=sb, out_dtype=torch.float16,
+                                 out=D)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                cublas_step()
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            c0.record(stream)
+            for _ in range(K):
+                cublas_step()
+            c1.record(stream)
+        torch.cuda.synchronize()
+        cv = K * flops / (c0.elapsed_time(c1) * 1e-3) / 1e12
+        cublas = {"value": cv, "unit": "TFLOP/s", "steps": K,
+                  "ours_over_cublas": (K * flops / (total * 1e-3) / 1e12) / cv}
+    except Exception as e:  # an older torch without the MX path: report why, not a number
+        cublas = {"unavailable": repr(e)[:200]}
     return {"metric": "block-scaled FP8 (MX E4M3, E8M0 per 32) GEMM TFLOP/s, fp16 out",
             "value": K * flops / (total * 1e-3) / 1e12, "unit": "TFLOP/s", "steps": K,
-            "per_workload": per, "clocks": clk,
+            "per_workload": per, "clocks": clk, "cublas_mxfp8_same_step": cublas,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak8,
                          "unit": "TFLOP/s", "frac": achieved / peak8, "traffic": None,
                          "peak_source": "measured bf16_tflops x 2 (nominal FP8 / 16-bit dense "

@@ -273,11 +273,16 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits)
 // kAccBufs: tensor-memory accumulators (2: the epilogue of tile i overlaps the MMAs of tile
 // i + 1; 1: a 256-column accumulator leaves room for the block scales, and the epilogue reads it
 // out into registers before it stores, so the MMAs wait only for that read).
+// kDBufs: shared-memory staging buffers of the TMA-store epilogue (2: a sub-tile is written
+// while the previous one is still being stored; 1 frees 16 KB for another pipeline stage where
+// the stores are off the critical path, as after a single accumulator has been read out).
 template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore = true, bool kMx = false,
-          int kAccBufs = 2>
+          int kAccBufs = 2, int kDBufs = 2>
 struct WsCfg {
     static_assert(kAccBufs == 1 || kAccBufs == 2, "one or two accumulators");
+    static_assert(kDBufs == 1 || kDBufs == 2, "one or two staging buffers");
     static constexpr uint32_t ACC_BUFS = kAccBufs;
+    static constexpr uint32_t D_BUFS = kDBufs;
     static_assert(kCtaGroup == 1 || kCtaGroup == 2, "a CTA or a CTA pair");
     static_assert(kBlockN % 64 == 0 && kBlockN >= 64 && kBlockN <= 256, "N tile");
     static constexpr uint32_t BN = kBlockN;
@@ -304,7 +309,7 @@ struct WsCfg {
     // the swizzled D staging buffers start on a 1024-byte boundary
     static constexpr uint32_t OFF_D = (OFF_SF + kStages * SF_BYTES + 1023u) & ~1023u;
     // Two staging buffers for the TMA-store epilogue; none when the epilogue stores directly.
-    static constexpr uint32_t OFF_BAR = OFF_D + (kTmaStore ? 2 * D_BYTES : 0);
+    static constexpr uint32_t OFF_BAR = OFF_D + (kTmaStore ? kDBufs * D_BYTES : 0);
     static constexpr uint32_t NUM_BARS = 2 * kStages + 5;    // full, empty, tfull x2, tempty x2, drain
     static constexpr uint32_t OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ABORT = OFF_SLOT + 4;
@@ -319,7 +324,7 @@ struct WsCfg {
 
 // kBf16: bf16 operands and output (fp16 otherwise); with kMx it selects the output type only.
 template <int kCtaGroup, int kBlockN, int kStages, bool kTmaStore, bool kBf16 = false,
-          bool kMx = false, int kAccBufs = 2>
+          bool kMx = false, int kAccBufs = 2, int kDBufs = 2>
 __global__ void __launch_bounds__(192, 1)
     gemm_ws_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(192, 1)
                    const __grid_constant__ CUtensorMap tmap_sfa,
                    const __grid_constant__ CUtensorMap tmap_sfb, uint32_t mx_idesc)
 {
-    using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore, kMx, kAccBufs>;
+    using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore, kMx, kAccBufs, kDBufs>;
     constexpr bool kPair = (kCtaGroup == 2);
     constexpr uint32_t idesc = make_idesc_f16(C::MMA_M, C::BN, kBf16 ? 1u : 0u);
     const bool fused = bias != nullptr || act != kActNone;
@@ -595,8 +600,8 @@ __global__ void __launch_bounds__(192, 1)
         // Store 64 columns (32 packed f16x2 words) of this thread's row at column col0.
         const auto store_chunk = [&](const uint32_t (&p)[32], int32_t m0, int32_t col0) {
             if constexpr (kTmaStore) {
-                // The store issued two sub-tiles ago read this buffer; wait until it has.
-                if (et == 0) bulk_wait_group_read<1>();
+                // The store issued D_BUFS sub-tiles ago read this buffer; wait until it has.
+                if (et == 0) bulk_wait_group_read<C::D_BUFS - 1>();
                 __syncwarp();
                 named_barrier_sync(1, C::EPI_THREADS);
                 const uint32_t dbuf = sD + sbuf * C::D_BYTES;
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(192, 1)
                     bulk_commit_group();
                 }
                 __syncwarp();
-                sbuf ^= 1u;
+                sbuf = (sbuf + 1u) % C::D_BUFS;
             } else {
                 // Each thread writes its own row: 64 fp16 as 8 16-byte vectors; the L2 merges
                 // the warp's 32 partial lines into full lines.
