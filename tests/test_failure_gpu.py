@@ -63,3 +63,37 @@ def test_wait_runs_out_and_context_survives(variant, expect_bits):
     d = D.cpu().double().numpy()
     ref = oracle.gemm_f64(A, B)
     assert (np.abs(d - ref) <= oracle.tolerance(ref, K)).all()
+
+
+@pytest.mark.parametrize("variant", [g.MX_VARIANTS["mx_128x128"], g.MX_VARIANTS["mx_pair_256x128"],
+                                     g.MX_VARIANTS["mx_pair_256x256"]])
+def test_block_scaled_wait_runs_out_and_context_survives(variant):
+    """The block-scaled kernels share the bounded waits: with no loads issued the MMA issuer's
+    wait for operand data (and its scales) runs out, and the next launch is correct."""
+    from blackwell_tensor_core_fp16_gb300.workloads import make_mx_inputs
+    M, N, K = 520, 776, 1056
+    A, B, SA, SB = make_mx_inputs(M, N, K, seed=701)
+    Ad, Bd = A.cuda(), B.cuda()
+    sfa, sfb = g.pack_scales(SA.cuda()), g.pack_scales(SB.cuda())
+    D = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+
+    def launch():
+        return g.gemm_mxf8_nt(Ad.data_ptr(), Bd.data_ptr(), sfa.data_ptr(), sfb.data_ptr(),
+                              D.data_ptr(), M, N, K, 0, 0, 0, 0, 0, variant, 0, 0, s)
+
+    assert g.gemm_f16_set_wait_timeout_ms(200) == g.OK
+    assert g.gemm_f16_set_fault_injection(1) == g.OK
+    assert launch() == g.OK
+    rc, bits = g.gemm_f16_check_status(s)
+    assert rc == g.ERR_TIMEOUT, (rc, bits)
+    assert bits & 2, f"bits 0x{bits:x}"
+    assert g.gemm_f16_check_status(s) == (g.OK, 0)
+
+    assert g.gemm_f16_set_fault_injection(0) == g.OK
+    assert g.gemm_f16_set_wait_timeout_ms(4000) == g.OK
+    assert launch() == g.OK
+    assert g.gemm_f16_check_status(s) == (g.OK, 0)
+    d = D.cpu().double().numpy()
+    ref, ref_abs = oracle.gemm_mx_f64(A, B, SA, SB)
+    assert (np.abs(d - ref) <= oracle.tolerance_mx(ref, ref_abs, K, "f16")).all()

@@ -237,14 +237,16 @@ def test_fused_epilogue(variant, activation):
     assert (err <= tol).all(), f"worst err/tol {float((err / tol).max()):.3f}"
 
 
-def test_stream_k_tail_parity():
-    """The 2048^3 workload on the 128x128 kernel leaves a partial last wave: with a workspace the
-    tail is split by K blocks across units."""
-    v = g.MX_VARIANTS["mx_128x128"]
-    A, B, SA, SB = mx_workload_inputs(MX_WORKLOADS["mx_square_2048"])
-    if g.gemm_mxf8_workspace_bytes(2048, 2048, 2048, v) == 0:
-        pytest.skip("no stream-K tail for this shape on this device")
-    full_parity(A, B, SA, SB, v, "2048^3 stream-K", workspace=True)
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["mx_square_2048", "mx_ragged_3000x5000x1056"])
+def test_stream_k_tail_parity(name, variant):
+    """With a workspace, the tiles of a partial last wave are split by K blocks across units
+    (the pieces are summed by the last contributor)."""
+    w = MX_WORKLOADS[name]
+    if g.gemm_mxf8_workspace_bytes(w.M, w.N, w.K, variant) == 0:
+        pytest.skip("no stream-K tail for this shape and variant on this device")
+    A, B, SA, SB = mx_workload_inputs(w)
+    full_parity(A, B, SA, SB, variant, f"{name} stream-K variant {variant}", workspace=True)
 
 
 def test_deterministic():
