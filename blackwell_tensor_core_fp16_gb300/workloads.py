@@ -181,3 +181,83 @@ def make_mx_inputs(M: int, N: int, K: int, seed: int, fmt_a: str = "e4m3",
 
 def mx_workload_inputs(w: MxWorkload):
     return make_mx_inputs(w.M, w.N, w.K, w.seed, w.fmt_a, w.fmt_b)
+
+
+# ---- Gated Delta Net prefill inputs --------------------------------------------------------------
+#
+# The six scenarios of the page "TIRx" (zixuwang.me), section "公开版本复测：六个场景": BF16 q/k/v,
+# head dimension 128, scale 0.73; single or packed sequences; multi-head (h_v == h_qk) or grouped
+# values (h_v = 2 h_qk); zero or given initial state (and then a final state out).
+# Draws, in this order from one torch.Generator: packed lengths (n - 1 cut points uniform on
+# 1 .. T - 1 without repeats), q and k normal(0, 1) then scaled to unit L2 norm per token and head
+# (the key normalisation that keeps the delta rule contractive), v normal(0, 1), all rounded to
+# bfloat16; alpha = exp(-U[0, 0.1)) and beta = sigmoid(normal(0, 1)) in float32; an initial
+# state normal(0, 0.1^2) in float32 when the scenario has one.
+
+@dataclass(frozen=True)
+class GdnWorkload:
+    name: str
+    T: int
+    n_seqs: int
+    h_qk: int
+    h_v: int
+    state: bool
+    seed: int
+    dk: int = 128
+    dv: int = 128
+    scale: float = 0.73
+
+    @property
+    def flops(self) -> int:
+        """Multiply-adds of the token recurrence, counted as two flops: per token and value head
+        the prediction (dv*dk), the rank-one update (dv*dk) and the output (dv*dk)."""
+        return 2 * 3 * self.T * self.h_v * self.dv * self.dk
+
+
+GDN_WORKLOADS = {
+    w.name: w
+    for w in [
+        GdnWorkload("single_t512_h8_mha_zero", 512, 1, 8, 8, False, 20),
+        GdnWorkload("single_t1024_h8_mha_state", 1024, 1, 8, 8, True, 21),
+        GdnWorkload("single_t1024_h8_hv16_gva_state", 1024, 1, 8, 16, True, 22),
+        GdnWorkload("single_t4096_h16_mha_zero", 4096, 1, 16, 16, False, 23),
+        GdnWorkload("packed_n10_t4096_h8_mha_state", 4096, 10, 8, 8, True, 24),
+        GdnWorkload("packed_n20_t8192_h8_hv16_gva_state", 8192, 20, 8, 16, True, 25),
+    ]
+}
+
+GDN_ORDER = list(GDN_WORKLOADS)
+
+
+def make_gdn_inputs(T: int, n_seqs: int, h_qk: int, h_v: int, dk: int, dv: int, seed: int,
+                    state: bool = False):
+    """dict of CPU tensors: q, k [T, h_qk, dk] and v [T, h_v, dv] bfloat16; alpha, beta [T, h_v]
+    float32; cu_seqlens [n_seqs + 1] int32; initial_state [n_seqs, h_v, dv, dk] float32 or
+    None."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    if n_seqs > 1:
+        cuts = torch.randperm(T - 1, generator=gen)[: n_seqs - 1] + 1
+        cu = torch.cat([torch.tensor([0]), torch.sort(cuts).values, torch.tensor([T])])
+    else:
+        cu = torch.tensor([0, T][: n_seqs + 1]) if n_seqs == 1 else torch.tensor([0])
+    cu = cu.to(torch.int32)
+
+    def unit(shape):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        return (x / x.norm(dim=-1, keepdim=True).clamp_min(1e-6)).to(torch.bfloat16)
+
+    q = unit((T, h_qk, dk))
+    k = unit((T, h_qk, dk))
+    v = torch.randn((T, h_v, dv), generator=gen, dtype=torch.float32).to(torch.bfloat16)
+    alpha = torch.exp(-0.1 * torch.rand((T, h_v), generator=gen, dtype=torch.float32))
+    beta = torch.sigmoid(torch.randn((T, h_v), generator=gen, dtype=torch.float32))
+    s0 = (0.1 * torch.randn((n_seqs, h_v, dv, dk), generator=gen, dtype=torch.float32)
+          if state else None)
+    return {"q": q.contiguous(), "k": k.contiguous(), "v": v.contiguous(),
+            "alpha": alpha.contiguous(), "beta": beta.contiguous(), "cu_seqlens": cu,
+            "initial_state": s0}
+
+
+def gdn_workload_inputs(w: GdnWorkload):
+    return make_gdn_inputs(w.T, w.n_seqs, w.h_qk, w.h_v, w.dk, w.dv, w.seed, w.state)

@@ -27,15 +27,15 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_ref.c")
-_SRCS = [_SRC, os.path.join(_HERE, "mx_ref.c")]
+_SRCS = [_SRC, os.path.join(_HERE, "mx_ref.c"), os.path.join(_HERE, "gdn_ref.c")]
 _LIB = os.path.join(_HERE, "liboracle_gemm.so")
 _lock = threading.Lock()
 _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile ``gemm_ref.c`` and ``mx_ref.c`` into ``liboracle_gemm.so`` next to them (gcc,
-    OpenMP)."""
+    """Compile ``gemm_ref.c``, ``mx_ref.c`` and ``gdn_ref.c`` into ``liboracle_gemm.so`` next to
+    them (gcc, OpenMP)."""
     stale = not os.path.exists(_LIB) or any(os.path.getmtime(_LIB) < os.path.getmtime(f)
                                             for f in _SRCS)
     if force or stale:
@@ -97,6 +97,10 @@ def _load():
                                                        ctypes.c_int, ctypes.c_int, i64p, i64p,
                                                        i64, f64p, f64p]
             lib.oracle_gemm_mx_f64_sampled.restype = ctypes.c_int
+            lib.oracle_gdn_f64.argtypes = [f64p, f64p, f64p, f64p, f64p, ctypes.c_void_p, i64,
+                                           i64, i64, i64, i64, ctypes.c_double, f64p, f64p,
+                                           f64p]
+            lib.oracle_gdn_f64.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -355,3 +359,53 @@ def tolerance_mx(d_ref: np.ndarray, d_abs: np.ndarray, K: int, out_dtype: str = 
     for fp16 output and 2^-7 for bfloat16."""
     rel = 2.0 ** -10 if out_dtype == "f16" else 2.0 ** -7
     return np.abs(d_ref) * rel + 4.0 * (K / 32.0 + 1.0) * 2.0 ** -24 * np.asarray(d_abs)
+
+
+# ---- Gated Delta Net prefill ----------------------------------------------------------------------
+
+def _f64(x, name) -> np.ndarray:
+    """A float array (numpy, or a CPU torch tensor of float32 / bfloat16 / float16) -> contiguous
+    binary64.  bfloat16 is widened with the oracle's own decoder."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().cpu().contiguous()
+        if x.dtype == torch.bfloat16:
+            return bf16_bits_to_f64(x)
+        if x.dtype == torch.float16:
+            return f16_bits_to_f64(x)
+        x = x.numpy()
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def gdn_f64(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_state=None):
+    """(o, final_state) of the gated delta rule, token by token in binary64.
+
+    q, k: [T, h_qk, dk]; v: [T, h_v, dv]; alpha, beta: [T, h_v]; cu_seqlens: n_seqs + 1 offsets;
+    initial_state: [n_seqs, h_v, dv, dk] or None (zero).  Returns o [T, h_v, dv] and the final
+    states [n_seqs, h_v, dv, dk], both binary64."""
+    qd, kd, vd = _f64(q, "q"), _f64(k, "k"), _f64(v, "v")
+    ad, bd = _f64(alpha, "alpha"), _f64(beta, "beta")
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens), dtype=np.int32)
+    T, h_qk, dk = qd.shape
+    h_v, dv = vd.shape[1], vd.shape[2]
+    n = cu.size - 1
+    if kd.shape != qd.shape or vd.shape[0] != T or ad.shape != (T, h_v) or bd.shape != (T, h_v):
+        raise ValueError("inconsistent shapes")
+    if n < 0 or cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must rise from 0 to T")
+    s0 = None
+    if initial_state is not None:
+        s0 = _f64(initial_state, "initial_state")
+        if s0.shape != (n, h_v, dv, dk):
+            raise ValueError(f"initial_state shape {s0.shape}; want {(n, h_v, dv, dk)}")
+    o = np.empty((T, h_v, dv), dtype=np.float64)
+    sf = np.empty((n, h_v, dv, dk), dtype=np.float64)
+    rc = _load().oracle_gdn_f64(qd.ctypes.data, kd.ctypes.data, vd.ctypes.data, ad.ctypes.data,
+                                bd.ctypes.data, cu.ctypes.data, n, h_qk, h_v, dk, dv,
+                                float(scale), None if s0 is None else s0.ctypes.data,
+                                o.ctypes.data, sf.ctypes.data)
+    if rc == -1:
+        raise ValueError("inconsistent sizes (h_v must be a multiple of h_qk)")
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its state")
+    return o, sf
