@@ -93,13 +93,17 @@ def dist_env():
     return world, rank, local
 
 
+GEMM_KERNEL_SOURCES = ("desc.h", "gemm_f16.cu", "gemm_kernels.cuh", "ptx.cuh")
+
+
 def kernel_source_hash() -> str:
+    """sha256 over the GEMM kernel's sources: a recorded ncu traffic figure applies only while
+    they are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blackwell_tensor_core_fp16_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in GEMM_KERNEL_SOURCES:
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
 
