@@ -137,6 +137,13 @@ def load():
         lib.gemm_mxf8_sf_desc.restype = ctypes.c_uint64
         lib.gemm_mxf8_get_variant_info.argtypes = [i32, ctypes.POINTER(VariantInfo)]
         lib.gemm_mxf8_get_variant_info.restype = i32
+        lib.gdn_prefill_workspace_bytes.argtypes = [i64, i64, i64, ctypes.POINTER(sz)]
+        lib.gdn_prefill_workspace_bytes.restype = i32
+        lib.gdn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                    ctypes.c_float, vp, vp, vp, vp, sz, vp]
+        lib.gdn_prefill.restype = i32
+        lib.gdn_last_error.argtypes = []
+        lib.gdn_last_error.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -292,12 +299,13 @@ def gemm_f16_ring_pos(it: int, stages: int):
 
 
 def exported_symbols(header_path: str | None = None):
-    """Names of the functions the public header declares."""
-    import os
-    path = header_path or os.path.join(_build.ROOT, "include", "gemm_f16.h")
-    text = open(path).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_(?:f16|mxf8)_\w+)\s*\(", text)))
+    """Names of the functions the public headers (include/gemm_f16.h, include/gdn.h) declare."""
+    paths = [header_path] if header_path else _build.HEADERS
+    names = set()
+    for path in paths:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names.update(re.findall(r"\b((?:gemm_(?:f16|mxf8)|gdn)_\w+)\s*\(", text))
+    return sorted(names)
 
 
 # ---- block-scaled FP8 (MX) ---------------------------------------------------------------------
@@ -428,6 +436,69 @@ def gemm_mx(A, B, SFA, SFB, out=None, fmt_a: str = "e4m3", fmt_b: str = "e4m3",
     if rc != OK:
         raise GemmError(rc, gemm_f16_last_error())
     return out
+
+
+# ---- Gated Delta Net prefill ----------------------------------------------------------------------
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+
+
+def gdn_prefill_workspace_bytes(total_tokens: int, n_seqs: int, h_v: int) -> int:
+    out = ctypes.c_size_t(0)
+    rc = load().gdn_prefill_workspace_bytes(total_tokens, n_seqs, h_v, ctypes.byref(out))
+    if rc != GDN_OK:
+        raise GemmError(rc, gdn_last_error())
+    return out.value
+
+
+def gdn_prefill(q: int, k: int, v: int, alpha: int, beta: int, cu_seqlens: int, n_seqs: int,
+                total_tokens: int, h_qk: int, h_v: int, head_dim: int, scale: float,
+                initial_state: int, o: int, final_state: int, workspace: int,
+                workspace_bytes: int, stream: int = 0) -> int:
+    return load().gdn_prefill(q, k, v, alpha, beta, cu_seqlens, n_seqs, total_tokens, h_qk, h_v,
+                              head_dim, scale, initial_state, o, final_state, workspace,
+                              workspace_bytes, stream)
+
+
+def gdn_last_error() -> str:
+    return load().gdn_last_error().decode()
+
+
+def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_state=None,
+                     output_final_state: bool = False, stream=None, workspace=None):
+    """Gated Delta Net prefill over packed sequences (CUDA tensors): q, k [T, h_qk, 128] and
+    v [T, h_v, 128] bfloat16; alpha, beta [T, h_v] float32; cu_seqlens [n + 1] int32;
+    initial_state [n, h_v, 128, 128] float32 or None.  Returns (o [T, h_v, 128] bfloat16,
+    final_state or None).  Asynchronous on ``stream``; raises GemmError on a non-zero status."""
+    import torch
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("alpha", alpha, torch.float32),
+                        ("beta", beta, torch.float32), ("cu_seqlens", cu_seqlens, torch.int32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
+    T, h_qk, d = q.shape
+    h_v = v.shape[1]
+    n = cu_seqlens.numel() - 1
+    if initial_state is not None and (initial_state.dtype != torch.float32 or
+                                      tuple(initial_state.shape) != (n, h_v, d, d) or
+                                      not initial_state.is_contiguous()):
+        raise ValueError("initial_state must be a contiguous float32 [n, h_v, d, d] tensor")
+    o = torch.empty((T, h_v, d), dtype=torch.bfloat16, device=q.device)
+    sf = (torch.empty((n, h_v, d, d), dtype=torch.float32, device=q.device)
+          if output_final_state else None)
+    if workspace is None:
+        need = gdn_prefill_workspace_bytes(T, n, h_v)
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s) if hasattr(s, "cuda_stream") else _nullctx():
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = gdn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(), beta.data_ptr(),
+                     cu_seqlens.data_ptr(), n, T, h_qk, h_v, d, float(scale),
+                     0 if initial_state is None else initial_state.data_ptr(), o.data_ptr(),
+                     0 if sf is None else sf.data_ptr(), workspace.data_ptr(),
+                     workspace.numel(), _stream_handle(stream))
+    if rc != GDN_OK:
+        raise GemmError(rc, gdn_last_error())
+    return o, sf
 
 
 # ---- torch convenience ----------------------------------------------------------------------

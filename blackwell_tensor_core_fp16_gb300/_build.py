@@ -8,7 +8,8 @@ import subprocess
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
-HEADER = os.path.join(ROOT, "include", "gemm_f16.h")
+HEADERS = [os.path.join(ROOT, "include", "gemm_f16.h"), os.path.join(ROOT, "include", "gdn.h")]
+SOURCES = ["gemm_f16.cu", "gdn.cu"]   # translation units, compiled in parallel
 LIB_PATH = os.path.join(PKG_DIR, "libgemm_f16.so")
 
 NVCC_FLAGS = [
@@ -32,7 +33,7 @@ def _nvcc() -> str:
 def _sources():
     srcs = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))
             if f.endswith((".cu", ".cuh", ".h"))]
-    return srcs + [HEADER]
+    return srcs + HEADERS
 
 
 def is_stale() -> bool:
@@ -43,17 +44,40 @@ def is_stale() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile csrc/gemm_f16.cu into libgemm_f16.so next to this file."""
+    """Compile csrc/gemm_f16.cu and csrc/gdn.cu (in parallel) and link libgemm_f16.so next to
+    this file."""
     if not force and not is_stale():
         return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *NVCC_FLAGS, "-o", tmp, os.path.join(CSRC, "gemm_f16.cu")]
+    tag = f"tmp{os.getpid()}"
+    compile_flags = [f for f in NVCC_FLAGS if f != "-shared"]
+    procs, objs = [], []
+    for src in SOURCES:
+        obj = os.path.join(PKG_DIR, f".{os.path.splitext(src)[0]}.{tag}.o")
+        cmd = [_nvcc(), *compile_flags, "-c", "-o", obj, os.path.join(CSRC, src)]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append(subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE,
+                                      text=True))
+        objs.append(obj)
+    errors, logs = [], []
+    for p in procs:
+        out, err = p.communicate()
+        logs.append(out + err)
+        if p.returncode != 0:
+            errors.append(f"nvcc failed ({p.returncode}):\n{out}\n{err}")
+    try:
+        if errors:
+            raise RuntimeError("\n".join(errors))
+        tmp = LIB_PATH + "." + tag
+        res = subprocess.run([_nvcc(), *NVCC_FLAGS, "-o", tmp, *objs], capture_output=True,
+                             text=True)
+        if res.returncode != 0:
+            raise RuntimeError(f"nvcc link failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.unlink(obj)
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({res.returncode}):\n{res.stdout}\n{res.stderr}")
-    if verbose:
-        print(res.stdout + res.stderr)
+        print("".join(logs))
     os.replace(tmp, LIB_PATH)
     return LIB_PATH

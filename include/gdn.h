@@ -1,0 +1,82 @@
+/*
+ * gdn.h -- C ABI of the Gated Delta Net prefill in libgemm_f16.so (GB300, sm_103a).
+ *
+ * The operation (page "TIRx" (zixuwang.me), section "用状态递推解释 GDN"): every sequence and
+ * value head carries a state H of shape [dv, dk].  Token by token:
+ *
+ *     H_decay    = alpha_t * H
+ *     prediction = H_decay k_t
+ *     update     = beta_t * (v_t - prediction)
+ *     H          = H_decay + update k_t^T
+ *     o_t        = scale * H q_t
+ *
+ * The kernels evaluate this recurrence in 64-token chunks (the page's GPU form): per chunk the
+ * decays' running products, the chunk's K K^T and Q K^T, and the triangular solve that turns the
+ * chunk's updates into matrix products; then a scan over each sequence's chunks carries the state
+ * and writes the outputs.  Arithmetic is fp32 throughout; the result differs from the
+ * token-by-token order only by rounding.
+ *
+ * Packed input (same page): the tokens of n_seqs independent sequences lie back to back;
+ * sequence i owns tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 and its own state.  The host never
+ * reads cu_seqlens: it is a device array the kernels consult.
+ *
+ * Heads: q and k have h_qk heads; v, alpha, beta, the states and o have h_v heads, a multiple of
+ * h_qk.  Value head j reads query/key head j / (h_v / h_qk): h_v == h_qk is multi-head attention,
+ * h_v > h_qk grouped values (GVA).
+ *
+ * Layouts (row-major, device memory of the current device):
+ *   q, k           bfloat16 [total_tokens][h_qk][head_dim]
+ *   v              bfloat16 [total_tokens][h_v][head_dim]
+ *   alpha, beta    float    [total_tokens][h_v]     alpha in (0, 1]; beta any real
+ *   cu_seqlens     int32    [n_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
+ *                                     cu_seqlens[n_seqs] = total_tokens
+ *   initial_state  float    [n_seqs][h_v][head_dim (dv)][head_dim (dk)], or NULL for zeros
+ *   o              bfloat16 [total_tokens][h_v][head_dim]   (written)
+ *   final_state    float    [n_seqs][h_v][dv][dk], or NULL   (written)
+ *   workspace      gdn_prefill_workspace_bytes() bytes, 16-byte aligned
+ *
+ * The chunked form divides running products of alpha within a chunk, so every alpha must be
+ * positive and the product of 64 consecutive alphas of a sequence must stay a normal fp32 number
+ * (above 1e-37); alpha = 0, a full reset, is outside this routine's domain.
+ *
+ * Ownership: the caller owns every buffer; nothing is retained after a call.  Asynchronous on
+ * `stream`.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, h_v not a multiple of
+ * h_qk, workspace too small), GDN_ERR_UNSUPPORTED (head_dim other than 128, misaligned
+ * q/k/v/o), GDN_ERR_CUDA (a launch failed; gdn_last_error() says why).  Nothing is enqueued on an
+ * error.  n_seqs == 0 does nothing.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_OK 0
+#define GDN_ERR_INVALID_ARG 1
+#define GDN_ERR_UNSUPPORTED 2
+#define GDN_ERR_CUDA 3
+
+/* Workspace bytes gdn_prefill needs for these sizes (an upper bound over all packings). */
+int gdn_prefill_workspace_bytes(int64_t total_tokens, int64_t n_seqs, int64_t h_v,
+                                size_t* bytes);
+
+/* The gated delta rule over packed sequences, as above. */
+int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
+                const float* beta, const int32_t* cu_seqlens, int64_t n_seqs,
+                int64_t total_tokens, int64_t h_qk, int64_t h_v, int64_t head_dim, float scale,
+                const float* initial_state, void* o, float* final_state, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream);
+
+/* The message of the calling thread's last failed gdn_* call ("" if none). */
+const char* gdn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

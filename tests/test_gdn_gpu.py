@@ -1,0 +1,162 @@
+"""Parity of the Gated Delta Net prefill (gdn_prefill) with the CPU oracle (needs a GB300).
+
+Each case runs the C ABI on seeded inputs (workloads.make_gdn_inputs) and compares the bfloat16
+outputs and the fp32 final states with the oracle's token-by-token binary64 recurrence.
+
+Bounds, from the arithmetic.  The kernels compute in fp32 (unit roundoff 2^-24) in 64-token
+chunks; each chunk adds rounding from sums of at most dk + 64 terms, and the state recurrence
+is contractive for unit keys, 0 <= beta <= 1, 0 < alpha <= 1, so chunk errors add up at most
+linearly over a sequence's n chunks.  With M the sequence's largest |o_ref| (largest |S_ref| for
+the state):
+    |o - o_ref| <= 2^-7 |o_ref| + n (dk + 64) 2^-22 M         (2^-7: twice bf16's half-ulp)
+    |S - S_ref| <= 2^-20 |S_ref| + n (dk + 64) 2^-22 M
+and, over a whole call, the root-mean-square error is at most 2^-8 of the RMS output (bfloat16
+rounding alone gives about 0.58 * 2^-8) and 2^-14 of the RMS state: a mistake that shifts a
+decay or drops a term fails these long before the elementwise bounds.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import blackwell_tensor_core_fp16_gb300 as g
+import oracle
+from blackwell_tensor_core_fp16_gb300.workloads import (GDN_WORKLOADS, gdn_workload_inputs,
+                                                         make_gdn_inputs)
+
+pytestmark = pytest.mark.gpu
+C = 64
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_library():
+    if not torch.cuda.is_available():
+        pytest.fail("the gpu tests need a CUDA device")
+    g.build()
+    g.load()
+    torch.cuda.init()
+
+
+def run(inp, h_qk, h_v, scale=0.73, want_state=True):
+    """gdn_prefill through the C ABI; outputs written into NaN-prefilled buffers."""
+    q, k, v = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda()
+    a, b = inp["alpha"].cuda(), inp["beta"].cuda()
+    cu = inp["cu_seqlens"].cuda()
+    s0 = None if inp["initial_state"] is None else inp["initial_state"].cuda()
+    T, _, d = q.shape
+    n = cu.numel() - 1
+    o = torch.full((T, h_v, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sf = torch.full((n, h_v, d, d), float("nan"), dtype=torch.float32, device="cuda") \
+        if want_state else None
+    need = g.gdn_prefill_workspace_bytes(T, n, h_v)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    rc = g.gdn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), a.data_ptr(), b.data_ptr(),
+                       cu.data_ptr(), n, T, h_qk, h_v, d, scale,
+                       0 if s0 is None else s0.data_ptr(), o.data_ptr(),
+                       0 if sf is None else sf.data_ptr(), ws.data_ptr(), need,
+                       torch.cuda.current_stream().cuda_stream)
+    assert rc == g.GDN_OK, g.gdn_last_error()
+    torch.cuda.synchronize()
+    return o.float().cpu().double().numpy(), (None if sf is None else sf.cpu().double().numpy())
+
+
+def assert_parity(inp, o, sf, scale, where):
+    ref_o, ref_s = oracle.gdn_f64(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"],
+                                  inp["cu_seqlens"], scale, inp["initial_state"])
+    cu = inp["cu_seqlens"].numpy()
+    assert np.isfinite(o).all(), f"{where}: an output was not written"
+    dk = inp["q"].shape[2]
+    for i in range(len(cu) - 1):
+        sl = slice(cu[i], cu[i + 1])
+        n = max(1, -(-(cu[i + 1] - cu[i]) // C))
+        ro = ref_o[sl]
+        if ro.size == 0:
+            continue
+        M = np.abs(ro).max(axis=(0, 2), keepdims=True)     # per value head
+        tol = 2.0 ** -7 * np.abs(ro) + n * (dk + C) * 2.0 ** -22 * M
+        err = np.abs(o[sl] - ro)
+        if (err > tol).any():
+            idx = np.argwhere(err > tol)[:4]
+            pytest.fail(f"{where}: sequence {i}: {int((err > tol).sum())} outputs out of bound, "
+                        f"worst err/tol {float((err / tol).max()):.3f}, first at {idx.tolist()}")
+        if sf is not None:
+            rs = ref_s[i]
+            Ms = np.abs(rs).max(axis=(1, 2), keepdims=True)
+            tols = 2.0 ** -20 * np.abs(rs) + n * (dk + C) * 2.0 ** -22 * Ms
+            errs = np.abs(sf[i] - rs)
+            assert (errs <= tols).all(), \
+                f"{where}: sequence {i}: state worst err/tol {float((errs / tols).max()):.3f}"
+    rms = lambda x: float(np.sqrt(np.mean(np.square(x)))) if x.size else 0.0
+    if ref_o.size:
+        assert rms(o - ref_o) <= 2.0 ** -8 * rms(ref_o), \
+            f"{where}: output RMS error {rms(o - ref_o) / rms(ref_o):.2e} of the RMS output"
+    if sf is not None and ref_s.size:
+        assert rms(sf - ref_s) <= 2.0 ** -14 * rms(ref_s), \
+            f"{where}: state RMS error {rms(sf - ref_s) / rms(ref_s):.2e} of the RMS state"
+
+
+@pytest.mark.parametrize("name", list(GDN_WORKLOADS))
+def test_page_scenarios(name):
+    w = GDN_WORKLOADS[name]
+    inp = gdn_workload_inputs(w)
+    o, sf = run(inp, w.h_qk, w.h_v, w.scale, want_state=w.state)
+    assert_parity(inp, o, sf, w.scale, name)
+
+
+SHAPES = [
+    # (T, n_seqs, h_qk, h_v, initial state)
+    (1, 1, 1, 1, False),       # one token
+    (7, 1, 2, 2, True),        # one short chunk
+    (64, 1, 1, 1, True),       # exactly one chunk
+    (65, 1, 1, 2, True),       # one chunk and one token, grouped values
+    (200, 1, 2, 2, False),     # three chunks and a tail
+    (300, 5, 2, 4, True),      # packed, ragged, grouped values
+    (130, 3, 1, 1, True),      # packed with chunk-boundary-crossing lengths
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_shapes(shape):
+    T, n, h_qk, h_v, st = shape
+    inp = make_gdn_inputs(T, n, h_qk, h_v, 128, 128, seed=300 + T + n, state=st)
+    o, sf = run(inp, h_qk, h_v)
+    assert_parity(inp, o, sf, 0.73, f"{shape}")
+
+
+def test_empty_sequences_keep_their_state():
+    inp = make_gdn_inputs(100, 1, 1, 1, 128, 128, seed=9, state=True)
+    # sequences of lengths 0, 40, 0, 60, 0 over the same 100 tokens
+    inp["cu_seqlens"] = torch.tensor([0, 0, 40, 40, 100, 100], dtype=torch.int32)
+    inp["initial_state"] = 0.1 * torch.randn((5, 1, 128, 128), generator=torch.Generator().manual_seed(3))
+    o, sf = run(inp, 1, 1)
+    assert_parity(inp, o, sf, 0.73, "empty sequences")
+    s0 = inp["initial_state"].double().numpy()
+    for i in (0, 2, 4):
+        assert np.array_equal(sf[i], s0[i]), f"empty sequence {i} changed its state"
+
+
+def test_deterministic():
+    inp = make_gdn_inputs(300, 3, 2, 4, 128, 128, seed=10, state=True)
+    o1, s1 = run(inp, 2, 4)
+    o2, s2 = run(inp, 2, 4)
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+
+
+def test_rejects_bad_arguments():
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    p = x.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(h_qk=1, h_v=1, d=128, n=1, T=4, wsb=1 << 20, qptr=p):
+        return g.gdn_prefill(qptr, p, p, p, p, p, n, T, h_qk, h_v, d, 1.0, 0, p, 0,
+                             ws.data_ptr(), wsb, s)
+
+    assert call(h_qk=2, h_v=3) == g.GDN_ERR_INVALID_ARG      # h_v not a multiple of h_qk
+    assert call(d=64) == g.GDN_ERR_UNSUPPORTED               # head dim other than 128
+    assert call(qptr=p + 2) == g.GDN_ERR_UNSUPPORTED         # misaligned q
+    assert call(wsb=16) == g.GDN_ERR_INVALID_ARG             # workspace too small
+    assert call(n=-1) == g.GDN_ERR_INVALID_ARG
+    assert call(n=0) == g.GDN_OK                             # nothing to do
+    torch.cuda.synchronize()
