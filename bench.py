@@ -68,6 +68,8 @@ def parse_args():
     p.add_argument("--mx-steps", type=int, default=200,
                    help="steps of the block-scaled FP8 leg (8192^3 and MLP shapes; 0: skip)")
     p.add_argument("--mx-variant", type=int, default=0, help="block-scaled variant (0 = auto)")
+    p.add_argument("--gdn-reps", type=int, default=20,
+                   help="timed calls per Gated Delta Net scenario (0: skip the leg)")
     p.add_argument("--sweep-mx", action="store_true",
                    help="in --sweep, time the block-scaled FP8 workloads instead")
     p.add_argument("--cublas-steps", type=int, default=-1,
@@ -370,6 +372,70 @@ def run_mx_leg(args, g, dev, stream, num_sms, peak16, uuid):
             "gpu_launches": K * len(work)}
 
 
+# ---- Gated Delta Net prefill leg -------------------------------------------------------------------
+
+# The page's own CUDA-event times of its public callable on an H20-3e (sm_90a), for context only:
+# another machine, another implementation ("TIRx" (zixuwang.me), "公开版本复测：六个场景").
+GDN_PAGE_H20_MS = {
+    "single_t512_h8_mha_zero": 0.102550, "single_t1024_h8_mha_state": 0.157430,
+    "single_t1024_h8_hv16_gva_state": 0.143251, "single_t4096_h16_mha_zero": 0.263054,
+    "packed_n10_t4096_h8_mha_state": 0.173384, "packed_n20_t8192_h8_hv16_gva_state": 0.520107,
+}
+
+
+def run_gdn_leg(args, g, dev, stream):
+    """Every scenario of the page: inputs resident, the workspace allocated once, CUDA events
+    around `gdn_reps` back-to-back calls after 3 warm-up calls."""
+    import torch
+    from blackwell_tensor_core_fp16_gb300.workloads import GDN_ORDER, GDN_WORKLOADS, \
+        gdn_workload_inputs
+    out = {}
+    for name in GDN_ORDER:
+        w = GDN_WORKLOADS[name]
+        inp = gdn_workload_inputs(w)
+        q, k, v = (inp[x].to(dev) for x in ("q", "k", "v"))
+        a, b, cu = inp["alpha"].to(dev), inp["beta"].to(dev), inp["cu_seqlens"].to(dev)
+        s0 = None if inp["initial_state"] is None else inp["initial_state"].to(dev)
+        n = cu.numel() - 1
+        o = torch.empty((w.T, w.h_v, w.dv), dtype=torch.bfloat16, device=dev)
+        sf = torch.empty((n, w.h_v, w.dv, w.dk), dtype=torch.float32, device=dev) if w.state \
+            else None
+        need = g.gdn_prefill_workspace_bytes(w.T, n, w.h_v)
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+
+        def call():
+            rc = g.gdn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), a.data_ptr(),
+                               b.data_ptr(), cu.data_ptr(), n, w.T, w.h_qk, w.h_v, w.dk, w.scale,
+                               0 if s0 is None else s0.data_ptr(), o.data_ptr(),
+                               0 if sf is None else sf.data_ptr(), ws.data_ptr(), need,
+                               stream.cuda_stream)
+            if rc != g.GDN_OK:
+                raise g.GemmError(rc, g.gdn_last_error())
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.gdn_reps):
+                call()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.gdn_reps
+        out[name] = {"ms": ms, "tokens_per_s": w.T / (ms * 1e-3),
+                     "recurrence_tflops": w.flops / (ms * 1e-3) / 1e12,
+                     "page_h20_ms_context": GDN_PAGE_H20_MS.get(name)}
+    return {"metric": "Gated Delta Net prefill: ms per call (bf16 q/k/v, head dim 128)",
+            "unit": "ms", "higher_is_better": False, "reps": args.gdn_reps,
+            "scenarios": out,
+            "gpu_launches_per_call": 3,
+            "note": "recurrence_tflops counts 6*T*h_v*dk*dv (prediction, rank-one update, "
+                    "output) per call; page_h20_ms_context is the page's own time on another "
+                    "machine"}
+
+
 # ---- our arm ---------------------------------------------------------------------------------
 
 def run_ours(args):
@@ -621,6 +687,7 @@ def run_ours(args):
     mx_leg = None
     if args.mx_steps > 0:
         mx_leg = run_mx_leg(args, g, dev, stream, num_sms, peak, uuid)
+    gdn_leg = run_gdn_leg(args, g, dev, stream) if args.gdn_reps > 0 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -659,6 +726,7 @@ def run_ours(args):
                         "neighbouring steps overlap the GEMMs"},
         "gpu_launches": K * len(work),
         "mx_fp8": mx_leg,
+        "gdn_prefill": gdn_leg,
         "clocks": clock_info,
         "wall_s_timed_region": wall_s,
     }
