@@ -36,7 +36,6 @@ namespace {
 constexpr int kC = 64;          // tokens per chunk
 constexpr int kD = 128;         // head dimension (dk = dv)
 constexpr int kRows = 16;       // value rows of the state per scan CTA
-constexpr int kPad = kD + 1;    // padded row length of [64][128] tiles in shared memory
 
 thread_local std::string t_gdn_error;
 
@@ -119,32 +118,39 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
     }
 }
 
-__device__ __forceinline__ void load_row_bf16(float* dst, const __nv_bfloat16* src, bool valid,
-                                              int lane16)
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_at(const __nv_bfloat16* p)
 {
-    // 128 bf16 = 16 x 16 bytes; lane16 = 0..15 loads one 16-byte piece
-    float f[8];
-    if (valid) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + lane16);
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            f[2 * i] = __uint_as_float(u[i] << 16);
-            f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) dst[lane16 * 8 + i] = f[i];
+    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
 }
 
-// ---- per (chunk, value head): W^T, U'^T, A^T and the cumulative decays ----------------------
-constexpr int kPrepThreads = 256;
-constexpr size_t kPrepSmem = sizeof(float) * (3 * kC * kPad + 2 * kC * (kC + 1) + 3 * kC);
+// 16-byte global -> shared copy that completes asynchronously; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, uint32_t src_bytes)
+{
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kPrepThreads, 1)
+// Rows of 128 bf16 in shared memory are padded to 136 elements (272 bytes): rows 16 apart then
+// start 4 banks apart, so the strided tiles below read them without bank conflicts.
+constexpr int kRowB = 136;
+
+// ---- per (chunk, value head): W^T, U'^T, A^T and the cumulative decays ----------------------
+// K, Q, V of the chunk sit in shared memory as padded bf16 rows.  Products K K^T and Q K^T are
+// register-tiled (each thread 4 x 4 entries, rows and columns 16 apart).  Then (I + L) X = R
+// is solved for the 256 right-hand-side columns R = [diag(beta g) K | diag(beta) V] by forward
+// substitution, one column per thread with the column held in registers: no inverse is formed
+// and no barrier is needed inside the solve.
+constexpr int kPrepThreads = 256;
+constexpr size_t kPrepSmem =
+    sizeof(__nv_bfloat16) * 3 * kC * kRowB + sizeof(float) * (kC * kC + kC * (kC + 1) + 4 * kC);
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
     gdn_prepare_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                        const __nv_bfloat16* __restrict__ v, const float* __restrict__ alpha,
                        const float* __restrict__ beta, const int4* __restrict__ chunks,
@@ -158,26 +164,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     const int4 info = chunks[ch];
     const int32_t t0 = info.y, len = info.z;
     const int32_t jq = j / (h_v / h_qk);
-    extern __shared__ float sm[];
-    float* Ks = sm;                       // [64][129]
-    float* Qs = Ks + kC * kPad;           // [64][129]
-    float* Vs = Qs + kC * kPad;           // [64][129]
-    float* Ls = Vs + kC * kPad;           // [64][65]  L (strictly lower)
-    float* Ts = Ls + kC * (kC + 1);       // [64][65]  T = (I + L)^-1
-    float* g = Ts + kC * (kC + 1);        // [64] cumulative decay
-    float* bt = g + kC;                   // [64] beta
-    float* al = bt + kC;                  // [64] alpha
+    extern __shared__ __align__(16) uint8_t smraw[];
+    __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(smraw);   // [64][136]
+    __nv_bfloat16* Qb = Kb + kC * kRowB;
+    __nv_bfloat16* Vb = Qb + kC * kRowB;
+    float* Ls = reinterpret_cast<float*>(Vb + kC * kRowB);          // [64][64] L, strictly lower
+    float* As = Ls + kC * kC;                                         // [64 s][65] A transposed
+    float* g = As + kC * (kC + 1);
+    float* bt = g + kC;
+    float* bg = bt + kC;
+    float* al = bg + kC;
     const int tid = threadIdx.x;
 
-    // rows of K, Q, V: 16 threads per row, 4 rows per pass of 64 threads ... 16 passes of 256
     for (int idx = tid; idx < kC * 16; idx += kPrepThreads) {
         const int t = idx / 16, p = idx % 16;
         const bool valid = t < len;
-        const int64_t tok = static_cast<int64_t>(t0) + t;
-        load_row_bf16(Ks + t * kPad, k + (tok * h_qk + jq) * kD, valid, p);
-        load_row_bf16(Qs + t * kPad, q + (tok * h_qk + jq) * kD, valid, p);
-        load_row_bf16(Vs + t * kPad, v + (tok * h_v + j) * kD, valid, p);
+        const int64_t tok = static_cast<int64_t>(t0) + (valid ? t : 0);
+        const uint32_t nb = valid ? 16u : 0u;
+        cp_async16(Kb + t * kRowB + p * 8, k + (tok * h_qk + jq) * kD + p * 8, nb);
+        cp_async16(Qb + t * kRowB + p * 8, q + (tok * h_qk + jq) * kD + p * 8, nb);
+        cp_async16(Vb + t * kRowB + p * 8, v + (tok * h_v + j) * kD + p * 8, nb);
     }
+    cp_async_commit();
     if (tid < kC) {
         const bool valid = tid < len;
         const int64_t tok = static_cast<int64_t>(t0) + tid;
@@ -185,78 +193,167 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         bt[tid] = valid ? beta[tok * h_v + j] : 0.f;
     }
     __syncthreads();
-    if (tid == 0) {
-        float p = 1.f;
-        for (int t = 0; t < kC; ++t) {
-            p *= al[t];
-            g[t] = p;
+    if (tid < 32) {
+        // running products of alpha: each lane multiplies two, then a warp product scan
+        float a0 = al[2 * tid], a1 = al[2 * tid + 1];
+        float p = a0 * a1;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, p, d);
+            if (tid >= d) p *= o;
         }
+        float before = __shfl_up_sync(0xffffffffu, p, 1);
+        if (tid == 0) before = 1.f;
+        g[2 * tid] = before * a0;
+        g[2 * tid + 1] = p;
     }
+    cp_async_wait_all();
     __syncthreads();
+    if (tid < kC) bg[tid] = bt[tid] * g[tid];
 
-    // L = strictly lower part of diag(beta) (g_t / g_s) K K^T; A^T[s][t] = (g_t / g_s) q_t . k_s
-    float* atc = at + (static_cast<int64_t>(ch) * h_v + j) * kC * kC;
-    for (int idx = tid; idx < kC * kC; idx += kPrepThreads) {
-        const int t = idx / kC, s = idx % kC;
-        float kk = 0.f, qk = 0.f;
-        if (s <= t) {
-            const float* kt = Ks + t * kPad;
-            const float* qt = Qs + t * kPad;
-            const float* ks = Ks + s * kPad;
-#pragma unroll 8
-            for (int c = 0; c < kD; ++c) {
-                kk = fmaf(kt[c], ks[c], kk);
-                qk = fmaf(qt[c], ks[c], qk);
-            }
-        }
-        const float ratio = s <= t ? g[t] / g[s] : 0.f;
-        Ls[t * (kC + 1) + s] = s < t ? bt[t] * ratio * kk : 0.f;
-        atc[s * kC + t] = ratio * qk;
-    }
-    __syncthreads();
-
-    // T = (I + L)^-1 by forward substitution, one row at a time (row t needs rows < t)
-    for (int t = 0; t < kC; ++t) {
-        if (tid < kC) {
-            const int s = tid;
-            float x = 0.f;
-            if (s < t) {
-                for (int m = s; m < t; ++m) x = fmaf(Ls[t * (kC + 1) + m], Ts[m * (kC + 1) + s], x);
-                x = -x;
-            } else if (s == t) {
-                x = 1.f;
-            }
-            Ts[t * (kC + 1) + s] = x;
-        }
-        __syncthreads();
-    }
-
-    // W^T[c][t] = sum_{s<=t} T[t][s] beta_s g_s K[s][c];  U'^T[c][t] = sum_{s<=t} T[t][s] beta_s V[s][c]
+    // K K^T and Q K^T: thread tile rows t = tt + 16 i, columns s = st + 16 jj
     {
-        const int t = tid % kC;
-        const int cg = tid / kC;                  // 4 groups of 32 columns
-        float* wtc = wt + (static_cast<int64_t>(ch) * h_v + j) * kD * kC;
-        float* utc = ut + (static_cast<int64_t>(ch) * h_v + j) * kD * kC;
-        for (int cc = 0; cc < 32; ++cc) {
-            const int c = cg * 32 + cc;
-            float w = 0.f, u = 0.f;
-            for (int s = 0; s <= t; ++s) {
-                const float ts = Ts[t * (kC + 1) + s] * bt[s];
-                w = fmaf(ts * g[s], Ks[s * kPad + c], w);
-                u = fmaf(ts, Vs[s * kPad + c], u);
+        const int tt = tid / 16, st = tid % 16;
+        float kk[4][4], qk[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) kk[i][jj] = qk[i][jj] = 0.f;
+        for (int d = 0; d < kD; d += 8) {
+            uint4 kt[4], qt[4], ks[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                kt[i] = *reinterpret_cast<const uint4*>(Kb + (tt + 16 * i) * kRowB + d);
+                qt[i] = *reinterpret_cast<const uint4*>(Qb + (tt + 16 * i) * kRowB + d);
+                ks[i] = *reinterpret_cast<const uint4*>(Kb + (st + 16 * i) * kRowB + d);
             }
-            wtc[c * kC + t] = w;
-            utc[c * kC + t] = u;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float a[4], b[4], c[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t ka = (&kt[i].x)[w], qa = (&qt[i].x)[w], kb = (&ks[i].x)[w];
+                        a[i] = h ? bf16_hi(ka) : bf16_lo(ka);
+                        b[i] = h ? bf16_hi(qa) : bf16_lo(qa);
+                        c[i] = h ? bf16_hi(kb) : bf16_lo(kb);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj) {
+                            kk[i][jj] = fmaf(a[i], c[jj], kk[i][jj]);
+                            qk[i][jj] = fmaf(b[i], c[jj], qk[i][jj]);
+                        }
+                }
+            }
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = tt + 16 * i;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int s = st + 16 * jj;
+                const float ratio = s <= t ? g[t] / g[s] : 0.f;
+                Ls[t * kC + s] = s < t ? bt[t] * ratio * kk[i][jj] : 0.f;
+                As[s * (kC + 1) + t] = ratio * qk[i][jj];
+            }
+        }
+    }
+    __syncthreads();
+
+    // A^T to global, coalesced
+    {
+        float* atc = at + (static_cast<int64_t>(ch) * h_v + j) * kC * kC;
+        for (int e = tid; e < kC * kC; e += kPrepThreads)
+            atc[e] = As[(e / kC) * (kC + 1) + e % kC];
+    }
+
+    // (I + L) X = R by forward substitution, one right-hand-side column per thread
+    {
+        const bool isw = tid < kD;
+        const int col = tid & (kD - 1);
+        const __nv_bfloat16* src = isw ? Kb : Vb;
+        const float* sc = isw ? bg : bt;
+        float x[kC];
+#pragma unroll
+        for (int t = 0; t < kC; ++t) {
+            float acc[4] = {sc[t] * bf16_at(src + t * kRowB + col), 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s4 = 0; s4 < (t & ~3); s4 += 4) {
+                const float4 l = *reinterpret_cast<const float4*>(Ls + t * kC + s4);
+                acc[0] = fmaf(-l.x, x[s4], acc[0]);
+                acc[1] = fmaf(-l.y, x[s4 + 1], acc[1]);
+                acc[2] = fmaf(-l.z, x[s4 + 2], acc[2]);
+                acc[3] = fmaf(-l.w, x[s4 + 3], acc[3]);
+            }
+#pragma unroll
+            for (int s = t & ~3; s < t; ++s) acc[0] = fmaf(-Ls[t * kC + s], x[s], acc[0]);
+            x[t] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+        float* dst = (isw ? wt : ut) + ((static_cast<int64_t>(ch) * h_v + j) * kD + col) * kC;
+#pragma unroll
+        for (int t = 0; t < kC; t += 4)
+            *reinterpret_cast<float4*>(dst + t) = make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
     }
     if (tid < kC) gam_out[(static_cast<int64_t>(ch) * h_v + j) * kC + tid] = g[tid];
 }
 
 // ---- per (sequence, value head, block of 16 value rows): the state scan over the chunks -----
-constexpr int kScanThreads = 128;
-constexpr size_t kScanSmem =
-    sizeof(float) * (kRows * kD + kD * kC + kC * kC + 2 * kRows * kC + kD * (kC + 1) + kC * kD +
-                     2 * kC);
+// The chunk's inputs are double-buffered: while chunk c is computed, cp.async brings chunk
+// c + 1 (W^T, A^T, the block's U'^T rows, decays, and q/k as padded bf16 rows).  The three
+// products are register-tiled, 4 tokens (or 4 state columns) x 4 state rows per thread, with
+// the reduction split over 4 (or 2) thread groups whose partial sums meet in shared memory:
+// every operand is one 16-byte load per 16 multiply-adds.  The state and U are kept transposed
+// ([c][r], [s][r]) so their rows of 4 are contiguous.
+constexpr int kScanThreads = 256;
+struct ScanBuf {
+    float wt[kD * kC];             // W^T [c][t]
+    float at[kC * kC];             // A^T [s][t]
+    float up[kRows * kC];          // U'^T rows r0 .. r0+15, [r][t]
+    float g[kC];
+    __nv_bfloat16 qb[kC * kRowB];  // q rows, padded
+    __nv_bfloat16 kb[kC * kRowB];  // k rows, padded
+};
+constexpr size_t kScanSmem = 2 * sizeof(ScanBuf) +
+                             sizeof(float) * (kD * kRows + kC * kRows + kC + 4 * kC * kRows) +
+                             sizeof(__nv_bfloat16) * kD * kC;
+
+__device__ __forceinline__ void scan_prefetch(ScanBuf& b, const __nv_bfloat16* __restrict__ q,
+                                              const __nv_bfloat16* __restrict__ k,
+                                              const float* __restrict__ wt,
+                                              const float* __restrict__ ut,
+                                              const float* __restrict__ at,
+                                              const float* __restrict__ gam, int64_t cj,
+                                              int32_t r0, int32_t t0, int32_t len, int32_t h_qk,
+                                              int32_t jq, int tid)
+{
+    const float* w = wt + cj * kD * kC;
+    for (int e = tid; e < kD * kC / 4; e += kScanThreads) cp_async16(b.wt + 4 * e, w + 4 * e, 16);
+    const float* a = at + cj * kC * kC;
+    for (int e = tid; e < kC * kC / 4; e += kScanThreads) cp_async16(b.at + 4 * e, a + 4 * e, 16);
+    const float* u = ut + (cj * kD + r0) * kC;
+    for (int e = tid; e < kRows * kC / 4; e += kScanThreads) cp_async16(b.up + 4 * e, u + 4 * e, 16);
+    if (tid < kC / 4) cp_async16(b.g + 4 * tid, gam + cj * kC + 4 * tid, 16);
+    for (int idx = tid; idx < kC * 16; idx += kScanThreads) {
+        const int t = idx / 16, p = idx % 16;
+        const bool valid = t < len;
+        const int64_t tok = static_cast<int64_t>(t0) + (valid ? t : 0);
+        cp_async16(b.qb + t * kRowB + p * 8, q + (tok * h_qk + jq) * kD + p * 8, valid ? 16u : 0u);
+        cp_async16(b.kb + t * kRowB + p * 8, k + (tok * h_qk + jq) * kD + p * 8, valid ? 16u : 0u);
+    }
+    cp_async_commit();
+}
+
+__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const float4 b)
+{
+    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[i][r] = fmaf(av[i], bv[r], acc[i][r]);
+}
 
 __global__ void __launch_bounds__(kScanThreads, 1)
     gdn_scan_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
@@ -270,134 +367,151 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const int32_t j = blockIdx.y;
     const int32_t r0 = blockIdx.z * kRows;
     const int32_t jq = j / (h_v / h_qk);
-    extern __shared__ float sm[];
-    float* S = sm;                        // [16][128] state rows r0 .. r0+15
-    float* Wt = S + kRows * kD;           // [128][64]
-    float* At = Wt + kD * kC;             // [64 s][64 t]
-    float* Up = At + kC * kC;             // [16][64]  U' rows
-    float* U = Up + kRows * kC;           // [16][64]  U rows
-    float* Qt = U + kRows * kC;           // [128][65] Q transposed
-    float* Kc = Qt + kD * (kC + 1);       // [64][128]
-    float* g = Kc + kC * kD;              // [64]
-    float* kf = g + kC;                   // [64] g_C / g_s
+    extern __shared__ __align__(16) uint8_t smraw[];
+    ScanBuf* buf = reinterpret_cast<ScanBuf*>(smraw);
+    float* St = reinterpret_cast<float*>(buf + 2);  // state transposed [c][r], 128 x 16
+    float* Ut = St + kD * kRows;                    // U transposed [s][r], 64 x 16
+    float* kf = Ut + kC * kRows;                    // [64] g_C / g_s
+    float* P = kf + kC;                             // partial sums [4][64][16]
+    __nv_bfloat16* Qt = reinterpret_cast<__nv_bfloat16*>(P + 4 * kC * kRows);   // [c][t] bf16
     const int tid = threadIdx.x;
 
     const int64_t sbase = ((static_cast<int64_t>(i) * h_v + j) * kD + r0) * kD;
-    for (int e = tid; e < kRows * kD; e += kScanThreads) S[e] = s0 ? s0[sbase + e] : 0.f;
+    for (int e = tid; e < kRows * kD; e += kScanThreads)
+        St[(e % kD) * kRows + e / kD] = s0 ? s0[sbase + e] : 0.f;
 
     const int32_t c_begin = chunk_offset[i], c_end = chunk_offset[i + 1];
-    const int32_t seq_start = cu[i];
+    const int32_t seq_start = cu[i], seq_end = cu[i + 1];
+    const auto chunk_t0 = [&](int32_t ch) { return seq_start + (ch - c_begin) * kC; };
+    if (c_begin < c_end)
+        scan_prefetch(buf[0], q, k, wt, ut, at, gam, static_cast<int64_t>(c_begin) * h_v + j, r0,
+                      chunk_t0(c_begin), min(kC, seq_end - chunk_t0(c_begin)), h_qk, jq, tid);
+    // U and O tiles: tokens 4 tt .. 4 tt + 3, rows 4 tr .. 4 tr + 3, reduction quarter tq
+    const int tt = tid % 16, tr = (tid / 16) % 4, tq = tid / 64;
+    // update tiles: columns 4 uc .. 4 uc + 3, rows 4 ur .. 4 ur + 3, reduction half uh
+    const int uc = tid % 32, ur = (tid / 32) % 4, uh = tid / 128;
+    // the reduce step: 4 consecutive (t, r) outputs per thread
+    const int oe = 4 * tid;                          // output index t * 16 + r .. + 3
+    const int ot = oe / kRows, orr = oe % kRows;
     for (int32_t ch = c_begin; ch < c_end; ++ch) {
-        const int32_t t0 = seq_start + (ch - c_begin) * kC;
-        const int32_t len = min(kC, cu[i + 1] - t0);
-        __syncthreads();   // the previous chunk's readers are done with the tiles
-        const int64_t cj = static_cast<int64_t>(ch) * h_v + j;
-        {
-            const float4* src = reinterpret_cast<const float4*>(wt + cj * kD * kC);
-            for (int e = tid; e < kD * kC / 4; e += kScanThreads)
-                reinterpret_cast<float4*>(Wt)[e] = __ldg(src + e);
-            const float4* asrc = reinterpret_cast<const float4*>(at + cj * kC * kC);
-            for (int e = tid; e < kC * kC / 4; e += kScanThreads)
-                reinterpret_cast<float4*>(At)[e] = __ldg(asrc + e);
-            const float4* usrc = reinterpret_cast<const float4*>(ut + (cj * kD + r0) * kC);
-            for (int e = tid; e < kRows * kC / 4; e += kScanThreads)
-                reinterpret_cast<float4*>(Up)[e] = __ldg(usrc + e);
-            if (tid < kC) g[tid] = __ldg(gam + cj * kC + tid);
-        }
-        for (int idx = tid; idx < kC * 16; idx += kScanThreads) {
-            const int t = idx / 16, p = idx % 16;
-            const bool valid = t < len;
-            const int64_t tok = static_cast<int64_t>(t0) + t;
-            float f[8];
-            const __nv_bfloat16* qsrc = q + (tok * h_qk + jq) * kD;
-            const __nv_bfloat16* ksrc = k + (tok * h_qk + jq) * kD;
-            if (valid) {
-                const uint4 w = __ldg(reinterpret_cast<const uint4*>(qsrc) + p);
-                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+        const int b = (ch - c_begin) & 1;
+        const int32_t t0 = chunk_t0(ch);
+        const int32_t len = min(kC, seq_end - t0);
+        cp_async_wait_all();
+        __syncthreads();   // chunk ch has landed; everyone is done with the other buffer
+        if (ch + 1 < c_end)
+            scan_prefetch(buf[b ^ 1], q, k, wt, ut, at, gam, static_cast<int64_t>(ch + 1) * h_v + j,
+                          r0, chunk_t0(ch + 1), min(kC, seq_end - chunk_t0(ch + 1)), h_qk, jq, tid);
+        const ScanBuf& B = buf[b];
+        if (tid < kC) kf[tid] = B.g[kC - 1] / B.g[tid];
+        for (int idx = tid; idx < kC * 16; idx += kScanThreads) {   // q -> Qt [c][t]
+            const int t = idx % kC, p = idx / kC;
+            const uint4 w = *reinterpret_cast<const uint4*>(B.qb + t * kRowB + p * 8);
+            const uint32_t u4[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    f[2 * e] = __uint_as_float(u[e] << 16);
-                    f[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            for (int e = 0; e < 4; ++e) {
+                Qt[(p * 8 + 2 * e) * kC + t] = __ushort_as_bfloat16(static_cast<uint16_t>(u4[e]));
+                Qt[(p * 8 + 2 * e + 1) * kC + t] =
+                    __ushort_as_bfloat16(static_cast<uint16_t>(u4[e] >> 16));
             }
+        }
+
+        // U = U' - W S^T: partial sums over c in [32 tq, 32 tq + 32)
+        {
+            float acc[4][4] = {};
+#pragma unroll 4
+            for (int c = 32 * tq; c < 32 * tq + 32; ++c)
+                fma4x4(acc, *reinterpret_cast<const float4*>(B.wt + c * kC + 4 * tt),
+                       *reinterpret_cast<const float4*>(St + c * kRows + 4 * tr));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) Qt[(p * 8 + e) * (kC + 1) + t] = f[e];
-            load_row_bf16(Kc + t * kD, ksrc, valid, p);
+            for (int ii = 0; ii < 4; ++ii)
+                *reinterpret_cast<float4*>(P + (tq * kC + 4 * tt + ii) * kRows + 4 * tr) =
+                    make_float4(acc[ii][0], acc[ii][1], acc[ii][2], acc[ii][3]);
         }
         __syncthreads();
-        if (tid < kC) kf[tid] = g[kC - 1] / g[tid];
-
-        // U[r][t] = U'[r][t] - sum_c W[t][c] S[r][c]
-        const int t = tid % kC;
-        const int rg = tid / kC;                  // rows rg*8 .. rg*8+7
         {
-            float acc[8];
+            float4 u;
+            float* uv = &u.x;
 #pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = Up[(rg * 8 + r) * kC + t];
-            for (int c = 0; c < kD; ++c) {
-                const float w = Wt[c * kC + t];
+            for (int e = 0; e < 4; ++e) {
+                float x = B.up[(orr + e) * kC + ot];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) acc[r] = fmaf(-w, S[(rg * 8 + r) * kD + c], acc[r]);
+                for (int qq = 0; qq < 4; ++qq) x -= P[(qq * kC + ot) * kRows + orr + e];
+                uv[e] = x;
             }
+            *reinterpret_cast<float4*>(Ut + ot * kRows + orr) = u;
+        }
+        __syncthreads();   // U and Qt complete
+
+        // O = scale (diag(g) Q S^T + A U): partial sums over c in [32 tq, +32) and s in [16 tq, +16)
+        {
+            float qs[4][4] = {}, au[4][4] = {};
+#pragma unroll 4
+            for (int c = 32 * tq; c < 32 * tq + 32; ++c) {
+                const uint2 w = *reinterpret_cast<const uint2*>(Qt + c * kC + 4 * tt);
+                fma4x4(qs, make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)),
+                       *reinterpret_cast<const float4*>(St + c * kRows + 4 * tr));
+            }
+#pragma unroll 4
+            for (int s = 16 * tq; s < 16 * tq + 16; ++s)   // A[t][s] = 0 for s > t
+                fma4x4(au, *reinterpret_cast<const float4*>(B.at + s * kC + 4 * tt),
+                       *reinterpret_cast<const float4*>(Ut + s * kRows + 4 * tr));
 #pragma unroll
-            for (int r = 0; r < 8; ++r) U[(rg * 8 + r) * kC + t] = acc[r];
+            for (int ii = 0; ii < 4; ++ii) {
+                const float gt = B.g[4 * tt + ii];
+                *reinterpret_cast<float4*>(P + (tq * kC + 4 * tt + ii) * kRows + 4 * tr) =
+                    make_float4(fmaf(gt, qs[ii][0], au[ii][0]), fmaf(gt, qs[ii][1], au[ii][1]),
+                                fmaf(gt, qs[ii][2], au[ii][2]), fmaf(gt, qs[ii][3], au[ii][3]));
+            }
         }
         __syncthreads();
-
-        // O[t][r] = scale (g_t sum_c Q[t][c] S[r][c] + sum_{s<=t} A[t][s] U[r][s])
-        {
-            float qs[8], au[8];
+        if (ot < len) {
+            float x[4];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) qs[r] = au[r] = 0.f;
-            for (int c = 0; c < kD; ++c) {
-                const float qv = Qt[c * (kC + 1) + t];
+            for (int e = 0; e < 4; ++e) {
+                float v = 0.f;
 #pragma unroll
-                for (int r = 0; r < 8; ++r) qs[r] = fmaf(qv, S[(rg * 8 + r) * kD + c], qs[r]);
+                for (int qq = 0; qq < 4; ++qq) v += P[(qq * kC + ot) * kRows + orr + e];
+                x[e] = scale * v;
             }
-            for (int s = 0; s <= t; ++s) {
-                const float a = At[s * kC + t];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) au[r] = fmaf(a, U[(rg * 8 + r) * kC + s], au[r]);
-            }
-            if (t < len) {
-                const int64_t tok = static_cast<int64_t>(t0) + t;
-                __nv_bfloat16* dst = o + (tok * h_v + j) * kD + r0 + rg * 8;
-                uint32_t packed[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x0 = scale * fmaf(g[t], qs[2 * e], au[2 * e]);
-                    const float x1 = scale * fmaf(g[t], qs[2 * e + 1], au[2 * e + 1]);
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-                    packed[e] = *reinterpret_cast<const uint32_t*>(&h);
-                }
-                *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2],
-                                                            packed[3]);
-            }
+            const __nv_bfloat162 h0 = __floats2bfloat162_rn(x[0], x[1]);
+            const __nv_bfloat162 h1 = __floats2bfloat162_rn(x[2], x[3]);
+            *reinterpret_cast<uint2*>(o + ((static_cast<int64_t>(t0) + ot) * h_v + j) * kD + r0 +
+                                      orr) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
+                           *reinterpret_cast<const uint32_t*>(&h1));
         }
-        __syncthreads();   // every reader of S is done before the update
 
-        // H_next[r][c] = g_C H[r][c] + sum_s U[r][s] (g_C / g_s) K[s][c]
+        // S^T_next[c][r] = g_C S^T[c][r] + sum_s (g_C / g_s) K[s][c] U[s][r]: partials over s in
+        // [32 uh, 32 uh + 32)
         {
-            const int c = tid;                    // 128 threads, one column each
-            const float gC = g[kC - 1];
-            float acc[kRows];
-#pragma unroll
-            for (int r = 0; r < kRows; ++r) acc[r] = gC * S[r * kD + c];
-            for (int s = 0; s < kC; ++s) {
-                const float kv = kf[s] * Kc[s * kD + c];
-#pragma unroll
-                for (int r = 0; r < kRows; ++r) acc[r] = fmaf(U[r * kC + s], kv, acc[r]);
+            float acc[4][4] = {};
+#pragma unroll 4
+            for (int s = 32 * uh; s < 32 * uh + 32; ++s) {
+                const uint2 w = *reinterpret_cast<const uint2*>(B.kb + s * kRowB + 4 * uc);
+                const float f = kf[s];
+                fma4x4(acc, make_float4(f * bf16_lo(w.x), f * bf16_hi(w.x), f * bf16_lo(w.y),
+                                        f * bf16_hi(w.y)),
+                       *reinterpret_cast<const float4*>(Ut + s * kRows + 4 * ur));
             }
+            __syncthreads();   // the output reduce has read P
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) S[r * kD + c] = acc[r];
+            for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<float4*>(P + (uh * kD + 4 * uc + cc) * kRows + 4 * ur) =
+                    make_float4(acc[cc][0], acc[cc][1], acc[cc][2], acc[cc][3]);
+        }
+        __syncthreads();
+        {
+            const float gC = B.g[kC - 1];
+            for (int e = tid; e < kD * kRows; e += kScanThreads)
+                St[e] = fmaf(gC, St[e], P[e] + P[kD * kRows + e]);
         }
     }
+    cp_async_wait_all();
     __syncthreads();
     if (s_final)
-        for (int e = tid; e < kRows * kD; e += kScanThreads) s_final[sbase + e] = S[e];
+        for (int e = tid; e < kRows * kD; e += kScanThreads)
+            s_final[sbase + e] = St[(e % kD) * kRows + e / kD];
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
