@@ -303,22 +303,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // ---- per (sequence, value head, block of 16 value rows): the state scan over the chunks -----
 // The chunk's inputs are double-buffered: while chunk c is computed, cp.async brings chunk
 // c + 1 (W^T, A^T, the block's U'^T rows, decays, and q/k as padded bf16 rows).  The three
-// products are register-tiled, 4 tokens (or 4 state columns) x 4 state rows per thread, with
-// the reduction split over 4 (or 2) thread groups whose partial sums meet in shared memory:
-// every operand is one 16-byte load per 16 multiply-adds.  The state and U are kept transposed
-// ([c][r], [s][r]) so their rows of 4 are contiguous.
+// products run on the tensor cores (mma.sync m16n8k8, TF32 inputs, fp32 accumulation), each
+// warp owning 16 x 8 output tiles.  Operands that are fp32 (W, A, the state, U, the decayed
+// keys) are split into a TF32 high part and the TF32 rounding of the rest, and each product
+// takes three passes (hi*hi + hi*lo + lo*hi), which keeps fp32 accuracy; q and k are bfloat16,
+// exact in TF32, so their passes need no split.
 constexpr int kScanThreads = 256;
+constexpr int kRowW = 72;          // padded W^T / A^T rows (floats): fragment loads hit 32 banks
+constexpr int kRowS = 24;          // padded S^T / U^T rows (floats)
 struct ScanBuf {
-    float wt[kD * kC];             // W^T [c][t]
-    float at[kC * kC];             // A^T [s][t]
+    float wt[kD * kRowW];          // W^T [c][t]
+    float at[kC * kRowW];          // A^T [s][t]
     float up[kRows * kC];          // U'^T rows r0 .. r0+15, [r][t]
     float g[kC];
     __nv_bfloat16 qb[kC * kRowB];  // q rows, padded
     __nv_bfloat16 kb[kC * kRowB];  // k rows, padded
 };
-constexpr size_t kScanSmem = 2 * sizeof(ScanBuf) +
-                             sizeof(float) * (kD * kRows + kC * kRows + kC + 4 * kC * kRows) +
-                             sizeof(__nv_bfloat16) * kD * kC;
+constexpr size_t kScanSmem = 2 * sizeof(ScanBuf) + sizeof(float) * (kD * kRowS + kC * kRowS + kC);
 
 __device__ __forceinline__ void scan_prefetch(ScanBuf& b, const __nv_bfloat16* __restrict__ q,
                                               const __nv_bfloat16* __restrict__ k,
@@ -330,9 +331,11 @@ __device__ __forceinline__ void scan_prefetch(ScanBuf& b, const __nv_bfloat16* _
                                               int32_t jq, int tid)
 {
     const float* w = wt + cj * kD * kC;
-    for (int e = tid; e < kD * kC / 4; e += kScanThreads) cp_async16(b.wt + 4 * e, w + 4 * e, 16);
+    for (int e = tid; e < kD * kC / 4; e += kScanThreads)
+        cp_async16(b.wt + (e / 16) * kRowW + (e % 16) * 4, w + 4 * e, 16);
     const float* a = at + cj * kC * kC;
-    for (int e = tid; e < kC * kC / 4; e += kScanThreads) cp_async16(b.at + 4 * e, a + 4 * e, 16);
+    for (int e = tid; e < kC * kC / 4; e += kScanThreads)
+        cp_async16(b.at + (e / 16) * kRowW + (e % 16) * 4, a + 4 * e, 16);
     const float* u = ut + (cj * kD + r0) * kC;
     for (int e = tid; e < kRows * kC / 4; e += kScanThreads) cp_async16(b.up + 4 * e, u + 4 * e, 16);
     if (tid < kC / 4) cp_async16(b.g + 4 * tid, gam + cj * kC + 4 * tid, 16);
@@ -346,13 +349,41 @@ __device__ __forceinline__ void scan_prefetch(ScanBuf& b, const __nv_bfloat16* _
     cp_async_commit();
 }
 
-__device__ __forceinline__ void fma4x4(float (&acc)[4][4], const float4 a, const float4 b)
+__device__ __forceinline__ uint32_t tf32_rna(float x)
 {
-    const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// x = hi + lo with hi, lo TF32 values (lo the TF32 rounding of x - hi)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo)
+{
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - __uint_as_float(hi));
+}
+
+// d += a * b for a 16 x 8 (k) A fragment and an 8 (k) x 8 B fragment (m16n8k8, TF32 -> f32)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// d += A * B with fp32 A (a[4]) and B (b[2]) fragments, three TF32 passes
+__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], const float (&b)[2])
+{
+    uint32_t ah[4], al[4], bh[2], bl[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) acc[i][r] = fmaf(av[i], bv[r], acc[i][r]);
+    for (int i = 0; i < 2; ++i) split_tf32(b[i], bh[i], bl[i]);
+    mma_tf32(d, al[0], al[1], al[2], al[3], bh[0], bh[1]);
+    mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
+    mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
 }
 
 __global__ void __launch_bounds__(kScanThreads, 1)
@@ -369,16 +400,16 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const int32_t jq = j / (h_v / h_qk);
     extern __shared__ __align__(16) uint8_t smraw[];
     ScanBuf* buf = reinterpret_cast<ScanBuf*>(smraw);
-    float* St = reinterpret_cast<float*>(buf + 2);  // state transposed [c][r], 128 x 16
-    float* Ut = St + kD * kRows;                    // U transposed [s][r], 64 x 16
-    float* kf = Ut + kC * kRows;                    // [64] g_C / g_s
-    float* P = kf + kC;                             // partial sums [4][64][16]
-    __nv_bfloat16* Qt = reinterpret_cast<__nv_bfloat16*>(P + 4 * kC * kRows);   // [c][t] bf16
+    float* St = reinterpret_cast<float*>(buf + 2);  // state transposed [c][r], 128 x 16 (+pad)
+    float* Ut = St + kD * kRowS;                    // U transposed [s][r], 64 x 16 (+pad)
+    float* kf = Ut + kC * kRowS;                    // [64] g_C / g_s
     const int tid = threadIdx.x;
+    const int warp = tid / 32, lane = tid % 32;
+    const int gq = lane >> 2, tg = lane & 3;        // fragment row group, thread in group
 
     const int64_t sbase = ((static_cast<int64_t>(i) * h_v + j) * kD + r0) * kD;
     for (int e = tid; e < kRows * kD; e += kScanThreads)
-        St[(e % kD) * kRows + e / kD] = s0 ? s0[sbase + e] : 0.f;
+        St[(e % kD) * kRowS + e / kD] = s0 ? s0[sbase + e] : 0.f;
 
     const int32_t c_begin = chunk_offset[i], c_end = chunk_offset[i + 1];
     const int32_t seq_start = cu[i], seq_end = cu[i + 1];
@@ -386,13 +417,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (c_begin < c_end)
         scan_prefetch(buf[0], q, k, wt, ut, at, gam, static_cast<int64_t>(c_begin) * h_v + j, r0,
                       chunk_t0(c_begin), min(kC, seq_end - chunk_t0(c_begin)), h_qk, jq, tid);
-    // U and O tiles: tokens 4 tt .. 4 tt + 3, rows 4 tr .. 4 tr + 3, reduction quarter tq
-    const int tt = tid % 16, tr = (tid / 16) % 4, tq = tid / 64;
-    // update tiles: columns 4 uc .. 4 uc + 3, rows 4 ur .. 4 ur + 3, reduction half uh
-    const int uc = tid % 32, ur = (tid / 32) % 4, uh = tid / 128;
-    // the reduce step: 4 consecutive (t, r) outputs per thread
-    const int oe = 4 * tid;                          // output index t * 16 + r .. + 3
-    const int ot = oe / kRows, orr = oe % kRows;
+    // U and O: warp tile rows (tokens) m0 .. m0+15, columns (state rows) n0 .. n0+7
+    const int m0 = 16 * (warp >> 1), n0 = 8 * (warp & 1);
     for (int32_t ch = c_begin; ch < c_end; ++ch) {
         const int b = (ch - c_begin) & 1;
         const int32_t t0 = chunk_t0(ch);
@@ -404,114 +430,103 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                           r0, chunk_t0(ch + 1), min(kC, seq_end - chunk_t0(ch + 1)), h_qk, jq, tid);
         const ScanBuf& B = buf[b];
         if (tid < kC) kf[tid] = B.g[kC - 1] / B.g[tid];
-        for (int idx = tid; idx < kC * 16; idx += kScanThreads) {   // q -> Qt [c][t]
-            const int t = idx % kC, p = idx / kC;
-            const uint4 w = *reinterpret_cast<const uint4*>(B.qb + t * kRowB + p * 8);
-            const uint32_t u4[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                Qt[(p * 8 + 2 * e) * kC + t] = __ushort_as_bfloat16(static_cast<uint16_t>(u4[e]));
-                Qt[(p * 8 + 2 * e + 1) * kC + t] =
-                    __ushort_as_bfloat16(static_cast<uint16_t>(u4[e] >> 16));
-            }
-        }
 
-        // U = U' - W S^T: partial sums over c in [32 tq, 32 tq + 32)
+        // U = U' - W S^T  (M = tokens, N = state rows, K = c)
         {
-            float acc[4][4] = {};
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-            for (int c = 32 * tq; c < 32 * tq + 32; ++c)
-                fma4x4(acc, *reinterpret_cast<const float4*>(B.wt + c * kC + 4 * tt),
-                       *reinterpret_cast<const float4*>(St + c * kRows + 4 * tr));
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii)
-                *reinterpret_cast<float4*>(P + (tq * kC + 4 * tt + ii) * kRows + 4 * tr) =
-                    make_float4(acc[ii][0], acc[ii][1], acc[ii][2], acc[ii][3]);
-        }
-        __syncthreads();
-        {
-            float4 u;
-            float* uv = &u.x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float x = B.up[(orr + e) * kC + ot];
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) x -= P[(qq * kC + ot) * kRows + orr + e];
-                uv[e] = x;
+            for (int k0 = 0; k0 < kD; k0 += 8) {
+                const float a[4] = {B.wt[(k0 + tg) * kRowW + m0 + gq],
+                                    B.wt[(k0 + tg) * kRowW + m0 + gq + 8],
+                                    B.wt[(k0 + tg + 4) * kRowW + m0 + gq],
+                                    B.wt[(k0 + tg + 4) * kRowW + m0 + gq + 8]};
+                const float bb[2] = {St[(k0 + tg) * kRowS + n0 + gq],
+                                     St[(k0 + tg + 4) * kRowS + n0 + gq]};
+                mma_3xtf32(d, a, bb);
             }
-            *reinterpret_cast<float4*>(Ut + ot * kRows + orr) = u;
+            const int t = m0 + gq, r = n0 + 2 * tg;
+            Ut[t * kRowS + r] = B.up[r * kC + t] - d[0];
+            Ut[t * kRowS + r + 1] = B.up[(r + 1) * kC + t] - d[1];
+            Ut[(t + 8) * kRowS + r] = B.up[r * kC + t + 8] - d[2];
+            Ut[(t + 8) * kRowS + r + 1] = B.up[(r + 1) * kC + t + 8] - d[3];
         }
-        __syncthreads();   // U and Qt complete
+        __syncthreads();   // U complete
 
-        // O = scale (diag(g) Q S^T + A U): partial sums over c in [32 tq, +32) and s in [16 tq, +16)
+        // O = scale (diag(g) Q S^T + A U)
         {
-            float qs[4][4] = {}, au[4][4] = {};
+            float qs[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-            for (int c = 32 * tq; c < 32 * tq + 32; ++c) {
-                const uint2 w = *reinterpret_cast<const uint2*>(Qt + c * kC + 4 * tt);
-                fma4x4(qs, make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)),
-                       *reinterpret_cast<const float4*>(St + c * kRows + 4 * tr));
+            for (int k0 = 0; k0 < kD; k0 += 8) {
+                // q is bf16: exact in TF32, so only the state needs a split
+                const uint32_t a0 = __float_as_uint(bf16_at(B.qb + (m0 + gq) * kRowB + k0 + tg));
+                const uint32_t a1 = __float_as_uint(bf16_at(B.qb + (m0 + gq + 8) * kRowB + k0 + tg));
+                const uint32_t a2 = __float_as_uint(bf16_at(B.qb + (m0 + gq) * kRowB + k0 + tg + 4));
+                const uint32_t a3 =
+                    __float_as_uint(bf16_at(B.qb + (m0 + gq + 8) * kRowB + k0 + tg + 4));
+                uint32_t bh0, bl0, bh1, bl1;
+                split_tf32(St[(k0 + tg) * kRowS + n0 + gq], bh0, bl0);
+                split_tf32(St[(k0 + tg + 4) * kRowS + n0 + gq], bh1, bl1);
+                mma_tf32(qs, a0, a1, a2, a3, bl0, bl1);
+                mma_tf32(qs, a0, a1, a2, a3, bh0, bh1);
             }
-#pragma unroll 4
-            for (int s = 16 * tq; s < 16 * tq + 16; ++s)   // A[t][s] = 0 for s > t
-                fma4x4(au, *reinterpret_cast<const float4*>(B.at + s * kC + 4 * tt),
-                       *reinterpret_cast<const float4*>(Ut + s * kRows + 4 * tr));
+            for (int k0 = 0; k0 < m0 + 16; k0 += 8) {   // A[t][s] = 0 for s > t
+                const float a[4] = {B.at[(k0 + tg) * kRowW + m0 + gq],
+                                    B.at[(k0 + tg) * kRowW + m0 + gq + 8],
+                                    B.at[(k0 + tg + 4) * kRowW + m0 + gq],
+                                    B.at[(k0 + tg + 4) * kRowW + m0 + gq + 8]};
+                const float bb[2] = {Ut[(k0 + tg) * kRowS + n0 + gq],
+                                     Ut[(k0 + tg + 4) * kRowS + n0 + gq]};
+                mma_3xtf32(au, a, bb);
+            }
+            const int t = m0 + gq, r = n0 + 2 * tg;
 #pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-                const float gt = B.g[4 * tt + ii];
-                *reinterpret_cast<float4*>(P + (tq * kC + 4 * tt + ii) * kRows + 4 * tr) =
-                    make_float4(fmaf(gt, qs[ii][0], au[ii][0]), fmaf(gt, qs[ii][1], au[ii][1]),
-                                fmaf(gt, qs[ii][2], au[ii][2]), fmaf(gt, qs[ii][3], au[ii][3]));
+            for (int h = 0; h < 2; ++h) {
+                const int tt = t + 8 * h;
+                if (tt < len) {
+                    const float gt = B.g[tt];
+                    const __nv_bfloat162 v2 =
+                        __floats2bfloat162_rn(scale * fmaf(gt, qs[2 * h], au[2 * h]),
+                                              scale * fmaf(gt, qs[2 * h + 1], au[2 * h + 1]));
+                    *reinterpret_cast<__nv_bfloat162*>(
+                        o + ((static_cast<int64_t>(t0) + tt) * h_v + j) * kD + r0 + r) = v2;
+                }
             }
         }
-        __syncthreads();
-        if (ot < len) {
-            float x[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float v = 0.f;
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) v += P[(qq * kC + ot) * kRows + orr + e];
-                x[e] = scale * v;
-            }
-            const __nv_bfloat162 h0 = __floats2bfloat162_rn(x[0], x[1]);
-            const __nv_bfloat162 h1 = __floats2bfloat162_rn(x[2], x[3]);
-            *reinterpret_cast<uint2*>(o + ((static_cast<int64_t>(t0) + ot) * h_v + j) * kD + r0 +
-                                      orr) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&h0),
-                           *reinterpret_cast<const uint32_t*>(&h1));
-        }
+        __syncthreads();   // every reader of S is done before the update
 
-        // S^T_next[c][r] = g_C S^T[c][r] + sum_s (g_C / g_s) K[s][c] U[s][r]: partials over s in
-        // [32 uh, 32 uh + 32)
-        {
-            float acc[4][4] = {};
-#pragma unroll 4
-            for (int s = 32 * uh; s < 32 * uh + 32; ++s) {
-                const uint2 w = *reinterpret_cast<const uint2*>(B.kb + s * kRowB + 4 * uc);
-                const float f = kf[s];
-                fma4x4(acc, make_float4(f * bf16_lo(w.x), f * bf16_hi(w.x), f * bf16_lo(w.y),
-                                        f * bf16_hi(w.y)),
-                       *reinterpret_cast<const float4*>(Ut + s * kRows + 4 * ur));
-            }
-            __syncthreads();   // the output reduce has read P
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<float4*>(P + (uh * kD + 4 * uc + cc) * kRows + 4 * ur) =
-                    make_float4(acc[cc][0], acc[cc][1], acc[cc][2], acc[cc][3]);
-        }
-        __syncthreads();
+        // S^T_next = g_C S^T + Kd^T U with Kd[s][c] = (g_C / g_s) K[s][c]  (M = c, N = rows, K = s)
         {
             const float gC = B.g[kC - 1];
-            for (int e = tid; e < kD * kRows; e += kScanThreads)
-                St[e] = fmaf(gC, St[e], P[e] + P[kD * kRows + e]);
+            const int mc = 16 * warp;                 // state columns mc .. mc + 15
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int nn = 8 * nt;
+                const int c = mc + gq, r = nn + 2 * tg;
+                float d[4] = {gC * St[c * kRowS + r], gC * St[c * kRowS + r + 1],
+                              gC * St[(c + 8) * kRowS + r], gC * St[(c + 8) * kRowS + r + 1]};
+#pragma unroll 2
+                for (int k0 = 0; k0 < kC; k0 += 8) {
+                    const float f0 = kf[k0 + tg], f1 = kf[k0 + tg + 4];
+                    const float a[4] = {f0 * bf16_at(B.kb + (k0 + tg) * kRowB + mc + gq),
+                                        f0 * bf16_at(B.kb + (k0 + tg) * kRowB + mc + gq + 8),
+                                        f1 * bf16_at(B.kb + (k0 + tg + 4) * kRowB + mc + gq),
+                                        f1 * bf16_at(B.kb + (k0 + tg + 4) * kRowB + mc + gq + 8)};
+                    const float bb[2] = {Ut[(k0 + tg) * kRowS + nn + gq],
+                                         Ut[(k0 + tg + 4) * kRowS + nn + gq]};
+                    mma_3xtf32(d, a, bb);
+                }
+                St[c * kRowS + r] = d[0];
+                St[c * kRowS + r + 1] = d[1];
+                St[(c + 8) * kRowS + r] = d[2];
+                St[(c + 8) * kRowS + r + 1] = d[3];
+            }
         }
     }
     cp_async_wait_all();
     __syncthreads();
     if (s_final)
         for (int e = tid; e < kRows * kD; e += kScanThreads)
-            s_final[sbase + e] = St[(e % kD) * kRows + e / kD];
+            s_final[sbase + e] = St[(e % kD) * kRowS + e / kD];
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
