@@ -118,8 +118,6 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
     }
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_at(const __nv_bfloat16* p)
 {
     return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
@@ -136,13 +134,24 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src,
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// d += a * b for a 16 x 16 (k) bf16 A fragment and a 16 (k) x 8 bf16 B fragment (m16n8k16,
+// fp32 accumulation); each 32-bit register holds two consecutive-k elements.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Rows of 128 bf16 in shared memory are padded to 136 elements (272 bytes): rows 16 apart then
 // start 4 banks apart, so the strided tiles below read them without bank conflicts.
 constexpr int kRowB = 136;
 
 // ---- per (chunk, value head): W^T, U'^T, A^T and the cumulative decays ----------------------
-// K, Q, V of the chunk sit in shared memory as padded bf16 rows.  Products K K^T and Q K^T are
-// register-tiled (each thread 4 x 4 entries, rows and columns 16 apart).  Then (I + L) X = R
+// K, Q, V of the chunk sit in shared memory as padded bf16 rows.  Products K K^T and Q K^T run
+// on the tensor cores (bf16 operands, exact products).  Then (I + L) X = R
 // is solved for the 256 right-hand-side columns R = [diag(beta g) K | diag(beta) V] by forward
 // substitution, one column per thread with the column held in registers: no inverse is formed
 // and no barrier is needed inside the solve.
@@ -211,53 +220,42 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     __syncthreads();
     if (tid < kC) bg[tid] = bt[tid] * g[tid];
 
-    // K K^T and Q K^T: thread tile rows t = tt + 16 i, columns s = st + 16 jj
+    // K K^T and Q K^T on the tensor cores: mma.sync m16n8k16 with bf16 operands (exact products,
+    // fp32 sums).  Warp w owns rows 16 (w / 2) .. + 15 and columns 32 (w % 2) .. + 31 of both.
     {
-        const int tt = tid / 16, st = tid % 16;
-        float kk[4][4], qk[4][4];
+        const int warp = tid / 32, lane = tid % 32;
+        const int gq = lane >> 2, tg = lane & 3;
+        const int m0 = 16 * (warp >> 1), nb = 32 * (warp & 1);
+        float kk[4][4] = {}, qk[4][4] = {};
+        const auto ld32 = [](const __nv_bfloat16* p) { return *reinterpret_cast<const uint32_t*>(p); };
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int k0 = 0; k0 < kD; k0 += 16) {
+            const uint32_t ka0 = ld32(Kb + (m0 + gq) * kRowB + k0 + 2 * tg);
+            const uint32_t ka1 = ld32(Kb + (m0 + gq + 8) * kRowB + k0 + 2 * tg);
+            const uint32_t ka2 = ld32(Kb + (m0 + gq) * kRowB + k0 + 2 * tg + 8);
+            const uint32_t ka3 = ld32(Kb + (m0 + gq + 8) * kRowB + k0 + 2 * tg + 8);
+            const uint32_t qa0 = ld32(Qb + (m0 + gq) * kRowB + k0 + 2 * tg);
+            const uint32_t qa1 = ld32(Qb + (m0 + gq + 8) * kRowB + k0 + 2 * tg);
+            const uint32_t qa2 = ld32(Qb + (m0 + gq) * kRowB + k0 + 2 * tg + 8);
+            const uint32_t qa3 = ld32(Qb + (m0 + gq + 8) * kRowB + k0 + 2 * tg + 8);
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) kk[i][jj] = qk[i][jj] = 0.f;
-        for (int d = 0; d < kD; d += 8) {
-            uint4 kt[4], qt[4], ks[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                kt[i] = *reinterpret_cast<const uint4*>(Kb + (tt + 16 * i) * kRowB + d);
-                qt[i] = *reinterpret_cast<const uint4*>(Qb + (tt + 16 * i) * kRowB + d);
-                ks[i] = *reinterpret_cast<const uint4*>(Kb + (st + 16 * i) * kRowB + d);
-            }
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float a[4], b[4], c[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t ka = (&kt[i].x)[w], qa = (&qt[i].x)[w], kb = (&ks[i].x)[w];
-                        a[i] = h ? bf16_hi(ka) : bf16_lo(ka);
-                        b[i] = h ? bf16_hi(qa) : bf16_lo(qa);
-                        c[i] = h ? bf16_hi(kb) : bf16_lo(kb);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj) {
-                            kk[i][jj] = fmaf(a[i], c[jj], kk[i][jj]);
-                            qk[i][jj] = fmaf(b[i], c[jj], qk[i][jj]);
-                        }
-                }
+            for (int nt = 0; nt < 4; ++nt) {
+                const int n0 = nb + 8 * nt;
+                const uint32_t b0 = ld32(Kb + (n0 + gq) * kRowB + k0 + 2 * tg);
+                const uint32_t b1 = ld32(Kb + (n0 + gq) * kRowB + k0 + 2 * tg + 8);
+                mma_bf16(kk[nt], ka0, ka1, ka2, ka3, b0, b1);
+                mma_bf16(qk[nt], qa0, qa1, qa2, qa3, b0, b1);
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = tt + 16 * i;
+        for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int s = st + 16 * jj;
+            for (int e = 0; e < 4; ++e) {
+                const int t = m0 + gq + 8 * (e >> 1);
+                const int s = nb + 8 * nt + 2 * tg + (e & 1);
                 const float ratio = s <= t ? g[t] / g[s] : 0.f;
-                Ls[t * kC + s] = s < t ? bt[t] * ratio * kk[i][jj] : 0.f;
-                As[s * (kC + 1) + t] = ratio * qk[i][jj];
+                Ls[t * kC + s] = s < t ? bt[t] * ratio * kk[nt][e] : 0.f;
+                As[s * (kC + 1) + t] = ratio * qk[nt][e];
             }
         }
     }

@@ -82,16 +82,34 @@ uint32_t l2_hint_setting()
     return v;
 }
 
-uint32_t group_m_setting()
+// Tile-rows per raster group: GEMM_F16_GROUP overrides (1..64); 0 when unset.
+uint32_t group_m_override()
 {
     static const uint32_t v = [] {
         const char* s = std::getenv("GEMM_F16_GROUP");
-        long g = s ? std::atol(s) : 8;
+        if (!s) return 0u;
+        long g = std::atol(s);
         if (g < 1) g = 1;
         if (g > 64) g = 64;
         return static_cast<uint32_t>(g);
     }();
     return v;
+}
+
+// Raster group size.  A group of G tile-rows walks the N tiles together, so every B tile is
+// loaded once per group instead of once per tile-row, while the group's G row bands of A
+// (mma_m rows x K each) stay resident in L2 for the whole sweep.  The rule: the largest power of
+// two, at most 16, whose A bands fill no more than a third of L2.  On a GB300 (about 126 MiB of
+// L2) with 256-row fp16 tiles this gives 8 at K = 8192 (4 MiB bands) and 16 at K = 4096; a
+// sustained sweep of 8, 12, 16 and 20 measured those two as the fastest for 8192^3 and
+// 16384x14336x4096 respectively.
+uint32_t group_m_for(int64_t mma_m, int64_t K, int64_t elem_bytes, int64_t l2_bytes)
+{
+    if (const uint32_t o = group_m_override()) return o;
+    const int64_t band = mma_m * K * elem_bytes;
+    uint32_t g = 1;
+    while (g < 16 && band * (2 * g) * 3 <= l2_bytes) g *= 2;
+    return g;
 }
 
 // ---- the variants ----------------------------------------------------------------------------
@@ -156,6 +174,7 @@ constexpr int kNumSlots = 64;
 struct DeviceState {
     bool ready = false;
     int sms = 0;
+    int64_t l2_bytes = 0;
     bool smem_set[kNumSlots] = {};    // max dynamic shared memory raised, per kernel slot
     int pair_clusters[kNumSlots] = {};  // co-resident CTA pairs, per kernel slot
 };
@@ -175,6 +194,10 @@ int device_state(DeviceState** out)
         int major = 0, minor = 0;
         if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        int l2 = 0;
+        if ((e = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute(L2 size)");
+        d.l2_bytes = l2;
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         if (major != 10 || minor != 3)
@@ -482,7 +505,8 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
                                        static_cast<uint16_t*>(D),
                                        (uint32_t)M, (uint32_t)N,
                                        (uint32_t)num_m, (uint32_t)num_n, (uint32_t)KB,
-                                       group_m_setting(), wait_timeout_ns(), l2_hint_setting(),
+                                       group_m_for(C::MMA_M, K, C::ELEM_BYTES, d.l2_bytes),
+                                       wait_timeout_ns(), l2_hint_setting(),
                                        ws_part, ws_count, (uint32_t)R,
                                        (uint32_t)(R ? sk_units_for(R, units_used) : units_used),
                                        static_cast<const uint16_t*>(epi.bias),
@@ -869,6 +893,11 @@ void gemm_f16_tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_t gr
     const gf16::TileCoord c = gf16::tile_coord(t, num_m, num_n, group);
     if (m_blk) *m_blk = c.m_blk;
     if (n_blk) *n_blk = c.n_blk;
+}
+
+uint32_t gemm_f16_raster_group(int64_t mma_m, int64_t K, int64_t elem_bytes, int64_t l2_bytes)
+{
+    return group_m_for(mma_m, K, elem_bytes, l2_bytes);
 }
 
 int64_t gemm_f16_sk_tail_tiles(int64_t tiles, int64_t units, int64_t k_blocks)

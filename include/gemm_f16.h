@@ -216,6 +216,12 @@ void gemm_f16_tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_t gr
 /* Pipeline iteration `it` -> ring stage and the parity of the "full" phase it waits for. */
 void gemm_f16_ring_pos(uint32_t it, uint32_t stages, uint32_t* stage, uint32_t* parity);
 
+/* Raster group size (tile-rows walked together) the library launches with for tiles of `mma_m`
+ * rows, depth K of `elem_bytes`-byte elements and an L2 of `l2_bytes`: the largest power of two up
+ * to 16 whose G row bands of A (mma_m x K elements each) fit in a third of L2.  The environment
+ * variable GEMM_F16_GROUP (1..64), read once per process, overrides it. */
+uint32_t gemm_f16_raster_group(int64_t mma_m, int64_t K, int64_t elem_bytes, int64_t l2_bytes);
+
 /* The persistent kernels' work split (host copies of the device arithmetic).  `tiles` output
  * tiles of `k_blocks` k-blocks each on `units` CTAs (or CTA pairs), of which the last `tail` run
  * stream-K (0: none).  gemm_f16_sk_tail_tiles: the tail the library chooses.

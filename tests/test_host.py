@@ -333,6 +333,23 @@ def test_stream_k_split_covers_each_k_block_once(T, U, KB):
             assert max(per_unit) - min(per_unit) <= KB  # at most one tile apart
 
 
+def test_raster_group_rule():
+    if "GEMM_F16_GROUP" in os.environ:
+        pytest.skip("GEMM_F16_GROUP overrides the rule in this process")
+    l2 = 126 << 20                                                  # a GB300's L2
+    assert g.gemm_f16_raster_group(256, 8192, 2, l2) == 8          # 8192^3 pair tiles
+    assert g.gemm_f16_raster_group(256, 4096, 2, l2) == 16         # 16384x14336x4096
+    assert g.gemm_f16_raster_group(128, 8192, 2, l2) == 16         # 128-row tiles
+    assert g.gemm_f16_raster_group(256, 8192, 1, l2) == 16         # fp8: one byte per element
+    assert g.gemm_f16_raster_group(256, 65536, 2, l2) == 1         # one band already over L2/3
+    assert g.gemm_f16_raster_group(256, 64, 2, l2) == 16           # capped at 16
+    for K in (64, 512, 4096, 8192, 16384, 32768):                  # the invariant itself
+        G = g.gemm_f16_raster_group(256, K, 2, l2)
+        assert G in (1, 2, 4, 8, 16)
+        assert G == 1 or G * 256 * K * 2 * 3 <= l2
+        assert G == 16 or 2 * G * 256 * K * 2 * 3 > l2
+
+
 def test_stream_k_tail_choice():
     assert g.gemm_f16_sk_tail_tiles(1024, 76, 128) == 36      # 8192^3: 13.47 waves of pairs
     assert g.gemm_f16_sk_tail_tiles(3584, 76, 64) == 12       # MLP: 47.16 waves
