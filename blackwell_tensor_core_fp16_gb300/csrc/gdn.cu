@@ -12,15 +12,25 @@
 // so the updates u_t satisfy (I + L) U = diag(beta) V - diag(beta g) K H0^T with the strictly
 // lower triangular L[t][s] = beta_t (g_t / g_s) (k_t . k_s).  With T = (I + L)^-1,
 //     W = T diag(beta g) K      (C x dk)      U' = T diag(beta) V      (C x dv)
-// depend on the chunk alone (gdn_prepare_kernel, all chunks in parallel), and the scan over a
-// sequence's chunks (gdn_scan_kernel) computes
-//     U = U' - W H0^T,   O = scale (diag(g) Q H0^T + A U),   H_next = g_C H0 + U^T diag(g_C / g) K
-// with A[t][s] = (g_t / g_s) (q_t . k_s) for s <= t.  Every value row of H evolves on its own,
-// so the scan splits a head's dv rows over several CTAs.
+// depend on the chunk alone (gdn_prepare_kernel, all chunks in parallel).  The scan over a
+// sequence's chunks (gdn_scan_kernel) then computes, with g_C the chunk's last decay,
+//     U  = U' - W H0^T                         (the chunk's true updates)
+//     U~ = diag(g_C / g) U                     (each update decayed to the chunk's end)
+//     O  = scale (diag(g) Q H0^T + A' U~),     A'[t][s] = (g_t / g_C) (q_t . k_s) for s <= t
+//     H_next = g_C H0 + U~^T K
+// (A' U~ equals the intra-chunk attention term sum_{s<=t} (g_t / g_s) (q_t . k_s) u_s).  Every
+// value row of H evolves on its own, so the scan splits a head's dv rows over several CTAs.
+//
+// Precision.  The products run on the tensor cores as bfloat16 x bfloat16 -> fp32 (exact
+// products).  q and k are bfloat16 already; an fp32 operand x is carried as three bfloat16
+// pieces x0 + x1 + x2 (x0 = bf16(x), x1 = bf16(x - x0), x2 = bf16(x - x0 - x1): |x - x0 - x1 -
+// x2| <= 2^-27 |x|), and a product of two such operands keeps the six terms of order <= 2, so
+// the state path stays at fp32 accuracy.  The output path (A' U~), which ends in a bfloat16
+// result, keeps two pieces of each and three terms (relative error about 2^-16).
 //
 // A sequence's last chunk may be short: its missing tokens are read as q = k = v = 0,
 // alpha = 1, beta = 0 (the page's rule for packed tails), which leaves the state and the valid
-// outputs unchanged.  All arithmetic is fp32; q, k, v and o are bfloat16.
+// outputs unchanged.  Non-product arithmetic is fp32; q, k, v and o are bfloat16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -52,9 +62,13 @@ int gdn_fail(int code, const char* fmt, ...)
 
 int64_t max_chunks_for(int64_t T, int64_t n) { return T / kC + n; }
 
-// Workspace layout (all offsets 256-byte aligned).
+// Workspace layout (all offsets 256-byte aligned), per chunk cj = chunk * h_v + value head:
+//   wp   bf16 [cj][3][64][128]  W in three pieces, rows t, columns c
+//   ap   bf16 [cj][2][64][64]   A' in two pieces, rows t, columns s (zero for s > t)
+//   ut   f32  [cj][128][64]     U'^T, rows v, columns t
+//   gam  f32  [cj][64]          g_t
 struct WsLayout {
-    size_t chunk_offset, n_chunks, chunks, wt, ut, at, gam, total;
+    size_t chunk_offset, n_chunks, chunks, wp, ap, ut, gam, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -62,15 +76,16 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 WsLayout layout_for(int64_t T, int64_t n, int64_t h_v)
 {
     const size_t mc = static_cast<size_t>(max_chunks_for(T, n));
+    const size_t cj = mc * static_cast<size_t>(h_v);
     WsLayout l{};
     size_t o = 0;
     l.chunk_offset = o; o = align256(o + sizeof(int32_t) * static_cast<size_t>(n + 1));
     l.n_chunks = o;     o = align256(o + sizeof(int32_t));
     l.chunks = o;       o = align256(o + sizeof(int4) * mc);
-    l.wt = o;           o = align256(o + sizeof(float) * mc * h_v * kD * kC);
-    l.ut = o;           o = align256(o + sizeof(float) * mc * h_v * kD * kC);
-    l.at = o;           o = align256(o + sizeof(float) * mc * h_v * kC * kC);
-    l.gam = o;          o = align256(o + sizeof(float) * mc * h_v * kC);
+    l.wp = o;           o = align256(o + sizeof(__nv_bfloat16) * cj * 3 * kC * kD);
+    l.ap = o;           o = align256(o + sizeof(__nv_bfloat16) * cj * 2 * kC * kC);
+    l.ut = o;           o = align256(o + sizeof(float) * cj * kD * kC);
+    l.gam = o;          o = align256(o + sizeof(float) * cj * kC);
     l.total = o;
     return l;
 }
@@ -144,28 +159,91 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1)
+{
+    mma_bf16(d, a[0], a[1], a[2], a[3], b0, b1);
+}
 
-// Rows of 128 bf16 in shared memory are padded to 136 elements (272 bytes): rows 16 apart then
-// start 4 banks apart, so the strided tiles below read them without bank conflicts.
-constexpr int kRowB = 136;
+// ldmatrix / stmatrix of 8 x 8 blocks of 16-bit elements; lane l supplies the shared address of
+// row l % 8 of block l / 8.
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void stsm_x2_trans(uint32_t addr, uint32_t r0, uint32_t r1)
+{
+    asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1, %2};"
+                 ::"r"(addr), "r"(r0), "r"(r1) : "memory");
+}
 
-// ---- per (chunk, value head): W^T, U'^T, A^T and the cumulative decays ----------------------
+// Three bfloat16 pieces of x (x0 + x1 + x2 within 2^-27 |x|), packed for two values a (low
+// half) and b (high half) of one fragment register.
+struct Pieces3 { uint32_t p[3]; };
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ Pieces3 split3(float a, float b)
+{
+    Pieces3 r;
+    const __nv_bfloat162 v0 = __floats2bfloat162_rn(a, b);
+    const float a1 = a - __low2float(v0), b1 = b - __high2float(v0);
+    const __nv_bfloat162 v1 = __floats2bfloat162_rn(a1, b1);
+    const float a2 = a1 - __low2float(v1), b2 = b1 - __high2float(v1);
+    r.p[0] = *reinterpret_cast<const uint32_t*>(&v0);
+    r.p[1] = *reinterpret_cast<const uint32_t*>(&v1);
+    r.p[2] = pack_bf16(a2, b2);
+    return r;
+}
+
+// Shared-memory tiles of bfloat16 rows stored in 16-byte granules, granule index XOR (row % 8):
+// the eight rows an ldmatrix / stmatrix block touches then fall in eight different bank groups.
+// Rows of 128 elements (256 bytes) and of 64 elements (128 bytes).
+__device__ __forceinline__ uint32_t sw256(int row, int col)
+{
+    return static_cast<uint32_t>(row * 256 + (((col >> 3) ^ (row & 7)) * 16) + (col & 7) * 2);
+}
+__device__ __forceinline__ uint32_t sw128(int row, int col)
+{
+    return static_cast<uint32_t>(row * 128 + (((col >> 3) ^ row) & 7) * 16 + (col & 7) * 2);
+}
+
+// ---- per (chunk, value head): W, U'^T, A' and the cumulative decays ----------------------------
 // K, Q, V of the chunk sit in shared memory as padded bf16 rows.  Products K K^T and Q K^T run
 // on the tensor cores (bf16 operands, exact products).  Then (I + L) X = R
 // is solved for the 256 right-hand-side columns R = [diag(beta g) K | diag(beta) V] by forward
 // substitution, one column per thread with the column held in registers: no inverse is formed
 // and no barrier is needed inside the solve.
+constexpr int kRowB = 136;     // padded bf16 rows of the prepare kernel (272 bytes)
+constexpr int kRowA = 72;      // padded bf16 rows of A' staging (144 bytes)
 constexpr int kPrepThreads = 256;
-constexpr size_t kPrepSmem =
-    sizeof(__nv_bfloat16) * 3 * kC * kRowB + sizeof(float) * (kC * kC + kC * (kC + 1) + 4 * kC);
+constexpr size_t kPrepSmem = sizeof(__nv_bfloat16) * (3 * kC * kRowB + 2 * kC * kRowA) +
+                             sizeof(float) * (kC * kC + 4 * kC);
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
     gdn_prepare_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                        const __nv_bfloat16* __restrict__ v, const float* __restrict__ alpha,
                        const float* __restrict__ beta, const int4* __restrict__ chunks,
                        const int32_t* __restrict__ n_chunks, int32_t h_qk, int32_t h_v,
-                       float* __restrict__ wt, float* __restrict__ ut, float* __restrict__ at,
-                       float* __restrict__ gam_out)
+                       __nv_bfloat16* __restrict__ wp, __nv_bfloat16* __restrict__ ap,
+                       float* __restrict__ ut, float* __restrict__ gam_out)
 {
     const int32_t ch = blockIdx.x;
     const int32_t j = blockIdx.y;
@@ -173,13 +251,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const int4 info = chunks[ch];
     const int32_t t0 = info.y, len = info.z;
     const int32_t jq = j / (h_v / h_qk);
+    const int64_t cj = static_cast<int64_t>(ch) * h_v + j;
     extern __shared__ __align__(16) uint8_t smraw[];
     __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(smraw);   // [64][136]
     __nv_bfloat16* Qb = Kb + kC * kRowB;
     __nv_bfloat16* Vb = Qb + kC * kRowB;
-    float* Ls = reinterpret_cast<float*>(Vb + kC * kRowB);          // [64][64] L, strictly lower
-    float* As = Ls + kC * kC;                                         // [64 s][65] A transposed
-    float* g = As + kC * (kC + 1);
+    __nv_bfloat16* Ap = Vb + kC * kRowB;                             // [2][64][72] A' pieces
+    float* Ls = reinterpret_cast<float*>(Ap + 2 * kC * kRowA);       // [64][64] L, strictly lower
+    float* g = Ls + kC * kC;
     float* bt = g + kC;
     float* bg = bt + kC;
     float* al = bg + kC;
@@ -247,25 +326,35 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                 mma_bf16(qk[nt], qa0, qa1, qa2, qa3, b0, b1);
             }
         }
+        const float inv_gc = 1.f / g[kC - 1];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int t = m0 + gq + 8 * (e >> 1);
-                const int s = nb + 8 * nt + 2 * tg + (e & 1);
-                const float ratio = s <= t ? g[t] / g[s] : 0.f;
-                Ls[t * kC + s] = s < t ? bt[t] * ratio * kk[nt][e] : 0.f;
-                As[s * (kC + 1) + t] = ratio * qk[nt][e];
+            for (int h = 0; h < 2; ++h) {
+                const int t = m0 + gq + 8 * h;
+                const int s = nb + 8 * nt + 2 * tg;
+                float av[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    Ls[t * kC + s + e] = s + e < t ? bt[t] * (g[t] / g[s + e]) * kk[nt][2 * h + e] : 0.f;
+                    av[e] = s + e <= t ? (g[t] * inv_gc) * qk[nt][2 * h + e] : 0.f;
+                }
+                const Pieces3 pa = split3(av[0], av[1]);
+                *reinterpret_cast<uint32_t*>(Ap + t * kRowA + s) = pa.p[0];
+                *reinterpret_cast<uint32_t*>(Ap + kC * kRowA + t * kRowA + s) = pa.p[1];
             }
         }
     }
     __syncthreads();
 
-    // A^T to global, coalesced
+    // A' pieces to global, 16-byte granules
     {
-        float* atc = at + (static_cast<int64_t>(ch) * h_v + j) * kC * kC;
-        for (int e = tid; e < kC * kC; e += kPrepThreads)
-            atc[e] = As[(e / kC) * (kC + 1) + e % kC];
+        __nv_bfloat16* apc = ap + cj * 2 * kC * kC;
+        for (int e = tid; e < 2 * kC * 8; e += kPrepThreads) {
+            const int p = e / (kC * 8), t = (e / 8) % kC, c8 = e % 8;
+            *reinterpret_cast<int4*>(apc + (p * kC + t) * kC + c8 * 8) =
+                *reinterpret_cast<const int4*>(Ap + (p * kC + t) * kRowA + c8 * 8);
+        }
     }
 
     // (I + L) X = R by forward substitution, one right-hand-side column per thread
@@ -290,105 +379,95 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             for (int s = t & ~3; s < t; ++s) acc[0] = fmaf(-Ls[t * kC + s], x[s], acc[0]);
             x[t] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
         }
-        float* dst = (isw ? wt : ut) + ((static_cast<int64_t>(ch) * h_v + j) * kD + col) * kC;
+        if (isw) {
+            // W in three bfloat16 pieces, rows t, columns c
+            __nv_bfloat16* w = wp + cj * 3 * kC * kD + col;
 #pragma unroll
-        for (int t = 0; t < kC; t += 4)
-            *reinterpret_cast<float4*>(dst + t) = make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
+            for (int t = 0; t < kC; ++t) {
+                const __nv_bfloat16 p0 = __float2bfloat16_rn(x[t]);
+                const float r1 = x[t] - __bfloat162float(p0);
+                const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
+                w[t * kD] = p0;
+                w[(kC + t) * kD] = p1;
+                w[(2 * kC + t) * kD] = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+            }
+        } else {
+            float* dst = ut + (cj * kD + col) * kC;
+#pragma unroll
+            for (int t = 0; t < kC; t += 4)
+                *reinterpret_cast<float4*>(dst + t) = make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
+        }
     }
-    if (tid < kC) gam_out[(static_cast<int64_t>(ch) * h_v + j) * kC + tid] = g[tid];
+    if (tid < kC) gam_out[cj * kC + tid] = g[tid];
 }
 
-// ---- per (sequence, value head, block of 16 value rows): the state scan over the chunks -----
-// The chunk's inputs are double-buffered: while chunk c is computed, cp.async brings chunk
-// c + 1 (W^T, A^T, the block's U'^T rows, decays, and q/k as padded bf16 rows).  The three
-// products run on the tensor cores (mma.sync m16n8k8, TF32 inputs, fp32 accumulation), each
-// warp owning 16 x 8 output tiles.  Operands that are fp32 (W, A, the state, U, the decayed
-// keys) are split into a TF32 high part and the TF32 rounding of the rest, and each product
-// takes three passes (hi*hi + hi*lo + lo*hi), which keeps fp32 accuracy; q and k are bfloat16,
-// exact in TF32, so their passes need no split.
+// ---- per (sequence, value head, block of 16 value rows): the state scan over the chunks -------
+// Each chunk's operands are double-buffered in shared memory: while chunk c is computed,
+// cp.async brings chunk c + 1 (the W and A' pieces, q and k rows, the block's U'^T rows and the
+// decays).  Eight warps; each product runs on mma.sync m16n8k16 (bf16 -> fp32) with fragments
+// loaded by ldmatrix from XOR-swizzled tiles.
+//   phase 1   U = U' - W S^T and P = Q S^T: warp w owns tokens 16 (w % 4) .. + 15 and state
+//             rows 8 (w / 4) .. + 7; U~ = diag(g_C / g) U goes to shared memory as pieces, [r][t]
+//   phase 2   S_next^T = g_C S^T + K^T U~: warp w owns key columns 16 w .. + 15, all 16 rows; the
+//             fp32 state lives in these registers from chunk to chunk, and its pieces go to shared
+//             memory, [r][c], for the next chunk's phase 1
+//             O = scale (diag(g) P + A' U~): the phase-1 tile of the warp, written to o
+// Two barriers per chunk: after phase 1 (U~ complete) and after phase 2 (state pieces complete,
+// next chunk landed).
 constexpr int kScanThreads = 256;
-constexpr int kRowW = 72;          // padded W^T / A^T rows (floats): fragment loads hit 32 banks
-constexpr int kRowS = 24;          // padded S^T / U^T rows (floats)
-struct ScanBuf {
-    float wt[kD * kRowW];          // W^T [c][t]
-    float at[kC * kRowW];          // A^T [s][t]
-    float up[kRows * kC];          // U'^T rows r0 .. r0+15, [r][t]
+struct ScanStage {
+    __nv_bfloat16 w[3][kC * kD];   // W pieces [t][c], 256-byte swizzled rows
+    __nv_bfloat16 q[kC * kD];      // q rows [t][c]
+    __nv_bfloat16 k[kC * kD];      // k rows [t][c]
+    __nv_bfloat16 a[2][kC * kC];   // A' pieces [t][s], 128-byte swizzled rows
+    float up[kRows * kC];          // U'^T rows r0 .. r0 + 15, [r][t]
     float g[kC];
-    __nv_bfloat16 qb[kC * kRowB];  // q rows, padded
-    __nv_bfloat16 kb[kC * kRowB];  // k rows, padded
 };
-constexpr size_t kScanSmem = 2 * sizeof(ScanBuf) + sizeof(float) * (kD * kRowS + kC * kRowS + kC);
+constexpr size_t kScanSmem =
+    2 * sizeof(ScanStage) + sizeof(__nv_bfloat16) * (3 * kRows * kD + 3 * kRows * kC);
 
-__device__ __forceinline__ void scan_prefetch(ScanBuf& b, const __nv_bfloat16* __restrict__ q,
+__device__ __forceinline__ void scan_prefetch(ScanStage& b, const __nv_bfloat16* __restrict__ q,
                                               const __nv_bfloat16* __restrict__ k,
-                                              const float* __restrict__ wt,
+                                              const __nv_bfloat16* __restrict__ wp,
+                                              const __nv_bfloat16* __restrict__ ap,
                                               const float* __restrict__ ut,
-                                              const float* __restrict__ at,
                                               const float* __restrict__ gam, int64_t cj,
                                               int32_t r0, int32_t t0, int32_t len, int32_t h_qk,
                                               int32_t jq, int tid)
 {
-    const float* w = wt + cj * kD * kC;
-    for (int e = tid; e < kD * kC / 4; e += kScanThreads)
-        cp_async16(b.wt + (e / 16) * kRowW + (e % 16) * 4, w + 4 * e, 16);
-    const float* a = at + cj * kC * kC;
-    for (int e = tid; e < kC * kC / 4; e += kScanThreads)
-        cp_async16(b.at + (e / 16) * kRowW + (e % 16) * 4, a + 4 * e, 16);
+    uint8_t* wb = reinterpret_cast<uint8_t*>(b.w);
+    const __nv_bfloat16* w = wp + cj * 3 * kC * kD;
+    for (int e = tid; e < 3 * kC * 16; e += kScanThreads) {   // (piece, row) x 16 granules
+        const int row = e / 16, gr = e % 16;
+        cp_async16(wb + row * 256 + ((gr ^ (row & 7)) * 16), w + row * kD + gr * 8, 16);
+    }
+    uint8_t* ab = reinterpret_cast<uint8_t*>(b.a);
+    const __nv_bfloat16* a = ap + cj * 2 * kC * kC;
+    for (int e = tid; e < 2 * kC * 8; e += kScanThreads) {
+        const int row = e / 8, gr = e % 8;
+        cp_async16(ab + row * 128 + ((gr ^ (row & 7)) * 16), a + row * kC + gr * 8, 16);
+    }
+    uint8_t* qb = reinterpret_cast<uint8_t*>(b.q);
+    uint8_t* kb = reinterpret_cast<uint8_t*>(b.k);
+    for (int e = tid; e < kC * 16; e += kScanThreads) {
+        const int t = e / 16, gr = e % 16;
+        const bool valid = t < len;
+        const int64_t tok = static_cast<int64_t>(t0) + (valid ? t : 0);
+        const uint32_t off = t * 256 + ((gr ^ (t & 7)) * 16);
+        cp_async16(qb + off, q + (tok * h_qk + jq) * kD + gr * 8, valid ? 16u : 0u);
+        cp_async16(kb + off, k + (tok * h_qk + jq) * kD + gr * 8, valid ? 16u : 0u);
+    }
     const float* u = ut + (cj * kD + r0) * kC;
     for (int e = tid; e < kRows * kC / 4; e += kScanThreads) cp_async16(b.up + 4 * e, u + 4 * e, 16);
     if (tid < kC / 4) cp_async16(b.g + 4 * tid, gam + cj * kC + 4 * tid, 16);
-    for (int idx = tid; idx < kC * 16; idx += kScanThreads) {
-        const int t = idx / 16, p = idx % 16;
-        const bool valid = t < len;
-        const int64_t tok = static_cast<int64_t>(t0) + (valid ? t : 0);
-        cp_async16(b.qb + t * kRowB + p * 8, q + (tok * h_qk + jq) * kD + p * 8, valid ? 16u : 0u);
-        cp_async16(b.kb + t * kRowB + p * 8, k + (tok * h_qk + jq) * kD + p * 8, valid ? 16u : 0u);
-    }
     cp_async_commit();
-}
-
-__device__ __forceinline__ uint32_t tf32_rna(float x)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// x = hi + lo with hi, lo TF32 values (lo the TF32 rounding of x - hi)
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo)
-{
-    hi = tf32_rna(x);
-    lo = tf32_rna(x - __uint_as_float(hi));
-}
-
-// d += a * b for a 16 x 8 (k) A fragment and an 8 (k) x 8 B fragment (m16n8k8, TF32 -> f32)
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
-                 "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// d += A * B with fp32 A (a[4]) and B (b[2]) fragments, three TF32 passes
-__device__ __forceinline__ void mma_3xtf32(float (&d)[4], const float (&a)[4], const float (&b)[2])
-{
-    uint32_t ah[4], al[4], bh[2], bl[2];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) split_tf32(a[i], ah[i], al[i]);
-#pragma unroll
-    for (int i = 0; i < 2; ++i) split_tf32(b[i], bh[i], bl[i]);
-    mma_tf32(d, al[0], al[1], al[2], al[3], bh[0], bh[1]);
-    mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bl[0], bl[1]);
-    mma_tf32(d, ah[0], ah[1], ah[2], ah[3], bh[0], bh[1]);
 }
 
 __global__ void __launch_bounds__(kScanThreads, 1)
     gdn_scan_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                     const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_offset,
-                    const float* __restrict__ wt, const float* __restrict__ ut,
-                    const float* __restrict__ at, const float* __restrict__ gam,
+                    const __nv_bfloat16* __restrict__ wp, const __nv_bfloat16* __restrict__ ap,
+                    const float* __restrict__ ut, const float* __restrict__ gam,
                     const float* __restrict__ s0, float* __restrict__ s_final,
                     __nv_bfloat16* __restrict__ o, int32_t h_qk, int32_t h_v, float scale)
 {
@@ -397,134 +476,177 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const int32_t r0 = blockIdx.z * kRows;
     const int32_t jq = j / (h_v / h_qk);
     extern __shared__ __align__(16) uint8_t smraw[];
-    ScanBuf* buf = reinterpret_cast<ScanBuf*>(smraw);
-    float* St = reinterpret_cast<float*>(buf + 2);  // state transposed [c][r], 128 x 16 (+pad)
-    float* Ut = St + kD * kRowS;                    // U transposed [s][r], 64 x 16 (+pad)
-    float* kf = Ut + kC * kRowS;                    // [64] g_C / g_s
+    ScanStage* stage = reinterpret_cast<ScanStage*>(smraw);
+    uint8_t* sp = reinterpret_cast<uint8_t*>(stage + 2);      // state pieces [3][16][128], swizzled
+    uint8_t* up = sp + 3 * kRows * kD * 2;                      // U~ pieces [3][16][64], swizzled
     const int tid = threadIdx.x;
     const int warp = tid / 32, lane = tid % 32;
-    const int gq = lane >> 2, tg = lane & 3;        // fragment row group, thread in group
+    const int gq = lane >> 2, tg = lane & 3;
+    const int lr = lane & 7, lb = lane >> 3;                    // ldmatrix row, block
+    const uint32_t sp_s = smem_u32(sp), up_s = smem_u32(up);
 
+    // phase-2 ownership: key columns c = 16 warp + gq (+8), rows r = 8 n + 2 tg (+1)
+    const int c_own = 16 * warp + gq;
+    float st[2][4];
     const int64_t sbase = ((static_cast<int64_t>(i) * h_v + j) * kD + r0) * kD;
-    for (int e = tid; e < kRows * kD; e += kScanThreads)
-        St[(e % kD) * kRowS + e / kD] = s0 ? s0[sbase + e] : 0.f;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int c = c_own + 8 * (e >> 1), r = 8 * n + 2 * tg + (e & 1);
+            st[n][e] = s0 ? s0[sbase + r * kD + c] : 0.f;
+        }
+    // state pieces -> shared memory [r][c] (stmatrix .trans of the [c][r] fragments)
+    const auto store_state = [&]() {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const Pieces3 lo = split3(st[n][0], st[n][1]);   // rows c, pairs (r, r + 1)
+            const Pieces3 hi = split3(st[n][2], st[n][3]);   // rows c + 8
+            // block lb (lanes 8 lb ..): stored row r = 8 n + lr, columns c = 16 warp + 8 lb
+            const uint32_t addr = sw256(8 * n + lr, 16 * warp + 8 * (lb & 1));
+#pragma unroll
+            for (int p = 0; p < 3; ++p)
+                stsm_x2_trans(sp_s + p * kRows * 256 + addr, lo.p[p], hi.p[p]);
+        }
+    };
+    store_state();
 
     const int32_t c_begin = chunk_offset[i], c_end = chunk_offset[i + 1];
     const int32_t seq_start = cu[i], seq_end = cu[i + 1];
     const auto chunk_t0 = [&](int32_t ch) { return seq_start + (ch - c_begin) * kC; };
     if (c_begin < c_end)
-        scan_prefetch(buf[0], q, k, wt, ut, at, gam, static_cast<int64_t>(c_begin) * h_v + j, r0,
+        scan_prefetch(stage[0], q, k, wp, ap, ut, gam, static_cast<int64_t>(c_begin) * h_v + j, r0,
                       chunk_t0(c_begin), min(kC, seq_end - chunk_t0(c_begin)), h_qk, jq, tid);
-    // U and O: warp tile rows (tokens) m0 .. m0+15, columns (state rows) n0 .. n0+7
-    const int m0 = 16 * (warp >> 1), n0 = 8 * (warp & 1);
+    cp_async_wait_all();
+    __syncthreads();
+
+    // phase-1 / output ownership: tokens m0 .. m0 + 15, state rows n0 .. n0 + 7
+    const int mt = warp & 3, m0 = 16 * mt, n0 = 8 * (warp >> 2);
     for (int32_t ch = c_begin; ch < c_end; ++ch) {
         const int b = (ch - c_begin) & 1;
         const int32_t t0 = chunk_t0(ch);
         const int32_t len = min(kC, seq_end - t0);
-        cp_async_wait_all();
-        __syncthreads();   // chunk ch has landed; everyone is done with the other buffer
         if (ch + 1 < c_end)
-            scan_prefetch(buf[b ^ 1], q, k, wt, ut, at, gam, static_cast<int64_t>(ch + 1) * h_v + j,
+            scan_prefetch(stage[b ^ 1], q, k, wp, ap, ut, gam, static_cast<int64_t>(ch + 1) * h_v + j,
                           r0, chunk_t0(ch + 1), min(kC, seq_end - chunk_t0(ch + 1)), h_qk, jq, tid);
-        const ScanBuf& B = buf[b];
-        if (tid < kC) kf[tid] = B.g[kC - 1] / B.g[tid];
+        const ScanStage& B = stage[b];
+        const uint32_t w_s = smem_u32(B.w), q_s = smem_u32(B.q), k_s = smem_u32(B.k),
+                       a_s = smem_u32(B.a);
 
-        // U = U' - W S^T  (M = tokens, N = state rows, K = c)
-        {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int k0 = 0; k0 < kD; k0 += 8) {
-                const float a[4] = {B.wt[(k0 + tg) * kRowW + m0 + gq],
-                                    B.wt[(k0 + tg) * kRowW + m0 + gq + 8],
-                                    B.wt[(k0 + tg + 4) * kRowW + m0 + gq],
-                                    B.wt[(k0 + tg + 4) * kRowW + m0 + gq + 8]};
-                const float bb[2] = {St[(k0 + tg) * kRowS + n0 + gq],
-                                     St[(k0 + tg + 4) * kRowS + n0 + gq]};
-                mma_3xtf32(d, a, bb);
-            }
-            const int t = m0 + gq, r = n0 + 2 * tg;
-            Ut[t * kRowS + r] = B.up[r * kC + t] - d[0];
-            Ut[t * kRowS + r + 1] = B.up[(r + 1) * kC + t] - d[1];
-            Ut[(t + 8) * kRowS + r] = B.up[r * kC + t + 8] - d[2];
-            Ut[(t + 8) * kRowS + r + 1] = B.up[(r + 1) * kC + t + 8] - d[3];
+        // ---- phase 1: U = U' - W S^T, P = Q S^T over key columns c (8 steps of 16) ----
+        float u_hi[4] = {0.f, 0.f, 0.f, 0.f}, u_lo[4] = {0.f, 0.f, 0.f, 0.f},
+              u_l2[4] = {0.f, 0.f, 0.f, 0.f};
+        float pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+        for (int kk = 0; kk < kD / 16; ++kk) {
+            // A fragments (rows m0 + (lane % 16), columns 16 kk + 8 (lane / 16))
+            const uint32_t aoff = sw256(m0 + (lane & 15), 16 * kk + 8 * (lane >> 4));
+            uint32_t w0[4], w1[4], w2[4], qa[4];
+            ldsm_x4(w0, w_s + aoff);
+            ldsm_x4(w1, w_s + kC * 256 + aoff);
+            ldsm_x4(w2, w_s + 2 * kC * 256 + aoff);
+            ldsm_x4(qa, q_s + aoff);
+            // B fragments of the state pieces (rows n0 + lr, columns 16 kk + 8 (lb & 1));
+            // blocks 0, 1 = piece p, blocks 2, 3 = piece p + 1
+            const uint32_t boff = sw256(n0 + lr, 16 * kk + 8 * (lb & 1));
+            uint32_t s01[4], s2[2];
+            ldsm_x4(s01, sp_s + (lb >> 1) * kRows * 256 + boff);
+            ldsm_x2(s2, sp_s + 2 * kRows * 256 + boff);
+            mma_bf16(u_hi, w0, s01[0], s01[1]);
+            mma_bf16(u_lo, w0, s01[2], s01[3]);
+            mma_bf16(u_l2, w1, s01[0], s01[1]);
+            mma_bf16(pq, qa, s01[0], s01[1]);
+            mma_bf16(u_lo, w0, s2[0], s2[1]);
+            mma_bf16(u_l2, w1, s01[2], s01[3]);
+            mma_bf16(pq, qa, s01[2], s01[3]);
+            mma_bf16(u_lo, w2, s01[0], s01[1]);
+            mma_bf16(pq, qa, s2[0], s2[1]);
         }
-        __syncthreads();   // U complete
-
-        // O = scale (diag(g) Q S^T + A U)
+        // U~ = (g_C / g_t)(U' - W S^T) -> pieces [r][t] (stmatrix .trans of the [t][r] fragments)
         {
-            float qs[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int k0 = 0; k0 < kD; k0 += 8) {
-                // q is bf16: exact in TF32, so only the state needs a split
-                const uint32_t a0 = __float_as_uint(bf16_at(B.qb + (m0 + gq) * kRowB + k0 + tg));
-                const uint32_t a1 = __float_as_uint(bf16_at(B.qb + (m0 + gq + 8) * kRowB + k0 + tg));
-                const uint32_t a2 = __float_as_uint(bf16_at(B.qb + (m0 + gq) * kRowB + k0 + tg + 4));
-                const uint32_t a3 =
-                    __float_as_uint(bf16_at(B.qb + (m0 + gq + 8) * kRowB + k0 + tg + 4));
-                uint32_t bh0, bl0, bh1, bl1;
-                split_tf32(St[(k0 + tg) * kRowS + n0 + gq], bh0, bl0);
-                split_tf32(St[(k0 + tg + 4) * kRowS + n0 + gq], bh1, bl1);
-                mma_tf32(qs, a0, a1, a2, a3, bl0, bl1);
-                mma_tf32(qs, a0, a1, a2, a3, bh0, bh1);
-            }
-            for (int k0 = 0; k0 < m0 + 16; k0 += 8) {   // A[t][s] = 0 for s > t
-                const float a[4] = {B.at[(k0 + tg) * kRowW + m0 + gq],
-                                    B.at[(k0 + tg) * kRowW + m0 + gq + 8],
-                                    B.at[(k0 + tg + 4) * kRowW + m0 + gq],
-                                    B.at[(k0 + tg + 4) * kRowW + m0 + gq + 8]};
-                const float bb[2] = {Ut[(k0 + tg) * kRowS + n0 + gq],
-                                     Ut[(k0 + tg + 4) * kRowS + n0 + gq]};
-                mma_3xtf32(au, a, bb);
-            }
+            const float gc = B.g[kC - 1];
             const int t = m0 + gq, r = n0 + 2 * tg;
+            const float f0 = gc / B.g[t], f1 = gc / B.g[t + 8];
+            const float x0 = f0 * (B.up[r * kC + t] - (u_hi[0] + (u_lo[0] + u_l2[0])));
+            const float x1 = f0 * (B.up[(r + 1) * kC + t] - (u_hi[1] + (u_lo[1] + u_l2[1])));
+            const float x2 = f1 * (B.up[r * kC + t + 8] - (u_hi[2] + (u_lo[2] + u_l2[2])));
+            const float x3 = f1 * (B.up[(r + 1) * kC + t + 8] - (u_hi[3] + (u_lo[3] + u_l2[3])));
+            const Pieces3 lo = split3(x0, x1), hi = split3(x2, x3);
+            // block lb (lanes 8 lb ..): stored row r = n0 + lr, columns t = m0 + 8 lb
+            const uint32_t addr = sw128(n0 + lr, m0 + 8 * (lb & 1));
+#pragma unroll
+            for (int p = 0; p < 3; ++p) stsm_x2_trans(up_s + p * kRows * 128 + addr, lo.p[p], hi.p[p]);
+        }
+        __syncthreads();   // U~ complete
+
+        // ---- phase 2a: S_next^T[c][r] = g_C S^T + K^T U~ over tokens t (4 steps of 16) ----
+        {
+            const float gc = B.g[kC - 1];
+            float acc[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[n][e] = gc * st[n][e];
+#pragma unroll
+            for (int kk = 0; kk < kC / 16; ++kk) {
+                // A = K^T: ldmatrix .trans of k rows t = 16 kk + lr + 8 (lane / 16), columns
+                // c = 16 warp + 8 ((lane / 8) % 2)
+                uint32_t ka[4];
+                ldsm_x4_trans(ka, k_s + sw256(16 * kk + lr + 8 * (lane >> 4), 16 * warp + 8 * (lb & 1)));
+                // B = U~ pieces [r][t]: blocks 0, 1 = rows 0..7 (t halves), 2, 3 = rows 8..15
+                const uint32_t boff = sw128(lr + 8 * (lb >> 1), 16 * kk + 8 * (lb & 1));
+#pragma unroll
+                for (int p = 0; p < 3; ++p) {
+                    uint32_t ub[4];
+                    ldsm_x4(ub, up_s + p * kRows * 128 + boff);
+                    mma_bf16(acc[0], ka, ub[0], ub[1]);
+                    mma_bf16(acc[1], ka, ub[2], ub[3]);
+                }
+            }
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) st[n][e] = acc[n][e];
+        }
+
+        // ---- phase 2b: O = scale (diag(g) P + A' U~) over tokens s <= t ----
+        {
+            const int t = m0 + gq;
+            float oacc[4] = {B.g[t] * pq[0], B.g[t] * pq[1], B.g[t + 8] * pq[2], B.g[t + 8] * pq[3]};
+            for (int kk = 0; kk <= mt; ++kk) {
+                const uint32_t aoff = sw128(m0 + (lane & 15), 16 * kk + 8 * (lane >> 4));
+                uint32_t a0[4], a1[4];
+                ldsm_x4(a0, a_s + aoff);
+                ldsm_x4(a1, a_s + kC * 128 + aoff);
+                // U~ pieces 0 and 1, rows n0 + lr: blocks 0, 1 = piece 0, 2, 3 = piece 1
+                uint32_t ub[4];
+                ldsm_x4(ub, up_s + (lb >> 1) * kRows * 128 + sw128(n0 + lr, 16 * kk + 8 * (lb & 1)));
+                mma_bf16(oacc, a0, ub[0], ub[1]);
+                mma_bf16(oacc, a0, ub[2], ub[3]);
+                mma_bf16(oacc, a1, ub[0], ub[1]);
+            }
+            const int r = n0 + 2 * tg;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int tt = t + 8 * h;
-                if (tt < len) {
-                    const float gt = B.g[tt];
-                    const __nv_bfloat162 v2 =
-                        __floats2bfloat162_rn(scale * fmaf(gt, qs[2 * h], au[2 * h]),
-                                              scale * fmaf(gt, qs[2 * h + 1], au[2 * h + 1]));
-                    *reinterpret_cast<__nv_bfloat162*>(
-                        o + ((static_cast<int64_t>(t0) + tt) * h_v + j) * kD + r0 + r) = v2;
-                }
+                if (tt < len)
+                    *reinterpret_cast<uint32_t*>(
+                        o + ((static_cast<int64_t>(t0) + tt) * h_v + j) * kD + r0 + r) =
+                        pack_bf16(scale * oacc[2 * h], scale * oacc[2 * h + 1]);
             }
         }
-        __syncthreads();   // every reader of S is done before the update
-
-        // S^T_next = g_C S^T + Kd^T U with Kd[s][c] = (g_C / g_s) K[s][c]  (M = c, N = rows, K = s)
-        {
-            const float gC = B.g[kC - 1];
-            const int mc = 16 * warp;                 // state columns mc .. mc + 15
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int nn = 8 * nt;
-                const int c = mc + gq, r = nn + 2 * tg;
-                float d[4] = {gC * St[c * kRowS + r], gC * St[c * kRowS + r + 1],
-                              gC * St[(c + 8) * kRowS + r], gC * St[(c + 8) * kRowS + r + 1]};
-#pragma unroll 2
-                for (int k0 = 0; k0 < kC; k0 += 8) {
-                    const float f0 = kf[k0 + tg], f1 = kf[k0 + tg + 4];
-                    const float a[4] = {f0 * bf16_at(B.kb + (k0 + tg) * kRowB + mc + gq),
-                                        f0 * bf16_at(B.kb + (k0 + tg) * kRowB + mc + gq + 8),
-                                        f1 * bf16_at(B.kb + (k0 + tg + 4) * kRowB + mc + gq),
-                                        f1 * bf16_at(B.kb + (k0 + tg + 4) * kRowB + mc + gq + 8)};
-                    const float bb[2] = {Ut[(k0 + tg) * kRowS + nn + gq],
-                                         Ut[(k0 + tg + 4) * kRowS + nn + gq]};
-                    mma_3xtf32(d, a, bb);
-                }
-                St[c * kRowS + r] = d[0];
-                St[c * kRowS + r + 1] = d[1];
-                St[(c + 8) * kRowS + r] = d[2];
-                St[(c + 8) * kRowS + r + 1] = d[3];
-            }
-        }
+        store_state();
+        cp_async_wait_all();
+        __syncthreads();   // state pieces complete, chunk ch + 1 landed; U~ free
     }
-    cp_async_wait_all();
-    __syncthreads();
     if (s_final)
-        for (int e = tid; e < kRows * kD; e += kScanThreads)
-            s_final[sbase + e] = St[(e % kD) * kRowS + e / kD];
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = c_own + 8 * (e >> 1), r = 8 * n + 2 * tg + (e & 1);
+                s_final[sbase + r * kD + c] = st[n][e];
+            }
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
@@ -586,9 +708,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     auto* chunk_offset = reinterpret_cast<int32_t*>(ws + l.chunk_offset);
     auto* n_chunks = reinterpret_cast<int32_t*>(ws + l.n_chunks);
     auto* chunks = reinterpret_cast<int4*>(ws + l.chunks);
-    auto* wt = reinterpret_cast<float*>(ws + l.wt);
+    auto* wp = reinterpret_cast<__nv_bfloat16*>(ws + l.wp);
+    auto* ap = reinterpret_cast<__nv_bfloat16*>(ws + l.ap);
     auto* ut = reinterpret_cast<float*>(ws + l.ut);
-    auto* at = reinterpret_cast<float*>(ws + l.at);
     auto* gm = reinterpret_cast<float*>(ws + l.gam);
     const int64_t mc = max_chunks_for(total_tokens, n_seqs);
 
@@ -611,14 +733,14 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
         gdn_prepare_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
             static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
             static_cast<const __nv_bfloat16*>(v), alpha, beta, chunks, n_chunks,
-            static_cast<int32_t>(h_qk), static_cast<int32_t>(h_v), wt, ut, at, gm);
+            static_cast<int32_t>(h_qk), static_cast<int32_t>(h_v), wp, ap, ut, gm);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
     }
     const dim3 sgrid(static_cast<uint32_t>(n_seqs), static_cast<uint32_t>(h_v), kD / kRows);
     gdn_scan_kernel<<<sgrid, kScanThreads, kScanSmem, stream>>>(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), cu_seqlens,
-        chunk_offset, wt, ut, at, gm, initial_state, final_state,
+        chunk_offset, wp, ap, ut, gm, initial_state, final_state,
         static_cast<__nv_bfloat16*>(o), static_cast<int32_t>(h_qk), static_cast<int32_t>(h_v),
         scale);
     if ((e = cudaGetLastError()) != cudaSuccess)
