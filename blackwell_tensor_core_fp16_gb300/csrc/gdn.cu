@@ -31,8 +31,10 @@
 // A sequence's last chunk may be short: its missing tokens are read as q = k = v = 0,
 // alpha = 1, beta = 0 (the page's rule for packed tails), which leaves the state and the valid
 // outputs unchanged.  Non-product arithmetic is fp32; q, k, v and o are bfloat16.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdarg>
 #include <cstdint>
@@ -40,6 +42,7 @@
 #include <string>
 
 #include "../../include/gdn.h"
+#include "ptx.cuh"
 
 namespace {
 
@@ -66,9 +69,10 @@ int64_t max_chunks_for(int64_t T, int64_t n) { return T / kC + n; }
 //   wp   bf16 [cj][3][64][128]  W in three pieces, rows t, columns c
 //   ap   bf16 [cj][2][64][64]   A' in two pieces, rows t, columns s (zero for s > t)
 //   ut   f32  [cj][128][64]     U'^T, rows v, columns t
-//   gam  f32  [cj][64]          g_t
+//   gam  f32  [cj][128]         g_t (t < 64), then g_C / g_t
+// plus a status word the scan sets when a wait for its loads runs out (gdn_check_status).
 struct WsLayout {
-    size_t chunk_offset, n_chunks, chunks, wp, ap, ut, gam, total;
+    size_t status, chunk_offset, n_chunks, chunks, wp, ap, ut, gam, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -79,13 +83,14 @@ WsLayout layout_for(int64_t T, int64_t n, int64_t h_v)
     const size_t cj = mc * static_cast<size_t>(h_v);
     WsLayout l{};
     size_t o = 0;
+    l.status = o;       o = align256(o + sizeof(uint32_t));
     l.chunk_offset = o; o = align256(o + sizeof(int32_t) * static_cast<size_t>(n + 1));
     l.n_chunks = o;     o = align256(o + sizeof(int32_t));
     l.chunks = o;       o = align256(o + sizeof(int4) * mc);
     l.wp = o;           o = align256(o + sizeof(__nv_bfloat16) * cj * 3 * kC * kD);
     l.ap = o;           o = align256(o + sizeof(__nv_bfloat16) * cj * 2 * kC * kC);
     l.ut = o;           o = align256(o + sizeof(float) * cj * kD * kC);
-    l.gam = o;          o = align256(o + sizeof(float) * cj * kC);
+    l.gam = o;          o = align256(o + sizeof(float) * cj * 2 * kC);
     l.total = o;
     return l;
 }
@@ -93,8 +98,10 @@ WsLayout layout_for(int64_t T, int64_t n, int64_t h_v)
 // ---- chunk list: per sequence, ceil(len / 64) chunks, numbered in sequence order -------------
 __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_seqs,
                                       int32_t* __restrict__ chunk_offset, int4* __restrict__ chunks,
-                                      int32_t max_chunks, int32_t* __restrict__ n_chunks)
+                                      int32_t max_chunks, int32_t* __restrict__ n_chunks,
+                                      uint32_t* __restrict__ status)
 {
+    if (threadIdx.x == 0) *status = 0u;   // this call's scan reports into it
     __shared__ int32_t scan[1024];
     __shared__ int32_t carry;
     if (threadIdx.x == 0) carry = 0;
@@ -398,156 +405,213 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                 *reinterpret_cast<float4*>(dst + t) = make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
         }
     }
-    if (tid < kC) gam_out[cj * kC + tid] = g[tid];
+    if (tid < kC) {
+        gam_out[cj * 2 * kC + tid] = g[tid];
+        gam_out[cj * 2 * kC + kC + tid] = g[kC - 1] / g[tid];
+    }
 }
 
 // ---- per (sequence, value head, block of 16 value rows): the state scan over the chunks -------
-// Each chunk's operands are double-buffered in shared memory: while chunk c is computed,
-// cp.async brings chunk c + 1 (the W and A' pieces, q and k rows, the block's U'^T rows and the
-// decays).  Eight warps; each product runs on mma.sync m16n8k16 (bf16 -> fp32) with fragments
-// loaded by ldmatrix from XOR-swizzled tiles.
-//   phase 1   U = U' - W S^T and P = Q S^T: warp w owns tokens 16 (w % 4) .. + 15 and state
-//             rows 8 (w / 4) .. + 7; U~ = diag(g_C / g) U goes to shared memory as pieces, [r][t]
-//   phase 2   S_next^T = g_C S^T + K^T U~: warp w owns key columns 16 w .. + 15, all 16 rows; the
-//             fp32 state lives in these registers from chunk to chunk, and its pieces go to shared
-//             memory, [r][c], for the next chunk's phase 1
-//             O = scale (diag(g) P + A' U~): the phase-1 tile of the warp, written to o
-// Two barriers per chunk: after phase 1 (U~ complete) and after phase 2 (state pieces complete,
-// next chunk landed).
-constexpr int kScanThreads = 256;
-struct ScanStage {
-    __nv_bfloat16 w[3][kC * kD];   // W pieces [t][c], 256-byte swizzled rows
-    __nv_bfloat16 q[kC * kD];      // q rows [t][c]
-    __nv_bfloat16 k[kC * kD];      // k rows [t][c]
-    __nv_bfloat16 a[2][kC * kC];   // A' pieces [t][s], 128-byte swizzled rows
-    float up[kRows * kC];          // U'^T rows r0 .. r0 + 15, [r][t]
-    float g[kC];
-};
-constexpr size_t kScanSmem =
-    2 * sizeof(ScanStage) + sizeof(__nv_bfloat16) * (3 * kRows * kD + 3 * kRows * kC);
+// Each chunk's operands are double-buffered in shared memory and arrive by TMA: while chunk c is
+// computed, one thread has the tensor-memory-access unit bring chunk c + 1 (the W and A' pieces
+// and the q / k rows as 128-byte-swizzled boxes, the block's U'^T rows and the decays as bulk
+// copies), all completing on the stage's mbarrier.  Sixteen warps; each product runs on
+// mma.sync m16n8k16 (bf16 -> fp32) with fragments loaded by ldmatrix.
+//   phase 1   U = U' - W S^T and P = Q S^T: warp w owns tokens 16 (w % 4) .. + 15, state rows
+//             8 ((w / 4) % 2) .. + 7 and half h = w / 8 of the key columns; the upper half's
+//             partial U goes through shared memory to the lower half's warp, which forms
+//             U~ = diag(g_C / g) U and stores it as pieces, [r][t]
+//   phase 2   S_next^T = g_C S^T + K^T U~: warp w owns key columns 16 (w % 8) .. + 15 and state
+//             rows 8 (w / 8) .. + 7; the fp32 state lives in these registers from chunk to
+//             chunk, and its pieces go to shared memory, [r][c], for the next chunk's phase 1
+//             O = scale (diag(g) P + A' U~): both warps of a phase-1 tile add their half of
+//             diag(g) P and about half of the causal A' U~ steps; the lower warp's partial goes
+//             through shared memory and the upper warp writes the sum to o at the start of the
+//             next chunk (or after the last)
+// Three barriers per chunk: U partials ready, U~ complete, state pieces complete and the next
+// chunk's loads landed.
+constexpr int kScanThreads = 512;
+// shared-memory layout (offsets from a 1024-byte-aligned base)
+constexpr uint32_t kStageBytes = 98304;               // TMA boxes of one chunk
+constexpr uint32_t kOffW = 0;                         // W pieces: 2 column halves x 192 rows x 128 B
+constexpr uint32_t kOffQ = 49152;                     // q: 2 halves x 64 rows x 128 B
+constexpr uint32_t kOffK = 65536;                     // k: same
+constexpr uint32_t kOffA = 81920;                     // A' pieces: 128 rows x 128 B
+constexpr uint32_t kOffUp = 2 * kStageBytes;          // U'^T rows [stage][16][64] f32
+constexpr uint32_t kOffG = kOffUp + 2 * kRows * kC * 4;      // [stage][g_t | g_C / g_t] f32
+constexpr uint32_t kOffSp = kOffG + 2 * 2 * kC * 4;          // state pieces [3][16][128] bf16
+constexpr uint32_t kOffUt = kOffSp + 3 * kRows * kD * 2;     // U~ pieces [3][16][64] bf16
+constexpr uint32_t kOffPart = kOffUt + 3 * kRows * kC * 2;   // partial sums [8 warps][4][32] f32
+constexpr uint32_t kOffBar = kOffPart + 8 * 4 * 32 * 4;      // two mbarriers
+constexpr uint32_t kStageTx = kStageBytes + kRows * kC * 4 + 2 * kC * 4;   // bytes per chunk
+constexpr size_t kScanSmem = kOffBar + 16 + 1024;            // + slack to align the base
+static_assert(kScanSmem <= 232448, "scan shared memory");
+constexpr uint64_t kScanWaitNs = 2000000000ull;              // a load wait that runs out: 2 s
 
-__device__ __forceinline__ void scan_prefetch(ScanStage& b, const __nv_bfloat16* __restrict__ q,
-                                              const __nv_bfloat16* __restrict__ k,
-                                              const __nv_bfloat16* __restrict__ wp,
-                                              const __nv_bfloat16* __restrict__ ap,
-                                              const float* __restrict__ ut,
-                                              const float* __restrict__ gam, int64_t cj,
-                                              int32_t r0, int32_t t0, int32_t len, int32_t h_qk,
-                                              int32_t jq, int tid)
+// Byte offset of element (row, col) in a 128-column bf16 tile that TMA wrote as two 64-column
+// halves of `rows` 128-byte rows each, 128-byte swizzle (16-byte granule g of row r at g ^ (r % 8)).
+__device__ __forceinline__ uint32_t tsw(int row, int col, int rows)
 {
-    uint8_t* wb = reinterpret_cast<uint8_t*>(b.w);
-    const __nv_bfloat16* w = wp + cj * 3 * kC * kD;
-    for (int e = tid; e < 3 * kC * 16; e += kScanThreads) {   // (piece, row) x 16 granules
-        const int row = e / 16, gr = e % 16;
-        cp_async16(wb + row * 256 + ((gr ^ (row & 7)) * 16), w + row * kD + gr * 8, 16);
+    return static_cast<uint32_t>((col >> 6) * rows * 128 + row * 128 +
+                                 ((((col >> 3) & 7) ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
+// Bulk (untiled) global -> shared copy completing on an mbarrier of this CTA.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// One thread: announce the chunk's bytes on the stage barrier and start its loads.
+__device__ __forceinline__ void scan_issue(uint32_t base, int s, uint32_t bar,
+                                           const CUtensorMap* map_w, const CUtensorMap* map_a,
+                                           const CUtensorMap* map_q, const CUtensorMap* map_k,
+                                           const float* __restrict__ ut,
+                                           const float* __restrict__ gam, int64_t cj, int32_t r0,
+                                           int32_t t0, int32_t jq)
+{
+    gf16::mbar_arrive_expect_tx(bar, kStageTx);
+    const uint32_t st = base + s * kStageBytes;
+    const int32_t yw = static_cast<int32_t>(cj * 3 * kC), ya = static_cast<int32_t>(cj * 2 * kC);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        gf16::tma_load_2d(st + kOffW + h * 3 * kC * 128, map_w, bar, 64 * h, yw);
+        gf16::tma_load_3d(st + kOffQ + h * kC * 128, map_q, bar, 64 * h, jq, t0);
+        gf16::tma_load_3d(st + kOffK + h * kC * 128, map_k, bar, 64 * h, jq, t0);
     }
-    uint8_t* ab = reinterpret_cast<uint8_t*>(b.a);
-    const __nv_bfloat16* a = ap + cj * 2 * kC * kC;
-    for (int e = tid; e < 2 * kC * 8; e += kScanThreads) {
-        const int row = e / 8, gr = e % 8;
-        cp_async16(ab + row * 128 + ((gr ^ (row & 7)) * 16), a + row * kC + gr * 8, 16);
-    }
-    uint8_t* qb = reinterpret_cast<uint8_t*>(b.q);
-    uint8_t* kb = reinterpret_cast<uint8_t*>(b.k);
-    for (int e = tid; e < kC * 16; e += kScanThreads) {
-        const int t = e / 16, gr = e % 16;
-        const bool valid = t < len;
-        const int64_t tok = static_cast<int64_t>(t0) + (valid ? t : 0);
-        const uint32_t off = t * 256 + ((gr ^ (t & 7)) * 16);
-        cp_async16(qb + off, q + (tok * h_qk + jq) * kD + gr * 8, valid ? 16u : 0u);
-        cp_async16(kb + off, k + (tok * h_qk + jq) * kD + gr * 8, valid ? 16u : 0u);
-    }
-    const float* u = ut + (cj * kD + r0) * kC;
-    for (int e = tid; e < kRows * kC / 4; e += kScanThreads) cp_async16(b.up + 4 * e, u + 4 * e, 16);
-    if (tid < kC / 4) cp_async16(b.g + 4 * tid, gam + cj * kC + 4 * tid, 16);
-    cp_async_commit();
+    gf16::tma_load_2d(st + kOffA, map_a, bar, 0, ya);
+    bulk_g2s(base + kOffUp + s * kRows * kC * 4, ut + (cj * kD + r0) * kC, kRows * kC * 4, bar);
+    bulk_g2s(base + kOffG + s * 2 * kC * 4, gam + cj * 2 * kC, 2 * kC * 4, bar);
 }
 
 __global__ void __launch_bounds__(kScanThreads, 1)
-    gdn_scan_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                    const int32_t* __restrict__ cu, const int32_t* __restrict__ chunk_offset,
-                    const __nv_bfloat16* __restrict__ wp, const __nv_bfloat16* __restrict__ ap,
-                    const float* __restrict__ ut, const float* __restrict__ gam,
-                    const float* __restrict__ s0, float* __restrict__ s_final,
-                    __nv_bfloat16* __restrict__ o, int32_t h_qk, int32_t h_v, float scale)
+    gdn_scan_kernel(const __grid_constant__ CUtensorMap map_w,
+                    const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_k, const int32_t* __restrict__ cu,
+                    const int32_t* __restrict__ chunk_offset, const float* __restrict__ ut,
+                    const float* __restrict__ gam, const float* __restrict__ s0,
+                    float* __restrict__ s_final, __nv_bfloat16* __restrict__ o,
+                    uint32_t* __restrict__ status, int32_t h_v, int32_t group, float scale,
+                    uint64_t wait_ns)
 {
     const int32_t i = blockIdx.x;
     const int32_t j = blockIdx.y;
     const int32_t r0 = blockIdx.z * kRows;
-    const int32_t jq = j / (h_v / h_qk);
+    const int32_t jq = j / group;
     extern __shared__ __align__(16) uint8_t smraw[];
-    ScanStage* stage = reinterpret_cast<ScanStage*>(smraw);
-    uint8_t* sp = reinterpret_cast<uint8_t*>(stage + 2);      // state pieces [3][16][128], swizzled
-    uint8_t* up = sp + 3 * kRows * kD * 2;                      // U~ pieces [3][16][64], swizzled
+    const uint32_t raw = smem_u32(smraw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smraw + (base - raw);
+    const float* upf = reinterpret_cast<const float*>(gbase + kOffUp);
+    const float* gf = reinterpret_cast<const float*>(gbase + kOffG);
+    float* part = reinterpret_cast<float*>(gbase + kOffPart);
+    const uint32_t sp_s = base + kOffSp, up_s = base + kOffUt, bar0 = base + kOffBar;
     const int tid = threadIdx.x;
     const int warp = tid / 32, lane = tid % 32;
     const int gq = lane >> 2, tg = lane & 3;
     const int lr = lane & 7, lb = lane >> 3;                    // ldmatrix row, block
-    const uint32_t sp_s = smem_u32(sp), up_s = smem_u32(up);
 
-    // phase-2 ownership: key columns c = 16 warp + gq (+8), rows r = 8 n + 2 tg (+1)
-    const int c_own = 16 * warp + gq;
-    float st[2][4];
+    if (tid == 0) {
+        gf16::mbar_init(bar0, 1);
+        gf16::mbar_init(bar0 + 8, 1);
+        gf16::fence_mbarrier_init();
+    }
+
+    // phase-2 ownership: key columns c = 16 (warp % 8) + gq (+8), rows r = 8 (warp / 8) + 2 tg (+1)
+    const int mc = warp & 7, nr = warp >> 3;
+    float st[4];
     const int64_t sbase = ((static_cast<int64_t>(i) * h_v + j) * kD + r0) * kD;
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int c = c_own + 8 * (e >> 1), r = 8 * n + 2 * tg + (e & 1);
-            st[n][e] = s0 ? s0[sbase + r * kD + c] : 0.f;
-        }
+    for (int e = 0; e < 4; ++e) {
+        const int c = 16 * mc + gq + 8 * (e >> 1), r = 8 * nr + 2 * tg + (e & 1);
+        st[e] = s0 ? s0[sbase + r * kD + c] : 0.f;
+    }
     // state pieces -> shared memory [r][c] (stmatrix .trans of the [c][r] fragments)
+    const uint32_t st_addr = sp_s + sw256(8 * nr + lr, 16 * mc + 8 * (lb & 1));
     const auto store_state = [&]() {
+        const Pieces3 lo = split3(st[0], st[1]);   // rows c, pairs (r, r + 1)
+        const Pieces3 hi = split3(st[2], st[3]);   // rows c + 8
 #pragma unroll
-        for (int n = 0; n < 2; ++n) {
-            const Pieces3 lo = split3(st[n][0], st[n][1]);   // rows c, pairs (r, r + 1)
-            const Pieces3 hi = split3(st[n][2], st[n][3]);   // rows c + 8
-            // block lb (lanes 8 lb ..): stored row r = 8 n + lr, columns c = 16 warp + 8 lb
-            const uint32_t addr = sw256(8 * n + lr, 16 * warp + 8 * (lb & 1));
-#pragma unroll
-            for (int p = 0; p < 3; ++p)
-                stsm_x2_trans(sp_s + p * kRows * 256 + addr, lo.p[p], hi.p[p]);
-        }
+        for (int p = 0; p < 3; ++p) stsm_x2_trans(st_addr + p * kRows * 256, lo.p[p], hi.p[p]);
     };
     store_state();
 
     const int32_t c_begin = chunk_offset[i], c_end = chunk_offset[i + 1];
     const int32_t seq_start = cu[i], seq_end = cu[i + 1];
     const auto chunk_t0 = [&](int32_t ch) { return seq_start + (ch - c_begin) * kC; };
-    if (c_begin < c_end)
-        scan_prefetch(stage[0], q, k, wp, ap, ut, gam, static_cast<int64_t>(c_begin) * h_v + j, r0,
-                      chunk_t0(c_begin), min(kC, seq_end - chunk_t0(c_begin)), h_qk, jq, tid);
-    cp_async_wait_all();
-    __syncthreads();
+    const auto cj_of = [&](int32_t ch) { return static_cast<int64_t>(ch) * h_v + j; };
+    __syncthreads();   // barriers initialised, state pieces visible
+    if (tid == 0 && c_begin < c_end) {   // (a sequence with tokens: the maps are real)
+        gf16::prefetch_tensormap(&map_w);
+        gf16::prefetch_tensormap(&map_a);
+        gf16::prefetch_tensormap(&map_q);
+        gf16::prefetch_tensormap(&map_k);
+    }
+    if (tid == 0 && c_begin < c_end)
+        scan_issue(base, 0, bar0, &map_w, &map_a, &map_q, &map_k, ut, gam, cj_of(c_begin), r0,
+                   chunk_t0(c_begin), jq);
+    {
+        const bool ok = c_begin >= c_end || gf16::mbar_wait(bar0, 0, nullptr, wait_ns);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) atomicExch(status, 1u);
+            return;
+        }
+    }
 
-    // phase-1 / output ownership: tokens m0 .. m0 + 15, state rows n0 .. n0 + 7
-    const int mt = warp & 3, m0 = 16 * mt, n0 = 8 * (warp >> 2);
+    // phase-1 / output ownership: tokens m0 .. m0 + 15, state rows n0 .. n0 + 7, key half kh
+    const int mt = warp & 3, m0 = 16 * mt, n0 = 8 * ((warp >> 2) & 1), kh = warp >> 3;
+    float* mypart = part + (warp & 7) * 128 + lane;   // 4 values x 32 lanes per warp pair
+    // causal output steps kk = 0 .. mt: the lower warp takes kk < kmid, the upper the rest
+    const int kmid = (mt + 2) >> 1;
+    const int kk_lo = kh ? kmid : 0, kk_hi = kh ? mt + 1 : kmid;
+    float pend[4] = {0.f, 0.f, 0.f, 0.f};   // upper warps: own output partial, stored next chunk
+    int32_t pend_t0 = 0, pend_len = 0;
+    // upper warps: o = scale (own partial + the lower warp's partial in shared memory)
+    const auto flush_output = [&]() {
+        const int t = m0 + gq, r = n0 + 2 * tg;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int tt = t + 8 * h;
+            if (tt < pend_len)
+                *reinterpret_cast<uint32_t*>(
+                    o + ((static_cast<int64_t>(pend_t0) + tt) * h_v + j) * kD + r0 + r) =
+                    pack_bf16(scale * (pend[2 * h] + mypart[(2 * h) * 32]),
+                              scale * (pend[2 * h + 1] + mypart[(2 * h + 1) * 32]));
+        }
+        pend_len = 0;
+    };
+
     for (int32_t ch = c_begin; ch < c_end; ++ch) {
         const int b = (ch - c_begin) & 1;
         const int32_t t0 = chunk_t0(ch);
         const int32_t len = min(kC, seq_end - t0);
-        if (ch + 1 < c_end)
-            scan_prefetch(stage[b ^ 1], q, k, wp, ap, ut, gam, static_cast<int64_t>(ch + 1) * h_v + j,
-                          r0, chunk_t0(ch + 1), min(kC, seq_end - chunk_t0(ch + 1)), h_qk, jq, tid);
-        const ScanStage& B = stage[b];
-        const uint32_t w_s = smem_u32(B.w), q_s = smem_u32(B.q), k_s = smem_u32(B.k),
-                       a_s = smem_u32(B.a);
+        if (kh && pend_len > 0) flush_output();   // before this warp reuses its partial slot
+        if (tid == 0 && ch + 1 < c_end)
+            scan_issue(base, b ^ 1, bar0 + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut, gam,
+                       cj_of(ch + 1), r0, chunk_t0(ch + 1), jq);
+        const uint32_t sb = base + b * kStageBytes;
+        const uint32_t w_s = sb + kOffW, q_s = sb + kOffQ, k_s = sb + kOffK, a_s = sb + kOffA;
+        const float* Bup = upf + b * kRows * kC;   // U'^T rows [r][t]
+        const float* Bg = gf + b * 2 * kC;         // g_t, then g_C / g_t
 
-        // ---- phase 1: U = U' - W S^T, P = Q S^T over key columns c (8 steps of 16) ----
+        // ---- phase 1: U = U' - W S^T, P = Q S^T over this warp's 64 key columns ----
         float u_hi[4] = {0.f, 0.f, 0.f, 0.f}, u_lo[4] = {0.f, 0.f, 0.f, 0.f},
-              u_l2[4] = {0.f, 0.f, 0.f, 0.f};
-        float pq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-        for (int kk = 0; kk < kD / 16; ++kk) {
+              u_l2[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * kh + k4;
             // A fragments (rows m0 + (lane % 16), columns 16 kk + 8 (lane / 16))
-            const uint32_t aoff = sw256(m0 + (lane & 15), 16 * kk + 8 * (lane >> 4));
+            const int arow = m0 + (lane & 15), acol = 16 * kk + 8 * (lane >> 4);
             uint32_t w0[4], w1[4], w2[4], qa[4];
-            ldsm_x4(w0, w_s + aoff);
-            ldsm_x4(w1, w_s + kC * 256 + aoff);
-            ldsm_x4(w2, w_s + 2 * kC * 256 + aoff);
-            ldsm_x4(qa, q_s + aoff);
+            ldsm_x4(w0, w_s + tsw(arow, acol, 3 * kC));
+            ldsm_x4(w1, w_s + tsw(kC + arow, acol, 3 * kC));
+            ldsm_x4(w2, w_s + tsw(2 * kC + arow, acol, 3 * kC));
+            ldsm_x4(qa, q_s + tsw(arow, acol, kC));
             // B fragments of the state pieces (rows n0 + lr, columns 16 kk + 8 (lb & 1));
-            // blocks 0, 1 = piece p, blocks 2, 3 = piece p + 1
+            // x4 blocks 0, 1 = piece 0, blocks 2, 3 = piece 1; x2 = piece 2
             const uint32_t boff = sw256(n0 + lr, 16 * kk + 8 * (lb & 1));
             uint32_t s01[4], s2[2];
             ldsm_x4(s01, sp_s + (lb >> 1) * kRows * 256 + boff);
@@ -562,15 +626,24 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             mma_bf16(u_lo, w2, s01[0], s01[1]);
             mma_bf16(pq, qa, s2[0], s2[1]);
         }
-        // U~ = (g_C / g_t)(U' - W S^T) -> pieces [r][t] (stmatrix .trans of the [t][r] fragments)
-        {
-            const float gc = B.g[kC - 1];
+        float u[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[e] = u_hi[e] + (u_lo[e] + u_l2[e]);
+        if (kh) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mypart[e * 32] = u[e];
+        }
+        __syncthreads();   // upper-half partial U ready
+        if (!kh) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) u[e] += mypart[e * 32];
+            // U~ = (g_C / g_t)(U' - W S^T) -> pieces [r][t] (stmatrix .trans of [t][r] fragments)
             const int t = m0 + gq, r = n0 + 2 * tg;
-            const float f0 = gc / B.g[t], f1 = gc / B.g[t + 8];
-            const float x0 = f0 * (B.up[r * kC + t] - (u_hi[0] + (u_lo[0] + u_l2[0])));
-            const float x1 = f0 * (B.up[(r + 1) * kC + t] - (u_hi[1] + (u_lo[1] + u_l2[1])));
-            const float x2 = f1 * (B.up[r * kC + t + 8] - (u_hi[2] + (u_lo[2] + u_l2[2])));
-            const float x3 = f1 * (B.up[(r + 1) * kC + t + 8] - (u_hi[3] + (u_lo[3] + u_l2[3])));
+            const float f0 = Bg[kC + t], f1 = Bg[kC + t + 8];
+            const float x0 = f0 * (Bup[r * kC + t] - u[0]);
+            const float x1 = f0 * (Bup[(r + 1) * kC + t] - u[1]);
+            const float x2 = f1 * (Bup[r * kC + t + 8] - u[2]);
+            const float x3 = f1 * (Bup[(r + 1) * kC + t + 8] - u[3]);
             const Pieces3 lo = split3(x0, x1), hi = split3(x2, x3);
             // block lb (lanes 8 lb ..): stored row r = n0 + lr, columns t = m0 + 8 lb
             const uint32_t addr = sw128(n0 + lr, m0 + 8 * (lb & 1));
@@ -581,43 +654,37 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
         // ---- phase 2a: S_next^T[c][r] = g_C S^T + K^T U~ over tokens t (4 steps of 16) ----
         {
-            const float gc = B.g[kC - 1];
-            float acc[2][4];
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[n][e] = gc * st[n][e];
+            const float gc = Bg[kC - 1];
+            float acc[4] = {gc * st[0], gc * st[1], gc * st[2], gc * st[3]};
+            float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < kC / 16; ++kk) {
                 // A = K^T: ldmatrix .trans of k rows t = 16 kk + lr + 8 (lane / 16), columns
-                // c = 16 warp + 8 ((lane / 8) % 2)
+                // c = 16 mc + 8 ((lane / 8) % 2)
                 uint32_t ka[4];
-                ldsm_x4_trans(ka, k_s + sw256(16 * kk + lr + 8 * (lane >> 4), 16 * warp + 8 * (lb & 1)));
-                // B = U~ pieces [r][t]: blocks 0, 1 = rows 0..7 (t halves), 2, 3 = rows 8..15
-                const uint32_t boff = sw128(lr + 8 * (lb >> 1), 16 * kk + 8 * (lb & 1));
-#pragma unroll
-                for (int p = 0; p < 3; ++p) {
-                    uint32_t ub[4];
-                    ldsm_x4(ub, up_s + p * kRows * 128 + boff);
-                    mma_bf16(acc[0], ka, ub[0], ub[1]);
-                    mma_bf16(acc[1], ka, ub[2], ub[3]);
-                }
+                ldsm_x4_trans(ka, k_s + tsw(16 * kk + lr + 8 * (lane >> 4), 16 * mc + 8 * (lb & 1), kC));
+                // B = U~ pieces [r][t], rows 8 nr + lr: x4 = pieces 0, 1; x2 = piece 2
+                const uint32_t boff = sw128(8 * nr + lr, 16 * kk + 8 * (lb & 1));
+                uint32_t u01[4], u2[2];
+                ldsm_x4(u01, up_s + (lb >> 1) * kRows * 128 + boff);
+                ldsm_x2(u2, up_s + 2 * kRows * 128 + boff);
+                mma_bf16(acc, ka, u01[0], u01[1]);
+                mma_bf16(acc2, ka, u01[2], u01[3]);
+                mma_bf16(acc2, ka, u2[0], u2[1]);
             }
 #pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) st[n][e] = acc[n][e];
+            for (int e = 0; e < 4; ++e) st[e] = acc[e] + acc2[e];
         }
 
-        // ---- phase 2b: O = scale (diag(g) P + A' U~) over tokens s <= t ----
+        // ---- phase 2b: this warp's share of O = diag(g) P + A' U~ (tokens s <= t) ----
         {
             const int t = m0 + gq;
-            float oacc[4] = {B.g[t] * pq[0], B.g[t] * pq[1], B.g[t + 8] * pq[2], B.g[t + 8] * pq[3]};
-            for (int kk = 0; kk <= mt; ++kk) {
-                const uint32_t aoff = sw128(m0 + (lane & 15), 16 * kk + 8 * (lane >> 4));
+            float oacc[4] = {Bg[t] * pq[0], Bg[t] * pq[1], Bg[t + 8] * pq[2], Bg[t + 8] * pq[3]};
+            for (int kk = kk_lo; kk < kk_hi; ++kk) {
+                const int arow = m0 + (lane & 15), acol = 16 * kk + 8 * (lane >> 4);
                 uint32_t a0[4], a1[4];
-                ldsm_x4(a0, a_s + aoff);
-                ldsm_x4(a1, a_s + kC * 128 + aoff);
+                ldsm_x4(a0, a_s + sw128(arow, acol));
+                ldsm_x4(a1, a_s + sw128(kC + arow, acol));
                 // U~ pieces 0 and 1, rows n0 + lr: blocks 0, 1 = piece 0, 2, 3 = piece 1
                 uint32_t ub[4];
                 ldsm_x4(ub, up_s + (lb >> 1) * kRows * 128 + sw128(n0 + lr, 16 * kk + 8 * (lb & 1)));
@@ -625,28 +692,34 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 mma_bf16(oacc, a0, ub[2], ub[3]);
                 mma_bf16(oacc, a1, ub[0], ub[1]);
             }
-            const int r = n0 + 2 * tg;
+            if (!kh) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int tt = t + 8 * h;
-                if (tt < len)
-                    *reinterpret_cast<uint32_t*>(
-                        o + ((static_cast<int64_t>(t0) + tt) * h_v + j) * kD + r0 + r) =
-                        pack_bf16(scale * oacc[2 * h], scale * oacc[2 * h + 1]);
+                for (int e = 0; e < 4; ++e) mypart[e * 32] = oacc[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pend[e] = oacc[e];
+                pend_t0 = t0;
+                pend_len = len;
             }
         }
         store_state();
-        cp_async_wait_all();
-        __syncthreads();   // state pieces complete, chunk ch + 1 landed; U~ free
+        {
+            const bool ok = ch + 1 >= c_end ||
+                            gf16::mbar_wait(bar0 + 8 * (b ^ 1), ((ch + 1 - c_begin) >> 1) & 1,
+                                            nullptr, wait_ns);
+            if (__syncthreads_or(!ok)) {   // state pieces complete, chunk ch + 1 landed
+                if (tid == 0) atomicExch(status, 1u);
+                return;
+            }
+        }
     }
+    if (kh && pend_len > 0) flush_output();
     if (s_final)
 #pragma unroll
-        for (int n = 0; n < 2; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = c_own + 8 * (e >> 1), r = 8 * n + 2 * tg + (e & 1);
-                s_final[sbase + r * kD + c] = st[n][e];
-            }
+        for (int e = 0; e < 4; ++e) {
+            const int c = 16 * mc + gq + 8 * (e >> 1), r = 8 * nr + 2 * tg + (e & 1);
+            s_final[sbase + r * kD + c] = st[e];
+        }
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
@@ -673,6 +746,40 @@ int check(const void* q, const void* k, const void* v, const float* alpha, const
         return gdn_fail(GDN_ERR_INVALID_ARG, "a tensor pointer is null");
     if (T > 0 && (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(o)))
         return gdn_fail(GDN_ERR_UNSUPPORTED, "q, k, v and o must be 16-byte aligned");
+    return GDN_OK;
+}
+
+
+// ---- TMA descriptors of the scan's operands -----------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 gdn_encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult res{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &res) != cudaSuccess ||
+            res != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// A bfloat16 tensor of `rank` dimensions (dims[0] contiguous; strides in bytes of dims 1..),
+// read in boxes of `box` elements with the 128-byte swizzle (box[0] = 64 elements = 128 bytes).
+int gdn_make_map(CUtensorMap* map, const void* ptr, uint32_t rank, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box, const char* what)
+{
+    auto fn = gdn_encode_fn();
+    if (!fn) return gdn_fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return gdn_fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d) for %s", (int)r,
+                        what);
     return GDN_OK;
 }
 
@@ -705,6 +812,7 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
         return gdn_fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) needed",
                         l.total);
     auto* ws = static_cast<uint8_t*>(workspace);
+    auto* status = reinterpret_cast<uint32_t*>(ws + l.status);
     auto* chunk_offset = reinterpret_cast<int32_t*>(ws + l.chunk_offset);
     auto* n_chunks = reinterpret_cast<int32_t*>(ws + l.n_chunks);
     auto* chunks = reinterpret_cast<int4*>(ws + l.chunks);
@@ -713,6 +821,30 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     auto* ut = reinterpret_cast<float*>(ws + l.ut);
     auto* gm = reinterpret_cast<float*>(ws + l.gam);
     const int64_t mc = max_chunks_for(total_tokens, n_seqs);
+    if (mc * h_v * 3 * kC >= (int64_t(1) << 31))
+        return gdn_fail(GDN_ERR_UNSUPPORTED, "too many chunks x value heads for one call (%lld)",
+                        (long long)(mc * h_v));
+
+    // TMA descriptors: W pieces [cj * 192 rows][128], A' pieces [cj * 128 rows][64], q and k as
+    // {128, h_qk, total_tokens}.  With no tokens the scan loads nothing and they stay zero.
+    CUtensorMap map_w{}, map_a{}, map_q{}, map_k{};
+    if (total_tokens > 0) {
+        const cuuint64_t dw[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(mc * h_v * 3 * kC)};
+        const cuuint64_t sw[1] = {kD * 2};
+        const cuuint32_t bw[2] = {64, 3 * kC};
+        const cuuint64_t da[2] = {static_cast<cuuint64_t>(kC), static_cast<cuuint64_t>(mc * h_v * 2 * kC)};
+        const cuuint64_t sa[1] = {kC * 2};
+        const cuuint32_t ba[2] = {64, 2 * kC};
+        const cuuint64_t dq[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(h_qk),
+                                  static_cast<cuuint64_t>(total_tokens)};
+        const cuuint64_t sq[2] = {kD * 2, static_cast<cuuint64_t>(h_qk) * kD * 2};
+        const cuuint32_t bq[3] = {64, 1, kC};
+        if ((rc = gdn_make_map(&map_w, wp, 2, dw, sw, bw, "W pieces")) != GDN_OK ||
+            (rc = gdn_make_map(&map_a, ap, 2, da, sa, ba, "A' pieces")) != GDN_OK ||
+            (rc = gdn_make_map(&map_q, q, 3, dq, sq, bq, "q")) != GDN_OK ||
+            (rc = gdn_make_map(&map_k, k, 3, dq, sq, bq, "k")) != GDN_OK)
+            return rc;
+    }
 
     static bool attrs = false;
     if (!attrs) {
@@ -724,7 +856,7 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     }
     gdn_chunk_list_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, static_cast<int32_t>(n_seqs),
                                                   chunk_offset, chunks, static_cast<int32_t>(mc),
-                                                  n_chunks);
+                                                  n_chunks, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "gdn_chunk_list_kernel: %s", cudaGetErrorString(e));
@@ -739,10 +871,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     }
     const dim3 sgrid(static_cast<uint32_t>(n_seqs), static_cast<uint32_t>(h_v), kD / kRows);
     gdn_scan_kernel<<<sgrid, kScanThreads, kScanSmem, stream>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), cu_seqlens,
-        chunk_offset, wp, ap, ut, gm, initial_state, final_state,
-        static_cast<__nv_bfloat16*>(o), static_cast<int32_t>(h_qk), static_cast<int32_t>(h_v),
-        scale);
+        map_w, map_a, map_q, map_k, cu_seqlens, chunk_offset, ut, gm, initial_state, final_state,
+        static_cast<__nv_bfloat16*>(o), status, static_cast<int32_t>(h_v),
+        static_cast<int32_t>(h_v / h_qk), scale, kScanWaitNs);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "gdn_scan_kernel: %s", cudaGetErrorString(e));
     return GDN_OK;
