@@ -140,11 +140,6 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
     }
 }
 
-__device__ __forceinline__ float bf16_at(const __nv_bfloat16* p)
-{
-    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
-}
-
 // 16-byte global -> shared copy that completes asynchronously; src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, uint32_t src_bytes)
 {
@@ -234,15 +229,64 @@ __device__ __forceinline__ uint32_t sw128(int row, int col)
 
 // ---- per (chunk, value head): W, U'^T, A' and the cumulative decays ----------------------------
 // K, Q, V of the chunk sit in shared memory as padded bf16 rows.  Products K K^T and Q K^T run
-// on the tensor cores (bf16 operands, exact products).  Then (I + L) X = R
-// is solved for the 256 right-hand-side columns R = [diag(beta g) K | diag(beta) V] by forward
-// substitution, one column per thread with the column held in registers: no inverse is formed
-// and no barrier is needed inside the solve.
+// on the tensor cores (bf16 operands, exact products).  T = (I + L)^-1 is then built in the
+// page's doubling stages: the eight 8 x 8 diagonal blocks by substitution, then for block sizes
+// b = 8, 16, 32 each pair of neighbouring inverted blocks [A 0; C B] becomes
+// [A^-1 0; -B^-1 C A^-1  B^-1] (fp32 products).  Finally W = T diag(beta g) K and
+// U' = T diag(beta) V run on the tensor cores: T diag(.) as three bfloat16 pieces against the
+// exact bfloat16 K or V, the three products keeping fp32 accuracy.
 constexpr int kRowB = 136;     // padded bf16 rows of the prepare kernel (272 bytes)
 constexpr int kRowA = 72;      // padded bf16 rows of A' staging (144 bytes)
+constexpr int kRowL = 68;      // padded fp32 rows of L and T (272 bytes)
+constexpr int kRowY = 33;      // fp32 rows of the doubling scratch
 constexpr int kPrepThreads = 256;
 constexpr size_t kPrepSmem = sizeof(__nv_bfloat16) * (3 * kC * kRowB + 2 * kC * kRowA) +
-                             sizeof(float) * (kC * kC + 4 * kC);
+                             sizeof(float) * (2 * kC * kRowL + 4 * kC);
+static_assert(sizeof(__nv_bfloat16) * 2 * kC * kRowA >= sizeof(float) * 32 * kRowY,
+              "the doubling scratch reuses the A' staging");
+
+// One doubling stage of T = (I + L)^-1 for block size b (T holds the inverted b x b diagonal
+// blocks; their upper parts are zero): for each pair [A 0; C B] at rows / columns r0 = 2 p b, the
+// lower-left block of the inverse is -B^-1 (C A^-1).  The 32 rows (p, i) of each product take
+// 8 threads apiece, b / 8 columns per thread, full-length (zero-padded) dot products.
+template <int b>
+__device__ __forceinline__ void invert_doubling_stage(const float* Ls, float* Ts, float* Yb, int tid)
+{
+    constexpr int U = b / 8;
+    const int row = tid >> 3, l8 = tid & 7;
+    const int p = row / b, i = row % b, r0 = 2 * p * b;
+    float acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+    {   // Y = C A^-1
+        const float* crow = Ls + (r0 + b + i) * kRowL + r0;
+        const float* acol = Ts + r0 * kRowL + r0 + l8;
+#pragma unroll
+        for (int m = 0; m < b; ++m) {
+            const float c = crow[m];
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc[u] = fmaf(c, acol[m * kRowL + 8 * u], acc[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) Yb[row * kRowY + l8 + 8 * u] = acc[u];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = 0.f;
+    {   // lower-left block = -B^-1 Y
+        const float* brow = Ts + (r0 + b + i) * kRowL + r0 + b;
+        const float* ycol = Yb + p * b * kRowY + l8;
+#pragma unroll
+        for (int m = 0; m < b; ++m) {
+            const float bb = brow[m];
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc[u] = fmaf(bb, ycol[m * kRowY + 8 * u], acc[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) Ts[(r0 + b + i) * kRowL + r0 + l8 + 8 * u] = -acc[u];
+    }
+    __syncthreads();
+}
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
     gdn_prepare_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
@@ -264,8 +308,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     __nv_bfloat16* Qb = Kb + kC * kRowB;
     __nv_bfloat16* Vb = Qb + kC * kRowB;
     __nv_bfloat16* Ap = Vb + kC * kRowB;                             // [2][64][72] A' pieces
-    float* Ls = reinterpret_cast<float*>(Ap + 2 * kC * kRowA);       // [64][64] L, strictly lower
-    float* g = Ls + kC * kC;
+    float* Yb = reinterpret_cast<float*>(Ap);                         // [32][33], after A' is out
+    float* Ls = reinterpret_cast<float*>(Ap + 2 * kC * kRowA);       // [64][68] L, strictly lower
+    float* Ts = Ls + kC * kRowL;                                      // [64][68] T = (I + L)^-1
+    float* g = Ts + kC * kRowL;
     float* bt = g + kC;
     float* bg = bt + kC;
     float* al = bg + kC;
@@ -281,6 +327,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         cp_async16(Vb + t * kRowB + p * 8, v + (tok * h_v + j) * kD + p * 8, nb);
     }
     cp_async_commit();
+    for (int e = tid; e < kC * kRowL; e += kPrepThreads) Ts[e] = 0.f;   // upper blocks stay zero
     if (tid < kC) {
         const bool valid = tid < len;
         const int64_t tok = static_cast<int64_t>(t0) + tid;
@@ -301,6 +348,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         if (tid == 0) before = 1.f;
         g[2 * tid] = before * a0;
         g[2 * tid + 1] = p;
+        al[2 * tid] = 1.f / (before * a0);   // from here on al holds 1 / g
+        al[2 * tid + 1] = 1.f / p;
     }
     cp_async_wait_all();
     __syncthreads();
@@ -313,24 +362,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const int gq = lane >> 2, tg = lane & 3;
         const int m0 = 16 * (warp >> 1), nb = 32 * (warp & 1);
         float kk[4][4] = {}, qk[4][4] = {};
-        const auto ld32 = [](const __nv_bfloat16* p) { return *reinterpret_cast<const uint32_t*>(p); };
+        const int lr = lane & 7, lb = lane >> 3;
 #pragma unroll
         for (int k0 = 0; k0 < kD; k0 += 16) {
-            const uint32_t ka0 = ld32(Kb + (m0 + gq) * kRowB + k0 + 2 * tg);
-            const uint32_t ka1 = ld32(Kb + (m0 + gq + 8) * kRowB + k0 + 2 * tg);
-            const uint32_t ka2 = ld32(Kb + (m0 + gq) * kRowB + k0 + 2 * tg + 8);
-            const uint32_t ka3 = ld32(Kb + (m0 + gq + 8) * kRowB + k0 + 2 * tg + 8);
-            const uint32_t qa0 = ld32(Qb + (m0 + gq) * kRowB + k0 + 2 * tg);
-            const uint32_t qa1 = ld32(Qb + (m0 + gq + 8) * kRowB + k0 + 2 * tg);
-            const uint32_t qa2 = ld32(Qb + (m0 + gq) * kRowB + k0 + 2 * tg + 8);
-            const uint32_t qa3 = ld32(Qb + (m0 + gq + 8) * kRowB + k0 + 2 * tg + 8);
+            // A fragments: rows m0 + (lane % 16), columns k0 + 8 (lane / 16)
+            uint32_t ka[4], qa[4];
+            const int aoff = (m0 + (lane & 15)) * kRowB + k0 + 8 * (lane >> 4);
+            ldsm_x4(ka, smem_u32(Kb + aoff));
+            ldsm_x4(qa, smem_u32(Qb + aoff));
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int n0 = nb + 8 * nt;
-                const uint32_t b0 = ld32(Kb + (n0 + gq) * kRowB + k0 + 2 * tg);
-                const uint32_t b1 = ld32(Kb + (n0 + gq) * kRowB + k0 + 2 * tg + 8);
-                mma_bf16(kk[nt], ka0, ka1, ka2, ka3, b0, b1);
-                mma_bf16(qk[nt], qa0, qa1, qa2, qa3, b0, b1);
+            for (int np = 0; np < 2; ++np) {
+                // B fragments of n-tiles 2 np, 2 np + 1: k rows n0 + lr, columns k0 + 8 (lb % 2)
+                uint32_t kb4[4];
+                ldsm_x4(kb4, smem_u32(Kb + (nb + 16 * np + 8 * (lb >> 1) + lr) * kRowB + k0 +
+                                      8 * (lb & 1)));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    mma_bf16(kk[2 * np + h], ka, kb4[2 * h], kb4[2 * h + 1]);
+                    mma_bf16(qk[2 * np + h], qa, kb4[2 * h], kb4[2 * h + 1]);
+                }
             }
         }
         const float inv_gc = 1.f / g[kC - 1];
@@ -343,7 +393,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                 float av[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    Ls[t * kC + s + e] = s + e < t ? bt[t] * (g[t] / g[s + e]) * kk[nt][2 * h + e] : 0.f;
+                    Ls[t * kRowL + s + e] = s + e < t ? bt[t] * (g[t] * al[s + e]) * kk[nt][2 * h + e] : 0.f;
                     av[e] = s + e <= t ? (g[t] * inv_gc) * qk[nt][2 * h + e] : 0.f;
                 }
                 const Pieces3 pa = split3(av[0], av[1]);
@@ -364,45 +414,89 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
     }
 
-    // (I + L) X = R by forward substitution, one right-hand-side column per thread
-    {
-        const bool isw = tid < kD;
-        const int col = tid & (kD - 1);
-        const __nv_bfloat16* src = isw ? Kb : Vb;
-        const float* sc = isw ? bg : bt;
-        float x[kC];
+    // ---- T = (I + L)^-1 in doubling stages ----
+    // the eight 8 x 8 diagonal blocks, one column per thread by substitution
+    if (tid < kC) {
+        const int r0 = 8 * (tid >> 3), jj = tid & 7;
+        float x[8];
 #pragma unroll
-        for (int t = 0; t < kC; ++t) {
-            float acc[4] = {sc[t] * bf16_at(src + t * kRowB + col), 0.f, 0.f, 0.f};
+        for (int m = 0; m < 8; ++m) {
+            float acc = m == jj ? 1.f : 0.f;
 #pragma unroll
-            for (int s4 = 0; s4 < (t & ~3); s4 += 4) {
-                const float4 l = *reinterpret_cast<const float4*>(Ls + t * kC + s4);
-                acc[0] = fmaf(-l.x, x[s4], acc[0]);
-                acc[1] = fmaf(-l.y, x[s4 + 1], acc[1]);
-                acc[2] = fmaf(-l.z, x[s4 + 2], acc[2]);
-                acc[3] = fmaf(-l.w, x[s4 + 3], acc[3]);
-            }
-#pragma unroll
-            for (int s = t & ~3; s < t; ++s) acc[0] = fmaf(-Ls[t * kC + s], x[s], acc[0]);
-            x[t] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            for (int n = 0; n < m; ++n) acc = fmaf(-Ls[(r0 + m) * kRowL + r0 + n], x[n], acc);
+            x[m] = acc;
         }
-        if (isw) {
-            // W in three bfloat16 pieces, rows t, columns c
-            __nv_bfloat16* w = wp + cj * 3 * kC * kD + col;
 #pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                const __nv_bfloat16 p0 = __float2bfloat16_rn(x[t]);
-                const float r1 = x[t] - __bfloat162float(p0);
-                const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
-                w[t * kD] = p0;
-                w[(kC + t) * kD] = p1;
-                w[(2 * kC + t) * kD] = __float2bfloat16_rn(r1 - __bfloat162float(p1));
+        for (int m = 0; m < 8; ++m) Ts[(r0 + m) * kRowL + r0 + jj] = x[m];
+    }
+    __syncthreads();
+    invert_doubling_stage<8>(Ls, Ts, Yb, tid);
+    invert_doubling_stage<16>(Ls, Ts, Yb, tid);
+    invert_doubling_stage<32>(Ls, Ts, Yb, tid);
+
+    // ---- W = T diag(beta g) K (warps 0-3) and U' = T diag(beta) V (warps 4-7) ----
+    // Warp w owns rows t of m-tile mt (the two halves take the tiles in opposite orders, so that
+    // the two warps of a scheduler share 5 causal steps) and all 128 columns (16 n-tiles).
+    {
+        const int warp = tid / 32, lane = tid % 32;
+        const int gq = lane >> 2, tg = lane & 3, lr = lane & 7, lb = lane >> 3;
+        const int half = warp >> 2;
+        const int mt = half ? 3 - (warp & 3) : (warp & 3);
+        const float* sc = half ? bt : bg;
+        const __nv_bfloat16* src = half ? Vb : Kb;
+        float acc[16][4];
+#pragma unroll
+        for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+        for (int kk = 0; kk <= mt; ++kk) {
+            // A = T diag(sc) for rows 16 mt + gq (+8), columns 16 kk + 2 tg (+1, +8, +9), in pieces
+            const int ta = 16 * mt + gq, sa = 16 * kk + 2 * tg;
+            const float* T0 = Ts + ta * kRowL + sa;
+            const float* T1 = T0 + 8 * kRowL;
+            const float c0 = sc[sa], c1 = sc[sa + 1], c8 = sc[sa + 8], c9 = sc[sa + 9];
+            const Pieces3 a0 = split3(T0[0] * c0, T0[1] * c1);
+            const Pieces3 a1 = split3(T1[0] * c0, T1[1] * c1);
+            const Pieces3 a2 = split3(T0[8] * c8, T0[9] * c9);
+            const Pieces3 a3 = split3(T1[8] * c8, T1[9] * c9);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                // B = K or V rows s = 16 kk .. + 15, columns of n-tiles 2q and 2q+1 (ldmatrix .trans)
+                uint32_t bfr[4];
+                ldsm_x4_trans(bfr, smem_u32(src + (16 * kk + lr + 8 * (lb & 1)) * kRowB +
+                                            8 * (2 * q + (lb >> 1))));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t b0 = bfr[2 * h], b1 = bfr[2 * h + 1];
+#pragma unroll
+                    for (int pc = 0; pc < 3; ++pc)
+                        mma_bf16(acc[2 * q + h], a0.p[pc], a1.p[pc], a2.p[pc], a3.p[pc], b0, b1);
+                }
+            }
+        }
+        const int t = 16 * mt + gq;
+        if (!half) {
+            // W in three bfloat16 pieces, rows t, columns c
+            __nv_bfloat16* w = wp + cj * 3 * kC * kD;
+#pragma unroll
+            for (int n = 0; n < 16; ++n) {
+                const int c = 8 * n + 2 * tg;
+                const Pieces3 lo = split3(acc[n][0], acc[n][1]), hi = split3(acc[n][2], acc[n][3]);
+#pragma unroll
+                for (int pc = 0; pc < 3; ++pc) {
+                    *reinterpret_cast<uint32_t*>(w + (pc * kC + t) * kD + c) = lo.p[pc];
+                    *reinterpret_cast<uint32_t*>(w + (pc * kC + t + 8) * kD + c) = hi.p[pc];
+                }
             }
         } else {
-            float* dst = ut + (cj * kD + col) * kC;
+            // U'^T, rows v, columns t
+            float* u = ut + cj * kD * kC;
 #pragma unroll
-            for (int t = 0; t < kC; t += 4)
-                *reinterpret_cast<float4*>(dst + t) = make_float4(x[t], x[t + 1], x[t + 2], x[t + 3]);
+            for (int n = 0; n < 16; ++n) {
+                const int v0 = 8 * n + 2 * tg;
+                u[v0 * kC + t] = acc[n][0];
+                u[(v0 + 1) * kC + t] = acc[n][1];
+                u[v0 * kC + t + 8] = acc[n][2];
+                u[(v0 + 1) * kC + t + 8] = acc[n][3];
+            }
         }
     }
     if (tid < kC) {
