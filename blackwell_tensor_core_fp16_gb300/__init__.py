@@ -146,6 +146,12 @@ def load():
         lib.gdn_prefill.restype = i32
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
+        lib.gdn_check_status.argtypes = [vp, vp]
+        lib.gdn_check_status.restype = i32
+        lib.gdn_set_wait_timeout_ms.argtypes = [u32]
+        lib.gdn_set_wait_timeout_ms.restype = i32
+        lib.gdn_set_fault_injection.argtypes = [i32]
+        lib.gdn_set_fault_injection.restype = i32
         _lib = lib
         return lib
 
@@ -446,7 +452,7 @@ def gemm_mx(A, B, SFA, SFB, out=None, fmt_a: str = "e4m3", fmt_b: str = "e4m3",
 
 # ---- Gated Delta Net prefill ----------------------------------------------------------------------
 
-GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA = 0, 1, 2, 3
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT = 0, 1, 2, 3, 4
 
 
 def gdn_prefill_workspace_bytes(total_tokens: int, n_seqs: int, h_v: int) -> int:
@@ -468,6 +474,18 @@ def gdn_prefill(q: int, k: int, v: int, alpha: int, beta: int, cu_seqlens: int, 
 
 def gdn_last_error() -> str:
     return load().gdn_last_error().decode()
+
+
+def gdn_check_status(workspace: int, stream: int) -> int:
+    return load().gdn_check_status(workspace, stream)
+
+
+def gdn_set_wait_timeout_ms(ms: int) -> int:
+    return load().gdn_set_wait_timeout_ms(ms)
+
+
+def gdn_set_fault_injection(mode: int) -> int:
+    return load().gdn_set_fault_injection(mode)
 
 
 def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_state=None,

@@ -38,6 +38,7 @@
 
 #include <cstdarg>
 #include <cstdint>
+#include <atomic>
 #include <cstdio>
 #include <string>
 
@@ -51,6 +52,8 @@ constexpr int kD = 128;         // head dimension (dk = dv)
 constexpr int kRows = 16;       // value rows of the state per scan CTA
 
 thread_local std::string t_gdn_error;
+std::atomic<uint64_t> g_gdn_wait_ns{2000000000ull};   // limit of one wait for a chunk's loads
+std::atomic<uint32_t> g_gdn_fault{0};                 // testing hook (gdn_set_fault_injection)
 
 int gdn_fail(int code, const char* fmt, ...)
 {
@@ -540,7 +543,6 @@ constexpr uint32_t kOffBar = kOffPart + 8 * 4 * 32 * 4;      // two mbarriers
 constexpr uint32_t kStageTx = kStageBytes + kRows * kC * 4 + 2 * kC * 4;   // bytes per chunk
 constexpr size_t kScanSmem = kOffBar + 16 + 1024;            // + slack to align the base
 static_assert(kScanSmem <= 232448, "scan shared memory");
-constexpr uint64_t kScanWaitNs = 2000000000ull;              // a load wait that runs out: 2 s
 
 // Byte offset of element (row, col) in a 128-column bf16 tile that TMA wrote as two 64-column
 // halves of `rows` 128-byte rows each, 128-byte swizzle (16-byte granule g of row r at g ^ (r % 8)).
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     const float* __restrict__ gam, const float* __restrict__ s0,
                     float* __restrict__ s_final, __nv_bfloat16* __restrict__ o,
                     uint32_t* __restrict__ status, int32_t h_v, int32_t group, float scale,
-                    uint64_t wait_ns)
+                    uint64_t wait_ns, uint32_t fault)
 {
     const int32_t i = blockIdx.x;
     const int32_t j = blockIdx.y;
@@ -683,7 +685,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         const int32_t t0 = chunk_t0(ch);
         const int32_t len = min(kC, seq_end - t0);
         if (kh && pend_len > 0) flush_output();   // before this warp reuses its partial slot
-        if (tid == 0 && ch + 1 < c_end)
+        // (fault == 1, a testing hook: the second chunk's loads are never issued, so the wait
+        // for them runs out with nothing in flight)
+        if (tid == 0 && ch + 1 < c_end && !(fault == 1 && ch == c_begin))
             scan_issue(base, b ^ 1, bar0 + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut, gam,
                        cj_of(ch + 1), r0, chunk_t0(ch + 1), jq);
         const uint32_t sb = base + b * kStageBytes;
@@ -967,12 +971,42 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     gdn_scan_kernel<<<sgrid, kScanThreads, kScanSmem, stream>>>(
         map_w, map_a, map_q, map_k, cu_seqlens, chunk_offset, ut, gm, initial_state, final_state,
         static_cast<__nv_bfloat16*>(o), status, static_cast<int32_t>(h_v),
-        static_cast<int32_t>(h_v / h_qk), scale, kScanWaitNs);
+        static_cast<int32_t>(h_v / h_qk), scale, g_gdn_wait_ns.load(), g_gdn_fault.load());
     if ((e = cudaGetLastError()) != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "gdn_scan_kernel: %s", cudaGetErrorString(e));
     return GDN_OK;
 }
 
 const char* gdn_last_error(void) { return t_gdn_error.c_str(); }
+
+int gdn_check_status(const void* workspace, cudaStream_t stream)
+{
+    t_gdn_error.clear();
+    if (workspace == nullptr) return gdn_fail(GDN_ERR_INVALID_ARG, "workspace is null");
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, static_cast<const uint8_t*>(workspace) +
+                                               layout_for(0, 0, 1).status,
+                                    sizeof(word), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return gdn_fail(GDN_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+    if (word != 0)
+        return gdn_fail(GDN_ERR_TIMEOUT, "a scan CTA gave up a bounded wait for its chunk loads");
+    return GDN_OK;
+}
+
+int gdn_set_wait_timeout_ms(uint32_t ms)
+{
+    if (ms == 0) return gdn_fail(GDN_ERR_INVALID_ARG, "timeout must be at least 1 ms");
+    g_gdn_wait_ns.store(static_cast<uint64_t>(ms) * 1000000ull);
+    return GDN_OK;
+}
+
+int gdn_set_fault_injection(int mode)
+{
+    if (mode < 0 || mode > 1) return gdn_fail(GDN_ERR_INVALID_ARG, "unknown injection %d", mode);
+    g_gdn_fault.store(static_cast<uint32_t>(mode));
+    return GDN_OK;
+}
 
 }  // extern "C"

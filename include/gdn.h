@@ -42,8 +42,13 @@
  * Ownership: the caller owns every buffer; nothing is retained after a call.  Asynchronous on
  * `stream`.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, h_v not a multiple of
  * h_qk, workspace too small), GDN_ERR_UNSUPPORTED (head_dim other than 128, misaligned
- * q/k/v/o), GDN_ERR_CUDA (a launch failed; gdn_last_error() says why).  Nothing is enqueued on an
- * error.  n_seqs == 0 does nothing.
+ * q/k/v/o, more than 2^31 / 192 chunks x value heads), GDN_ERR_CUDA (a launch failed;
+ * gdn_last_error() says why).  Nothing is enqueued on an error.  n_seqs == 0 does nothing.
+ *
+ * Device-side failure: every wait of the scan kernel for a chunk's loads is bounded (default
+ * 2000 ms, gdn_set_wait_timeout_ms).  A wait that runs out makes the kernel stop cleanly and set
+ * a status word in the workspace, which gdn_check_status reads (GDN_ERR_TIMEOUT); the outputs of
+ * that call are then undefined.  Each gdn_prefill call clears the word when it starts.
  */
 #ifndef GDN_H
 #define GDN_H
@@ -60,6 +65,7 @@ extern "C" {
 #define GDN_ERR_INVALID_ARG 1
 #define GDN_ERR_UNSUPPORTED 2
 #define GDN_ERR_CUDA 3
+#define GDN_ERR_TIMEOUT 4
 
 /* Workspace bytes gdn_prefill needs for these sizes (an upper bound over all packings). */
 int gdn_prefill_workspace_bytes(int64_t total_tokens, int64_t n_seqs, int64_t h_v,
@@ -74,6 +80,20 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
 
 /* The message of the calling thread's last failed gdn_* call ("" if none). */
 const char* gdn_last_error(void);
+
+/* Waits for `stream`, then reads the status word of the last gdn_prefill call that used
+ * `workspace`: GDN_OK, or GDN_ERR_TIMEOUT if a scan CTA gave up a bounded wait; GDN_ERR_CUDA if
+ * the stream reported an error. */
+int gdn_check_status(const void* workspace, cudaStream_t stream);
+
+/* Limit of one wait of the scan kernel for a chunk's loads, for later calls of this process
+ * (ms >= 1; default 2000). */
+int gdn_set_wait_timeout_ms(uint32_t ms);
+
+/* Testing hook, 0 = off (default).  1: the scan kernels never issue the loads of each sequence's
+ * second chunk, so the wait for them runs out (nothing is in flight) and the call reports
+ * GDN_ERR_TIMEOUT through gdn_check_status.  For failure-detection tests only. */
+int gdn_set_fault_injection(int mode);
 
 #ifdef __cplusplus
 }

@@ -97,3 +97,44 @@ def test_block_scaled_wait_runs_out_and_context_survives(variant):
     d = D.cpu().double().numpy()
     ref, ref_abs = oracle.gemm_mx_f64(A, B, SA, SB)
     assert (np.abs(d - ref) <= oracle.tolerance_mx(ref, ref_abs, K, "f16")).all()
+
+
+def test_gdn_scan_wait_runs_out_and_context_survives():
+    """The Gated Delta Net scan waits on an mbarrier for each chunk's TMA loads.  With
+    gdn_set_fault_injection(1) the second chunk's loads are never issued, the 200 ms wait runs
+    out, every scan CTA stops cleanly and gdn_check_status reads GDN_ERR_TIMEOUT; the next call
+    (which clears the status word) matches the oracle."""
+    from blackwell_tensor_core_fp16_gb300.workloads import make_gdn_inputs
+    inp = make_gdn_inputs(200, 2, 1, 2, 128, 128, seed=702, state=True)
+    q, k, v = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda()
+    a, b, cu = inp["alpha"].cuda(), inp["beta"].cuda(), inp["cu_seqlens"].cuda()
+    s0 = inp["initial_state"].cuda()
+    T, n, h_qk, h_v = 200, 2, 1, 2
+    o = torch.zeros((T, h_v, 128), dtype=torch.bfloat16, device="cuda")
+    sf = torch.zeros((n, h_v, 128, 128), dtype=torch.float32, device="cuda")
+    need = g.gdn_prefill_workspace_bytes(T, n, h_v)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        return g.gdn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), a.data_ptr(), b.data_ptr(),
+                             cu.data_ptr(), n, T, h_qk, h_v, 128, 0.73, s0.data_ptr(),
+                             o.data_ptr(), sf.data_ptr(), ws.data_ptr(), need, s)
+
+    assert int(inp["cu_seqlens"].diff().max()) > 64, "a sequence needs a second chunk"
+    try:
+        assert g.gdn_set_wait_timeout_ms(200) == g.GDN_OK
+        assert g.gdn_set_fault_injection(1) == g.GDN_OK
+        assert call() == g.GDN_OK
+        assert g.gdn_check_status(ws.data_ptr(), s) == g.GDN_ERR_TIMEOUT
+        assert "bounded wait" in g.gdn_last_error()
+    finally:
+        g.gdn_set_fault_injection(0)
+        g.gdn_set_wait_timeout_ms(2000)
+    assert call() == g.GDN_OK
+    assert g.gdn_check_status(ws.data_ptr(), s) == g.GDN_OK
+    ref_o, ref_s = oracle.gdn_f64(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"],
+                                  inp["cu_seqlens"], 0.73, inp["initial_state"])
+    ob = o.float().cpu().double().numpy()
+    assert np.abs(ob - ref_o).max() <= 2.0 ** -6 * np.abs(ref_o).max()
+    assert np.abs(sf.cpu().double().numpy() - ref_s).max() <= 2.0 ** -16 * np.abs(ref_s).max()
