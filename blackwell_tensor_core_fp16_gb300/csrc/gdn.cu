@@ -297,13 +297,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                        const float* __restrict__ beta, const int4* __restrict__ chunks,
                        const int32_t* __restrict__ n_chunks, int32_t h_qk, int32_t h_v,
                        __nv_bfloat16* __restrict__ wp, __nv_bfloat16* __restrict__ ap,
-                       float* __restrict__ ut, float* __restrict__ gam_out)
+                       float* __restrict__ ut, float* __restrict__ gam_out, int32_t single_T,
+                       uint32_t* __restrict__ status)
 {
     const int32_t ch = blockIdx.x;
     const int32_t j = blockIdx.y;
-    if (ch >= *n_chunks) return;
-    const int4 info = chunks[ch];
-    const int32_t t0 = info.y, len = info.z;
+    // one sequence (single_T >= 0): chunk ch covers tokens 64 ch .. (no chunk list is built,
+    // and this kernel clears the call's status word); otherwise the chunk list says
+    int32_t t0, len;
+    if (single_T >= 0) {
+        t0 = ch * kC;
+        if (t0 >= single_T) return;
+        len = min(kC, single_T - t0);
+        if (ch == 0 && j == 0 && threadIdx.x == 0) *status = 0u;
+    } else {
+        if (ch >= *n_chunks) return;
+        const int4 info = chunks[ch];
+        t0 = info.y;
+        len = info.z;
+    }
     const int32_t jq = j / (h_v / h_qk);
     const int64_t cj = static_cast<int64_t>(ch) * h_v + j;
     extern __shared__ __align__(16) uint8_t smraw[];
@@ -591,7 +603,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     const float* __restrict__ gam, const float* __restrict__ s0,
                     float* __restrict__ s_final, __nv_bfloat16* __restrict__ o,
                     uint32_t* __restrict__ status, int32_t h_v, int32_t group, float scale,
-                    uint64_t wait_ns, uint32_t fault)
+                    uint64_t wait_ns, uint32_t fault, int32_t single_T)
 {
     const int32_t i = blockIdx.x;
     const int32_t j = blockIdx.y;
@@ -635,8 +647,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     };
     store_state();
 
-    const int32_t c_begin = chunk_offset[i], c_end = chunk_offset[i + 1];
-    const int32_t seq_start = cu[i], seq_end = cu[i + 1];
+    // one sequence (single_T >= 0): chunks 0 .. ceil(T / 64) - 1 of tokens 0 .. T - 1
+    const int32_t c_begin = single_T >= 0 ? 0 : chunk_offset[i];
+    const int32_t c_end = single_T >= 0 ? (single_T + kC - 1) / kC : chunk_offset[i + 1];
+    const int32_t seq_start = single_T >= 0 ? 0 : cu[i];
+    const int32_t seq_end = single_T >= 0 ? single_T : cu[i + 1];
     const auto chunk_t0 = [&](int32_t ch) { return seq_start + (ch - c_begin) * kC; };
     const auto cj_of = [&](int32_t ch) { return static_cast<int64_t>(ch) * h_v + j; };
     __syncthreads();   // barriers initialised, state pieces visible
@@ -952,18 +967,25 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                              static_cast<int>(kScanSmem));
         attrs = true;
     }
-    gdn_chunk_list_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, static_cast<int32_t>(n_seqs),
-                                                  chunk_offset, chunks, static_cast<int32_t>(mc),
-                                                  n_chunks, status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return gdn_fail(GDN_ERR_CUDA, "gdn_chunk_list_kernel: %s", cudaGetErrorString(e));
+    // One sequence with tokens: cu_seqlens is [0, total_tokens] by contract, so the kernels
+    // number the chunks themselves and the chunk-list launch is skipped.
+    const int32_t single_T = (n_seqs == 1 && total_tokens > 0) ? static_cast<int32_t>(total_tokens)
+                                                                : -1;
+    cudaError_t e = cudaSuccess;
+    if (single_T < 0) {
+        gdn_chunk_list_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, static_cast<int32_t>(n_seqs),
+                                                      chunk_offset, chunks,
+                                                      static_cast<int32_t>(mc), n_chunks, status);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return gdn_fail(GDN_ERR_CUDA, "gdn_chunk_list_kernel: %s", cudaGetErrorString(e));
+    }
     if (mc > 0 && total_tokens > 0) {
         const dim3 pgrid(static_cast<uint32_t>(mc), static_cast<uint32_t>(h_v));
         gdn_prepare_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
             static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
             static_cast<const __nv_bfloat16*>(v), alpha, beta, chunks, n_chunks,
-            static_cast<int32_t>(h_qk), static_cast<int32_t>(h_v), wp, ap, ut, gm);
+            static_cast<int32_t>(h_qk), static_cast<int32_t>(h_v), wp, ap, ut, gm, single_T,
+            status);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
     }
@@ -971,7 +993,8 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     gdn_scan_kernel<<<sgrid, kScanThreads, kScanSmem, stream>>>(
         map_w, map_a, map_q, map_k, cu_seqlens, chunk_offset, ut, gm, initial_state, final_state,
         static_cast<__nv_bfloat16*>(o), status, static_cast<int32_t>(h_v),
-        static_cast<int32_t>(h_v / h_qk), scale, g_gdn_wait_ns.load(), g_gdn_fault.load());
+        static_cast<int32_t>(h_v / h_qk), scale, g_gdn_wait_ns.load(), g_gdn_fault.load(),
+        single_T);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "gdn_scan_kernel: %s", cudaGetErrorString(e));
     return GDN_OK;

@@ -213,6 +213,15 @@ class GdnWorkload:
         the prediction (dv*dk), the rank-one update (dv*dk) and the output (dv*dk)."""
         return 2 * 3 * self.T * self.h_v * self.dv * self.dk
 
+    @property
+    def min_bytes(self) -> int:
+        """Bytes a call must move at least: q, k, v and o (bf16), alpha and beta (fp32), and the
+        fp32 initial and final states when the scenario carries them."""
+        b = 2 * self.T * (2 * self.h_qk * self.dk + 2 * self.h_v * self.dv) + 8 * self.T * self.h_v
+        if self.state:
+            b += 2 * 4 * self.n_seqs * self.h_v * self.dv * self.dk
+        return b
+
 
 GDN_WORKLOADS = {
     w.name: w
