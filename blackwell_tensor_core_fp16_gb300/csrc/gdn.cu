@@ -73,9 +73,11 @@ int64_t max_chunks_for(int64_t T, int64_t n) { return T / kC + n; }
 //   ap   bf16 [cj][2][64][64]   A' in two pieces, rows t, columns s (zero for s > t)
 //   ut   f32  [cj][128][64]     U'^T, rows v, columns t
 //   gam  f32  [cj][128]         g_t (t < 64), then g_C / g_t
-// plus a status word the scan sets when a wait for its loads runs out (gdn_check_status).
+// plus a status word the scan sets when a wait for its loads runs out (gdn_check_status), the
+// scan's work-item counter and the order in which it takes the sequences (with their chunk and
+// token ranges).
 struct WsLayout {
-    size_t status, chunk_offset, n_chunks, chunks, wp, ap, ut, gam, total;
+    size_t status, counter, order, seqinfo, chunk_offset, n_chunks, chunks, wp, ap, ut, gam, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -87,6 +89,9 @@ WsLayout layout_for(int64_t T, int64_t n, int64_t h_v)
     WsLayout l{};
     size_t o = 0;
     l.status = o;       o = align256(o + sizeof(uint32_t));
+    l.counter = o;      o = align256(o + sizeof(uint32_t));
+    l.order = o;        o = align256(o + sizeof(int32_t) * static_cast<size_t>(n));
+    l.seqinfo = o;      o = align256(o + sizeof(int4) * static_cast<size_t>(n));
     l.chunk_offset = o; o = align256(o + sizeof(int32_t) * static_cast<size_t>(n + 1));
     l.n_chunks = o;     o = align256(o + sizeof(int32_t));
     l.chunks = o;       o = align256(o + sizeof(int4) * mc);
@@ -102,10 +107,15 @@ WsLayout layout_for(int64_t T, int64_t n, int64_t h_v)
 __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_seqs,
                                       int32_t* __restrict__ chunk_offset, int4* __restrict__ chunks,
                                       int32_t max_chunks, int32_t* __restrict__ n_chunks,
-                                      uint32_t* __restrict__ status)
+                                      uint32_t* __restrict__ status, int32_t* __restrict__ order,
+                                      int4* __restrict__ seqinfo, uint32_t* __restrict__ counter)
 {
-    if (threadIdx.x == 0) *status = 0u;   // this call's scan reports into it
+    if (threadIdx.x == 0) {
+        *status = 0u;    // this call's scan reports into it
+        *counter = 0u;   // the scan's work-item counter
+    }
     __shared__ int32_t scan[1024];
+    __shared__ int32_t ncs[1024];
     __shared__ int32_t carry;
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
@@ -118,6 +128,7 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
             nc = len > 0 ? (len + kC - 1) / kC : 0;
         }
         scan[threadIdx.x] = nc;
+        ncs[threadIdx.x] = nc;
         __syncthreads();
         for (int32_t d = 1; d < static_cast<int32_t>(blockDim.x); d <<= 1) {   // inclusive scan
             const int32_t add = threadIdx.x >= static_cast<uint32_t>(d) ? scan[threadIdx.x - d] : 0;
@@ -140,6 +151,21 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
     if (threadIdx.x == 0) {
         chunk_offset[n_seqs] = carry;
         *n_chunks = carry;
+    }
+    __syncthreads();   // chunk_offset complete
+    // The scan takes sequences longest first (fewer idle SMs at the end): order[rank] = sequence,
+    // ranked by chunk count, ties by index, and seqinfo[rank] = {first chunk, end chunk, first
+    // token, end token}.  Up to 1024 sequences (the counts are still in ncs); beyond that, in
+    // index order.
+    for (int32_t i = threadIdx.x; i < n_seqs; i += blockDim.x) {
+        int32_t rank = i;
+        if (n_seqs <= static_cast<int32_t>(blockDim.x)) {
+            const int32_t mine = ncs[i];
+            rank = 0;
+            for (int32_t o = 0; o < n_seqs; ++o) rank += ncs[o] > mine || (ncs[o] == mine && o < i);
+        }
+        order[rank] = i;
+        seqinfo[rank] = make_int4(chunk_offset[i], chunk_offset[i + 1], cu[i], cu[i + 1]);
     }
 }
 
@@ -298,18 +324,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                        const int32_t* __restrict__ n_chunks, int32_t h_qk, int32_t h_v,
                        __nv_bfloat16* __restrict__ wp, __nv_bfloat16* __restrict__ ap,
                        float* __restrict__ ut, float* __restrict__ gam_out, int32_t single_T,
-                       uint32_t* __restrict__ status)
+                       uint32_t* __restrict__ status, uint32_t* __restrict__ counter)
 {
     const int32_t ch = blockIdx.x;
     const int32_t j = blockIdx.y;
     // one sequence (single_T >= 0): chunk ch covers tokens 64 ch .. (no chunk list is built,
-    // and this kernel clears the call's status word); otherwise the chunk list says
+    // and this kernel clears the call's status word and work counter); otherwise the chunk list
+    // says
     int32_t t0, len;
     if (single_T >= 0) {
         t0 = ch * kC;
         if (t0 >= single_T) return;
         len = min(kC, single_T - t0);
-        if (ch == 0 && j == 0 && threadIdx.x == 0) *status = 0u;
+        if (ch == 0 && j == 0 && threadIdx.x == 0) {
+            *status = 0u;
+            *counter = 0u;
+        }
     } else {
         if (ch >= *n_chunks) return;
         const int4 info = chunks[ch];
@@ -552,8 +582,9 @@ constexpr uint32_t kOffSp = kOffG + 2 * 2 * kC * 4;          // state pieces [3]
 constexpr uint32_t kOffUt = kOffSp + 3 * kRows * kD * 2;     // U~ pieces [3][16][64] bf16
 constexpr uint32_t kOffPart = kOffUt + 3 * kRows * kC * 2;   // partial sums [8 warps][4][32] f32
 constexpr uint32_t kOffBar = kOffPart + 8 * 4 * 32 * 4;      // two mbarriers
+constexpr uint32_t kOffItem = kOffBar + 16;                  // the CTA's next item
 constexpr uint32_t kStageTx = kStageBytes + kRows * kC * 4 + 2 * kC * 4;   // bytes per chunk
-constexpr size_t kScanSmem = kOffBar + 16 + 1024;            // + slack to align the base
+constexpr size_t kScanSmem = kOffItem + 16 + 1024;           // + slack to align the base
 static_assert(kScanSmem <= 232448, "scan shared memory");
 
 // Byte offset of element (row, col) in a 128-column bf16 tile that TMA wrote as two 64-column
@@ -594,21 +625,21 @@ __device__ __forceinline__ void scan_issue(uint32_t base, int s, uint32_t bar,
     bulk_g2s(base + kOffG + s * 2 * kC * 4, gam + cj * 2 * kC, 2 * kC * 4, bar);
 }
 
+// kMulti: a CTA may take more than one work item (more items than CTAs); without it every CTA
+// runs exactly item blockIdx.x and the scheduling code drops out.
+template <bool kMulti>
 __global__ void __launch_bounds__(kScanThreads, 1)
     gdn_scan_kernel(const __grid_constant__ CUtensorMap map_w,
                     const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_q,
-                    const __grid_constant__ CUtensorMap map_k, const int32_t* __restrict__ cu,
-                    const int32_t* __restrict__ chunk_offset, const float* __restrict__ ut,
+                    const __grid_constant__ CUtensorMap map_k, const int32_t* __restrict__ order,
+                    const int4* __restrict__ seqinfo, uint32_t* __restrict__ counter,
+                    int32_t n_items, const float* __restrict__ ut,
                     const float* __restrict__ gam, const float* __restrict__ s0,
                     float* __restrict__ s_final, __nv_bfloat16* __restrict__ o,
                     uint32_t* __restrict__ status, int32_t h_v, int32_t group, float scale,
                     uint64_t wait_ns, uint32_t fault, int32_t single_T)
 {
-    const int32_t i = blockIdx.x;
-    const int32_t j = blockIdx.y;
-    const int32_t r0 = blockIdx.z * kRows;
-    const int32_t jq = j / group;
     extern __shared__ __align__(16) uint8_t smraw[];
     const uint32_t raw = smem_u32(smraw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -616,6 +647,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const float* upf = reinterpret_cast<const float*>(gbase + kOffUp);
     const float* gf = reinterpret_cast<const float*>(gbase + kOffG);
     float* part = reinterpret_cast<float*>(gbase + kOffPart);
+    volatile int32_t* next_item = reinterpret_cast<volatile int32_t*>(gbase + kOffItem);
     const uint32_t sp_s = base + kOffSp, up_s = base + kOffUt, bar0 = base + kOffBar;
     const int tid = threadIdx.x;
     const int warp = tid / 32, lane = tid % 32;
@@ -628,15 +660,42 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         gf16::fence_mbarrier_init();
     }
 
+    // Work items are (sequence, value head, block of 16 state rows), numbered sequence-major in
+    // the order `order` gives (longest sequences first); item q -> rank q / (8 h_v), head
+    // (q / 8) % h_v, rows 16 (q % 8) ...  With G = gridDim.x, CTA b's first item is b and each
+    // later one G + a value drawn from `counter` when the item before it starts (a
+    // longest-processing-time schedule).  Thread 0 makes the draw as the item starts and
+    // publishes it at the first chunk's middle barrier; the next item's table entry is loaded
+    // then and used at the end, when the last chunk has already fetched the next item's first
+    // chunk.  With no more items than CTAs nothing is drawn.
+    struct Item {
+        int32_t i, j, r0, c_begin, c_end, seq_start, seq_end;
+    };
+    const auto decode = [&](int32_t q) {
+        Item it;
+        const int32_t rank = q / (8 * h_v), rem = q - rank * 8 * h_v;
+        it.j = rem >> 3;
+        it.r0 = (rem & 7) * kRows;
+        if (single_T >= 0) {   // one sequence: chunks 0 .. ceil(T / 64) - 1 of tokens 0 .. T - 1
+            it.i = 0;
+            it.c_begin = 0;
+            it.c_end = (single_T + kC - 1) / kC;
+            it.seq_start = 0;
+            it.seq_end = single_T;
+        } else {               // two independent loads (their use can come much later)
+            it.i = order[rank];
+            const int4 si = seqinfo[rank];
+            it.c_begin = si.x;
+            it.c_end = si.y;
+            it.seq_start = si.z;
+            it.seq_end = si.w;
+        }
+        return it;
+    };
+
     // phase-2 ownership: key columns c = 16 (warp % 8) + gq (+8), rows r = 8 (warp / 8) + 2 tg (+1)
     const int mc = warp & 7, nr = warp >> 3;
-    float st[4];
-    const int64_t sbase = ((static_cast<int64_t>(i) * h_v + j) * kD + r0) * kD;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int c = 16 * mc + gq + 8 * (e >> 1), r = 8 * nr + 2 * tg + (e & 1);
-        st[e] = s0 ? s0[sbase + r * kD + c] : 0.f;
-    }
+    float st[4] = {0.f, 0.f, 0.f, 0.f};
     // state pieces -> shared memory [r][c] (stmatrix .trans of the [c][r] fragments)
     const uint32_t st_addr = sp_s + sw256(8 * nr + lr, 16 * mc + 8 * (lb & 1));
     const auto store_state = [&]() {
@@ -645,194 +704,232 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
         for (int p = 0; p < 3; ++p) stsm_x2_trans(st_addr + p * kRows * 256, lo.p[p], hi.p[p]);
     };
-    store_state();
-
-    // one sequence (single_T >= 0): chunks 0 .. ceil(T / 64) - 1 of tokens 0 .. T - 1
-    const int32_t c_begin = single_T >= 0 ? 0 : chunk_offset[i];
-    const int32_t c_end = single_T >= 0 ? (single_T + kC - 1) / kC : chunk_offset[i + 1];
-    const int32_t seq_start = single_T >= 0 ? 0 : cu[i];
-    const int32_t seq_end = single_T >= 0 ? single_T : cu[i + 1];
-    const auto chunk_t0 = [&](int32_t ch) { return seq_start + (ch - c_begin) * kC; };
-    const auto cj_of = [&](int32_t ch) { return static_cast<int64_t>(ch) * h_v + j; };
-    __syncthreads();   // barriers initialised, state pieces visible
-    if (tid == 0 && c_begin < c_end) {   // (a sequence with tokens: the maps are real)
-        gf16::prefetch_tensormap(&map_w);
-        gf16::prefetch_tensormap(&map_a);
-        gf16::prefetch_tensormap(&map_q);
-        gf16::prefetch_tensormap(&map_k);
-    }
-    if (tid == 0 && c_begin < c_end)
-        scan_issue(base, 0, bar0, &map_w, &map_a, &map_q, &map_k, ut, gam, cj_of(c_begin), r0,
-                   chunk_t0(c_begin), jq);
-    {
-        const bool ok = c_begin >= c_end || gf16::mbar_wait(bar0, 0, nullptr, wait_ns);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicExch(status, 1u);
-            return;
-        }
-    }
-
     // phase-1 / output ownership: tokens m0 .. m0 + 15, state rows n0 .. n0 + 7, key half kh
     const int mt = warp & 3, m0 = 16 * mt, n0 = 8 * ((warp >> 2) & 1), kh = warp >> 3;
     float* mypart = part + (warp & 7) * 128 + lane;   // 4 values x 32 lanes per warp pair
     // causal output steps kk = 0 .. mt: the lower warp takes kk < kmid, the upper the rest
     const int kmid = (mt + 2) >> 1;
     const int kk_lo = kh ? kmid : 0, kk_hi = kh ? mt + 1 : kmid;
-    float pend[4] = {0.f, 0.f, 0.f, 0.f};   // upper warps: own output partial, stored next chunk
-    int32_t pend_t0 = 0, pend_len = 0;
-    // upper warps: o = scale (own partial + the lower warp's partial in shared memory)
-    const auto flush_output = [&]() {
-        const int t = m0 + gq, r = n0 + 2 * tg;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int tt = t + 8 * h;
-            if (tt < pend_len)
-                *reinterpret_cast<uint32_t*>(
-                    o + ((static_cast<int64_t>(pend_t0) + tt) * h_v + j) * kD + r0 + r) =
-                    pack_bf16(scale * (pend[2 * h] + mypart[(2 * h) * 32]),
-                              scale * (pend[2 * h + 1] + mypart[(2 * h + 1) * 32]));
-        }
-        pend_len = 0;
-    };
 
-    for (int32_t ch = c_begin; ch < c_end; ++ch) {
-        const int b = (ch - c_begin) & 1;
-        const int32_t t0 = chunk_t0(ch);
-        const int32_t len = min(kC, seq_end - t0);
-        if (kh && pend_len > 0) flush_output();   // before this warp reuses its partial slot
-        // (fault == 1, a testing hook: the second chunk's loads are never issued, so the wait
-        // for them runs out with nothing in flight)
-        if (tid == 0 && ch + 1 < c_end && !(fault == 1 && ch == c_begin))
-            scan_issue(base, b ^ 1, bar0 + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut, gam,
-                       cj_of(ch + 1), r0, chunk_t0(ch + 1), jq);
-        const uint32_t sb = base + b * kStageBytes;
-        const uint32_t w_s = sb + kOffW, q_s = sb + kOffQ, k_s = sb + kOffK, a_s = sb + kOffA;
-        const float* Bup = upf + b * kRows * kC;   // U'^T rows [r][t]
-        const float* Bg = gf + b * 2 * kC;         // g_t, then g_C / g_t
-
-        // ---- phase 1: U = U' - W S^T, P = Q S^T over this warp's 64 key columns ----
-        float u_hi[4] = {0.f, 0.f, 0.f, 0.f}, u_lo[4] = {0.f, 0.f, 0.f, 0.f},
-              u_l2[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t n = 0;            // chunk loads consumed by this CTA: stage n % 2, phase n / 2
+    bool have_first = false;   // the current item's first chunk was loaded by the previous item
+    const int32_t G = static_cast<int32_t>(gridDim.x);
+    const bool draws = kMulti && n_items > G;
+    Item it = decode(blockIdx.x);
+    if (tid == 0 && it.c_begin < it.c_end) {   // (this CTA loads chunks: the maps are real)
+        gf16::prefetch_tensormap(&map_w);
+        gf16::prefetch_tensormap(&map_a);
+        gf16::prefetch_tensormap(&map_q);
+        gf16::prefetch_tensormap(&map_k);
+    }
+    for (int32_t q = blockIdx.x; q < n_items;) {
+        uint32_t drawn = 0;   // (thread 0) the draw for the next item
+        if (tid == 0 && draws) drawn = atomicAdd(counter, 1u);
+        int32_t qn = n_items;   // the next item, known from the first chunk's middle barrier
+        Item nx{};
+        const int32_t j = it.j, r0 = it.r0, jq = j / group;
+        const int32_t c_begin = it.c_begin, c_end = it.c_end;
+        const int32_t seq_start = it.seq_start, seq_end = it.seq_end;
+        const auto chunk_t0 = [&](int32_t ch) { return seq_start + (ch - c_begin) * kC; };
+        const auto cj_of = [&](int32_t ch) { return static_cast<int64_t>(ch) * h_v + j; };
+        const int64_t sbase = ((static_cast<int64_t>(it.i) * h_v + j) * kD + r0) * kD;
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-            const int kk = 4 * kh + k4;
-            // A fragments (rows m0 + (lane % 16), columns 16 kk + 8 (lane / 16))
-            const int arow = m0 + (lane & 15), acol = 16 * kk + 8 * (lane >> 4);
-            uint32_t w0[4], w1[4], w2[4], qa[4];
-            ldsm_x4(w0, w_s + tsw(arow, acol, 3 * kC));
-            ldsm_x4(w1, w_s + tsw(kC + arow, acol, 3 * kC));
-            ldsm_x4(w2, w_s + tsw(2 * kC + arow, acol, 3 * kC));
-            ldsm_x4(qa, q_s + tsw(arow, acol, kC));
-            // B fragments of the state pieces (rows n0 + lr, columns 16 kk + 8 (lb & 1));
-            // x4 blocks 0, 1 = piece 0, blocks 2, 3 = piece 1; x2 = piece 2
-            const uint32_t boff = sw256(n0 + lr, 16 * kk + 8 * (lb & 1));
-            uint32_t s01[4], s2[2];
-            ldsm_x4(s01, sp_s + (lb >> 1) * kRows * 256 + boff);
-            ldsm_x2(s2, sp_s + 2 * kRows * 256 + boff);
-            mma_bf16(u_hi, w0, s01[0], s01[1]);
-            mma_bf16(u_lo, w0, s01[2], s01[3]);
-            mma_bf16(u_l2, w1, s01[0], s01[1]);
-            mma_bf16(pq, qa, s01[0], s01[1]);
-            mma_bf16(u_lo, w0, s2[0], s2[1]);
-            mma_bf16(u_l2, w1, s01[2], s01[3]);
-            mma_bf16(pq, qa, s01[2], s01[3]);
-            mma_bf16(u_lo, w2, s01[0], s01[1]);
-            mma_bf16(pq, qa, s2[0], s2[1]);
-        }
-        float u[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) u[e] = u_hi[e] + (u_lo[e] + u_l2[e]);
-        if (kh) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) mypart[e * 32] = u[e];
-        }
-        __syncthreads();   // upper-half partial U ready
-        if (!kh) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) u[e] += mypart[e * 32];
-            // U~ = (g_C / g_t)(U' - W S^T) -> pieces [r][t] (stmatrix .trans of [t][r] fragments)
-            const int t = m0 + gq, r = n0 + 2 * tg;
-            const float f0 = Bg[kC + t], f1 = Bg[kC + t + 8];
-            const float x0 = f0 * (Bup[r * kC + t] - u[0]);
-            const float x1 = f0 * (Bup[(r + 1) * kC + t] - u[1]);
-            const float x2 = f1 * (Bup[r * kC + t + 8] - u[2]);
-            const float x3 = f1 * (Bup[(r + 1) * kC + t + 8] - u[3]);
-            const Pieces3 lo = split3(x0, x1), hi = split3(x2, x3);
-            // block lb (lanes 8 lb ..): stored row r = n0 + lr, columns t = m0 + 8 lb
-            const uint32_t addr = sw128(n0 + lr, m0 + 8 * (lb & 1));
-#pragma unroll
-            for (int p = 0; p < 3; ++p) stsm_x2_trans(up_s + p * kRows * 128 + addr, lo.p[p], hi.p[p]);
-        }
-        __syncthreads();   // U~ complete
-
-        // ---- phase 2a: S_next^T[c][r] = g_C S^T + K^T U~ over tokens t (4 steps of 16) ----
-        {
-            const float gc = Bg[kC - 1];
-            float acc[4] = {gc * st[0], gc * st[1], gc * st[2], gc * st[3]};
-            float acc2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < kC / 16; ++kk) {
-                // A = K^T: ldmatrix .trans of k rows t = 16 kk + lr + 8 (lane / 16), columns
-                // c = 16 mc + 8 ((lane / 8) % 2)
-                uint32_t ka[4];
-                ldsm_x4_trans(ka, k_s + tsw(16 * kk + lr + 8 * (lane >> 4), 16 * mc + 8 * (lb & 1), kC));
-                // B = U~ pieces [r][t], rows 8 nr + lr: x4 = pieces 0, 1; x2 = piece 2
-                const uint32_t boff = sw128(8 * nr + lr, 16 * kk + 8 * (lb & 1));
-                uint32_t u01[4], u2[2];
-                ldsm_x4(u01, up_s + (lb >> 1) * kRows * 128 + boff);
-                ldsm_x2(u2, up_s + 2 * kRows * 128 + boff);
-                mma_bf16(acc, ka, u01[0], u01[1]);
-                mma_bf16(acc2, ka, u01[2], u01[3]);
-                mma_bf16(acc2, ka, u2[0], u2[1]);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) st[e] = acc[e] + acc2[e];
-        }
-
-        // ---- phase 2b: this warp's share of O = diag(g) P + A' U~ (tokens s <= t) ----
-        {
-            const int t = m0 + gq;
-            float oacc[4] = {Bg[t] * pq[0], Bg[t] * pq[1], Bg[t + 8] * pq[2], Bg[t + 8] * pq[3]};
-            for (int kk = kk_lo; kk < kk_hi; ++kk) {
-                const int arow = m0 + (lane & 15), acol = 16 * kk + 8 * (lane >> 4);
-                uint32_t a0[4], a1[4];
-                ldsm_x4(a0, a_s + sw128(arow, acol));
-                ldsm_x4(a1, a_s + sw128(kC + arow, acol));
-                // U~ pieces 0 and 1, rows n0 + lr: blocks 0, 1 = piece 0, 2, 3 = piece 1
-                uint32_t ub[4];
-                ldsm_x4(ub, up_s + (lb >> 1) * kRows * 128 + sw128(n0 + lr, 16 * kk + 8 * (lb & 1)));
-                mma_bf16(oacc, a0, ub[0], ub[1]);
-                mma_bf16(oacc, a0, ub[2], ub[3]);
-                mma_bf16(oacc, a1, ub[0], ub[1]);
-            }
-            if (!kh) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mypart[e * 32] = oacc[e];
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) pend[e] = oacc[e];
-                pend_t0 = t0;
-                pend_len = len;
-            }
+        for (int e = 0; e < 4; ++e) {
+            const int c = 16 * mc + gq + 8 * (e >> 1), r = 8 * nr + 2 * tg + (e & 1);
+            st[e] = s0 ? s0[sbase + r * kD + c] : 0.f;
         }
         store_state();
-        {
-            const bool ok = ch + 1 >= c_end ||
-                            gf16::mbar_wait(bar0 + 8 * (b ^ 1), ((ch + 1 - c_begin) >> 1) & 1,
-                                            nullptr, wait_ns);
-            if (__syncthreads_or(!ok)) {   // state pieces complete, chunk ch + 1 landed
+        __syncthreads();   // barriers initialised, state pieces visible
+        if (kMulti && c_begin >= c_end) {   // an empty sequence: only its state passes through
+            if (tid == 0) *next_item = draws ? G + static_cast<int32_t>(drawn) : n_items;
+            __syncthreads();
+            qn = *next_item;
+            if (qn < n_items) nx = decode(qn);
+            __syncthreads();   // all have read next_item
+        }
+        if (c_begin < c_end && !have_first) {
+            if (tid == 0)
+                scan_issue(base, n & 1, bar0 + 8 * (n & 1), &map_w, &map_a, &map_q, &map_k, ut,
+                           gam, cj_of(c_begin), r0, chunk_t0(c_begin), jq);
+            const bool ok = gf16::mbar_wait(bar0 + 8 * (n & 1), (n >> 1) & 1, nullptr, wait_ns);
+            if (__syncthreads_or(!ok)) {
                 if (tid == 0) atomicExch(status, 1u);
                 return;
             }
         }
-    }
-    if (kh && pend_len > 0) flush_output();
-    if (s_final)
+        float pend[4] = {0.f, 0.f, 0.f, 0.f};   // upper warps: own output partial, stored next chunk
+        int32_t pend_t0 = 0, pend_len = 0;
+        // upper warps: o = scale (own partial + the lower warp's partial in shared memory)
+        const auto flush_output = [&]() {
+            const int t = m0 + gq, r = n0 + 2 * tg;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int c = 16 * mc + gq + 8 * (e >> 1), r = 8 * nr + 2 * tg + (e & 1);
-            s_final[sbase + r * kD + c] = st[e];
+            for (int h = 0; h < 2; ++h) {
+                const int tt = t + 8 * h;
+                if (tt < pend_len)
+                    *reinterpret_cast<uint32_t*>(
+                        o + ((static_cast<int64_t>(pend_t0) + tt) * h_v + j) * kD + r0 + r) =
+                        pack_bf16(scale * (pend[2 * h] + mypart[(2 * h) * 32]),
+                                  scale * (pend[2 * h + 1] + mypart[(2 * h + 1) * 32]));
+            }
+            pend_len = 0;
+        };
+
+        for (int32_t ch = c_begin; ch < c_end; ++ch) {
+            const int b = n & 1;
+            const int32_t t0 = chunk_t0(ch);
+            const int32_t len = min(kC, seq_end - t0);
+            if (kh && pend_len > 0) flush_output();   // before this warp reuses its partial slot
+            // the next chunk of this item, or the next item's first chunk (fault == 1, a testing
+            // hook: an item's second chunk is never loaded, so the wait for it runs out with nothing
+            // in flight)
+            if (tid == 0 && ch + 1 < c_end && !(fault == 1 && ch == c_begin))
+                scan_issue(base, b ^ 1, bar0 + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut,
+                           gam, cj_of(ch + 1), r0, chunk_t0(ch + 1), jq);
+            const uint32_t sb = base + b * kStageBytes;
+            const uint32_t w_s = sb + kOffW, q_s = sb + kOffQ, k_s = sb + kOffK, a_s = sb + kOffA;
+            const float* Bup = upf + b * kRows * kC;   // U'^T rows [r][t]
+            const float* Bg = gf + b * 2 * kC;         // g_t, then g_C / g_t
+
+            // ---- phase 1: U = U' - W S^T, P = Q S^T over this warp's 64 key columns ----
+            float u_hi[4] = {0.f, 0.f, 0.f, 0.f}, u_lo[4] = {0.f, 0.f, 0.f, 0.f},
+                  u_l2[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int kk = 4 * kh + k4;
+                // A fragments (rows m0 + (lane % 16), columns 16 kk + 8 (lane / 16))
+                const int arow = m0 + (lane & 15), acol = 16 * kk + 8 * (lane >> 4);
+                uint32_t w0[4], w1[4], w2[4], qa[4];
+                ldsm_x4(w0, w_s + tsw(arow, acol, 3 * kC));
+                ldsm_x4(w1, w_s + tsw(kC + arow, acol, 3 * kC));
+                ldsm_x4(w2, w_s + tsw(2 * kC + arow, acol, 3 * kC));
+                ldsm_x4(qa, q_s + tsw(arow, acol, kC));
+                // B fragments of the state pieces (rows n0 + lr, columns 16 kk + 8 (lb & 1));
+                // x4 blocks 0, 1 = piece 0, blocks 2, 3 = piece 1; x2 = piece 2
+                const uint32_t boff = sw256(n0 + lr, 16 * kk + 8 * (lb & 1));
+                uint32_t s01[4], s2[2];
+                ldsm_x4(s01, sp_s + (lb >> 1) * kRows * 256 + boff);
+                ldsm_x2(s2, sp_s + 2 * kRows * 256 + boff);
+                mma_bf16(u_hi, w0, s01[0], s01[1]);
+                mma_bf16(u_lo, w0, s01[2], s01[3]);
+                mma_bf16(u_l2, w1, s01[0], s01[1]);
+                mma_bf16(pq, qa, s01[0], s01[1]);
+                mma_bf16(u_lo, w0, s2[0], s2[1]);
+                mma_bf16(u_l2, w1, s01[2], s01[3]);
+                mma_bf16(pq, qa, s01[2], s01[3]);
+                mma_bf16(u_lo, w2, s01[0], s01[1]);
+                mma_bf16(pq, qa, s2[0], s2[1]);
+            }
+            float u[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) u[e] = u_hi[e] + (u_lo[e] + u_l2[e]);
+            if (kh) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) mypart[e * 32] = u[e];
+            }
+            if (kMulti && tid == 0 && ch == c_begin)
+                *next_item = draws ? G + static_cast<int32_t>(drawn) : n_items;
+            __syncthreads();   // upper-half partial U ready (and, at the first chunk, the next item)
+            if (kMulti && ch == c_begin) {
+                qn = *next_item;
+                if (qn < n_items) nx = decode(qn);   // used at the item's end
+            }
+            if (!kh) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[e] += mypart[e * 32];
+                // U~ = (g_C / g_t)(U' - W S^T) -> pieces [r][t] (stmatrix .trans of [t][r] fragments)
+                const int t = m0 + gq, r = n0 + 2 * tg;
+                const float f0 = Bg[kC + t], f1 = Bg[kC + t + 8];
+                const float x0 = f0 * (Bup[r * kC + t] - u[0]);
+                const float x1 = f0 * (Bup[(r + 1) * kC + t] - u[1]);
+                const float x2 = f1 * (Bup[r * kC + t + 8] - u[2]);
+                const float x3 = f1 * (Bup[(r + 1) * kC + t + 8] - u[3]);
+                const Pieces3 lo = split3(x0, x1), hi = split3(x2, x3);
+                // block lb (lanes 8 lb ..): stored row r = n0 + lr, columns t = m0 + 8 lb
+                const uint32_t addr = sw128(n0 + lr, m0 + 8 * (lb & 1));
+#pragma unroll
+                for (int p = 0; p < 3; ++p) stsm_x2_trans(up_s + p * kRows * 128 + addr, lo.p[p], hi.p[p]);
+            }
+            __syncthreads();   // U~ complete
+            // the last chunk: the next item's first chunk goes into the other stage now
+            if (kMulti && tid == 0 && ch + 1 == c_end && qn < n_items && nx.c_begin < nx.c_end)
+                scan_issue(base, b ^ 1, bar0 + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut, gam,
+                           static_cast<int64_t>(nx.c_begin) * h_v + nx.j, nx.r0, nx.seq_start,
+                           nx.j / group);
+
+            // ---- phase 2a: S_next^T[c][r] = g_C S^T + K^T U~ over tokens t (4 steps of 16) ----
+            {
+                const float gc = Bg[kC - 1];
+                float acc[4] = {gc * st[0], gc * st[1], gc * st[2], gc * st[3]};
+                float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < kC / 16; ++kk) {
+                    // A = K^T: ldmatrix .trans of k rows t = 16 kk + lr + 8 (lane / 16), columns
+                    // c = 16 mc + 8 ((lane / 8) % 2)
+                    uint32_t ka[4];
+                    ldsm_x4_trans(ka, k_s + tsw(16 * kk + lr + 8 * (lane >> 4), 16 * mc + 8 * (lb & 1), kC));
+                    // B = U~ pieces [r][t], rows 8 nr + lr: x4 = pieces 0, 1; x2 = piece 2
+                    const uint32_t boff = sw128(8 * nr + lr, 16 * kk + 8 * (lb & 1));
+                    uint32_t u01[4], u2[2];
+                    ldsm_x4(u01, up_s + (lb >> 1) * kRows * 128 + boff);
+                    ldsm_x2(u2, up_s + 2 * kRows * 128 + boff);
+                    mma_bf16(acc, ka, u01[0], u01[1]);
+                    mma_bf16(acc2, ka, u01[2], u01[3]);
+                    mma_bf16(acc2, ka, u2[0], u2[1]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) st[e] = acc[e] + acc2[e];
+            }
+
+            // ---- phase 2b: this warp's share of O = diag(g) P + A' U~ (tokens s <= t) ----
+            {
+                const int t = m0 + gq;
+                float oacc[4] = {Bg[t] * pq[0], Bg[t] * pq[1], Bg[t + 8] * pq[2], Bg[t + 8] * pq[3]};
+                for (int kk = kk_lo; kk < kk_hi; ++kk) {
+                    const int arow = m0 + (lane & 15), acol = 16 * kk + 8 * (lane >> 4);
+                    uint32_t a0[4], a1[4];
+                    ldsm_x4(a0, a_s + sw128(arow, acol));
+                    ldsm_x4(a1, a_s + sw128(kC + arow, acol));
+                    // U~ pieces 0 and 1, rows n0 + lr: blocks 0, 1 = piece 0, 2, 3 = piece 1
+                    uint32_t ub[4];
+                    ldsm_x4(ub, up_s + (lb >> 1) * kRows * 128 + sw128(n0 + lr, 16 * kk + 8 * (lb & 1)));
+                    mma_bf16(oacc, a0, ub[0], ub[1]);
+                    mma_bf16(oacc, a0, ub[2], ub[3]);
+                    mma_bf16(oacc, a1, ub[0], ub[1]);
+                }
+                if (!kh) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) mypart[e * 32] = oacc[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) pend[e] = oacc[e];
+                    pend_t0 = t0;
+                    pend_len = len;
+                }
+            }
+            store_state();
+            {
+                const bool more =
+                    ch + 1 < c_end || (kMulti && qn < n_items && nx.c_begin < nx.c_end);
+                const bool ok = !more || gf16::mbar_wait(bar0 + 8 * (b ^ 1), ((n + 1) >> 1) & 1,
+                                                         nullptr, wait_ns);
+                if (__syncthreads_or(!ok)) {   // state pieces complete, the next chunk landed
+                    if (tid == 0) atomicExch(status, 1u);
+                    return;
+                }
+            }
+            ++n;
         }
+        if (kh && pend_len > 0) flush_output();
+        if (s_final)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = 16 * mc + gq + 8 * (e >> 1), r = 8 * nr + 2 * tg + (e & 1);
+                s_final[sbase + r * kD + c] = st[e];
+            }
+        have_first = c_begin < c_end && qn < n_items && nx.c_begin < nx.c_end;
+        q = qn;
+        it = nx;
+    }
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
@@ -926,6 +1023,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                         l.total);
     auto* ws = static_cast<uint8_t*>(workspace);
     auto* status = reinterpret_cast<uint32_t*>(ws + l.status);
+    auto* order = reinterpret_cast<int32_t*>(ws + l.order);
+    auto* counter = reinterpret_cast<uint32_t*>(ws + l.counter);
+    auto* seqinfo = reinterpret_cast<int4*>(ws + l.seqinfo);
     auto* chunk_offset = reinterpret_cast<int32_t*>(ws + l.chunk_offset);
     auto* n_chunks = reinterpret_cast<int32_t*>(ws + l.n_chunks);
     auto* chunks = reinterpret_cast<int4*>(ws + l.chunks);
@@ -934,6 +1034,8 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     auto* ut = reinterpret_cast<float*>(ws + l.ut);
     auto* gm = reinterpret_cast<float*>(ws + l.gam);
     const int64_t mc = max_chunks_for(total_tokens, n_seqs);
+    if (n_seqs * h_v * (kD / kRows) >= (int64_t(1) << 31))
+        return gdn_fail(GDN_ERR_UNSUPPORTED, "too many sequences x value heads for one call");
     if (mc * h_v * 3 * kC >= (int64_t(1) << 31))
         return gdn_fail(GDN_ERR_UNSUPPORTED, "too many chunks x value heads for one call (%lld)",
                         (long long)(mc * h_v));
@@ -963,7 +1065,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     if (!attrs) {
         cudaFuncSetAttribute(gdn_prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kPrepSmem));
-        cudaFuncSetAttribute(gdn_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gdn_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kScanSmem));
+        cudaFuncSetAttribute(gdn_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kScanSmem));
         attrs = true;
     }
@@ -975,7 +1079,8 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     if (single_T < 0) {
         gdn_chunk_list_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, static_cast<int32_t>(n_seqs),
                                                       chunk_offset, chunks,
-                                                      static_cast<int32_t>(mc), n_chunks, status);
+                                                      static_cast<int32_t>(mc), n_chunks, status,
+                                                      order, seqinfo, counter);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_chunk_list_kernel: %s", cudaGetErrorString(e));
     }
@@ -985,13 +1090,22 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
             static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
             static_cast<const __nv_bfloat16*>(v), alpha, beta, chunks, n_chunks,
             static_cast<int32_t>(h_qk), static_cast<int32_t>(h_v), wp, ap, ut, gm, single_T,
-            status);
+            status, counter);
         if ((e = cudaGetLastError()) != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
     }
-    const dim3 sgrid(static_cast<uint32_t>(n_seqs), static_cast<uint32_t>(h_v), kD / kRows);
-    gdn_scan_kernel<<<sgrid, kScanThreads, kScanSmem, stream>>>(
-        map_w, map_a, map_q, map_k, cu_seqlens, chunk_offset, ut, gm, initial_state, final_state,
+    // persistent scan: one CTA per SM (at most one per work item) taking items dynamically
+    const int64_t n_items = n_seqs * h_v * (kD / kRows);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return gdn_fail(GDN_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    const int64_t ctas = n_items < sms ? n_items : sms;
+    auto* scan = n_items > sms ? gdn_scan_kernel<true> : gdn_scan_kernel<false>;
+    scan<<<static_cast<uint32_t>(ctas), kScanThreads, kScanSmem, stream>>>(
+        map_w, map_a, map_q, map_k, single_T >= 0 ? nullptr : order,
+        single_T >= 0 ? nullptr : seqinfo, counter, static_cast<int32_t>(n_items), ut, gm,
+        initial_state, final_state,
         static_cast<__nv_bfloat16*>(o), status, static_cast<int32_t>(h_v),
         static_cast<int32_t>(h_v / h_qk), scale, g_gdn_wait_ns.load(), g_gdn_fault.load(),
         single_T);
