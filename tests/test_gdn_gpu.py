@@ -160,3 +160,31 @@ def test_rejects_bad_arguments():
     assert call(n=-1) == g.GDN_ERR_INVALID_ARG
     assert call(n=0) == g.GDN_OK                             # nothing to do
     torch.cuda.synchronize()
+
+
+def test_many_items_with_empty_sequences():
+    """More work items than SMs (30 sequences x 8 value heads x 8 row blocks = 1920), so CTAs draw
+    items dynamically and prefetch across items; a third of the sequences are empty and lie
+    between non-empty ones."""
+    T, n, h_qk, h_v = 2000, 30, 2, 8
+    inp = make_gdn_inputs(T, n, h_qk, h_v, 128, 128, seed=41, state=True)
+    g_ = torch.Generator().manual_seed(5)
+    lens = torch.randint(1, 60, (n,), generator=g_)
+    lens[::3] = 0                                   # every third sequence empty
+    lens[-1] += T - int(lens.sum())                 # the rest to the last one
+    assert int(lens.min()) >= 0 and int(lens.sum()) == T
+    inp["cu_seqlens"] = torch.cat([torch.zeros(1, dtype=torch.int64), lens.cumsum(0)]).to(torch.int32)
+    o, sf = run(inp, h_qk, h_v)
+    assert_parity(inp, o, sf, 0.73, "30 sequences with empty ones")
+    s0 = inp["initial_state"].double().numpy()
+    for i in range(0, n, 3):
+        assert np.array_equal(sf[i], s0[i]), f"empty sequence {i} changed its state"
+
+
+def test_more_sequences_than_the_ranking_block():
+    """1100 short sequences: beyond 1024 the scan takes sequences in index order."""
+    n = 1100
+    T = 3 * n
+    inp = make_gdn_inputs(T, n, 1, 1, 128, 128, seed=42, state=True)
+    o, sf = run(inp, 1, 1)
+    assert_parity(inp, o, sf, 0.73, "1100 sequences")
