@@ -169,17 +169,6 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
     }
 }
 
-// 16-byte global -> shared copy that completes asynchronously; src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src, uint32_t src_bytes)
-{
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem_src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
 // d += a * b for a 16 x 16 (k) bf16 A fragment and a 16 (k) x 8 bf16 B fragment (m16n8k16,
 // fp32 accumulation); each 32-bit register holds two consecutive-k elements.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -256,21 +245,31 @@ __device__ __forceinline__ uint32_t sw128(int row, int col)
     return static_cast<uint32_t>(row * 128 + (((col >> 3) ^ row) & 7) * 16 + (col & 7) * 2);
 }
 
+// Byte offset of element (row, col) in a 128-column bf16 tile that TMA wrote as two 64-column
+// halves of `rows` 128-byte rows each, 128-byte swizzle (16-byte granule g of row r at g ^ (r % 8)).
+__device__ __forceinline__ uint32_t tsw(int row, int col, int rows)
+{
+    return static_cast<uint32_t>((col >> 6) * rows * 128 + row * 128 +
+                                 ((((col >> 3) & 7) ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
 // ---- per (chunk, value head): W, U'^T, A' and the cumulative decays ----------------------------
-// K, Q, V of the chunk sit in shared memory as padded bf16 rows.  Products K K^T and Q K^T run
-// on the tensor cores (bf16 operands, exact products).  T = (I + L)^-1 is then built in the
+// K, Q, V of the chunk arrive by TMA as 128-byte-swizzled bf16 tiles.  Products K K^T and Q K^T
+// run on the tensor cores (bf16 operands, exact products).  T = (I + L)^-1 is then built in the
 // page's doubling stages: the eight 8 x 8 diagonal blocks by substitution, then for block sizes
 // b = 8, 16, 32 each pair of neighbouring inverted blocks [A 0; C B] becomes
 // [A^-1 0; -B^-1 C A^-1  B^-1] (fp32 products).  Finally W = T diag(beta g) K and
 // U' = T diag(beta) V run on the tensor cores: T diag(.) as three bfloat16 pieces against the
 // exact bfloat16 K or V, the three products keeping fp32 accuracy.
-constexpr int kRowB = 136;     // padded bf16 rows of the prepare kernel (272 bytes)
 constexpr int kRowA = 72;      // padded bf16 rows of A' staging (144 bytes)
 constexpr int kRowL = 68;      // padded fp32 rows of L and T (272 bytes)
 constexpr int kRowY = 33;      // fp32 rows of the doubling scratch
 constexpr int kPrepThreads = 256;
-constexpr size_t kPrepSmem = sizeof(__nv_bfloat16) * (3 * kC * kRowB + 2 * kC * kRowA) +
-                             sizeof(float) * (2 * kC * kRowL + 4 * kC);
+// K, Q, V: 128-byte-swizzled TMA tiles (two 64-column halves of 64 rows) at a 1024-byte-aligned
+// base, then the A' staging, L, T and the per-token vectors, then the load barrier.
+constexpr uint32_t kPrepTile = 2 * kC * 128;   // one of K, Q, V
+constexpr size_t kPrepSmem = 3 * kPrepTile + sizeof(__nv_bfloat16) * 2 * kC * kRowA +
+                             sizeof(float) * (2 * kC * kRowL + 4 * kC) + 16 + 1024;
 static_assert(sizeof(__nv_bfloat16) * 2 * kC * kRowA >= sizeof(float) * 32 * kRowY,
               "the doubling scratch reuses the A' staging");
 
@@ -318,13 +317,15 @@ __device__ __forceinline__ void invert_doubling_stage(const float* Ls, float* Ts
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
-    gdn_prepare_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                       const __nv_bfloat16* __restrict__ v, const float* __restrict__ alpha,
+    gdn_prepare_kernel(const __grid_constant__ CUtensorMap map_q,
+                       const __grid_constant__ CUtensorMap map_k,
+                       const __grid_constant__ CUtensorMap map_v, const float* __restrict__ alpha,
                        const float* __restrict__ beta, const int4* __restrict__ chunks,
-                       const int32_t* __restrict__ n_chunks, int32_t h_qk, int32_t h_v,
+                       const int32_t* __restrict__ n_chunks, int32_t h_v, int32_t group,
                        __nv_bfloat16* __restrict__ wp, __nv_bfloat16* __restrict__ ap,
                        float* __restrict__ ut, float* __restrict__ gam_out, int32_t single_T,
-                       uint32_t* __restrict__ status, uint32_t* __restrict__ counter)
+                       uint32_t* __restrict__ status, uint32_t* __restrict__ counter,
+                       uint64_t wait_ns)
 {
     const int32_t ch = blockIdx.x;
     const int32_t j = blockIdx.y;
@@ -346,13 +347,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         t0 = info.y;
         len = info.z;
     }
-    const int32_t jq = j / (h_v / h_qk);
+    const int32_t jq = j / group;
     const int64_t cj = static_cast<int64_t>(ch) * h_v + j;
+    const int tid = threadIdx.x;
+    // alpha and beta first: their latency overlaps the tile loads
+    float a_in = 1.f, b_in = 0.f;
+    if (tid < kC && tid < len) {
+        const int64_t tok = static_cast<int64_t>(t0) + tid;
+        a_in = alpha[tok * h_v + j];
+        b_in = beta[tok * h_v + j];
+    }
     extern __shared__ __align__(16) uint8_t smraw[];
-    __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(smraw);   // [64][136]
-    __nv_bfloat16* Qb = Kb + kC * kRowB;
-    __nv_bfloat16* Vb = Qb + kC * kRowB;
-    __nv_bfloat16* Ap = Vb + kC * kRowB;                             // [2][64][72] A' pieces
+    const uint32_t raw = smem_u32(smraw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smraw + (base - raw);
+    const uint32_t kb_s = base, qb_s = base + kPrepTile, vb_s = base + 2 * kPrepTile;
+    __nv_bfloat16* Ap = reinterpret_cast<__nv_bfloat16*>(gbase + 3 * kPrepTile);   // [2][64][72]
     float* Yb = reinterpret_cast<float*>(Ap);                         // [32][33], after A' is out
     float* Ls = reinterpret_cast<float*>(Ap + 2 * kC * kRowA);       // [64][68] L, strictly lower
     float* Ts = Ls + kC * kRowL;                                      // [64][68] T = (I + L)^-1
@@ -360,24 +370,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     float* bt = g + kC;
     float* bg = bt + kC;
     float* al = bg + kC;
-    const int tid = threadIdx.x;
+    const uint32_t bar = smem_u32(al + kC);
 
-    for (int idx = tid; idx < kC * 16; idx += kPrepThreads) {
-        const int t = idx / 16, p = idx % 16;
-        const bool valid = t < len;
-        const int64_t tok = static_cast<int64_t>(t0) + (valid ? t : 0);
-        const uint32_t nb = valid ? 16u : 0u;
-        cp_async16(Kb + t * kRowB + p * 8, k + (tok * h_qk + jq) * kD + p * 8, nb);
-        cp_async16(Qb + t * kRowB + p * 8, q + (tok * h_qk + jq) * kD + p * 8, nb);
-        cp_async16(Vb + t * kRowB + p * 8, v + (tok * h_v + j) * kD + p * 8, nb);
+    // K, Q, V rows by TMA (two 64-column halves each).  Rows past the chunk's end read the next
+    // sequence's tokens (zeros past the last token); their beta is 0, which zeroes their rows of
+    // L, W and U', and A' keeps only s <= t.
+    if (tid == 0) {
+        gf16::mbar_init(bar, 1);
+        gf16::fence_mbarrier_init();
+        gf16::mbar_arrive_expect_tx(bar, 3 * kPrepTile);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            gf16::tma_load_3d(kb_s + h * kC * 128, &map_k, bar, 64 * h, jq, t0);
+            gf16::tma_load_3d(qb_s + h * kC * 128, &map_q, bar, 64 * h, jq, t0);
+            gf16::tma_load_3d(vb_s + h * kC * 128, &map_v, bar, 64 * h, j, t0);
+        }
     }
-    cp_async_commit();
     for (int e = tid; e < kC * kRowL; e += kPrepThreads) Ts[e] = 0.f;   // upper blocks stay zero
     if (tid < kC) {
-        const bool valid = tid < len;
-        const int64_t tok = static_cast<int64_t>(t0) + tid;
-        al[tid] = valid ? alpha[tok * h_v + j] : 1.f;
-        bt[tid] = valid ? beta[tok * h_v + j] : 0.f;
+        al[tid] = a_in;
+        bt[tid] = b_in;
     }
     __syncthreads();
     if (tid < 32) {
@@ -396,8 +408,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         al[2 * tid] = 1.f / (before * a0);   // from here on al holds 1 / g
         al[2 * tid + 1] = 1.f / p;
     }
-    cp_async_wait_all();
-    __syncthreads();
+    {
+        const bool ok = gf16::mbar_wait(bar, 0, nullptr, wait_ns);
+        if (__syncthreads_or(!ok)) {   // the tiles never landed: report and stop
+            if (tid == 0) atomicExch(status, 1u);
+            return;
+        }
+    }
     if (tid < kC) bg[tid] = bt[tid] * g[tid];
 
     // K K^T and Q K^T on the tensor cores: mma.sync m16n8k16 with bf16 operands (exact products,
@@ -412,15 +429,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         for (int k0 = 0; k0 < kD; k0 += 16) {
             // A fragments: rows m0 + (lane % 16), columns k0 + 8 (lane / 16)
             uint32_t ka[4], qa[4];
-            const int aoff = (m0 + (lane & 15)) * kRowB + k0 + 8 * (lane >> 4);
-            ldsm_x4(ka, smem_u32(Kb + aoff));
-            ldsm_x4(qa, smem_u32(Qb + aoff));
+            const uint32_t aoff = tsw(m0 + (lane & 15), k0 + 8 * (lane >> 4), kC);
+            ldsm_x4(ka, kb_s + aoff);
+            ldsm_x4(qa, qb_s + aoff);
 #pragma unroll
             for (int np = 0; np < 2; ++np) {
                 // B fragments of n-tiles 2 np, 2 np + 1: k rows n0 + lr, columns k0 + 8 (lb % 2)
                 uint32_t kb4[4];
-                ldsm_x4(kb4, smem_u32(Kb + (nb + 16 * np + 8 * (lb >> 1) + lr) * kRowB + k0 +
-                                      8 * (lb & 1)));
+                ldsm_x4(kb4, kb_s + tsw(nb + 16 * np + 8 * (lb >> 1) + lr, k0 + 8 * (lb & 1), kC));
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     mma_bf16(kk[2 * np + h], ka, kb4[2 * h], kb4[2 * h + 1]);
@@ -488,7 +504,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const int half = warp >> 2;
         const int mt = half ? 3 - (warp & 3) : (warp & 3);
         const float* sc = half ? bt : bg;
-        const __nv_bfloat16* src = half ? Vb : Kb;
+        const uint32_t src_s = half ? vb_s : kb_s;
         float acc[16][4];
 #pragma unroll
         for (int n = 0; n < 16; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
@@ -506,8 +522,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             for (int q = 0; q < 8; ++q) {
                 // B = K or V rows s = 16 kk .. + 15, columns of n-tiles 2q and 2q+1 (ldmatrix .trans)
                 uint32_t bfr[4];
-                ldsm_x4_trans(bfr, smem_u32(src + (16 * kk + lr + 8 * (lb & 1)) * kRowB +
-                                            8 * (2 * q + (lb >> 1))));
+                ldsm_x4_trans(bfr, src_s + tsw(16 * kk + lr + 8 * (lb & 1), 8 * (2 * q + (lb >> 1)), kC));
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t b0 = bfr[2 * h], b1 = bfr[2 * h + 1];
@@ -587,13 +602,6 @@ constexpr uint32_t kStageTx = kStageBytes + kRows * kC * 4 + 2 * kC * 4;   // by
 constexpr size_t kScanSmem = kOffItem + 16 + 1024;           // + slack to align the base
 static_assert(kScanSmem <= 232448, "scan shared memory");
 
-// Byte offset of element (row, col) in a 128-column bf16 tile that TMA wrote as two 64-column
-// halves of `rows` 128-byte rows each, 128-byte swizzle (16-byte granule g of row r at g ^ (r % 8)).
-__device__ __forceinline__ uint32_t tsw(int row, int col, int rows)
-{
-    return static_cast<uint32_t>((col >> 6) * rows * 128 + row * 128 +
-                                 ((((col >> 3) & 7) ^ (row & 7)) << 4) + (col & 7) * 2);
-}
 
 // Bulk (untiled) global -> shared copy completing on an mbarrier of this CTA.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
@@ -1041,8 +1049,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                         (long long)(mc * h_v));
 
     // TMA descriptors: W pieces [cj * 192 rows][128], A' pieces [cj * 128 rows][64], q and k as
-    // {128, h_qk, total_tokens}.  With no tokens the scan loads nothing and they stay zero.
-    CUtensorMap map_w{}, map_a{}, map_q{}, map_k{};
+    // {128, h_qk, total_tokens}, v as {128, h_v, total_tokens}.  With no tokens nothing is loaded
+    // and they stay zero.
+    CUtensorMap map_w{}, map_a{}, map_q{}, map_k{}, map_v{};
     if (total_tokens > 0) {
         const cuuint64_t dw[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(mc * h_v * 3 * kC)};
         const cuuint64_t sw[1] = {kD * 2};
@@ -1059,6 +1068,10 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
             (rc = gdn_make_map(&map_q, q, 3, dq, sq, bq, "q")) != GDN_OK ||
             (rc = gdn_make_map(&map_k, k, 3, dq, sq, bq, "k")) != GDN_OK)
             return rc;
+        const cuuint64_t dv[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(h_v),
+                                  static_cast<cuuint64_t>(total_tokens)};
+        const cuuint64_t sv[2] = {kD * 2, static_cast<cuuint64_t>(h_v) * kD * 2};
+        if ((rc = gdn_make_map(&map_v, v, 3, dv, sv, bq, "v")) != GDN_OK) return rc;
     }
 
     static bool attrs = false;
@@ -1087,10 +1100,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     if (mc > 0 && total_tokens > 0) {
         const dim3 pgrid(static_cast<uint32_t>(mc), static_cast<uint32_t>(h_v));
         gdn_prepare_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
-            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-            static_cast<const __nv_bfloat16*>(v), alpha, beta, chunks, n_chunks,
-            static_cast<int32_t>(h_qk), static_cast<int32_t>(h_v), wp, ap, ut, gm, single_T,
-            status, counter);
+            map_q, map_k, map_v, alpha, beta, chunks, n_chunks, static_cast<int32_t>(h_v),
+            static_cast<int32_t>(h_v / h_qk), wp, ap, ut, gm, single_T, status, counter,
+            g_gdn_wait_ns.load());
         if ((e = cudaGetLastError()) != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
     }
