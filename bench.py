@@ -393,7 +393,7 @@ GDN_PAGE_H20_MS = {
 
 def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
     """Every scenario of the page: inputs resident, the workspace allocated once, CUDA events
-    around `gdn_reps` back-to-back calls after 3 warm-up calls."""
+    around `gdn_reps` back-to-back calls after about 10 ms of warm-up calls."""
     import torch
     from blackwell_tensor_core_fp16_gb300.workloads import GDN_ORDER, GDN_WORKLOADS, \
         gdn_workload_inputs
@@ -420,10 +420,16 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
             if rc != g.GDN_OK:
                 raise g.GemmError(rc, g.gdn_last_error())
 
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                call()
-        torch.cuda.synchronize()
+        # warm up for about 10 ms of calls (at least 3): the leg follows the power-capped GEMM
+        # legs, and a few calls of a 35 us scenario would be timed before the clocks settle
+        t_w = time.perf_counter()
+        n_w = 0
+        while n_w < 3 or time.perf_counter() - t_w < 0.01:
+            with torch.cuda.stream(stream):
+                for _ in range(8):
+                    call()
+            torch.cuda.synchronize()
+            n_w += 8
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record(stream)
