@@ -95,6 +95,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's `value` (a job's time is its slowest rank's); the same value
+    on every rank.  Works on any initialised process group (NCCL on the GPUs, gloo on the CPU)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, steps: int, flops_step: float, total_ms: float) -> float:
+    """Every rank runs the same step on its own GPU (replicas): the job's throughput is all
+    ranks' FLOPs over the slowest rank's time."""
+    return world * steps * flops_step / (total_ms * 1e-3) / 1e12
+
+
 GEMM_KERNEL_SOURCES = ("desc.h", "gemm_f16.cu", "gemm_kernels.cuh", "ptx.cuh")
 
 
@@ -546,12 +564,9 @@ def run_ours(args):
 
     durs = [events[i].elapsed_time(events[i + 1]) for i in range(len(events) - 1)]
     total_ms = events[0].elapsed_time(events[-1])
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     flops_step = sum(2.0 * w.M * w.N * w.K for (w, *_rest) in work)
-    value = world * K * flops_step / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, K, flops_step, total_ms)
 
     per = {}
     kernel_ms_total = 0.0
@@ -684,12 +699,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         g.check_status(stream)
-        e2e_ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e_value = world * e2e_steps * flops_step / (e2e_ms * 1e-3) / 1e12
+        e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+        e2e_value = whole_job_tflops(world, e2e_steps, flops_step, e2e_ms)
         # The copy roofline of this leg: the measured rate of concurrent pinned-host copies in
         # both directions (256 MiB each way, the same streams), and the TFLOP/s a step could
         # reach if its copies ran at that rate and the GEMMs hid under them.

@@ -1,0 +1,87 @@
+"""The multi-rank side of bench.py on the CPU: two processes on the gloo backend.
+
+With N GPUs bench.py runs N independent replicas of the step (the GEMMs shard into independent
+problems; no collective sits on the data path).  What multi-rank code there is lives on the host:
+the slowest rank's time decides the job's time, the job's throughput counts every rank's work,
+only rank 0 prints, and the reference arm runs on rank 0 alone.  These tests run that logic in
+two gloo processes (127.0.0.1) without a GPU.
+"""
+from __future__ import annotations
+
+import importlib.util
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def load_bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank: int, world: int, port: int, out):
+    sys.path.insert(0, ROOT)
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
+                            world_size=world)
+    try:
+        bench = load_bench()
+        w, r, local = bench.dist_env()
+        local_ms = 10.0 + 5.0 * rank          # rank 1 is the slower replica
+        job_ms = bench.max_over_ranks(local_ms, w, "cpu")
+        value = bench.whole_job_tflops(w, 4, 1e12, job_ms)
+        out.put((rank, w, r, local, job_ms, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_timing_on_gloo():
+    world, port = 2, free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, w, r, local, job_ms, value in results:
+        assert (w, r, local) == (2, rank, rank)
+        assert job_ms == 15.0                    # the slowest rank's time, on every rank
+        # both replicas' work over the slowest time: 2 ranks x 4 steps x 1 TFLOP / 15 ms
+        assert value == pytest.approx(2 * 4 * 1e12 / 15e-3 / 1e12)
+
+
+def test_single_rank_needs_no_group():
+    bench = load_bench()
+    assert bench.max_over_ranks(7.5, 1) == 7.5
+    assert bench.whole_job_tflops(1, 10, 2e12, 20.0) == pytest.approx(10 * 2e12 / 0.02 / 1e12)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
+    """Under torchrun every rank but 0 leaves the reference arm at once, printing nothing."""
+    bench = load_bench()
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.run_reference(None) == 0
+    assert buf.getvalue() == ""
