@@ -101,6 +101,12 @@ def _load():
                                            i64, i64, i64, i64, ctypes.c_double, f64p, f64p,
                                            f64p]
             lib.oracle_gdn_f64.restype = ctypes.c_int
+            lib.oracle_gdn_heads_f64.argtypes = [f64p, f64p, f64p, f64p, f64p, ctypes.c_void_p,
+                                                 i64, i64, i64, i64, i64, i64, ctypes.c_double,
+                                                 f64p, f64p, f64p]
+            lib.oracle_gdn_heads_f64.restype = ctypes.c_int
+            lib.oracle_gdn_out_heads.argtypes = [i64, i64, i64]
+            lib.oracle_gdn_out_heads.restype = i64
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -377,35 +383,50 @@ def _f64(x, name) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.float64)
 
 
+def gdn_out_heads(h_q: int, h_k: int, h_v: int) -> int:
+    """Output heads of the head layout (h_q, h_k, h_v); ValueError if it is none of MHA, GVA,
+    GQA (h_v a multiple of h_k; h_q == h_k, or h_q a multiple of h_v)."""
+    h_o = _load().oracle_gdn_out_heads(h_q, h_k, h_v)
+    if h_o < 0:
+        raise ValueError(f"head counts q {h_q}, k {h_k}, v {h_v} form no supported layout")
+    return int(h_o)
+
+
 def gdn_f64(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_state=None):
     """(o, final_state) of the gated delta rule, token by token in binary64.
 
-    q, k: [T, h_qk, dk]; v: [T, h_v, dv]; alpha, beta: [T, h_v]; cu_seqlens: n_seqs + 1 offsets;
-    initial_state: [n_seqs, h_v, dv, dk] or None (zero).  Returns o [T, h_v, dv] and the final
-    states [n_seqs, h_v, dv, dk], both binary64."""
+    q: [T, h_q, dk]; k: [T, h_k, dk]; v: [T, h_v, dv]; alpha, beta: [T, h_v]; cu_seqlens: n_seqs + 1
+    offsets; initial_state: [n_seqs, h_v, dv, dk] or None (zero).  h_v is a multiple of h_k, and
+    either h_q == h_k (one output per value head: MHA, GVA) or h_q is a multiple of h_v (one
+    output per query head: GQA).  Returns o [T, h_o, dv] and the final states
+    [n_seqs, h_v, dv, dk], both binary64."""
     qd, kd, vd = _f64(q, "q"), _f64(k, "k"), _f64(v, "v")
     ad, bd = _f64(alpha, "alpha"), _f64(beta, "beta")
     cu = np.ascontiguousarray(np.asarray(cu_seqlens), dtype=np.int32)
-    T, h_qk, dk = qd.shape
+    T, h_q, dk = qd.shape
+    h_k = kd.shape[1]
     h_v, dv = vd.shape[1], vd.shape[2]
     n = cu.size - 1
-    if kd.shape != qd.shape or vd.shape[0] != T or ad.shape != (T, h_v) or bd.shape != (T, h_v):
+    if kd.shape != (T, h_k, dk) or vd.shape[0] != T or ad.shape != (T, h_v) or \
+            bd.shape != (T, h_v):
         raise ValueError("inconsistent shapes")
     if n < 0 or cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
         raise ValueError("cu_seqlens must rise from 0 to T")
+    h_o = gdn_out_heads(h_q, h_k, h_v)
     s0 = None
     if initial_state is not None:
         s0 = _f64(initial_state, "initial_state")
         if s0.shape != (n, h_v, dv, dk):
             raise ValueError(f"initial_state shape {s0.shape}; want {(n, h_v, dv, dk)}")
-    o = np.empty((T, h_v, dv), dtype=np.float64)
+    o = np.empty((T, h_o, dv), dtype=np.float64)
     sf = np.empty((n, h_v, dv, dk), dtype=np.float64)
-    rc = _load().oracle_gdn_f64(qd.ctypes.data, kd.ctypes.data, vd.ctypes.data, ad.ctypes.data,
-                                bd.ctypes.data, cu.ctypes.data, n, h_qk, h_v, dk, dv,
-                                float(scale), None if s0 is None else s0.ctypes.data,
-                                o.ctypes.data, sf.ctypes.data)
+    rc = _load().oracle_gdn_heads_f64(qd.ctypes.data, kd.ctypes.data, vd.ctypes.data,
+                                      ad.ctypes.data, bd.ctypes.data, cu.ctypes.data, n, h_q,
+                                      h_k, h_v, dk, dv, float(scale),
+                                      None if s0 is None else s0.ctypes.data, o.ctypes.data,
+                                      sf.ctypes.data)
     if rc == -1:
-        raise ValueError("inconsistent sizes (h_v must be a multiple of h_qk)")
+        raise ValueError("inconsistent sizes")
     if rc != 0:
         raise MemoryError("oracle could not allocate its state")
     return o, sf

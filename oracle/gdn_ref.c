@@ -19,12 +19,16 @@
  * sequences are stored back to back; sequence i owns tokens cu_seqlens[i] .. cu_seqlens[i+1]-1
  * and its own state, which starts from initial_state[i] (or zero) and ends in final_state[i].
  *
- * Heads: q and k have h_qk heads, v, alpha, beta, the state and the output have h_v heads, with
- * h_v a multiple of h_qk.  Value head j reads q/k head j / (h_v / h_qk): h_v == h_qk is
- * multi-head attention (MHA), h_v > h_qk the grouped-value form (GVA) the page names.
+ * Heads (the page names three relations: MHA, GQA and GVA).  q has h_q heads, k has h_k, and v,
+ * alpha, beta and the states have h_v, with h_v a multiple of h_k: state head j reads key head
+ * j / (h_v / h_k).  The outputs follow one of two layouts:
+ *   h_q == h_k            one output per value head (h_o = h_v); state j reads query head
+ *                         j / (h_v / h_k): MHA when h_v == h_k, GVA (grouped values) when larger;
+ *   h_q a multiple of h_v one output per query head (h_o = h_q); query head m reads state
+ *                         m / (h_q / h_v): GQA (grouped queries), when h_q > h_v == h_k.
  *
- * Layouts (row-major): q, k [T][h_qk][dk]; v [T][h_v][dv]; alpha, beta [T][h_v];
- * states [n_seqs][h_v][dv][dk]; o [T][h_v][dv].
+ * Layouts (row-major): q [T][h_q][dk]; k [T][h_k][dk]; v [T][h_v][dv]; alpha, beta [T][h_v];
+ * states [n_seqs][h_v][dv][dk]; o [T][h_o][dv].
  *
  * Nothing here is shared with the GPU path: no header, helper or table.
  */
@@ -32,16 +36,30 @@
 #include <stdlib.h>
 #include <string.h>
 
-/* Returns 0, or -1 for inconsistent sizes, -2 if a work buffer cannot be allocated. */
-int oracle_gdn_f64(const double* q, const double* k, const double* v, const double* alpha,
-                   const double* beta, const int32_t* cu_seqlens, int64_t n_seqs, int64_t h_qk,
-                   int64_t h_v, int64_t dk, int64_t dv, double scale,
-                   const double* initial_state, double* o, double* final_state)
+/* Output heads for (h_q, h_k, h_v), or -1 if the three do not form one of the layouts above. */
+int64_t oracle_gdn_out_heads(int64_t h_q, int64_t h_k, int64_t h_v)
 {
-    if (n_seqs < 0 || h_qk <= 0 || h_v <= 0 || h_v % h_qk != 0 || dk <= 0 || dv <= 0) return -1;
+    if (h_q <= 0 || h_k <= 0 || h_v <= 0 || h_v % h_k != 0) return -1;
+    if (h_q == h_k) return h_v;
+    if (h_q % h_v == 0) return h_q;
+    return -1;
+}
+
+/* Returns 0, or -1 for inconsistent sizes, -2 if a work buffer cannot be allocated. */
+int oracle_gdn_heads_f64(const double* q, const double* k, const double* v, const double* alpha,
+                         const double* beta, const int32_t* cu_seqlens, int64_t n_seqs,
+                         int64_t h_q, int64_t h_k, int64_t h_v, int64_t dk, int64_t dv,
+                         double scale, const double* initial_state, double* o,
+                         double* final_state)
+{
+    const int64_t h_o = oracle_gdn_out_heads(h_q, h_k, h_v);
+    if (n_seqs < 0 || h_o < 0 || dk <= 0 || dv <= 0) return -1;
     for (int64_t i = 0; i < n_seqs; ++i)
         if (cu_seqlens[i + 1] < cu_seqlens[i]) return -1;
-    const int64_t group = h_v / h_qk;
+    /* per state head j: its key head, and its query heads m0 .. m0 + nq - 1 with outputs at
+     * output heads o0 .. o0 + nq - 1 */
+    const int64_t kgroup = h_v / h_k;
+    const int64_t nq = h_o == h_v ? 1 : h_q / h_v;
     int err = 0;
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int64_t i = 0; i < n_seqs; ++i) {
@@ -57,10 +75,11 @@ int oracle_gdn_f64(const double* q, const double* k, const double* v, const doub
             }
             const double* h0 = initial_state ? initial_state + ((i * h_v + j) * dv) * dk : NULL;
             for (int64_t e = 0; e < dv * dk; ++e) H[e] = h0 ? h0[e] : 0.0;
-            const int64_t jq = j / group;
+            const int64_t jk = j / kgroup;
+            const int64_t m0 = h_o == h_v ? j / kgroup : j * nq;   /* first query head */
+            const int64_t o0 = h_o == h_v ? j : j * nq;            /* its output head */
             for (int64_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) {
-                const double* qt = q + (t * h_qk + jq) * dk;
-                const double* kt = k + (t * h_qk + jq) * dk;
+                const double* kt = k + (t * h_k + jk) * dk;
                 const double* vt = v + (t * h_v + j) * dv;
                 const double a = alpha[t * h_v + j];
                 const double b = beta[t * h_v + j];
@@ -75,12 +94,15 @@ int oracle_gdn_f64(const double* q, const double* k, const double* v, const doub
                 /* H = H_decay + update k^T */
                 for (int64_t r = 0; r < dv; ++r)
                     for (int64_t c = 0; c < dk; ++c) H[r * dk + c] += upd[r] * kt[c];
-                /* o = scale * H q */
-                double* ot = o + (t * h_v + j) * dv;
-                for (int64_t r = 0; r < dv; ++r) {
-                    double s = 0.0;
-                    for (int64_t c = 0; c < dk; ++c) s += H[r * dk + c] * qt[c];
-                    ot[r] = scale * s;
+                /* o = scale * H q, for each query head this state serves */
+                for (int64_t g = 0; g < nq; ++g) {
+                    const double* qt = q + (t * h_q + m0 + g) * dk;
+                    double* ot = o + (t * h_o + o0 + g) * dv;
+                    for (int64_t r = 0; r < dv; ++r) {
+                        double s = 0.0;
+                        for (int64_t c = 0; c < dk; ++c) s += H[r * dk + c] * qt[c];
+                        ot[r] = scale * s;
+                    }
                 }
             }
             if (final_state) memcpy(final_state + ((i * h_v + j) * dv) * dk, H,
@@ -90,4 +112,14 @@ int oracle_gdn_f64(const double* q, const double* k, const double* v, const doub
         }
     }
     return err;
+}
+
+/* q and k sharing h_qk heads (MHA, GVA): the layout above with h_q = h_k = h_qk. */
+int oracle_gdn_f64(const double* q, const double* k, const double* v, const double* alpha,
+                   const double* beta, const int32_t* cu_seqlens, int64_t n_seqs, int64_t h_qk,
+                   int64_t h_v, int64_t dk, int64_t dv, double scale,
+                   const double* initial_state, double* o, double* final_state)
+{
+    return oracle_gdn_heads_f64(q, k, v, alpha, beta, cu_seqlens, n_seqs, h_qk, h_qk, h_v, dk, dv,
+                                scale, initial_state, o, final_state);
 }

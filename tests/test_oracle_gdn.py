@@ -243,3 +243,119 @@ def test_pins_catch_planted_mistakes(mutant):
 def test_unmutated_numpy_copy_passes_every_pin():
     g = _np_gdn(None)
     assert all(pin(g) == 0 for pin in PINS)
+
+
+# ---- grouped queries (GQA) and mixed layouts ---------------------------------------------------
+# q: [T, h_q, dk], k: [T, h_k, dk], v: [T, h_v, dv].  With h_q a multiple of h_v, query head m
+# reads state m / (h_q / h_v) and has its own output.  Each pin reduces a grouped layout to
+# single-head runs, which the pins above fix.
+
+def _rand_heads(rng, T, h_q, h_k, h_v, dk, dv):
+    q = rng.standard_normal((T, h_q, dk))
+    k = rng.standard_normal((T, h_k, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, h_v, dv))
+    a = rng.uniform(0.8, 1.0, (T, h_v))
+    b = rng.uniform(0.0, 1.0, (T, h_v))
+    return q, k, v, a, b
+
+
+def _single_head_runs(gdn, q, k, v, a, b, cu, scale, s0, state_of, key_of):
+    """Outputs and states of every query head m run alone with its state's key, value, decays."""
+    h_q, h_v = q.shape[1], v.shape[1]
+    outs = []
+    for m in range(h_q):
+        j = state_of(m)
+        om, sm = gdn(q[:, m:m + 1], k[:, key_of(j):key_of(j) + 1], v[:, j:j + 1],
+                     a[:, j:j + 1], b[:, j:j + 1], cu, scale,
+                     None if s0 is None else s0[:, j:j + 1])
+        outs.append((om[:, 0], sm[:, 0]))
+    return outs
+
+
+def pin_grouped_queries_are_single_head_runs(gdn):
+    rng = np.random.default_rng(10)
+    T, h_q, h_kv = 9, 6, 2
+    q, k, v, a, b = _rand_heads(rng, T, h_q, h_kv, h_kv, 4, 3)
+    cu = [0, 4, 9]
+    s0 = rng.standard_normal((2, h_kv, 3, 4))
+    o, sf = gdn(q, k, v, a, b, cu, 0.8, s0)
+    r = h_q // h_kv
+    fails = int(o.shape != (T, h_q, 3))
+    for m, (om, sm) in enumerate(_single_head_runs(gdn, q, k, v, a, b, cu, 0.8, s0,
+                                                  lambda m: m // r, lambda j: j)):
+        fails += int(not np.array_equal(o[:, m], om))
+        fails += int(not np.array_equal(sf[:, m // r], sm))
+    return fails
+
+
+def pin_mixed_layout_is_single_head_runs(gdn):
+    """h_q = 4 query heads over h_v = 2 states that share h_k = 1 key head."""
+    rng = np.random.default_rng(11)
+    T = 7
+    q, k, v, a, b = _rand_heads(rng, T, 4, 1, 2, 4, 4)
+    o, sf = gdn(q, k, v, a, b, [0, T], 1.1, None)
+    fails = int(o.shape != (T, 4, 4))
+    for m, (om, sm) in enumerate(_single_head_runs(gdn, q, k, v, a, b, [0, T], 1.1, None,
+                                                  lambda m: m // 2, lambda j: 0)):
+        fails += int(not np.array_equal(o[:, m], om))
+    return fails
+
+
+GQA_PINS = [pin_grouped_queries_are_single_head_runs, pin_mixed_layout_is_single_head_runs]
+
+
+@pytest.mark.parametrize("pin", GQA_PINS, ids=lambda p: p.__name__)
+def test_oracle_passes_grouped_query_pin(pin):
+    assert pin(_oracle) == 0
+
+
+def test_head_layouts():
+    assert oracle.gdn_out_heads(2, 2, 2) == 2      # MHA
+    assert oracle.gdn_out_heads(2, 2, 6) == 6      # GVA
+    assert oracle.gdn_out_heads(8, 2, 2) == 8      # GQA
+    assert oracle.gdn_out_heads(4, 1, 2) == 4      # grouped queries over grouped values
+    for bad in [(2, 4, 2), (3, 2, 2), (2, 1, 4), (6, 2, 4)]:
+        with pytest.raises(ValueError):
+            oracle.gdn_out_heads(*bad)
+
+
+def _np_gdn_heads(mutant=None):
+    """A numpy statement of the head layouts, with planted head-mapping mistakes."""
+    def gdn(q, k, v, a, b, cu, scale, s0=None):
+        q, k, v, a, b = (np.asarray(x, dtype=np.float64) for x in (q, k, v, a, b))
+        T, hq, dk = q.shape
+        hk, hv, dv = k.shape[1], v.shape[1], v.shape[2]
+        ho = hv if hq == hk else hq
+        r = 1 if ho == hv else hq // hv
+        o = np.zeros((T, ho, dv))
+        sf = np.zeros((len(cu) - 1, hv, dv, dk))
+        for i in range(len(cu) - 1):
+            for j in range(hv):
+                H = np.zeros((dv, dk)) if s0 is None else np.array(s0[i, j], dtype=np.float64)
+                jk = j // (hv // hk)
+                for t in range(cu[i], cu[i + 1]):
+                    kt, vt = k[t, jk], v[t, j]
+                    Hd = a[t, j] * H
+                    H = Hd + np.outer(b[t, j] * (vt - Hd @ kt), kt)
+                    for g in range(r):
+                        m = (j // (hv // hk)) if ho == hv else j * r + g
+                        if mutant == "interleaved_queries" and ho != hv:
+                            m = g * hv + j            # query m read from state m % h_v
+                        if mutant == "first_query_only" and g > 0:
+                            continue
+                        o[t, (j if ho == hv else j * r + g)] = scale * (H @ q[t, m])
+                sf[i, j] = H
+        return o, sf
+    return gdn
+
+
+@pytest.mark.parametrize("mutant", ["interleaved_queries", "first_query_only"])
+def test_grouped_query_pins_catch_planted_mistakes(mutant):
+    g = _np_gdn_heads(mutant)
+    assert sum(pin(g) for pin in GQA_PINS) >= 1, f"no pin caught {mutant}"
+
+
+def test_unmutated_head_layout_copy_passes_the_grouped_query_pins():
+    g = _np_gdn_heads(None)
+    assert all(pin(g) == 0 for pin in GQA_PINS)
