@@ -144,6 +144,9 @@ def load():
         lib.gdn_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
                                     ctypes.c_float, vp, vp, vp, vp, sz, vp]
         lib.gdn_prefill.restype = i32
+        lib.gdn_prefill_heads.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                          ctypes.c_float, vp, vp, vp, vp, sz, vp]
+        lib.gdn_prefill_heads.restype = i32
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
         lib.gdn_check_status.argtypes = [vp, vp]
@@ -472,6 +475,26 @@ def gdn_prefill(q: int, k: int, v: int, alpha: int, beta: int, cu_seqlens: int, 
                               workspace_bytes, stream)
 
 
+def gdn_prefill_heads(q: int, k: int, v: int, alpha: int, beta: int, cu_seqlens: int,
+                      n_seqs: int, total_tokens: int, h_q: int, h_k: int, h_v: int,
+                      head_dim: int, scale: float, initial_state: int, o: int, final_state: int,
+                      workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    return load().gdn_prefill_heads(q, k, v, alpha, beta, cu_seqlens, n_seqs, total_tokens, h_q,
+                                    h_k, h_v, head_dim, scale, initial_state, o, final_state,
+                                    workspace, workspace_bytes, stream)
+
+
+def gdn_out_heads(h_q: int, h_k: int, h_v: int) -> int:
+    """Output heads of a head layout: h_v with h_q == h_k (MHA, GVA), h_q with h_q a multiple
+    of h_v (GQA); ValueError otherwise (h_v must be a multiple of h_k)."""
+    if h_q > 0 and h_k > 0 and h_v > 0 and h_v % h_k == 0:
+        if h_q == h_k:
+            return h_v
+        if h_q % h_v == 0:
+            return h_q
+    raise ValueError(f"heads q {h_q}, k {h_k}, v {h_v} form no supported layout")
+
+
 def gdn_last_error() -> str:
     return load().gdn_last_error().decode()
 
@@ -490,24 +513,27 @@ def gdn_set_fault_injection(mode: int) -> int:
 
 def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_state=None,
                      output_final_state: bool = False, stream=None, workspace=None):
-    """Gated Delta Net prefill over packed sequences (CUDA tensors): q, k [T, h_qk, 128] and
-    v [T, h_v, 128] bfloat16; alpha, beta [T, h_v] float32; cu_seqlens [n + 1] int32;
-    initial_state [n, h_v, 128, 128] float32 or None.  Returns (o [T, h_v, 128] bfloat16,
-    final_state or None).  Asynchronous on ``stream``; raises GemmError on a non-zero status."""
+    """Gated Delta Net prefill over packed sequences (CUDA tensors): q [T, h_q, 128], k
+    [T, h_k, 128] and v [T, h_v, 128] bfloat16; alpha, beta [T, h_v] float32; cu_seqlens [n + 1]
+    int32; initial_state [n, h_v, 128, 128] float32 or None.  h_v is a multiple of h_k, and h_q
+    equals h_k (MHA, GVA: o has h_v heads) or is a multiple of h_v (GQA: o has h_q heads).
+    Returns (o [T, h_o, 128] bfloat16, final_state or None).  Asynchronous on ``stream``; raises
+    GemmError on a non-zero status."""
     import torch
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
                         ("v", v, torch.bfloat16), ("alpha", alpha, torch.float32),
                         ("beta", beta, torch.float32), ("cu_seqlens", cu_seqlens, torch.int32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
-    T, h_qk, d = q.shape
-    h_v = v.shape[1]
+    T, h_q, d = q.shape
+    h_k, h_v = k.shape[1], v.shape[1]
+    h_o = gdn_out_heads(h_q, h_k, h_v)
     n = cu_seqlens.numel() - 1
     if initial_state is not None and (initial_state.dtype != torch.float32 or
                                       tuple(initial_state.shape) != (n, h_v, d, d) or
                                       not initial_state.is_contiguous()):
         raise ValueError("initial_state must be a contiguous float32 [n, h_v, d, d] tensor")
-    o = torch.empty((T, h_v, d), dtype=torch.bfloat16, device=q.device)
+    o = torch.empty((T, h_o, d), dtype=torch.bfloat16, device=q.device)
     sf = (torch.empty((n, h_v, d, d), dtype=torch.float32, device=q.device)
           if output_final_state else None)
     if workspace is None:
@@ -515,11 +541,11 @@ def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_sta
         s = stream if stream is not None else torch.cuda.current_stream()
         with torch.cuda.stream(s) if hasattr(s, "cuda_stream") else _nullctx():
             workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    rc = gdn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(), beta.data_ptr(),
-                     cu_seqlens.data_ptr(), n, T, h_qk, h_v, d, float(scale),
-                     0 if initial_state is None else initial_state.data_ptr(), o.data_ptr(),
-                     0 if sf is None else sf.data_ptr(), workspace.data_ptr(),
-                     workspace.numel(), _stream_handle(stream))
+    rc = gdn_prefill_heads(q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(),
+                           beta.data_ptr(), cu_seqlens.data_ptr(), n, T, h_q, h_k, h_v, d,
+                           float(scale), 0 if initial_state is None else initial_state.data_ptr(),
+                           o.data_ptr(), 0 if sf is None else sf.data_ptr(), workspace.data_ptr(),
+                           workspace.numel(), _stream_handle(stream))
     if rc != GDN_OK:
         raise GemmError(rc, gdn_last_error())
     return o, sf

@@ -321,7 +321,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                        const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v, const float* __restrict__ alpha,
                        const float* __restrict__ beta, const int4* __restrict__ chunks,
-                       const int32_t* __restrict__ n_chunks, int32_t h_v, int32_t group,
+                       const int32_t* __restrict__ n_chunks, int32_t h_v, int32_t qgroup,
+                       int32_t kgroup, int32_t clear_status,
                        __nv_bfloat16* __restrict__ wp, __nv_bfloat16* __restrict__ ap,
                        float* __restrict__ ut, float* __restrict__ gam_out, int32_t single_T,
                        uint32_t* __restrict__ status, uint32_t* __restrict__ counter,
@@ -330,24 +331,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const int32_t ch = blockIdx.x;
     const int32_t j = blockIdx.y;
     // one sequence (single_T >= 0): chunk ch covers tokens 64 ch .. (no chunk list is built,
-    // and this kernel clears the call's status word and work counter); otherwise the chunk list
-    // says
+    // and the first pass of a call clears its status word here); otherwise the chunk list says
     int32_t t0, len;
     if (single_T >= 0) {
         t0 = ch * kC;
         if (t0 >= single_T) return;
         len = min(kC, single_T - t0);
-        if (ch == 0 && j == 0 && threadIdx.x == 0) {
-            *status = 0u;
-            *counter = 0u;
-        }
+        if (ch == 0 && j == 0 && threadIdx.x == 0 && clear_status) *status = 0u;
     } else {
         if (ch >= *n_chunks) return;
         const int4 info = chunks[ch];
         t0 = info.y;
         len = info.z;
     }
-    const int32_t jq = j / group;
+    if (ch == 0 && j == 0 && threadIdx.x == 0) *counter = 0u;   // the scan's work counter
+    const int32_t jq = j / qgroup, jk = j / kgroup;   // query / key head of state head j
     const int64_t cj = static_cast<int64_t>(ch) * h_v + j;
     const int tid = threadIdx.x;
     // alpha and beta first: their latency overlaps the tile loads
@@ -381,7 +379,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         gf16::mbar_arrive_expect_tx(bar, 3 * kPrepTile);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            gf16::tma_load_3d(kb_s + h * kC * 128, &map_k, bar, 64 * h, jq, t0);
+            gf16::tma_load_3d(kb_s + h * kC * 128, &map_k, bar, 64 * h, jk, t0);
             gf16::tma_load_3d(qb_s + h * kC * 128, &map_q, bar, 64 * h, jq, t0);
             gf16::tma_load_3d(vb_s + h * kC * 128, &map_v, bar, 64 * h, j, t0);
         }
@@ -617,7 +615,7 @@ __device__ __forceinline__ void scan_issue(uint32_t base, int s, uint32_t bar,
                                            const CUtensorMap* map_q, const CUtensorMap* map_k,
                                            const float* __restrict__ ut,
                                            const float* __restrict__ gam, int64_t cj, int32_t r0,
-                                           int32_t t0, int32_t jq)
+                                           int32_t t0, int32_t jq, int32_t jk)
 {
     gf16::mbar_arrive_expect_tx(bar, kStageTx);
     const uint32_t st = base + s * kStageBytes;
@@ -626,7 +624,7 @@ __device__ __forceinline__ void scan_issue(uint32_t base, int s, uint32_t bar,
     for (int h = 0; h < 2; ++h) {
         gf16::tma_load_2d(st + kOffW + h * 3 * kC * 128, map_w, bar, 64 * h, yw);
         gf16::tma_load_3d(st + kOffQ + h * kC * 128, map_q, bar, 64 * h, jq, t0);
-        gf16::tma_load_3d(st + kOffK + h * kC * 128, map_k, bar, 64 * h, jq, t0);
+        gf16::tma_load_3d(st + kOffK + h * kC * 128, map_k, bar, 64 * h, jk, t0);
     }
     gf16::tma_load_2d(st + kOffA, map_a, bar, 0, ya);
     bulk_g2s(base + kOffUp + s * kRows * kC * 4, ut + (cj * kD + r0) * kC, kRows * kC * 4, bar);
@@ -645,7 +643,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     int32_t n_items, const float* __restrict__ ut,
                     const float* __restrict__ gam, const float* __restrict__ s0,
                     float* __restrict__ s_final, __nv_bfloat16* __restrict__ o,
-                    uint32_t* __restrict__ status, int32_t h_v, int32_t group, float scale,
+                    uint32_t* __restrict__ status, int32_t h_v, int32_t qgroup, int32_t kgroup,
+                    int32_t o_tok, int32_t o_hmul, float scale,
                     uint64_t wait_ns, uint32_t fault, int32_t single_T)
 {
     extern __shared__ __align__(16) uint8_t smraw[];
@@ -735,7 +734,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (tid == 0 && draws) drawn = atomicAdd(counter, 1u);
         int32_t qn = n_items;   // the next item, known from the first chunk's middle barrier
         Item nx{};
-        const int32_t j = it.j, r0 = it.r0, jq = j / group;
+        const int32_t j = it.j, r0 = it.r0, jq = j / qgroup, jk = j / kgroup;
         const int32_t c_begin = it.c_begin, c_end = it.c_end;
         const int32_t seq_start = it.seq_start, seq_end = it.seq_end;
         const auto chunk_t0 = [&](int32_t ch) { return seq_start + (ch - c_begin) * kC; };
@@ -758,7 +757,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (c_begin < c_end && !have_first) {
             if (tid == 0)
                 scan_issue(base, n & 1, bar0 + 8 * (n & 1), &map_w, &map_a, &map_q, &map_k, ut,
-                           gam, cj_of(c_begin), r0, chunk_t0(c_begin), jq);
+                           gam, cj_of(c_begin), r0, chunk_t0(c_begin), jq, jk);
             const bool ok = gf16::mbar_wait(bar0 + 8 * (n & 1), (n >> 1) & 1, nullptr, wait_ns);
             if (__syncthreads_or(!ok)) {
                 if (tid == 0) atomicExch(status, 1u);
@@ -775,7 +774,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 const int tt = t + 8 * h;
                 if (tt < pend_len)
                     *reinterpret_cast<uint32_t*>(
-                        o + ((static_cast<int64_t>(pend_t0) + tt) * h_v + j) * kD + r0 + r) =
+                        o + ((static_cast<int64_t>(pend_t0) + tt) * o_tok + j * o_hmul) * kD +
+                            r0 + r) =
                         pack_bf16(scale * (pend[2 * h] + mypart[(2 * h) * 32]),
                                   scale * (pend[2 * h + 1] + mypart[(2 * h + 1) * 32]));
             }
@@ -792,7 +792,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             // in flight)
             if (tid == 0 && ch + 1 < c_end && !(fault == 1 && ch == c_begin))
                 scan_issue(base, b ^ 1, bar0 + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut,
-                           gam, cj_of(ch + 1), r0, chunk_t0(ch + 1), jq);
+                           gam, cj_of(ch + 1), r0, chunk_t0(ch + 1), jq, jk);
             const uint32_t sb = base + b * kStageBytes;
             const uint32_t w_s = sb + kOffW, q_s = sb + kOffQ, k_s = sb + kOffK, a_s = sb + kOffA;
             const float* Bup = upf + b * kRows * kC;   // U'^T rows [r][t]
@@ -862,7 +862,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             if (kMulti && tid == 0 && ch + 1 == c_end && qn < n_items && nx.c_begin < nx.c_end)
                 scan_issue(base, b ^ 1, bar0 + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut, gam,
                            static_cast<int64_t>(nx.c_begin) * h_v + nx.j, nx.r0, nx.seq_start,
-                           nx.j / group);
+                           nx.j / qgroup, nx.j / kgroup);
 
             // ---- phase 2a: S_next^T[c][r] = g_C S^T + K^T U~ over tokens t (4 steps of 16) ----
             {
@@ -942,21 +942,33 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
+// Output heads of the head layout (h_q, h_k, h_v), or -1: h_v a multiple of h_k, and either
+// h_q == h_k (one output per value head: MHA, GVA) or h_q a multiple of h_v (one output per
+// query head, query head m reading state m / (h_q / h_v): GQA).
+int64_t out_heads(int64_t h_q, int64_t h_k, int64_t h_v)
+{
+    if (h_q <= 0 || h_k <= 0 || h_v <= 0 || h_v % h_k != 0) return -1;
+    if (h_q == h_k) return h_v;
+    if (h_q % h_v == 0) return h_q;
+    return -1;
+}
+
 int check(const void* q, const void* k, const void* v, const float* alpha, const float* beta,
-          const int32_t* cu, int64_t n_seqs, int64_t T, int64_t h_qk, int64_t h_v,
+          const int32_t* cu, int64_t n_seqs, int64_t T, int64_t h_q, int64_t h_k, int64_t h_v,
           int64_t head_dim, const void* o)
 {
-    if (n_seqs < 0 || T < 0 || h_qk <= 0 || h_v <= 0)
+    if (n_seqs < 0 || T < 0 || h_q <= 0 || h_k <= 0 || h_v <= 0)
         return gdn_fail(GDN_ERR_INVALID_ARG, "negative size or no heads (n_seqs=%lld T=%lld "
-                        "h_qk=%lld h_v=%lld)", (long long)n_seqs, (long long)T,
-                        (long long)h_qk, (long long)h_v);
-    if (h_v % h_qk != 0)
-        return gdn_fail(GDN_ERR_INVALID_ARG, "h_v=%lld is not a multiple of h_qk=%lld",
-                        (long long)h_v, (long long)h_qk);
+                        "h_q=%lld h_k=%lld h_v=%lld)", (long long)n_seqs, (long long)T,
+                        (long long)h_q, (long long)h_k, (long long)h_v);
+    if (out_heads(h_q, h_k, h_v) < 0)
+        return gdn_fail(GDN_ERR_INVALID_ARG, "heads q=%lld k=%lld v=%lld: h_v must be a multiple "
+                        "of h_k, and h_q equal h_k or be a multiple of h_v", (long long)h_q,
+                        (long long)h_k, (long long)h_v);
     if (head_dim != kD)
         return gdn_fail(GDN_ERR_UNSUPPORTED, "head_dim=%lld; this build supports 128",
                         (long long)head_dim);
-    if (T > (1ll << 30) || n_seqs > (1ll << 30) || h_v > 65535)
+    if (T > (1ll << 30) || n_seqs > (1ll << 30) || h_v > 65535 || h_q > 65535)
         return gdn_fail(GDN_ERR_INVALID_ARG, "size out of range");
     if (n_seqs == 0) return GDN_OK;
     if (cu == nullptr) return gdn_fail(GDN_ERR_INVALID_ARG, "cu_seqlens is null");
@@ -1015,15 +1027,16 @@ int gdn_prefill_workspace_bytes(int64_t total_tokens, int64_t n_seqs, int64_t h_
     return GDN_OK;
 }
 
-int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
-                const float* beta, const int32_t* cu_seqlens, int64_t n_seqs,
-                int64_t total_tokens, int64_t h_qk, int64_t h_v, int64_t head_dim, float scale,
-                const float* initial_state, void* o, float* final_state, void* workspace,
-                size_t workspace_bytes, cudaStream_t stream)
+int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* alpha,
+                      const float* beta, const int32_t* cu_seqlens, int64_t n_seqs,
+                      int64_t total_tokens, int64_t h_q, int64_t h_k, int64_t h_v,
+                      int64_t head_dim, float scale, const float* initial_state, void* o,
+                      float* final_state, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream)
 {
     t_gdn_error.clear();
-    int rc = check(q, k, v, alpha, beta, cu_seqlens, n_seqs, total_tokens, h_qk, h_v, head_dim,
-                   o);
+    int rc = check(q, k, v, alpha, beta, cu_seqlens, n_seqs, total_tokens, h_q, h_k, h_v,
+                   head_dim, o);
     if (rc != GDN_OK || n_seqs == 0) return rc;
     const WsLayout l = layout_for(total_tokens, n_seqs, h_v);
     if (workspace == nullptr || workspace_bytes < l.total || misaligned(workspace))
@@ -1048,31 +1061,16 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
         return gdn_fail(GDN_ERR_UNSUPPORTED, "too many chunks x value heads for one call (%lld)",
                         (long long)(mc * h_v));
 
-    // TMA descriptors: W pieces [cj * 192 rows][128], A' pieces [cj * 128 rows][64], q and k as
-    // {128, h_qk, total_tokens}, v as {128, h_v, total_tokens}.  With no tokens nothing is loaded
-    // and they stay zero.
-    CUtensorMap map_w{}, map_a{}, map_q{}, map_k{}, map_v{};
-    if (total_tokens > 0) {
-        const cuuint64_t dw[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(mc * h_v * 3 * kC)};
-        const cuuint64_t sw[1] = {kD * 2};
-        const cuuint32_t bw[2] = {64, 3 * kC};
-        const cuuint64_t da[2] = {static_cast<cuuint64_t>(kC), static_cast<cuuint64_t>(mc * h_v * 2 * kC)};
-        const cuuint64_t sa[1] = {kC * 2};
-        const cuuint32_t ba[2] = {64, 2 * kC};
-        const cuuint64_t dq[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(h_qk),
-                                  static_cast<cuuint64_t>(total_tokens)};
-        const cuuint64_t sq[2] = {kD * 2, static_cast<cuuint64_t>(h_qk) * kD * 2};
-        const cuuint32_t bq[3] = {64, 1, kC};
-        if ((rc = gdn_make_map(&map_w, wp, 2, dw, sw, bw, "W pieces")) != GDN_OK ||
-            (rc = gdn_make_map(&map_a, ap, 2, da, sa, ba, "A' pieces")) != GDN_OK ||
-            (rc = gdn_make_map(&map_q, q, 3, dq, sq, bq, "q")) != GDN_OK ||
-            (rc = gdn_make_map(&map_k, k, 3, dq, sq, bq, "k")) != GDN_OK)
-            return rc;
-        const cuuint64_t dv[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(h_v),
-                                  static_cast<cuuint64_t>(total_tokens)};
-        const cuuint64_t sv[2] = {kD * 2, static_cast<cuuint64_t>(h_v) * kD * 2};
-        if ((rc = gdn_make_map(&map_v, v, 3, dv, sv, bq, "v")) != GDN_OK) return rc;
-    }
+    // Heads.  State head j reads key head j / kgroup.  With h_q == h_k its one output is output
+    // head j and its query head j / kgroup (one pass).  With grouped queries (h_q a multiple of
+    // h_v) it serves query heads j r + g, g < r = h_q / h_v, written to output heads j r + g:
+    // pass g runs the whole pipeline on the strided view of q that holds heads j r + g (the state
+    // recurrence does not read q, so every pass reproduces the same states; only pass 0 writes
+    // the final states).
+    const int64_t h_o = out_heads(h_q, h_k, h_v);
+    const int64_t passes = h_o == h_v ? 1 : h_q / h_v;
+    const int32_t kgroup = static_cast<int32_t>(h_v / h_k);
+    const int32_t qgroup = passes == 1 ? kgroup : 1;
 
     static bool attrs = false;
     if (!attrs) {
@@ -1088,7 +1086,55 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
     // number the chunks themselves and the chunk-list launch is skipped.
     const int32_t single_T = (n_seqs == 1 && total_tokens > 0) ? static_cast<int32_t>(total_tokens)
                                                                 : -1;
+    const int64_t n_items = n_seqs * h_v * (kD / kRows);
+    int dev = 0, sms = 0;
     cudaError_t e = cudaSuccess;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return gdn_fail(GDN_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+
+    // TMA descriptors that do not depend on the pass: W pieces [cj * 192 rows][128], A' pieces
+    // [cj * 128 rows][64], k as {128, h_k, total_tokens}, v as {128, h_v, total_tokens}.  With no
+    // tokens nothing is loaded and they stay zero.
+    CUtensorMap map_w{}, map_a{}, map_k{}, map_v{};
+    const cuuint32_t bq[3] = {64, 1, kC};
+    if (total_tokens > 0) {
+        const cuuint64_t dw[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(mc * h_v * 3 * kC)};
+        const cuuint64_t sw[1] = {kD * 2};
+        const cuuint32_t bw[2] = {64, 3 * kC};
+        const cuuint64_t da[2] = {static_cast<cuuint64_t>(kC), static_cast<cuuint64_t>(mc * h_v * 2 * kC)};
+        const cuuint64_t sa[1] = {kC * 2};
+        const cuuint32_t ba[2] = {64, 2 * kC};
+        const cuuint64_t dk3[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(h_k),
+                                   static_cast<cuuint64_t>(total_tokens)};
+        const cuuint64_t sk3[2] = {kD * 2, static_cast<cuuint64_t>(h_k) * kD * 2};
+        const cuuint64_t dv3[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(h_v),
+                                   static_cast<cuuint64_t>(total_tokens)};
+        const cuuint64_t sv3[2] = {kD * 2, static_cast<cuuint64_t>(h_v) * kD * 2};
+        if ((rc = gdn_make_map(&map_w, wp, 2, dw, sw, bw, "W pieces")) != GDN_OK ||
+            (rc = gdn_make_map(&map_a, ap, 2, da, sa, ba, "A' pieces")) != GDN_OK ||
+            (rc = gdn_make_map(&map_k, k, 3, dk3, sk3, bq, "k")) != GDN_OK ||
+            (rc = gdn_make_map(&map_v, v, 3, dv3, sv3, bq, "v")) != GDN_OK)
+            return rc;
+    }
+    // q as seen by pass g: h_q heads (one pass), or the h_v heads j r + g (stride r heads)
+    CUtensorMap map_q[8];
+    const int64_t map_passes = total_tokens > 0 ? passes : 1;
+    if (map_passes > 8)
+        return gdn_fail(GDN_ERR_UNSUPPORTED, "more than 8 query heads per state head");
+    for (int64_t gp = 0; gp < map_passes; ++gp) {
+        map_q[gp] = CUtensorMap{};
+        if (total_tokens == 0) continue;
+        const cuuint64_t dq[3] = {static_cast<cuuint64_t>(kD),
+                                  static_cast<cuuint64_t>(passes == 1 ? h_q : h_v),
+                                  static_cast<cuuint64_t>(total_tokens)};
+        const cuuint64_t sq[2] = {static_cast<cuuint64_t>(passes) * kD * 2,
+                                  static_cast<cuuint64_t>(h_q) * kD * 2};
+        if ((rc = gdn_make_map(&map_q[gp], static_cast<const __nv_bfloat16*>(q) + gp * kD, 3, dq,
+                               sq, bq, "q")) != GDN_OK)
+            return rc;
+    }
+
     if (single_T < 0) {
         gdn_chunk_list_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, static_cast<int32_t>(n_seqs),
                                                       chunk_offset, chunks,
@@ -1097,33 +1143,42 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
         if ((e = cudaGetLastError()) != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_chunk_list_kernel: %s", cudaGetErrorString(e));
     }
-    if (mc > 0 && total_tokens > 0) {
-        const dim3 pgrid(static_cast<uint32_t>(mc), static_cast<uint32_t>(h_v));
-        gdn_prepare_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
-            map_q, map_k, map_v, alpha, beta, chunks, n_chunks, static_cast<int32_t>(h_v),
-            static_cast<int32_t>(h_v / h_qk), wp, ap, ut, gm, single_T, status, counter,
-            g_gdn_wait_ns.load());
+    // with no tokens every state only passes through: one pass
+    for (int64_t gp = 0; gp < map_passes; ++gp) {
+        if (mc > 0 && total_tokens > 0) {
+            const dim3 pgrid(static_cast<uint32_t>(mc), static_cast<uint32_t>(h_v));
+            gdn_prepare_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
+                map_q[gp], map_k, map_v, alpha, beta, chunks, n_chunks, static_cast<int32_t>(h_v),
+                qgroup, kgroup, gp == 0, wp, ap, ut, gm, single_T, status, counter,
+                g_gdn_wait_ns.load());
+            if ((e = cudaGetLastError()) != cudaSuccess)
+                return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
+        }
+        // persistent scan: one CTA per SM (at most one per work item) taking items dynamically
+        const int64_t ctas = n_items < sms ? n_items : sms;
+        auto* scan = n_items > sms ? gdn_scan_kernel<true> : gdn_scan_kernel<false>;
+        scan<<<static_cast<uint32_t>(ctas), kScanThreads, kScanSmem, stream>>>(
+            map_w, map_a, map_q[gp], map_k, single_T >= 0 ? nullptr : order,
+            single_T >= 0 ? nullptr : seqinfo, counter, static_cast<int32_t>(n_items), ut, gm,
+            initial_state, gp == 0 ? final_state : nullptr,
+            static_cast<__nv_bfloat16*>(o) + gp * kD, status, static_cast<int32_t>(h_v), qgroup,
+            kgroup, static_cast<int32_t>(h_o), static_cast<int32_t>(passes), scale,
+            g_gdn_wait_ns.load(), g_gdn_fault.load(), single_T);
         if ((e = cudaGetLastError()) != cudaSuccess)
-            return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
+            return gdn_fail(GDN_ERR_CUDA, "gdn_scan_kernel: %s", cudaGetErrorString(e));
     }
-    // persistent scan: one CTA per SM (at most one per work item) taking items dynamically
-    const int64_t n_items = n_seqs * h_v * (kD / kRows);
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return gdn_fail(GDN_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
-    const int64_t ctas = n_items < sms ? n_items : sms;
-    auto* scan = n_items > sms ? gdn_scan_kernel<true> : gdn_scan_kernel<false>;
-    scan<<<static_cast<uint32_t>(ctas), kScanThreads, kScanSmem, stream>>>(
-        map_w, map_a, map_q, map_k, single_T >= 0 ? nullptr : order,
-        single_T >= 0 ? nullptr : seqinfo, counter, static_cast<int32_t>(n_items), ut, gm,
-        initial_state, final_state,
-        static_cast<__nv_bfloat16*>(o), status, static_cast<int32_t>(h_v),
-        static_cast<int32_t>(h_v / h_qk), scale, g_gdn_wait_ns.load(), g_gdn_fault.load(),
-        single_T);
-    if ((e = cudaGetLastError()) != cudaSuccess)
-        return gdn_fail(GDN_ERR_CUDA, "gdn_scan_kernel: %s", cudaGetErrorString(e));
     return GDN_OK;
+}
+
+int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
+                const float* beta, const int32_t* cu_seqlens, int64_t n_seqs,
+                int64_t total_tokens, int64_t h_qk, int64_t h_v, int64_t head_dim, float scale,
+                const float* initial_state, void* o, float* final_state, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream)
+{
+    return gdn_prefill_heads(q, k, v, alpha, beta, cu_seqlens, n_seqs, total_tokens, h_qk, h_qk,
+                             h_v, head_dim, scale, initial_state, o, final_state, workspace,
+                             workspace_bytes, stream);
 }
 
 const char* gdn_last_error(void) { return t_gdn_error.c_str(); }

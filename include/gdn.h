@@ -20,18 +20,26 @@
  * sequence i owns tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 and its own state.  The host never
  * reads cu_seqlens: it is a device array the kernels consult.
  *
- * Heads: q and k have h_qk heads; v, alpha, beta, the states and o have h_v heads, a multiple of
- * h_qk.  Value head j reads query/key head j / (h_v / h_qk): h_v == h_qk is multi-head attention,
- * h_v > h_qk grouped values (GVA).
+ * Heads (the page's three relations: MHA, GQA, GVA).  q has h_q heads, k h_k, and v, alpha,
+ * beta and the states h_v, a multiple of h_k; state head j reads key head j / (h_v / h_k).
+ *   h_q == h_k            o has h_v heads; state j reads query head j / (h_v / h_k) and writes
+ *                         output head j (h_v == h_k: multi-head attention; larger: grouped
+ *                         values, GVA)
+ *   h_q a multiple of h_v o has h_q heads; query head m reads state m / (h_q / h_v) and writes
+ *                         output head m (grouped queries, GQA; at most 8 query heads per state).
+ *                         The state recurrence does not read q: the call runs the pipeline once
+ *                         per query head of a group, each pass reproducing the same states.
+ * gdn_prefill is gdn_prefill_heads with h_q == h_k == h_qk.
  *
  * Layouts (row-major, device memory of the current device):
- *   q, k           bfloat16 [total_tokens][h_qk][head_dim]
+ *   q              bfloat16 [total_tokens][h_q][head_dim]
+ *   k              bfloat16 [total_tokens][h_k][head_dim]
  *   v              bfloat16 [total_tokens][h_v][head_dim]
  *   alpha, beta    float    [total_tokens][h_v]     alpha in (0, 1]; beta any real
  *   cu_seqlens     int32    [n_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
  *                                     cu_seqlens[n_seqs] = total_tokens
  *   initial_state  float    [n_seqs][h_v][head_dim (dv)][head_dim (dk)], or NULL for zeros
- *   o              bfloat16 [total_tokens][h_v][head_dim]   (written)
+ *   o              bfloat16 [total_tokens][h_o][head_dim]   (written; h_o as above)
  *   final_state    float    [n_seqs][h_v][dv][dk], or NULL   (written)
  *   workspace      gdn_prefill_workspace_bytes() bytes, 16-byte aligned
  *
@@ -40,9 +48,10 @@
  * (above 1e-37); alpha = 0, a full reset, is outside this routine's domain.
  *
  * Ownership: the caller owns every buffer; nothing is retained after a call.  Asynchronous on
- * `stream`.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, h_v not a multiple of
- * h_qk, workspace too small), GDN_ERR_UNSUPPORTED (head_dim other than 128, misaligned
- * q/k/v/o, more than 2^31 / 192 chunks x value heads), GDN_ERR_CUDA (a launch failed;
+ * `stream`.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, heads in none of the
+ * layouts above, workspace too small), GDN_ERR_UNSUPPORTED (head_dim other than 128, misaligned
+ * q/k/v/o, more than 8 query heads per state head, more than 2^31 / 192 chunks x value heads),
+ * GDN_ERR_CUDA (a launch failed;
  * gdn_last_error() says why).  Nothing is enqueued on an error.  n_seqs == 0 does nothing.
  *
  * Device-side failure: every wait of the scan kernel for a chunk's loads is bounded (default
@@ -71,12 +80,20 @@ extern "C" {
 int gdn_prefill_workspace_bytes(int64_t total_tokens, int64_t n_seqs, int64_t h_v,
                                 size_t* bytes);
 
-/* The gated delta rule over packed sequences, as above. */
+/* The gated delta rule over packed sequences, as above, q and k sharing h_qk heads. */
 int gdn_prefill(const void* q, const void* k, const void* v, const float* alpha,
                 const float* beta, const int32_t* cu_seqlens, int64_t n_seqs,
                 int64_t total_tokens, int64_t h_qk, int64_t h_v, int64_t head_dim, float scale,
                 const float* initial_state, void* o, float* final_state, void* workspace,
                 size_t workspace_bytes, cudaStream_t stream);
+
+/* The same with separate query, key and value head counts (MHA, GVA and GQA, as above). */
+int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* alpha,
+                      const float* beta, const int32_t* cu_seqlens, int64_t n_seqs,
+                      int64_t total_tokens, int64_t h_q, int64_t h_k, int64_t h_v,
+                      int64_t head_dim, float scale, const float* initial_state, void* o,
+                      float* final_state, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
 
 /* The message of the calling thread's last failed gdn_* call ("" if none). */
 const char* gdn_last_error(void);

@@ -188,3 +188,79 @@ def test_more_sequences_than_the_ranking_block():
     inp = make_gdn_inputs(T, n, 1, 1, 128, 128, seed=42, state=True)
     o, sf = run(inp, 1, 1)
     assert_parity(inp, o, sf, 0.73, "1100 sequences")
+
+
+def _grouped_query_inputs(T, n, h_q, h_k, h_v, seed, state=True):
+    """make_gdn_inputs with h_k key heads, plus a separate q of h_q unit-norm bf16 heads."""
+    inp = make_gdn_inputs(T, n, h_k, h_v, 128, 128, seed=seed, state=state)
+    gq = torch.Generator().manual_seed(seed + 1000)
+    x = torch.randn((T, h_q, 128), generator=gq)
+    inp["q"] = (x / x.norm(dim=-1, keepdim=True).clamp_min(1e-6)).to(torch.bfloat16)
+    return inp
+
+
+def run_heads(inp, h_q, h_k, h_v, scale=0.73):
+    """gdn_prefill_heads through the C ABI; outputs written into NaN-prefilled buffers."""
+    q, k, v = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda()
+    a, b = inp["alpha"].cuda(), inp["beta"].cuda()
+    cu = inp["cu_seqlens"].cuda()
+    s0 = None if inp["initial_state"] is None else inp["initial_state"].cuda()
+    T = q.shape[0]
+    n = cu.numel() - 1
+    h_o = g.gdn_out_heads(h_q, h_k, h_v)
+    o = torch.full((T, h_o, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sf = torch.full((n, h_v, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    need = g.gdn_prefill_workspace_bytes(T, n, h_v)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    rc = g.gdn_prefill_heads(q.data_ptr(), k.data_ptr(), v.data_ptr(), a.data_ptr(), b.data_ptr(),
+                             cu.data_ptr(), n, T, h_q, h_k, h_v, 128, scale,
+                             0 if s0 is None else s0.data_ptr(), o.data_ptr(), sf.data_ptr(),
+                             ws.data_ptr(), need, torch.cuda.current_stream().cuda_stream)
+    assert rc == g.GDN_OK, g.gdn_last_error()
+    torch.cuda.synchronize()
+    return o.float().cpu().double().numpy(), sf.cpu().double().numpy()
+
+
+GQA_SHAPES = [
+    # (T, n_seqs, h_q, h_k, h_v)
+    (300, 3, 4, 2, 2),      # GQA, 2 query heads per state, packed
+    (200, 1, 8, 2, 2),      # GQA, 4 query heads per state, one sequence
+    (150, 2, 4, 1, 2),      # grouped queries over grouped values
+    (700, 30, 4, 1, 2),     # more work items than SMs, 2 passes
+]
+
+
+@pytest.mark.parametrize("shape", GQA_SHAPES, ids=lambda s: "-".join(map(str, s)))
+def test_grouped_queries(shape):
+    T, n, h_q, h_k, h_v = shape
+    inp = _grouped_query_inputs(T, n, h_q, h_k, h_v, seed=500 + T + n)
+    o, sf = run_heads(inp, h_q, h_k, h_v)
+    assert o.shape[1] == h_q
+    assert_parity(inp, o, sf, 0.73, f"heads {shape}")
+
+
+def test_grouped_query_torch_entry_point():
+    inp = _grouped_query_inputs(130, 2, 4, 2, 2, seed=77)
+    d = {k: (v.cuda() if v is not None else None) for k, v in inp.items()}
+    o, sf = g.gated_delta_rule(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["cu_seqlens"],
+                               0.73, d["initial_state"], output_final_state=True)
+    torch.cuda.synchronize()
+    assert tuple(o.shape) == (130, 4, 128)
+    assert_parity(inp, o.float().cpu().double().numpy(), sf.cpu().double().numpy(), 0.73,
+                  "gated_delta_rule, grouped queries")
+
+
+def test_rejects_bad_head_layouts():
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    p = x.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(h_q, h_k, h_v):
+        return g.gdn_prefill_heads(p, p, p, p, p, p, 1, 4, h_q, h_k, h_v, 128, 1.0, 0, p, 0,
+                                   ws.data_ptr(), 1 << 20, s)
+
+    assert call(3, 2, 2) == g.GDN_ERR_INVALID_ARG     # h_q neither h_k nor a multiple of h_v
+    assert call(2, 2, 3) == g.GDN_ERR_INVALID_ARG     # h_v not a multiple of h_k
+    assert call(18, 1, 2) == g.GDN_ERR_UNSUPPORTED    # 9 query heads per state
+    torch.cuda.synchronize()
