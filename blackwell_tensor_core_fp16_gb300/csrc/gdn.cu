@@ -800,7 +800,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
             // ---- phase 1: U = U' - W S^T, P = Q S^T over this warp's 64 key columns ----
             float u_hi[4] = {0.f, 0.f, 0.f, 0.f}, u_lo[4] = {0.f, 0.f, 0.f, 0.f},
-                  u_l2[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+                  u_l2[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f},
+                  pq2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4) {
                 const int kk = 4 * kh + k4;
@@ -823,13 +824,21 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 mma_bf16(pq, qa, s01[0], s01[1]);
                 mma_bf16(u_lo, w0, s2[0], s2[1]);
                 mma_bf16(u_l2, w1, s01[2], s01[3]);
-                mma_bf16(pq, qa, s01[2], s01[3]);
+                mma_bf16(pq2, qa, s01[2], s01[3]);
                 mma_bf16(u_lo, w2, s01[0], s01[1]);
-                mma_bf16(pq, qa, s2[0], s2[1]);
+                mma_bf16(pq2, qa, s2[0], s2[1]);
             }
             float u[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) u[e] = u_hi[e] + (u_lo[e] + u_l2[e]);
+            for (int e = 0; e < 4; ++e) {
+                u[e] = u_hi[e] + (u_lo[e] + u_l2[e]);
+                pq[e] += pq2[e];
+            }
+            // (lower warps) the epilogue's U' rows and decay ratios, read before the barrier
+            const int te = m0 + gq, re = n0 + 2 * tg;
+            const float f0 = Bg[kC + te], f1 = Bg[kC + te + 8];
+            const float up0 = Bup[re * kC + te], up1 = Bup[(re + 1) * kC + te];
+            const float up2 = Bup[re * kC + te + 8], up3 = Bup[(re + 1) * kC + te + 8];
             if (kh) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) mypart[e * 32] = u[e];
@@ -845,12 +854,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) u[e] += mypart[e * 32];
                 // U~ = (g_C / g_t)(U' - W S^T) -> pieces [r][t] (stmatrix .trans of [t][r] fragments)
-                const int t = m0 + gq, r = n0 + 2 * tg;
-                const float f0 = Bg[kC + t], f1 = Bg[kC + t + 8];
-                const float x0 = f0 * (Bup[r * kC + t] - u[0]);
-                const float x1 = f0 * (Bup[(r + 1) * kC + t] - u[1]);
-                const float x2 = f1 * (Bup[r * kC + t + 8] - u[2]);
-                const float x3 = f1 * (Bup[(r + 1) * kC + t + 8] - u[3]);
+                const float x0 = f0 * (up0 - u[0]);
+                const float x1 = f0 * (up1 - u[1]);
+                const float x2 = f1 * (up2 - u[2]);
+                const float x3 = f1 * (up3 - u[3]);
                 const Pieces3 lo = split3(x0, x1), hi = split3(x2, x3);
                 // block lb (lanes 8 lb ..): stored row r = n0 + lr, columns t = m0 + 8 lb
                 const uint32_t addr = sw128(n0 + lr, m0 + 8 * (lb & 1));
@@ -868,7 +875,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             {
                 const float gc = Bg[kC - 1];
                 float acc[4] = {gc * st[0], gc * st[1], gc * st[2], gc * st[3]};
-                float acc2[4] = {0.f, 0.f, 0.f, 0.f};
+                float acc2[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int kk = 0; kk < kC / 16; ++kk) {
                     // A = K^T: ldmatrix .trans of k rows t = 16 kk + lr + 8 (lane / 16), columns
@@ -882,10 +889,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     ldsm_x2(u2, up_s + 2 * kRows * 128 + boff);
                     mma_bf16(acc, ka, u01[0], u01[1]);
                     mma_bf16(acc2, ka, u01[2], u01[3]);
-                    mma_bf16(acc2, ka, u2[0], u2[1]);
+                    mma_bf16(acc3, ka, u2[0], u2[1]);
                 }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) st[e] = acc[e] + acc2[e];
+                for (int e = 0; e < 4; ++e) st[e] = acc[e] + (acc2[e] + acc3[e]);
             }
 
             // ---- phase 2b: this warp's share of O = diag(g) P + A' U~ (tokens s <= t) ----
