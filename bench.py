@@ -95,6 +95,19 @@ def dist_env():
     return world, rank, local
 
 
+def clocks_rejected(info) -> bool:
+    """True for a clock record the timing rules reject: hw_slowdown, hw_thermal_slowdown or
+    sw_thermal_slowdown active, or a median SM clock under 60% of its maximum with no reason
+    (sw_power_cap alone is normal under a dense GEMM and is kept)."""
+    if not info:
+        return False
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(info.get("reasons") or []):
+        return True
+    sm, mx = info.get("sm_mhz"), info.get("sm_max_mhz")
+    return bool(sm and mx and sm < 0.6 * mx and not info.get("reasons"))
+
+
 def max_over_ranks(value: float, world: int, device=None) -> float:
     """The largest of every rank's `value` (a job's time is its slowest rank's); the same value
     on every rank.  Works on any initialised process group (NCCL on the GPUs, gloo on the CPU)."""
@@ -542,25 +555,38 @@ def run_ours(args):
         uuid = "GPU-" + str(props.uuid)
     except Exception:
         pass
-    clocks = ClockSampler(uuid)
-    clocks.start()
-    time.sleep(0.3)
-    barrier()
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter()
-    with torch.cuda.stream(stream):
-        events[0].record(stream)
-        e = 1
-        for _ in range(K):
-            for item in work:
-                launch(item)
-                events[e].record(stream)
-                e += 1
-    torch.cuda.synchronize()
-    barrier()
-    wall_s = time.perf_counter() - t_wall
-    clock_info = clocks.stop()
-    g.check_status(stream)
+
+    def timed_region():
+        clocks = ClockSampler(uuid)
+        clocks.start()
+        time.sleep(0.3)
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            events[0].record(stream)
+            e = 1
+            for _ in range(K):
+                for item in work:
+                    launch(item)
+                    events[e].record(stream)
+                    e += 1
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - t0
+        info = clocks.stop()
+        g.check_status(stream)
+        return wall, info
+
+    wall_s, clock_info = timed_region()
+    # A run whose clocks show a hardware or thermal slowdown, or SM clocks stuck far below their
+    # maximum with no reason given (a clock lock left by someone), is measured once more; the
+    # second run's numbers are reported, with the first run's clocks beside them.
+    first_clocks = None
+    if clocks_rejected(clock_info):
+        first_clocks = clock_info
+        wall_s, clock_info = timed_region()
+        clock_info = dict(clock_info or {}, remeasured_after=first_clocks)
 
     durs = [events[i].elapsed_time(events[i + 1]) for i in range(len(events) - 1)]
     total_ms = events[0].elapsed_time(events[-1])

@@ -85,3 +85,15 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     with redirect_stdout(buf):
         assert bench.run_reference(None) == 0
     assert buf.getvalue() == ""
+
+
+def test_clock_records_that_force_a_second_measurement():
+    bench = load_bench()
+    ok = {"sm_mhz": 1400.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 20}
+    assert not bench.clocks_rejected(ok)                     # the power cap alone is kept
+    assert not bench.clocks_rejected(None)                   # no nvidia-smi: nothing to judge
+    for reason in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.clocks_rejected(dict(ok, reasons=["sw_power_cap", reason]))
+    locked = {"sm_mhz": 900.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 20}
+    assert bench.clocks_rejected(locked)                     # stuck low with no reason
+    assert not bench.clocks_rejected(dict(locked, reasons=["sw_power_cap"]))
