@@ -41,6 +41,7 @@
 #include <atomic>
 #include <cstdio>
 #include <string>
+#include <type_traits>
 
 #include "../../include/gdn.h"
 #include "ptx.cuh"
@@ -263,7 +264,7 @@ __device__ __forceinline__ uint32_t tsw(int row, int col, int rows)
 // exact bfloat16 K or V, the three products keeping fp32 accuracy.
 constexpr int kRowA = 72;      // padded bf16 rows of A' staging (144 bytes)
 constexpr int kRowL = 68;      // padded fp32 rows of L and T (272 bytes)
-constexpr int kRowY = 33;      // fp32 rows of the doubling scratch
+constexpr int kRowY = 36;      // fp32 rows of the doubling scratch (144 bytes: 16-byte aligned)
 constexpr int kPrepThreads = 256;
 // K, Q, V: 128-byte-swizzled TMA tiles (two 64-column halves of 64 rows) at a 1024-byte-aligned
 // base, then the A' staging, L, T and the per-token vectors, then the load barrier.
@@ -276,42 +277,45 @@ static_assert(sizeof(__nv_bfloat16) * 2 * kC * kRowA >= sizeof(float) * 32 * kRo
 // One doubling stage of T = (I + L)^-1 for block size b (T holds the inverted b x b diagonal
 // blocks; their upper parts are zero): for each pair [A 0; C B] at rows / columns r0 = 2 p b, the
 // lower-left block of the inverse is -B^-1 (C A^-1).  The 32 rows (p, i) of each product take
-// 8 threads apiece, b / 8 columns per thread, full-length (zero-padded) dot products.
+// 8 threads apiece, each thread U = b / 8 consecutive columns (one vector load per operand row),
+// full-length (zero-padded) dot products.
 template <int b>
 __device__ __forceinline__ void invert_doubling_stage(const float* Ls, float* Ts, float* Yb, int tid)
 {
     constexpr int U = b / 8;
+    using Vec = typename std::conditional<U == 4, float4, typename std::conditional<U == 2, float2,
+                                                                                    float>::type>::type;
     const int row = tid >> 3, l8 = tid & 7;
     const int p = row / b, i = row % b, r0 = 2 * p * b;
+    const auto fma_vec = [](float c, const Vec& x, float (&acc)[U]) {
+        const float* xv = reinterpret_cast<const float*>(&x);
+#pragma unroll
+        for (int u = 0; u < U; ++u) acc[u] = fmaf(c, xv[u], acc[u]);
+    };
     float acc[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) acc[u] = 0.f;
     {   // Y = C A^-1
         const float* crow = Ls + (r0 + b + i) * kRowL + r0;
-        const float* acol = Ts + r0 * kRowL + r0 + l8;
+        const float* acol = Ts + r0 * kRowL + r0 + U * l8;
 #pragma unroll
-        for (int m = 0; m < b; ++m) {
-            const float c = crow[m];
-#pragma unroll
-            for (int u = 0; u < U; ++u) acc[u] = fmaf(c, acol[m * kRowL + 8 * u], acc[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) Yb[row * kRowY + l8 + 8 * u] = acc[u];
+        for (int m = 0; m < b; ++m)
+            fma_vec(crow[m], *reinterpret_cast<const Vec*>(acol + m * kRowL), acc);
+        *reinterpret_cast<Vec*>(Yb + row * kRowY + U * l8) = *reinterpret_cast<const Vec*>(acc);
     }
     __syncthreads();
 #pragma unroll
     for (int u = 0; u < U; ++u) acc[u] = 0.f;
     {   // lower-left block = -B^-1 Y
         const float* brow = Ts + (r0 + b + i) * kRowL + r0 + b;
-        const float* ycol = Yb + p * b * kRowY + l8;
+        const float* ycol = Yb + p * b * kRowY + U * l8;
 #pragma unroll
-        for (int m = 0; m < b; ++m) {
-            const float bb = brow[m];
+        for (int m = 0; m < b; ++m)
+            fma_vec(brow[m], *reinterpret_cast<const Vec*>(ycol + m * kRowY), acc);
 #pragma unroll
-            for (int u = 0; u < U; ++u) acc[u] = fmaf(bb, ycol[m * kRowY + 8 * u], acc[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) Ts[(r0 + b + i) * kRowL + r0 + l8 + 8 * u] = -acc[u];
+        for (int u = 0; u < U; ++u) acc[u] = -acc[u];
+        *reinterpret_cast<Vec*>(Ts + (r0 + b + i) * kRowL + r0 + U * l8) =
+            *reinterpret_cast<const Vec*>(acc);
     }
     __syncthreads();
 }
