@@ -111,6 +111,7 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
                                       uint32_t* __restrict__ status, int32_t* __restrict__ order,
                                       int4* __restrict__ seqinfo, uint32_t* __restrict__ counter)
 {
+    gf16::grid_dep_launch();   // the prepare kernel may set itself up meanwhile
     if (threadIdx.x == 0) {
         *status = 0u;    // this call's scan reports into it
         *counter = 0u;   // the scan's work-item counter
@@ -334,21 +335,30 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 {
     const int32_t ch = blockIdx.x;
     const int32_t j = blockIdx.y;
+    // This kernel may start while the kernel before it on the stream (the chunk list, or the
+    // previous pass's scan) still runs.  Until grid_dep_wait() it reads only the call's inputs
+    // (q, k, v, alpha, beta); the chunk list, the workspace and the counter wait for it.  Every
+    // CTA passes grid_dep_wait() before it exits.
+    gf16::grid_dep_launch();   // the scan may set itself up meanwhile
     // one sequence (single_T >= 0): chunk ch covers tokens 64 ch .. (no chunk list is built,
-    // and the first pass of a call clears its status word here); otherwise the chunk list says
+    // and the first pass of a call, always launched after everything before it, clears its
+    // status word here); otherwise the chunk list says
     int32_t t0, len;
     if (single_T >= 0) {
         t0 = ch * kC;
-        if (t0 >= single_T) return;
+        if (t0 >= single_T) {
+            gf16::grid_dep_wait();
+            return;
+        }
         len = min(kC, single_T - t0);
         if (ch == 0 && j == 0 && threadIdx.x == 0 && clear_status) *status = 0u;
     } else {
+        gf16::grid_dep_wait();
         if (ch >= *n_chunks) return;
         const int4 info = chunks[ch];
         t0 = info.y;
         len = info.z;
     }
-    if (ch == 0 && j == 0 && threadIdx.x == 0) *counter = 0u;   // the scan's work counter
     const int32_t jq = j / qgroup, jk = j / kgroup;   // query / key head of state head j
     const int64_t cj = static_cast<int64_t>(ch) * h_v + j;
     const int tid = threadIdx.x;
@@ -414,6 +424,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const bool ok = gf16::mbar_wait(bar, 0, nullptr, wait_ns);
         if (__syncthreads_or(!ok)) {   // the tiles never landed: report and stop
             if (tid == 0) atomicExch(status, 1u);
+            gf16::grid_dep_wait();
             return;
         }
     }
@@ -467,6 +478,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     __syncthreads();
 
+    // From here on the workspace is written: the kernel before this one must have finished
+    // with it (the previous pass's scan reads it and draws from the counter).
+    gf16::grid_dep_wait();
+    if (ch == 0 && j == 0 && tid == 0) *counter = 0u;   // the scan's work counter
     // A' pieces to global, 16-byte granules
     {
         __nv_bfloat16* apc = ap + cj * 2 * kC * kC;
@@ -726,6 +741,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     bool have_first = false;   // the current item's first chunk was loaded by the previous item
     const int32_t G = static_cast<int32_t>(gridDim.x);
     const bool draws = kMulti && n_items > G;
+    // This kernel may start while the prepare kernel before it still runs.  Until
+    // grid_dep_wait() it reads only the call's inputs (the first item's initial state); the
+    // chunk list's tables, the workspace and the counter wait for it.
+    gf16::grid_dep_launch();
+    if (single_T < 0) gf16::grid_dep_wait();   // order and seqinfo, for the first item
     Item it = decode(blockIdx.x);
     if (tid == 0 && it.c_begin < it.c_end) {   // (this CTA loads chunks: the maps are real)
         gf16::prefetch_tensormap(&map_w);
@@ -734,8 +754,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         gf16::prefetch_tensormap(&map_k);
     }
     for (int32_t q = blockIdx.x; q < n_items;) {
-        uint32_t drawn = 0;   // (thread 0) the draw for the next item
-        if (tid == 0 && draws) drawn = atomicAdd(counter, 1u);
         int32_t qn = n_items;   // the next item, known from the first chunk's middle barrier
         Item nx{};
         const int32_t j = it.j, r0 = it.r0, jq = j / qgroup, jk = j / kgroup;
@@ -750,6 +768,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             st[e] = s0 ? s0[sbase + r * kD + c] : 0.f;
         }
         store_state();
+        if (q == static_cast<int32_t>(blockIdx.x)) gf16::grid_dep_wait();
+        uint32_t drawn = 0;   // (thread 0) the draw for the next item
+        if (tid == 0 && draws) drawn = atomicAdd(counter, 1u);
         __syncthreads();   // barriers initialised, state pieces visible
         if (kMulti && c_begin >= c_end) {   // an empty sequence: only its state passes through
             if (tid == 0) *next_item = draws ? G + static_cast<int32_t>(drawn) : n_items;
@@ -1024,6 +1045,28 @@ int gdn_make_map(CUtensorMap* map, const void* ptr, uint32_t rank, const cuuint6
     return GDN_OK;
 }
 
+// Launches `kernel` on `stream`.  The first kernel of a call (first == true, which this clears)
+// is ordered after all earlier work as usual; a later one is launched with programmatic stream
+// serialization, so it may start as soon as every CTA of its predecessor has called
+// grid_dep_launch(); it then waits in grid_dep_wait() for the predecessor to finish.
+template <typename... KArgs, typename... Args>
+cudaError_t gdn_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, bool& first, Args... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = first ? 0u : 1u;
+    first = false;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1146,36 +1189,46 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
             return rc;
     }
 
+    // The call's first kernel starts after all earlier work on the stream; each later one may
+    // start while the one before it finishes (programmatic dependent launch: the kernels wait
+    // for their predecessor before they touch what it writes).
+    bool first = true;
     if (single_T < 0) {
-        gdn_chunk_list_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, static_cast<int32_t>(n_seqs),
-                                                      chunk_offset, chunks,
-                                                      static_cast<int32_t>(mc), n_chunks, status,
-                                                      order, seqinfo, counter);
-        if ((e = cudaGetLastError()) != cudaSuccess)
+        e = gdn_launch(gdn_chunk_list_kernel, dim3(1), dim3(1024), 0, stream, first, cu_seqlens,
+                       static_cast<int32_t>(n_seqs), chunk_offset, chunks,
+                       static_cast<int32_t>(mc), n_chunks, status, order, seqinfo, counter);
+        if (e != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_chunk_list_kernel: %s", cudaGetErrorString(e));
     }
-    // with no tokens every state only passes through: one pass
+    // with no tokens every state only passes through: one pass.  Every pass reads the initial
+    // states and the last one writes the final states, so the two may be one buffer.
     for (int64_t gp = 0; gp < map_passes; ++gp) {
         if (mc > 0 && total_tokens > 0) {
             const dim3 pgrid(static_cast<uint32_t>(mc), static_cast<uint32_t>(h_v));
-            gdn_prepare_kernel<<<pgrid, kPrepThreads, kPrepSmem, stream>>>(
-                map_q[gp], map_k, map_v, alpha, beta, chunks, n_chunks, static_cast<int32_t>(h_v),
-                qgroup, kgroup, gp == 0, wp, ap, ut, gm, single_T, status, counter,
-                g_gdn_wait_ns.load());
-            if ((e = cudaGetLastError()) != cudaSuccess)
+            e = gdn_launch(gdn_prepare_kernel, pgrid, dim3(kPrepThreads), kPrepSmem, stream,
+                           first, map_q[gp], map_k, map_v, alpha, beta,
+                           static_cast<const int4*>(chunks), static_cast<const int32_t*>(n_chunks),
+                           static_cast<int32_t>(h_v), qgroup, kgroup,
+                           static_cast<int32_t>(gp == 0), wp, ap, ut, gm, single_T, status,
+                           counter, g_gdn_wait_ns.load());
+            if (e != cudaSuccess)
                 return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
         }
         // persistent scan: one CTA per SM (at most one per work item) taking items dynamically
         const int64_t ctas = n_items < sms ? n_items : sms;
         auto* scan = n_items > sms ? gdn_scan_kernel<true> : gdn_scan_kernel<false>;
-        scan<<<static_cast<uint32_t>(ctas), kScanThreads, kScanSmem, stream>>>(
-            map_w, map_a, map_q[gp], map_k, single_T >= 0 ? nullptr : order,
-            single_T >= 0 ? nullptr : seqinfo, counter, static_cast<int32_t>(n_items), ut, gm,
-            initial_state, gp == 0 ? final_state : nullptr,
-            static_cast<__nv_bfloat16*>(o) + gp * kD, status, static_cast<int32_t>(h_v), qgroup,
-            kgroup, static_cast<int32_t>(h_o), static_cast<int32_t>(passes), scale,
-            g_gdn_wait_ns.load(), g_gdn_fault.load(), single_T);
-        if ((e = cudaGetLastError()) != cudaSuccess)
+        e = gdn_launch(scan, dim3(static_cast<uint32_t>(ctas)), dim3(kScanThreads), kScanSmem,
+                       stream, first, map_w, map_a, map_q[gp], map_k,
+                       static_cast<const int32_t*>(single_T >= 0 ? nullptr : order),
+                       static_cast<const int4*>(single_T >= 0 ? nullptr : seqinfo), counter,
+                       static_cast<int32_t>(n_items), static_cast<const float*>(ut),
+                       static_cast<const float*>(gm), initial_state,
+                       gp == map_passes - 1 ? final_state : nullptr,
+                       static_cast<__nv_bfloat16*>(o) + gp * kD, status,
+                       static_cast<int32_t>(h_v), qgroup, kgroup, static_cast<int32_t>(h_o),
+                       static_cast<int32_t>(passes), scale, g_gdn_wait_ns.load(),
+                       g_gdn_fault.load(), single_T);
+        if (e != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_scan_kernel: %s", cudaGetErrorString(e));
     }
     return GDN_OK;

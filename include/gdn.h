@@ -40,15 +40,18 @@
  *                                     cu_seqlens[n_seqs] = total_tokens
  *   initial_state  float    [n_seqs][h_v][head_dim (dv)][head_dim (dk)], or NULL for zeros
  *   o              bfloat16 [total_tokens][h_o][head_dim]   (written; h_o as above)
- *   final_state    float    [n_seqs][h_v][dv][dk], or NULL   (written)
+ *   final_state    float    [n_seqs][h_v][dv][dk], or NULL   (written; may be the
+ *                                     initial_state buffer itself, updated in place)
  *   workspace      gdn_prefill_workspace_bytes() bytes, 16-byte aligned
  *
  * The chunked form divides running products of alpha within a chunk, so every alpha must be
  * positive and the product of 64 consecutive alphas of a sequence must stay a normal fp32 number
  * (above 1e-37); alpha = 0, a full reset, is outside this routine's domain.
  *
- * Ownership: the caller owns every buffer; nothing is retained after a call.  Asynchronous on
- * `stream`.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, heads in none of the
+ * Ownership: the caller owns every buffer; nothing is retained after a call.  Apart from the
+ * state pair above, no written buffer may overlap another buffer of the call.  Asynchronous on
+ * `stream`: the call's first kernel starts after all earlier work on the stream, and its later
+ * kernels use programmatic dependent launch among themselves.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, heads in none of the
  * layouts above, workspace too small), GDN_ERR_UNSUPPORTED (head_dim other than 128, misaligned
  * q/k/v/o, more than 8 query heads per state head, more than 2^31 / 192 chunks x value heads),
  * GDN_ERR_CUDA (a launch failed;

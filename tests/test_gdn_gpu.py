@@ -61,7 +61,7 @@ def run(inp, h_qk, h_v, scale=0.73, want_state=True):
     return o.float().cpu().double().numpy(), (None if sf is None else sf.cpu().double().numpy())
 
 
-def assert_parity(inp, o, sf, scale, where):
+def assert_parity(inp, o, sf, scale, where, extra_chunks=0):
     ref_o, ref_s = oracle.gdn_f64(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"],
                                   inp["cu_seqlens"], scale, inp["initial_state"])
     cu = inp["cu_seqlens"].numpy()
@@ -69,7 +69,7 @@ def assert_parity(inp, o, sf, scale, where):
     dk = inp["q"].shape[2]
     for i in range(len(cu) - 1):
         sl = slice(cu[i], cu[i + 1])
-        n = max(1, -(-(cu[i + 1] - cu[i]) // C))
+        n = max(1, -(-(cu[i + 1] - cu[i]) // C)) + extra_chunks
         ro = ref_o[sl]
         if ro.size == 0:
             continue
@@ -264,3 +264,54 @@ def test_rejects_bad_head_layouts():
     assert call(2, 2, 3) == g.GDN_ERR_INVALID_ARG     # h_v not a multiple of h_k
     assert call(18, 1, 2) == g.GDN_ERR_UNSUPPORTED    # 9 query heads per state
     torch.cuda.synchronize()
+
+
+CARRY_CASES = [
+    # (T, n_seqs, h_q, h_k, h_v)
+    (300, 1, 2, 2, 2),      # one sequence, multi-head
+    (500, 3, 4, 1, 2),      # packed, grouped queries over grouped values: two passes a call
+    (700, 30, 2, 2, 4),     # grouped values, more work items than SMs
+]
+
+
+@pytest.mark.parametrize("case", CARRY_CASES, ids=lambda s: "-".join(map(str, s)))
+def test_state_carried_in_place_across_calls(case):
+    """Every sequence cut in two and run as two calls on one stream, one workspace and one state
+    buffer that is both calls' initial and final state (updated in place), with no host
+    synchronisation between the calls: the second call must see the first call's states, and
+    the first call's workspace must be free before the second call writes it.  Compared with
+    the oracle over the uncut sequences."""
+    T, n, h_q, h_k, h_v = case
+    inp = _grouped_query_inputs(T, n, h_q, h_k, h_v, seed=900 + T + n)
+    cu = inp["cu_seqlens"].tolist()
+    parts = ([], [])
+    lens = ([], [])
+    for i in range(n):
+        mid = cu[i] + (cu[i + 1] - cu[i]) // 2
+        for p, (a, b) in enumerate(((cu[i], mid), (mid, cu[i + 1]))):
+            parts[p].append(torch.arange(a, b))
+            lens[p].append(b - a)
+    h_o = g.gdn_out_heads(h_q, h_k, h_v)
+    o = torch.full((T, h_o, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    state = inp["initial_state"].cuda().clone()
+    need = g.gdn_prefill_workspace_bytes(T, n, h_v)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    keep = []
+    for p in range(2):
+        idx = torch.cat(parts[p])
+        Tp = int(idx.numel())
+        cup = torch.tensor([0] + list(np.cumsum(lens[p])), dtype=torch.int32).cuda()
+        d = {key: inp[key][idx].contiguous().cuda() for key in ("q", "k", "v", "alpha", "beta")}
+        op = torch.empty((Tp, h_o, 128), dtype=torch.bfloat16, device="cuda")
+        rc = g.gdn_prefill_heads(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
+                                 d["alpha"].data_ptr(), d["beta"].data_ptr(), cup.data_ptr(), n,
+                                 Tp, h_q, h_k, h_v, 128, 0.73, state.data_ptr(), op.data_ptr(),
+                                 state.data_ptr(), ws.data_ptr(), need, stream)
+        assert rc == g.GDN_OK, g.gdn_last_error()
+        keep.append((d, cup, op, idx))
+    torch.cuda.synchronize()
+    for d, cup, op, idx in keep:
+        o[idx.cuda()] = op
+    assert_parity(inp, o.float().cpu().double().numpy(), state.cpu().double().numpy(), 0.73,
+                  f"carried state {case}", extra_chunks=1)
