@@ -255,6 +255,22 @@ __device__ __forceinline__ uint32_t tsw(int row, int col, int rows)
                                  ((((col >> 3) & 7) ^ (row & 7)) << 4) + (col & 7) * 2);
 }
 
+// Byte offset of element (row, col) in a 64-column fp32 tile that TMA reads or writes as two
+// 32-column halves of 128 rows of 128 bytes each, 128-byte swizzle.
+__device__ __forceinline__ uint32_t tsw32(int row, int col)
+{
+    return static_cast<uint32_t>((col >> 5) * 128 * 128 + row * 128 +
+                                 ((((col >> 2) & 7) ^ (row & 7)) << 4) + (col & 3) * 4);
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // ---- per (chunk, value head): W, U'^T, A' and the cumulative decays ----------------------------
 // K, Q, V of the chunk arrive by TMA as 128-byte-swizzled bf16 tiles.  Products K K^T and Q K^T
 // run on the tensor cores (bf16 operands, exact products).  T = (I + L)^-1 is then built in the
@@ -274,6 +290,10 @@ constexpr size_t kPrepSmem = 3 * kPrepTile + sizeof(__nv_bfloat16) * 2 * kC * kR
                              sizeof(float) * (2 * kC * kRowL + 4 * kC) + 16 + 1024;
 static_assert(sizeof(__nv_bfloat16) * 2 * kC * kRowA >= sizeof(float) * 32 * kRowY,
               "the doubling scratch reuses the A' staging");
+static_assert(3 * kPrepTile == 3 * kC * kD * 2, "W's three pieces are staged over K, Q and V");
+static_assert(sizeof(float) * kD * kC <=
+                  sizeof(__nv_bfloat16) * 2 * kC * kRowA + sizeof(float) * kC * kRowL,
+              "U'^T is staged over the A' staging and L, before T");
 
 // One doubling stage of T = (I + L)^-1 for block size b (T holds the inverted b x b diagonal
 // blocks; their upper parts are zero): for each pair [A 0; C B] at rows / columns r0 = 2 p b, the
@@ -324,12 +344,13 @@ __device__ __forceinline__ void invert_doubling_stage(const float* Ls, float* Ts
 __global__ void __launch_bounds__(kPrepThreads, 2)
     gdn_prepare_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
-                       const __grid_constant__ CUtensorMap map_v, const float* __restrict__ alpha,
+                       const __grid_constant__ CUtensorMap map_v,
+                       const __grid_constant__ CUtensorMap map_w,
+                       const __grid_constant__ CUtensorMap map_ut, const float* __restrict__ alpha,
                        const float* __restrict__ beta, const int4* __restrict__ chunks,
                        const int32_t* __restrict__ n_chunks, int32_t h_v, int32_t qgroup,
-                       int32_t kgroup, int32_t clear_status,
-                       __nv_bfloat16* __restrict__ wp, __nv_bfloat16* __restrict__ ap,
-                       float* __restrict__ ut, float* __restrict__ gam_out, int32_t single_T,
+                       int32_t kgroup, int32_t clear_status, __nv_bfloat16* __restrict__ ap,
+                       float* __restrict__ gam_out, int32_t single_T,
                        uint32_t* __restrict__ status, uint32_t* __restrict__ counter,
                        uint64_t wait_ns)
 {
@@ -374,6 +395,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smraw + (base - raw);
     const uint32_t kb_s = base, qb_s = base + kPrepTile, vb_s = base + 2 * kPrepTile;
+    const uint32_t ut_s = base + 3 * kPrepTile;   // U'^T staging at the end (A' staging and L)
     __nv_bfloat16* Ap = reinterpret_cast<__nv_bfloat16*>(gbase + 3 * kPrepTile);   // [2][64][72]
     float* Yb = reinterpret_cast<float*>(Ap);                         // [32][33], after A' is out
     float* Ls = reinterpret_cast<float*>(Ap + 2 * kC * kRowA);       // [64][68] L, strictly lower
@@ -549,37 +571,53 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                 }
             }
         }
+        // Both results leave through shared memory and TMA stores: W as three bfloat16 pieces
+        // [piece][t][c] over the K / Q / V tiles (two 64-column halves of 192 rows, 128-byte
+        // swizzle), U'^T as fp32 [v][t] over the A' staging and L (two 32-token halves of 128
+        // rows, 128-byte swizzle).  Each warp's 4-byte stores land in 32 distinct banks.
         const int t = 16 * mt + gq;
+        __syncthreads();   // every warp is done reading K, V and T
         if (!half) {
-            // W in three bfloat16 pieces, rows t, columns c
-            __nv_bfloat16* w = wp + cj * 3 * kC * kD;
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
                 const int c = 8 * n + 2 * tg;
                 const Pieces3 lo = split3(acc[n][0], acc[n][1]), hi = split3(acc[n][2], acc[n][3]);
 #pragma unroll
                 for (int pc = 0; pc < 3; ++pc) {
-                    *reinterpret_cast<uint32_t*>(w + (pc * kC + t) * kD + c) = lo.p[pc];
-                    *reinterpret_cast<uint32_t*>(w + (pc * kC + t + 8) * kD + c) = hi.p[pc];
+                    st_shared_u32(kb_s + tsw(pc * kC + t, c, 3 * kC), lo.p[pc]);
+                    st_shared_u32(kb_s + tsw(pc * kC + t + 8, c, 3 * kC), hi.p[pc]);
                 }
             }
         } else {
-            // U'^T, rows v, columns t
-            float* u = ut + cj * kD * kC;
 #pragma unroll
             for (int n = 0; n < 16; ++n) {
                 const int v0 = 8 * n + 2 * tg;
-                u[v0 * kC + t] = acc[n][0];
-                u[(v0 + 1) * kC + t] = acc[n][1];
-                u[v0 * kC + t + 8] = acc[n][2];
-                u[(v0 + 1) * kC + t + 8] = acc[n][3];
+                st_shared_f32(ut_s + tsw32(v0, t), acc[n][0]);
+                st_shared_f32(ut_s + tsw32(v0 + 1, t), acc[n][1]);
+                st_shared_f32(ut_s + tsw32(v0, t + 8), acc[n][2]);
+                st_shared_f32(ut_s + tsw32(v0 + 1, t + 8), acc[n][3]);
             }
+        }
+        gf16::fence_proxy_async_smem();   // visible to the tensor-memory-access unit
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                gf16::tma_store_2d(&map_w, kb_s + h * 3 * kC * 128, 64 * h,
+                                   static_cast<int32_t>(cj * 3 * kC));
+                gf16::tma_store_2d(&map_ut, ut_s + h * kD * 128, 32 * h,
+                                   static_cast<int32_t>(cj * kD));
+            }
+            gf16::bulk_commit_group();
         }
     }
     if (tid < kC) {
         gam_out[cj * 2 * kC + tid] = g[tid];
         gam_out[cj * 2 * kC + kC + tid] = g[kC - 1] / g[tid];
     }
+    // The CTA's shared memory must outlive the stores' reads of it; their writes are complete
+    // when the grid is (the next kernel reads them after grid_dep_wait()).
+    if (tid == 0) gf16::bulk_wait_group_read<0>();
 }
 
 // ---- per (sequence, value head, block of 16 value rows): the state scan over the chunks -------
@@ -1027,15 +1065,18 @@ PFN_cuTensorMapEncodeTiled_v12000 gdn_encode_fn()
     return fn;
 }
 
-// A bfloat16 tensor of `rank` dimensions (dims[0] contiguous; strides in bytes of dims 1..),
-// read in boxes of `box` elements with the 128-byte swizzle (box[0] = 64 elements = 128 bytes).
+// A tensor of `rank` dimensions (dims[0] contiguous; strides in bytes of dims 1..), moved in
+// boxes of `box` elements with the 128-byte swizzle (box[0] elements = 128 bytes): bfloat16, or
+// fp32 when `f32`.
 int gdn_make_map(CUtensorMap* map, const void* ptr, uint32_t rank, const cuuint64_t* dims,
-                 const cuuint64_t* strides, const cuuint32_t* box, const char* what)
+                 const cuuint64_t* strides, const cuuint32_t* box, const char* what,
+                 bool f32 = false)
 {
     auto fn = gdn_encode_fn();
     if (!fn) return gdn_fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims,
+    const CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          rank, const_cast<void*>(ptr), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1147,15 +1188,19 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
 
-    // TMA descriptors that do not depend on the pass: W pieces [cj * 192 rows][128], A' pieces
+    // TMA descriptors that do not depend on the pass: W pieces [cj * 192 rows][128] (stored by
+    // the prepare kernel, loaded by the scan), U'^T [cj * 128 rows][64] fp32 (stored), A' pieces
     // [cj * 128 rows][64], k as {128, h_k, total_tokens}, v as {128, h_v, total_tokens}.  With no
-    // tokens nothing is loaded and they stay zero.
-    CUtensorMap map_w{}, map_a{}, map_k{}, map_v{};
+    // tokens nothing is moved and they stay zero.
+    CUtensorMap map_w{}, map_ut{}, map_a{}, map_k{}, map_v{};
     const cuuint32_t bq[3] = {64, 1, kC};
     if (total_tokens > 0) {
         const cuuint64_t dw[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(mc * h_v * 3 * kC)};
         const cuuint64_t sw[1] = {kD * 2};
         const cuuint32_t bw[2] = {64, 3 * kC};
+        const cuuint64_t du[2] = {static_cast<cuuint64_t>(kC), static_cast<cuuint64_t>(mc * h_v * kD)};
+        const cuuint64_t su[1] = {kC * 4};
+        const cuuint32_t bu[2] = {32, kD};
         const cuuint64_t da[2] = {static_cast<cuuint64_t>(kC), static_cast<cuuint64_t>(mc * h_v * 2 * kC)};
         const cuuint64_t sa[1] = {kC * 2};
         const cuuint32_t ba[2] = {64, 2 * kC};
@@ -1166,6 +1211,7 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
                                    static_cast<cuuint64_t>(total_tokens)};
         const cuuint64_t sv3[2] = {kD * 2, static_cast<cuuint64_t>(h_v) * kD * 2};
         if ((rc = gdn_make_map(&map_w, wp, 2, dw, sw, bw, "W pieces")) != GDN_OK ||
+            (rc = gdn_make_map(&map_ut, ut, 2, du, su, bu, "U'^T", true)) != GDN_OK ||
             (rc = gdn_make_map(&map_a, ap, 2, da, sa, ba, "A' pieces")) != GDN_OK ||
             (rc = gdn_make_map(&map_k, k, 3, dk3, sk3, bq, "k")) != GDN_OK ||
             (rc = gdn_make_map(&map_v, v, 3, dv3, sv3, bq, "v")) != GDN_OK)
@@ -1206,11 +1252,11 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
         if (mc > 0 && total_tokens > 0) {
             const dim3 pgrid(static_cast<uint32_t>(mc), static_cast<uint32_t>(h_v));
             e = gdn_launch(gdn_prepare_kernel, pgrid, dim3(kPrepThreads), kPrepSmem, stream,
-                           first, map_q[gp], map_k, map_v, alpha, beta,
+                           first, map_q[gp], map_k, map_v, map_w, map_ut, alpha, beta,
                            static_cast<const int4*>(chunks), static_cast<const int32_t*>(n_chunks),
                            static_cast<int32_t>(h_v), qgroup, kgroup,
-                           static_cast<int32_t>(gp == 0), wp, ap, ut, gm, single_T, status,
-                           counter, g_gdn_wait_ns.load());
+                           static_cast<int32_t>(gp == 0), ap, gm, single_T, status, counter,
+                           g_gdn_wait_ns.load());
             if (e != cudaSuccess)
                 return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
         }
