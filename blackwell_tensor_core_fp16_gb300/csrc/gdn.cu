@@ -104,6 +104,20 @@ WsLayout layout_for(int64_t T, int64_t n, int64_t h_v)
     return l;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization may
+// start while the kernel before it on the stream still runs; grid_dep_wait() returns once that
+// kernel has completed and its memory writes are visible (at once when the launch had no such
+// dependency).  grid_dep_launch() lets the next kernel of the stream start early; it launches
+// once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- chunk list: per sequence, ceil(len / 64) chunks, numbered in sequence order -------------
 __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_seqs,
                                       int32_t* __restrict__ chunk_offset, int4* __restrict__ chunks,
@@ -111,7 +125,7 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
                                       uint32_t* __restrict__ status, int32_t* __restrict__ order,
                                       int4* __restrict__ seqinfo, uint32_t* __restrict__ counter)
 {
-    gf16::grid_dep_launch();   // the prepare kernel may set itself up meanwhile
+    grid_dep_launch();   // the prepare kernel may set itself up meanwhile
     if (threadIdx.x == 0) {
         *status = 0u;    // this call's scan reports into it
         *counter = 0u;   // the scan's work-item counter
@@ -360,7 +374,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     // previous pass's scan) still runs.  Until grid_dep_wait() it reads only the call's inputs
     // (q, k, v, alpha, beta); the chunk list, the workspace and the counter wait for it.  Every
     // CTA passes grid_dep_wait() before it exits.
-    gf16::grid_dep_launch();   // the scan may set itself up meanwhile
+    grid_dep_launch();   // the scan may set itself up meanwhile
     // one sequence (single_T >= 0): chunk ch covers tokens 64 ch .. (no chunk list is built,
     // and the first pass of a call, always launched after everything before it, clears its
     // status word here); otherwise the chunk list says
@@ -368,13 +382,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     if (single_T >= 0) {
         t0 = ch * kC;
         if (t0 >= single_T) {
-            gf16::grid_dep_wait();
+            grid_dep_wait();
             return;
         }
         len = min(kC, single_T - t0);
         if (ch == 0 && j == 0 && threadIdx.x == 0 && clear_status) *status = 0u;
     } else {
-        gf16::grid_dep_wait();
+        grid_dep_wait();
         if (ch >= *n_chunks) return;
         const int4 info = chunks[ch];
         t0 = info.y;
@@ -446,7 +460,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const bool ok = gf16::mbar_wait(bar, 0, nullptr, wait_ns);
         if (__syncthreads_or(!ok)) {   // the tiles never landed: report and stop
             if (tid == 0) atomicExch(status, 1u);
-            gf16::grid_dep_wait();
+            grid_dep_wait();
             return;
         }
     }
@@ -502,7 +516,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
     // From here on the workspace is written: the kernel before this one must have finished
     // with it (the previous pass's scan reads it and draws from the counter).
-    gf16::grid_dep_wait();
+    grid_dep_wait();
     if (ch == 0 && j == 0 && tid == 0) *counter = 0u;   // the scan's work counter
     // A' pieces to global, 16-byte granules
     {
@@ -782,8 +796,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     // This kernel may start while the prepare kernel before it still runs.  Until
     // grid_dep_wait() it reads only the call's inputs (the first item's initial state); the
     // chunk list's tables, the workspace and the counter wait for it.
-    gf16::grid_dep_launch();
-    if (single_T < 0) gf16::grid_dep_wait();   // order and seqinfo, for the first item
+    grid_dep_launch();
+    if (single_T < 0) grid_dep_wait();   // order and seqinfo, for the first item
     Item it = decode(blockIdx.x);
     if (tid == 0 && it.c_begin < it.c_end) {   // (this CTA loads chunks: the maps are real)
         gf16::prefetch_tensormap(&map_w);
@@ -806,7 +820,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             st[e] = s0 ? s0[sbase + r * kD + c] : 0.f;
         }
         store_state();
-        if (q == static_cast<int32_t>(blockIdx.x)) gf16::grid_dep_wait();
+        if (q == static_cast<int32_t>(blockIdx.x)) grid_dep_wait();
         uint32_t drawn = 0;   // (thread 0) the draw for the next item
         if (tid == 0 && draws) drawn = atomicAdd(counter, 1u);
         __syncthreads();   // barriers initialised, state pieces visible

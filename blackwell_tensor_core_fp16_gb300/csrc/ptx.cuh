@@ -64,21 +64,6 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Programmatic dependent launch.  A kernel launched with programmatic stream serialization may
-// start while the kernel before it on the stream still runs; grid_dep_wait() returns once that
-// kernel has completed and its memory writes are visible (at once when the launch had no such
-// dependency).  grid_dep_launch() lets the next kernel of the stream start early; it launches
-// once every CTA of this grid has called it or exited.
-__device__ __forceinline__ void grid_dep_wait()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ void grid_dep_launch()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // True in exactly one lane of the (converged) warp: the lowest active lane.
 __device__ __forceinline__ bool elect_one_sync()
 {
