@@ -69,7 +69,10 @@ def parse_args():
                    help="steps of the block-scaled FP8 leg (8192^3 and MLP shapes; 0: skip)")
     p.add_argument("--mx-variant", type=int, default=0, help="block-scaled variant (0 = auto)")
     p.add_argument("--gdn-reps", type=int, default=20,
-                   help="timed calls per Gated Delta Net scenario (0: skip the leg)")
+                   help="fewest timed calls per Gated Delta Net scenario (0: skip the leg)")
+    p.add_argument("--gdn-min-ms", type=float, default=5.0,
+                   help="time at least this many milliseconds of calls per Gated Delta Net "
+                        "scenario (0: exactly --gdn-reps calls)")
     p.add_argument("--sweep-mx", action="store_true",
                    help="in --sweep, time the block-scaled FP8 workloads instead")
     p.add_argument("--cublas-steps", type=int, default=-1,
@@ -424,7 +427,8 @@ GDN_PAGE_H20_MS = {
 
 def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
     """Every scenario of the page: inputs resident, the workspace allocated once, CUDA events
-    around `gdn_reps` back-to-back calls after about 10 ms of warm-up calls."""
+    around back-to-back calls (at least `gdn_reps` of them and `gdn_min_ms` of time) after about
+    50 ms of warm-up calls."""
     import torch
     from blackwell_tensor_core_fp16_gb300.workloads import GDN_ORDER, GDN_WORKLOADS, \
         gdn_workload_inputs
@@ -451,25 +455,28 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
             if rc != g.GDN_OK:
                 raise g.GemmError(rc, g.gdn_last_error())
 
-        # warm up for about 10 ms of calls (at least 3): the leg follows the power-capped GEMM
-        # legs, and a few calls of a 35 us scenario would be timed before the clocks settle
+        # warm up for about 50 ms of calls (at least 3): the leg follows the power-capped GEMM
+        # legs, and the SM clock takes tens of milliseconds to climb back once they stop; then
+        # time at least `gdn_reps` calls and at least about 5 ms of them
         t_w = time.perf_counter()
         n_w = 0
-        while n_w < 3 or time.perf_counter() - t_w < 0.01:
+        while n_w < 3 or time.perf_counter() - t_w < 0.05:
             with torch.cuda.stream(stream):
                 for _ in range(8):
                     call()
             torch.cuda.synchronize()
             n_w += 8
+        per_call_s = (time.perf_counter() - t_w) / n_w
+        reps = max(args.gdn_reps, int(math.ceil(args.gdn_min_ms * 1e-3 / per_call_s)))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record(stream)
-            for _ in range(args.gdn_reps):
+            for _ in range(reps):
                 call()
             e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / args.gdn_reps
-        out[name] = {"ms": ms, "tokens_per_s": w.T / (ms * 1e-3),
+        ms = e0.elapsed_time(e1) / max(reps, 1)
+        out[name] = {"ms": ms, "reps": reps, "tokens_per_s": w.T / (ms * 1e-3),
                      "recurrence_tflops": w.flops / (ms * 1e-3) / 1e12,
                      "hbm_gbs_algorithmic": w.min_bytes / (ms * 1e-3) / 1e9,
                      "page_h20_ms_context": GDN_PAGE_H20_MS.get(name)}
@@ -484,7 +491,8 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
                         "the measured dense bf16 peak; the call is latency-bound by the chunk "
                         "chain (about 2.2 us per 64-token step of a sequence)"}
     return {"metric": "Gated Delta Net prefill: ms per call (bf16 q/k/v, head dim 128)",
-            "unit": "ms", "higher_is_better": False, "reps": args.gdn_reps,
+            "unit": "ms", "higher_is_better": False, "min_reps": args.gdn_reps,
+            "min_timed_ms": args.gdn_min_ms,
             "scenarios": out,
             "roofline": roofline,
             "gpu_launches_per_call": 3,
