@@ -40,6 +40,7 @@
 #include <cstdint>
 #include <atomic>
 #include <cstdio>
+#include <mutex>
 #include <string>
 #include <type_traits>
 
@@ -51,6 +52,7 @@ namespace {
 constexpr int kC = 64;          // tokens per chunk
 constexpr int kD = 128;         // head dimension (dk = dv)
 constexpr int kRows = 16;       // value rows of the state per scan CTA
+constexpr int kMaxDevices = 64;  // device ordinals the per-device set-up covers
 
 thread_local std::string t_gdn_error;
 std::atomic<uint64_t> g_gdn_wait_ns{2000000000ull};   // limit of one wait for a chunk's loads
@@ -1100,6 +1102,33 @@ int gdn_make_map(CUtensorMap* map, const void* ptr, uint32_t rank, const cuuint6
     return GDN_OK;
 }
 
+// The kernels' dynamic shared memory above the 48 KB default is an attribute of each device's
+// copy of the kernel: set once per device, under a lock (calls may come from several threads).
+int gdn_ensure_smem(int dev)
+{
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    if (dev < 0 || dev >= kMaxDevices)
+        return gdn_fail(GDN_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices - 1);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return GDN_OK;
+    cudaError_t e = cudaFuncSetAttribute(gdn_prepare_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kPrepSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gdn_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kScanSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gdn_scan_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kScanSmem));
+    if (e != cudaSuccess)
+        return gdn_fail(GDN_ERR_CUDA, "cudaFuncSetAttribute (dynamic shared memory): %s",
+                        cudaGetErrorString(e));
+    done[dev] = true;
+    return GDN_OK;
+}
+
 // Launches `kernel` on `stream`.  The first kernel of a call (first == true, which this clears)
 // is ordered after all earlier work as usual; a later one is launched with programmatic stream
 // serialization, so it may start as soon as every CTA of its predecessor has called
@@ -1174,23 +1203,13 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
     // head j and its query head j / kgroup (one pass).  With grouped queries (h_q a multiple of
     // h_v) it serves query heads j r + g, g < r = h_q / h_v, written to output heads j r + g:
     // pass g runs the whole pipeline on the strided view of q that holds heads j r + g (the state
-    // recurrence does not read q, so every pass reproduces the same states; only pass 0 writes
-    // the final states).
+    // recurrence does not read q, so every pass reproduces the same states; only the last pass
+    // writes the final states).
     const int64_t h_o = out_heads(h_q, h_k, h_v);
     const int64_t passes = h_o == h_v ? 1 : h_q / h_v;
     const int32_t kgroup = static_cast<int32_t>(h_v / h_k);
     const int32_t qgroup = passes == 1 ? kgroup : 1;
 
-    static bool attrs = false;
-    if (!attrs) {
-        cudaFuncSetAttribute(gdn_prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPrepSmem));
-        cudaFuncSetAttribute(gdn_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kScanSmem));
-        cudaFuncSetAttribute(gdn_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kScanSmem));
-        attrs = true;
-    }
     // One sequence with tokens: cu_seqlens is [0, total_tokens] by contract, so the kernels
     // number the chunks themselves and the chunk-list launch is skipped.
     const int32_t single_T = (n_seqs == 1 && total_tokens > 0) ? static_cast<int32_t>(total_tokens)
@@ -1201,6 +1220,7 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+    if ((rc = gdn_ensure_smem(dev)) != GDN_OK) return rc;
 
     // TMA descriptors that do not depend on the pass: W pieces [cj * 192 rows][128] (stored by
     // the prepare kernel, loaded by the scan), U'^T [cj * 128 rows][64] fp32 (stored), A' pieces
