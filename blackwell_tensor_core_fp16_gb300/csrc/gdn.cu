@@ -1102,8 +1102,9 @@ int gdn_make_map(CUtensorMap* map, const void* ptr, uint32_t rank, const cuuint6
     return GDN_OK;
 }
 
-// The kernels' dynamic shared memory above the 48 KB default is an attribute of each device's
-// copy of the kernel: set once per device, under a lock (calls may come from several threads).
+// Once per device, under a lock (calls may come from several threads): the device must be an
+// sm_103 part, and the kernels' dynamic shared memory above the 48 KB default is raised (an
+// attribute of each device's copy of the kernel).
 int gdn_ensure_smem(int dev)
 {
     static std::mutex mu;
@@ -1112,6 +1113,13 @@ int gdn_ensure_smem(int dev)
         return gdn_fail(GDN_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices - 1);
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return GDN_OK;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return gdn_fail(GDN_ERR_UNSUPPORTED,
+                        "device %d is sm_%d%d; these kernels are built for sm_103a only", dev,
+                        major, minor);
     cudaError_t e = cudaFuncSetAttribute(gdn_prepare_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kPrepSmem));
