@@ -520,19 +520,38 @@ def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_sta
     Returns (o [T, h_o, 128] bfloat16, final_state or None).  Asynchronous on ``stream``; raises
     GemmError on a non-zero status."""
     import torch
+    # shapes first: the kernels read exactly these extents, and no device check can catch a
+    # buffer that is too small
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k and v must be [T, heads, head_dim] tensors")
+    T, h_q, d = q.shape
+    h_k, h_v = k.shape[1], v.shape[1]
+    if tuple(k.shape) != (T, h_k, d) or tuple(v.shape) != (T, h_v, d):
+        raise ValueError(f"k {tuple(k.shape)} and v {tuple(v.shape)} must have q's tokens and "
+                         f"head dim ({T}, ., {d})")
+    if tuple(alpha.shape) != (T, h_v) or tuple(beta.shape) != (T, h_v):
+        raise ValueError(f"alpha {tuple(alpha.shape)} and beta {tuple(beta.shape)} must be "
+                         f"[T, h_v] = ({T}, {h_v})")
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens must be a 1-D tensor of n_seqs + 1 offsets")
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
                         ("v", v, torch.bfloat16), ("alpha", alpha, torch.float32),
                         ("beta", beta, torch.float32), ("cu_seqlens", cu_seqlens, torch.int32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
-    T, h_q, d = q.shape
-    h_k, h_v = k.shape[1], v.shape[1]
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     h_o = gdn_out_heads(h_q, h_k, h_v)
     n = cu_seqlens.numel() - 1
     if initial_state is not None and (initial_state.dtype != torch.float32 or
                                       tuple(initial_state.shape) != (n, h_v, d, d) or
                                       not initial_state.is_contiguous()):
         raise ValueError("initial_state must be a contiguous float32 [n, h_v, d, d] tensor")
+    if initial_state is not None and initial_state.device != q.device:
+        raise ValueError(f"initial_state is on {initial_state.device}, q on {q.device}")
+    if workspace is not None and (not workspace.is_cuda or workspace.device != q.device or
+                                  not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous tensor on q's device")
     o = torch.empty((T, h_o, d), dtype=torch.bfloat16, device=q.device)
     sf = (torch.empty((n, h_v, d, d), dtype=torch.float32, device=q.device)
           if output_final_state else None)
@@ -545,7 +564,7 @@ def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_sta
                            beta.data_ptr(), cu_seqlens.data_ptr(), n, T, h_q, h_k, h_v, d,
                            float(scale), 0 if initial_state is None else initial_state.data_ptr(),
                            o.data_ptr(), 0 if sf is None else sf.data_ptr(), workspace.data_ptr(),
-                           workspace.numel(), _stream_handle(stream))
+                           workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc != GDN_OK:
         raise GemmError(rc, gdn_last_error())
     return o, sf

@@ -73,3 +73,30 @@ def test_settings_hooks():
     assert g.gdn_set_fault_injection(2) == g.GDN_ERR_INVALID_ARG
     assert g.gdn_set_fault_injection(0) == g.GDN_OK
     assert g.gdn_check_status(0, 0) == g.GDN_ERR_INVALID_ARG             # no workspace
+
+
+def test_torch_entry_point_checks_shapes_before_anything_else():
+    """Shape mistakes are caught on the host, before any device is touched (CPU tensors here:
+    every case fails its shape check before the device check)."""
+    import torch
+    T, h, d = 10, 2, 128
+    bf = torch.bfloat16
+    good = dict(q=torch.zeros(T, h, d, dtype=bf), k=torch.zeros(T, h, d, dtype=bf),
+                v=torch.zeros(T, h, d, dtype=bf), alpha=torch.ones(T, h),
+                beta=torch.zeros(T, h), cu_seqlens=torch.tensor([0, T], dtype=torch.int32))
+    bad = [
+        dict(q=torch.zeros(T, h * d, dtype=bf)),          # q not 3-D
+        dict(k=torch.zeros(T - 1, h, d, dtype=bf)),       # k missing a token
+        dict(v=torch.zeros(T, h, 64, dtype=bf)),          # v with another head dim
+        dict(alpha=torch.ones(T, h + 1)),                 # alpha over the wrong heads
+        dict(beta=torch.zeros(T)),                        # beta not [T, h_v]
+        dict(cu_seqlens=torch.zeros((), dtype=torch.int32)),
+    ]
+    for change in bad:
+        args = dict(good, **change)
+        with pytest.raises(ValueError, match="must"):
+            g.gated_delta_rule(args["q"], args["k"], args["v"], args["alpha"], args["beta"],
+                               args["cu_seqlens"], 1.0)
+    with pytest.raises(ValueError, match="CUDA"):       # right shapes, CPU tensors
+        g.gated_delta_rule(good["q"], good["k"], good["v"], good["alpha"], good["beta"],
+                           good["cu_seqlens"], 1.0)
