@@ -210,9 +210,14 @@ def linear(A, W, bias=None, activation: str = "none", out=None, variant: int = 0
         raise ValueError("bias must be a contiguous CUDA vector of N elements")
     if out is None:
         out = torch.empty((M, N), dtype=A.dtype, device=A.device)
-    rc = gemm_f16_nt_fused(A.data_ptr(), W.data_ptr(), out.data_ptr(), M, N, K, DTYPES[dt],
-                           0 if bias is None else bias.data_ptr(), ACTIVATIONS[activation],
-                           int(variant), 0, 0, _stream_handle(stream))
+    elif (out.dtype != A.dtype or not out.is_cuda or tuple(out.shape) != (M, N)
+          or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous (M, N) CUDA tensor of A's dtype")
+    dev = _one_device(("A", A), ("W", W), ("bias", bias), ("out", out))
+    with torch.cuda.device(dev):
+        rc = gemm_f16_nt_fused(A.data_ptr(), W.data_ptr(), out.data_ptr(), M, N, K, DTYPES[dt],
+                               0 if bias is None else bias.data_ptr(), ACTIVATIONS[activation],
+                               int(variant), 0, 0, _stream_handle(stream))
     if rc != OK:
         raise GemmError(rc, gemm_f16_last_error())
     return out
@@ -389,7 +394,8 @@ def pack_scales(S, K: int | None = None, stream=None):
         raise ValueError("S must have K/32 columns")
     out = torch.empty(max(gemm_mxf8_scale_bytes(rows, K), 0), dtype=torch.uint8,
                       device=S.device)
-    rc = gemm_mxf8_pack_scales(S.data_ptr(), out.data_ptr(), rows, K, _stream_handle(stream))
+    with torch.cuda.device(S.device):
+        rc = gemm_mxf8_pack_scales(S.data_ptr(), out.data_ptr(), rows, K, _stream_handle(stream))
     if rc != OK:
         raise GemmError(rc, gemm_f16_last_error())
     return out
@@ -444,10 +450,14 @@ def gemm_mx(A, B, SFA, SFB, out=None, fmt_a: str = "e4m3", fmt_b: str = "e4m3",
                 workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
     if workspace is not None and workspace is not True and workspace is not False:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    rc = gemm_mxf8_nt(A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(), out.data_ptr(),
-                      M, N, K, FP8_FORMATS[fmt_a], FP8_FORMATS[fmt_b], DTYPES[out_dtype],
-                      0 if bias is None else bias.data_ptr(), ACTIVATIONS[activation],
-                      int(variant), ws_ptr, ws_bytes, _stream_handle(stream))
+    dev = _one_device(("A", A), ("B", B), ("SFA", SFA), ("SFB", SFB), ("out", out),
+                      ("bias", bias), ("workspace", workspace if ws_ptr else None))
+    with torch.cuda.device(dev):
+        rc = gemm_mxf8_nt(A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
+                          out.data_ptr(), M, N, K, FP8_FORMATS[fmt_a], FP8_FORMATS[fmt_b],
+                          DTYPES[out_dtype], 0 if bias is None else bias.data_ptr(),
+                          ACTIVATIONS[activation], int(variant), ws_ptr, ws_bytes,
+                          _stream_handle(stream))
     if rc != OK:
         raise GemmError(rc, gemm_f16_last_error())
     return out
@@ -539,19 +549,17 @@ def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_sta
                         ("beta", beta, torch.float32), ("cu_seqlens", cu_seqlens, torch.int32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor")
-        if t.device != q.device:
-            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     h_o = gdn_out_heads(h_q, h_k, h_v)
     n = cu_seqlens.numel() - 1
     if initial_state is not None and (initial_state.dtype != torch.float32 or
                                       tuple(initial_state.shape) != (n, h_v, d, d) or
                                       not initial_state.is_contiguous()):
         raise ValueError("initial_state must be a contiguous float32 [n, h_v, d, d] tensor")
-    if initial_state is not None and initial_state.device != q.device:
-        raise ValueError(f"initial_state is on {initial_state.device}, q on {q.device}")
-    if workspace is not None and (not workspace.is_cuda or workspace.device != q.device or
-                                  not workspace.is_contiguous()):
-        raise ValueError("workspace must be a contiguous tensor on q's device")
+    dev = _one_device(("q", q), ("k", k), ("v", v), ("alpha", alpha), ("beta", beta),
+                      ("cu_seqlens", cu_seqlens), ("initial_state", initial_state),
+                      ("workspace", workspace))
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
     o = torch.empty((T, h_o, d), dtype=torch.bfloat16, device=q.device)
     sf = (torch.empty((n, h_v, d, d), dtype=torch.float32, device=q.device)
           if output_final_state else None)
@@ -560,11 +568,14 @@ def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_sta
         s = stream if stream is not None else torch.cuda.current_stream()
         with torch.cuda.stream(s) if hasattr(s, "cuda_stream") else _nullctx():
             workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    rc = gdn_prefill_heads(q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(),
-                           beta.data_ptr(), cu_seqlens.data_ptr(), n, T, h_q, h_k, h_v, d,
-                           float(scale), 0 if initial_state is None else initial_state.data_ptr(),
-                           o.data_ptr(), 0 if sf is None else sf.data_ptr(), workspace.data_ptr(),
-                           workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    with torch.cuda.device(dev):
+        rc = gdn_prefill_heads(q.data_ptr(), k.data_ptr(), v.data_ptr(), alpha.data_ptr(),
+                               beta.data_ptr(), cu_seqlens.data_ptr(), n, T, h_q, h_k, h_v, d,
+                               float(scale),
+                               0 if initial_state is None else initial_state.data_ptr(),
+                               o.data_ptr(), 0 if sf is None else sf.data_ptr(),
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               _stream_handle(stream))
     if rc != GDN_OK:
         raise GemmError(rc, gdn_last_error())
     return o, sf
@@ -612,8 +623,11 @@ def gemm(A, B, out=None, variant: int | str = 0, stream=None, workspace=True):
                 workspace = torch.empty(need, dtype=torch.uint8, device=A.device)
     if workspace is not None and workspace is not True and workspace is not False:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    rc = gemm_f16_nt_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, int(variant),
-                        ws_ptr, ws_bytes, _stream_handle(stream))
+    dev = _one_device(("A", A), ("B", B), ("out", out),
+                      ("workspace", workspace if ws_ptr else None))
+    with torch.cuda.device(dev):
+        rc = gemm_f16_nt_ex(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, int(variant),
+                            ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != OK:
         raise GemmError(rc, gemm_f16_last_error())
     return out
@@ -625,6 +639,21 @@ class _nullctx:
 
     def __exit__(self, *a):
         return False
+
+
+def _one_device(*named):
+    """The device that every given tensor (None entries skipped) lives on.  The C entry points
+    launch on the current CUDA device, so the torch entry points run them under this one: a
+    tensor on another device would otherwise be read by the wrong GPU."""
+    dev = None
+    for name, t in named:
+        if t is None or isinstance(t, bool):
+            continue
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other operands on {dev}")
+    return dev
 
 
 def check_status(stream=None) -> None:
