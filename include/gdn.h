@@ -51,7 +51,10 @@
  * Ownership: the caller owns every buffer; nothing is retained after a call.  Apart from the
  * state pair above, no written buffer may overlap another buffer of the call.  Asynchronous on
  * `stream`: the call's first kernel starts after all earlier work on the stream, and its later
- * kernels use programmatic dependent launch among themselves.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, heads in none of the
+ * kernels use programmatic dependent launch among themselves.  A call enqueues kernel launches
+ * only (no allocation, copy or synchronisation), so it may be recorded into a CUDA graph; the
+ * first call on each device also sets the kernels' shared-memory attributes, so make that one
+ * outside a capture.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, heads in none of the
  * layouts above, workspace too small), GDN_ERR_UNSUPPORTED (head_dim other than 128, misaligned
  * q/k/v/o, more than 8 query heads per state head, more than 2^31 / 192 chunks x value heads),
  * GDN_ERR_CUDA (a launch failed;
