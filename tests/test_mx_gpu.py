@@ -238,14 +238,21 @@ def test_fused_epilogue(variant, activation):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("name", ["mx_square_2048", "mx_ragged_3000x5000x1056"])
+@pytest.mark.parametrize("name", ["mx_square_2048", "ragged_1000x1800x1568"])
 def test_stream_k_tail_parity(name, variant):
     """With a workspace, the tiles of a partial last wave are split by K blocks across units
-    (the pieces are summed by the last contributor)."""
-    w = MX_WORKLOADS[name]
-    if g.gemm_mxf8_workspace_bytes(w.M, w.N, w.K, variant) == 0:
-        pytest.skip("no stream-K tail for this shape and variant on this device")
-    A, B, SA, SB = mx_workload_inputs(w)
+    (the pieces are summed by the last contributor).  Both shapes leave a partial last wave for
+    every variant on a 152-SM GB300; the ragged one also has partial M / N tiles and a partial
+    last K block (1568 = 12 x 128 + 32)."""
+    if name in MX_WORKLOADS:
+        w = MX_WORKLOADS[name]
+        M, N, K = w.M, w.N, w.K
+        A, B, SA, SB = mx_workload_inputs(w)
+    else:
+        M, N, K = 1000, 1800, 1568
+        A, B, SA, SB = make_mx_inputs(M, N, K, seed=1568)
+    assert g.gemm_mxf8_workspace_bytes(M, N, K, variant) > 0, \
+        "this shape is meant to take the stream-K tail"
     full_parity(A, B, SA, SB, variant, f"{name} stream-K variant {variant}", workspace=True)
 
 
