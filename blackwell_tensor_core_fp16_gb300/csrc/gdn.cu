@@ -913,11 +913,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 u[e] = u_hi[e] + (u_lo[e] + u_l2[e]);
                 pq[e] += pq2[e];
             }
-            // (lower warps) the epilogue's U' rows and decay ratios, read before the barrier
+            // (lower warps) the epilogue's U' rows and decay ratios, read before the barrier; the
+            // upper warps skip these loads (lanes of one token share a bank: 4-way conflicts)
             const int te = m0 + gq, re = n0 + 2 * tg;
-            const float f0 = Bg[kC + te], f1 = Bg[kC + te + 8];
-            const float up0 = Bup[re * kC + te], up1 = Bup[(re + 1) * kC + te];
-            const float up2 = Bup[re * kC + te + 8], up3 = Bup[(re + 1) * kC + te + 8];
+            float f0 = 0.f, f1 = 0.f, up0 = 0.f, up1 = 0.f, up2 = 0.f, up3 = 0.f;
+            if (!kh) {
+                f0 = Bg[kC + te];
+                f1 = Bg[kC + te + 8];
+                up0 = Bup[re * kC + te];
+                up1 = Bup[(re + 1) * kC + te];
+                up2 = Bup[re * kC + te + 8];
+                up3 = Bup[(re + 1) * kC + te + 8];
+            }
             if (kh) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) mypart[e * 32] = u[e];
