@@ -31,7 +31,7 @@ __all__ = [
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA_ERROR", 4: "TIMEOUT"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 VARIANTS = {"auto": 0, "tile": 1, "ws_128x256": 2, "ws_pair": 3, "ws_128x128": 4,
-            "ws_pair_direct": 5}
+            "ws_pair_direct": 5, "ws_pair_256x192": 6}
 
 build = _build.build
 LIB_PATH = _build.LIB_PATH

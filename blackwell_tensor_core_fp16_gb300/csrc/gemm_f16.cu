@@ -117,6 +117,7 @@ using Ws128x256 = gf16::WsCfg<1, 256, 4, true>;
 using WsPair = gf16::WsCfg<2, 256, 6, true>;
 using Ws128x128 = gf16::WsCfg<1, 128, 6, true>;
 using WsPairDirect = gf16::WsCfg<2, 256, 7, false>;
+using WsPair192 = gf16::WsCfg<2, 192, 6, true>;
 
 bool variant_info(int v, gemm_f16_variant_info* o)
 {
@@ -140,6 +141,10 @@ bool variant_info(int v, gemm_f16_variant_info* o)
     case GEMM_F16_VARIANT_WS_PAIR_DIRECT:
         *o = {2, 256, 256, 64, 7, (int)WsPairDirect::THREADS, (int)WsPairDirect::SMEM_ALLOC,
               (int)WsPairDirect::TMEM_COLS, (int)WsPairDirect::STAGE_TX, 1};
+        return true;
+    case GEMM_F16_VARIANT_WS_PAIR_256x192:
+        *o = {2, 256, 192, 64, 6, (int)WsPair192::THREADS, (int)WsPair192::SMEM_ALLOC,
+              (int)WsPair192::TMEM_COLS, (int)WsPair192::STAGE_TX, 1};
         return true;
     default:
         return false;
@@ -589,9 +594,15 @@ int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                                                          ws, ws_bytes, bytes_needed, epi)
                       : launch_ws<1, 128, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
                                                    ws_bytes, bytes_needed, epi);
+        case GEMM_F16_VARIANT_WS_PAIR_256x192:
+            return bf ? launch_ws<2, 192, 6, true, true>(variant, A, B, D, M, N, K, stream, *d, dev,
+                                                         ws, ws_bytes, bytes_needed, epi)
+                      : launch_ws<2, 192, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                                   ws_bytes, bytes_needed, epi);
         default:
             return fail(GEMM_F16_ERR_UNSUPPORTED,
-                        "variant %d has no bf16 / fused-epilogue form (use 0, 2, 3 or 4)", variant);
+                        "variant %d has no bf16 / fused-epilogue form (use 0, 2, 3, 4 or 6)",
+                        variant);
         }
     }
     switch (variant) {
@@ -610,6 +621,9 @@ int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
     case GEMM_F16_VARIANT_WS_PAIR_DIRECT:
         return launch_ws<2, 256, 7, false>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
                                            ws_bytes, bytes_needed);
+    case GEMM_F16_VARIANT_WS_PAIR_256x192:
+        return launch_ws<2, 192, 6, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
+                                          ws_bytes, bytes_needed);
     default:
         return fail(GEMM_F16_ERR_INVALID_ARG, "unknown variant %d", variant);
     }

@@ -300,7 +300,9 @@ struct WsCfg {
     static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES + SF_BYTES) * kCtaGroup;
     static constexpr uint32_t D_COLS = 64;                   // one 128-byte swizzle row of fp16
     static constexpr uint32_t D_BYTES = kBlockM * D_COLS * 2;
-    static constexpr uint32_t TMEM_COLS = kMx ? 512u : kAccBufs * kBlockN;  // accumulators (+ scales)
+    // accumulators (+ scales), rounded up to the power of two tcgen05.alloc takes
+    static constexpr uint32_t TMEM_COLS =
+        kMx ? 512u : (kAccBufs * kBlockN <= 128u ? 128u : kAccBufs * kBlockN <= 256u ? 256u : 512u);
     static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM columns");
     static_assert(!kMx || TMEM_SF + kStages * SF_COLS <= TMEM_COLS, "TMEM scale-factor ring");
     static constexpr uint32_t OFF_A = 0;

@@ -55,7 +55,9 @@ extern "C" {
 #define GEMM_F16_VARIANT_WS_PAIR 3    /* persistent, warp-specialised, CTA pair per 256x256 */
 #define GEMM_F16_VARIANT_WS_128x128 4 /* persistent, warp-specialised, 1 CTA per 128x128 tile */
 #define GEMM_F16_VARIANT_WS_PAIR_DIRECT 5 /* as WS_PAIR, 7 stages, epilogue stores from registers */
-#define GEMM_F16_NUM_VARIANTS 6
+#define GEMM_F16_VARIANT_WS_PAIR_256x192 6 /* as WS_PAIR with 256x192 tiles; explicit only: 0.91-0.99
+                                             of WS_PAIR on every shape measured */
+#define GEMM_F16_NUM_VARIANTS 7
 
 /*
  * D = A * B^T for fp16 A (M x K), B (N x K), D (M x N), fp32 accumulation, on `stream`.

@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 GUARD = 4096          # fp16 elements on each side of D (8 KiB: keeps D 16-byte aligned)
 FILL = 0x7E5A         # a NaN bit pattern
 WS_VARIANTS = [g.VARIANTS["ws_128x256"], g.VARIANTS["ws_pair"], g.VARIANTS["ws_128x128"],
-               g.VARIANTS["ws_pair_direct"]]
+               g.VARIANTS["ws_pair_direct"], g.VARIANTS["ws_pair_256x192"]]
 ALL_VARIANTS = [g.VARIANTS["tile"], g.VARIANTS["auto"]] + WS_VARIANTS
 
 

@@ -101,7 +101,7 @@ def test_expect_tx_bytes_match_page():
     assert (info["block_m"], info["block_n"], info["block_k"]) == (int(bm), int(bn), int(bk))
     assert info["stage_tx_bytes"] == int(want)
     # the same formula for the other variants (a pair counts both CTAs' loads)
-    for name in ("ws_128x256", "ws_128x128", "ws_pair"):
+    for name in ("ws_128x256", "ws_128x128", "ws_pair", "ws_pair_256x192"):
         v = g.gemm_f16_get_variant_info(g.VARIANTS[name])
         assert v["stage_tx_bytes"] == (v["block_m"] * v["block_k"] + v["block_n"] * v["block_k"]) * 2
 
@@ -114,7 +114,9 @@ def test_variant_info_resources():
         assert info["smem_bytes"] <= 232448          # 227 KB per CTA
         assert info["tmem_cols"] in (32, 64, 128, 256, 512)
         if info["persistent"]:
-            assert info["tmem_cols"] == 2 * info["block_n"]  # two accumulators
+            # two accumulators, in the power of two that tcgen05.alloc takes
+            assert info["tmem_cols"] >= 2 * info["block_n"]
+            assert info["tmem_cols"] < 4 * info["block_n"]
     with pytest.raises(g.GemmError):
         g.gemm_f16_get_variant_info(99)
 
