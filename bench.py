@@ -54,7 +54,7 @@ def parse_args():
                         "bench line")
     p.add_argument("--sweep-workloads", default="",
                    help="comma-separated subset of workloads for --sweep (default: all five)")
-    p.add_argument("--sweep-variants", default="1,2,3,4,5",
+    p.add_argument("--sweep-variants", default="1,2,3,4,5,6",
                    help="variants for --sweep; 'auto' = the automatic choice only")
     p.add_argument("--sweep-reps", type=int, default=0,
                    help="timed launches per case in --sweep (0: about 0.3 s of work)")
