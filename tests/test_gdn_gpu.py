@@ -315,3 +315,14 @@ def test_state_carried_in_place_across_calls(case):
         o[idx.cuda()] = op
     assert_parity(inp, o.float().cpu().double().numpy(), state.cpu().double().numpy(), 0.73,
                   f"carried state {case}", extra_chunks=1)
+
+
+def test_long_sequence():
+    """One sequence of 65,573 tokens (1,025 chunk steps, a ragged last chunk) in the grouped-value
+    layout with an initial state: 64-bit offsets into q / k / v / o and a workspace of several
+    hundred megabytes, and the chunk chain's rounding over a thousand dependent steps, against
+    the oracle on every head."""
+    T = 1025 * 64 - 27
+    inp = make_gdn_inputs(T, 1, 2, 4, 128, 128, seed=65536, state=True)
+    o, sf = run(inp, 2, 4)
+    assert_parity(inp, o, sf, 0.73, f"one sequence of {T} tokens")
