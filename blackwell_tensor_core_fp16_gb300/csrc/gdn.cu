@@ -1059,7 +1059,7 @@ int check(const void* q, const void* k, const void* v, const float* alpha, const
                         "of h_k, and h_q equal h_k or be a multiple of h_v", (long long)h_q,
                         (long long)h_k, (long long)h_v);
     if (head_dim != kD)
-        return gdn_fail(GDN_ERR_UNSUPPORTED, "head_dim=%lld; this build supports 128",
+        return gdn_fail(GDN_ERR_UNSUPPORTED, "head_dim=%lld; only head_dim 128 is supported",
                         (long long)head_dim);
     if (T > (1ll << 30) || n_seqs > (1ll << 30) || h_v > 65535 || h_q > 65535)
         return gdn_fail(GDN_ERR_INVALID_ARG, "size out of range");

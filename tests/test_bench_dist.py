@@ -91,7 +91,7 @@ def test_clock_records_that_force_a_second_measurement():
     bench = load_bench()
     ok = {"sm_mhz": 1400.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 20}
     assert not bench.clocks_rejected(ok)                     # the power cap alone is kept
-    assert not bench.clocks_rejected(None)                   # no nvidia-smi: nothing to judge
+    assert not bench.clocks_rejected(None)                   # no nvidia-smi: nothing to reject
     for reason in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
         assert bench.clocks_rejected(dict(ok, reasons=["sw_power_cap", reason]))
     locked = {"sm_mhz": 900.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 20}
