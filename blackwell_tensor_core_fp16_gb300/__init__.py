@@ -225,7 +225,8 @@ def linear(A, W, bias=None, activation: str = "none", out=None, variant: int = 0
 
 def gemm_f16_nt_noalloc(A: int, B: int, D: int, M: int, N: int, K: int, stream: int = 0) -> int:
     """D = A * B^T using the library's fixed device scratch instead of any allocation (for
-    callers that cannot allocate, e.g. while recording a CUDA graph); see include/gemm_f16.h."""
+    callers that cannot allocate, e.g. a server whose device memory all belongs to its own pool);
+    see include/gemm_f16.h."""
     return load().gemm_f16_nt_noalloc(A, B, D, M, N, K, stream)
 
 

@@ -127,9 +127,9 @@ int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, 
                    int variant, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * D = A * B^T without allocating anything, for callers that cannot allocate device memory: code
- * recording a CUDA graph (cudaMalloc cannot be captured and would end the capture), servers that
- * hand all device memory to their own pool at start-up and forbid other allocations, and
+ * D = A * B^T without allocating anything, for callers that cannot allocate device memory:
+ * servers that hand all device memory to their own pool at start-up and forbid any other
+ * allocation, plug-ins running inside a host program that owns every allocation, and
  * latency-bound loops that cannot afford cudaMalloc's implicit synchronisation.  The GEMM pages
  * have no counterpart to this entry point; it is a deployment convenience.
  *

@@ -1,8 +1,8 @@
 """The allocation-free entry point gemm_f16_nt_noalloc (needs a GB300).
 
-Some callers cannot allocate device memory at the moment they need a GEMM: code recording a CUDA
-graph (cudaMalloc cannot be captured), servers whose device memory all belongs to their own pool,
-and latency-bound loops that cannot take cudaMalloc's synchronisation.  gemm_f16_nt_noalloc
+Some callers cannot allocate device memory at the moment they need a GEMM: servers whose device
+memory all belongs to their own pool, plug-ins inside a host program that owns every allocation,
+and latency-bound loops that cannot take cudaMalloc's implicit synchronisation.  gemm_f16_nt_noalloc
 serves them by running the stream-K schedule with its workspace in a fixed device array that the
 library reserves when it is loaded.
 
