@@ -97,3 +97,12 @@ def test_clock_records_that_force_a_second_measurement():
     locked = {"sm_mhz": 900.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 20}
     assert bench.clocks_rejected(locked)                     # stuck low with no reason
     assert not bench.clocks_rejected(dict(locked, reasons=["sw_power_cap"]))
+
+
+def test_roofline_peak_follows_the_timed_region():
+    bench = load_bench()
+    # a long back-to-back region runs at the power-capped clock: the sustained figure
+    assert bench.roofline_peak(1919.4, 1711.7, 1500.0) == (1711.7, "bf16_tflops_sustained")
+    # a short region (and a peaks file without a sustained figure) takes the burst figure
+    assert bench.roofline_peak(1919.4, 1711.7, 20.0)[0] == 1919.4
+    assert bench.roofline_peak(1919.4, 0.0, 5000.0)[0] == 1919.4
