@@ -82,6 +82,19 @@ uint32_t l2_hint_setting()
     return v;
 }
 
+// Programmatic dependent launch of the persistent kernels (default on; GEMM_F16_PDL=0 turns it
+// off).  With it, a GEMM launched right after another on the same stream does its set-up
+// (barriers, tensor memory, descriptor prefetch) on SMs the previous one has left, and only its
+// first global-memory access waits for the previous kernel to finish.
+bool pdl_setting()
+{
+    static const bool v = [] {
+        const char* s = std::getenv("GEMM_F16_PDL");
+        return !(s && s[0] == '0');
+    }();
+    return v;
+}
+
 // Tile-rows per raster group: GEMM_F16_GROUP overrides (1..64); 0 when unset.
 uint32_t group_m_override()
 {
@@ -443,7 +456,7 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
     if (tiles > 0x7FFFFFFFll) return fail(GEMM_F16_ERR_UNSUPPORTED, "too many tiles");
 
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(C::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = stream;
@@ -468,8 +481,15 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
             units = d.pair_clusters[slot];
         }
     } else {
-        cfg.attrs = nullptr;
+        cfg.attrs = attr;
         cfg.numAttrs = 0;
+    }
+    if (pdl_setting()) {
+        // The kernel waits (griddepcontrol.wait) before its first global-memory access, so the
+        // launch may overlap the end of the kernel before it on the stream.
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
     }
     const int64_t KB = cdiv(K, C::BLOCK_K);
     // Stream-K tail: all units take part; otherwise no more units than tiles.

@@ -404,6 +404,13 @@ __global__ void __launch_bounds__(192, 1)
     tcgen05_fence_after();
     const uint32_t tmem_base = *slot_ptr;
 
+    // Everything above touches only shared memory, tensor memory and the kernel parameters, so
+    // it may overlap the end of the previous kernel on the stream.  Let the next GEMM begin its
+    // own set-up as SMs free up, then wait for the previous kernel's writes (A and B may be its
+    // output, D its input) before the first access to global memory.
+    grid_dep_launch();
+    grid_dep_wait();
+
     if (warp == 0) {
         // ---- TMA producer ------------------------------------------------------------------
         // The whole warp runs the loop, so every value it computes is warp-uniform; the waits'

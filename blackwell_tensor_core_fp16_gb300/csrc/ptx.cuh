@@ -64,6 +64,21 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Programmatic dependent launch.  grid_dep_launch() lets the next kernel on the stream, if it
+// was launched with programmatic stream serialization, start once every CTA of this grid has
+// called it or exited.  grid_dep_wait() returns once the kernel before this one on the stream
+// has completed and its memory writes are visible; it returns at once when this launch had no
+// programmatic dependency.
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // True in exactly one lane of the (converged) warp: the lowest active lane.
 __device__ __forceinline__ bool elect_one_sync()
 {

@@ -21,6 +21,13 @@
  * synchronise.  Errors that need the GPU to detect (a bounded wait that ran out) are reported
  * by gemm_f16_check_status().
  *
+ * Stream order: the persistent kernels (every variant but GEMM_F16_VARIANT_TILE) are launched
+ * with programmatic stream serialization.  A launch may start its set-up on SMs that the kernel
+ * before it on the stream has already left, but it reads and writes no global memory until that
+ * kernel has completed and its writes are visible, so results are ordered exactly as on a plain
+ * stream.  Setting the environment variable GEMM_F16_PDL=0 (read once per process) launches them
+ * the plain way.
+ *
  * Thread safety: entry points may be called from several host threads at once.
  */
 #ifndef GEMM_F16_H
