@@ -214,6 +214,41 @@ def test_back_to_back_shapes_on_one_stream():
         assert_parity(D.cpu(), ref, K, "back-to-back")
 
 
+@pytest.mark.parametrize("variant", [0, g.VARIANTS["ws_pair"], g.VARIANTS["ws_128x128"]])
+def test_dependent_launches_keep_stream_order(variant):
+    """Consecutive launches on one stream may overlap their set-up (programmatic dependent
+    launch) but never their memory accesses.  Three GEMMs run with no synchronisation between
+    them, three times over: the second reads the first's output D1 (read after write) and the
+    third overwrites D1 while the second may still be reading it (write after read).  Every
+    operand entry is -1, 0 or 1 and K1 * N1 <= 2048, so every partial sum and every element of
+    D1 and D2 is an integer that fp32 and fp16 hold exactly: both must equal the oracle bit for
+    bit."""
+    gen = torch.Generator().manual_seed(31)
+
+    def ternary(rows, cols):
+        return torch.randint(-1, 2, (rows, cols), generator=gen).to(torch.float16)
+
+    M, K1, N1, N2 = 16384, 16, 128, 256
+    A, B1, B2, B3 = ternary(M, K1), ternary(N1, K1), ternary(N2, N1), ternary(N1, K1)
+    Ad, B1d, B2d, B3d = A.cuda(), B1.cuda(), B2.cuda(), B3.cuda()
+    D1 = torch.full((M, N1), float("nan"), dtype=torch.float16, device="cuda")
+    D2 = torch.full((M, N2), float("nan"), dtype=torch.float16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    for _ in range(3):
+        for (a, b, d, n, k) in ((Ad, B1d, D1, N1, K1), (D1, B2d, D2, N2, N1),
+                                (Ad, B3d, D1, N1, K1)):
+            assert g.gemm_f16_nt_variant(a.data_ptr(), b.data_ptr(), d.data_ptr(), M, n, k, s,
+                                         variant) == g.OK, g.gemm_f16_last_error()
+    rc, bits = g.gemm_f16_check_status(s)
+    assert rc == g.OK, f"status bits 0x{bits:x}"
+    d1_first = oracle.gemm_f64(A, B1)                      # what the second GEMM must have read
+    d2_ref = oracle.gemm_f64(d1_first.astype(np.float16), B2)
+    d1_ref = oracle.gemm_f64(A, B3)                        # what the third GEMM left in D1
+    assert np.abs(d2_ref).max() <= 2048 and np.abs(d1_first).max() <= K1
+    assert np.array_equal(D2.cpu().double().numpy(), d2_ref), "D2 read a stale or overwritten D1"
+    assert np.array_equal(D1.cpu().double().numpy(), d1_ref), "D1 not the last GEMM's output"
+
+
 def test_torch_binding():
     A, B = make_inputs(200, 96, 64, seed=9)
     D = g.gemm(A.cuda(), B.cuda())
