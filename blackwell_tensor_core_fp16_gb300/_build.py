@@ -2,8 +2,10 @@
 from __future__ import annotations
 
 import os
+import re
 import shutil
 import subprocess
+import tempfile
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
@@ -81,3 +83,44 @@ def build(force: bool = False, verbose: bool = False) -> str:
         print("".join(logs))
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
+
+
+def ptxas_report() -> dict:
+    """Resource usage ptxas reports for every function of the library (nvcc -Xptxas -v): per
+    mangled name, its stack frame, spill stores and spill loads in bytes, and, for kernels, the
+    registers per thread.  Compiles into a temporary directory; the library is left as it is."""
+    compile_flags = [f for f in NVCC_FLAGS if f != "-shared"]
+    funcs: dict = {}
+    with tempfile.TemporaryDirectory() as tmp:
+        procs = []
+        for src in SOURCES:
+            obj = os.path.join(tmp, os.path.splitext(src)[0] + ".o")
+            cmd = [_nvcc(), "-Xptxas=-v", *compile_flags, "-c", "-o", obj,
+                   os.path.join(CSRC, src)]
+            procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                                stderr=subprocess.STDOUT, text=True)))
+        for src, p in procs:
+            out, _ = p.communicate()
+            if p.returncode != 0:
+                raise RuntimeError(f"nvcc failed on {src} ({p.returncode}):\n{out}")
+            current = None
+            for line in out.splitlines():
+                m = re.search(r"Function properties for (\S+)", line)
+                if m:
+                    current = funcs.setdefault(m.group(1), {"source": src})
+                    continue
+                m = re.search(r"Compiling entry function '([^']+)'", line)
+                if m:
+                    current = funcs.setdefault(m.group(1), {"source": src})
+                    current["entry"] = True
+                    continue
+                m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, "
+                              r"(\d+) bytes spill loads", line)
+                if m and current is not None:
+                    current.update(stack=int(m.group(1)), spill_stores=int(m.group(2)),
+                                   spill_loads=int(m.group(3)))
+                    continue
+                m = re.search(r"Used (\d+) registers", line)
+                if m and current is not None:
+                    current["registers"] = int(m.group(1))
+    return funcs

@@ -368,3 +368,24 @@ def test_failure_hooks_validate_arguments():
     assert g.gemm_f16_set_fault_injection(-1) == g.ERR_INVALID_ARG
     assert g.gemm_f16_set_fault_injection(0) == g.OK
     assert g.gemm_f16_set_wait_timeout_ms(4000) == g.OK
+
+
+# ---- code-generation records: no stack frame, no spills -------------------------------------
+
+def test_every_kernel_compiles_without_stack_or_spills():
+    """The page "TIRx" (zixuwang.me), section "验证如何支撑结论", keeps code-generation records
+    with zero spills and a zero stack among its validation checks.  The same record here: ptxas
+    reports, for every function of the library (each kernel instance and each non-inlined
+    helper), a zero-byte stack frame and no spill stores or loads, so no kernel touches local
+    memory.  Compiles into a temporary directory; needs nvcc, not a GPU."""
+    from blackwell_tensor_core_fp16_gb300 import _build
+    report = _build.ptxas_report()
+    names = " ".join(report)
+    for kernel in ("gemm_ws_kernel", "gemm_tile_kernel", "mx_pack_scales_kernel",
+                   "gdn_scan_kernel", "gdn_prepare_kernel", "gdn_chunk_list_kernel"):
+        assert kernel in names, f"ptxas reported no {kernel}"
+    for name, r in report.items():
+        assert {"stack", "spill_stores", "spill_loads"} <= r.keys(), f"no record for {name}"
+        assert (r["stack"], r["spill_stores"], r["spill_loads"]) == (0, 0, 0), (name, r)
+        if r.get("entry"):
+            assert 0 < r["registers"] <= 255, (name, r)
