@@ -389,3 +389,75 @@ def test_every_kernel_compiles_without_stack_or_spills():
         assert (r["stack"], r["spill_stores"], r["spill_loads"]) == (0, 0, 0), (name, r)
         if r.get("entry"):
             assert 0 < r["registers"] <= 255, (name, r)
+
+
+# ---- the persistent kernels' address arithmetic, replayed on the CPU ---------------------------
+# A stand-in for a memory checker (none runs on this hardware here): the coordinates and
+# workspace offsets gemm_ws_kernel computes, rebuilt from the library's own scheduling functions
+# for every variant and workload shape, must stay inside what the launch provides, and the
+# output boxes must cover D exactly once.
+
+GB300_L2 = 126 << 20
+
+
+def _replay(variant, M, N, K, units, stream_k):
+    info = g.gemm_f16_get_variant_info(variant)
+    cg, mma_m, bn = info["cta_group"], info["block_m"], info["block_n"]
+    b_rows = bn // cg
+    num_m, num_n, KB = -(-M // mma_m), -(-N // bn), -(-K // 64)
+    T = num_m * num_n
+    R = g.gemm_f16_sk_tail_tiles(T, units, KB) if stream_k else 0
+    used = units if R else min(T, units)
+    ws_bytes = 4096 + units * 2 * cg * 128 * bn * 4          # the header's workspace size
+    part_bytes = 128 * bn * 4
+    group = g.gemm_f16_raster_group(mma_m, K, 2, GB300_L2)
+    stores = {}
+    written = {}      # (unit, tail tile) -> piece slot the unit wrote
+    first_tail = {}   # unit -> its first tail tile (the kernel's sk_lo / KB)
+    for c in range(used):
+        for i in range(g.gemm_f16_sk_items(T, used, KB, R, c)):
+            tile, kb0, kb1, piece, partial = g.gemm_f16_sk_item(T, used, KB, R, c, i)
+            m_blk, n_blk = g.gemm_f16_tile_coord(tile, num_m, num_n, group)
+            assert m_blk < num_m and n_blk < num_n
+            assert 0 <= kb0 < kb1 <= KB and (kb0 * 64 * 2) % 16 == 0   # TMA x: 16-byte aligned
+            r = tile - (T - R)
+            if r >= 0:
+                first_tail.setdefault(c, r)
+                written[(c, r)] = piece
+            if partial:
+                assert piece in (0, 1)
+                for rank in range(cg):
+                    slot = (c * 2 + piece) * cg + rank
+                    assert 4096 + (slot + 1) * part_bytes <= ws_bytes
+                    assert (r * cg + rank) * 4 < 4096                     # tile counters
+                u1 = g.gemm_f16_sk_unit_of(T, used, KB, R, r * KB + KB - 1)
+                if c != u1:
+                    continue                                          # the last one stores
+            for rank in range(cg):
+                m0 = m_blk * mma_m + rank * 128
+                assert m0 >= 0 and n_blk * bn + rank * b_rows >= 0    # load boxes
+                for ch in range(bn // 64):
+                    col0 = n_blk * bn + 64 * ch
+                    if col0 < N and m0 < M:                           # stores never start outside
+                        assert (col0 * 2) % 16 == 0
+                        stores[(m0, col0)] = stores.get((m0, col0), 0) + 1
+    # the fix-up reads, for tail tile r, piece r - first_tail[u] of each contributor u
+    for r in range(R):
+        u0 = g.gemm_f16_sk_unit_of(T, used, KB, R, r * KB)
+        u1 = g.gemm_f16_sk_unit_of(T, used, KB, R, r * KB + KB - 1)
+        for u in range(u0, u1 + 1):
+            assert written[(u, r)] == r - first_tail[u]
+    expect = {(128 * i, 64 * j) for i in range(-(-M // 128)) for j in range(-(-N // 64))}
+    assert set(stores) == expect and set(stores.values()) == {1}
+
+
+@pytest.mark.parametrize("variant", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("shape", [(128, 128, 64), (2048, 2048, 2048), (3000, 5000, 1000),
+                                   (8192, 8192, 8192), (16384, 14336, 4096), (129, 136, 72)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_kernel_addresses_stay_in_bounds_and_cover_d_once(variant, shape):
+    M, N, K = shape
+    units = 152 // g.gemm_f16_get_variant_info(variant)["cta_group"]
+    for u in (units, units - 3):          # fewer co-resident units than SMs allow
+        for stream_k in (False, True):
+            _replay(variant, M, N, K, u, stream_k)
