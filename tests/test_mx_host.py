@@ -118,3 +118,23 @@ def test_rejects_before_touching_the_gpu():
     assert g.gemm_mxf8_nt(16, 16, 16, 16, 16, 0, 128, 64, 0, 0, 0, 0, 0, 0, 0, 0, 0) == g.OK
     assert g.gemm_mxf8_nt(16, 16, 16, 16, 16, 128, 128, 64, 0, 0, 0, 0, 0, 7, 0, 0, 0) \
         == g.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
+def test_b_scales_of_every_n_tile_fit_the_stage_slot(variant):
+    """A stage loads `chunks` 128-row groups of B's scales, starting with the group that holds
+    the tile's first row, into 4 tensor-memory columns per group after A's 4 (32 rows per
+    column).  An N tile that starts inside a group (192-wide tiles start 64 rows in on every
+    other tile) reads its scales from a column (rows into the group) / 32 further on.  For every
+    tile position: the tile's rows lie in the groups the stage loads, and the columns the MMA
+    reads stay inside the stage's slot."""
+    info = g.gemm_mxf8_get_variant_info(variant)
+    bn = info["block_n"]
+    chunks = bn // 128 if bn % 128 == 0 else bn // 128 + 1
+    slot_cols = 4 * (1 + chunks)
+    for n_blk in range(64):
+        row0 = n_blk * bn
+        first_group, last_group = row0 // 128, (row0 + bn - 1) // 128
+        assert last_group - first_group + 1 <= chunks
+        shift = (row0 % 128) // 32
+        assert 4 + shift + bn // 32 <= slot_cols
