@@ -18,7 +18,9 @@
  *
  * Packed input (same page): the tokens of n_seqs independent sequences lie back to back;
  * sequence i owns tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 and its own state.  The host never
- * reads cu_seqlens: it is a device array the kernels consult.
+ * reads cu_seqlens: it is a device array the kernels consult, and they trust it.  Offsets that
+ * break its contract below (one outside [0, total_tokens], or a decreasing pair) make the kernels
+ * read and write outside q, k, v, alpha, beta and o; the caller must not pass them.
  *
  * Heads (the page's three relations: MHA, GQA, GVA).  q has h_q heads, k h_k, and v, alpha,
  * beta and the states h_v, a multiple of h_k; state head j reads key head j / (h_v / h_k).
