@@ -526,7 +526,9 @@ def gated_delta_rule(q, k, v, alpha, beta, cu_seqlens, scale: float, initial_sta
                      output_final_state: bool = False, stream=None, workspace=None):
     """Gated Delta Net prefill over packed sequences (CUDA tensors): q [T, h_q, 128], k
     [T, h_k, 128] and v [T, h_v, 128] bfloat16; alpha, beta [T, h_v] float32; cu_seqlens [n + 1]
-    int32; initial_state [n, h_v, 128, 128] float32 or None.  h_v is a multiple of h_k, and h_q
+    int32, non-decreasing from 0 to T (not checked: the kernels trust these offsets and would
+    access memory outside the tensors for others); initial_state [n, h_v, 128, 128] float32 or
+    None.  h_v is a multiple of h_k, and h_q
     equals h_k (MHA, GVA: o has h_v heads) or is a multiple of h_v (GQA: o has h_q heads).
     Returns (o [T, h_o, 128] bfloat16, final_state or None).  Asynchronous on ``stream``; raises
     GemmError on a non-zero status."""
