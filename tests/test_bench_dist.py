@@ -106,3 +106,34 @@ def test_roofline_peak_follows_the_timed_region():
     # a short region (and a peaks file without a sustained figure) takes the burst figure
     assert bench.roofline_peak(1919.4, 1711.7, 20.0)[0] == 1919.4
     assert bench.roofline_peak(1919.4, 0.0, 5000.0)[0] == 1919.4
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle, timed on the host cores) prints exactly one JSON
+    line with the keys the benchmark contract names, on the same metric and workload as the
+    CUDA arm, with no host-device traffic."""
+    import json
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
+                       cwd=root, env=env, timeout=600)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, p.stdout
+    line = json.loads(lines[0])
+    bench = load_bench()
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert (line["steps"], line["warmup"], line["n_gpus"]) == (2, 1, 1)
+    assert line["config"]["workload"] == "square_8192+mlp_up_16384x14336x4096"
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"]
+    assert cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
