@@ -290,7 +290,9 @@ def test_encode_random_vs_numpy():
         rng.uniform(-2.0 ** -13, 2.0 ** -13, size=20000),
     ])
     got = oracle.f64_to_f16_bits(x)
-    assert np.array_equal(got, x.astype(F16).view(np.uint16))
+    with np.errstate(over="ignore"):   # values past 65520 round to infinity on purpose
+        want = x.astype(F16).view(np.uint16)
+    assert np.array_equal(got, want)
 
 
 def test_encode_special_values():
