@@ -20,7 +20,8 @@ __all__ = [
     "gemm_f16_nt", "gemm_f16_nt_variant", "gemm_f16_choose_variant", "gemm_f16_check_status",
     "gemm_f16_last_error", "gemm_f16_version", "gemm_f16_get_variant_info", "gemm_f16_idesc",
     "gemm_f16_smem_desc_sw128", "gemm_f16_sw128", "gemm_f16_tile_coord", "gemm_f16_ring_pos",
-    "gemm_f16_nt_ws", "gemm_f16_nt_ex", "gemm_f16_nt_noalloc", "gemm_f16_workspace_bytes",
+    "gemm_f16_nt_ws", "gemm_f16_nt_ex", "gemm_f16_nt_noalloc", "gemm_f16_noalloc_scratch_bytes",
+    "gemm_f16_workspace_bytes",
     "gemm_f16_nt_fused", "linear", "DTYPES", "ACTIVATIONS", "gemm_f16_set_wait_timeout_ms",
     "gemm_f16_set_fault_injection",
     "gemm_f16_sk_tail_tiles", "gemm_f16_raster_group",
@@ -101,6 +102,8 @@ def load():
         lib.gemm_f16_nt_ex.restype = i32
         lib.gemm_f16_nt_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, vp]
         lib.gemm_f16_nt_noalloc.restype = i32
+        lib.gemm_f16_noalloc_scratch_bytes.argtypes = []
+        lib.gemm_f16_noalloc_scratch_bytes.restype = sz
         lib.gemm_f16_nt_fused.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, i32, i32, vp, sz,
                                           vp]
         lib.gemm_f16_nt_fused.restype = i32
@@ -151,6 +154,10 @@ def load():
         lib.gdn_last_error.restype = ctypes.c_char_p
         lib.gdn_check_status.argtypes = [vp, vp]
         lib.gdn_check_status.restype = i32
+        lib.gdn_check_offsets.argtypes = [vp, i64, i64, i64, vp, sz, vp]
+        lib.gdn_check_offsets.restype = i32
+        lib.gdn_offsets_valid_host.argtypes = [ctypes.POINTER(ctypes.c_int32), i64, i64]
+        lib.gdn_offsets_valid_host.restype = i32
         lib.gdn_set_wait_timeout_ms.argtypes = [u32]
         lib.gdn_set_wait_timeout_ms.restype = i32
         lib.gdn_set_fault_injection.argtypes = [i32]
@@ -228,6 +235,11 @@ def gemm_f16_nt_noalloc(A: int, B: int, D: int, M: int, N: int, K: int, stream: 
     callers that cannot allocate, e.g. a server whose device memory all belongs to its own pool);
     see include/gemm_f16.h."""
     return load().gemm_f16_nt_noalloc(A, B, D, M, N, K, stream)
+
+
+def gemm_f16_noalloc_scratch_bytes() -> int:
+    """Size of the fixed device array gemm_f16_nt_noalloc uses (host-only)."""
+    return int(load().gemm_f16_noalloc_scratch_bytes())
 
 
 def gemm_f16_workspace_bytes(M: int, N: int, K: int, variant: int = 0) -> int:
@@ -512,6 +524,19 @@ def gdn_last_error() -> str:
 
 def gdn_check_status(workspace: int, stream: int) -> int:
     return load().gdn_check_status(workspace, stream)
+
+
+def gdn_check_offsets(cu_seqlens: int, n_seqs: int, total_tokens: int, h_v: int,
+                      workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    """Check cu_seqlens on the device (include/gdn.h); read the verdict with gdn_check_status."""
+    return load().gdn_check_offsets(cu_seqlens, n_seqs, total_tokens, h_v, workspace,
+                                    workspace_bytes, stream)
+
+
+def gdn_offsets_valid_host(cu_seqlens, total_tokens: int) -> bool:
+    """The offsets' contract applied to a host sequence of n_seqs + 1 offsets."""
+    arr = (ctypes.c_int32 * len(cu_seqlens))(*[int(x) for x in cu_seqlens])
+    return bool(load().gdn_offsets_valid_host(arr, len(cu_seqlens) - 1, total_tokens))
 
 
 def gdn_set_wait_timeout_ms(ms: int) -> int:

@@ -45,6 +45,7 @@
 #include <type_traits>
 
 #include "../../include/gdn.h"
+#include "gdn_offsets.h"
 #include "ptx.cuh"
 
 namespace {
@@ -121,16 +122,36 @@ __device__ __forceinline__ void grid_dep_launch()
 }
 
 // ---- chunk list: per sequence, ceil(len / 64) chunks, numbered in sequence order -------------
+// The offsets are checked first (non-decreasing, from 0 to total_tokens).  Offsets that break
+// that contract are refused: the status word gets kStatusBadOffsets and every sequence is listed
+// as empty (no chunk, no token), so the prepare kernel does nothing and the scan only passes the
+// states through.  Either way this kernel writes only the workspace's tables, at indices bounded
+// by n_seqs and max_chunks.
 __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_seqs,
+                                      int32_t total_tokens,
                                       int32_t* __restrict__ chunk_offset, int4* __restrict__ chunks,
                                       int32_t max_chunks, int32_t* __restrict__ n_chunks,
                                       uint32_t* __restrict__ status, int32_t* __restrict__ order,
                                       int4* __restrict__ seqinfo, uint32_t* __restrict__ counter)
 {
     grid_dep_launch();   // the prepare kernel may set itself up meanwhile
+    bool bad = false;
+    for (int32_t i = threadIdx.x; i < n_seqs; i += blockDim.x)
+        bad |= !gdn::offsets_pair_ok(cu[i], cu[i + 1]);
+    if (threadIdx.x == 0) bad |= !gdn::offsets_ends_ok(cu[0], cu[n_seqs], total_tokens);
+    bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) {
-        *status = 0u;    // this call's scan reports into it
-        *counter = 0u;   // the scan's work-item counter
+        *status = bad ? gdn::kStatusBadOffsets : 0u;   // this call's kernels report into it
+        *counter = 0u;                                 // the scan's work-item counter
+    }
+    if (bad) {   // refused: every sequence empty, in index order
+        for (int32_t i = threadIdx.x; i <= n_seqs; i += blockDim.x) chunk_offset[i] = 0;
+        for (int32_t i = threadIdx.x; i < n_seqs; i += blockDim.x) {
+            order[i] = i;
+            seqinfo[i] = make_int4(0, 0, 0, 0);
+        }
+        if (threadIdx.x == 0) *n_chunks = 0;
+        return;
     }
     __shared__ int32_t scan[1024];
     __shared__ int32_t ncs[1024];
@@ -367,8 +388,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                        const int32_t* __restrict__ n_chunks, int32_t h_v, int32_t qgroup,
                        int32_t kgroup, int32_t clear_status, __nv_bfloat16* __restrict__ ap,
                        float* __restrict__ gam_out, int32_t single_T,
-                       uint32_t* __restrict__ status, uint32_t* __restrict__ counter,
-                       uint64_t wait_ns)
+                       const int32_t* __restrict__ cu, uint32_t* __restrict__ status,
+                       uint32_t* __restrict__ counter, uint64_t wait_ns)
 {
     const int32_t ch = blockIdx.x;
     const int32_t j = blockIdx.y;
@@ -377,18 +398,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     // (q, k, v, alpha, beta); the chunk list, the workspace and the counter wait for it.  Every
     // CTA passes grid_dep_wait() before it exits.
     grid_dep_launch();   // the scan may set itself up meanwhile
-    // one sequence (single_T >= 0): chunk ch covers tokens 64 ch .. (no chunk list is built,
-    // and the first pass of a call, always launched after everything before it, clears its
-    // status word here); otherwise the chunk list says
+    // one sequence (single_T >= 0): chunk ch covers tokens 64 ch .. (no chunk list is built;
+    // the first pass of a call, always launched after everything before it, checks that the
+    // offsets are [0, single_T] and sets the call's status word here, and offsets that are not
+    // leave every chunk undone); otherwise the chunk list says
     int32_t t0, len;
     if (single_T >= 0) {
+        const bool ok = gdn::offsets_single_ok(cu[0], cu[1], single_T);
+        if (ch == 0 && j == 0 && threadIdx.x == 0 && clear_status)
+            *status = ok ? 0u : gdn::kStatusBadOffsets;
         t0 = ch * kC;
-        if (t0 >= single_T) {
+        if (!ok || t0 >= single_T) {
             grid_dep_wait();
             return;
         }
         len = min(kC, single_T - t0);
-        if (ch == 0 && j == 0 && threadIdx.x == 0 && clear_status) *status = 0u;
     } else {
         grid_dep_wait();
         if (ch >= *n_chunks) return;
@@ -461,7 +485,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     {
         const bool ok = gf16::mbar_wait(bar, 0, nullptr, wait_ns);
         if (__syncthreads_or(!ok)) {   // the tiles never landed: report and stop
-            if (tid == 0) atomicExch(status, 1u);
+            if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
             grid_dep_wait();
             return;
         }
@@ -718,7 +742,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     float* __restrict__ s_final, __nv_bfloat16* __restrict__ o,
                     uint32_t* __restrict__ status, int32_t h_v, int32_t qgroup, int32_t kgroup,
                     int32_t o_tok, int32_t o_hmul, float scale,
-                    uint64_t wait_ns, uint32_t fault, int32_t single_T)
+                    uint64_t wait_ns, uint32_t fault, int32_t single_T,
+                    const int32_t* __restrict__ cu)
 {
     extern __shared__ __align__(16) uint8_t smraw[];
     const uint32_t raw = smem_u32(smraw);
@@ -751,6 +776,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     struct Item {
         int32_t i, j, r0, c_begin, c_end, seq_start, seq_end;
     };
+    // One sequence: its offsets must be [0, single_T] (an input, read before grid_dep_wait);
+    // otherwise it is taken as empty and only its state passes through.
+    const bool single_ok = single_T < 0 || gdn::offsets_single_ok(cu[0], cu[1], single_T);
     const auto decode = [&](int32_t q) {
         Item it;
         const int32_t rank = q / (8 * h_v), rem = q - rank * 8 * h_v;
@@ -759,9 +787,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (single_T >= 0) {   // one sequence: chunks 0 .. ceil(T / 64) - 1 of tokens 0 .. T - 1
             it.i = 0;
             it.c_begin = 0;
-            it.c_end = (single_T + kC - 1) / kC;
+            it.c_end = single_ok ? (single_T + kC - 1) / kC : 0;
             it.seq_start = 0;
-            it.seq_end = single_T;
+            it.seq_end = single_ok ? single_T : 0;
         } else {               // two independent loads (their use can come much later)
             it.i = order[rank];
             const int4 si = seqinfo[rank];
@@ -839,7 +867,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                            gam, cj_of(c_begin), r0, chunk_t0(c_begin), jq, jk);
             const bool ok = gf16::mbar_wait(bar0 + 8 * (n & 1), (n >> 1) & 1, nullptr, wait_ns);
             if (__syncthreads_or(!ok)) {
-                if (tid == 0) atomicExch(status, 1u);
+                if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
                 return;
             }
         }
@@ -1014,7 +1042,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 const bool ok = !more || gf16::mbar_wait(bar0 + 8 * (b ^ 1), ((n + 1) >> 1) & 1,
                                                          nullptr, wait_ns);
                 if (__syncthreads_or(!ok)) {   // state pieces complete, the next chunk landed
-                    if (tid == 0) atomicExch(status, 1u);
+                    if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
                     return;
                 }
             }
@@ -1290,7 +1318,8 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
     bool first = true;
     if (single_T < 0) {
         e = gdn_launch(gdn_chunk_list_kernel, dim3(1), dim3(1024), 0, stream, first, cu_seqlens,
-                       static_cast<int32_t>(n_seqs), chunk_offset, chunks,
+                       static_cast<int32_t>(n_seqs), static_cast<int32_t>(total_tokens),
+                       chunk_offset, chunks,
                        static_cast<int32_t>(mc), n_chunks, status, order, seqinfo, counter);
         if (e != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_chunk_list_kernel: %s", cudaGetErrorString(e));
@@ -1304,8 +1333,8 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
                            first, map_q[gp], map_k, map_v, map_w, map_ut, alpha, beta,
                            static_cast<const int4*>(chunks), static_cast<const int32_t*>(n_chunks),
                            static_cast<int32_t>(h_v), qgroup, kgroup,
-                           static_cast<int32_t>(gp == 0), ap, gm, single_T, status, counter,
-                           g_gdn_wait_ns.load());
+                           static_cast<int32_t>(gp == 0), ap, gm, single_T, cu_seqlens, status,
+                           counter, g_gdn_wait_ns.load());
             if (e != cudaSuccess)
                 return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
         }
@@ -1322,7 +1351,7 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
                        static_cast<__nv_bfloat16*>(o) + gp * kD, status,
                        static_cast<int32_t>(h_v), qgroup, kgroup, static_cast<int32_t>(h_o),
                        static_cast<int32_t>(passes), scale, g_gdn_wait_ns.load(),
-                       g_gdn_fault.load(), single_T);
+                       g_gdn_fault.load(), single_T, cu_seqlens);
         if (e != cudaSuccess)
             return gdn_fail(GDN_ERR_CUDA, "gdn_scan_kernel: %s", cudaGetErrorString(e));
     }
@@ -1353,9 +1382,48 @@ int gdn_check_status(const void* workspace, cudaStream_t stream)
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+    if (word & gdn::kStatusBadOffsets)
+        return gdn_fail(GDN_ERR_INVALID_ARG, "cu_seqlens broke its contract (it must start at 0, "
+                        "end at total_tokens and never decrease); no token was processed");
     if (word != 0)
         return gdn_fail(GDN_ERR_TIMEOUT, "a scan CTA gave up a bounded wait for its chunk loads");
     return GDN_OK;
+}
+
+int gdn_check_offsets(const int32_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens,
+                      int64_t h_v, void* workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    t_gdn_error.clear();
+    if (n_seqs < 0 || total_tokens < 0 || h_v <= 0)
+        return gdn_fail(GDN_ERR_INVALID_ARG, "negative size or no heads");
+    if (total_tokens > (1ll << 30) || n_seqs > (1ll << 30))
+        return gdn_fail(GDN_ERR_INVALID_ARG, "size out of range");
+    if (cu_seqlens == nullptr) return gdn_fail(GDN_ERR_INVALID_ARG, "cu_seqlens is null");
+    const WsLayout l = layout_for(total_tokens, n_seqs, h_v);
+    if (workspace == nullptr || workspace_bytes < l.total || misaligned(workspace))
+        return gdn_fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) needed",
+                        l.total);
+    auto* ws = static_cast<uint8_t*>(workspace);
+    bool first = true;
+    const cudaError_t e = gdn_launch(
+        gdn_chunk_list_kernel, dim3(1), dim3(1024), 0, stream, first, cu_seqlens,
+        static_cast<int32_t>(n_seqs), static_cast<int32_t>(total_tokens),
+        reinterpret_cast<int32_t*>(ws + l.chunk_offset), reinterpret_cast<int4*>(ws + l.chunks),
+        static_cast<int32_t>(max_chunks_for(total_tokens, n_seqs)),
+        reinterpret_cast<int32_t*>(ws + l.n_chunks), reinterpret_cast<uint32_t*>(ws + l.status),
+        reinterpret_cast<int32_t*>(ws + l.order), reinterpret_cast<int4*>(ws + l.seqinfo),
+        reinterpret_cast<uint32_t*>(ws + l.counter));
+    if (e != cudaSuccess)
+        return gdn_fail(GDN_ERR_CUDA, "gdn_chunk_list_kernel: %s", cudaGetErrorString(e));
+    return GDN_OK;
+}
+
+int gdn_offsets_valid_host(const int32_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens)
+{
+    if (cu_seqlens == nullptr || n_seqs < 0) return 0;
+    for (int64_t i = 0; i < n_seqs; ++i)
+        if (!gdn::offsets_pair_ok(cu_seqlens[i], cu_seqlens[i + 1])) return 0;
+    return gdn::offsets_ends_ok(cu_seqlens[0], cu_seqlens[n_seqs], total_tokens) ? 1 : 0;
 }
 
 int gdn_set_wait_timeout_ms(uint32_t ms)

@@ -17,10 +17,15 @@
  * token-by-token order only by rounding.
  *
  * Packed input (same page): the tokens of n_seqs independent sequences lie back to back;
- * sequence i owns tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 and its own state.  The host never
- * reads cu_seqlens: it is a device array the kernels consult, and they trust it.  Offsets that
- * break its contract below (one outside [0, total_tokens], or a decreasing pair) make the kernels
- * read and write outside q, k, v, alpha, beta and o; the caller must not pass them.
+ * sequence i owns tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 and its own state, and a sequence's
+ * replay never crosses its boundary.  The host never reads cu_seqlens: it is a device array, and
+ * the call's first kernel checks it on the device before any token is touched.  Offsets that
+ * break the contract below (a first offset other than 0, a last one other than total_tokens, or
+ * a decreasing pair) are refused there: every sequence is then taken as empty, no token of q, k,
+ * v, alpha, beta or o is read or written, the final states (if asked for) equal the initial
+ * ones, and gdn_check_status returns GDN_ERR_INVALID_ARG for the call.  A one-sequence call,
+ * which numbers its chunks from total_tokens, requires cu_seqlens = [0, total_tokens] the same
+ * way.
  *
  * Heads (the page's three relations: MHA, GQA, GVA).  q has h_q heads, k h_k, and v, alpha,
  * beta and the states h_v, a multiple of h_k; state head j reads key head j / (h_v / h_k).
@@ -106,10 +111,24 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
 /* The message of the calling thread's last failed gdn_* call ("" if none). */
 const char* gdn_last_error(void);
 
-/* Waits for `stream`, then reads the status word of the last gdn_prefill call that used
- * `workspace`: GDN_OK, or GDN_ERR_TIMEOUT if a scan CTA gave up a bounded wait; GDN_ERR_CUDA if
- * the stream reported an error. */
+/* Waits for `stream`, then reads the status word of the last gdn_prefill (or
+ * gdn_check_offsets) call that used `workspace`: GDN_OK; GDN_ERR_INVALID_ARG if that call's
+ * cu_seqlens broke its contract (nothing was processed); GDN_ERR_TIMEOUT if a scan CTA gave up a
+ * bounded wait; GDN_ERR_CUDA if the stream reported an error. */
 int gdn_check_status(const void* workspace, cudaStream_t stream);
+
+/* Checks cu_seqlens [n_seqs + 1] (device memory) against the contract above on the device, with
+ * the one small kernel a packed gdn_prefill call starts with, and nothing after it: it reads the
+ * n_seqs + 1 offsets and writes only the workspace (sized by gdn_prefill_workspace_bytes for
+ * total_tokens, n_seqs, h_v).  Asynchronous on `stream`; gdn_check_status then returns
+ * GDN_ERR_INVALID_ARG for offsets that break the contract, else GDN_OK.  Errors as for
+ * gdn_prefill (argument checks on the host; nothing is enqueued on an error). */
+int gdn_check_offsets(const int32_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens,
+                      int64_t h_v, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The same rule on a host copy of the offsets (1: valid, 0: not); the device check and this
+ * function share one definition of the rule.  Host-only. */
+int gdn_offsets_valid_host(const int32_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens);
 
 /* Limit of one wait of the scan kernel for a chunk's loads, for later calls of this process
  * (ms >= 1; default 2000). */

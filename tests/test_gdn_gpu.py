@@ -21,9 +21,9 @@ import pytest
 import torch
 
 import blackwell_tensor_core_fp16_gb300 as g
-import oracle
 from blackwell_tensor_core_fp16_gb300.workloads import (GDN_WORKLOADS, gdn_workload_inputs,
                                                          make_gdn_inputs)
+from gdn_bounds import assert_parity
 
 pytestmark = pytest.mark.gpu
 C = 64
@@ -59,41 +59,6 @@ def run(inp, h_qk, h_v, scale=0.73, want_state=True):
     assert rc == g.GDN_OK, g.gdn_last_error()
     torch.cuda.synchronize()
     return o.float().cpu().double().numpy(), (None if sf is None else sf.cpu().double().numpy())
-
-
-def assert_parity(inp, o, sf, scale, where, extra_chunks=0):
-    ref_o, ref_s = oracle.gdn_f64(inp["q"], inp["k"], inp["v"], inp["alpha"], inp["beta"],
-                                  inp["cu_seqlens"], scale, inp["initial_state"])
-    cu = inp["cu_seqlens"].numpy()
-    assert np.isfinite(o).all(), f"{where}: an output was not written"
-    dk = inp["q"].shape[2]
-    for i in range(len(cu) - 1):
-        sl = slice(cu[i], cu[i + 1])
-        n = max(1, -(-(cu[i + 1] - cu[i]) // C)) + extra_chunks
-        ro = ref_o[sl]
-        if ro.size == 0:
-            continue
-        M = np.abs(ro).max(axis=(0, 2), keepdims=True)     # per value head
-        tol = 2.0 ** -7 * np.abs(ro) + n * (dk + C) * 2.0 ** -22 * M
-        err = np.abs(o[sl] - ro)
-        if (err > tol).any():
-            idx = np.argwhere(err > tol)[:4]
-            pytest.fail(f"{where}: sequence {i}: {int((err > tol).sum())} outputs out of bound, "
-                        f"worst err/tol {float((err / tol).max()):.3f}, first at {idx.tolist()}")
-        if sf is not None:
-            rs = ref_s[i]
-            Ms = np.abs(rs).max(axis=(1, 2), keepdims=True)
-            tols = 2.0 ** -20 * np.abs(rs) + n * (dk + C) * 2.0 ** -22 * Ms
-            errs = np.abs(sf[i] - rs)
-            assert (errs <= tols).all(), \
-                f"{where}: sequence {i}: state worst err/tol {float((errs / tols).max()):.3f}"
-    rms = lambda x: float(np.sqrt(np.mean(np.square(x)))) if x.size else 0.0
-    if ref_o.size:
-        assert rms(o - ref_o) <= 2.0 ** -8 * rms(ref_o), \
-            f"{where}: output RMS error {rms(o - ref_o) / rms(ref_o):.2e} of the RMS output"
-    if sf is not None and ref_s.size:
-        assert rms(sf - ref_s) <= 2.0 ** -14 * rms(ref_s), \
-            f"{where}: state RMS error {rms(sf - ref_s) / rms(ref_s):.2e} of the RMS state"
 
 
 @pytest.mark.parametrize("name", list(GDN_WORKLOADS))
@@ -160,6 +125,79 @@ def test_rejects_bad_arguments():
     assert call(n=-1) == g.GDN_ERR_INVALID_ARG
     assert call(n=0) == g.GDN_OK                             # nothing to do
     torch.cuda.synchronize()
+
+
+# ---- cu_seqlens checked on the device -----------------------------------------------------------
+
+@pytest.mark.parametrize("cu,T,ok", [
+    ([0, 70, 100], 100, True),
+    ([0, 0, 100, 100], 100, True),
+    ([0, 70, 101], 100, False),          # past the last token
+    ([0, -3, 100], 100, False),          # below 0
+    ([0, 2 ** 31 - 1, 100], 100, False),
+    ([0, 80, 70, 100], 100, False),      # decreasing
+    ([5, 70, 100], 100, False),          # first offset not 0
+    ([0, 70, 90], 100, False),           # last offset short
+] + [([0] + list(range(3, 3 * 2000, 3)) + [6000], 6000, True),      # 2001 offsets, several
+     ([0] + list(range(3, 3 * 2000, 3))[::-1] + [6000], 6000, False)],   # passes of the block
+    ids=lambda x: None)
+def test_offsets_checked_on_the_device(cu, T, ok):
+    """gdn_check_offsets runs the chunk-list kernel alone: it reads the n + 1 offsets and writes
+    only the workspace's tables, so offsets outside [0, T] are safe to give it.  The verdict read
+    through gdn_check_status must follow the contract, and a valid check after a refused one
+    clears the word."""
+    n = len(cu) - 1
+    need = g.gdn_prefill_workspace_bytes(T, n, 4)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    dcu = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert g.gdn_check_offsets(dcu.data_ptr(), n, T, 4, ws.data_ptr(), need, s) == g.GDN_OK
+    rc = g.gdn_check_status(ws.data_ptr(), s)
+    assert rc == (g.GDN_OK if ok else g.GDN_ERR_INVALID_ARG), g.gdn_last_error()
+    if not ok:
+        assert "cu_seqlens" in g.gdn_last_error()
+        good = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+        assert g.gdn_check_offsets(good.data_ptr(), 1, T, 4, ws.data_ptr(), need, s) == g.GDN_OK
+        assert g.gdn_check_status(ws.data_ptr(), s) == g.GDN_OK
+
+
+@pytest.mark.parametrize("cu", [[0, 99], [1, 100], [0, 120, 80, 200], [0, 100, 150],
+                                [7, 90, 200]], ids=lambda c: "_".join(map(str, c)))
+def test_broken_offsets_refuse_the_call(cu):
+    """A whole call with offsets that break the contract but stay inside [0, T] (so that even an
+    unchecked kernel could not leave its buffers): the call is refused on the device, no output is
+    written (o keeps its NaN fill), every final state equals its initial state, and
+    gdn_check_status reports GDN_ERR_INVALID_ARG.  The same workspace then serves a valid call,
+    which matches the oracle."""
+    T = 100 if len(cu) == 2 else 200
+    n = len(cu) - 1
+    inp = make_gdn_inputs(T, n, 1, 2, 128, 128, seed=61, state=True)
+    q, k, v = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda()
+    a, b = inp["alpha"].cuda(), inp["beta"].cuda()
+    s0 = inp["initial_state"].cuda()
+    o = torch.full((T, 2, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sf = torch.full((n, 2, 128, 128), float("nan"), dtype=torch.float32, device="cuda")
+    need = g.gdn_prefill_workspace_bytes(T, n, 2)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(cu_dev):
+        return g.gdn_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), a.data_ptr(),
+                             b.data_ptr(), cu_dev.data_ptr(), n, T, 1, 2, 128, 0.73,
+                             s0.data_ptr(), o.data_ptr(), sf.data_ptr(), ws.data_ptr(), need, s)
+
+    bad = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    assert call(bad) == g.GDN_OK                       # enqueued: the host never reads cu
+    assert g.gdn_check_status(ws.data_ptr(), s) == g.GDN_ERR_INVALID_ARG
+    assert bool(torch.isnan(o.float()).all()), "a refused call wrote outputs"
+    assert torch.equal(sf, s0), "a refused call changed a state"
+    # the same buffers, valid offsets
+    o.fill_(float("nan"))
+    sf.fill_(float("nan"))
+    assert call(inp["cu_seqlens"].cuda()) == g.GDN_OK
+    assert g.gdn_check_status(ws.data_ptr(), s) == g.GDN_OK
+    assert_parity(inp, o.float().cpu().double().numpy(), sf.cpu().double().numpy(), 0.73,
+                  f"valid call after refused offsets {cu}")
 
 
 def test_many_items_with_empty_sequences():

@@ -100,3 +100,53 @@ def test_torch_entry_point_checks_shapes_before_anything_else():
     with pytest.raises(ValueError, match="CUDA"):       # right shapes, CPU tensors
         g.gated_delta_rule(good["q"], good["k"], good["v"], good["alpha"], good["beta"],
                            good["cu_seqlens"], 1.0)
+
+
+def _offsets_rule(cu, total_tokens):
+    """The packed-input contract written out plainly: starts at 0, ends at total_tokens, never
+    decreases (so every sequence stays inside [0, total_tokens) and none crosses another)."""
+    if len(cu) == 0 or cu[0] != 0 or cu[-1] != total_tokens:
+        return False
+    return all(a <= b for a, b in zip(cu[:-1], cu[1:]))
+
+
+@pytest.mark.parametrize("cu,T,ok", [
+    ([0, 100], 100, True),                 # one sequence
+    ([0, 30, 30, 100], 100, True),         # an empty sequence inside
+    ([0, 0, 0], 0, True),                  # no tokens at all
+    ([0, 100], 99, False),                 # last offset past total_tokens
+    ([0, 99], 100, False),                 # last offset short of total_tokens
+    ([1, 100], 100, False),                # first offset not 0
+    ([0, 60, 40, 100], 100, False),        # a decreasing pair
+    ([0, -5, 100], 100, False),            # an offset below 0
+    ([0, 2 ** 31 - 1, 100], 100, False),   # an offset far past the end
+    ([0], 0, True),                        # no sequence (n_seqs = 0)
+    ([0], 5, False),
+])
+def test_offsets_rule_host_replay(cu, T, ok):
+    """The device kernels' check of cu_seqlens, replayed on the host through the library's own
+    copy of the rule, against the contract written out in this test."""
+    assert _offsets_rule(cu, T) == ok
+    assert g.gdn_offsets_valid_host(cu, T) == ok
+
+
+def test_offsets_rule_random_arrays():
+    import random
+    rng = random.Random(5)
+    for _ in range(2000):
+        n = rng.randint(0, 6)
+        T = rng.randint(0, 300)
+        cu = sorted(rng.randint(0, T) for _ in range(n + 1))
+        if cu:
+            cu[0], cu[-1] = 0, T
+        if rng.random() < 0.5 and n > 0:   # break it somewhere
+            i = rng.randint(0, n)
+            cu[i] += rng.choice([-3, -1, 1, 7])
+        assert g.gdn_offsets_valid_host(cu, T) == _offsets_rule(cu, T), (cu, T)
+
+
+def test_check_offsets_argument_checks():
+    assert g.gdn_check_offsets(0, 2, 100, 4, FAKE, 1 << 30, 0) == g.GDN_ERR_INVALID_ARG
+    assert g.gdn_check_offsets(FAKE, -1, 100, 4, FAKE, 1 << 30, 0) == g.GDN_ERR_INVALID_ARG
+    assert g.gdn_check_offsets(FAKE, 2, 100, 4, FAKE, 16, 0) == g.GDN_ERR_INVALID_ARG
+    assert g.gdn_check_offsets(FAKE, 2, 100, 4, 0, 1 << 30, 0) == g.GDN_ERR_INVALID_ARG
