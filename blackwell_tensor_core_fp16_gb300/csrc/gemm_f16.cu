@@ -846,15 +846,16 @@ int gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_
                  &need);
         if (rc != GEMM_F16_OK) return rc;
     }
-    if (need > kNoAllocScratchBytes)
-        return fail(GEMM_F16_ERR_UNSUPPORTED,
-                    "this shape needs %zu bytes of scratch; the fixed scratch holds %zu", need,
-                    kNoAllocScratchBytes);
+    // A stream-K workspace larger than the fixed array (a GPU with many more SMs than a GB300)
+    // is not offered: the launch then takes the plain data-parallel schedule, which needs none.
+    if (need > kNoAllocScratchBytes) need = 0;
     void* scratch = nullptr;
     if (need > 0 && (rc = noalloc_scratch(&scratch)) != GEMM_F16_OK) return rc;
     return run(A, B, D, M, N, K, stream, GEMM_F16_VARIANT_AUTO, scratch,
                need > 0 ? kNoAllocScratchBytes : 0);
 }
+
+size_t gemm_f16_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 int gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, size_t* bytes)
 {

@@ -150,11 +150,16 @@ int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, 
  * point.  Every call shares the one array and finds the previous call's contents in it; the
  * counters that must start at zero are cleared on `stream` before each launch.  Calls that
  * overlap on the GPU (on different streams) race on the array and give wrong results: serialise
- * them.  A shape whose stream-K workspace would exceed 40 MiB (not possible on a 152-SM GB300,
- * whose largest request is about 38 MiB) returns GEMM_F16_ERR_UNSUPPORTED and does nothing.
+ * them.  A shape whose stream-K workspace would exceed the array (not possible on a 152-SM
+ * GB300, whose largest request is about 38 MiB; possible on a GPU with many more SMs) runs the
+ * plain data-parallel schedule instead, which needs no workspace: the result is the same, only
+ * the last partial wave is not split.  Errors are those of gemm_f16_nt.
  */
 int gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                         cudaStream_t stream);
+
+/* Size in bytes of the fixed array gemm_f16_nt_noalloc uses (40 MiB).  Host-only. */
+size_t gemm_f16_noalloc_scratch_bytes(void);
 
 /* Workspace bytes gemm_f16_nt_ws / gemm_f16_nt_ex need for this shape and variant on the current
  * device (0: the shape gets no stream-K tail).  At most 4 KiB + 2 x units x 128 x 256 x 4 bytes

@@ -362,6 +362,18 @@ def test_stream_k_tail_choice():
     assert g.gemm_f16_sk_tail_tiles(240, 76, 3) == 0          # pieces under 4 k-blocks
 
 
+def test_noalloc_scratch_holds_every_gb300_workspace():
+    """The allocation-free entry point's fixed array (40 MiB) holds the largest stream-K
+    workspace any variant requests on a 152-SM GB300: 4 KiB of counters plus 2 pieces x 128 x
+    256 fp32 per CTA (76 pairs or 152 single CTAs).  A device whose request would not fit (here
+    a hypothetical 200-SM part) is served by the data-parallel schedule, which needs none."""
+    cap = g.gemm_f16_noalloc_scratch_bytes()
+    assert cap == 40 << 20
+    per_cta = 2 * 128 * 256 * 4
+    assert 4096 + 152 * per_cta <= cap            # 38.0 MiB: 1-CTA 128x256 or 76 CTA pairs
+    assert 4096 + 200 * per_cta > cap             # would take the no-workspace path
+
+
 def test_failure_hooks_validate_arguments():
     assert g.gemm_f16_set_wait_timeout_ms(0) == g.ERR_INVALID_ARG
     assert g.gemm_f16_set_fault_injection(2) == g.ERR_INVALID_ARG
