@@ -75,6 +75,17 @@ def parse_args():
                         "scenario (0: exactly --gdn-reps calls)")
     p.add_argument("--sweep-mx", action="store_true",
                    help="in --sweep, time the block-scaled FP8 workloads instead")
+    p.add_argument("--config-ms", type=float, default=200.0,
+                   help="back-to-back milliseconds per config in the per_config leg (single tile, "
+                        "2048^3, 3000x5000x1000; 0: skip)")
+    p.add_argument("--sustained-ms", type=float, default=1500.0,
+                   help="length of the sustained leg: the headline step back to back for at "
+                        "least this long, with its own clock record (0: skip)")
+    p.add_argument("--record-traffic", default="",
+                   help="read an ncu CSV log of the two GEMM launches of one step (metrics "
+                        "dram__bytes_read.sum, dram__bytes_write.sum, gpu__time_duration.sum; "
+                        "-k regex:gemm_ws) and write profiles/ncu_traffic.json for the current "
+                        "kernel sources, then exit")
     p.add_argument("--cublas-steps", type=int, default=-1,
                    help="steps of torch.mm on the same shapes, for context (-1: as many as "
                         "--steps, 0: skip)")
@@ -185,6 +196,57 @@ def recorded_traffic(variant_name: str):
     if d.get("kernel_src_sha256") != kernel_source_hash():
         return None
     return d.get("per_launch_dram_bytes", {}).get(variant_name)
+
+
+_UNIT = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+         "nsecond": 1e-9, "usecond": 1e-6, "msecond": 1e-3, "second": 1.0,
+         "ns": 1e-9, "us": 1e-6, "ms": 1e-3, "s": 1.0}
+
+
+def parse_ncu_csv(path):
+    """Per captured launch (in capture order): kernel name and {metric: value in bytes or
+    seconds} from an `ncu --csv --log-file` log (lines that are not CSV rows are skipped)."""
+    import csv
+    lines = [ln for ln in open(path) if ln.startswith('"')]
+    launches = {}
+    for row in csv.DictReader(lines):
+        key = row["ID"]
+        d = launches.setdefault(key, {"kernel": row["Kernel Name"], "metrics": {}})
+        val = float(row["Metric Value"].replace(",", ""))
+        d["metrics"][row["Metric Name"]] = val * _UNIT.get(row.get("Metric Unit", ""), 1.0)
+    return [launches[k] for k in sorted(launches, key=int)]
+
+
+def record_traffic(csv_path, command=""):
+    """profiles/ncu_traffic.json from the capture of one step's two launches (8192^3, then the
+    MLP shape), tagged with the hash of the kernel sources it describes."""
+    launches = parse_ncu_csv(csv_path)
+    if len(launches) != len(WORKLOADS):
+        raise SystemExit(f"expected {len(WORKLOADS)} launches in {csv_path}, found {len(launches)}")
+    by_w, total = {}, 0.0
+    for name, l in zip(WORKLOADS, launches):
+        m = l["metrics"]
+        rd, wr = m["dram__bytes_read.sum"], m["dram__bytes_write.sum"]
+        by_w[name] = {"kernel": l["kernel"], "dram_read_bytes": int(rd),
+                      "dram_write_bytes": int(wr), "dram_bytes": int(rd + wr),
+                      "duration_us": m.get("gpu__time_duration.sum", 0.0) * 1e6}
+        total += rd + wr
+    out = {"kernel_src_sha256": kernel_source_hash(),
+           "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+                     "gpu__time_duration.sum --clock-control none -k regex:gemm_ws, one launch per "
+                     "workload, written by bench.py --record-traffic",
+           "command": command,
+           "per_launch_dram_bytes_by_workload": {k: v["dram_bytes"] for k, v in by_w.items()},
+           "launches": by_w,
+           "per_launch_dram_bytes": {"ws_pair": int(total)},
+           "per_launch_note": "ws_pair entry is the sum over the two launches of one bench step "
+                              "(the unit 'achieved' uses)"}
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    with open(path, "w") as f:
+        json.dump(out, f, indent=2)
+        f.write("\n")
+    print(json.dumps(out))
+    return 0
 
 
 # ---- clocks --------------------------------------------------------------------------------
@@ -514,6 +576,152 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
                     "machine"}
 
 
+# ---- the other configs: single tile, 2048^3, 3000x5000x1000 ----------------------------------
+
+CONFIGS = ("single_tile_128x128x64", "square_2048", "ragged_3000x5000x1000")
+
+
+def run_config_leg(args, g, dev, stream, num_sms, peak_burst, hbm_peak, uuid):
+    """The three smaller configs on the automatic variant, inputs resident: warm (back-to-back
+    launches between two CUDA events, about `config_ms` of work after warm-up) and cold (a 512 MiB
+    scratch write before each launch, events around the launch alone), with the clocks sampled
+    over the warm loops."""
+    import torch
+    from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS as W, workload_inputs
+    scratch = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.2)
+    for name in CONFIGS:
+        w = W[name]
+        A, B = workload_inputs(w)
+        Ad, Bd = A.to(dev), B.to(dev)
+        D = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+        variant = g.gemm_f16_choose_variant(w.M, w.N, w.K, num_sms)
+
+        def launch():
+            rc = g.gemm_f16_nt(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), w.M, w.N, w.K,
+                               stream.cuda_stream)
+            if rc != g.OK:
+                raise g.GemmError(rc, g.gemm_f16_last_error())
+
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                launch()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                launch()
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 20
+        reps = max(100, min(200000, int(args.config_ms * 1e-3 / max(per, 1e-6))))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                launch()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / reps
+        # cold L2: 512 MiB written before each launch (outside the events)
+        cold_reps = 50
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(cold_reps)]
+        with torch.cuda.stream(stream):
+            for i in range(cold_reps):
+                scratch.fill_(i & 0xFF)
+                ev[i][0].record(stream)
+                launch()
+                ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        g.check_status(stream)
+        cold_us = 1e3 * sum(a.elapsed_time(b) for a, b in ev) / cold_reps
+        tf = w.flops / (us * 1e-6) / 1e12
+        out[name] = {"M": w.M, "N": w.N, "K": w.K, "variant": variant, "launches": reps,
+                     "us_per_launch": us, "tflops": tf, "frac_of_burst": tf / peak_burst,
+                     "hbm_gbs_algorithmic": w.min_bytes / (us * 1e-6) / 1e9,
+                     "hbm_frac": w.min_bytes / (us * 1e-6) / 1e9 / hbm_peak,
+                     "cold_l2_us_per_launch": cold_us,
+                     "cold_l2_tflops": w.flops / (cold_us * 1e-6) / 1e12}
+        del Ad, Bd, D
+    clk = sampler.stop()
+    del scratch
+    return {"metric": "fp16 GEMM per config, automatic variant (gemm_f16_nt)",
+            "timing": "warm: back-to-back launches between two CUDA events on the launching "
+                      "stream; cold: a 512 MiB scratch write before each launch, events around "
+                      "the launch alone",
+            "configs": out, "clocks": clk,
+            "gpu_launches": sum(v["launches"] + 50 for v in out.values())}
+
+
+def run_sustained_leg(args, g, stream, work, launch, flops_step, peak_burst, peak_sus, num_sms,
+                      uuid):
+    """The headline step back to back for at least `sustained_ms` (the power-capped regime the
+    sustained peak was measured in), timed with CUDA events on the launching stream (one after
+    every launch, for the per-shape split), with its own clock record; then cuBLAS (torch.mm) on
+    the same resident inputs for the same number of steps, for context."""
+    import torch
+    step_t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            for item in work:
+                launch(item)
+    torch.cuda.synchronize()
+    step_ms = 1e3 * (time.perf_counter() - step_t0) / 3
+    steps = max(10, int(math.ceil(args.sustained_ms / max(step_ms, 1e-3))))
+
+    def timed(fn):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(work) * steps + 1)]
+        sampler = ClockSampler(uuid)
+        sampler.start()
+        time.sleep(0.2)
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            e = 1
+            for _ in range(steps):
+                for item in work:
+                    fn(item)
+                    ev[e].record(stream)
+                    e += 1
+        torch.cuda.synchronize()
+        clk = sampler.stop()
+        ms = ev[0].elapsed_time(ev[-1])
+        durs = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(ev) - 1)]
+        per = {}
+        for j, item in enumerate(work):
+            w = item[0]
+            m = sum(durs[j::len(work)]) / steps
+            per[w.name] = {"ms_per_launch": m, "tflops": w.flops / (m * 1e-3) / 1e12}
+        tf = steps * flops_step / (ms * 1e-3) / 1e12
+        return tf, ms, per, clk
+
+    tf, ms, per, clk = timed(launch)
+    g.check_status(stream)
+    res = {"value": tf, "unit": "TFLOP/s", "steps": steps, "timed_ms": ms,
+           "per_workload": per, "peak_sustained": peak_sus,
+           "frac_of_sustained": tf / peak_sus if peak_sus else None,
+           "frac_of_burst": tf / peak_burst, "clocks": clk, "gpu_launches": steps * len(work)}
+    if clk and clk.get("sm_mhz"):
+        cpk = num_sms * FLOP_PER_CLK_PER_SM * clk["sm_mhz"] * 1e6 / 1e12
+        res["clock_peak_tflops"] = cpk
+        res["frac_of_clock_peak"] = tf / cpk
+    if args.cublas_steps != 0:
+        def mm(item):
+            _w, Ad, Bd, D, _v = item
+            torch.mm(Ad, Bd.t(), out=D)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                for item in work:
+                    mm(item)
+        torch.cuda.synchronize()
+        ctf, cms, cper, cclk = timed(mm)
+        res["cublas_same_step"] = {"value": ctf, "timed_ms": cms, "per_workload": cper,
+                                   "clocks": cclk, "ours_over_cublas": tf / ctf}
+    return res
+
+
 # ---- our arm ---------------------------------------------------------------------------------
 
 def run_ours(args):
@@ -689,6 +897,11 @@ def run_ours(args):
                                               "tflops": 2.0 * w.M * w.N * w.K / (ms * 1e-3) / 1e12}
         cublas["ours_over_cublas"] = value / world / cublas["value"]
 
+    sustained = None
+    if args.sustained_ms > 0:
+        sustained = run_sustained_leg(args, g, stream, work, launch, flops_step, peak_burst,
+                                      peak_sus, num_sms, uuid)
+
     # End to end through the public API: every step copies its inputs from pinned host memory
     # to the device, runs the GEMMs with gemm(), and copies each result back to pinned host
     # memory.  Copies run on their own streams with two buffer slots, so the upload of step
@@ -772,6 +985,11 @@ def run_ours(args):
         copy_roof = flops_step / ((h2d + d2h) / (link_gbs * 1e9)) / 1e12
         del hsrc, hdst, dsrc, ddst
 
+    config_leg = None
+    if args.config_ms > 0 and not args.only:
+        config_leg = run_config_leg(args, g, dev, stream, num_sms, peak_burst,
+                                    measured_hbm_gbs(), uuid)
+
     mx_leg = None
     if args.mx_steps > 0:
         mx_leg = run_mx_leg(args, g, dev, stream, num_sms, peak_burst, uuid)
@@ -814,6 +1032,8 @@ def run_ours(args):
                         "D -> pinned host (copy stream); two buffer slots, copies of "
                         "neighbouring steps overlap the GEMMs"},
         "gpu_launches": K * len(work),
+        "per_config": config_leg,
+        "sustained": sustained,
         "mx_fp8": mx_leg,
         "gdn_prefill": gdn_leg,
         "clocks": clock_info,
@@ -986,6 +1206,8 @@ def run_sweep_processes(args):
 
 def main():
     args = parse_args()
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, os.environ.get("TRAFFIC_COMMAND", ""))
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep and args.sweep_processes > 1:

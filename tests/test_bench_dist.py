@@ -137,3 +137,33 @@ def test_reference_arm_prints_one_contract_line():
     assert cpu["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_ncu_csv_parsing_scales_units(tmp_path):
+    """bench.py --record-traffic reads an ncu --csv log: rows grouped per launch in capture order,
+    values scaled by their unit, non-CSV lines skipped."""
+    bench = load_bench()
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+           '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+           '"Metric Value"')
+    rows = [
+        ("0", "dram__bytes_read.sum", "Gbyte", "1.03"),
+        ("0", "dram__bytes_write.sum", "Mbyte", "124.50"),
+        ("0", "gpu__time_duration.sum", "ns", "612500"),
+        ("1", "dram__bytes_read.sum", "Mbyte", "743.00"),
+        ("1", "dram__bytes_write.sum", "Gbyte", "0.45"),
+        ("1", "gpu__time_duration.sum", "msecond", "1.03"),
+    ]
+    lines = ["==PROF== Connected to process", hdr]
+    for i, name, unit, val in rows:
+        lines.append(f'"{i}","1","python","h","gemm_ws_kernel","1","7","(192, 1, 1)","(152, 1, 1)",'
+                     f'"0","10.3","Command line profiler metrics","{name}","{unit}","{val}"')
+    p = tmp_path / "l.csv"
+    p.write_text("\n".join(lines) + "\n")
+    got = bench.parse_ncu_csv(str(p))
+    assert len(got) == 2 and got[0]["kernel"] == "gemm_ws_kernel"
+    assert got[0]["metrics"]["dram__bytes_read.sum"] == pytest.approx(1.03e9)
+    assert got[0]["metrics"]["dram__bytes_write.sum"] == pytest.approx(124.5e6)
+    assert got[1]["metrics"]["gpu__time_duration.sum"] == pytest.approx(1.03e-3)
+    assert got[0]["metrics"]["gpu__time_duration.sum"] == pytest.approx(612.5e-6)
+    assert got[1]["metrics"]["dram__bytes_write.sum"] == pytest.approx(0.45e9)
