@@ -73,6 +73,10 @@ def parse_args():
     p.add_argument("--gdn-min-ms", type=float, default=5.0,
                    help="time at least this many milliseconds of calls per Gated Delta Net "
                         "scenario (0: exactly --gdn-reps calls)")
+    p.add_argument("--gdn-scan", default="auto", choices=["auto", "tensor_core", "mma_sync"],
+                   help="scan kernel of the Gated Delta Net leg")
+    p.add_argument("--gdn-only", action="store_true",
+                   help="run only the Gated Delta Net leg and print its JSON")
     p.add_argument("--sweep-mx", action="store_true",
                    help="in --sweep, time the block-scaled FP8 workloads instead")
     p.add_argument("--config-ms", type=float, default=200.0,
@@ -507,6 +511,8 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
     import torch
     from blackwell_tensor_core_fp16_gb300.workloads import GDN_ORDER, GDN_WORKLOADS, \
         gdn_workload_inputs
+    if g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS[args.gdn_scan]) != g.GDN_OK:
+        raise g.GemmError(1, g.gdn_last_error())
     out = {}
     for name in GDN_ORDER:
         w = GDN_WORKLOADS[name]
@@ -565,8 +571,10 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
                 "note": "achieved = the token recurrence's 6*T*h_v*dk*dv flops / call time against "
                         "the measured dense bf16 peak; the call is latency-bound by the chunk "
                         "chain (about 2.2 us per 64-token step of a sequence)"}
+    g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS["auto"])
     return {"metric": "Gated Delta Net prefill: ms per call (bf16 q/k/v, head dim 128)",
-            "unit": "ms", "higher_is_better": False, "min_reps": args.gdn_reps,
+            "unit": "ms", "higher_is_better": False, "scan_kernel": args.gdn_scan,
+            "min_reps": args.gdn_reps,
             "min_timed_ms": args.gdn_min_ms,
             "scenarios": out,
             "roofline": roofline,
@@ -735,6 +743,14 @@ def run_ours(args):
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA device")
     torch.cuda.set_device(local)
+    if args.gdn_only:
+        g.build()
+        g.load()
+        dev = torch.device("cuda", local)
+        leg = run_gdn_leg(args, g, dev, torch.cuda.Stream(device=dev),
+                          measured_peaks()[0], measured_hbm_gbs())
+        print(json.dumps(leg), flush=True)
+        return 0
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     g.build()

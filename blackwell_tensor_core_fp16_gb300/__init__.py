@@ -160,6 +160,8 @@ def load():
         lib.gdn_offsets_valid_host.restype = i32
         lib.gdn_set_wait_timeout_ms.argtypes = [u32]
         lib.gdn_set_wait_timeout_ms.restype = i32
+        lib.gdn_set_scan_kernel.argtypes = [i32]
+        lib.gdn_set_scan_kernel.restype = i32
         lib.gdn_set_fault_injection.argtypes = [i32]
         lib.gdn_set_fault_injection.restype = i32
         _lib = lib
@@ -541,6 +543,14 @@ def gdn_offsets_valid_host(cu_seqlens, total_tokens: int) -> bool:
 
 def gdn_set_wait_timeout_ms(ms: int) -> int:
     return load().gdn_set_wait_timeout_ms(ms)
+
+
+GDN_SCAN_KERNELS = {"auto": 0, "tensor_core": 1, "mma_sync": 2}
+
+
+def gdn_set_scan_kernel(kernel: int) -> int:
+    """Scan kernel for later calls: GDN_SCAN_KERNELS (include/gdn.h)."""
+    return load().gdn_set_scan_kernel(kernel)
 
 
 def gdn_set_fault_injection(mode: int) -> int:

@@ -45,6 +45,7 @@
 #include <type_traits>
 
 #include "../../include/gdn.h"
+#include "desc.h"
 #include "gdn_offsets.h"
 #include "ptx.cuh"
 
@@ -58,6 +59,7 @@ constexpr int kMaxDevices = 64;  // device ordinals the per-device set-up covers
 thread_local std::string t_gdn_error;
 std::atomic<uint64_t> g_gdn_wait_ns{2000000000ull};   // limit of one wait for a chunk's loads
 std::atomic<uint32_t> g_gdn_fault{0};                 // testing hook (gdn_set_fault_injection)
+std::atomic<int> g_gdn_scan{GDN_SCAN_AUTO};           // scan kernel (gdn_set_scan_kernel)
 
 int gdn_fail(int code, const char* fmt, ...)
 {
@@ -1061,6 +1063,530 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     }
 }
 
+// ---- the same scan with its chunk products on the fifth-generation tensor cores -------------------
+// One CTA per work item (sequence, value head, block of 16 state rows), as gdn_scan_kernel; the
+// chunk's operands arrive by TMA into the same double-buffered stages (the q rows beside the W
+// pieces, see below).  Every product is one tcgen05.mma stream issued by one thread, reading its
+// operands from shared memory and accumulating in tensor memory, with the fp32 pieces stacked
+// along M and N so that each shared-memory tile is read once per product:
+//   P1   D_a = [W0; W1] [S0; S1; S2]^T      (M 128: tokens of pieces 0 and 1; N 48; K 128)
+//        D_b = [W2; Q ] [S0; S1; S2]^T      (M 128: tokens of piece 2 and of q)
+//        U   = W0 (S0 + S1 + S2) + W1 (S0 + S1) + W2 S0     (the six terms of order <= 2)
+//        P   = Q (S0 + S1 + S2)
+//   P2   D_2 = K^T [U~0; U~1; U~2]^T        (M 128: key columns; N 48; K 64 tokens; K^T read
+//                                           MN-major straight from the q/k tile)
+//        S_next = g_C S + (the three column blocks of D_2)
+//   P3   D_3 = [A'0; A'1] [U~0; U~1]^T      (M 128; N 32; K 64)
+//        O   = scale (g P + A'0 (U~0 + U~1) + A'1 U~0)
+// Precision as in gdn_scan_kernel (three bfloat16 pieces per fp32 operand, the terms of order
+// <= 2), with the pieces cut by truncation, which makes x0 + x1 + x2 = x exact.
+// The state S (fp32, 16 rows x 128 columns) lives in registers: thread (lane quarter lq, half h)
+// holds rows 8h .. 8h + 7 of column 32 lq + lane; its three bfloat16 pieces are written to shared
+// memory in the K-major layout P1 reads.  Every epilogue is spread over all eight warps.  P3
+// commits to its own barrier and a chunk's outputs are finished while the next chunk's P1 runs,
+// so only P1 -> U~ -> P2 -> S sits on the chain from chunk to chunk.
+namespace tc {
+constexpr int kThreads = 256;
+// stage layout (bytes from the stage base; every operand tile 1024-byte aligned, 128-byte
+// swizzle, 128-byte rows): per 64-column half h of the 128 key columns, at h * 32 KB, the rows
+// W0 (64), W1 (64), W2 (64), q (64); then k as two 64-column halves of 64 token rows; then the
+// A' pieces (128 rows of 64 tokens)
+constexpr uint32_t kHalf = 32768;
+constexpr uint32_t kOffW2 = 16384;     // [W2; q] inside a half
+constexpr uint32_t kOffQ = 24576;
+constexpr uint32_t kOffK = 65536;
+constexpr uint32_t kOffA = 81920;
+constexpr uint32_t kStage = 98304;
+constexpr uint32_t kOffUp = 2 * kStage;                    // U'^T rows [stage][16][64] f32
+constexpr uint32_t kOffG = kOffUp + 2 * kRows * kC * 4;    // [stage][g_t | g_C / g_t] f32
+constexpr uint32_t kOffB1 = kOffG + 2 * 2 * kC * 4;        // state pieces: 48 x 128 bf16
+constexpr uint32_t kOffB2 = kOffB1 + 2 * 48 * 128;         // U~ pieces: 48 x 64 bf16
+constexpr uint32_t kOffX = kOffB2 + 48 * 128;              // exchange [64][16] f32
+constexpr uint32_t kOffBar = kOffX + kC * kRows * 4;       // 2 stage + 3 MMA barriers
+constexpr uint32_t kOffSlot = kOffBar + 5 * 8;             // TMEM base address
+constexpr uint32_t kOffItem = kOffSlot + 4;                // the CTA's next item
+constexpr size_t kSmem = kOffItem + 4 + 1024;
+static_assert(kOffB1 % 1024 == 0 && kOffB2 % 1024 == 0, "operand tiles");
+static_assert(kSmem <= 232448, "tcgen05 scan shared memory");
+constexpr uint32_t kStageTx = kStage + kRows * kC * 4 + 2 * kC * 4;   // bytes per chunk
+// tensor-memory columns: D_a, D_b, D_2 (48 each), D_3 (32)
+constexpr uint32_t kColA = 0, kColB = 48, kCol2 = 96, kCol3 = 144, kCols = 256;
+
+// The state pieces (B of P1: N = 48 rows n = 16 p + r, K = 128 key columns) and the U~ pieces
+// (B of P2 and P3: N = 48, K = 64 tokens) are MN-major tiles without swizzle: 8 x 8 core matrices
+// of 128 contiguous bytes (8 K rows of 8 consecutive n), core matrices kSbo = 128 bytes apart
+// along N and kLbo = 6 x 128 bytes apart along K.  A thread holding 8 consecutive rows n of one
+// K index writes them as one 16-byte store.
+constexpr uint32_t kSbo = 128, kLbo = 6 * 128;
+__device__ __forceinline__ uint32_t piece_off(int n, int k)
+{
+    return static_cast<uint32_t>((n >> 3) * kSbo + (k >> 3) * kLbo + (k & 7) * 16 + (n & 7) * 2);
+}
+// Shared-memory descriptor of such a tile (no swizzle: layout field 0).
+__device__ __forceinline__ uint64_t desc_mn_none(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((kLbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((kSbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+// Pieces of 8 values as three 16-byte rows of bfloat16 (value e in element e).  The split is by
+// truncation: x0 keeps the sign, exponent and top 7 mantissa bits of x (the low 16 bits of its
+// fp32 pattern cleared), x - x0 is exact in fp32, x1 is its truncation the same way and
+// x2 = x - x0 - x1 has at most 8 significant bits, so x0 + x1 + x2 = x exactly (for normal
+// values whose pieces stay normal) with |x1| < 2^-7 |x| and |x2| < 2^-15 |x|.  The high halves
+// of two fp32 patterns make one bfloat16x2 word (byte permute).
+__device__ __forceinline__ void store_pieces8(uint32_t addr0, uint32_t piece_stride,
+                                              const float (&v)[8])
+{
+    uint32_t w[3][4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+        uint32_t p[2][3];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float x = v[e + h];
+            const uint32_t x0 = __float_as_uint(x) & 0xFFFF0000u;
+            const float r1 = x - __uint_as_float(x0);
+            const uint32_t x1 = __float_as_uint(r1) & 0xFFFF0000u;
+            const float r2 = r1 - __uint_as_float(x1);
+            p[h][0] = x0;
+            p[h][1] = x1;
+            p[h][2] = __float_as_uint(r2);
+        }
+#pragma unroll
+        for (int pc = 0; pc < 3; ++pc) w[pc][e / 2] = __byte_perm(p[0][pc], p[1][pc], 0x7632);
+    }
+#pragma unroll
+    for (int pc = 0; pc < 3; ++pc)
+        gf16::st_shared_v4(addr0 + pc * piece_stride, w[pc][0], w[pc][1], w[pc][2], w[pc][3]);
+}
+// 8 consecutive 32-bit columns of the thread's own TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+// Shared-memory descriptor of an MN-major operand with the 128-byte swizzle: 64 MN elements per
+// 128-byte row, 8 K rows per 1024-byte atom (SBO between atoms along K), atoms along MN LBO apart.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// One thread: announce the chunk's bytes on the stage barrier and start its loads.
+__device__ __forceinline__ void issue(uint32_t base, int s, uint32_t bar, const CUtensorMap* map_w,
+                                      const CUtensorMap* map_a, const CUtensorMap* map_q,
+                                      const CUtensorMap* map_k, const float* __restrict__ ut,
+                                      const float* __restrict__ gam, int64_t cj, int32_t r0,
+                                      int32_t t0, int32_t jq, int32_t jk)
+{
+    gf16::mbar_arrive_expect_tx(bar, kStageTx);
+    const uint32_t st = base + s * kStage;
+    const int32_t yw = static_cast<int32_t>(cj * 3 * kC), ya = static_cast<int32_t>(cj * 2 * kC);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        gf16::tma_load_2d(st + h * kHalf, map_w, bar, 64 * h, yw);            // W0, W1, W2
+        gf16::tma_load_3d(st + h * kHalf + kOffQ, map_q, bar, 64 * h, jq, t0);
+        gf16::tma_load_3d(st + kOffK + h * kC * 128, map_k, bar, 64 * h, jk, t0);
+    }
+    gf16::tma_load_2d(st + kOffA, map_a, bar, 0, ya);
+    bulk_g2s(base + kOffUp + s * kRows * kC * 4, ut + (cj * kD + r0) * kC, kRows * kC * 4, bar);
+    bulk_g2s(base + kOffG + s * 2 * kC * 4, gam + cj * 2 * kC, 2 * kC * 4, bar);
+}
+}  // namespace tc
+
+template <bool kMulti>
+__global__ void __launch_bounds__(tc::kThreads, 1)
+    gdn_scan_tc_kernel(const __grid_constant__ CUtensorMap map_w,
+                       const __grid_constant__ CUtensorMap map_a,
+                       const __grid_constant__ CUtensorMap map_q,
+                       const __grid_constant__ CUtensorMap map_k, const int32_t* __restrict__ order,
+                       const int4* __restrict__ seqinfo, uint32_t* __restrict__ counter,
+                       int32_t n_items, const float* __restrict__ ut,
+                       const float* __restrict__ gam, const float* __restrict__ s0,
+                       float* __restrict__ s_final, __nv_bfloat16* __restrict__ o,
+                       uint32_t* __restrict__ status, int32_t h_v, int32_t qgroup, int32_t kgroup,
+                       int32_t o_tok, int32_t o_hmul, float scale,
+                       uint64_t wait_ns, uint32_t fault, int32_t single_T,
+                       const int32_t* __restrict__ cu)
+{
+    extern __shared__ __align__(16) uint8_t smraw[];
+    const uint32_t raw = smem_u32(smraw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smraw + (base - raw);
+    const float* upf = reinterpret_cast<const float*>(gbase + tc::kOffUp);
+    const float* gf = reinterpret_cast<const float*>(gbase + tc::kOffG);
+    float* xch = reinterpret_cast<float*>(gbase + tc::kOffX);   // [16 rows][64 tokens]
+    volatile int32_t* next_item = reinterpret_cast<volatile int32_t*>(gbase + tc::kOffItem);
+    const uint32_t b1_s = base + tc::kOffB1, b2_s = base + tc::kOffB2;
+    const uint32_t bar_full = base + tc::kOffBar, bar_p1 = bar_full + 16, bar_p2 = bar_full + 24,
+                   bar_p3 = bar_full + 32;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    // Thread roles.  Tensor-memory lane quarter lq = warp % 4 holds rows 32 lq .. + 31 of every
+    // accumulator; the two warps of a quarter split the 16 state rows, rh = 8 (warp / 4) .. + 7.
+    //   quarters 0-1: the W0 / W2 rows of P1, i.e. token t = 32 lq + lane: U, then U~
+    //   quarters 2-3: the W1 / q rows, token t = 32 (lq - 2) + lane: the W1 partial of U, P, O
+    //   every quarter in P2: key column c = 32 lq + lane: the state S[rh .. rh + 7][c]
+    const int lq = warp & 3, rh = 8 * (warp >> 2);
+    const int t_lo = 32 * lq + lane;          // token of quarters 0-1
+    const int t_hi = 32 * (lq - 2) + lane;    // token of quarters 2-3
+    const int c_me = 32 * lq + lane;          // key column in P2
+
+    if (tid == 0) {
+        gf16::mbar_init(bar_full, 1);
+        gf16::mbar_init(bar_full + 8, 1);
+        gf16::mbar_init(bar_p1, 1);
+        gf16::mbar_init(bar_p2, 1);
+        gf16::mbar_init(bar_p3, 1);
+        gf16::fence_mbarrier_init();
+    }
+    if (warp == 0) {
+        gf16::tmem_alloc<1>(base + tc::kOffSlot, tc::kCols);
+        gf16::tmem_relinquish<1>();
+    }
+
+    // Work items as in gdn_scan_kernel: item q -> rank q / (8 h_v), head (q / 8) % h_v, rows
+    // 16 (q % 8) ...; CTA b starts with item b and draws each later one from `counter`.
+    struct Item {
+        int32_t i, j, r0, c_begin, c_end, seq_start, seq_end;
+    };
+    const bool single_ok = single_T < 0 || gdn::offsets_single_ok(cu[0], cu[1], single_T);
+    const auto decode = [&](int32_t q) {
+        Item it;
+        const int32_t rank = q / (8 * h_v), rem = q - rank * 8 * h_v;
+        it.j = rem >> 3;
+        it.r0 = (rem & 7) * kRows;
+        if (single_T >= 0) {
+            it.i = 0;
+            it.c_begin = 0;
+            it.c_end = single_ok ? (single_T + kC - 1) / kC : 0;
+            it.seq_start = 0;
+            it.seq_end = single_ok ? single_T : 0;
+        } else {
+            it.i = order[rank];
+            const int4 si = seqinfo[rank];
+            it.c_begin = si.x;
+            it.c_end = si.y;
+            it.seq_start = si.z;
+            it.seq_end = si.w;
+        }
+        return it;
+    };
+
+    // instruction descriptors: bf16 x bf16 -> f32, M 128; shared-memory descriptors of the fixed
+    // tiles (the stage tiles add the stage's offset): a K step adds its byte offset / 16
+    // (every B is MN-major: bit 16; P2's A, K^T from the k tile, too: bit 15)
+    const uint32_t id48 = gf16::make_idesc_f16(128, 48, 1) | (1u << 16);
+    const uint32_t id32 = gf16::make_idesc_f16(128, 32, 1) | (1u << 16);
+    const uint32_t id48_mn = id48 | (1u << 15);
+    const uint64_t d_b1 = tc::desc_mn_none(b1_s);
+    const uint64_t d_b2 = tc::desc_mn_none(b2_s);
+    // a K step of 16 covers two core matrices along K
+    constexpr uint32_t kStepB = (2 * tc::kLbo) >> 4;
+
+    const int32_t G = static_cast<int32_t>(gridDim.x);
+    const bool draws = kMulti && n_items > G;
+    grid_dep_launch();
+    if (single_T < 0) grid_dep_wait();   // order and seqinfo, for the first item
+    Item it = decode(blockIdx.x);
+    if (tid == 0 && it.c_begin < it.c_end) {
+        gf16::prefetch_tensormap(&map_w);
+        gf16::prefetch_tensormap(&map_a);
+        gf16::prefetch_tensormap(&map_q);
+        gf16::prefetch_tensormap(&map_k);
+    }
+    gf16::tcgen05_fence_before();
+    __syncthreads();
+    gf16::tcgen05_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + tc::kOffSlot);
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * lq) << 16);   // this quarter's lanes
+
+    // S[rh + e][c_me], e < 8: this thread's part of the state, fp32, chunk to chunk
+    float S[8];
+    const auto store_state = [&]() {
+        tc::store_pieces8(b1_s + tc::piece_off(rh, c_me), 2 * tc::kSbo, S);
+        gf16::fence_proxy_async_smem();
+    };
+    // Outputs of a chunk are finished during the next chunk's P1 (or after an item's last
+    // chunk): quarters 2-3 keep their P = Q S^T rows and the decays g_t until then.
+    float P[8];
+    float pend_g = 0.f;
+    int32_t pend_t0 = 0, pend_len = 0, pend_j = 0, pend_r0 = 0;
+    bool pend = false;
+    uint32_t pend_par = 0;
+    bool failed = false;
+    // O = scale (g P + A'0 (U~0 + U~1) + A'1 U~0) of the pending chunk: quarters 0-1 pass the
+    // A'0 sums through xch; quarters 2-3 add their A'1 U~0 and write o.  Ends with the block's
+    // barrier (xch is free again).
+    const auto flush_output = [&]() {
+        failed |= !gf16::mbar_wait(bar_p3, pend_par, nullptr, wait_ns);
+        gf16::tcgen05_fence_after();
+        uint32_t x[8], y[8];
+        if (lq < 2) {
+            tc::tmem_ld8(tl + tc::kCol3 + rh, x);
+            tc::tmem_ld8(tl + tc::kCol3 + 16 + rh, y);
+            gf16::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                xch[(rh + e) * kC + t_lo] = __uint_as_float(x[e]) + __uint_as_float(y[e]);
+        } else {
+            tc::tmem_ld8(tl + tc::kCol3 + rh, x);
+            gf16::tmem_ld_wait();
+        }
+        gf16::tcgen05_fence_before();
+        __syncthreads();
+        if (lq >= 2 && t_hi < pend_len) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2)
+                w[e / 2] = pack_bf16(
+                    scale * fmaf(pend_g, P[e], __uint_as_float(x[e]) + xch[(rh + e) * kC + t_hi]),
+                    scale * fmaf(pend_g, P[e + 1],
+                                 __uint_as_float(x[e + 1]) + xch[(rh + e + 1) * kC + t_hi]));
+            __nv_bfloat16* dst = o + ((static_cast<int64_t>(pend_t0) + t_hi) * o_tok +
+                                      pend_j * o_hmul) * kD + pend_r0 + rh;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        pend = false;
+    };
+
+    uint32_t n = 0;            // chunks this CTA consumed: stage n % 2, barrier phases
+    bool have_first = false;
+    for (int32_t q = blockIdx.x; q < n_items;) {
+        int32_t qn = n_items;
+        Item nx{};
+        const int32_t j = it.j, r0 = it.r0, jq = j / qgroup, jk = j / kgroup;
+        const int32_t c_begin = it.c_begin, c_end = it.c_end;
+        const int32_t seq_start = it.seq_start, seq_end = it.seq_end;
+        const auto chunk_t0 = [&](int32_t ch) { return seq_start + (ch - c_begin) * kC; };
+        const auto cj_of = [&](int32_t ch) { return static_cast<int64_t>(ch) * h_v + j; };
+        const int64_t sbase = ((static_cast<int64_t>(it.i) * h_v + j) * kD + r0) * kD;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) S[e] = s0 ? s0[sbase + (rh + e) * kD + c_me] : 0.f;
+        store_state();
+        if (q == static_cast<int32_t>(blockIdx.x)) grid_dep_wait();
+        uint32_t drawn = 0;
+        if (tid == 0 && draws) drawn = atomicAdd(counter, 1u);
+        __syncthreads();   // state pieces visible
+        if (kMulti && c_begin >= c_end) {   // an empty sequence: only its state passes through
+            if (tid == 0) *next_item = draws ? G + static_cast<int32_t>(drawn) : n_items;
+            __syncthreads();
+            qn = *next_item;
+            if (qn < n_items) nx = decode(qn);
+            __syncthreads();
+        }
+        if (c_begin < c_end && !have_first) {
+            if (tid == 0)
+                tc::issue(base, n & 1, bar_full + 8 * (n & 1), &map_w, &map_a, &map_q, &map_k, ut,
+                          gam, cj_of(c_begin), r0, chunk_t0(c_begin), jq, jk);
+            const bool ok = gf16::mbar_wait(bar_full + 8 * (n & 1), (n >> 1) & 1, nullptr, wait_ns);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
+                failed = true;
+                break;
+            }
+        }
+
+        for (int32_t ch = c_begin; ch < c_end; ++ch) {
+            const int b = n & 1;
+            const uint32_t par = n & 1;   // phase parity of the three MMA barriers
+            const int32_t t0 = chunk_t0(ch);
+            const int32_t len = min(kC, seq_end - t0);
+            // (warp 4 issues the loads, so that warp 0 goes straight to the MMAs)
+            if (tid == 128 && ch + 1 < c_end && !(fault == 1 && ch == c_begin))
+                tc::issue(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut,
+                          gam, cj_of(ch + 1), r0, chunk_t0(ch + 1), jq, jk);
+            const uint32_t sb = base + b * tc::kStage;
+            const float* Bup = upf + b * kRows * kC;
+            const float* Bg = gf + b * 2 * kC;
+
+            // ---- P1: D_a = [W0; W1] [S0; S1; S2]^T, D_b = [W2; q] [S0; S1; S2]^T ----
+            if (warp == 0) {
+                if (gf16::elect_one_sync()) {
+                    gf16::tcgen05_fence_after();
+                    const uint64_t d_st = gf16::make_smem_desc_sw128(sb, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t ka = ((kk >> 2) * tc::kHalf + (kk & 3) * 32) >> 4;
+                        const uint32_t kb = kk * kStepB;
+                        gf16::mma_f16<1>(tmem + tc::kColA, d_st + ka, d_b1 + kb, id48, kk > 0);
+                        gf16::mma_f16<1>(tmem + tc::kColB, d_st + ka + (tc::kOffW2 >> 4),
+                                         d_b1 + kb, id48, kk > 0);
+                    }
+                    gf16::mma_commit(bar_p1);
+                }
+                __syncwarp();
+            }
+            // the previous chunk's outputs, while P1 runs
+            if (pend) flush_output();
+
+            // ---- epilogue 1 ----
+            float u[8];
+            failed |= !gf16::mbar_wait(bar_p1, par, nullptr, wait_ns);
+            gf16::tcgen05_fence_after();
+            if (lq < 2) {   // U partial: W0 (S0 + S1 + S2) + W2 S0 for token t_lo
+                uint32_t x[8], y[8], z[8], w[8];
+                tc::tmem_ld8(tl + tc::kColA + rh, x);
+                tc::tmem_ld8(tl + tc::kColA + 16 + rh, y);
+                tc::tmem_ld8(tl + tc::kColA + 32 + rh, z);
+                tc::tmem_ld8(tl + tc::kColB + rh, w);
+                gf16::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    u[e] = (__uint_as_float(x[e]) + __uint_as_float(y[e])) +
+                           (__uint_as_float(z[e]) + __uint_as_float(w[e]));
+            } else {        // W1 (S0 + S1) for token t_hi into xch; P = q (S0 + S1 + S2)
+                uint32_t x[8], y[8], z[8], w[8], v[8];
+                tc::tmem_ld8(tl + tc::kColA + rh, x);
+                tc::tmem_ld8(tl + tc::kColA + 16 + rh, y);
+                tc::tmem_ld8(tl + tc::kColB + rh, z);
+                tc::tmem_ld8(tl + tc::kColB + 16 + rh, w);
+                tc::tmem_ld8(tl + tc::kColB + 32 + rh, v);
+                gf16::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    xch[(rh + e) * kC + t_hi] = __uint_as_float(x[e]) + __uint_as_float(y[e]);
+                    P[e] = __uint_as_float(z[e]) + (__uint_as_float(w[e]) + __uint_as_float(v[e]));
+                }
+                pend_g = Bg[t_hi];
+            }
+            if (kMulti && tid == 0 && ch == c_begin)
+                *next_item = draws ? G + static_cast<int32_t>(drawn) : n_items;
+            gf16::tcgen05_fence_before();
+            if (__syncthreads_or(failed)) {   // W1 partials ready (and the next item)
+                // an MMA wait ran out: report, let the next chunk's loads (if issued) land, stop
+                failed = true;
+                if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
+                if (tid == 128 && ch + 1 < c_end && !(fault == 1 && ch == c_begin))
+                    gf16::mbar_wait(bar_full + 8 * (b ^ 1), ((n + 1) >> 1) & 1, nullptr, wait_ns);
+                break;
+            }
+            if (kMulti && ch == c_begin) {
+                qn = *next_item;
+                if (qn < n_items) nx = decode(qn);
+            }
+            if (lq < 2) {   // U~ = (g_C / g_t)(U' - U) -> pieces [16 p + r][t]
+                // every load first: the stores below are ordered asm statements
+                const float f = Bg[kC + t_lo];
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[e] = Bup[(rh + e) * kC + t_lo] - (u[e] + xch[(rh + e) * kC + t_lo]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] *= f;
+                tc::store_pieces8(b2_s + tc::piece_off(rh, t_lo), 2 * tc::kSbo, v);
+                gf16::fence_proxy_async_smem();
+            }
+            __syncthreads();   // U~ pieces complete; the exchange buffer is free again
+            // ---- P2 (state) and P3 (outputs) ----
+            if (warp == 0) {
+                if (gf16::elect_one_sync()) {
+                    gf16::tcgen05_fence_after();
+                    const uint64_t d_k = tc::desc_mn_sw128(sb + tc::kOffK, kC * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        gf16::mma_f16<1>(tmem + tc::kCol2, d_k + ((kk * 2048) >> 4),
+                                         d_b2 + kk * kStepB, id48_mn, kk > 0);
+                    gf16::mma_commit(bar_p2);
+                }
+                __syncwarp();
+            }
+            // the last chunk: the next item's first chunk goes into the other stage now
+            if (kMulti && tid == 128 && ch + 1 == c_end && qn < n_items && nx.c_begin < nx.c_end)
+                tc::issue(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut,
+                          gam, static_cast<int64_t>(nx.c_begin) * h_v + nx.j, nx.r0, nx.seq_start,
+                          nx.j / qgroup, nx.j / kgroup);
+            {   // ---- epilogue 2: S_next = g_C S + K^T U~ ----
+                failed |= !gf16::mbar_wait(bar_p2, par, nullptr, wait_ns);
+                gf16::tcgen05_fence_after();
+                // P3 (outputs) behind P2 in the tensor pipe: issued by warp 4 once P2 is done, so
+                // warp 0 goes on to its part of the state at once
+                if (warp == 4) {
+                    if (gf16::elect_one_sync()) {
+                        const uint64_t d_a = gf16::make_smem_desc_sw128(sb + tc::kOffA, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            gf16::mma_f16<1>(tmem + tc::kCol3, d_a + ((kk * 32) >> 4),
+                                             d_b2 + kk * kStepB, id32, kk > 0);
+                        gf16::mma_commit(bar_p3);
+                    }
+                    __syncwarp();
+                }
+                uint32_t x[8], y[8], z[8];
+                tc::tmem_ld8(tl + tc::kCol2 + rh, x);
+                tc::tmem_ld8(tl + tc::kCol2 + 16 + rh, y);
+                tc::tmem_ld8(tl + tc::kCol2 + 32 + rh, z);
+                gf16::tmem_ld_wait();
+                const float gc = Bg[kC - 1];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    S[e] = fmaf(gc, S[e], __uint_as_float(x[e]) +
+                                              (__uint_as_float(y[e]) + __uint_as_float(z[e])));
+                store_state();
+            }
+            pend = true;
+            pend_par = par;
+            pend_t0 = t0;
+            pend_len = len;
+            pend_j = j;
+            pend_r0 = r0;
+            gf16::tcgen05_fence_before();
+            {   // state pieces complete, the next chunk landed
+                const bool more =
+                    ch + 1 < c_end || (kMulti && qn < n_items && nx.c_begin < nx.c_end);
+                const bool ok = !more || gf16::mbar_wait(bar_full + 8 * (b ^ 1),
+                                                         ((n + 1) >> 1) & 1, nullptr, wait_ns);
+                failed |= !ok;
+                if (__syncthreads_or(failed)) {
+                    failed = true;
+                    if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
+                    break;
+                }
+            }
+            ++n;
+        }
+        if (failed) break;
+        // the item's last outputs (they would otherwise wait for a chunk of the next item, whose
+        // P1 overwrites nothing they need, but the next item may have none)
+        if (pend) {
+            flush_output();
+            if (__syncthreads_or(failed)) {
+                failed = true;
+                if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
+                break;
+            }
+        }
+        if (s_final)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s_final[sbase + (rh + e) * kD + c_me] = S[e];
+        have_first = c_begin < c_end && qn < n_items && nx.c_begin < nx.c_end;
+        q = qn;
+        it = nx;
+    }
+    // Every MMA this CTA issued has completed before its tensor memory is freed: each commit was
+    // waited on, except, after a timeout, that of a chunk's output product, waited on here.  The
+    // TMA loads in flight after a timeout are those of one stage at most, which the wait that ran
+    // out or the drain above covered.
+    if (pend && tid == 0) gf16::mbar_wait(bar_p3, pend_par, nullptr, wait_ns);
+    gf16::tcgen05_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        gf16::tcgen05_fence_after();
+        gf16::tmem_dealloc<1>(tmem, tc::kCols);
+    }
+}
+
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 // Output heads of the head layout (h_q, h_k, h_v), or -1: h_v a multiple of h_k, and either
@@ -1165,6 +1691,14 @@ int gdn_ensure_smem(int dev)
         e = cudaFuncSetAttribute(gdn_scan_kernel<false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kScanSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gdn_scan_tc_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tc::kSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gdn_scan_tc_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tc::kSmem));
     if (e != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "cudaFuncSetAttribute (dynamic shared memory): %s",
                         cudaGetErrorString(e));
@@ -1258,6 +1792,7 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
     const int32_t single_T = (n_seqs == 1 && total_tokens > 0) ? static_cast<int32_t>(total_tokens)
                                                                 : -1;
     const int64_t n_items = n_seqs * h_v * (kD / kRows);
+    const int scan_kernel = g_gdn_scan.load();
     int dev = 0, sms = 0;
     cudaError_t e = cudaSuccess;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
@@ -1338,10 +1873,16 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
             if (e != cudaSuccess)
                 return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
         }
-        // persistent scan: one CTA per SM (at most one per work item) taking items dynamically
+        // persistent scan: one CTA per SM (at most one per work item) taking items dynamically;
+        // its chunk products on tcgen05 (default) or on mma.sync
         const int64_t ctas = n_items < sms ? n_items : sms;
-        auto* scan = n_items > sms ? gdn_scan_kernel<true> : gdn_scan_kernel<false>;
-        e = gdn_launch(scan, dim3(static_cast<uint32_t>(ctas)), dim3(kScanThreads), kScanSmem,
+        const bool tensor_core = scan_kernel != GDN_SCAN_MMA_SYNC;
+        auto* scan = tensor_core ? (n_items > sms ? gdn_scan_tc_kernel<true>
+                                                  : gdn_scan_tc_kernel<false>)
+                                 : (n_items > sms ? gdn_scan_kernel<true> : gdn_scan_kernel<false>);
+        e = gdn_launch(scan, dim3(static_cast<uint32_t>(ctas)),
+                       dim3(tensor_core ? tc::kThreads : kScanThreads),
+                       tensor_core ? tc::kSmem : kScanSmem,
                        stream, first, map_w, map_a, map_q[gp], map_k,
                        static_cast<const int32_t*>(single_T >= 0 ? nullptr : order),
                        static_cast<const int4*>(single_T >= 0 ? nullptr : seqinfo), counter,
@@ -1430,6 +1971,14 @@ int gdn_set_wait_timeout_ms(uint32_t ms)
 {
     if (ms == 0) return gdn_fail(GDN_ERR_INVALID_ARG, "timeout must be at least 1 ms");
     g_gdn_wait_ns.store(static_cast<uint64_t>(ms) * 1000000ull);
+    return GDN_OK;
+}
+
+int gdn_set_scan_kernel(int kernel)
+{
+    if (kernel < GDN_SCAN_AUTO || kernel > GDN_SCAN_MMA_SYNC)
+        return gdn_fail(GDN_ERR_INVALID_ARG, "unknown scan kernel %d", kernel);
+    g_gdn_scan.store(kernel);
     return GDN_OK;
 }
 

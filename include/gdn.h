@@ -134,6 +134,16 @@ int gdn_offsets_valid_host(const int32_t* cu_seqlens, int64_t n_seqs, int64_t to
  * (ms >= 1; default 2000). */
 int gdn_set_wait_timeout_ms(uint32_t ms);
 
+/* Which kernel runs the scan over each sequence's chunks, for later calls of this process:
+ * GDN_SCAN_AUTO (default) and GDN_SCAN_TENSOR_CORE run its chunk products as tcgen05.mma streams
+ * from shared memory into tensor memory; GDN_SCAN_MMA_SYNC runs them as register-tile mma.sync.
+ * Both compute the same recurrence at the same precision (fp32 operands as three bfloat16
+ * pieces); the switch exists for comparison and measurement. */
+#define GDN_SCAN_AUTO 0
+#define GDN_SCAN_TENSOR_CORE 1
+#define GDN_SCAN_MMA_SYNC 2
+int gdn_set_scan_kernel(int kernel);
+
 /* Testing hook, 0 = off (default).  1: the scan kernels never issue the loads of each sequence's
  * second chunk, so the wait for them runs out (nothing is in flight) and the call reports
  * GDN_ERR_TIMEOUT through gdn_check_status.  For failure-detection tests only. */

@@ -100,7 +100,8 @@ def test_block_scaled_wait_runs_out_and_context_survives(variant):
     assert (np.abs(d - ref) <= oracle.tolerance_mx(ref, ref_abs, K, "f16")).all()
 
 
-def test_gdn_scan_wait_runs_out_and_context_survives():
+@pytest.mark.parametrize("scan", ["tensor_core", "mma_sync"])
+def test_gdn_scan_wait_runs_out_and_context_survives(scan):
     """The Gated Delta Net scan waits on an mbarrier for each chunk's TMA loads.  With
     gdn_set_fault_injection(1) the second chunk's loads are never issued, the 200 ms wait runs
     out, every scan CTA stops cleanly and gdn_check_status reads GDN_ERR_TIMEOUT; the next call
@@ -123,6 +124,7 @@ def test_gdn_scan_wait_runs_out_and_context_survives():
                              o.data_ptr(), sf.data_ptr(), ws.data_ptr(), need, s)
 
     assert int(inp["cu_seqlens"].diff().max()) > 64, "a sequence needs a second chunk"
+    assert g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS[scan]) == g.GDN_OK
     try:
         assert g.gdn_set_wait_timeout_ms(200) == g.GDN_OK
         assert g.gdn_set_fault_injection(1) == g.GDN_OK
@@ -138,3 +140,4 @@ def test_gdn_scan_wait_runs_out_and_context_survives():
     assert g.gdn_check_status(ws.data_ptr(), s) == g.GDN_OK
     assert_parity(inp, o.float().cpu().double().numpy(), sf.cpu().double().numpy(), 0.73,
                   "the call after the timeout")
+    g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS["auto"])

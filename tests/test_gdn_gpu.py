@@ -38,6 +38,14 @@ def cuda_library():
     torch.cuda.init()
 
 
+@pytest.fixture(autouse=True, params=["tensor_core", "mma_sync"])
+def scan_kernel(request, cuda_library):
+    """Every case runs under both scan kernels: the tcgen05 one (the default) and mma.sync."""
+    assert g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS[request.param]) == g.GDN_OK
+    yield request.param
+    g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS["auto"])
+
+
 def run(inp, h_qk, h_v, scale=0.73, want_state=True):
     """gdn_prefill through the C ABI; outputs written into NaN-prefilled buffers."""
     q, k, v = inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda()
