@@ -73,7 +73,8 @@ def parse_args():
     p.add_argument("--gdn-min-ms", type=float, default=5.0,
                    help="time at least this many milliseconds of calls per Gated Delta Net "
                         "scenario (0: exactly --gdn-reps calls)")
-    p.add_argument("--gdn-scan", default="auto", choices=["auto", "tensor_core", "mma_sync"],
+    p.add_argument("--gdn-scan", default="auto",
+                   choices=["auto", "tensor_core", "mma_sync", "tensor_core_16", "tensor_core_32"],
                    help="scan kernel of the Gated Delta Net leg")
     p.add_argument("--gdn-only", action="store_true",
                    help="run only the Gated Delta Net leg and print its JSON")

@@ -545,7 +545,8 @@ def gdn_set_wait_timeout_ms(ms: int) -> int:
     return load().gdn_set_wait_timeout_ms(ms)
 
 
-GDN_SCAN_KERNELS = {"auto": 0, "tensor_core": 1, "mma_sync": 2}
+GDN_SCAN_KERNELS = {"auto": 0, "tensor_core": 1, "mma_sync": 2, "tensor_core_16": 3,
+                    "tensor_core_32": 4}
 
 
 def gdn_set_scan_kernel(kernel: int) -> int:

@@ -1087,48 +1087,71 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 // so only P1 -> U~ -> P2 -> S sits on the chain from chunk to chunk.
 namespace tc {
 constexpr int kThreads = 256;
-// stage layout (bytes from the stage base; every operand tile 1024-byte aligned, 128-byte
-// swizzle, 128-byte rows): per 64-column half h of the 128 key columns, at h * 32 KB, the rows
-// W0 (64), W1 (64), W2 (64), q (64); then k as two 64-column halves of 64 token rows; then the
-// A' pieces (128 rows of 64 tokens)
-constexpr uint32_t kHalf = 32768;
-constexpr uint32_t kOffW2 = 16384;     // [W2; q] inside a half
-constexpr uint32_t kOffQ = 24576;
-constexpr uint32_t kOffK = 65536;
-constexpr uint32_t kOffA = 81920;
-constexpr uint32_t kStage = 98304;
-constexpr uint32_t kOffUp = 2 * kStage;                    // U'^T rows [stage][16][64] f32
-constexpr uint32_t kOffG = kOffUp + 2 * kRows * kC * 4;    // [stage][g_t | g_C / g_t] f32
-constexpr uint32_t kOffB1 = kOffG + 2 * 2 * kC * 4;        // state pieces: 48 x 128 bf16
-constexpr uint32_t kOffB2 = kOffB1 + 2 * 48 * 128;         // U~ pieces: 48 x 64 bf16
-constexpr uint32_t kOffX = kOffB2 + 48 * 128;              // exchange [64][16] f32
-constexpr uint32_t kOffBar = kOffX + kC * kRows * 4;       // 2 stage + 3 MMA barriers
-constexpr uint32_t kOffSlot = kOffBar + 5 * 8;             // TMEM base address
-constexpr uint32_t kOffItem = kOffSlot + 4;                // the CTA's next item
-constexpr size_t kSmem = kOffItem + 4 + 1024;
-static_assert(kOffB1 % 1024 == 0 && kOffB2 % 1024 == 0, "operand tiles");
-static_assert(kSmem <= 232448, "tcgen05 scan shared memory");
-constexpr uint32_t kStageTx = kStage + kRows * kC * 4 + 2 * kC * 4;   // bytes per chunk
-// tensor-memory columns: D_a, D_b, D_2 (48 each), D_3 (32)
-constexpr uint32_t kColA = 0, kColB = 48, kCol2 = 96, kCol3 = 144, kCols = 256;
 
-// The state pieces (B of P1: N = 48 rows n = 16 p + r, K = 128 key columns) and the U~ pieces
-// (B of P2 and P3: N = 48, K = 64 tokens) are MN-major tiles without swizzle: 8 x 8 core matrices
-// of 128 contiguous bytes (8 K rows of 8 consecutive n), core matrices kSbo = 128 bytes apart
-// along N and kLbo = 6 x 128 bytes apart along K.  A thread holding 8 consecutive rows n of one
-// K index writes them as one 16-byte store.
-constexpr uint32_t kSbo = 128, kLbo = 6 * 128;
+// Layout of the scan for kR state rows per CTA (16 or 32).  Offsets in bytes from a
+// 1024-byte-aligned base; every operand tile 1024-byte aligned.
+//   stage s (two of them): per 64-column half h of the 128 key columns, at s * kStage + h * 32 KB,
+//     the rows W0 (64), W1 (64), W2 (64), q (64), 128-byte swizzle; with kR = 16 also the k tile
+//     (two 64-column halves of 64 token rows) and the A' pieces (128 rows of 64 tokens)
+//   with kR = 32 the k tile and the A' pieces are single-buffered after the stages, loaded a
+//   chunk ahead as soon as the previous chunk's P2 and P3 have read them (shared memory has no
+//   room for a second copy beside the wider state and U~ pieces)
+//   U'^T rows [stage][kR][64] f32, the decays [stage][g_t | g_C / g_t] f32, the state pieces,
+//   the U~ pieces, the exchange buffer [kR][64] f32, the barriers, the TMEM address, the next item
+template <int kR>
+struct Cfg {
+    static constexpr bool kSingleKA = kR == 32;
+    static constexpr int kRH = kR / 2;                 // state rows per thread
+    static constexpr uint32_t kN1 = 3 * kR;            // N of P1 and P2 (three pieces)
+    static constexpr uint32_t kN3 = 2 * kR;            // N of P3 (two pieces)
+    static constexpr uint32_t kHalf = 32768;
+    static constexpr uint32_t kOffW2 = 16384;          // [W2; q] inside a half
+    static constexpr uint32_t kOffQ = 24576;
+    static constexpr uint32_t kStage = kSingleKA ? 65536 : 98304;
+    static constexpr uint32_t kOffK = kSingleKA ? 2 * kStage : 65536;            // in-stage for 16
+    static constexpr uint32_t kOffA = kSingleKA ? 2 * kStage + 16384 : 81920;
+    static constexpr uint32_t kOffUp = kSingleKA ? 2 * kStage + 32768 : 2 * kStage;
+    static constexpr uint32_t kUpBytes = kR * kC * 4;
+    static constexpr uint32_t kOffG = kOffUp + 2 * kUpBytes;
+    static constexpr uint32_t kSbo = 128;                       // between core matrices along N
+    static constexpr uint32_t kLbo = (kN1 / 8) * 128;           // between core matrices along K
+    static constexpr uint32_t kOffB1 = kOffG + 2 * 2 * kC * 4;  // state pieces: kN1 x 128 bf16
+    static constexpr uint32_t kOffB2 = kOffB1 + 16 * kLbo;      // U~ pieces: kN1 x 64 bf16
+    static constexpr uint32_t kOffX = kOffB2 + 8 * kLbo;        // exchange [kR][64] f32
+    static constexpr uint32_t kOffBar = kOffX + kR * kC * 4;    // barriers (7 slots)
+    static constexpr uint32_t kOffSlot = kOffBar + 7 * 8;
+    static constexpr uint32_t kOffItem = kOffSlot + 4;
+    static constexpr size_t kSmem = kOffItem + 4 + 1024;
+    // bytes the stage barrier counts per chunk
+    static constexpr uint32_t kStageTx =
+        2 * (3 * kC * 128 + kC * 128) + (kSingleKA ? 0 : 2 * (2 * kC * 128)) + kUpBytes + 2 * kC * 4;
+    // tensor-memory columns: D_a, D_b, D_2 (kN1 each), D_3 (kN3)
+    static constexpr uint32_t kColA = 0, kColB = kN1, kCol2 = 2 * kN1, kCol3 = 3 * kN1;
+    static constexpr uint32_t kCols = kR == 16 ? 256 : 512;
+    static_assert(kOffB1 % 1024 == 0 && kOffB2 % 1024 == 0, "operand tiles");
+    static_assert(kSmem <= 232448, "tcgen05 scan shared memory");
+    static_assert(kCol3 + kN3 <= kCols, "tensor-memory columns");
+};
+
+// The state pieces (B of P1: N = 3 kR rows n = kR p + r, K = 128 key columns) and the U~ pieces
+// (B of P2 and P3: N = 3 kR or 2 kR, K = 64 tokens) are MN-major tiles without swizzle: 8 x 8
+// core matrices of 128 contiguous bytes (8 K rows of 8 consecutive n), kSbo = 128 bytes apart
+// along N and kLbo = 3 kR / 8 x 128 bytes apart along K.  A thread holding 8 consecutive rows n
+// of one K index writes them as one 16-byte store.
+template <int kR>
 __device__ __forceinline__ uint32_t piece_off(int n, int k)
 {
-    return static_cast<uint32_t>((n >> 3) * kSbo + (k >> 3) * kLbo + (k & 7) * 16 + (n & 7) * 2);
+    return static_cast<uint32_t>((n >> 3) * Cfg<kR>::kSbo + (k >> 3) * Cfg<kR>::kLbo +
+                                 (k & 7) * 16 + (n & 7) * 2);
 }
 // Shared-memory descriptor of such a tile (no swizzle: layout field 0).
+template <int kR>
 __device__ __forceinline__ uint64_t desc_mn_none(uint32_t smem_addr)
 {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>((kLbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((kSbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>((Cfg<kR>::kLbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((Cfg<kR>::kSbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
     return d;
 }
@@ -1139,7 +1162,7 @@ __device__ __forceinline__ uint64_t desc_mn_none(uint32_t smem_addr)
 // values whose pieces stay normal) with |x1| < 2^-7 |x| and |x2| < 2^-15 |x|.  The high halves
 // of two fp32 patterns make one bfloat16x2 word (byte permute).
 __device__ __forceinline__ void store_pieces8(uint32_t addr0, uint32_t piece_stride,
-                                              const float (&v)[8])
+                                              const float* v)
 {
     uint32_t w[3][4];
 #pragma unroll
@@ -1164,12 +1187,19 @@ __device__ __forceinline__ void store_pieces8(uint32_t addr0, uint32_t piece_str
         gf16::st_shared_v4(addr0 + pc * piece_stride, w[pc][0], w[pc][1], w[pc][2], w[pc][3]);
 }
 // 8 consecutive 32-bit columns of the thread's own TMEM lane.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r)
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                    "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr));
+}
+// n consecutive columns (a multiple of 8) of the thread's own TMEM lane.
+template <int n>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[n])
+{
+#pragma unroll
+    for (int i = 0; i < n; i += 8) tmem_ld8(taddr + i, r + i);
 }
 // Shared-memory descriptor of an MN-major operand with the 128-byte swizzle: 64 MN elements per
 // 128-byte row, 8 K rows per 1024-byte atom (SBO between atoms along K), atoms along MN LBO apart.
@@ -1184,29 +1214,49 @@ __device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t smem_addr, uint32_t l
     return d;
 }
 
-// One thread: announce the chunk's bytes on the stage barrier and start its loads.
+// One thread: announce a chunk's stage bytes on the stage barrier and start those loads (W, q,
+// the block's U'^T rows and the decays; with kR = 16 also k and A').
+template <int kR>
 __device__ __forceinline__ void issue(uint32_t base, int s, uint32_t bar, const CUtensorMap* map_w,
                                       const CUtensorMap* map_a, const CUtensorMap* map_q,
                                       const CUtensorMap* map_k, const float* __restrict__ ut,
                                       const float* __restrict__ gam, int64_t cj, int32_t r0,
                                       int32_t t0, int32_t jq, int32_t jk)
 {
-    gf16::mbar_arrive_expect_tx(bar, kStageTx);
-    const uint32_t st = base + s * kStage;
-    const int32_t yw = static_cast<int32_t>(cj * 3 * kC), ya = static_cast<int32_t>(cj * 2 * kC);
+    using C = Cfg<kR>;
+    gf16::mbar_arrive_expect_tx(bar, C::kStageTx);
+    const uint32_t st = base + s * C::kStage;
+    const int32_t yw = static_cast<int32_t>(cj * 3 * kC);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        gf16::tma_load_2d(st + h * kHalf, map_w, bar, 64 * h, yw);            // W0, W1, W2
-        gf16::tma_load_3d(st + h * kHalf + kOffQ, map_q, bar, 64 * h, jq, t0);
-        gf16::tma_load_3d(st + kOffK + h * kC * 128, map_k, bar, 64 * h, jk, t0);
+        gf16::tma_load_2d(st + h * C::kHalf, map_w, bar, 64 * h, yw);            // W0, W1, W2
+        gf16::tma_load_3d(st + h * C::kHalf + C::kOffQ, map_q, bar, 64 * h, jq, t0);
+        if constexpr (!C::kSingleKA)
+            gf16::tma_load_3d(st + C::kOffK + h * kC * 128, map_k, bar, 64 * h, jk, t0);
     }
-    gf16::tma_load_2d(st + kOffA, map_a, bar, 0, ya);
-    bulk_g2s(base + kOffUp + s * kRows * kC * 4, ut + (cj * kD + r0) * kC, kRows * kC * 4, bar);
-    bulk_g2s(base + kOffG + s * 2 * kC * 4, gam + cj * 2 * kC, 2 * kC * 4, bar);
+    if constexpr (!C::kSingleKA)
+        gf16::tma_load_2d(st + C::kOffA, map_a, bar, 0, static_cast<int32_t>(cj * 2 * kC));
+    bulk_g2s(base + C::kOffUp + s * C::kUpBytes, ut + (cj * kD + r0) * kC, C::kUpBytes, bar);
+    bulk_g2s(base + C::kOffG + s * 2 * kC * 4, gam + cj * 2 * kC, 2 * kC * 4, bar);
+}
+// kR = 32: the single-buffered k tile of a chunk (tokens t0 .., key head jk) on `bar`.
+__device__ __forceinline__ void issue_k(uint32_t dst, uint32_t bar, const CUtensorMap* map_k,
+                                        int32_t t0, int32_t jk)
+{
+    gf16::mbar_arrive_expect_tx(bar, 2 * kC * 128);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) gf16::tma_load_3d(dst + h * kC * 128, map_k, bar, 64 * h, jk, t0);
+}
+// kR = 32: the single-buffered A' pieces of chunk cj on `bar`.
+__device__ __forceinline__ void issue_a(uint32_t dst, uint32_t bar, const CUtensorMap* map_a,
+                                        int64_t cj)
+{
+    gf16::mbar_arrive_expect_tx(bar, 2 * kC * 128);
+    gf16::tma_load_2d(dst, map_a, bar, 0, static_cast<int32_t>(cj * 2 * kC));
 }
 }  // namespace tc
 
-template <bool kMulti>
+template <bool kMulti, int kR>
 __global__ void __launch_bounds__(tc::kThreads, 1)
     gdn_scan_tc_kernel(const __grid_constant__ CUtensorMap map_w,
                        const __grid_constant__ CUtensorMap map_a,
@@ -1221,52 +1271,54 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
                        uint64_t wait_ns, uint32_t fault, int32_t single_T,
                        const int32_t* __restrict__ cu)
 {
+    using C = tc::Cfg<kR>;
+    constexpr int RH = C::kRH;                 // state rows per thread
+    constexpr int kBlocks = kD / kR;           // row blocks per head
     extern __shared__ __align__(16) uint8_t smraw[];
     const uint32_t raw = smem_u32(smraw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smraw + (base - raw);
-    const float* upf = reinterpret_cast<const float*>(gbase + tc::kOffUp);
-    const float* gf = reinterpret_cast<const float*>(gbase + tc::kOffG);
-    float* xch = reinterpret_cast<float*>(gbase + tc::kOffX);   // [16 rows][64 tokens]
-    volatile int32_t* next_item = reinterpret_cast<volatile int32_t*>(gbase + tc::kOffItem);
-    const uint32_t b1_s = base + tc::kOffB1, b2_s = base + tc::kOffB2;
-    const uint32_t bar_full = base + tc::kOffBar, bar_p1 = bar_full + 16, bar_p2 = bar_full + 24,
-                   bar_p3 = bar_full + 32;
+    const float* upf = reinterpret_cast<const float*>(gbase + C::kOffUp);
+    const float* gf = reinterpret_cast<const float*>(gbase + C::kOffG);
+    float* xch = reinterpret_cast<float*>(gbase + C::kOffX);   // [kR rows][64 tokens]
+    volatile int32_t* next_item = reinterpret_cast<volatile int32_t*>(gbase + C::kOffItem);
+    const uint32_t b1_s = base + C::kOffB1, b2_s = base + C::kOffB2;
+    // barriers: stage 0, stage 1, P1, P2, P3, and (kR = 32) the k tile and the A' pieces
+    const uint32_t bar_full = base + C::kOffBar, bar_p1 = bar_full + 16, bar_p2 = bar_full + 24,
+                   bar_p3 = bar_full + 32, bar_k = bar_full + 40, bar_a = bar_full + 48;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     // Thread roles.  Tensor-memory lane quarter lq = warp % 4 holds rows 32 lq .. + 31 of every
-    // accumulator; the two warps of a quarter split the 16 state rows, rh = 8 (warp / 4) .. + 7.
+    // accumulator; the two warps of a quarter split the kR state rows, rh = RH (warp / 4) ...
     //   quarters 0-1: the W0 / W2 rows of P1, i.e. token t = 32 lq + lane: U, then U~
     //   quarters 2-3: the W1 / q rows, token t = 32 (lq - 2) + lane: the W1 partial of U, P, O
-    //   every quarter in P2: key column c = 32 lq + lane: the state S[rh .. rh + 7][c]
-    const int lq = warp & 3, rh = 8 * (warp >> 2);
+    //   every quarter in P2: key column c = 32 lq + lane: the state S[rh .. rh + RH - 1][c]
+    const int lq = warp & 3, rh = RH * (warp >> 2);
     const int t_lo = 32 * lq + lane;          // token of quarters 0-1
     const int t_hi = 32 * (lq - 2) + lane;    // token of quarters 2-3
     const int c_me = 32 * lq + lane;          // key column in P2
 
     if (tid == 0) {
-        gf16::mbar_init(bar_full, 1);
-        gf16::mbar_init(bar_full + 8, 1);
-        gf16::mbar_init(bar_p1, 1);
-        gf16::mbar_init(bar_p2, 1);
-        gf16::mbar_init(bar_p3, 1);
+#pragma unroll
+        for (int i = 0; i < 7; ++i) gf16::mbar_init(bar_full + 8 * i, 1);
         gf16::fence_mbarrier_init();
     }
     if (warp == 0) {
-        gf16::tmem_alloc<1>(base + tc::kOffSlot, tc::kCols);
+        gf16::tmem_alloc<1>(base + C::kOffSlot, C::kCols);
         gf16::tmem_relinquish<1>();
     }
 
-    // Work items as in gdn_scan_kernel: item q -> rank q / (8 h_v), head (q / 8) % h_v, rows
-    // 16 (q % 8) ...; CTA b starts with item b and draws each later one from `counter`.
+    // Work items as in gdn_scan_kernel, with kBlocks row blocks of kR rows per head: item q ->
+    // rank q / (kBlocks h_v), head (q / kBlocks) % h_v, rows kR (q % kBlocks) ...; CTA b starts
+    // with item b and draws each later one from `counter`.
     struct Item {
         int32_t i, j, r0, c_begin, c_end, seq_start, seq_end;
     };
     const bool single_ok = single_T < 0 || gdn::offsets_single_ok(cu[0], cu[1], single_T);
     const auto decode = [&](int32_t q) {
         Item it;
-        const int32_t rank = q / (8 * h_v), rem = q - rank * 8 * h_v;
-        it.j = rem >> 3;
-        it.r0 = (rem & 7) * kRows;
+        const int32_t rank = q / (kBlocks * h_v), rem = q - rank * kBlocks * h_v;
+        it.j = rem / kBlocks;
+        it.r0 = (rem % kBlocks) * kR;
         if (single_T >= 0) {
             it.i = 0;
             it.c_begin = 0;
@@ -1284,16 +1336,14 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         return it;
     };
 
-    // instruction descriptors: bf16 x bf16 -> f32, M 128; shared-memory descriptors of the fixed
-    // tiles (the stage tiles add the stage's offset): a K step adds its byte offset / 16
-    // (every B is MN-major: bit 16; P2's A, K^T from the k tile, too: bit 15)
-    const uint32_t id48 = gf16::make_idesc_f16(128, 48, 1) | (1u << 16);
-    const uint32_t id32 = gf16::make_idesc_f16(128, 32, 1) | (1u << 16);
-    const uint32_t id48_mn = id48 | (1u << 15);
-    const uint64_t d_b1 = tc::desc_mn_none(b1_s);
-    const uint64_t d_b2 = tc::desc_mn_none(b2_s);
-    // a K step of 16 covers two core matrices along K
-    constexpr uint32_t kStepB = (2 * tc::kLbo) >> 4;
+    // instruction descriptors: bf16 x bf16 -> f32, M 128; every B is MN-major (bit 16), P2's A
+    // (K^T from the k tile) too (bit 15)
+    const uint32_t id1 = gf16::make_idesc_f16(128, C::kN1, 1) | (1u << 16);
+    const uint32_t id3 = gf16::make_idesc_f16(128, C::kN3, 1) | (1u << 16);
+    const uint32_t id1_mn = id1 | (1u << 15);
+    const uint64_t d_b1 = tc::desc_mn_none<kR>(b1_s);
+    const uint64_t d_b2 = tc::desc_mn_none<kR>(b2_s);
+    constexpr uint32_t kStepB = (2 * C::kLbo) >> 4;   // a K step of 16: two core matrices
 
     const int32_t G = static_cast<int32_t>(gridDim.x);
     const bool draws = kMulti && n_items > G;
@@ -1309,56 +1359,73 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     gf16::tcgen05_fence_before();
     __syncthreads();
     gf16::tcgen05_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + tc::kOffSlot);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + C::kOffSlot);
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * lq) << 16);   // this quarter's lanes
 
-    // S[rh + e][c_me], e < 8: this thread's part of the state, fp32, chunk to chunk
-    float S[8];
+    // S[rh + e][c_me], e < RH: this thread's part of the state, fp32, chunk to chunk
+    float S[RH];
     const auto store_state = [&]() {
-        tc::store_pieces8(b1_s + tc::piece_off(rh, c_me), 2 * tc::kSbo, S);
+#pragma unroll
+        for (int e = 0; e < RH; e += 8)
+            tc::store_pieces8(b1_s + tc::piece_off<kR>(rh + e, c_me), (kR / 8) * C::kSbo, S + e);
         gf16::fence_proxy_async_smem();
     };
     // Outputs of a chunk are finished during the next chunk's P1 (or after an item's last
     // chunk): quarters 2-3 keep their P = Q S^T rows and the decays g_t until then.
-    float P[8];
+    float P[RH];
     float pend_g = 0.f;
     int32_t pend_t0 = 0, pend_len = 0, pend_j = 0, pend_r0 = 0;
     bool pend = false;
     uint32_t pend_par = 0;
     bool failed = false;
+    // kR = 32: loads of the single-buffered k / A' tiles issued and not yet consumed (their
+    // barriers complete once per chunk, in order, so the parity of the next completion is the
+    // number of completions so far, mod 2)
+    uint32_t k_issued = 0, a_issued = 0, k_done = 0, a_done = 0;
+    const auto issue_k = [&](int32_t t0_, int32_t jk_) {
+        if (tid == 128) tc::issue_k(base + C::kOffK, bar_k, &map_k, t0_, jk_);
+        ++k_issued;
+    };
+    const auto issue_a = [&](int64_t cj_) {
+        if (tid == 128) tc::issue_a(base + C::kOffA, bar_a, &map_a, cj_);
+        ++a_issued;
+    };
     // O = scale (g P + A'0 (U~0 + U~1) + A'1 U~0) of the pending chunk: quarters 0-1 pass the
-    // A'0 sums through xch; quarters 2-3 add their A'1 U~0 and write o.  Ends with the block's
-    // barrier (xch is free again).
+    // A'0 sums through xch; quarters 2-3 add their A'1 U~0 and write o.
     const auto flush_output = [&]() {
         failed |= !gf16::mbar_wait(bar_p3, pend_par, nullptr, wait_ns);
         gf16::tcgen05_fence_after();
-        uint32_t x[8], y[8];
+        uint32_t x[RH], y[RH];
         if (lq < 2) {
-            tc::tmem_ld8(tl + tc::kCol3 + rh, x);
-            tc::tmem_ld8(tl + tc::kCol3 + 16 + rh, y);
+            tc::tmem_ldn<RH>(tl + C::kCol3 + rh, x);
+            tc::tmem_ldn<RH>(tl + C::kCol3 + kR + rh, y);
             gf16::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
+            for (int e = 0; e < RH; ++e)
                 xch[(rh + e) * kC + t_lo] = __uint_as_float(x[e]) + __uint_as_float(y[e]);
         } else {
-            tc::tmem_ld8(tl + tc::kCol3 + rh, x);
+            tc::tmem_ldn<RH>(tl + C::kCol3 + rh, x);
             gf16::tmem_ld_wait();
         }
         gf16::tcgen05_fence_before();
         __syncthreads();
         if (lq >= 2 && t_hi < pend_len) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 8; e += 2)
-                w[e / 2] = pack_bf16(
-                    scale * fmaf(pend_g, P[e], __uint_as_float(x[e]) + xch[(rh + e) * kC + t_hi]),
-                    scale * fmaf(pend_g, P[e + 1],
-                                 __uint_as_float(x[e + 1]) + xch[(rh + e + 1) * kC + t_hi]));
             __nv_bfloat16* dst = o + ((static_cast<int64_t>(pend_t0) + t_hi) * o_tok +
                                       pend_j * o_hmul) * kD + pend_r0 + rh;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int e0 = 0; e0 < RH; e0 += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = e0; e < e0 + 8; e += 2)
+                    w[(e - e0) / 2] = pack_bf16(
+                        scale * fmaf(pend_g, P[e], __uint_as_float(x[e]) + xch[(rh + e) * kC + t_hi]),
+                        scale * fmaf(pend_g, P[e + 1],
+                                     __uint_as_float(x[e + 1]) + xch[(rh + e + 1) * kC + t_hi]));
+                *reinterpret_cast<uint4*>(dst + e0) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
         pend = false;
+        if constexpr (C::kSingleKA) __syncthreads();   // xch is written again in epilogue 1
     };
 
     uint32_t n = 0;            // chunks this CTA consumed: stage n % 2, barrier phases
@@ -1373,7 +1440,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         const auto cj_of = [&](int32_t ch) { return static_cast<int64_t>(ch) * h_v + j; };
         const int64_t sbase = ((static_cast<int64_t>(it.i) * h_v + j) * kD + r0) * kD;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) S[e] = s0 ? s0[sbase + (rh + e) * kD + c_me] : 0.f;
+        for (int e = 0; e < RH; ++e) S[e] = s0 ? s0[sbase + (rh + e) * kD + c_me] : 0.f;
         store_state();
         if (q == static_cast<int32_t>(blockIdx.x)) grid_dep_wait();
         uint32_t drawn = 0;
@@ -1388,9 +1455,14 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         }
         if (c_begin < c_end && !have_first) {
             if (tid == 0)
-                tc::issue(base, n & 1, bar_full + 8 * (n & 1), &map_w, &map_a, &map_q, &map_k, ut,
-                          gam, cj_of(c_begin), r0, chunk_t0(c_begin), jq, jk);
-            const bool ok = gf16::mbar_wait(bar_full + 8 * (n & 1), (n >> 1) & 1, nullptr, wait_ns);
+                tc::issue<kR>(base, n & 1, bar_full + 8 * (n & 1), &map_w, &map_a, &map_q, &map_k,
+                              ut, gam, cj_of(c_begin), r0, chunk_t0(c_begin), jq, jk);
+            if constexpr (C::kSingleKA) {
+                issue_k(chunk_t0(c_begin), jk);
+                issue_a(cj_of(c_begin));
+            }
+            const bool ok =
+                gf16::mbar_wait(bar_full + 8 * (n & 1), (n >> 1) & 1, nullptr, wait_ns);
             if (__syncthreads_or(!ok)) {
                 if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
                 failed = true;
@@ -1400,16 +1472,19 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
         for (int32_t ch = c_begin; ch < c_end; ++ch) {
             const int b = n & 1;
-            const uint32_t par = n & 1;   // phase parity of the three MMA barriers
+            const uint32_t par = n & 1;   // phase parity of the MMA barriers (and k, A')
             const int32_t t0 = chunk_t0(ch);
             const int32_t len = min(kC, seq_end - t0);
+            const bool next_in_item = ch + 1 < c_end && !(fault == 1 && ch == c_begin);
             // (warp 4 issues the loads, so that warp 0 goes straight to the MMAs)
-            if (tid == 128 && ch + 1 < c_end && !(fault == 1 && ch == c_begin))
-                tc::issue(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut,
-                          gam, cj_of(ch + 1), r0, chunk_t0(ch + 1), jq, jk);
-            const uint32_t sb = base + b * tc::kStage;
-            const float* Bup = upf + b * kRows * kC;
+            if (tid == 128 && next_in_item)
+                tc::issue<kR>(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k,
+                              ut, gam, cj_of(ch + 1), r0, chunk_t0(ch + 1), jq, jk);
+            const uint32_t sb = base + b * C::kStage;
+            const float* Bup = upf + b * (C::kUpBytes / 4);
             const float* Bg = gf + b * 2 * kC;
+            const uint32_t k_tile = C::kSingleKA ? base + C::kOffK : sb + C::kOffK;
+            const uint32_t a_tile = C::kSingleKA ? base + C::kOffA : sb + C::kOffA;
 
             // ---- P1: D_a = [W0; W1] [S0; S1; S2]^T, D_b = [W2; q] [S0; S1; S2]^T ----
             if (warp == 0) {
@@ -1418,57 +1493,108 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
                     const uint64_t d_st = gf16::make_smem_desc_sw128(sb, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t ka = ((kk >> 2) * tc::kHalf + (kk & 3) * 32) >> 4;
+                        const uint32_t ka = ((kk >> 2) * C::kHalf + (kk & 3) * 32) >> 4;
                         const uint32_t kb = kk * kStepB;
-                        gf16::mma_f16<1>(tmem + tc::kColA, d_st + ka, d_b1 + kb, id48, kk > 0);
-                        gf16::mma_f16<1>(tmem + tc::kColB, d_st + ka + (tc::kOffW2 >> 4),
-                                         d_b1 + kb, id48, kk > 0);
+                        gf16::mma_f16<1>(tmem + C::kColA, d_st + ka, d_b1 + kb, id1, kk > 0);
+                        gf16::mma_f16<1>(tmem + C::kColB, d_st + ka + (C::kOffW2 >> 4),
+                                         d_b1 + kb, id1, kk > 0);
                     }
                     gf16::mma_commit(bar_p1);
                 }
                 __syncwarp();
             }
-            // the previous chunk's outputs, while P1 runs
-            if (pend) flush_output();
+            // the previous chunk's outputs, while P1 runs; after them (kR = 32) this chunk's A'
+            // pieces may replace the previous chunk's
+            if (pend) {
+                flush_output();
+                if constexpr (C::kSingleKA) {
+                    if (ch != c_begin) issue_a(cj_of(ch));
+                }
+            }
 
             // ---- epilogue 1 ----
             float u[8];
             failed |= !gf16::mbar_wait(bar_p1, par, nullptr, wait_ns);
             gf16::tcgen05_fence_after();
-            if (lq < 2) {   // U partial: W0 (S0 + S1 + S2) + W2 S0 for token t_lo
-                uint32_t x[8], y[8], z[8], w[8];
-                tc::tmem_ld8(tl + tc::kColA + rh, x);
-                tc::tmem_ld8(tl + tc::kColA + 16 + rh, y);
-                tc::tmem_ld8(tl + tc::kColA + 32 + rh, z);
-                tc::tmem_ld8(tl + tc::kColB + rh, w);
-                gf16::tmem_ld_wait();
+            if constexpr (kR == 16) {
+                // U partial (quarters 0-1): W0 (S0 + S1 + S2) + W2 S0; quarters 2-3 pass
+                // W1 (S0 + S1) through xch and keep P = q (S0 + S1 + S2) for the outputs
+                if (lq < 2) {
+                    uint32_t x[8], y[8], z[8], w[8];
+                    tc::tmem_ld8(tl + C::kColA + rh, x);
+                    tc::tmem_ld8(tl + C::kColA + kR + rh, y);
+                    tc::tmem_ld8(tl + C::kColA + 2 * kR + rh, z);
+                    tc::tmem_ld8(tl + C::kColB + rh, w);
+                    gf16::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    u[e] = (__uint_as_float(x[e]) + __uint_as_float(y[e])) +
-                           (__uint_as_float(z[e]) + __uint_as_float(w[e]));
-            } else {        // W1 (S0 + S1) for token t_hi into xch; P = q (S0 + S1 + S2)
-                uint32_t x[8], y[8], z[8], w[8], v[8];
-                tc::tmem_ld8(tl + tc::kColA + rh, x);
-                tc::tmem_ld8(tl + tc::kColA + 16 + rh, y);
-                tc::tmem_ld8(tl + tc::kColB + rh, z);
-                tc::tmem_ld8(tl + tc::kColB + 16 + rh, w);
-                tc::tmem_ld8(tl + tc::kColB + 32 + rh, v);
-                gf16::tmem_ld_wait();
+                    for (int e = 0; e < 8; ++e)
+                        u[e] = (__uint_as_float(x[e]) + __uint_as_float(y[e])) +
+                               (__uint_as_float(z[e]) + __uint_as_float(w[e]));
+                } else {
+                    uint32_t x[8], y[8], z[8], w[8], v[8];
+                    tc::tmem_ld8(tl + C::kColA + rh, x);
+                    tc::tmem_ld8(tl + C::kColA + kR + rh, y);
+                    tc::tmem_ld8(tl + C::kColB + rh, z);
+                    tc::tmem_ld8(tl + C::kColB + kR + rh, w);
+                    tc::tmem_ld8(tl + C::kColB + 2 * kR + rh, v);
+                    gf16::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    xch[(rh + e) * kC + t_hi] = __uint_as_float(x[e]) + __uint_as_float(y[e]);
-                    P[e] = __uint_as_float(z[e]) + (__uint_as_float(w[e]) + __uint_as_float(v[e]));
+                    for (int e = 0; e < 8; ++e) {
+                        xch[(rh + e) * kC + t_hi] = __uint_as_float(x[e]) + __uint_as_float(y[e]);
+                        P[e] = __uint_as_float(z[e]) +
+                               (__uint_as_float(w[e]) + __uint_as_float(v[e]));
+                    }
+                    pend_g = Bg[t_hi];
                 }
-                pend_g = Bg[t_hi];
+            } else {
+                // 16 rows per thread: quarters 0-1 keep the U partial of rows rh .. rh + 7 and
+                // pass rows rh + 8 .. to quarters 2-3, which pass their W1 partial of rows
+                // rh .. rh + 7 back; each side then finishes 8 rows of its token
+                if (lq < 2) {
+                    uint32_t x[16], y[16], z[16], w[16];
+                    tc::tmem_ldn<16>(tl + C::kColA + rh, x);
+                    tc::tmem_ldn<16>(tl + C::kColA + kR + rh, y);
+                    tc::tmem_ldn<16>(tl + C::kColA + 2 * kR + rh, z);
+                    tc::tmem_ldn<16>(tl + C::kColB + rh, w);
+                    gf16::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float v = (__uint_as_float(x[e]) + __uint_as_float(y[e])) +
+                                        (__uint_as_float(z[e]) + __uint_as_float(w[e]));
+                        if (e < 8) u[e] = v;
+                        else xch[(rh + e) * kC + t_lo] = v;
+                    }
+                } else {
+                    uint32_t x[16], y[16];
+                    tc::tmem_ldn<16>(tl + C::kColA + rh, x);
+                    tc::tmem_ldn<16>(tl + C::kColA + kR + rh, y);
+                    gf16::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float w1 = __uint_as_float(x[e]) + __uint_as_float(y[e]);
+                        if (e < 8) xch[(rh + e) * kC + t_hi] = w1;
+                        else u[e - 8] = w1;
+                    }
+                    tc::tmem_ldn<16>(tl + C::kColB + rh, x);
+                    tc::tmem_ldn<16>(tl + C::kColB + kR + rh, y);
+                    gf16::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) P[e] = __uint_as_float(x[e]) + __uint_as_float(y[e]);
+                    tc::tmem_ldn<16>(tl + C::kColB + 2 * kR + rh, x);
+                    gf16::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) P[e] += __uint_as_float(x[e]);
+                    pend_g = Bg[t_hi];
+                }
             }
             if (kMulti && tid == 0 && ch == c_begin)
                 *next_item = draws ? G + static_cast<int32_t>(drawn) : n_items;
             gf16::tcgen05_fence_before();
-            if (__syncthreads_or(failed)) {   // W1 partials ready (and the next item)
-                // an MMA wait ran out: report, let the next chunk's loads (if issued) land, stop
+            if (__syncthreads_or(failed)) {   // partials exchanged (and the next item)
+                // an MMA wait ran out: report, let the loads in flight land, stop
                 failed = true;
                 if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
-                if (tid == 128 && ch + 1 < c_end && !(fault == 1 && ch == c_begin))
+                if (tid == 128 && next_in_item)
                     gf16::mbar_wait(bar_full + 8 * (b ^ 1), ((n + 1) >> 1) & 1, nullptr, wait_ns);
                 break;
             }
@@ -1476,61 +1602,92 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
                 qn = *next_item;
                 if (qn < n_items) nx = decode(qn);
             }
-            if (lq < 2) {   // U~ = (g_C / g_t)(U' - U) -> pieces [16 p + r][t]
-                // every load first: the stores below are ordered asm statements
-                const float f = Bg[kC + t_lo];
+            // U~ = (g_C / g_t)(U' - U) -> pieces [kR p + r][t]; every load first: the stores
+            // below are ordered asm statements
+            if constexpr (kR == 16) {
+                if (lq < 2) {
+                    const float f = Bg[kC + t_lo];
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        v[e] = f * (Bup[(rh + e) * kC + t_lo] - (u[e] + xch[(rh + e) * kC + t_lo]));
+                    tc::store_pieces8(b2_s + tc::piece_off<kR>(rh, t_lo), (kR / 8) * C::kSbo, v);
+                    gf16::fence_proxy_async_smem();
+                }
+            } else {
+                const int t = lq < 2 ? t_lo : t_hi;
+                const int r8 = lq < 2 ? rh : rh + 8;
+                const float f = Bg[kC + t];
                 float v[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    v[e] = Bup[(rh + e) * kC + t_lo] - (u[e] + xch[(rh + e) * kC + t_lo]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] *= f;
-                tc::store_pieces8(b2_s + tc::piece_off(rh, t_lo), 2 * tc::kSbo, v);
+                    v[e] = f * (Bup[(r8 + e) * kC + t] - (u[e] + xch[(r8 + e) * kC + t]));
+                tc::store_pieces8(b2_s + tc::piece_off<kR>(r8, t), (kR / 8) * C::kSbo, v);
                 gf16::fence_proxy_async_smem();
             }
             __syncthreads();   // U~ pieces complete; the exchange buffer is free again
-            // ---- P2 (state) and P3 (outputs) ----
+            // ---- P2 (state) ----
+            bool k_ok = true;
             if (warp == 0) {
-                if (gf16::elect_one_sync()) {
+                if constexpr (C::kSingleKA) {   // this chunk's k tile has landed
+                    k_ok = gf16::mbar_wait(bar_k, k_done & 1, nullptr, wait_ns);
+                }
+                if (gf16::elect_one_sync() && k_ok) {
                     gf16::tcgen05_fence_after();
-                    const uint64_t d_k = tc::desc_mn_sw128(sb + tc::kOffK, kC * 128, 1024);
+                    const uint64_t d_k = tc::desc_mn_sw128(k_tile, kC * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        gf16::mma_f16<1>(tmem + tc::kCol2, d_k + ((kk * 2048) >> 4),
-                                         d_b2 + kk * kStepB, id48_mn, kk > 0);
+                        gf16::mma_f16<1>(tmem + C::kCol2, d_k + ((kk * 2048) >> 4),
+                                         d_b2 + kk * kStepB, id1_mn, kk > 0);
                     gf16::mma_commit(bar_p2);
                 }
                 __syncwarp();
             }
+            if constexpr (C::kSingleKA) ++k_done;
+            failed |= !k_ok;
             // the last chunk: the next item's first chunk goes into the other stage now
-            if (kMulti && tid == 128 && ch + 1 == c_end && qn < n_items && nx.c_begin < nx.c_end)
-                tc::issue(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k, ut,
-                          gam, static_cast<int64_t>(nx.c_begin) * h_v + nx.j, nx.r0, nx.seq_start,
-                          nx.j / qgroup, nx.j / kgroup);
+            const bool next_item_first =
+                kMulti && ch + 1 == c_end && qn < n_items && nx.c_begin < nx.c_end;
+            if (tid == 128 && next_item_first)
+                tc::issue<kR>(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k,
+                              ut, gam, static_cast<int64_t>(nx.c_begin) * h_v + nx.j, nx.r0,
+                              nx.seq_start, nx.j / qgroup, nx.j / kgroup);
             {   // ---- epilogue 2: S_next = g_C S + K^T U~ ----
-                failed |= !gf16::mbar_wait(bar_p2, par, nullptr, wait_ns);
+                failed |= !(k_ok && gf16::mbar_wait(bar_p2, par, nullptr, wait_ns));
                 gf16::tcgen05_fence_after();
-                // P3 (outputs) behind P2 in the tensor pipe: issued by warp 4 once P2 is done, so
-                // warp 0 goes on to its part of the state at once
+                // P3 (outputs) behind P2 in the tensor pipe: issued by warp 4 once P2 is done
+                // (and, kR = 32, once this chunk's A' pieces have landed), so warp 0 goes on
+                // to its part of the state at once
                 if (warp == 4) {
-                    if (gf16::elect_one_sync()) {
-                        const uint64_t d_a = gf16::make_smem_desc_sw128(sb + tc::kOffA, 1024);
+                    bool a_ok = true;
+                    if constexpr (C::kSingleKA)
+                        a_ok = gf16::mbar_wait(bar_a, a_done & 1, nullptr, wait_ns);
+                    if (gf16::elect_one_sync() && a_ok) {
+                        const uint64_t d_a = gf16::make_smem_desc_sw128(a_tile, 1024);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            gf16::mma_f16<1>(tmem + tc::kCol3, d_a + ((kk * 32) >> 4),
-                                             d_b2 + kk * kStepB, id32, kk > 0);
+                            gf16::mma_f16<1>(tmem + C::kCol3, d_a + ((kk * 32) >> 4),
+                                             d_b2 + kk * kStepB, id3, kk > 0);
                         gf16::mma_commit(bar_p3);
                     }
                     __syncwarp();
+                    failed |= !a_ok;
                 }
-                uint32_t x[8], y[8], z[8];
-                tc::tmem_ld8(tl + tc::kCol2 + rh, x);
-                tc::tmem_ld8(tl + tc::kCol2 + 16 + rh, y);
-                tc::tmem_ld8(tl + tc::kCol2 + 32 + rh, z);
+                if constexpr (C::kSingleKA) {
+                    ++a_done;
+                    // the k tile is free: the next chunk's (of this item, or the next item's
+                    // first) comes in now
+                    if (next_in_item) issue_k(chunk_t0(ch + 1), jk);
+                    else if (next_item_first) issue_k(nx.seq_start, nx.j / kgroup);
+                }
+                uint32_t x[RH], y[RH], z[RH];
+                tc::tmem_ldn<RH>(tl + C::kCol2 + rh, x);
+                tc::tmem_ldn<RH>(tl + C::kCol2 + kR + rh, y);
+                tc::tmem_ldn<RH>(tl + C::kCol2 + 2 * kR + rh, z);
                 gf16::tmem_ld_wait();
                 const float gc = Bg[kC - 1];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
+                for (int e = 0; e < RH; ++e)
                     S[e] = fmaf(gc, S[e], __uint_as_float(x[e]) +
                                               (__uint_as_float(y[e]) + __uint_as_float(z[e])));
                 store_state();
@@ -1543,8 +1700,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
             pend_r0 = r0;
             gf16::tcgen05_fence_before();
             {   // state pieces complete, the next chunk landed
-                const bool more =
-                    ch + 1 < c_end || (kMulti && qn < n_items && nx.c_begin < nx.c_end);
+                const bool more = ch + 1 < c_end || next_item_first;
                 const bool ok = !more || gf16::mbar_wait(bar_full + 8 * (b ^ 1),
                                                          ((n + 1) >> 1) & 1, nullptr, wait_ns);
                 failed |= !ok;
@@ -1557,10 +1713,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
             ++n;
         }
         if (failed) break;
-        // the item's last outputs (they would otherwise wait for a chunk of the next item, whose
-        // P1 overwrites nothing they need, but the next item may have none)
+        // the item's last outputs (the next item may have no chunk whose P1 they could follow)
         if (pend) {
             flush_output();
+            if constexpr (C::kSingleKA) {   // the next item's first A' pieces may come in now
+                if (kMulti && qn < n_items && nx.c_begin < nx.c_end)
+                    issue_a(static_cast<int64_t>(nx.c_begin) * h_v + nx.j);
+            }
             if (__syncthreads_or(failed)) {
                 failed = true;
                 if (tid == 0) atomicOr(status, gdn::kStatusTimeout);
@@ -1569,7 +1728,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         }
         if (s_final)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s_final[sbase + (rh + e) * kD + c_me] = S[e];
+            for (int e = 0; e < RH; ++e) s_final[sbase + (rh + e) * kD + c_me] = S[e];
         have_first = c_begin < c_end && qn < n_items && nx.c_begin < nx.c_end;
         q = qn;
         it = nx;
@@ -1577,13 +1736,18 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     // Every MMA this CTA issued has completed before its tensor memory is freed: each commit was
     // waited on, except, after a timeout, that of a chunk's output product, waited on here.  The
     // TMA loads in flight after a timeout are those of one stage at most, which the wait that ran
-    // out or the drain above covered.
-    if (pend && tid == 0) gf16::mbar_wait(bar_p3, pend_par, nullptr, wait_ns);
+    // out or the drain above covered, and (kR = 32) k and A' tiles issued but not consumed,
+    // waited on here.
+    if (tid == 0 && pend) gf16::mbar_wait(bar_p3, pend_par, nullptr, wait_ns);
+    if (tid == 128) {
+        if (k_issued > k_done) gf16::mbar_wait(bar_k, k_done & 1, nullptr, wait_ns);
+        if (a_issued > a_done) gf16::mbar_wait(bar_a, a_done & 1, nullptr, wait_ns);
+    }
     gf16::tcgen05_fence_before();
     __syncthreads();
     if (warp == 0) {
         gf16::tcgen05_fence_after();
-        gf16::tmem_dealloc<1>(tmem, tc::kCols);
+        gf16::tmem_dealloc<1>(tmem, C::kCols);
     }
 }
 
@@ -1692,13 +1856,21 @@ int gdn_ensure_smem(int dev)
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kScanSmem));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gdn_scan_tc_kernel<true>,
+        e = cudaFuncSetAttribute(gdn_scan_tc_kernel<true, 16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tc::kSmem));
+                                 static_cast<int>(tc::Cfg<16>::kSmem));
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gdn_scan_tc_kernel<false>,
+        e = cudaFuncSetAttribute(gdn_scan_tc_kernel<false, 16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(tc::kSmem));
+                                 static_cast<int>(tc::Cfg<16>::kSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gdn_scan_tc_kernel<true, 32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tc::Cfg<32>::kSmem));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gdn_scan_tc_kernel<false, 32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(tc::Cfg<32>::kSmem));
     if (e != cudaSuccess)
         return gdn_fail(GDN_ERR_CUDA, "cudaFuncSetAttribute (dynamic shared memory): %s",
                         cudaGetErrorString(e));
@@ -1874,19 +2046,29 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
                 return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
         }
         // persistent scan: one CTA per SM (at most one per work item) taking items dynamically;
-        // its chunk products on tcgen05 (default) or on mma.sync
-        const int64_t ctas = n_items < sms ? n_items : sms;
+        // its chunk products on tcgen05 (default) or on mma.sync.  The tcgen05 scan takes 32
+        // state rows per item (N 96 per MMA, about the cost of N 48) when 16-row items would
+        // give every SM at least eight: it halves the MMAs per row where throughput, not the
+        // length of one chain, sets the time.  With fewer items, 16-row items finish sooner and
+        // balance better (measured: 20 packed sequences x 16 value heads, 17 items per SM, 260
+        // against 325 us; 10 x 8, 4 per SM, 97 against 92 us).
         const bool tensor_core = scan_kernel != GDN_SCAN_MMA_SYNC;
-        auto* scan = tensor_core ? (n_items > sms ? gdn_scan_tc_kernel<true>
-                                                  : gdn_scan_tc_kernel<false>)
-                                 : (n_items > sms ? gdn_scan_kernel<true> : gdn_scan_kernel<false>);
+        const bool wide = tensor_core && scan_kernel != GDN_SCAN_TENSOR_CORE_16 &&
+                          (scan_kernel == GDN_SCAN_TENSOR_CORE_32 || n_items >= 8 * sms);
+        const int64_t items = wide ? n_items / 2 : n_items;
+        const int64_t ctas = items < sms ? items : sms;
+        auto* scan = !tensor_core ? (items > sms ? gdn_scan_kernel<true> : gdn_scan_kernel<false>)
+                     : wide ? (items > sms ? gdn_scan_tc_kernel<true, 32>
+                                           : gdn_scan_tc_kernel<false, 32>)
+                            : (items > sms ? gdn_scan_tc_kernel<true, 16>
+                                           : gdn_scan_tc_kernel<false, 16>);
         e = gdn_launch(scan, dim3(static_cast<uint32_t>(ctas)),
                        dim3(tensor_core ? tc::kThreads : kScanThreads),
-                       tensor_core ? tc::kSmem : kScanSmem,
+                       !tensor_core ? kScanSmem : wide ? tc::Cfg<32>::kSmem : tc::Cfg<16>::kSmem,
                        stream, first, map_w, map_a, map_q[gp], map_k,
                        static_cast<const int32_t*>(single_T >= 0 ? nullptr : order),
                        static_cast<const int4*>(single_T >= 0 ? nullptr : seqinfo), counter,
-                       static_cast<int32_t>(n_items), static_cast<const float*>(ut),
+                       static_cast<int32_t>(items), static_cast<const float*>(ut),
                        static_cast<const float*>(gm), initial_state,
                        gp == map_passes - 1 ? final_state : nullptr,
                        static_cast<__nv_bfloat16*>(o) + gp * kD, status,
@@ -1976,7 +2158,7 @@ int gdn_set_wait_timeout_ms(uint32_t ms)
 
 int gdn_set_scan_kernel(int kernel)
 {
-    if (kernel < GDN_SCAN_AUTO || kernel > GDN_SCAN_MMA_SYNC)
+    if (kernel < GDN_SCAN_AUTO || kernel > GDN_SCAN_TENSOR_CORE_32)
         return gdn_fail(GDN_ERR_INVALID_ARG, "unknown scan kernel %d", kernel);
     g_gdn_scan.store(kernel);
     return GDN_OK;

@@ -136,12 +136,16 @@ int gdn_set_wait_timeout_ms(uint32_t ms);
 
 /* Which kernel runs the scan over each sequence's chunks, for later calls of this process:
  * GDN_SCAN_AUTO (default) and GDN_SCAN_TENSOR_CORE run its chunk products as tcgen05.mma streams
- * from shared memory into tensor memory; GDN_SCAN_MMA_SYNC runs them as register-tile mma.sync.
- * Both compute the same recurrence at the same precision (fp32 operands as three bfloat16
- * pieces); the switch exists for comparison and measurement. */
+ * from shared memory into tensor memory, with 32 state rows per work item when 16-row items
+ * would give every SM at least two, else 16; GDN_SCAN_TENSOR_CORE_16 / _32 fix the row count;
+ * GDN_SCAN_MMA_SYNC runs the products as register-tile mma.sync.  All compute the same
+ * recurrence at the same precision (fp32 operands as three bfloat16 pieces); the switch exists
+ * for comparison and measurement. */
 #define GDN_SCAN_AUTO 0
 #define GDN_SCAN_TENSOR_CORE 1
 #define GDN_SCAN_MMA_SYNC 2
+#define GDN_SCAN_TENSOR_CORE_16 3
+#define GDN_SCAN_TENSOR_CORE_32 4
 int gdn_set_scan_kernel(int kernel);
 
 /* Testing hook, 0 = off (default).  1: the scan kernels never issue the loads of each sequence's

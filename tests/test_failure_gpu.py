@@ -100,7 +100,7 @@ def test_block_scaled_wait_runs_out_and_context_survives(variant):
     assert (np.abs(d - ref) <= oracle.tolerance_mx(ref, ref_abs, K, "f16")).all()
 
 
-@pytest.mark.parametrize("scan", ["tensor_core", "mma_sync"])
+@pytest.mark.parametrize("scan", ["tensor_core_16", "tensor_core_32", "mma_sync"])
 def test_gdn_scan_wait_runs_out_and_context_survives(scan):
     """The Gated Delta Net scan waits on an mbarrier for each chunk's TMA loads.  With
     gdn_set_fault_injection(1) the second chunk's loads are never issued, the 200 ms wait runs

@@ -38,9 +38,10 @@ def cuda_library():
     torch.cuda.init()
 
 
-@pytest.fixture(autouse=True, params=["tensor_core", "mma_sync"])
+@pytest.fixture(autouse=True, params=["tensor_core_16", "tensor_core_32", "mma_sync"])
 def scan_kernel(request, cuda_library):
-    """Every case runs under both scan kernels: the tcgen05 one (the default) and mma.sync."""
+    """Every case runs under every scan kernel: tcgen05 with 16 and with 32 state rows per work
+    item (the default picks one by the item count) and mma.sync."""
     assert g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS[request.param]) == g.GDN_OK
     yield request.param
     g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS["auto"])
