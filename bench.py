@@ -648,7 +648,51 @@ def run_config_leg(args, g, dev, stream, num_sms, peak_burst, hbm_peak, uuid):
         g.check_status(stream)
         cold_us = 1e3 * sum(a.elapsed_time(b) for a, b in ev) / cold_reps
         tf = w.flops / (us * 1e-6) / 1e12
+        # the same launches recorded in a CUDA graph (50 per graph) and replayed: the device-side
+        # time per launch without the host's per-call cost
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(50):
+                launch()
+        g_replays = max(2, reps // 50)
+        with torch.cuda.stream(stream):
+            graph.replay()
+            ge0, ge1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ge0.record(stream)
+            for _ in range(g_replays):
+                graph.replay()
+            ge1.record(stream)
+        torch.cuda.synchronize()
+        g.check_status(stream)
+        graph_us = 1e3 * ge0.elapsed_time(ge1) / (50 * g_replays)
+        del graph
+        # cuBLAS (torch.mm) on the same resident inputs, for context: 50 calls recorded in a
+        # CUDA graph and replayed, so that the host's dispatch rate does not set the figure
+        cublas_us = None
+        if args.cublas_steps != 0:
+            with torch.cuda.stream(stream):
+                for _ in range(20):
+                    torch.mm(Ad, Bd.t(), out=D)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(50):
+                    torch.mm(Ad, Bd.t(), out=D)
+            replays = max(2, reps // 50)
+            with torch.cuda.stream(stream):
+                graph.replay()
+                c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                c0.record(stream)
+                for _ in range(replays):
+                    graph.replay()
+                c1.record(stream)
+            torch.cuda.synchronize()
+            cublas_us = 1e3 * c0.elapsed_time(c1) / (50 * replays)
+            del graph
         out[name] = {"M": w.M, "N": w.N, "K": w.K, "variant": variant, "launches": reps,
+                     "us_per_launch_graph": graph_us,
+                     "tflops_graph": w.flops / (graph_us * 1e-6) / 1e12,
+                     "cublas_us_per_launch_graph_context": cublas_us,
                      "us_per_launch": us, "tflops": tf, "frac_of_burst": tf / peak_burst,
                      "hbm_gbs_algorithmic": w.min_bytes / (us * 1e-6) / 1e9,
                      "hbm_frac": w.min_bytes / (us * 1e-6) / 1e9 / hbm_peak,
@@ -659,10 +703,12 @@ def run_config_leg(args, g, dev, stream, num_sms, peak_burst, hbm_peak, uuid):
     del scratch
     return {"metric": "fp16 GEMM per config, automatic variant (gemm_f16_nt)",
             "timing": "warm: back-to-back launches between two CUDA events on the launching "
-                      "stream; cold: a 512 MiB scratch write before each launch, events around "
-                      "the launch alone",
+                      "stream; graph: the same launches recorded 50 to a CUDA graph and "
+                      "replayed (no per-call host cost); cold: a 512 MiB scratch write before "
+                      "each launch, events around the launch alone",
             "configs": out, "clocks": clk,
-            "gpu_launches": sum(v["launches"] + 50 for v in out.values())}
+            "gpu_launches": sum(v["launches"] + 50 + 50 * (max(2, v["launches"] // 50) + 1)
+                                for v in out.values())}
 
 
 def run_sustained_leg(args, g, stream, work, launch, flops_step, peak_burst, peak_sus, num_sms,

@@ -166,19 +166,21 @@ bool variant_info(int v, gemm_f16_variant_info* o)
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Automatic variant.  Measured on GB300 (bench.py --sweep): the CTA pair is fastest once its
-// tiles fill the GPU (3000x5000x1000, 8192^3, MLP shape); when every 128x256 tile fits in one
-// wave that keeps at least half the SMs busy, the single-CTA 128x256 kernel wins (2048^3: 16.8 us
-// against 18.9 us for the pair); below that, 128x128 tiles keep more SMs busy.
+// Automatic variant, from bench.py --sweep on GB300 (back-to-back launches): the CTA pair on
+// 2048^3, 3000x5000x1000 (34.5 us against 49.9 us for 128x256), 8192^3 and the MLP shape;
+// 128x128 tiles where neither larger tile keeps half the SMs busy.
 int choose_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
 {
     if (num_sms < 2) num_sms = 2;
     const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 256);
     const int64_t tiles_128x256 = cdiv(M, 128) * cdiv(N, 256);
-    if (tiles_128x256 <= num_sms && 2 * tiles_128x256 >= num_sms)
-        return GEMM_F16_VARIANT_WS_128x256;
-    if (M > 128 && pair_tiles >= num_sms / 2) return GEMM_F16_VARIANT_WS_PAIR;
-    if (tiles_128x256 >= num_sms) return GEMM_F16_VARIANT_WS_128x256;
+    // The CTA pair once its tiles occupy at least half the SMs: it loads 32 KB per CTA and
+    // k-block against 48 KB for a lone 128 x 256 CTA, so a single wave of it is not starved by
+    // L2 (2048^3, 64 pair tiles: 14.95 us against 16.8 us for 128 x 256, back-to-back launches
+    // with programmatic dependent launch); then 128 x 256 while its tiles fill half the SMs;
+    // else 128 x 128.
+    if (M > 128 && 4 * pair_tiles >= num_sms) return GEMM_F16_VARIANT_WS_PAIR;
+    if (2 * tiles_128x256 >= num_sms) return GEMM_F16_VARIANT_WS_128x256;
     return GEMM_F16_VARIANT_WS_128x128;
 }
 

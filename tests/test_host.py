@@ -231,6 +231,20 @@ def test_choose_variant_returns_a_variant():
         assert v in (1, 2, 3, 4)
 
 
+def test_choose_variant_on_the_workloads():
+    """The automatic choice on a 152-SM GB300 for the five workloads: one 128 x 128 CTA for the
+    single tile, the 256 x 256 CTA pair for every other (2048^3 has 64 pair tiles: at least half
+    the SMs), and 128 x 256 / 128 x 128 for shapes too short for a pair."""
+    pair, w256, w128 = g.VARIANTS["ws_pair"], g.VARIANTS["ws_128x256"], g.VARIANTS["ws_128x128"]
+    assert g.gemm_f16_choose_variant(128, 128, 64, 152) == w128
+    for shape in [(2048, 2048, 2048), (3000, 5000, 1000), (8192, 8192, 8192),
+                  (16384, 14336, 4096)]:
+        assert g.gemm_f16_choose_variant(*shape, 152) == pair, shape
+    assert g.gemm_f16_choose_variant(128, 65536, 4096, 152) == w256     # 256 tiles of 128 x 256
+    assert g.gemm_f16_choose_variant(128, 16384, 4096, 152) == w128     # 64: under half the SMs
+    assert g.gemm_f16_choose_variant(512, 1024, 4096, 152) == w128      # 8 pair tiles only
+
+
 # ---- argument checks (return before any CUDA call) ---------------------------------------------
 
 FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced: every case below fails validation
