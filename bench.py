@@ -296,10 +296,12 @@ class ClockSampler:
             return None
         sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
         mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        pw = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w": statistics.median(pw) if pw else None,
                 "samples": len(rows)}
 
 
@@ -754,10 +756,12 @@ def run_sustained_leg(args, g, stream, work, launch, flops_step, peak_burst, pea
 
     tf, ms, per, clk = timed(launch)
     g.check_status(stream)
+    pj = lambda t, c: (c["power_w"] / (t * 1e12) * 1e12) if c and c.get("power_w") else None
     res = {"value": tf, "unit": "TFLOP/s", "steps": steps, "timed_ms": ms,
            "per_workload": per, "peak_sustained": peak_sus,
            "frac_of_sustained": tf / peak_sus if peak_sus else None,
-           "frac_of_burst": tf / peak_burst, "clocks": clk, "gpu_launches": steps * len(work)}
+           "frac_of_burst": tf / peak_burst, "clocks": clk, "gpu_launches": steps * len(work),
+           "pj_per_flop": pj(tf, clk)}
     if clk and clk.get("sm_mhz"):
         cpk = num_sms * FLOP_PER_CLK_PER_SM * clk["sm_mhz"] * 1e6 / 1e12
         res["clock_peak_tflops"] = cpk
@@ -773,7 +777,8 @@ def run_sustained_leg(args, g, stream, work, launch, flops_step, peak_burst, pea
         torch.cuda.synchronize()
         ctf, cms, cper, cclk = timed(mm)
         res["cublas_same_step"] = {"value": ctf, "timed_ms": cms, "per_workload": cper,
-                                   "clocks": cclk, "ours_over_cublas": tf / ctf}
+                                   "clocks": cclk, "ours_over_cublas": tf / ctf,
+                                   "pj_per_flop": pj(ctf, cclk)}
     return res
 
 

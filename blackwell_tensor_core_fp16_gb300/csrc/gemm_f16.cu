@@ -63,10 +63,15 @@ uint64_t wait_timeout_ns()
 
 uint32_t debug_flags() { return g_debug_flags.load(std::memory_order_relaxed); }
 
-// L2 priorities for the A and B loads: bits 1:0 A, bits 3:2 B (0 normal, 1 evict_first,
-// 2 evict_last).  Default: A evict_last (a band of A rows is reused by every tile of its group
-// of tile-rows across several waves), B normal; measured 0.5-1.5% faster under the power cap
-// than no hint.  GEMM_F16_L2_A / GEMM_F16_L2_B = normal | first | last override.
+// L2 priorities for the A and B loads and the D stores: bits 1:0 A, bits 3:2 B, bits 5:4 D
+// (0 normal, 1 evict_first, 2 evict_last).  Default: A and B evict_last, D normal.  A band of A
+// rows is reused by every tile of its group of tile-rows, and a band of B rows by every group
+// that sweeps it; with A alone evict_last the runs were 0.5-1.5% faster than with no hint, and
+// B evict_last too added 0.5% on 8192^3 and 1.6% on the MLP shape (700-step loops, two
+// alternations on one box; B evict_first, B normal and A normal were slower).  D stores with
+// evict_first measured within noise (+0.3%), and would push out a result the next kernel often
+// reads, so D stays normal.  GEMM_F16_L2_A / GEMM_F16_L2_B / GEMM_F16_L2_D = normal | first |
+// last override.
 uint32_t l2_hint_setting()
 {
     static const uint32_t v = [] {
@@ -77,7 +82,8 @@ uint32_t l2_hint_setting()
             return 0u;
         };
         return parse(std::getenv("GEMM_F16_L2_A"), 2u) |
-               (parse(std::getenv("GEMM_F16_L2_B"), 0u) << 2);
+               (parse(std::getenv("GEMM_F16_L2_B"), 2u) << 2) |
+               (parse(std::getenv("GEMM_F16_L2_D"), 0u) << 4);
     }();
     return v;
 }

@@ -605,6 +605,8 @@ __global__ void __launch_bounds__(192, 1)
         volatile uint32_t* epi_word =
             reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_EPI_WORD);
         uint32_t sbuf = 0;
+        // L2 priority of the D stores (bits 5:4 of l2_hints; 0 = normal)
+        const uint64_t pol_d = make_l2_policy((l2_hints >> 4) & 3u);
 
         // Store 64 columns (32 packed f16x2 words) of this thread's row at column col0.
         const auto store_chunk = [&](const uint32_t (&p)[32], int32_t m0, int32_t col0) {
@@ -621,7 +623,7 @@ __global__ void __launch_bounds__(192, 1)
                 fence_proxy_async_smem();
                 named_barrier_sync(1, C::EPI_THREADS);
                 if (et == 0) {
-                    tma_store_2d(&tmap_d, dbuf, col0, m0);
+                    tma_store_2d_hint(&tmap_d, dbuf, col0, m0, pol_d);
                     bulk_commit_group();
                 }
                 __syncwarp();

@@ -309,6 +309,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                  : "memory");
 }
 
+// The same with an L2 eviction-priority policy (make_l2_policy) for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, uint32_t src, int32_t x,
+                                                  int32_t y, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint "
+                 "[%0, {%2, %3}], [%1], %4;"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
