@@ -1072,6 +1072,20 @@ def run_ours(args):
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
                "kind": "oracle", "sample": desc + " (binary64 dot products, OpenMP)",
                "seconds": s}
+        if config_leg is not None:
+            # the three smaller configs through the oracle in full (every output element)
+            from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS as W2
+            per_cfg = {}
+            for name in CONFIGS:
+                w = W2[name]
+                A, B = host_inputs((name,))[name]
+                t = time.perf_counter()
+                oracle.gemm_f64(A, B)
+                dt = time.perf_counter() - t
+                per_cfg[name] = {"seconds": dt, "gflops": w.flops / dt / 1e9,
+                                 "gpu_over_cpu": dt / (config_leg["configs"][name]
+                                                       ["us_per_launch"] * 1e-6)}
+            cpu["per_config_full"] = per_cfg
 
     in_bytes = [2 * (w.M * w.K + w.N * w.K) for (w, *_r) in work]
     line = {
