@@ -1384,10 +1384,12 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     uint32_t k_issued = 0, a_issued = 0, k_done = 0, a_done = 0;
     const auto issue_k = [&](int32_t t0_, int32_t jk_) {
         if (tid == 128) tc::issue_k(base + C::kOffK, bar_k, &map_k, t0_, jk_);
+        __syncwarp();
         ++k_issued;
     };
     const auto issue_a = [&](int64_t cj_) {
         if (tid == 128) tc::issue_a(base + C::kOffA, bar_a, &map_a, cj_);
+        __syncwarp();
         ++a_issued;
     };
     // O = scale (g P + A'0 (U~0 + U~1) + A'1 U~0) of the pending chunk: quarters 0-1 pass the
@@ -1476,10 +1478,19 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
             const int32_t t0 = chunk_t0(ch);
             const int32_t len = min(kC, seq_end - t0);
             const bool next_in_item = ch + 1 < c_end && !(fault == 1 && ch == c_begin);
-            // (warp 4 issues the loads, so that warp 0 goes straight to the MMAs)
-            if (tid == 128 && next_in_item)
-                tc::issue<kR>(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k,
-                              ut, gam, cj_of(ch + 1), r0, chunk_t0(ch + 1), jq, jk);
+            // (warp 4 issues the loads, so that warp 0 goes straight to the MMAs).  With kR = 16
+            // the other stage still holds the previous chunk's A' pieces, which its output
+            // product P3 may still be reading: the loads wait for that product first.
+            if (next_in_item) {
+                if constexpr (!C::kSingleKA) {
+                    if (tid == 128 && pend)
+                        failed |= !gf16::mbar_wait(bar_p3, pend_par, nullptr, wait_ns);
+                }
+                if (tid == 128)
+                    tc::issue<kR>(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q,
+                                  &map_k, ut, gam, cj_of(ch + 1), r0, chunk_t0(ch + 1), jq, jk);
+                __syncwarp();   // warp 4 whole again before any .aligned instruction
+            }
             const uint32_t sb = base + b * C::kStage;
             const float* Bup = upf + b * (C::kUpBytes / 4);
             const float* Bg = gf + b * 2 * kC;
@@ -1648,10 +1659,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
             // the last chunk: the next item's first chunk goes into the other stage now
             const bool next_item_first =
                 kMulti && ch + 1 == c_end && qn < n_items && nx.c_begin < nx.c_end;
-            if (tid == 128 && next_item_first)
-                tc::issue<kR>(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q, &map_k,
-                              ut, gam, static_cast<int64_t>(nx.c_begin) * h_v + nx.j, nx.r0,
-                              nx.seq_start, nx.j / qgroup, nx.j / kgroup);
+            if (next_item_first) {
+                if (tid == 128)
+                    tc::issue<kR>(base, b ^ 1, bar_full + 8 * (b ^ 1), &map_w, &map_a, &map_q,
+                                  &map_k, ut, gam, static_cast<int64_t>(nx.c_begin) * h_v + nx.j,
+                                  nx.r0, nx.seq_start, nx.j / qgroup, nx.j / kgroup);
+                __syncwarp();
+            }
             {   // ---- epilogue 2: S_next = g_C S + K^T U~ ----
                 failed |= !(k_ok && gf16::mbar_wait(bar_p2, par, nullptr, wait_ns));
                 gf16::tcgen05_fence_after();
