@@ -1155,6 +1155,8 @@ def run_sweep(args):
                     else [int(v) for v in args.sweep_variants.split(",")])
         for variant in variants:
             for use_ws in ((False,) if args.sweep_no_stream_k else (False, True)):
+                # the stream-K leg turns the (default-off) tail on for its launches only
+                g.gemm_f16_set_stream_k(1 if use_ws else 0)
                 need = g.gemm_f16_workspace_bytes(w.M, w.N, w.K, variant) if use_ws else 0
                 if use_ws and need == 0:
                     continue
@@ -1212,6 +1214,7 @@ def run_sweep(args):
                     "auto_variant": auto, "stream_k": bool(need), "launches": reps,
                     "l2": "warm (back-to-back launches)", "ms_per_launch": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
                     "hbm_gbs_algorithmic": w.min_bytes / (ms * 1e-3) / 1e9}), flush=True)
+    g.gemm_f16_set_stream_k(0)
     return 0
 
 

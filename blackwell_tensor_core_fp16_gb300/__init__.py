@@ -24,7 +24,7 @@ __all__ = [
     "gemm_f16_workspace_bytes",
     "gemm_f16_nt_fused", "linear", "DTYPES", "ACTIVATIONS", "gemm_f16_set_wait_timeout_ms",
     "gemm_f16_set_fault_injection",
-    "gemm_f16_sk_tail_tiles", "gemm_f16_raster_group",
+    "gemm_f16_sk_tail_tiles", "gemm_f16_raster_group", "gemm_f16_set_stream_k",
     "gemm_f16_sk_items", "gemm_f16_sk_item", "gemm_f16_sk_unit_of",
     "exported_symbols", "VARIANTS", "STATUS",
 ]
@@ -115,6 +115,8 @@ def load():
         lib.gemm_f16_workspace_bytes.restype = i32
         lib.gemm_f16_sk_tail_tiles.argtypes = [i64, i64, i64]
         lib.gemm_f16_sk_tail_tiles.restype = i64
+        lib.gemm_f16_set_stream_k.argtypes = [i32]
+        lib.gemm_f16_set_stream_k.restype = i32
         lib.gemm_f16_raster_group.argtypes = [i64, i64, i64, i64]
         lib.gemm_f16_raster_group.restype = u32
         lib.gemm_f16_sk_items.argtypes = [u32, u32, u32, u32, u32]
@@ -254,6 +256,11 @@ def gemm_f16_workspace_bytes(M: int, N: int, K: int, variant: int = 0) -> int:
 
 def gemm_f16_sk_tail_tiles(tiles: int, units: int, k_blocks: int) -> int:
     return load().gemm_f16_sk_tail_tiles(tiles, units, k_blocks)
+
+
+def gemm_f16_set_stream_k(enable: int) -> int:
+    """Turn the stream-K tail of launches with a workspace on (1) or off (0, the default)."""
+    return load().gemm_f16_set_stream_k(int(enable))
 
 
 def gemm_f16_raster_group(mma_m: int, K: int, elem_bytes: int, l2_bytes: int) -> int:

@@ -398,7 +398,7 @@ int launch_tile(const void* A, const void* B, void* D, int64_t M, int64_t N, int
 }
 
 // Units that share the stream-K tail of R tiles: at most 3 per tile, so a tile has at most
-// 4 contributors (the kernel's fix-up keeps up to 4 partial loads in flight per slice).
+// 4 contributors (gf16::kMaxContrib: the piece that finishes a tile adds up to 3 others).
 int64_t sk_units_for(int64_t R, int64_t U)
 {
     return R * 3 < U ? R * 3 : U;
@@ -417,15 +417,24 @@ int64_t sk_tail_tiles(int64_t T, int64_t U, int64_t KB)
     return R;
 }
 
-// Workspace layout: [counters, kWsCountBytes][partials: units x 2 pieces x cta_group x
-// 128 x BN fp32].  Counters must be zero when a launch starts; the host clears the ones a
-// launch uses with cudaMemsetAsync on the launch's stream.
-constexpr size_t kWsCountBytes = 4096;
-
+// Workspace layout: [header, gf16::kSkHeaderBytes][partial sums: units x cta_group x 128 x BN
+// fp32].  The header must be zero when a workspace is first used and the kernel keeps it so
+// (see gf16::kSkHeaderBytes).  A caller's workspace has its header cleared with
+// cudaMemsetAsync on the launch's stream before each launch, so it needs no initialising; the
+// library's own fixed array (gemm_f16_nt_noalloc) starts at zero and skips that clear.
 size_t ws_bytes_for(int64_t units, int cta_group, int block_n)
 {
-    return kWsCountBytes + static_cast<size_t>(units) * 2u * cta_group * 128u * block_n * 4u;
+    return gf16::kSkHeaderBytes + static_cast<size_t>(units) * cta_group * 128u * block_n * 4u;
 }
+
+// Set while gemm_f16_nt_noalloc runs a launch on its fixed array (see ws_bytes_for).
+thread_local bool t_ws_kept_clean = false;
+
+// Whether launches given a workspace run the stream-K tail (gemm_f16_set_stream_k).  Off by
+// default: measured on GB300, it was slower than the data-parallel schedule on every workload
+// (a CTA parks 128 KB of fp32 partial sums at about 25 bytes per cycle, and the finishing CTA
+// reads them back, which costs more than the idle part of the last wave).
+std::atomic<int> g_stream_k{0};
 
 // Epilogue options of a launch: element type, bias (N elements of that type, or null) and
 // activation.
@@ -501,7 +510,9 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
     }
     const int64_t KB = cdiv(K, C::BLOCK_K);
     // Stream-K tail: all units take part; otherwise no more units than tiles.
-    int64_t R = sk_tail_tiles(tiles, units, KB);
+    int64_t R = g_stream_k.load(std::memory_order_relaxed) ? sk_tail_tiles(tiles, units, KB) : 0;
+    // one flag per (tail tile, contributor, CTA) in each of the header's two flag regions
+    if (R * gf16::kMaxContrib * kCtaGroup > gf16::kSkFlagWords) R = 0;
     const size_t need = R ? ws_bytes_for(units, kCtaGroup, kBlockN) : 0;
     if (bytes_needed) {
         *bytes_needed = need;
@@ -525,14 +536,15 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
     if ((cdiv(tiles - R, units_used) + 1) * KB >= (int64_t(1) << 31))
         return fail(GEMM_F16_ERR_UNSUPPORTED, "problem too large for one launch (M=%lld N=%lld "
                     "K=%lld)", (long long)M, (long long)N, (long long)K);
-    uint32_t* ws_count = nullptr;
+    uint32_t* ws_hdr = nullptr;
     float* ws_part = nullptr;
     if (R) {
-        ws_count = static_cast<uint32_t*>(workspace);
-        ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kWsCountBytes);
-        cudaError_t e = cudaMemsetAsync(ws_count, 0, static_cast<size_t>(R) * kCtaGroup * 4u,
-                                        stream);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(stream-K counters)");
+        ws_hdr = static_cast<uint32_t*>(workspace);
+        ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + gf16::kSkHeaderBytes);
+        if (!t_ws_kept_clean) {
+            cudaError_t e = cudaMemsetAsync(ws_hdr, 0, gf16::kSkHeaderBytes, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(stream-K header)");
+        }
     }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, maps->ma, maps->mb, maps->md,
                                        static_cast<uint16_t*>(D),
@@ -540,7 +552,7 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
                                        (uint32_t)num_m, (uint32_t)num_n, (uint32_t)KB,
                                        group_m_for(C::MMA_M, K, C::ELEM_BYTES, d.l2_bytes),
                                        wait_timeout_ns(), l2_hint_setting(),
-                                       ws_part, ws_count, (uint32_t)R,
+                                       ws_part, ws_hdr, (uint32_t)R,
                                        (uint32_t)(R ? sk_units_for(R, units_used) : units_used),
                                        static_cast<const uint16_t*>(epi.bias),
                                        static_cast<uint32_t>(epi.act), debug_flags(),
@@ -859,8 +871,14 @@ int gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_
     if (need > kNoAllocScratchBytes) need = 0;
     void* scratch = nullptr;
     if (need > 0 && (rc = noalloc_scratch(&scratch)) != GEMM_F16_OK) return rc;
-    return run(A, B, D, M, N, K, stream, GEMM_F16_VARIANT_AUTO, scratch,
-               need > 0 ? kNoAllocScratchBytes : 0);
+    // The array's stream-K header starts at zero and every launch leaves it consistent, so
+    // the launch needs no clearing copy before it (which would also break the overlap of
+    // consecutive launches).
+    t_ws_kept_clean = true;
+    rc = run(A, B, D, M, N, K, stream, GEMM_F16_VARIANT_AUTO, scratch,
+             need > 0 ? kNoAllocScratchBytes : 0);
+    t_ws_kept_clean = false;
+    return rc;
 }
 
 size_t gemm_f16_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
@@ -946,6 +964,14 @@ uint32_t gemm_f16_raster_group(int64_t mma_m, int64_t K, int64_t elem_bytes, int
 int64_t gemm_f16_sk_tail_tiles(int64_t tiles, int64_t units, int64_t k_blocks)
 {
     return sk_tail_tiles(tiles, units, k_blocks);
+}
+
+int gemm_f16_set_stream_k(int enable)
+{
+    if (enable != 0 && enable != 1)
+        return fail(GEMM_F16_ERR_INVALID_ARG, "stream-K switch %d is not 0 or 1", enable);
+    g_stream_k.store(enable, std::memory_order_relaxed);
+    return GEMM_F16_OK;
 }
 
 static gf16::WorkSplit host_split(uint32_t tiles, uint32_t units, uint32_t k_blocks,

@@ -76,6 +76,19 @@ __device__ __forceinline__ uint32_t tiles_of(uint32_t c, uint32_t units, uint32_
 
 constexpr uint32_t kBlockM = 128;  // rows of A (and D) per CTA
 constexpr uint32_t kMaxContrib = 4;  // most stream-K pieces one tile is split into
+
+// Stream-K workspace: a header of kSkHeaderBytes, then one slot of fp32 partial sums per unit
+// and CTA.  The header must be zero when a workspace is first used; launches keep it so:
+//   word 0   which of the two flag regions the current launch uses (0 or 1);
+//   word 1   CTAs of the current launch that have finished (the last flips word 0 and clears
+//            this count, so the next launch uses the other region);
+//   words kSkFlagBase ..  flag region 0, then flag region 1, kSkFlagWords words each.  Flag
+//            (tail tile r, contributor j, CTA rank) is 1 once that contributor's partial sums
+//            are in its slot.  Each launch clears the region it does not use, so the next
+//            launch finds its region zero, even after a launch that gave up a wait.
+constexpr uint32_t kSkHeaderBytes = 8192;
+constexpr uint32_t kSkFlagBase = 64;
+constexpr uint32_t kSkFlagWords = (kSkHeaderBytes / 4u - kSkFlagBase) / 2u;
 constexpr uint32_t kBlockK = 64;   // one 128-byte swizzle row of fp16
 constexpr uint32_t kUmmaK = 16;    // K per tcgen05.mma of kind::f16
 
@@ -312,7 +325,7 @@ struct WsCfg {
     static constexpr uint32_t OFF_D = (OFF_SF + kStages * SF_BYTES + 1023u) & ~1023u;
     // Two staging buffers for the TMA-store epilogue; none when the epilogue stores directly.
     static constexpr uint32_t OFF_BAR = OFF_D + (kTmaStore ? kDBufs * D_BYTES : 0);
-    static constexpr uint32_t NUM_BARS = 2 * kStages + 5;    // full, empty, tfull x2, tempty x2, drain
+    static constexpr uint32_t NUM_BARS = 2 * kStages + 6;  // full, empty, tfull x2, tempty x2, drain, pair
     static constexpr uint32_t OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr uint32_t OFF_ABORT = OFF_SLOT + 4;
     static constexpr uint32_t OFF_EPI_WORD = OFF_ABORT + 4;      // epilogue broadcast word
@@ -334,7 +347,7 @@ __global__ void __launch_bounds__(192, 1)
                    uint32_t M, uint32_t N,
                    uint32_t num_m_blocks, uint32_t num_n_blocks, uint32_t num_k_blocks,
                    uint32_t group_m, uint64_t timeout_ns, uint32_t l2_hints,
-                   float* __restrict__ ws_part, uint32_t* __restrict__ ws_count,
+                   float* __restrict__ ws_part, uint32_t* __restrict__ ws_hdr,
                    uint32_t sk_tiles, uint32_t sk_units, const uint16_t* __restrict__ bias,
                    uint32_t act, uint32_t debug_flags,
                    const __grid_constant__ CUtensorMap tmap_sfa,
@@ -359,6 +372,7 @@ __global__ void __launch_bounds__(192, 1)
     const auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2u * kStages + b); };
     const auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2u * kStages + 2u + b); };
     const uint32_t drain_bar = bar0 + 8u * (2u * kStages + 4u);
+    const uint32_t pair_bar = bar0 + 8u * (2u * kStages + 5u);   // teardown rendezvous of a pair
     volatile uint32_t* slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_SLOT);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
 
@@ -391,6 +405,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(tempty_bar(b), 4u * kCtaGroup);  // one arrival per epilogue warp per CTA
         }
         mbar_init(drain_bar, 1);
+        mbar_init(pair_bar, 1);
         *abort_flag = 0u;
         fence_mbarrier_init();
     }
@@ -400,16 +415,22 @@ __global__ void __launch_bounds__(192, 1)
         tmem_relinquish<kCtaGroup>();
     }
     tcgen05_fence_before();
-    if constexpr (kPair) cluster_sync(); else __syncthreads();
-    tcgen05_fence_after();
-    const uint32_t tmem_base = *slot_ptr;
-
-    // Everything above touches only shared memory, tensor memory and the kernel parameters, so
-    // it may overlap the end of the previous kernel on the stream.  Let the next GEMM begin its
-    // own set-up as SMs free up, then wait for the previous kernel's writes (A and B may be its
-    // output, D its input) before the first access to global memory.
+    // The barriers and the TMEM address become visible to the CTA (to the pair: at the cluster
+    // barrier, whose latency, about 1000 cycles on GB300, each role overlaps with its own
+    // register-only set-up before it waits).
+    if constexpr (kPair) cluster_arrive(); else __syncthreads();
+    // Everything so far touches only shared memory, tensor memory and the kernel parameters, so
+    // it may overlap the end of the previous kernel on the stream: let the next GEMM begin its
+    // own set-up as SMs free up.  The roles that touch global memory (the producer's loads of
+    // A and B, which may be the previous kernel's output; the epilogue's stores of D, which it
+    // may read) wait for the previous kernel first; the MMA issuer needs no wait.
     grid_dep_launch();
-    grid_dep_wait();
+    uint32_t tmem_base = 0;
+    const auto setup_done = [&]() {
+        if constexpr (kPair) cluster_wait();
+        tcgen05_fence_after();
+        tmem_base = *slot_ptr;
+    };
 
     if (warp == 0) {
         // ---- TMA producer ------------------------------------------------------------------
@@ -425,15 +446,19 @@ __global__ void __launch_bounds__(192, 1)
         WorkItem wi = work_item(split, cid, 0);
         uint32_t kb = wi.kb0;
         int32_t m0 = 0, n0 = 0, sf_rb_b = 0;
+        const auto tile_origin = [&]() {
+            const TileCoord tc = tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
+            m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
+            n0 = static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS);
+            // the 128-row group of B's scales that holds the tile's first row
+            sf_rb_b = static_cast<int32_t>(tc.n_blk * C::BN / 128u);
+        };
+        tile_origin();
         const uint32_t produce = (debug_flags & kDebugNoLoads) ? 0u : total;
+        setup_done();
+        grid_dep_wait();
         for (; it < produce; ++it) {
-            if (kb == wi.kb0) {
-                const TileCoord tc = tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
-                m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
-                n0 = static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS);
-                // the 128-row group of B's scales that holds the tile's first row
-                sf_rb_b = static_cast<int32_t>(tc.n_blk * C::BN / 128u);
-            }
+            if (kb == wi.kb0 && it != 0) tile_origin();
             const RingPos p = ring_pos(it, kStages);
             const bool w = mbar_wait<kPair>(empty_bar(p.stage), p.parity ^ 1u, abort_flag,
                                             timeout_ns);
@@ -505,6 +530,7 @@ __global__ void __launch_bounds__(192, 1)
         // ---- MMA issuer (the even CTA of a pair issues for both) ----------------------------
         // Warp-uniform loop as in the producer; one elected lane issues the MMAs and commits
         // (a commit tracks the MMAs its own thread issued, so it is always the same lane).
+        setup_done();
         if (rank == 0) {
             const bool leader = elect_one_sync();
             uint32_t item = 0;
@@ -594,16 +620,41 @@ __global__ void __launch_bounds__(192, 1)
                 if (!mbar_wait<false>(drain_bar, 0, nullptr, timeout_ns))
                     atomicOr(&gemm_f16_status_word, kStatusDrainTimeout);
             }
+            if constexpr (kPair) {
+                // Both CTAs' epilogues hand each accumulator back with an arrival on this CTA's
+                // barriers, the other CTA's from afar: wait for the last hand-backs, so that
+                // none is still on its way when this CTA exits.
+                for (uint32_t a = acc; ok && a < acc + C::ACC_BUFS; ++a) {
+                    if (a < C::ACC_BUFS) continue;   // this buffer was never used
+                    const bool w = mbar_wait<kPair>(tempty_bar(a % C::ACC_BUFS),
+                                                    ((a / C::ACC_BUFS) & 1u) ^ 1u, abort_flag,
+                                                    timeout_ns);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        if (leader) report(kStatusMmaTimeout, abort_flag);
+                        ok = false;
+                    }
+                }
+            }
         }
         __syncwarp();
     } else {
         // ---- epilogue warpgroup ------------------------------------------------------------
+        setup_done();
+        grid_dep_wait();
         const uint32_t quad = warp & 3u;             // TMEM lanes 32*quad .. 32*quad + 31
         const uint32_t row = quad * 32u + lane;      // row of this CTA's 128-row slab
         const uint32_t et = threadIdx.x - 64u;       // 0 .. 127
+        // Stream-K: this launch's flag region; the other one is cleared for the next launch.
+        uint32_t* sk_flags = nullptr;
+        if (sk_tiles != 0u) {
+            const uint32_t region = __ldcg(ws_hdr) & 1u;
+            sk_flags = ws_hdr + kSkFlagBase + region * kSkFlagWords;
+            uint32_t* other = ws_hdr + kSkFlagBase + (region ^ 1u) * kSkFlagWords;
+            for (uint32_t w = blockIdx.x * C::EPI_THREADS + et; w < kSkFlagWords;
+                 w += gridDim.x * C::EPI_THREADS)
+                other[w] = 0u;
+        }
         const uint32_t lane_off = (quad * 32u) << 16;
-        volatile uint32_t* epi_word =
-            reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_EPI_WORD);
         uint32_t sbuf = 0;
         // L2 priority of the D stores (bits 5:4 of l2_hints; 0 = normal)
         const uint64_t pol_d = make_l2_policy((l2_hints >> 4) & 3u);
@@ -645,12 +696,51 @@ __global__ void __launch_bounds__(192, 1)
             }
         };
 
-        // Partial accumulators live in the workspace in a layout where a warp's 32 rows of one
-        // 16-byte column group are contiguous: float4 index ((chunk * 16 + j) * 128 + row).
-        const auto part_of = [&](uint32_t unit, uint32_t piece) {
+        // A unit's partial sums live in its workspace slot in a layout where a warp's 32 rows
+        // of one 16-byte column group are contiguous: float4 index ((chunk * 16 + j) * 128 + row).
+        const auto part_of = [&](uint32_t unit) {
             return reinterpret_cast<float4*>(
-                ws_part + (static_cast<uint64_t>(unit * 2u + piece) * kCtaGroup + rank) *
-                              C::PART_FLOATS);
+                ws_part + (static_cast<uint64_t>(unit) * kCtaGroup + rank) * C::PART_FLOATS);
+        };
+
+        // Hand accumulator b back to the MMA issuer once this warp's loads of it are complete.
+        const auto hand_back = [&](uint32_t b) {
+            tcgen05_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (kPair) mbar_arrive_remote(mapa_shared(tempty_bar(b), 0));
+                else mbar_arrive_local(tempty_bar(b));
+            }
+            __syncwarp();
+        };
+        // Fused epilogue (if any), rounding and store of 64 fp32 columns (v0: the first 32).
+        const auto emit64 = [&](uint32_t (&v0)[32], uint32_t (&v1)[32], int32_t m0, int32_t col0) {
+            if (fused) {
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float f[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v0[8 * g8 + i]);
+                    epilogue8<kBf16>(f, bias, col0 + 8 * g8, N, act);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v0[8 * g8 + i] = __float_as_uint(f[i]);
+                }
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float f[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v1[8 * g8 + i]);
+                    epilogue8<kBf16>(f, bias, col0 + 32 + 8 * g8, N, act);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v1[8 * g8 + i] = __float_as_uint(f[i]);
+                }
+            }
+            uint32_t p[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) p[i] = pack2<kBf16>(v0[2 * i], v0[2 * i + 1]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) p[16 + i] = pack2<kBf16>(v1[2 * i], v1[2 * i + 1]);
+            store_chunk(p, m0, col0);
         };
 
         uint32_t acc = 0;
@@ -724,26 +814,53 @@ __global__ void __launch_bounds__(192, 1)
                     continue;
                 }
             }
-            float4* my_part = wi.partial ? part_of(cid, wi.piece) : nullptr;
-#pragma unroll 1
-            for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
-                uint32_t v0[32], v1[32];
-                const uint32_t taddr = tmem_base + lane_off + b * C::BN + c * C::D_COLS;
-                tmem_ld_32x32b_x32(taddr, v0, 0);
-                tmem_ld_32x32b_x32(taddr, v1, 32);
-                tmem_ld_wait();
-                if (c == C::BN / C::D_COLS - 1) {
-                    // This warp is done with accumulator b: hand it back to the MMA issuer.
-                    tcgen05_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (kPair) mbar_arrive_remote(mapa_shared(tempty_bar(b), 0));
-                        else mbar_arrive_local(tempty_bar(b));
+            if (!wi.partial) {
+                // A whole tile: two 64-column chunks per round, both chunks' loads in flight
+                // before one wait.
+                constexpr uint32_t NC = C::BN / C::D_COLS;
+#pragma unroll
+                for (uint32_t c2 = 0; c2 < NC; c2 += 2) {
+                    uint32_t v[4][32];
+                    const uint32_t taddr = tmem_base + lane_off + b * C::BN + c2 * C::D_COLS;
+#pragma unroll
+                    for (uint32_t h = 0; h < 4; ++h)
+                        if (c2 + h / 2 < NC)
+                            tmem_ld_32x32b_x32(taddr, v[h], static_cast<int>(32u * h));
+                    tmem_ld_wait();
+                    if (c2 + 2 >= NC) hand_back(b);   // this warp is done with accumulator b
+#pragma unroll
+                    for (uint32_t cc = 0; cc < 2; ++cc) {
+                        const uint32_t c = c2 + cc;
+                        const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
+                        if (c < NC && col0 < static_cast<int32_t>(N) && rows_in)
+                            emit64(v[2 * cc], v[2 * cc + 1], m0, col0);
                     }
-                    __syncwarp();
                 }
-                if (wi.partial) {
-                    // Stream-K piece: park the fp32 partial sums in the workspace.
+                continue;
+            }
+            // Stream-K piece of tail tile r, whose k-blocks units u0 .. u1 share in order.  The
+            // piece that starts the tile (k-block 0) finishes it: it adds the other pieces'
+            // fp32 partial sums, in unit order, to its own and stores the tile.  That piece is
+            // always its unit's last item, and every other piece of the tile is its unit's
+            // first (or only) stream-K piece, which parks its partial sums in the unit's one
+            // slot and raises its flag: so a finishing piece waits only for pieces that wait for
+            // nothing (a unit's data-parallel tiles, before its pieces, wait for nothing either).
+            const uint32_t r = wi.tile - (num_tiles - sk_tiles);
+            const uint32_t u0 = sk_unit_of(split, r * num_k_blocks);
+            const uint32_t u1 = sk_unit_of(split, r * num_k_blocks + num_k_blocks - 1u);
+            const auto flag_of = [&](uint32_t u) {
+                return sk_flags + (r * kMaxContrib + (u - u0)) * kCtaGroup + rank;
+            };
+            if (wi.kb0 != 0u) {
+                float4* my_part = part_of(cid);
+#pragma unroll 1
+                for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
+                    uint32_t v0[32], v1[32];
+                    const uint32_t taddr = tmem_base + lane_off + b * C::BN + c * C::D_COLS;
+                    tmem_ld_32x32b_x32(taddr, v0, 0);
+                    tmem_ld_32x32b_x32(taddr, v1, 32);
+                    tmem_ld_wait();
+                    if (c == C::BN / C::D_COLS - 1) hand_back(b);
                     float4* dst = my_part + c * 16u * 128u + row;
 #pragma unroll
                     for (uint32_t j = 0; j < 8; ++j)
@@ -755,128 +872,118 @@ __global__ void __launch_bounds__(192, 1)
                         dst[(8 + j) * 128u] = make_float4(
                             __uint_as_float(v1[4 * j]), __uint_as_float(v1[4 * j + 1]),
                             __uint_as_float(v1[4 * j + 2]), __uint_as_float(v1[4 * j + 3]));
-                    continue;
                 }
-                const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
-                if (col0 < static_cast<int32_t>(N) && rows_in) {
-                    if (fused) {
-#pragma unroll
-                        for (int g8 = 0; g8 < 4; ++g8) {
-                            float f[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v0[8 * g8 + i]);
-                            epilogue8<kBf16>(f, bias, col0 + 8 * g8, N, act);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) v0[8 * g8 + i] = __float_as_uint(f[i]);
-                        }
-#pragma unroll
-                        for (int g8 = 0; g8 < 4; ++g8) {
-                            float f[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v1[8 * g8 + i]);
-                            epilogue8<kBf16>(f, bias, col0 + 32 + 8 * g8, N, act);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) v1[8 * g8 + i] = __float_as_uint(f[i]);
-                        }
-                    }
-                    uint32_t p[32];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) p[i] = pack2<kBf16>(v0[2 * i], v0[2 * i + 1]);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        p[16 + i] = pack2<kBf16>(v1[2 * i], v1[2 * i + 1]);
-                    store_chunk(p, m0, col0);
-                }
-            }
-            if (!wi.partial) continue;
-
-            // Count this CTA's contribution to the tile; the contributor that arrives last sums
-            // every piece (in unit order, so the result does not depend on arrival order),
-            // stores the tile and resets the counter for the next launch.
-            const uint32_t r = wi.tile - (num_tiles - sk_tiles);
-            const uint32_t u0 = sk_unit_of(split, r * num_k_blocks);
-            const uint32_t u1 = sk_unit_of(split, r * num_k_blocks + num_k_blocks - 1u);
-            __threadfence();
-            named_barrier_sync(1, C::EPI_THREADS);
-            if (et == 0) {
                 __threadfence();
-                *epi_word = atomicAdd(&ws_count[r * kCtaGroup + rank], 1u);
+                named_barrier_sync(1, C::EPI_THREADS);
+                if (et == 0) {
+                    __threadfence();
+                    st_release_gpu(flag_of(cid), 1u);
+                }
+                continue;
             }
-            named_barrier_sync(1, C::EPI_THREADS);
-            const uint32_t arrived = *epi_word;
-            if (arrived != u1 - u0) continue;
+            // The finishing piece: every other contributor's partial sums must be in place.
+            uint32_t ready = 1u;
+            if (et == 0) {
+                for (uint32_t u = u0 + 1u; u <= u1 && ready; ++u)
+                    ready = wait_flag(flag_of(u), abort_flag, timeout_ns) ? 1u : 0u;
+            }
+            ready = named_barrier_and(2, C::EPI_THREADS, ready);
+            if (!ready) {
+                if (et == 0) report(kStatusEpilogueTimeout, abort_flag);
+                ok = false;
+                break;
+            }
             __threadfence();
-            // Up to kMaxContrib pieces per tile (the host bounds it); all their loads for a
-            // 32-column slice are issued before any is summed.
-            const float4* srcs[kMaxContrib];
+            // Up to kMaxContrib - 1 other pieces (the host bounds it); a slice's loads from all
+            // of them are issued before any is added.
+            const uint32_t nother = u1 - u0;
+            const float4* srcs[kMaxContrib - 1];
 #pragma unroll
-            for (uint32_t q = 0; q < kMaxContrib; ++q) {
-                const uint32_t u = u0 + q <= u1 ? u0 + q : u1;
-                srcs[q] = part_of(u, r - sk_lo(split, u) / num_k_blocks) + row;
-            }
-            const uint32_t ncontrib = u1 - u0 + 1u;
+            for (uint32_t q = 0; q < kMaxContrib - 1; ++q)
+                srcs[q] = part_of(u0 + 1u + q <= u1 ? u0 + 1u + q : u1) + row;
 #pragma unroll 1
             for (uint32_t c = 0; c < C::BN / C::D_COLS; ++c) {
-                const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
-                uint32_t p[32];
+                uint32_t v[2][32];
+                const uint32_t taddr = tmem_base + lane_off + b * C::BN + c * C::D_COLS;
+                tmem_ld_32x32b_x32(taddr, v[0], 0);
+                tmem_ld_32x32b_x32(taddr, v[1], 32);
+                tmem_ld_wait();
+                if (c == C::BN / C::D_COLS - 1) hand_back(b);
 #pragma unroll
-                for (uint32_t h = 0; h < 4; ++h) {   // 16 columns per step
-                    float4 x[kMaxContrib][4];
+                for (uint32_t h = 0; h < 4; ++h) {   // 16 columns (4 groups of 4) per step
+                    float4 x[kMaxContrib - 1][4];
 #pragma unroll
-                    for (uint32_t q = 0; q < kMaxContrib; ++q)
+                    for (uint32_t q = 0; q < kMaxContrib - 1; ++q)
 #pragma unroll
                         for (uint32_t j = 0; j < 4; ++j)
-                            x[q][j] = q < ncontrib
+                            x[q][j] = q < nother
                                           ? __ldcg(srcs[q] + (c * 16u + h * 4u + j) * 128u)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-                    float f[16];
 #pragma unroll
                     for (uint32_t j = 0; j < 4; ++j) {
-                        float4 t = x[0][j];
+                        const uint32_t g = h * 4u + j;              // 16-byte group 0 .. 15
+                        uint32_t* e = &v[g / 8u][(g % 8u) * 4u];    // its 4 fp32 values
+                        float t0 = __uint_as_float(e[0]), t1 = __uint_as_float(e[1]);
+                        float t2 = __uint_as_float(e[2]), t3 = __uint_as_float(e[3]);
 #pragma unroll
-                        for (uint32_t q = 1; q < kMaxContrib; ++q) {
-                            t.x += x[q][j].x;
-                            t.y += x[q][j].y;
-                            t.z += x[q][j].z;
-                            t.w += x[q][j].w;
+                        for (uint32_t q = 0; q < kMaxContrib - 1; ++q) {
+                            t0 += x[q][j].x;
+                            t1 += x[q][j].y;
+                            t2 += x[q][j].z;
+                            t3 += x[q][j].w;
                         }
-                        f[4 * j] = t.x;
-                        f[4 * j + 1] = t.y;
-                        f[4 * j + 2] = t.z;
-                        f[4 * j + 3] = t.w;
+                        e[0] = __float_as_uint(t0);
+                        e[1] = __float_as_uint(t1);
+                        e[2] = __float_as_uint(t2);
+                        e[3] = __float_as_uint(t3);
                     }
-                    if (fused) {
-#pragma unroll
-                        for (int g8 = 0; g8 < 2; ++g8) {
-                            float e[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) e[i] = f[8 * g8 + i];
-                            epilogue8<kBf16>(e, bias, col0 + static_cast<int32_t>(h * 16u) + 8 * g8,
-                                             N, act);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) f[8 * g8 + i] = e[i];
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        p[h * 8 + i] = pack2<kBf16>(__float_as_uint(f[2 * i]),
-                                                    __float_as_uint(f[2 * i + 1]));
                 }
-                if (col0 < static_cast<int32_t>(N) && rows_in) store_chunk(p, m0, col0);
+                const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
+                if (col0 < static_cast<int32_t>(N) && rows_in) emit64(v[0], v[1], m0, col0);
             }
-            if (et == 0) ws_count[r * kCtaGroup + rank] = 0u;
         }
         (void)ok;
         if constexpr (kTmaStore) {
-            if (et == 0) bulk_wait_group_all();
+            // The staging buffers must outlive the copies that read them; the stores' writes
+            // complete on their own before the grid does.
+            if (et == 0) bulk_wait_group_read<0>();
         }
         __syncwarp();
     }
 
     // ---- teardown ------------------------------------------------------------------------
+    // Every role of this CTA is done with tensor memory and with the shared memory that copies
+    // and MMAs use.  In a pair, every operation one CTA aims at the other has been waited for
+    // by its target by now (loads and MMA commits by the roles that consume them, the
+    // epilogues' hand-backs by the MMA issuer above); the two TMEM owners still meet before
+    // freeing their columns, through one barrier of each CTA (a cheaper rendezvous than the
+    // cluster barrier, and a bounded one: its limit is a multiple of every role's own, so that
+    // after a fault both CTAs still get here before it runs out).
     tcgen05_fence_before();
-    if constexpr (kPair) cluster_sync(); else __syncthreads();
+    __syncthreads();
+    if (sk_tiles != 0u && threadIdx.x == 0) {
+        // The last CTA of the launch to finish hands the other flag region to the next launch.
+        __threadfence();
+        if (atomicAdd(ws_hdr + 1, 1u) == gridDim.x - 1u) {
+            atomicExch(ws_hdr + 1, 0u);
+            atomicXor(ws_hdr, 1u);
+        }
+    }
     if (warp == 1) {
+        if constexpr (kPair) {
+            if (elect_one_sync()) {
+                bool w;
+                if (rank == 0) {
+                    w = mbar_wait<kPair>(pair_bar, 0, nullptr, 4 * timeout_ns);
+                    mbar_arrive_remote(mapa_shared(pair_bar, 1));
+                } else {
+                    mbar_arrive_remote(mapa_shared(pair_bar, 0));
+                    w = mbar_wait<kPair>(pair_bar, 0, nullptr, 4 * timeout_ns);
+                }
+                if (!w) atomicOr(&gemm_f16_status_word, kStatusDrainTimeout);
+            }
+            __syncwarp();
+        }
         tcgen05_fence_after();
         tmem_dealloc<kCtaGroup>(tmem_base, C::TMEM_COLS);
     }

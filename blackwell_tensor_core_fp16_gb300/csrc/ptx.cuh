@@ -64,6 +64,18 @@ __device__ __forceinline__ void cluster_sync()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync(), so that work that needs no other thread's writes can run
+// between them.
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Programmatic dependent launch.  grid_dep_launch() lets the next kernel on the stream, if it
 // was launched with programmatic stream serialization, start once every CTA of this grid has
 // called it or exited.  grid_dep_wait() returns once the kernel before this one on the stream
@@ -183,6 +195,37 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t bar, uint32_t parity)
 
 // Upper bound on polls of one wait, a backstop behind the wall-clock limit.
 constexpr uint32_t kMaxPolls = 1u << 28;
+
+// A flag in global memory that another CTA of the grid raises: a GPU-scope release store by
+// the raiser, an acquire load by the waiter.
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until *p is non-zero (false: the wall-clock limit ran out, or another role of
+// this CTA raised `abort_flag`).
+static __device__ __noinline__ bool wait_flag(const uint32_t* p, const volatile uint32_t* abort_flag,
+                                              uint64_t timeout_ns)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+        if (ld_acquire_gpu(p) != 0u) return true;
+        if ((i & 15u) == 15u) {
+            if (abort_flag != nullptr && *abort_flag) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+        __nanosleep(64);
+    }
+    return false;
+}
 
 template <bool kClusterScope>
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,

@@ -114,15 +114,18 @@ int gemm_f16_nt_fused(const void* A, const void* B, void* D, int64_t M, int64_t 
 
 /*
  * D = A * B^T with a caller-provided workspace, which lets the persistent kernels run the tiles
- * of the last, partial wave "stream-K": their k-blocks are split evenly over all CTAs, each CTA
- * parks its fp32 partial sums in the workspace, and the last contributor to a tile adds the
- * pieces and stores the tile.  This keeps every SM busy to the end of the launch.
+ * of the last, partial wave "stream-K" once gemm_f16_set_stream_k(1) has turned that on: the
+ * tail tiles' k-blocks are split evenly over the CTAs; the CTA whose piece starts a tile
+ * finishes it, adding the other pieces' fp32 partial sums (which their CTAs park in the
+ * workspace, raising a flag each) in k order to its own, so the result does not depend on
+ * timing.  With stream-K off (the default) the workspace is not used.
  *
  * workspace:       device memory, 256-byte aligned, at least gemm_f16_workspace_bytes(...) bytes
  *                  (or null / too small: the call runs without the stream-K tail).  The library
- *                  clears the counters it uses with cudaMemsetAsync on `stream` before each launch
- *                  and overwrites the rest; nothing needs initialising.  Launches that share a
- *                  workspace must not overlap on the GPU (use one workspace per stream).
+ *                  clears the workspace's 8 KiB header (flags and their bookkeeping) with
+ *                  cudaMemsetAsync on `stream` before each stream-K launch and overwrites the
+ *                  rest; nothing needs initialising.  Launches that share a workspace must not
+ *                  overlap on the GPU (use one workspace per stream).
  * Everything else is as gemm_f16_nt.  The result differs from gemm_f16_nt's only in the order of
  * the fp32 additions of the tail tiles (both within the tolerance of an fp32 accumulation).
  */
@@ -133,6 +136,14 @@ int gemm_f16_nt_ws(const void* A, const void* B, void* D, int64_t M, int64_t N, 
 int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                    int variant, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Whether later launches of this process that have a workspace (gemm_f16_nt_ws, _ex, _fused,
+ * gemm_f16_nt_noalloc) run the stream-K tail: 1 on, 0 off (the default).  Off by default because
+ * on GB300 it measured slower than the data-parallel schedule on every workload tried (2048^3,
+ * 3000x5000x1000, 8192^3, the MLP shape: 0.6-70% more time): parking a CTA's 128 KB of fp32
+ * partial sums and reading them back costs more than the idle part of the last wave.  Returns
+ * GEMM_F16_OK, or GEMM_F16_ERR_INVALID_ARG for any other value.  Host-only. */
+int gemm_f16_set_stream_k(int enable);
+
 /*
  * D = A * B^T without allocating anything, for callers that cannot allocate device memory:
  * servers that hand all device memory to their own pool at start-up and forbid any other
@@ -140,15 +151,16 @@ int gemm_f16_nt_ex(const void* A, const void* B, void* D, int64_t M, int64_t N, 
  * latency-bound loops that cannot afford cudaMalloc's implicit synchronisation.  The GEMM pages
  * have no counterpart to this entry point; it is a deployment convenience.
  *
- * It computes what gemm_f16_nt_ws computes, with the stream-K workspace taken from a fixed 40 MiB
- * array of device memory that the library reserves on every device that loads it, for the life
- * of the process.  The caller passes A, B and D as for gemm_f16_nt.  Nothing else is allocated:
- * no cudaMalloc, cudaFree or allocating library routine is called.
+ * It computes what gemm_f16_nt_ws computes, with the stream-K workspace (when stream-K is on)
+ * taken from a fixed 40 MiB array of device memory that the library reserves on every device
+ * that loads it, for the life of the process.  The caller passes A, B and D as for gemm_f16_nt.
+ * Nothing else is allocated: no cudaMalloc, cudaFree or allocating library routine is called.
  *
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture that uses this entry
- * point.  Every call shares the one array and finds the previous call's contents in it; the
- * counters that must start at zero are cleared on `stream` before each launch.  Calls that
+ * point.  Every call shares the one array and finds the previous call's contents in it: the
+ * array starts at zero and every launch leaves its 8 KiB header consistent (each launch clears
+ * the flags the next one uses), so no clearing copy runs before a launch.  Calls that
  * overlap on the GPU (on different streams) race on the array and give wrong results: serialise
  * them.  A shape whose stream-K workspace would exceed the array (not possible on a 152-SM
  * GB300, whose largest request is about 38 MiB; possible on a GPU with many more SMs) runs the
@@ -162,8 +174,9 @@ int gemm_f16_nt_noalloc(const void* A, const void* B, void* D, int64_t M, int64_
 size_t gemm_f16_noalloc_scratch_bytes(void);
 
 /* Workspace bytes gemm_f16_nt_ws / gemm_f16_nt_ex need for this shape and variant on the current
- * device (0: the shape gets no stream-K tail).  At most 4 KiB + 2 x units x 128 x 256 x 4 bytes
- * (about 38 MiB on a 152-SM GPU).  Queries the device; launches nothing. */
+ * device (0: the shape gets no stream-K tail, or stream-K is off).  At most 8 KiB + units x
+ * CTAs per unit x 128 x 256 x 4 bytes (about 19 MiB on a 152-SM GPU).  Queries the device;
+ * launches nothing. */
 int gemm_f16_workspace_bytes(int64_t M, int64_t N, int64_t K, int variant, size_t* bytes);
 
 /* The variant GEMM_F16_VARIANT_AUTO picks for this shape on a device with `num_sms`

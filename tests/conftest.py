@@ -18,3 +18,12 @@ def pytest_collection_modifyitems(config, items):
     on a run that selected them with -m gpu, so a box without a working device shows
     up as failures rather than as a green run."""
     return None
+
+
+@pytest.fixture
+def stream_k_on():
+    """Turns the GEMM's stream-K tail on for one test (it is off by default) and off again."""
+    import blackwell_tensor_core_fp16_gb300 as g
+    assert g.gemm_f16_set_stream_k(1) == g.OK
+    yield
+    g.gemm_f16_set_stream_k(0)

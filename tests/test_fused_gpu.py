@@ -87,7 +87,7 @@ def test_bias_and_activation(dtype, act, variant):
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("act", ["relu", "gelu"])
-def test_activation_without_bias_and_stream_k(dtype, act):
+def test_activation_without_bias_and_stream_k(dtype, act, stream_k_on):
     """No bias, and the stream-K fix-up path (the epilogue runs after the pieces are summed)."""
     M, N, K = 1000, 1032, 1536
     A, B = make_inputs(M, N, K, seed=600, a_dist="normal", a_scale=K ** -0.5,

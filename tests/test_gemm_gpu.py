@@ -262,9 +262,14 @@ def test_torch_binding():
 
 # ---- stream-K tail (caller-provided workspace) -----------------------------------------------
 
+SK_HEADER_WORDS = 8192 // 4   # stream-K workspace header: region, finished CTAs, 2 flag regions
+SK_FLAG_BASE = 64
+SK_FLAG_WORDS = (SK_HEADER_WORDS - SK_FLAG_BASE) // 2
+
+
 def run_ws(A_cpu, B_cpu, variant=0, repeats=1):
-    """Like run(), through gemm_f16_nt_ex with a workspace; also checks that the stream-K
-    counters are back to zero after every launch.  Returns (D, workspace bytes used)."""
+    """Like run(), through gemm_f16_nt_ex with a workspace; also checks the stream-K header the
+    launch leaves behind.  Returns (D, workspace bytes used)."""
     A = A_cpu.cuda()
     B = B_cpu.cuda()
     M, K = A.shape
@@ -283,10 +288,15 @@ def run_ws(A_cpu, B_cpu, variant=0, repeats=1):
         assert rc == g.OK, f"status bits 0x{bits:x}"
         assert bool((buf[:GUARD] == FILL).all()) and bool((buf[GUARD + M * N:] == FILL).all())
         if need:
-            # counters the launch used are zero again; the rest of the block is untouched fill
-            cnt = ws[:4096].view(torch.int32)
-            assert bool(((cnt == 0) | (cnt == 0x5A5A5A5A)).all()), "counters not reset"
-            assert bool((cnt[:1] == 0).all())
+            # The header is cleared before the launch, which then used flag region 0: it hands
+            # region 1 (cleared) to the next launch and leaves no CTA counted as finished; its
+            # own flags are 0 or 1.
+            hdr = ws[:4 * SK_HEADER_WORDS].view(torch.int32)
+            assert int(hdr[0]) == 1 and int(hdr[1]) == 0, (int(hdr[0]), int(hdr[1]))
+            reg0 = hdr[SK_FLAG_BASE:SK_FLAG_BASE + SK_FLAG_WORDS]
+            reg1 = hdr[SK_FLAG_BASE + SK_FLAG_WORDS:SK_FLAG_BASE + 2 * SK_FLAG_WORDS]
+            assert bool(((reg0 == 0) | (reg0 == 1)).all()) and int(reg0.sum()) > 0
+            assert bool((reg1 == 0).all())
         outs.append(D.cpu())
     return outs, need
 
@@ -300,7 +310,7 @@ SK_SHAPES = [  # shapes whose last wave runs stream-K for the pair / single-CTA 
 
 @pytest.mark.parametrize("variant", [0] + WS_VARIANTS)
 @pytest.mark.parametrize("shape", SK_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_stream_k_parity(shape, variant):
+def test_stream_k_parity(shape, variant, stream_k_on):
     M, N, K = shape
     A, B = make_inputs(M, N, K, seed=300 + M + N + K)
     outs, need = run_ws(A, B, variant, repeats=2)
@@ -310,7 +320,7 @@ def test_stream_k_parity(shape, variant):
 
 
 @pytest.mark.parametrize("name", ["square_8192", "mlp_up_16384x14336x4096"])
-def test_stream_k_large_workloads_sampled(name):
+def test_stream_k_large_workloads_sampled(name, stream_k_on):
     w = WORKLOADS[name]
     A, B = workload_inputs(w)
     outs, need = run_ws(A, B, 0)
@@ -325,7 +335,7 @@ def test_stream_k_large_workloads_sampled(name):
     assert_parity(got, ref, w.K, f"{name} stream-K (sampled)")
 
 
-def test_stream_k_matches_data_parallel_all_ones():
+def test_stream_k_matches_data_parallel_all_ones(stream_k_on):
     """All-ones inputs are exact in any summation order: the stream-K result equals K bit for
     bit in every element, including every tail tile."""
     M, N, K = 8192, 8192, 8192

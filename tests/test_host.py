@@ -376,16 +376,28 @@ def test_stream_k_tail_choice():
     assert g.gemm_f16_sk_tail_tiles(240, 76, 3) == 0          # pieces under 4 k-blocks
 
 
+SK_HEADER = 8192                         # stream-K workspace header (flags and bookkeeping)
+SK_FLAG_BASE, SK_FLAG_WORDS = 64, (8192 // 4 - 64) // 2
+MAX_CONTRIB = 4
+
+
 def test_noalloc_scratch_holds_every_gb300_workspace():
     """The allocation-free entry point's fixed array (40 MiB) holds the largest stream-K
-    workspace any variant requests on a 152-SM GB300: 4 KiB of counters plus 2 pieces x 128 x
-    256 fp32 per CTA (76 pairs or 152 single CTAs).  A device whose request would not fit (here
-    a hypothetical 200-SM part) is served by the data-parallel schedule, which needs none."""
+    workspace any variant requests on a 152-SM GB300: an 8 KiB header plus one 128 x 256 fp32
+    slot per CTA (76 pairs or 152 single CTAs).  A device whose request would not fit (here a
+    hypothetical 400-SM part) is served by the data-parallel schedule, which needs none."""
     cap = g.gemm_f16_noalloc_scratch_bytes()
     assert cap == 40 << 20
-    per_cta = 2 * 128 * 256 * 4
-    assert 4096 + 152 * per_cta <= cap            # 38.0 MiB: 1-CTA 128x256 or 76 CTA pairs
-    assert 4096 + 200 * per_cta > cap             # would take the no-workspace path
+    per_cta = 128 * 256 * 4
+    assert SK_HEADER + 152 * per_cta <= cap       # 19 MiB: 1-CTA 128x256 or 76 CTA pairs
+    assert SK_HEADER + 400 * per_cta > cap        # would take the no-workspace path
+
+
+def test_stream_k_switch():
+    assert g.gemm_f16_set_stream_k(2) == g.ERR_INVALID_ARG
+    assert g.gemm_f16_set_stream_k(-1) == g.ERR_INVALID_ARG
+    assert g.gemm_f16_set_stream_k(1) == g.OK
+    assert g.gemm_f16_set_stream_k(0) == g.OK
 
 
 def test_failure_hooks_validate_arguments():
@@ -434,31 +446,40 @@ def _replay(variant, M, N, K, units, stream_k):
     T = num_m * num_n
     R = g.gemm_f16_sk_tail_tiles(T, units, KB) if stream_k else 0
     used = units if R else min(T, units)
-    ws_bytes = 4096 + units * 2 * cg * 128 * bn * 4          # the header's workspace size
+    ws_bytes = SK_HEADER + units * cg * 128 * bn * 4         # the header's workspace size
     part_bytes = 128 * bn * 4
+    if R:
+        assert R * MAX_CONTRIB * cg <= SK_FLAG_WORDS             # the host's flag bound
     group = g.gemm_f16_raster_group(mma_m, K, 2, GB300_L2)
     stores = {}
-    written = {}      # (unit, tail tile) -> piece slot the unit wrote
-    first_tail = {}   # unit -> its first tail tile (the kernel's sk_lo / KB)
+    parked = {}       # tail tile -> units that parked partial sums for it (one slot per unit)
+    finished = {}     # tail tile -> the unit whose piece starts it and stores it
     for c in range(used):
-        for i in range(g.gemm_f16_sk_items(T, used, KB, R, c)):
+        n_items = g.gemm_f16_sk_items(T, used, KB, R, c)
+        for i in range(n_items):
             tile, kb0, kb1, piece, partial = g.gemm_f16_sk_item(T, used, KB, R, c, i)
             m_blk, n_blk = g.gemm_f16_tile_coord(tile, num_m, num_n, group)
             assert m_blk < num_m and n_blk < num_n
             assert 0 <= kb0 < kb1 <= KB and (kb0 * 64 * 2) % 16 == 0   # TMA x: 16-byte aligned
             r = tile - (T - R)
-            if r >= 0:
-                first_tail.setdefault(c, r)
-                written[(c, r)] = piece
             if partial:
-                assert piece in (0, 1)
-                for rank in range(cg):
-                    slot = (c * 2 + piece) * cg + rank
-                    assert 4096 + (slot + 1) * part_bytes <= ws_bytes
-                    assert (r * cg + rank) * 4 < 4096                     # tile counters
+                u0 = g.gemm_f16_sk_unit_of(T, used, KB, R, r * KB)
                 u1 = g.gemm_f16_sk_unit_of(T, used, KB, R, r * KB + KB - 1)
-                if c != u1:
-                    continue                                          # the last one stores
+                assert u0 <= c <= u1 and u1 - u0 < MAX_CONTRIB
+                for rank in range(cg):        # this piece's flag stays inside its region
+                    assert (r * MAX_CONTRIB + (c - u0)) * cg + rank < SK_FLAG_WORDS
+                if kb0 != 0:
+                    # parks: the unit's first stream-K piece (after any data-parallel tiles,
+                    # which wait for nothing either), into the unit's one slot
+                    assert piece == 0
+                    assert c not in {u for us in parked.values() for u in us}
+                    parked.setdefault(r, set()).add(c)
+                    for rank in range(cg):
+                        assert SK_HEADER + ((c * cg + rank) + 1) * part_bytes <= ws_bytes
+                    continue
+                # finishes: the unit's last piece (so it waits only for first pieces)
+                assert i == n_items - 1 and c == u0
+                finished[r] = c
             for rank in range(cg):
                 m0 = m_blk * mma_m + rank * 128
                 assert m0 >= 0 and n_blk * bn + rank * b_rows >= 0    # load boxes
@@ -467,12 +488,11 @@ def _replay(variant, M, N, K, units, stream_k):
                     if col0 < N and m0 < M:                           # stores never start outside
                         assert (col0 * 2) % 16 == 0
                         stores[(m0, col0)] = stores.get((m0, col0), 0) + 1
-    # the fix-up reads, for tail tile r, piece r - first_tail[u] of each contributor u
-    for r in range(R):
-        u0 = g.gemm_f16_sk_unit_of(T, used, KB, R, r * KB)
+    # the piece that finishes tail tile r reads the slots of units u0 + 1 .. u1: exactly the
+    # units that parked partial sums for it
+    for r, u0 in finished.items():
         u1 = g.gemm_f16_sk_unit_of(T, used, KB, R, r * KB + KB - 1)
-        for u in range(u0, u1 + 1):
-            assert written[(u, r)] == r - first_tail[u]
+        assert parked.get(r, set()) == set(range(u0 + 1, u1 + 1))
     expect = {(128 * i, 64 * j) for i in range(-(-M // 128)) for j in range(-(-N // 64))}
     assert set(stores) == expect and set(stores.values()) == {1}
 

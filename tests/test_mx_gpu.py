@@ -239,7 +239,7 @@ def test_fused_epilogue(variant, activation):
 
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("name", ["mx_square_2048", "ragged_1000x1800x1568"])
-def test_stream_k_tail_parity(name, variant):
+def test_stream_k_tail_parity(name, variant, stream_k_on):
     """With a workspace, the tiles of a partial last wave are split by K blocks across units
     (the pieces are summed by the last contributor).  Both shapes leave a partial last wave for
     every variant on a 152-SM GB300; the ragged one also has partial M / N tiles and a partial

@@ -3,14 +3,15 @@
 Some callers cannot allocate device memory at the moment they need a GEMM: servers whose device
 memory all belongs to their own pool, plug-ins inside a host program that owns every allocation,
 and latency-bound loops that cannot take cudaMalloc's implicit synchronisation.  gemm_f16_nt_noalloc
-serves them by running the stream-K schedule with its workspace in a fixed device array that the
-library reserves when it is loaded.
+serves them with the data-parallel schedule, or, with the stream-K tail turned on, with the
+stream-K workspace in a fixed device array that the library reserves when it is loaded.
 
-Every call shares that array and finds the previous call's partial sums and counters in it.  The
-test calls the entry point through the C ABI on a sequence of shapes whose stream-K layouts
-differ (CTA pairs with 36 tail tiles, single 128 x 128 CTAs with 72 and 96, single 128 x 256 CTAs
-with 128), one shape twice in a row and the first shape again at the end, and checks every output
-element against the CPU oracle's binary64 sum with the parity tests' bound
+Every stream-K call shares that array and finds the previous call's partial sums and flags in it.
+The test calls the entry point through the C ABI, with stream-K on and off, on a sequence of
+shapes whose stream-K layouts differ (CTA pairs with 36 tail tiles and with all 64 tiles split,
+single 128 x 128 CTAs with 72 and 96), one shape twice in a row and the first shape again at the
+end, and checks every output element against the CPU oracle's binary64 sum with the parity tests'
+bound
 |D - D_ref| <= 1e-3 * sqrt(K) + 2^-10 * |D_ref| (in full for the mid-size shapes, on sampled
 elements for 8192^3), plus the status word after each call.  The file is named so that pytest
 collects it last.
@@ -63,18 +64,32 @@ SEQUENCE = [
     (8192, 8192, 8192),    # CTA pair 256 x 256, 36 tail tiles over 76 pairs
     (1000, 1032, 1536),    # 128 x 128, all 72 tiles stream-K over 152 CTAs
     (1000, 1032, 1536),    # the same again: finds its own leftovers
-    (2048, 2048, 2048),    # 128 x 256, all 128 tiles stream-K
+    (2048, 2048, 2048),    # CTA pair, all 64 tiles stream-K
     (700, 2000, 4000),     # 128 x 128, 96 tiles
     (8192, 8192, 8192),    # back to the pair layout
 ]
 
 
-def test_noalloc_sequence_matches_oracle():
+@pytest.mark.parametrize("stream_k", [1, 0], ids=["stream_k", "data_parallel"])
+def test_noalloc_sequence_matches_oracle(stream_k):
     stream = torch.cuda.current_stream()
     cache = {}
+    assert g.gemm_f16_set_stream_k(stream_k) == g.OK
+    try:
+        _run_sequence(stream, cache, stream_k)
+    finally:
+        g.gemm_f16_set_stream_k(0)
+
+
+def _run_sequence(stream, cache, stream_k):
     for call, (M, N, K) in enumerate(SEQUENCE):
-        where = f"call {call} ({M}x{N}x{K})"
-        assert g.gemm_f16_workspace_bytes(M, N, K, 0) > 0, f"{where} is meant to use the scratch"
+        where = f"call {call} ({M}x{N}x{K}, stream-K {'on' if stream_k else 'off'})"
+        need = g.gemm_f16_workspace_bytes(M, N, K, 0)
+        if stream_k:
+            assert 0 < need <= g.gemm_f16_noalloc_scratch_bytes(), \
+                f"{where} is meant to use the scratch"
+        else:
+            assert need == 0, f"{where}: stream-K is off"
         if (M, N, K) not in cache:
             A_cpu, B_cpu = make_inputs(M, N, K, seed=900 + M + N + K, a_dist="normal",
                                        a_scale=K ** -0.5, b_dist="normal", b_scale=1.0)
