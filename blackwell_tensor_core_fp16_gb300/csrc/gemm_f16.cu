@@ -88,7 +88,7 @@ uint32_t l2_hint_setting()
     return v;
 }
 
-// Programmatic dependent launch of the persistent kernels (default on; GEMM_F16_PDL=0 turns it
+// Programmatic dependent launch of the GEMM kernels (default on; GEMM_F16_PDL=0 turns it
 // off).  With it, a GEMM launched right after another on the same stream does its set-up
 // (barriers, tensor memory, descriptor prefetch) on SMs the previous one has left, and only its
 // first global-memory access waits for the previous kernel to finish.
@@ -142,8 +142,9 @@ bool variant_info(int v, gemm_f16_variant_info* o)
 {
     switch (v) {
     case GEMM_F16_VARIANT_TILE:
-        *o = {1, 128, 128, 64, 1, (int)gf16::TileCfg::THREADS, (int)gf16::TileCfg::SMEM_ALLOC,
-              (int)gf16::TileCfg::TMEM_COLS, (int)gf16::TileCfg::STAGE_TX, 0};
+        *o = {1, 128, 128, 64, 2, (int)gf16::TileCfg<128>::THREADS,
+              (int)gf16::TileCfg<128>::SMEM_ALLOC, (int)gf16::TileCfg<128>::TMEM_COLS,
+              (int)gf16::TileCfg<128>::STAGE_TX, 0};
         return true;
     case GEMM_F16_VARIANT_WS_128x256:
         *o = {1, 128, 256, 64, 4, (int)Ws128x256::THREADS, (int)Ws128x256::SMEM_ALLOC,
@@ -175,9 +176,14 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Automatic variant, from bench.py --sweep on GB300 (back-to-back launches): the CTA pair on
 // 2048^3, 3000x5000x1000 (34.5 us against 49.9 us for 128x256), 8192^3 and the MLP shape;
 // 128x128 tiles where neither larger tile keeps half the SMs busy.
-int choose_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
+int choose_variant(int64_t M, int64_t N, int64_t K, int num_sms)
 {
     if (num_sms < 2) num_sms = 2;
+    // A few tiles of short K: the one-tile kernel with its N tile narrowed to spread D over more
+    // SMs (128 x 128 x 64: 1.82 us per launch against 2.95 us for the persistent 128 x 128
+    // kernel, graph-replayed; 1024 x 1024 x 256: 3.89 against 4.02 us; with K = 512 the
+    // persistent kernel's deeper pipeline wins, 4.97 against 5.17 us at 512^3).
+    if (K <= 256 && cdiv(M, 128) * cdiv(N, 128) <= num_sms) return GEMM_F16_VARIANT_TILE;
     const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 256);
     const int64_t tiles_128x256 = cdiv(M, 128) * cdiv(N, 256);
     // The CTA pair once its tiles occupy at least half the SMs: it loads 32 KB per CTA and
@@ -193,7 +199,7 @@ int choose_variant(int64_t M, int64_t N, int64_t /*K*/, int num_sms)
 // ---- per-device state ------------------------------------------------------------------------
 // Kernel slots (one per compiled kernel instance) for the per-device caches below:
 // 16-bit path: variant + (bf16 ? GEMM_F16_NUM_VARIANTS : 0); block-scaled path: kMxSlot0 +
-// 2 * variant + (bf16 output ? 1 : 0).
+// 2 * variant + (bf16 output ? 1 : 0); the one-tile kernel's four N tiles: 56 .. 59.
 constexpr int kMxSlot0 = 32;
 constexpr int kNumSlots = 64;
 
@@ -378,22 +384,47 @@ int get_maps(const MapKey& k, uint32_t a_box_rows, uint32_t b_box_rows, bool nee
 }
 
 // ---- launches --------------------------------------------------------------------------------
+// The tile variant's N tile: the narrowest of 16, 32, 64 whose grid still fits one wave of
+// `sms` CTAs, else 128.  A small D then spreads over more SMs, each loading and storing less.
+int tile_bn_for(int64_t M, int64_t N, int sms)
+{
+    for (int bn = 16; bn < 128; bn *= 2)
+        if (cdiv(M, 128) * cdiv(N, bn) <= sms) return bn;
+    return 128;
+}
+
+template <uint32_t kBN>
 int launch_tile(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                 cudaStream_t stream, DeviceState& d, int dev)
 {
-    using C = gf16::TileCfg;
-    int rc = ensure_smem(d, GEMM_F16_VARIANT_TILE, gf16::gemm_tile_kernel, C::SMEM_ALLOC);
+    using C = gf16::TileCfg<kBN>;
+    // kernel slots 56 .. 59 and descriptor-cache keys 116 .. 228, one per N tile
+    constexpr int slot = kBN == 16 ? 56 : kBN == 32 ? 57 : kBN == 64 ? 58 : 59;
+    int rc = ensure_smem(d, slot, gf16::gemm_tile_kernel<kBN>, C::SMEM_ALLOC);
     if (rc != GEMM_F16_OK) return rc;
     const MapEntry* maps = nullptr;
-    MapKey key{A, B, D, M, N, K, GEMM_F16_VARIANT_TILE, dev};
-    if ((rc = get_maps(key, 128, 128, false, &maps)) != GEMM_F16_OK) return rc;
-    const dim3 grid(static_cast<uint32_t>(cdiv(N, 128)), static_cast<uint32_t>(cdiv(M, 128)));
+    MapKey key{A, B, D, M, N, K, 100 + static_cast<int>(kBN), dev};
+    if ((rc = get_maps(key, 128, kBN, false, &maps)) != GEMM_F16_OK) return rc;
+    const dim3 grid(static_cast<uint32_t>(cdiv(N, kBN)), static_cast<uint32_t>(cdiv(M, 128)));
     if (grid.y > 65535u) return fail(GEMM_F16_ERR_UNSUPPORTED, "M too large for the tile variant");
-    gf16::gemm_tile_kernel<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(
-        maps->ma, maps->mb, static_cast<uint16_t*>(D), (uint32_t)M, (uint32_t)N, (uint32_t)cdiv(K, 64),
-        wait_timeout_ns(), debug_flags());
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch of gemm_tile_kernel");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    if (pdl_setting()) {
+        // The kernel waits (griddepcontrol.wait) before its first global-memory access.
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gf16::gemm_tile_kernel<kBN>, maps->ma, maps->mb,
+                                       static_cast<uint16_t*>(D), (uint32_t)M, (uint32_t)N,
+                                       (uint32_t)cdiv(K, 64), wait_timeout_ns(), debug_flags());
+    if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_tile_kernel)");
     return GEMM_F16_OK;
 }
 
@@ -605,9 +636,13 @@ int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
     if ((rc = device_state(&d)) != GEMM_F16_OK) return rc;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (variant == GEMM_F16_VARIANT_AUTO) variant = choose_variant(M, N, K, d->sms);
     const bool plain = epi.dtype == GEMM_F16_DTYPE_F16 && epi.bias == nullptr &&
                        epi.act == GEMM_F16_ACT_NONE;
+    if (variant == GEMM_F16_VARIANT_AUTO) {
+        variant = choose_variant(M, N, K, d->sms);
+        // the one-tile kernel has no bf16 / fused-epilogue form
+        if (!plain && variant == GEMM_F16_VARIANT_TILE) variant = GEMM_F16_VARIANT_WS_128x128;
+    }
     if (!plain) {
         if (epi.dtype != GEMM_F16_DTYPE_F16 && epi.dtype != GEMM_F16_DTYPE_BF16)
             return fail(GEMM_F16_ERR_INVALID_ARG, "unknown dtype %d", epi.dtype);
@@ -648,7 +683,12 @@ int run(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
     switch (variant) {
     case GEMM_F16_VARIANT_TILE:
         if (bytes_needed) return GEMM_F16_OK;
-        return launch_tile(A, B, D, M, N, K, stream, *d, dev);
+        switch (tile_bn_for(M, N, d->sms)) {
+        case 16: return launch_tile<16>(A, B, D, M, N, K, stream, *d, dev);
+        case 32: return launch_tile<32>(A, B, D, M, N, K, stream, *d, dev);
+        case 64: return launch_tile<64>(A, B, D, M, N, K, stream, *d, dev);
+        default: return launch_tile<128>(A, B, D, M, N, K, stream, *d, dev);
+        }
     case GEMM_F16_VARIANT_WS_128x256:
         return launch_ws<1, 256, 4, true>(variant, A, B, D, M, N, K, stream, *d, dev, ws,
                                           ws_bytes, bytes_needed);

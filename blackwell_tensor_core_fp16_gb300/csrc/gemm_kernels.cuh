@@ -93,39 +93,47 @@ constexpr uint32_t kBlockK = 64;   // one 128-byte swizzle row of fp16
 constexpr uint32_t kUmmaK = 16;    // K per tcgen05.mma of kind::f16
 
 // ==============================================================================================
-// gemm_tile_kernel: one 128 x 128 tile per CTA, single stage, synchronous K loop.
+// gemm_tile_kernel: one 128 x kBN tile per CTA (kBN = 16 .. 128), a two-stage K loop run by one
+// thread (the load of k-block kb + 1 overlaps the MMAs of k-block kb), the epilogue stores from
+// registers.  For problems of a few tiles, where a launch's fixed costs dominate: a narrow kBN
+// spreads a small D over more SMs, each loading and storing less.
 // ==============================================================================================
+template <uint32_t kBN>
 struct TileCfg {
-    static constexpr uint32_t BN = 128;
+    static_assert(kBN >= 16 && kBN <= 128 && kBN % 16 == 0, "N of a kind::f16 MMA with M = 128");
+    static constexpr uint32_t BN = kBN;
     static constexpr uint32_t A_BYTES = kBlockM * kBlockK * 2;  // 16384
-    static constexpr uint32_t B_BYTES = BN * kBlockK * 2;       // 16384
-    static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;     // 32768
-    static constexpr uint32_t OFF_A = 0;
-    static constexpr uint32_t OFF_B = A_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_B + B_BYTES;        // tma, mma, drain
-    static constexpr uint32_t OFF_SLOT = OFF_BAR + 3 * 8;
+    static constexpr uint32_t B_BYTES = BN * kBlockK * 2;       // 2048 .. 16384
+    static constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+    static constexpr uint32_t STAGE_BYTES = (STAGE_TX + 1023u) & ~1023u;
+    static constexpr uint32_t STAGES = 2;
+    static constexpr uint32_t OFF_BAR = STAGES * STAGE_BYTES;   // tma x2, mma, drain
+    static constexpr uint32_t OFF_SLOT = OFF_BAR + 4 * 8;
     static constexpr uint32_t OFF_ABORT = OFF_SLOT + 4;
     static constexpr uint32_t SMEM_ALLOC = OFF_ABORT + 4 + 1024;
-    static constexpr uint32_t TMEM_COLS = 128;
+    static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;   // a power of two >= 32
+    static constexpr uint32_t LD_CHUNKS = (BN + 31) / 32;     // 32-column TMEM loads
     static constexpr uint32_t THREADS = 128;
 };
 
+template <uint32_t kBN>
 __global__ void __launch_bounds__(128, 1)
     gemm_tile_kernel(const __grid_constant__ CUtensorMap tmap_a,
                      const __grid_constant__ CUtensorMap tmap_b, uint16_t* __restrict__ D,
                      uint32_t M, uint32_t N, uint32_t num_k_blocks, uint64_t timeout_ns,
                      uint32_t debug_flags)
 {
-    using C = TileCfg;
+    using C = TileCfg<kBN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
-    const uint32_t sA = base + C::OFF_A;
-    const uint32_t sB = base + C::OFF_B;
-    const uint32_t tma_bar = base + C::OFF_BAR;
-    const uint32_t mma_bar = tma_bar + 8;
-    const uint32_t drain_bar = tma_bar + 16;
+    const auto stage_a = [&](uint32_t s) { return base + s * C::STAGE_BYTES; };
+    const auto stage_b = [&](uint32_t s) { return base + s * C::STAGE_BYTES + C::A_BYTES; };
+    const uint32_t bar0 = base + C::OFF_BAR;
+    const auto tma_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+    const uint32_t mma_bar = bar0 + 16;
+    const uint32_t drain_bar = bar0 + 24;
     volatile uint32_t* slot_ptr = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_SLOT);
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base_ptr + C::OFF_ABORT);
 
@@ -138,7 +146,8 @@ __global__ void __launch_bounds__(128, 1)
     if (threadIdx.x == 0) {
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
-        mbar_init(tma_bar, 1);
+        mbar_init(tma_bar(0), 1);
+        mbar_init(tma_bar(1), 1);
         mbar_init(mma_bar, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0u;
@@ -150,43 +159,74 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     tcgen05_fence_after();
     const uint32_t tmem_base = *slot_ptr;
+    // As in the persistent kernels: the set-up above may overlap the end of the previous kernel
+    // on the stream; global memory (A and B may be its output, D its input) waits for it.
+    grid_dep_launch();
+    grid_dep_wait();
 
     if (threadIdx.x == 0) {
-        uint32_t phase = 0;
+        const bool loads = !(debug_flags & kDebugNoLoads);
+        uint32_t loaded = 0, landed = 0;   // k-blocks whose loads were issued / waited for
+        const auto load = [&](uint32_t kb) {
+            const uint32_t s = kb & 1u;
+            const int32_t k0 = static_cast<int32_t>(kb * kBlockK);
+            mbar_arrive_expect_tx(tma_bar(s), C::STAGE_TX);
+            tma_load_2d(stage_a(s), &tmap_a, tma_bar(s), k0, m0);
+            tma_load_2d(stage_b(s), &tmap_b, tma_bar(s), k0, n0);
+            ++loaded;
+        };
         bool ok = true;
         bool issued_mma = false;
+        // Phase j of mma_bar completes when the MMAs of k-block j are done.  A parity names one
+        // phase only while at most one phase is pending, so each k-block's MMAs are committed
+        // only after the previous k-block's are done (which also frees that k-block's stage for
+        // the next load), and the phases are waited for in order.
+        uint32_t mma_done = 0;
+        const auto wait_mma = [&](uint32_t upto) {   // phases mma_done .. upto - 1
+            for (; mma_done < upto; ++mma_done)
+                if (!mbar_wait(mma_bar, mma_done & 1u, abort_flag, timeout_ns)) return false;
+            return true;
+        };
+        if (loads) load(0);
         for (uint32_t kb = 0; kb < num_k_blocks; ++kb) {
-            const int32_t k0 = static_cast<int32_t>(kb * kBlockK);
-            if (!(debug_flags & kDebugNoLoads)) {
-                mbar_arrive_expect_tx(tma_bar, C::STAGE_TX);
-                tma_load_2d(sA, &tmap_a, tma_bar, k0, m0);
-                tma_load_2d(sB, &tmap_b, tma_bar, k0, n0);
-            }
-            if (!mbar_wait(tma_bar, phase, abort_flag, timeout_ns)) {
-                report(kStatusProducerTimeout, abort_flag);
-                ok = false;
-                break;
-            }
-            tcgen05_fence_after();
-            const uint64_t ad = make_smem_desc_sw128(sA, 1024);
-            const uint64_t bd = make_smem_desc_sw128(sB, 1024);
-#pragma unroll
-            for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
-                mma_f16<1>(tmem_base, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0u);
-            mma_commit(mma_bar);
-            issued_mma = true;
-            if (!mbar_wait(mma_bar, phase, abort_flag, timeout_ns)) {
+            const uint32_t s = kb & 1u;
+            if (!wait_mma(kb)) {
                 report(kStatusMmaTimeout, abort_flag);
                 ok = false;
                 break;
             }
-            phase ^= 1u;
+            // the other stage was last read by the MMAs of k-block kb - 1, now done
+            if (kb + 1 < num_k_blocks && loads) load(kb + 1);
+            if (!mbar_wait(tma_bar(s), (kb >> 1) & 1u, abort_flag, timeout_ns)) {
+                report(kStatusProducerTimeout, abort_flag);
+                ok = false;
+                break;
+            }
+            ++landed;
+            tcgen05_fence_after();
+            const uint64_t ad = make_smem_desc_sw128(stage_a(s), 1024);
+            const uint64_t bd = make_smem_desc_sw128(stage_b(s), 1024);
+#pragma unroll
+            for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
+                mma_f16<1>(tmem_base, ad + 2ull * k, bd + 2ull * k, idesc, (kb | k) != 0u);
+            mma_commit(mma_bar);   // phase kb of mma_bar: the MMAs of k-block kb are done
+            issued_mma = true;
         }
-        if (!ok && issued_mma) {
-            // Let every MMA this thread issued finish before TMEM is freed.
-            mma_commit(drain_bar);
-            if (!mbar_wait(drain_bar, 0, nullptr, timeout_ns))
-                atomicOr(&gemm_f16_status_word, kStatusDrainTimeout);
+        if (ok && !wait_mma(num_k_blocks)) {
+            report(kStatusMmaTimeout, abort_flag);
+            ok = false;
+        }
+        if (!ok) {
+            // Let every MMA this thread issued finish before TMEM is freed, and every load
+            // issued land before the CTA exits (bounded waits that ignore the abort flag).
+            if (issued_mma) {
+                mma_commit(drain_bar);
+                if (!mbar_wait(drain_bar, 0, nullptr, timeout_ns))
+                    atomicOr(&gemm_f16_status_word, kStatusDrainTimeout);
+            }
+            for (uint32_t kb = landed; kb < loaded; ++kb)
+                if (!mbar_wait(tma_bar(kb & 1u), (kb >> 1) & 1u, nullptr, timeout_ns))
+                    atomicOr(&gemm_f16_status_word, kStatusDrainTimeout);
         }
     }
     __syncwarp();
@@ -195,22 +235,26 @@ __global__ void __launch_bounds__(128, 1)
     tcgen05_fence_after();
 
     if (*abort_flag == 0u) {
-        // TMEM lane = row of the tile; warp w may read lanes 32w .. 32w + 31.
+        // TMEM lane = row of the tile; warp w may read lanes 32w .. 32w + 31.  All the 32-column
+        // loads are in flight before one wait (past column BN they read unused columns).
         const uint32_t row = warp * 32u + lane;
         const uint32_t grow = static_cast<uint32_t>(m0) + row;
-#pragma unroll 1
-        for (uint32_t c = 0; c < C::BN / 32u; ++c) {
-            uint32_t v[32];
-            tmem_ld_32x32b_x32(tmem_base + ((warp * 32u) << 16), v, static_cast<int>(c * 32u));
-            tmem_ld_wait();
-            uint32_t p[16];
+        uint32_t v[C::LD_CHUNKS][32];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) p[i] = pack_f16x2_rn(v[2 * i], v[2 * i + 1]);
-            if (grow < M) {
+        for (uint32_t c = 0; c < C::LD_CHUNKS; ++c)
+            tmem_ld_32x32b_x32(tmem_base + ((warp * 32u) << 16), v[c], static_cast<int>(c * 32u));
+        tmem_ld_wait();
+        if (grow < M) {
+#pragma unroll
+            for (uint32_t c = 0; c < C::LD_CHUNKS; ++c) {
+                uint32_t p[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) p[i] = pack_f16x2_rn(v[c][2 * i], v[c][2 * i + 1]);
 #pragma unroll
                 for (uint32_t q = 0; q < 4; ++q) {
                     const uint32_t col = static_cast<uint32_t>(n0) + c * 32u + q * 8u;
-                    if (col < N)  // N is a multiple of 8: a vector is all in or all out
+                    // N is a multiple of 8: a vector is all in or all out
+                    if (c * 32u + q * 8u < C::BN && col < N)
                         st_global_v4(D + static_cast<uint64_t>(grow) * N + col, p[4 * q],
                                      p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
                 }

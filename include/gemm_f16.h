@@ -57,7 +57,10 @@ extern "C" {
 
 /* Kernel variants (gemm_f16_nt_variant).  All compute the same D. */
 #define GEMM_F16_VARIANT_AUTO 0       /* choose by shape and device */
-#define GEMM_F16_VARIANT_TILE 1       /* one 128x128 tile per CTA, synchronous K loop */
+#define GEMM_F16_VARIANT_TILE 1       /* one 128 x n tile per CTA, two-stage K loop; n is the
+                                         narrowest of 16, 32, 64 whose grid fits one wave, else
+                                         128 (fp16 only; chosen for short K and at most one wave
+                                         of 128 x 128 tiles) */
 #define GEMM_F16_VARIANT_WS_128x256 2 /* persistent, warp-specialised, 1 CTA per 128x256 tile */
 #define GEMM_F16_VARIANT_WS_PAIR 3    /* persistent, warp-specialised, CTA pair per 256x256 */
 #define GEMM_F16_VARIANT_WS_128x128 4 /* persistent, warp-specialised, 1 CTA per 128x128 tile */

@@ -232,11 +232,16 @@ def test_choose_variant_returns_a_variant():
 
 
 def test_choose_variant_on_the_workloads():
-    """The automatic choice on a 152-SM GB300 for the five workloads: one 128 x 128 CTA for the
-    single tile, the 256 x 256 CTA pair for every other (2048^3 has 64 pair tiles: at least half
-    the SMs), and 128 x 256 / 128 x 128 for shapes too short for a pair."""
+    """The automatic choice on a 152-SM GB300 for the five workloads: the one-tile kernel for the
+    single tile (short K, a grid of at most one wave), the 256 x 256 CTA pair for every other
+    (2048^3 has 64 pair tiles: at least half the SMs), and 128 x 256 / 128 x 128 for shapes too
+    short for a pair."""
     pair, w256, w128 = g.VARIANTS["ws_pair"], g.VARIANTS["ws_128x256"], g.VARIANTS["ws_128x128"]
-    assert g.gemm_f16_choose_variant(128, 128, 64, 152) == w128
+    tile = g.VARIANTS["tile"]
+    assert g.gemm_f16_choose_variant(128, 128, 64, 152) == tile
+    assert g.gemm_f16_choose_variant(1024, 1024, 256, 152) == tile      # 64 tiles, K = 256
+    assert g.gemm_f16_choose_variant(1024, 1024, 512, 152) == w128      # K = 512: the pipeline
+    assert g.gemm_f16_choose_variant(2048, 2048, 64, 152) != tile       # 256 tiles: over a wave
     for shape in [(2048, 2048, 2048), (3000, 5000, 1000), (8192, 8192, 8192),
                   (16384, 14336, 4096)]:
         assert g.gemm_f16_choose_variant(*shape, 152) == pair, shape
