@@ -38,6 +38,7 @@
 
 #include <cstdarg>
 #include <cstdint>
+#include <cstdlib>
 #include <atomic>
 #include <cstdio>
 #include <mutex>
@@ -136,6 +137,10 @@ __global__ void gdn_chunk_list_kernel(const int32_t* __restrict__ cu, int32_t n_
                                       uint32_t* __restrict__ status, int32_t* __restrict__ order,
                                       int4* __restrict__ seqinfo, uint32_t* __restrict__ counter)
 {
+    // The call's first kernel, launched programmatically: it waits for whatever ran before it
+    // on the stream (which may have written cu_seqlens, or still read the workspace's tables)
+    // before it reads or writes anything, and only then lets the prepare kernel start.
+    grid_dep_wait();
     grid_dep_launch();   // the prepare kernel may set itself up meanwhile
     bool bad = false;
     for (int32_t i = threadIdx.x; i < n_seqs; i += blockDim.x)
@@ -391,17 +396,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
                        int32_t kgroup, int32_t clear_status, __nv_bfloat16* __restrict__ ap,
                        float* __restrict__ gam_out, int32_t single_T,
                        const int32_t* __restrict__ cu, uint32_t* __restrict__ status,
-                       uint32_t* __restrict__ counter, uint64_t wait_ns)
+                       uint32_t* __restrict__ counter, uint64_t wait_ns, int32_t first_in_call)
 {
     const int32_t ch = blockIdx.x;
     const int32_t j = blockIdx.y;
     // This kernel may start while the kernel before it on the stream (the chunk list, or the
     // previous pass's scan) still runs.  Until grid_dep_wait() it reads only the call's inputs
     // (q, k, v, alpha, beta); the chunk list, the workspace and the counter wait for it.  Every
-    // CTA passes grid_dep_wait() before it exits.
+    // CTA passes grid_dep_wait() before it exits.  As a call's first kernel (one sequence, first
+    // pass) it waits before anything: the kernel before it may be the previous call's scan, or
+    // whatever wrote this call's inputs; and the scan may start only after that wait (it reads
+    // its initial state early, which may be the previous call's final state).
+    if (first_in_call) grid_dep_wait();
     grid_dep_launch();   // the scan may set itself up meanwhile
     // one sequence (single_T >= 0): chunk ch covers tokens 64 ch .. (no chunk list is built;
-    // the first pass of a call, always launched after everything before it, checks that the
+    // the first pass of a call, past its wait for everything before it, checks that the
     // offsets are [0, single_T] and sets the call's status word here, and offsets that are not
     // leave every chunk undone); otherwise the chunk list says
     int32_t t0, len;
@@ -1892,13 +1901,26 @@ int gdn_ensure_smem(int dev)
     return GDN_OK;
 }
 
-// Launches `kernel` on `stream`.  The first kernel of a call (first == true, which this clears)
-// is ordered after all earlier work as usual; a later one is launched with programmatic stream
-// serialization, so it may start as soon as every CTA of its predecessor has called
-// grid_dep_launch(); it then waits in grid_dep_wait() for the predecessor to finish.
+// Launches `kernel` on `stream` with programmatic stream serialization: it may start as soon as
+// every CTA of the kernel before it has called grid_dep_launch() (or at once, when that kernel
+// never does), and waits in grid_dep_wait() for it to finish before it touches what that kernel
+// may write.  A call's first kernel waits before it touches any memory at all (the kernel before
+// it belongs to the caller), so consecutive calls, and a call after a GEMM of this library,
+// overlap their launch gaps.
+// GDN_PDL=0 (read once per process) launches a call's first kernel the plain way instead, for
+// comparison; its wait then returns at once.
+bool gdn_first_pdl()
+{
+    static const bool v = [] {
+        const char* e = std::getenv("GDN_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return v;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t gdn_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, bool& first, Args... args)
+                       cudaStream_t stream, bool first, Args... args)
 {
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1909,8 +1931,7 @@ cudaError_t gdn_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = first ? 0u : 1u;
-    first = false;
+    cfg.numAttrs = (first && !gdn_first_pdl()) ? 0u : 1u;
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
@@ -2033,12 +2054,11 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
             return rc;
     }
 
-    // The call's first kernel starts after all earlier work on the stream; each later one may
-    // start while the one before it finishes (programmatic dependent launch: the kernels wait
-    // for their predecessor before they touch what it writes).
-    bool first = true;
+    // Each kernel may start while the one before it finishes (programmatic dependent launch:
+    // the kernels wait for their predecessor before they touch what it writes, and the call's
+    // first kernel, the chunk list or the first pass's prepare, before it touches anything).
     if (single_T < 0) {
-        e = gdn_launch(gdn_chunk_list_kernel, dim3(1), dim3(1024), 0, stream, first, cu_seqlens,
+        e = gdn_launch(gdn_chunk_list_kernel, dim3(1), dim3(1024), 0, stream, true, cu_seqlens,
                        static_cast<int32_t>(n_seqs), static_cast<int32_t>(total_tokens),
                        chunk_offset, chunks,
                        static_cast<int32_t>(mc), n_chunks, status, order, seqinfo, counter);
@@ -2051,11 +2071,13 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
         if (mc > 0 && total_tokens > 0) {
             const dim3 pgrid(static_cast<uint32_t>(mc), static_cast<uint32_t>(h_v));
             e = gdn_launch(gdn_prepare_kernel, pgrid, dim3(kPrepThreads), kPrepSmem, stream,
-                           first, map_q[gp], map_k, map_v, map_w, map_ut, alpha, beta,
+                           single_T >= 0 && gp == 0, map_q[gp], map_k, map_v, map_w, map_ut,
+                           alpha, beta,
                            static_cast<const int4*>(chunks), static_cast<const int32_t*>(n_chunks),
                            static_cast<int32_t>(h_v), qgroup, kgroup,
                            static_cast<int32_t>(gp == 0), ap, gm, single_T, cu_seqlens, status,
-                           counter, g_gdn_wait_ns.load());
+                           counter, g_gdn_wait_ns.load(),
+                           static_cast<int32_t>(single_T >= 0 && gp == 0));
             if (e != cudaSuccess)
                 return gdn_fail(GDN_ERR_CUDA, "gdn_prepare_kernel: %s", cudaGetErrorString(e));
         }
@@ -2079,7 +2101,7 @@ int gdn_prefill_heads(const void* q, const void* k, const void* v, const float* 
         e = gdn_launch(scan, dim3(static_cast<uint32_t>(ctas)),
                        dim3(tensor_core ? tc::kThreads : kScanThreads),
                        !tensor_core ? kScanSmem : wide ? tc::Cfg<32>::kSmem : tc::Cfg<16>::kSmem,
-                       stream, first, map_w, map_a, map_q[gp], map_k,
+                       stream, false, map_w, map_a, map_q[gp], map_k,
                        static_cast<const int32_t*>(single_T >= 0 ? nullptr : order),
                        static_cast<const int4*>(single_T >= 0 ? nullptr : seqinfo), counter,
                        static_cast<int32_t>(items), static_cast<const float*>(ut),
@@ -2141,9 +2163,8 @@ int gdn_check_offsets(const int32_t* cu_seqlens, int64_t n_seqs, int64_t total_t
         return gdn_fail(GDN_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) needed",
                         l.total);
     auto* ws = static_cast<uint8_t*>(workspace);
-    bool first = true;
     const cudaError_t e = gdn_launch(
-        gdn_chunk_list_kernel, dim3(1), dim3(1024), 0, stream, first, cu_seqlens,
+        gdn_chunk_list_kernel, dim3(1), dim3(1024), 0, stream, true, cu_seqlens,
         static_cast<int32_t>(n_seqs), static_cast<int32_t>(total_tokens),
         reinterpret_cast<int32_t*>(ws + l.chunk_offset), reinterpret_cast<int4*>(ws + l.chunks),
         static_cast<int32_t>(max_chunks_for(total_tokens, n_seqs)),

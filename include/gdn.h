@@ -57,8 +57,10 @@
  *
  * Ownership: the caller owns every buffer; nothing is retained after a call.  Apart from the
  * state pair above, no written buffer may overlap another buffer of the call.  Asynchronous on
- * `stream`: the call's first kernel starts after all earlier work on the stream, and its later
- * kernels use programmatic dependent launch among themselves.  A call enqueues kernel launches
+ * `stream`, in stream order: every kernel of a call is launched with programmatic dependent
+ * launch, so it may be placed while the kernel before it finishes; the call's first kernel waits
+ * for all earlier work on the stream before it reads or writes anything, the later ones before
+ * they touch what an earlier kernel of the call writes.  A call enqueues kernel launches
  * only (no allocation, copy or synchronisation), so it may be recorded into a CUDA graph; the
  * first call on each device also sets the kernels' shared-memory attributes, so make that one
  * outside a capture.  Errors: GDN_ERR_INVALID_ARG (null pointer, negative size, heads in none of the
