@@ -110,6 +110,25 @@ def test_ragged_shapes(shape, variant):
     full_parity(A, B, variant, f"{shape} variant {variant}")
 
 
+# The one-tile variant narrows its N tile to the narrowest of 16, 32, 64 whose grid fits one
+# wave of 152 CTAs, else 128.  One shape per tile width (the ragged shapes above take 16 and 32),
+# with K tails and odd k-block counts for its two-stage K loop.
+TILE_N_SHAPES = [
+    (128, 128, 64),       # 8 CTAs of 128 x 16
+    (128, 4096, 200),     # 128 CTAs of 128 x 32 (4 k-blocks, the last of 8)
+    (1000, 1032, 328),    # 136 CTAs of 128 x 64 (6 k-blocks, K tail of 8)
+    (2048, 1000, 136),    # 128 x 128 tiles, 128 CTAs (3 k-blocks)
+    (3000, 2048, 64),     # 128 x 128 tiles, 384 CTAs: more than one wave
+]
+
+
+@pytest.mark.parametrize("shape", TILE_N_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tile_variant_every_n_tile(shape):
+    M, N, K = shape
+    A, B = make_inputs(M, N, K, seed=700 + M + N + K)
+    full_parity(A, B, g.VARIANTS["tile"], f"{shape} one-tile variant")
+
+
 @pytest.mark.parametrize("variant", [0] + WS_VARIANTS)
 def test_square_2048_workload(variant):
     A, B = workload_inputs(WORKLOADS["square_2048"])
