@@ -26,6 +26,7 @@ __all__ = [
     "gemm_f16_set_fault_injection",
     "gemm_f16_sk_tail_tiles", "gemm_f16_raster_group", "gemm_f16_set_stream_k",
     "gemm_f16_sk_items", "gemm_f16_sk_item", "gemm_f16_sk_unit_of",
+    "gemm_f16_half_tail_tiles", "gemm_f16_half_items", "gemm_f16_half_item",
     "exported_symbols", "VARIANTS", "STATUS",
 ]
 
@@ -125,6 +126,12 @@ def load():
         lib.gemm_f16_sk_item.restype = None
         lib.gemm_f16_sk_unit_of.argtypes = [u32, u32, u32, u32, u32]
         lib.gemm_f16_sk_unit_of.restype = u32
+        lib.gemm_f16_half_tail_tiles.argtypes = [i64, i64]
+        lib.gemm_f16_half_tail_tiles.restype = i64
+        lib.gemm_f16_half_items.argtypes = [u32, u32, u32, u32, u32]
+        lib.gemm_f16_half_items.restype = u32
+        lib.gemm_f16_half_item.argtypes = [u32, u32, u32, u32, u32, u32, u32p]
+        lib.gemm_f16_half_item.restype = None
         lib.gemm_mxf8_nt.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, i32, i32, vp, i32,
                                      i32, vp, sz, vp]
         lib.gemm_mxf8_nt.restype = i32
@@ -279,6 +286,20 @@ def gemm_f16_sk_item(tiles: int, units: int, k_blocks: int, tail: int, unit: int
 
 def gemm_f16_sk_unit_of(tiles: int, units: int, k_blocks: int, tail: int, x: int) -> int:
     return load().gemm_f16_sk_unit_of(tiles, units, k_blocks, tail, x)
+
+
+def gemm_f16_half_tail_tiles(tiles: int, units: int) -> int:
+    return load().gemm_f16_half_tail_tiles(tiles, units)
+
+
+def gemm_f16_half_items(tiles: int, units: int, k_blocks: int, half: int, unit: int) -> int:
+    return load().gemm_f16_half_items(tiles, units, k_blocks, half, unit)
+
+
+def gemm_f16_half_item(tiles: int, units: int, k_blocks: int, half: int, unit: int, idx: int):
+    out = (ctypes.c_uint32 * 4)()
+    load().gemm_f16_half_item(tiles, units, k_blocks, half, unit, idx, out)
+    return tuple(out)
 
 
 def gemm_f16_choose_variant(M: int, N: int, K: int, num_sms: int) -> int:

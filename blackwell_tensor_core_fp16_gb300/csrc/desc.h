@@ -174,19 +174,26 @@ GF16_HD TileCoord tile_coord(uint32_t t, uint32_t num_m, uint32_t num_n, uint32_
 //     R <= S a range is at most KB long, so a unit has at most two pieces, and a tail tile has
 //     at most ceil(S / R) + 1 contributors.
 // A piece that does not cover its whole tile is "partial": its fp32 accumulator is summed with
-// the other pieces of that tile by whichever contributor finishes last.
+// the other pieces of the tile by the piece that starts the tile.
+//
+// Half-width tail (H > 0, then R = 0): the last H tiles (the partial wave, or every tile when
+// there are fewer tiles than units), each cut into two items of half its columns, so that the
+// 2 H <= U items run in about half a tile's time: unit c < 2 H takes half c % 2 of tail tile
+// T - H + c / 2 after its data-parallel tiles [0, T - H), a multiple of U.
 // ---------------------------------------------------------------------------------------------
 struct WorkSplit {
     uint32_t T, U, KB, R;
-    uint32_t S;  // units sharing the stream-K k-blocks (units S .. U-1 get none); S <= U
+    uint32_t S;      // units sharing the stream-K k-blocks (units S .. U-1 get none); S <= U
+    uint32_t H = 0;  // tail tiles cut into two half-width items (0: none)
 };
 
 struct WorkItem {
-    uint32_t tile;     // tile number in the grouped order
-    uint32_t kb0;      // first k-block
-    uint32_t kb1;      // one past the last k-block
-    uint32_t piece;    // 0 or 1 for stream-K pieces (workspace slot), unused otherwise
-    uint32_t partial;  // 1 if the piece's accumulator must be combined with others
+    uint32_t tile;      // tile number in the grouped order
+    uint32_t kb0;       // first k-block
+    uint32_t kb1;       // one past the last k-block
+    uint32_t piece;     // 0 or 1 for stream-K pieces (workspace slot), unused otherwise
+    uint32_t partial;   // 1 if the piece's accumulator must be combined with others
+    uint32_t half = 0;  // 0: the whole tile; 1, 2: its first or second half of the columns
 };
 
 GF16_HD uint32_t sk_lo(const WorkSplit& w, uint32_t c)
@@ -197,9 +204,14 @@ GF16_HD uint32_t sk_lo(const WorkSplit& w, uint32_t c)
 
 GF16_HD uint32_t dp_tiles_of(const WorkSplit& w, uint32_t c)
 {
-    const uint32_t dp = w.T - w.R;
-    if (w.R > 0) return dp / w.U;
+    const uint32_t dp = w.T - w.R - w.H;
+    if (w.R > 0 || w.H > 0) return dp / w.U;
     return c < dp ? (dp - c + w.U - 1) / w.U : 0u;
+}
+
+GF16_HD uint32_t half_items_of(const WorkSplit& w, uint32_t c)
+{
+    return c < 2u * w.H ? 1u : 0u;
 }
 
 GF16_HD uint32_t sk_pieces_of(const WorkSplit& w, uint32_t c)
@@ -211,19 +223,21 @@ GF16_HD uint32_t sk_pieces_of(const WorkSplit& w, uint32_t c)
 
 GF16_HD uint32_t items_of(const WorkSplit& w, uint32_t c)
 {
-    return dp_tiles_of(w, c) + sk_pieces_of(w, c);
+    return dp_tiles_of(w, c) + sk_pieces_of(w, c) + half_items_of(w, c);
 }
 
 // Total k-block iterations of unit c (the pipeline counters run over these).
 GF16_HD uint32_t iterations_of(const WorkSplit& w, uint32_t c)
 {
-    return dp_tiles_of(w, c) * w.KB + (w.R ? sk_lo(w, c + 1) - sk_lo(w, c) : 0u);
+    return dp_tiles_of(w, c) * w.KB + (w.R ? sk_lo(w, c + 1) - sk_lo(w, c) : 0u) +
+           half_items_of(w, c) * w.KB;
 }
 
 GF16_HD WorkItem work_item(const WorkSplit& w, uint32_t c, uint32_t idx)
 {
     const uint32_t ndp = dp_tiles_of(w, c);
     if (idx < ndp) return WorkItem{c + idx * w.U, 0u, w.KB, 0u, 0u};
+    if (w.H > 0) return WorkItem{w.T - w.H + c / 2u, 0u, w.KB, 0u, 0u, 1u + c % 2u};
     const uint32_t j = idx - ndp;
     const uint32_t lo = sk_lo(w, c), hi = sk_lo(w, c + 1);
     const uint32_t r = lo / w.KB + j;

@@ -337,6 +337,7 @@ struct MapKey {
 struct MapEntry {
     MapKey key;
     CUtensorMap ma, mb, md, msfa, msfb;
+    CUtensorMap mbh;   // B in boxes of half the rows (half-width tail items; 16-bit path)
     bool valid;
 };
 
@@ -365,6 +366,12 @@ int get_maps(const MapKey& k, uint32_t a_box_rows, uint32_t b_box_rows, bool nee
         return rc;
     if ((rc = make_map(&e.mb, k.b, k.N, k.K, b_box_rows, box_k, !mx && bf, mx)) != GEMM_F16_OK)
         return rc;
+    if (!mx && b_box_rows >= 16) {
+        if ((rc = make_map(&e.mbh, k.b, k.N, k.K, b_box_rows / 2, box_k, bf)) != GEMM_F16_OK)
+            return rc;
+    } else {
+        std::memset(&e.mbh, 0, sizeof(e.mbh));
+    }
     if (need_d) {
         if ((rc = make_map(&e.md, k.d, k.M, k.N, 128, 64, bf)) != GEMM_F16_OK) return rc;
     } else {
@@ -446,6 +453,26 @@ int64_t sk_tail_tiles(int64_t T, int64_t U, int64_t KB)
     if (R * 10 > U * 9) return 0;   // the last wave is at least 90% full already
     if (R * KB < 4 * sk_units_for(R, U)) return 0;   // under 4 k-blocks per unit
     return R;
+}
+
+// Half-width tail: the tiles of the last, partial wave (all of them when there are fewer tiles
+// than units) each become two items of half the columns, when those fit in one wave (2 R <= U).
+// The last wave then takes about half a tile's time.  0: none.
+int64_t half_tail_tiles(int64_t T, int64_t U)
+{
+    if (T <= 0 || U <= 0) return 0;
+    const int64_t R = T < U ? T : T % U;
+    return R > 0 && 2 * R <= U ? R : 0;
+}
+
+// GEMM_F16_HALF_TAIL=0 (read once per process) turns the half-width tail off, for comparison.
+bool half_tail_setting()
+{
+    static const bool v = [] {
+        const char* s = std::getenv("GEMM_F16_HALF_TAIL");
+        return !(s && s[0] == '0');
+    }();
+    return v;
 }
 
 // Workspace layout: [header, gf16::kSkHeaderBytes][partial sums: units x cta_group x 128 x BN
@@ -561,7 +588,14 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
     if (R && (workspace == nullptr || workspace_bytes < need ||
               (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         R = 0;  // no usable workspace: plain data-parallel schedule
-    const int64_t units_used = R ? units : (tiles < units ? tiles : units);
+    // Without a stream-K tail, the last partial wave may run as half-width items (16-bit path;
+    // the epilogue stores 64-column chunks, so half a tile must be a whole number of them).
+    const int64_t H = (!kMx && R == 0 && (C::BN / 2) % 64 == 0 && half_tail_setting())
+                          ? half_tail_tiles(tiles, units)
+                          : 0;
+    const int64_t units_used = R ? units
+                               : H ? (tiles == H ? 2 * H : units)
+                                   : (tiles < units ? tiles : units);
     cfg.gridDim = dim3(static_cast<uint32_t>(kCtaGroup * units_used));
     // Pipeline positions are 32-bit counters over a unit's k-block iterations.
     if ((cdiv(tiles - R, units_used) + 1) * KB >= (int64_t(1) << 31))
@@ -587,7 +621,8 @@ int launch_ws(int variant, const void* A, const void* B, void* D, int64_t M, int
                                        (uint32_t)(R ? sk_units_for(R, units_used) : units_used),
                                        static_cast<const uint16_t*>(epi.bias),
                                        static_cast<uint32_t>(epi.act), debug_flags(),
-                                       maps->msfa, maps->msfb, mx_idesc);
+                                       maps->msfa, maps->msfb, mx_idesc, maps->mbh,
+                                       static_cast<uint32_t>(H));
     if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelEx(gemm_ws_kernel)");
     return GEMM_F16_OK;
 }
@@ -1042,6 +1077,36 @@ uint32_t gemm_f16_sk_unit_of(uint32_t tiles, uint32_t units, uint32_t k_blocks, 
                              uint32_t x)
 {
     return gf16::sk_unit_of(host_split(tiles, units, k_blocks, tail), x);
+}
+
+int64_t gemm_f16_half_tail_tiles(int64_t tiles, int64_t units)
+{
+    return half_tail_tiles(tiles, units);
+}
+
+static gf16::WorkSplit host_half_split(uint32_t tiles, uint32_t units, uint32_t k_blocks,
+                                       uint32_t half)
+{
+    gf16::WorkSplit w{tiles, units, k_blocks, 0u, units};
+    w.H = half;
+    return w;
+}
+
+uint32_t gemm_f16_half_items(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t half,
+                             uint32_t unit)
+{
+    return gf16::items_of(host_half_split(tiles, units, k_blocks, half), unit);
+}
+
+void gemm_f16_half_item(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t half,
+                        uint32_t unit, uint32_t idx, uint32_t out[4])
+{
+    const gf16::WorkItem w =
+        gf16::work_item(host_half_split(tiles, units, k_blocks, half), unit, idx);
+    out[0] = w.tile;
+    out[1] = w.kb0;
+    out[2] = w.kb1;
+    out[3] = w.half;
 }
 
 int gemm_mxf8_nt(const void* A, const void* B, const void* SFA, const void* SFB, void* D,

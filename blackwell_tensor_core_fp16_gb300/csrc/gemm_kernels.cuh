@@ -355,6 +355,8 @@ struct WsCfg {
     static constexpr uint32_t TMEM_SF = kAccBufs * kBlockN;    // first scale-factor column
     // Bytes that complete on the issuing CTA's "full" barrier per stage (both CTAs' loads).
     static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES + SF_BYTES) * kCtaGroup;
+    // a half-width item (the first B_ROWS / 2 rows of each CTA's B stage; no scales)
+    static constexpr uint32_t STAGE_TX_HALF = (A_BYTES + B_BYTES / 2) * kCtaGroup;
     static constexpr uint32_t D_COLS = 64;                   // one 128-byte swizzle row of fp16
     static constexpr uint32_t D_BYTES = kBlockM * D_COLS * 2;
     // accumulators (+ scales), rounded up to the power of two tcgen05.alloc takes
@@ -395,11 +397,16 @@ __global__ void __launch_bounds__(192, 1)
                    uint32_t sk_tiles, uint32_t sk_units, const uint16_t* __restrict__ bias,
                    uint32_t act, uint32_t debug_flags,
                    const __grid_constant__ CUtensorMap tmap_sfa,
-                   const __grid_constant__ CUtensorMap tmap_sfb, uint32_t mx_idesc)
+                   const __grid_constant__ CUtensorMap tmap_sfb, uint32_t mx_idesc,
+                   const __grid_constant__ CUtensorMap tmap_b_half, uint32_t half_tiles)
 {
     using C = WsCfg<kCtaGroup, kBlockN, kStages, kTmaStore, kMx, kAccBufs, kDBufs>;
     constexpr bool kPair = (kCtaGroup == 2);
     constexpr uint32_t idesc = make_idesc_f16(C::MMA_M, C::BN, kBf16 ? 1u : 0u);
+    constexpr uint32_t idesc_half = make_idesc_f16(C::MMA_M, C::BN / 2, kBf16 ? 1u : 0u);
+    // Half-width tail items exist only on the 16-bit path and when half a tile is a whole number
+    // of the epilogue's 64-column chunks (the host passes half_tiles = 0 otherwise).
+    constexpr bool kHalves = !kMx && (kBlockN / 2) % 64 == 0;
     const bool fused = bias != nullptr || act != kActNone;
 
     extern __shared__ uint8_t smem_raw[];
@@ -427,7 +434,7 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t ncl = kPair ? num_clusters_x() : gridDim.x;
     const uint32_t num_tiles = num_m_blocks * num_n_blocks;
     // Work of this unit: its data-parallel tiles, then (sk_tiles > 0) its stream-K pieces.
-    const WorkSplit split{num_tiles, ncl, num_k_blocks, sk_tiles, sk_units};
+    const WorkSplit split{num_tiles, ncl, num_k_blocks, sk_tiles, sk_units, half_tiles};
     const uint32_t n_items = items_of(split, cid);
     const uint32_t total = iterations_of(split, cid);
 
@@ -436,6 +443,7 @@ __global__ void __launch_bounds__(192, 1)
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_b);
         prefetch_tensormap(&tmap_d);
+        if (half_tiles != 0u) prefetch_tensormap(&tmap_b_half);
         if constexpr (kMx) {
             prefetch_tensormap(&tmap_sfa);
             prefetch_tensormap(&tmap_sfb);
@@ -493,7 +501,12 @@ __global__ void __launch_bounds__(192, 1)
         const auto tile_origin = [&]() {
             const TileCoord tc = tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
             m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
-            n0 = static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS);
+            // a half-width item: its columns start half a tile in for the second half, and each
+            // CTA loads half as many rows of B
+            n0 = (!kHalves || wi.half == 0u)
+                     ? static_cast<int32_t>(tc.n_blk * C::BN + rank * C::B_ROWS)
+                     : static_cast<int32_t>(tc.n_blk * C::BN + (wi.half - 1u) * (C::BN / 2u) +
+                                            rank * (C::B_ROWS / 2u));
             // the 128-row group of B's scales that holds the tile's first row
             sf_rb_b = static_cast<int32_t>(tc.n_blk * C::BN / 128u);
         };
@@ -516,10 +529,12 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t dA = sA + p.stage * C::A_BYTES;
                 const uint32_t dB = sB + p.stage * C::B_BYTES;
                 const uint32_t dS = sSF + p.stage * C::SF_BYTES;
+                const bool hw = kHalves && wi.half != 0u;   // a half-width item
                 if constexpr (!kPair) {
-                    mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
+                    mbar_arrive_expect_tx(full_bar(p.stage), hw ? C::STAGE_TX_HALF : C::STAGE_TX);
                     tma_load_2d_hint(dA, &tmap_a, full_bar(p.stage), k0, m0, pol_a);
-                    tma_load_2d_hint(dB, &tmap_b, full_bar(p.stage), k0, n0, pol_b);
+                    tma_load_2d_hint(dB, hw ? &tmap_b_half : &tmap_b, full_bar(p.stage), k0, n0,
+                                     pol_b);
                     if constexpr (kMx) {
                         // scale chunks (K-block group kb): A's row group, then B's groups
                         tma_load_3d(dS, &tmap_sfa, full_bar(p.stage), 0, static_cast<int32_t>(kb),
@@ -528,10 +543,12 @@ __global__ void __launch_bounds__(192, 1)
                                     static_cast<int32_t>(kb), sf_rb_b);
                     }
                 } else {
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(p.stage), C::STAGE_TX);
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(full_bar(p.stage),
+                                              hw ? C::STAGE_TX_HALF : C::STAGE_TX);
                     const uint32_t fb = mapa_shared(full_bar(p.stage), 0);
                     tma_load_2d_pair_hint(dA, &tmap_a, fb, k0, m0, pol_a);
-                    tma_load_2d_pair_hint(dB, &tmap_b, fb, k0, n0, pol_b);
+                    tma_load_2d_pair_hint(dB, hw ? &tmap_b_half : &tmap_b, fb, k0, n0, pol_b);
                     if constexpr (kMx) {
                         tma_load_3d_pair(dS, &tmap_sfa, fb, 0, static_cast<int32_t>(kb), m0 / 128);
                         tma_load_3d_pair(dS + 512u, &tmap_sfb, fb, 0, static_cast<int32_t>(kb),
@@ -633,9 +650,11 @@ __global__ void __launch_bounds__(192, 1)
                                               sf_col + 4u + sfb_shift,
                                               ((kb - wi.kb0) | k) != 0u);
                     } else {
+                        // a half-width item: N = BN / 2 from the first rows of each B stage
+                        const uint32_t id = (kHalves && wi.half != 0u) ? idesc_half : idesc;
 #pragma unroll
                         for (uint32_t k = 0; k < kBlockK / kUmmaK; ++k)
-                            mma_f16<kCtaGroup>(d_tmem, ad + 2ull * k, bd + 2ull * k, idesc,
+                            mma_f16<kCtaGroup>(d_tmem, ad + 2ull * k, bd + 2ull * k, id,
                                                ((kb - wi.kb0) | k) != 0u);
                     }
                     if constexpr (kPair) mma_commit_pair(empty_bar(p.stage), 0x3);
@@ -793,7 +812,10 @@ __global__ void __launch_bounds__(192, 1)
             const WorkItem wi = work_item(split, cid, item);
             const TileCoord tc = tile_coord(wi.tile, num_m_blocks, num_n_blocks, group_m);
             const int32_t m0 = static_cast<int32_t>(tc.m_blk * C::MMA_M + rank * kBlockM);
-            const int32_t n0 = static_cast<int32_t>(tc.n_blk * C::BN);
+            // a half-width item holds BN / 2 columns, from half a tile in for the second half
+            const int32_t n0 = static_cast<int32_t>(
+                tc.n_blk * C::BN +
+                ((kHalves && wi.half != 0u) ? (wi.half - 1u) * (C::BN / 2u) : 0u));
             const bool rows_in = m0 < static_cast<int32_t>(M);
             const uint32_t b = acc % C::ACC_BUFS;
             const uint32_t aph = (acc / C::ACC_BUFS) & 1u;
@@ -862,21 +884,23 @@ __global__ void __launch_bounds__(192, 1)
                 // A whole tile: two 64-column chunks per round, both chunks' loads in flight
                 // before one wait.
                 constexpr uint32_t NC = C::BN / C::D_COLS;
+                const uint32_t nc = (kHalves && wi.half != 0u) ? NC / 2u : NC;   // this item's chunks
 #pragma unroll
                 for (uint32_t c2 = 0; c2 < NC; c2 += 2) {
+                    if (c2 >= nc) break;
                     uint32_t v[4][32];
                     const uint32_t taddr = tmem_base + lane_off + b * C::BN + c2 * C::D_COLS;
 #pragma unroll
                     for (uint32_t h = 0; h < 4; ++h)
-                        if (c2 + h / 2 < NC)
+                        if (c2 + h / 2 < nc)
                             tmem_ld_32x32b_x32(taddr, v[h], static_cast<int>(32u * h));
                     tmem_ld_wait();
-                    if (c2 + 2 >= NC) hand_back(b);   // this warp is done with accumulator b
+                    if (c2 + 2 >= nc) hand_back(b);   // this warp is done with accumulator b
 #pragma unroll
                     for (uint32_t cc = 0; cc < 2; ++cc) {
                         const uint32_t c = c2 + cc;
                         const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
-                        if (c < NC && col0 < static_cast<int32_t>(N) && rows_in)
+                        if (c < nc && col0 < static_cast<int32_t>(N) && rows_in)
                             emit64(v[2 * cc], v[2 * cc + 1], m0, col0);
                     }
                 }

@@ -266,6 +266,18 @@ void gemm_f16_sk_item(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_
 uint32_t gemm_f16_sk_unit_of(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t tail,
                              uint32_t x);
 
+/* The half-width tail (without stream-K): the tiles of the last, partial wave (all tiles when
+ * there are fewer than `units`) each run as two items of half the tile's columns, when those fit
+ * in one wave (2 x tail <= units).  gemm_f16_half_tail_tiles: that tail (0: none).
+ * gemm_f16_half_items / gemm_f16_half_item: as gemm_f16_sk_items / _item for a split whose last
+ * `half` tiles are cut this way; an item is {tile, first k-block, end k-block, half: 0 the whole
+ * tile, 1 or 2 its first or second half of the columns}. */
+int64_t gemm_f16_half_tail_tiles(int64_t tiles, int64_t units);
+uint32_t gemm_f16_half_items(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t half,
+                             uint32_t unit);
+void gemm_f16_half_item(uint32_t tiles, uint32_t units, uint32_t k_blocks, uint32_t half,
+                        uint32_t unit, uint32_t idx, uint32_t out[4]);
+
 /* ---- block-scaled FP8 GEMM (MX formats) ------------------------------------------------------
  *
  * The operation (page "TIRx Layout API", sections "示例：Blackwell Tensor Memory" and

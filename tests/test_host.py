@@ -512,3 +512,68 @@ def test_kernel_addresses_stay_in_bounds_and_cover_d_once(variant, shape):
     for u in (units, units - 3):          # fewer co-resident units than SMs allow
         for stream_k in (False, True):
             _replay(variant, M, N, K, u, stream_k)
+
+
+# ---- the half-width tail, replayed on the CPU --------------------------------------------------
+
+def _replay_half(variant, M, N, K, units):
+    """The items and boxes of a launch whose last partial wave runs as half-width items (no
+    stream-K): every output box is stored once, every B box starts at an aligned column, and the
+    half items cover the tail tiles' two halves exactly."""
+    info = g.gemm_f16_get_variant_info(variant)
+    cg, mma_m, bn = info["cta_group"], info["block_m"], info["block_n"]
+    b_rows = bn // cg
+    num_m, num_n, KB = -(-M // mma_m), -(-N // bn), -(-K // 64)
+    T = num_m * num_n
+    H = g.gemm_f16_half_tail_tiles(T, units) if (bn // 2) % 64 == 0 else 0
+    if H == 0:
+        return 0
+    assert 2 * H <= units and (T - H) % units == 0
+    used = 2 * H if T == H else units                 # the launch's grid, in units
+    group = g.gemm_f16_raster_group(mma_m, K, 2, GB300_L2)
+    stores, halves = {}, {}
+    for c in range(used):
+        for i in range(g.gemm_f16_half_items(T, used, KB, H, c)):
+            tile, kb0, kb1, half = g.gemm_f16_half_item(T, used, KB, H, c, i)
+            assert (kb0, kb1) == (0, KB)
+            assert (half == 0) == (tile < T - H), (tile, half)
+            m_blk, n_blk = g.gemm_f16_tile_coord(tile, num_m, num_n, group)
+            assert m_blk < num_m and n_blk < num_n
+            width = bn if half == 0 else bn // 2
+            col_base = n_blk * bn + (half - 1) * (bn // 2 if half else 0)
+            if half:
+                halves.setdefault(tile, []).append(half)
+            for rank in range(cg):
+                m0 = m_blk * mma_m + rank * 128
+                b0 = col_base + rank * (b_rows if half == 0 else b_rows // 2)
+                assert b0 >= 0                                   # B box row
+                for ch in range(width // 64):
+                    col0 = col_base + 64 * ch
+                    if col0 < N and m0 < M:
+                        assert (col0 * 2) % 16 == 0
+                        stores[(m0, col0)] = stores.get((m0, col0), 0) + 1
+    assert sorted(halves) == list(range(T - H, T))
+    assert all(sorted(h) == [1, 2] for h in halves.values())
+    expect = {(128 * i, 64 * j) for i in range(-(-M // 128)) for j in range(-(-N // 64))}
+    assert set(stores) == expect and set(stores.values()) == {1}
+    return H
+
+
+@pytest.mark.parametrize("variant", [2, 3, 4, 5])
+@pytest.mark.parametrize("shape", [(8192, 8192, 8192), (16384, 14336, 4096), (3000, 5000, 1000),
+                                   (2048, 2048, 2048), (512, 1024, 4096), (129, 136, 72)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_half_width_tail_covers_d_once(variant, shape):
+    M, N, K = shape
+    units = 152 // g.gemm_f16_get_variant_info(variant)["cta_group"]
+    for u in (units, units - 3):
+        _replay_half(variant, M, N, K, u)
+
+
+def test_half_width_tail_rule():
+    assert g.gemm_f16_half_tail_tiles(1024, 76) == 36       # 8192^3 pairs: 13 waves + 36
+    assert g.gemm_f16_half_tail_tiles(3584, 76) == 12       # the MLP shape
+    assert g.gemm_f16_half_tail_tiles(64, 76) == 0          # 2048^3: 128 halves would not fit
+    assert g.gemm_f16_half_tail_tiles(8, 76) == 8           # few tiles: all of them halved
+    assert g.gemm_f16_half_tail_tiles(152, 76) == 0         # whole waves
+    assert g.gemm_f16_half_tail_tiles(76 + 39, 76) == 0     # 2 x 39 > 76
