@@ -884,20 +884,23 @@ __global__ void __launch_bounds__(192, 1)
                 // A whole tile: two 64-column chunks per round, both chunks' loads in flight
                 // before one wait.
                 constexpr uint32_t NC = C::BN / C::D_COLS;
+                // chunks whose loads are in flight together: two for the wide tiles, one for
+                // 128 columns (whose registers would not hold two with the rest of the kernel)
+                constexpr uint32_t kBatch = NC >= 4 ? 2u : 1u;
                 const uint32_t nc = (kHalves && wi.half != 0u) ? NC / 2u : NC;   // this item's chunks
 #pragma unroll
-                for (uint32_t c2 = 0; c2 < NC; c2 += 2) {
+                for (uint32_t c2 = 0; c2 < NC; c2 += kBatch) {
                     if (c2 >= nc) break;
-                    uint32_t v[4][32];
+                    uint32_t v[2 * kBatch][32];
                     const uint32_t taddr = tmem_base + lane_off + b * C::BN + c2 * C::D_COLS;
 #pragma unroll
-                    for (uint32_t h = 0; h < 4; ++h)
+                    for (uint32_t h = 0; h < 2 * kBatch; ++h)
                         if (c2 + h / 2 < nc)
                             tmem_ld_32x32b_x32(taddr, v[h], static_cast<int>(32u * h));
                     tmem_ld_wait();
-                    if (c2 + 2 >= nc) hand_back(b);   // this warp is done with accumulator b
+                    if (c2 + kBatch >= nc) hand_back(b);   // this warp is done with accumulator b
 #pragma unroll
-                    for (uint32_t cc = 0; cc < 2; ++cc) {
+                    for (uint32_t cc = 0; cc < kBatch; ++cc) {
                         const uint32_t c = c2 + cc;
                         const int32_t col0 = n0 + static_cast<int32_t>(c * C::D_COLS);
                         if (c < nc && col0 < static_cast<int32_t>(N) && rows_in)
