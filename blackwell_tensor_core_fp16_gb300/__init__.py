@@ -558,7 +558,7 @@ def gdn_check_status(workspace: int, stream: int) -> int:
 
 def gdn_check_offsets(cu_seqlens: int, n_seqs: int, total_tokens: int, h_v: int,
                       workspace: int, workspace_bytes: int, stream: int = 0) -> int:
-    """Check cu_seqlens on the device (include/gdn.h); read the verdict with gdn_check_status."""
+    """Check cu_seqlens on the device (include/gdn.h); read the result with gdn_check_status."""
     return load().gdn_check_offsets(cu_seqlens, n_seqs, total_tokens, h_v, workspace,
                                     workspace_bytes, stream)
 

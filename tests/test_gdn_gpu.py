@@ -152,7 +152,7 @@ def test_rejects_bad_arguments():
     ids=lambda x: None)
 def test_offsets_checked_on_the_device(cu, T, ok):
     """gdn_check_offsets runs the chunk-list kernel alone: it reads the n + 1 offsets and writes
-    only the workspace's tables, so offsets outside [0, T] are safe to give it.  The verdict read
+    only the workspace's tables, so offsets outside [0, T] are safe to give it.  The result read
     through gdn_check_status must follow the contract, and a valid check after a refused one
     clears the word."""
     n = len(cu) - 1
