@@ -3,13 +3,14 @@
 //
 // Two kernels:
 //
-//  * gemm_tile_kernel: one 128x128 output tile per CTA on a 2-D grid, 4 warps, a single
-//    shared-memory stage.  Thread 0 issues the TMA loads of a 64-wide K chunk, waits for them,
-//    issues four K=16 tcgen05.mma and waits for their commit before loading the next chunk;
-//    then every warp reads its 32 TMEM lanes, converts and stores its rows directly.  This is
-//    the synchronous protocol of Steps 2-4 on the page "TIRx 与高性能GEMM (上)": a K loop whose
-//    first MMA overwrites the accumulator, an mbarrier phase flipped on every use, TMA loads
-//    completing on a transaction-count barrier.  It is the cross-check for the fast kernel.
+//  * gemm_tile_kernel<BN>: one 128 x BN output tile per CTA (BN = 16 .. 128) on a 2-D grid, 4
+//    warps, two shared-memory stages.  Thread 0 issues the TMA loads of a 64-wide K chunk a chunk
+//    ahead, waits for them, issues four K=16 tcgen05.mma and commits them; then every warp reads
+//    its 32 TMEM lanes, converts and stores its rows directly.  This is the protocol of Steps
+//    2-4 on the page "TIRx 与高性能GEMM (上)" (a K loop whose first MMA overwrites the
+//    accumulator, mbarrier phases flipped on every use, TMA loads completing on a
+//    transaction-count barrier) with one load in flight behind the MMAs.  With a narrow BN it
+//    is the fast path for problems of a few tiles, and the cross-check for the persistent kernel.
 //
 //  * gemm_ws_kernel<CtaGroup, BlockN, Stages>: the persistent, warp-specialised kernel.
 //      warp 0      TMA producer: fills a ring of `Stages` shared-memory stages (A 128x64 and
@@ -29,7 +30,9 @@
 //    With CtaGroup == 2, a cluster of two CTAs computes a 256 x BlockN tile with
 //    tcgen05.mma.cta_group::2 (M = 256): each CTA loads its own 128 rows of A and its own half
 //    of the BlockN rows of B, both CTAs' loads complete on the even CTA's "full" barrier, and
-//    the MMA commit signals both CTAs.  No operand is shared, so no load is multicast.
+//    the MMA commit signals both CTAs.  No operand is shared, so no load is multicast.  The
+//    last partial wave may run as half-width items (two per tile, N = BlockN / 2), and the
+//    stream-K tail, when turned on, splits its tiles by k-blocks.
 //
 // Tails: TMA loads fill elements outside [0,M)x[0,K) and [0,N)x[0,K) with zeros, so partial K
 // chunks add nothing and partial M/N tiles compute zeros in the padding; TMA stores and the
