@@ -83,6 +83,12 @@ def parse_args():
     p.add_argument("--config-ms", type=float, default=200.0,
                    help="back-to-back milliseconds per config in the per_config leg (single tile, "
                         "2048^3, 3000x5000x1000; 0: skip)")
+    p.add_argument("--config-processes", type=int, default=3,
+                   help="processes the per_config leg runs in (this one and fresh ones); each "
+                        "figure is the median of the per-process means")
+    p.add_argument("--config-only", action="store_true",
+                   help="run only the per_config leg in this process and print it (the fresh "
+                        "processes of --config-processes)")
     p.add_argument("--sustained-ms", type=float, default=1500.0,
                    help="length of the sustained leg: the headline step back to back for at "
                         "least this long, with its own clock record (0: skip)")
@@ -800,6 +806,64 @@ def run_sustained_leg(args, g, stream, work, launch, flops_step, peak_burst, pea
     return res
 
 
+def merge_config_processes(args, first):
+    """Runs the per_config leg in args.config_processes - 1 fresh processes as well; per config,
+    each time figure becomes the median of the per-process means (all of them listed)."""
+    runs = [first]
+    cmd = [sys.executable, os.path.abspath(__file__), "--config-only", "--config-ms",
+           str(args.config_ms), "--cublas-steps", str(args.cublas_steps)]
+    for _ in range(args.config_processes - 1):
+        out = subprocess.run(cmd, check=True, capture_output=True, text=True).stdout
+        runs.append(json.loads([ln for ln in out.splitlines() if ln.startswith("{")][-1]))
+    merged = dict(first)
+    merged["processes"] = len(runs)
+    merged["timing"] = (first["timing"] + "; each figure is the median over " + str(len(runs)) +
+                        " processes of the per-process means (listed per process)")
+    cfgs = {}
+    for name, c in first["configs"].items():
+        d = dict(c)
+        flops = 2.0 * c["M"] * c["N"] * c["K"]
+        for key in ("us_per_launch", "us_per_launch_graph", "cold_l2_us_per_launch",
+                    "cublas_us_per_launch_graph_context"):
+            vals = [r["configs"][name][key] for r in runs if r["configs"][name].get(key)]
+            if not vals:
+                continue
+            d[key] = statistics.median(vals)
+            d[key + "_per_process"] = vals
+        d["tflops"] = flops / (d["us_per_launch"] * 1e-6) / 1e12
+        d["tflops_graph"] = flops / (d["us_per_launch_graph"] * 1e-6) / 1e12
+        d["cold_l2_tflops"] = flops / (d["cold_l2_us_per_launch"] * 1e-6) / 1e12
+        d["frac_of_burst"] = d["tflops"] * c["frac_of_burst"] / c["tflops"]
+        bytes_ = c["hbm_gbs_algorithmic"] * c["us_per_launch"] * 1e-6 * 1e9
+        d["hbm_gbs_algorithmic"] = bytes_ / (d["us_per_launch"] * 1e-6) / 1e9
+        d["hbm_frac"] = d["hbm_gbs_algorithmic"] * c["hbm_frac"] / c["hbm_gbs_algorithmic"]
+        cfgs[name] = d
+    merged["configs"] = cfgs
+    merged["gpu_launches"] = sum(r["gpu_launches"] for r in runs)
+    return merged
+
+
+def run_config_only(args):
+    """--config-only: the per_config leg alone, printed as one JSON line."""
+    import torch
+    import blackwell_tensor_core_fp16_gb300 as g
+    g.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    peak_burst, _peak_sus, _src = measured_peaks()
+    leg = run_config_leg(args, g, dev, stream, props.multi_processor_count, peak_burst,
+                         measured_hbm_gbs(), uuid)
+    print(json.dumps(leg), flush=True)
+    return 0
+
+
 # ---- our arm ---------------------------------------------------------------------------------
 
 def run_ours(args):
@@ -1117,6 +1181,8 @@ def run_ours(args):
     if args.config_ms > 0 and not args.only:
         config_leg = run_config_leg(args, g, dev, stream, num_sms, peak_burst,
                                     measured_hbm_gbs(), uuid)
+        if args.config_processes > 1 and world == 1:
+            config_leg = merge_config_processes(args, config_leg)
 
     mx_leg = None
     if args.mx_steps > 0:
@@ -1357,6 +1423,8 @@ def main():
         return run_reference(args)
     if args.sweep and args.sweep_processes > 1:
         return run_sweep_processes(args)
+    if args.config_only:
+        return run_config_only(args)
     if args.sweep:
         return run_sweep(args)
     return run_ours(args)
