@@ -43,6 +43,9 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--variant", type=int, default=0, help="kernel variant (0 = auto)")
     p.add_argument("--e2e-steps", type=int, default=30)
+    p.add_argument("--e2e-repeats", type=int, default=3,
+                   help="timed regions of the e2e leg; it reports their median (the host link "
+                        "is shared with other jobs on the host)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
@@ -1101,6 +1104,7 @@ def run_ours(args):
     # from before the first upload to after the last download.
     e2e_steps = 0 if args.skip_e2e else max(3, min(args.e2e_steps, K))
     e2e_value = None
+    e2e_runs = []
     link_gbs = copy_roof = None
     h2d = d2h = 0
     if e2e_steps:
@@ -1127,36 +1131,41 @@ def run_ours(args):
             d2h += 2 * w.M * w.N
         ev0 = torch.cuda.Event(enable_timing=True)
         ev1 = torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        s_up.wait_event(ev0)
-        s_down.wait_event(ev0)
-        for i in range(e2e_steps):
-            for (w, Ah, Bh, Dh, Ad2, Bd2, D2, variant, ev) in slots[i % 2]:
-                if i >= 2:
-                    s_up.wait_event(ev["mm"])       # step i-2 finished reading this slot
-                with torch.cuda.stream(s_up):
-                    Ad2.copy_(Ah, non_blocking=True)
-                    Bd2.copy_(Bh, non_blocking=True)
-                    ev["up"].record(s_up)
-                stream.wait_event(ev["up"])
-                if i >= 2:
-                    stream.wait_event(ev["down"])   # step i-2's result has left this slot
-                g.gemm(Ad2, Bd2, out=D2, variant=variant, stream=stream)
-                ev["mm"].record(stream)
-                s_down.wait_event(ev["mm"])
-                with torch.cuda.stream(s_down):
-                    Dh.copy_(D2, non_blocking=True)
-                    ev["down"].record(s_down)
-        stream.wait_stream(s_up)
-        stream.wait_stream(s_down)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        g.check_status(stream)
-        e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
-        e2e_value = whole_job_tflops(world, e2e_steps, flops_step, e2e_ms)
+
+        def e2e_region():
+            barrier()
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            s_up.wait_event(ev0)
+            s_down.wait_event(ev0)
+            for i in range(e2e_steps):
+                for (w, Ah, Bh, Dh, Ad2, Bd2, D2, variant, ev) in slots[i % 2]:
+                    if i >= 2:
+                        s_up.wait_event(ev["mm"])       # step i-2 finished reading this slot
+                    with torch.cuda.stream(s_up):
+                        Ad2.copy_(Ah, non_blocking=True)
+                        Bd2.copy_(Bh, non_blocking=True)
+                        ev["up"].record(s_up)
+                    stream.wait_event(ev["up"])
+                    if i >= 2:
+                        stream.wait_event(ev["down"])   # step i-2's result has left this slot
+                    g.gemm(Ad2, Bd2, out=D2, variant=variant, stream=stream)
+                    ev["mm"].record(stream)
+                    s_down.wait_event(ev["mm"])
+                    with torch.cuda.stream(s_down):
+                        Dh.copy_(D2, non_blocking=True)
+                        ev["down"].record(s_down)
+            stream.wait_stream(s_up)
+            stream.wait_stream(s_down)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            g.check_status(stream)
+            return max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+
+        e2e_runs = [whole_job_tflops(world, e2e_steps, flops_step, e2e_region())
+                    for _ in range(max(1, args.e2e_repeats))]
+        e2e_value = statistics.median(e2e_runs)
         # The copy roofline of this leg: the measured rate of concurrent pinned-host copies in
         # both directions (256 MiB each way, the same streams), and the TFLOP/s a step could
         # reach if its copies ran at that rate and the GEMMs hid under them.
@@ -1233,6 +1242,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "repeats": e2e_runs, "value_def": "median over the repeated timed regions",
                 "copy_link_gbs_measured": link_gbs,
                 "copy_roofline_tflops": copy_roof,
                 "frac_of_copy_roofline": (e2e_value / world / copy_roof) if copy_roof else None,
