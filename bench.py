@@ -592,8 +592,10 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
                 "unit": "TFLOP/s", "frac": tf / peak16, "traffic": None,
                 "hbm_achieved_gbs": gbs, "hbm_peak_gbs": hbm_peak, "hbm_frac": gbs / hbm_peak,
                 "note": "achieved = the token recurrence's 6*T*h_v*dk*dv flops / call time against "
-                        "the measured dense bf16 peak; the call is latency-bound by the chunk "
-                        "chain (about 2.2 us per 64-token step of a sequence)"}
+                        "the measured dense bf16 peak; the call is latency-bound: the scan by "
+                        "its chain of dependent 64-token chunk steps (about 1.7 us each on the "
+                        "tcgen05 scan), the prepare kernel (about a third of the call) by its "
+                        "per-chunk chain of products, inverse and stores"}
     g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS["auto"])
     return {"metric": "Gated Delta Net prefill: ms per call (bf16 q/k/v, head dim 128)",
             "unit": "ms", "higher_is_better": False, "scan_kernel": args.gdn_scan,
