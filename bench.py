@@ -81,6 +81,11 @@ def parse_args():
                    help="scan kernel of the Gated Delta Net leg")
     p.add_argument("--gdn-only", action="store_true",
                    help="run only the Gated Delta Net leg and print its JSON")
+    p.add_argument("--gdn-scenarios", default="",
+                   help="comma-separated Gated Delta Net scenarios to time (default: all six)")
+    p.add_argument("--gdn-warm-ms", type=float, default=50.0,
+                   help="warm-up time per Gated Delta Net scenario, in batches of 8 calls "
+                        "(0: exactly one batch)")
     p.add_argument("--sweep-mx", action="store_true",
                    help="in --sweep, time the block-scaled FP8 workloads instead")
     p.add_argument("--config-ms", type=float, default=200.0,
@@ -95,6 +100,12 @@ def parse_args():
     p.add_argument("--sustained-ms", type=float, default=1500.0,
                    help="length of the sustained leg: the headline step back to back for at "
                         "least this long, with its own clock record (0: skip)")
+    p.add_argument("--record-traffic-mx", default="",
+                   help="write profiles/ncu_traffic_mx.json from an ncu csv log of the block-scaled "
+                        "FP8 step's two launches")
+    p.add_argument("--record-traffic-gdn", default="",
+                   help="write profiles/ncu_traffic_gdn.json from an ncu csv log of one Gated "
+                        "Delta Net call's launches (the roofline scenario)")
     p.add_argument("--record-traffic", default="",
                    help="read an ncu CSV log of the two GEMM launches of one step (metrics "
                         "dram__bytes_read.sum, dram__bytes_write.sum, gpu__time_duration.sum; "
@@ -155,14 +166,15 @@ def whole_job_tflops(world: int, steps: int, flops_step: float, total_ms: float)
 
 
 GEMM_KERNEL_SOURCES = ("desc.h", "gemm_f16.cu", "gemm_kernels.cuh", "ptx.cuh")
+GDN_KERNEL_SOURCES = ("desc.h", "gdn.cu", "gdn_offsets.h", "ptx.cuh")
 
 
-def kernel_source_hash() -> str:
-    """sha256 over the GEMM kernel's sources: a recorded ncu traffic figure applies only while
-    they are unchanged."""
+def kernel_source_hash(sources=GEMM_KERNEL_SOURCES) -> str:
+    """sha256 over a kernel's sources (the GEMM's by default): a recorded ncu traffic figure
+    applies only while they are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "blackwell_tensor_core_fp16_gb300", "csrc")
-    for f in GEMM_KERNEL_SOURCES:
+    for f in sources:
         h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
@@ -199,15 +211,16 @@ def measured_hbm_gbs() -> float:
         return 6800.0
 
 
-def recorded_traffic(variant_name: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on this kernel source."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+def recorded_traffic(variant_name: str, file="ncu_traffic.json", sources=GEMM_KERNEL_SOURCES):
+    """DRAM bytes per launch (or per step or call, as the file says) from a committed ncu
+    summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", file)
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("kernel_src_sha256") != kernel_source_hash():
+    if d.get("kernel_src_sha256") != kernel_source_hash(sources):
         return None
     return d.get("per_launch_dram_bytes", {}).get(variant_name)
 
@@ -261,6 +274,61 @@ def record_traffic(csv_path, command=""):
         f.write("\n")
     print(json.dumps(out))
     return 0
+
+
+def _write_traffic(file, out):
+    path = os.path.join(ROOT, "profiles", file)
+    with open(path, "w") as f:
+        json.dump(out, f, indent=2)
+        f.write("\n")
+    print(json.dumps(out))
+    return 0
+
+
+def _launch_bytes(l):
+    m = l["metrics"]
+    rd, wr = m["dram__bytes_read.sum"], m["dram__bytes_write.sum"]
+    return {"kernel": l["kernel"], "dram_read_bytes": int(rd), "dram_write_bytes": int(wr),
+            "dram_bytes": int(rd + wr), "duration_us": m.get("gpu__time_duration.sum", 0.0) * 1e6}
+
+
+def record_traffic_mx(csv_path, command=""):
+    """profiles/ncu_traffic_mx.json from the capture of the block-scaled FP8 step's two launches
+    (8192^3, then the MLP shape), tagged with the hash of the kernel sources."""
+    launches = parse_ncu_csv(csv_path)
+    if len(launches) != len(MX_STEP):
+        raise SystemExit(f"expected {len(MX_STEP)} launches in {csv_path}, found {len(launches)}")
+    by_w = {name: _launch_bytes(l) for name, l in zip(MX_STEP, launches)}
+    return _write_traffic("ncu_traffic_mx.json", {
+        "kernel_src_sha256": kernel_source_hash(),
+        "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+                  "gpu__time_duration.sum --clock-control none, the block-scaled FP8 step's two "
+                  "launches, written by bench.py --record-traffic-mx",
+        "command": command, "launches": by_w,
+        "per_launch_dram_bytes": {"mx_step": sum(v["dram_bytes"] for v in by_w.values())},
+        "per_launch_note": "mx_step is the sum over the two launches of one step (the unit the "
+                           "leg's 'achieved' uses)"})
+
+
+def record_traffic_gdn(csv_path, command=""):
+    """profiles/ncu_traffic_gdn.json from the capture of one Gated Delta Net call of the roofline
+    scenario (its chunk list, prepare and scan launches), tagged with the hash of the Gated Delta
+    Net kernel sources."""
+    launches = parse_ncu_csv(csv_path)
+    if not 2 <= len(launches) <= 3:
+        raise SystemExit(f"expected the 2 or 3 launches of one call in {csv_path}, found "
+                         f"{len(launches)}")
+    ls = [_launch_bytes(l) for l in launches]
+    return _write_traffic("ncu_traffic_gdn.json", {
+        "kernel_src_sha256": kernel_source_hash(GDN_KERNEL_SOURCES),
+        "scenario": GDN_ROOFLINE_SCENARIO,
+        "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+                  "gpu__time_duration.sum --clock-control none, the launches of one call, "
+                  "written by bench.py --record-traffic-gdn",
+        "command": command, "launches": ls,
+        "per_launch_dram_bytes": {GDN_ROOFLINE_SCENARIO: sum(v["dram_bytes"] for v in ls)},
+        "per_launch_note": "the entry is the sum over the launches of one call (the unit the "
+                           "leg's 'achieved' uses)"})
 
 
 # ---- clocks --------------------------------------------------------------------------------
@@ -397,6 +465,7 @@ def run_reference(args):
 # ---- block-scaled FP8 leg ---------------------------------------------------------------------
 
 MX_STEP = ("mx_square_8192", "mx_mlp_up_16384x14336x4096")
+GDN_ROOFLINE_SCENARIO = "packed_n20_t8192_h8_hv16_gva_state"   # the longest call
 FP8_OVER_16BIT = 2.0   # nominal dense rate ratio of the FP8 and 16-bit tensor paths (4.5 / 2.25 PF)
 
 
@@ -510,7 +579,9 @@ def run_mx_leg(args, g, dev, stream, num_sms, peak16, uuid):
             "value": K * flops / (total * 1e-3) / 1e12, "unit": "TFLOP/s", "steps": K,
             "per_workload": per, "clocks": clk, "cublas_mxfp8_same_step": cublas,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak8,
-                         "unit": "TFLOP/s", "frac": achieved / peak8, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak8,
+                         "traffic": recorded_traffic("mx_step", "ncu_traffic_mx.json"),
+                         "traffic_unit": "DRAM bytes per step (ncu, both launches)",
                          "peak_source": "measured bf16_tflops x 2 (nominal FP8 / 16-bit dense "
                                         "rate ratio, 4.5 / 2.25 PFLOP/s)"},
             "gpu_launches": 2 * K * len(work)}
@@ -537,7 +608,8 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
     if g.gdn_set_scan_kernel(g.GDN_SCAN_KERNELS[args.gdn_scan]) != g.GDN_OK:
         raise g.GemmError(1, g.gdn_last_error())
     out = {}
-    for name in GDN_ORDER:
+    names = [n for n in args.gdn_scenarios.split(",") if n] or GDN_ORDER
+    for name in names:
         w = GDN_WORKLOADS[name]
         inp = gdn_workload_inputs(w)
         q, k, v = (inp[x].to(dev) for x in ("q", "k", "v"))
@@ -564,7 +636,7 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
         # time at least `gdn_reps` calls and at least about 5 ms of them
         t_w = time.perf_counter()
         n_w = 0
-        while n_w < 3 or time.perf_counter() - t_w < 0.05:
+        while n_w < 3 or time.perf_counter() - t_w < args.gdn_warm_ms * 1e-3:
             with torch.cuda.stream(stream):
                 for _ in range(8):
                     call()
@@ -588,8 +660,11 @@ def run_gdn_leg(args, g, dev, stream, peak16, hbm_peak):
     # is a chain of dependent 64-token chunk steps), and both fractions say so.
     big = max(out, key=lambda n: out[n]["ms"])
     tf, gbs = out[big]["recurrence_tflops"], out[big]["hbm_gbs_algorithmic"]
+    traffic = (recorded_traffic(big, "ncu_traffic_gdn.json", GDN_KERNEL_SOURCES)
+               if big == GDN_ROOFLINE_SCENARIO else None)
     roofline = {"scenario": big, "bound": "tensor", "achieved": tf, "peak": peak16,
-                "unit": "TFLOP/s", "frac": tf / peak16, "traffic": None,
+                "unit": "TFLOP/s", "frac": tf / peak16, "traffic": traffic,
+                "traffic_unit": "DRAM bytes per call (ncu, all launches of one call)",
                 "hbm_achieved_gbs": gbs, "hbm_peak_gbs": hbm_peak, "hbm_frac": gbs / hbm_peak,
                 "note": "achieved = the token recurrence's 6*T*h_v*dk*dv flops / call time against "
                         "the measured dense bf16 peak; the call is latency-bound: the scan by "
@@ -1431,6 +1506,10 @@ def main():
     args = parse_args()
     if args.record_traffic:
         return record_traffic(args.record_traffic, os.environ.get("TRAFFIC_COMMAND", ""))
+    if args.record_traffic_mx:
+        return record_traffic_mx(args.record_traffic_mx, os.environ.get("TRAFFIC_COMMAND", ""))
+    if args.record_traffic_gdn:
+        return record_traffic_gdn(args.record_traffic_gdn, os.environ.get("TRAFFIC_COMMAND", ""))
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep and args.sweep_processes > 1:

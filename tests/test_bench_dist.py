@@ -167,3 +167,40 @@ def test_ncu_csv_parsing_scales_units(tmp_path):
     assert got[1]["metrics"]["gpu__time_duration.sum"] == pytest.approx(1.03e-3)
     assert got[0]["metrics"]["gpu__time_duration.sum"] == pytest.approx(612.5e-6)
     assert got[1]["metrics"]["dram__bytes_write.sum"] == pytest.approx(0.45e9)
+
+
+def test_traffic_records_follow_their_kernel_sources(tmp_path, monkeypatch):
+    """A recorded DRAM figure is reported only while the hash of the sources it was taken on
+    matches; the Gated Delta Net record sums the launches of one call and is tagged with the Gated
+    Delta Net sources' hash, the block-scaled FP8 record with the GEMM sources'."""
+    bench = load_bench()
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash",
+                        lambda sources=bench.GEMM_KERNEL_SOURCES: "hash-of-" + sources[1])
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+           '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+           '"Metric Value"')
+
+    def log(n_launch, name):
+        lines = [hdr]
+        for i in range(n_launch):
+            for metric, val in (("dram__bytes_read.sum", 1000 * (i + 1)),
+                                ("dram__bytes_write.sum", 10 * (i + 1)),
+                                ("gpu__time_duration.sum", 5000)):
+                unit = "ns" if metric.startswith("gpu") else "byte"
+                lines.append(f'"{i}","1","python","h","{name}","1","7","(256, 1, 1)",'
+                             f'"(152, 1, 1)","0","10.3","m","{metric}","{unit}","{val}"')
+        p = tmp_path / f"{name}.csv"
+        p.write_text("\n".join(lines) + "\n")
+        return str(p)
+
+    assert bench.record_traffic_gdn(log(3, "gdn"), "cmd") == 0
+    big = bench.GDN_ROOFLINE_SCENARIO
+    assert bench.recorded_traffic(big, "ncu_traffic_gdn.json", bench.GDN_KERNEL_SOURCES) == \
+        1010 + 2020 + 3030
+    assert bench.recorded_traffic(big, "ncu_traffic_gdn.json") is None   # another source set
+    assert bench.record_traffic_mx(log(2, "mx"), "cmd") == 0
+    assert bench.recorded_traffic("mx_step", "ncu_traffic_mx.json") == 1010 + 2020
+    with pytest.raises(SystemExit):
+        bench.record_traffic_mx(log(3, "mx3"))
