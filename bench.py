@@ -384,6 +384,28 @@ class ClockSampler:
 
 # ---- CPU oracle sample ----------------------------------------------------------------------
 
+def host_cpu() -> dict:
+    """The host's CPU model (lscpu, else /proc/cpuinfo) and logical CPU count."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                model = ln.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for ln in open("/proc/cpuinfo"):
+                if ln.lower().startswith(("model name", "cpu model")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return {"cpu_model": model, "nproc": os.cpu_count()}
+
+
 def oracle_sample(inputs, seconds_target, rng_seed=0):
     """Time the oracle on random output elements of each GEMM, sized to ~seconds_target.
     Returns (flops, seconds, description)."""
@@ -453,6 +475,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": cfg,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "host": host_cpu(),
                          "kind": "oracle",
                          "sample": f"per step, {desc} (binary64 dot products)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -1282,6 +1305,7 @@ def run_ours(args):
         oracle.build()
         f, s, desc = oracle_sample(inputs, args.cpu_seconds)
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+               "host": host_cpu(),
                "kind": "oracle", "sample": desc + " (binary64 dot products, OpenMP)",
                "seconds": s}
         if config_leg is not None:
