@@ -320,7 +320,8 @@ __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
 // run on the tensor cores (bf16 operands, exact products).  T = (I + L)^-1 is then built in the
 // page's doubling stages: the eight 8 x 8 diagonal blocks by substitution, then for block sizes
 // b = 8, 16, 32 each pair of neighbouring inverted blocks [A 0; C B] becomes
-// [A^-1 0; -B^-1 C A^-1  B^-1] (fp32 products).  Finally W = T diag(beta g) K and
+// [A^-1 0; -B^-1 C A^-1  B^-1] (fp32 dot products for b = 8; for b = 16 and 32 tensor-core
+// products of three-piece bfloat16 operands, at fp32 accuracy).  Finally W = T diag(beta g) K and
 // U' = T diag(beta) V run on the tensor cores: T diag(.) as three bfloat16 pieces against the
 // exact bfloat16 K or V, the three products keeping fp32 accuracy.
 constexpr int kRowA = 72;      // padded bf16 rows of A' staging (144 bytes)
@@ -386,6 +387,68 @@ __device__ __forceinline__ void invert_doubling_stage(const float* Ls, float* Ts
         for (int u = 0; u < U; ++u) acc[u] = -acc[u];
         *reinterpret_cast<Vec*>(Ts + (r0 + b + i) * kRowL + r0 + U * l8) =
             *reinterpret_cast<const Vec*>(acc);
+    }
+    __syncthreads();
+}
+
+// The same doubling stage on the tensor cores, for b = 16 and 32: both products of a pair run as
+// mma.sync m16n8k16 with each fp32 operand split into three bfloat16 pieces, keeping the six
+// piece products above 2^-16 of the leading one (so the sum keeps fp32 accuracy).  Warp w owns
+// output tile w of the stage: (pair, 16-row tile, 8-column tile); with b = 16 the four tiles
+// leave warps 4-7 idle.  Y goes through the scratch rows as in the scalar stage.
+template <int b>
+__device__ __forceinline__ void invert_doubling_stage_tc(const float* Ls, float* Ts, float* Yb,
+                                                         int tid)
+{
+    static_assert(b == 16 || b == 32, "tensor-core doubling stages are 16 and 32 wide");
+    constexpr int kNT = b / 8;                 // 8-column tiles per pair
+    constexpr int kTiles = (kC / (2 * b)) * (b / 16) * kNT;
+    const int warp = tid / 32, lane = tid % 32;
+    const int gq = lane >> 2, tg = lane & 3;
+    const bool active = warp < kTiles;
+    const int p = warp / ((b / 16) * kNT), mt = (warp / kNT) % (b / 16), nt = warp % kNT;
+    const int r0 = 2 * p * b;
+    // d = X Z over k = 0 .. b-1 for the warp's tile: X row-major fp32 (row stride xs), Z fp32
+    // read as Z[k][n] (row stride zs).  The piece products of each order (i + j = 0, 1, 2) have
+    // an accumulator of their own, so that no more than six MMAs wait on one another; the
+    // smaller orders are added first.
+    const auto product = [&](float (&d)[4], const float* X, int xs, const float* Z, int zs) {
+        float e[3][4] = {};
+#pragma unroll
+        for (int kk = 0; kk < b / 16; ++kk) {
+            const float* x0 = X + (16 * mt + gq) * xs + 16 * kk + 2 * tg;
+            const float2 v00 = *reinterpret_cast<const float2*>(x0);
+            const float2 v10 = *reinterpret_cast<const float2*>(x0 + 8 * xs);
+            const float2 v01 = *reinterpret_cast<const float2*>(x0 + 8);
+            const float2 v11 = *reinterpret_cast<const float2*>(x0 + 8 * xs + 8);
+            const float* z0 = Z + (16 * kk + 2 * tg) * zs + 8 * nt + gq;
+            const Pieces3 a0 = split3(v00.x, v00.y), a1 = split3(v10.x, v10.y);
+            const Pieces3 a2 = split3(v01.x, v01.y), a3 = split3(v11.x, v11.y);
+            const Pieces3 b0 = split3(z0[0], z0[zs]), b1 = split3(z0[8 * zs], z0[9 * zs]);
+            // pieces (i, j) with i + j <= 2
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+#pragma unroll
+                for (int j = 0; i + j < 3; ++j)
+                    mma_bf16(e[i + j], a0.p[i], a1.p[i], a2.p[i], a3.p[i], b0.p[j], b1.p[j]);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) d[r] = (e[2][r] + e[1][r]) + e[0][r];
+    };
+    if (active) {   // Y = C A^-1
+        float d[4];
+        product(d, Ls + (r0 + b) * kRowL + r0, kRowL, Ts + r0 * kRowL + r0, kRowL);
+        float* y = Yb + (p * b + 16 * mt + gq) * kRowY + 8 * nt + 2 * tg;
+        *reinterpret_cast<float2*>(y) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2*>(y + 8 * kRowY) = make_float2(d[2], d[3]);
+    }
+    __syncthreads();
+    if (active) {   // lower-left block = -B^-1 Y
+        float d[4];
+        product(d, Ts + (r0 + b) * kRowL + r0 + b, kRowL, Yb + p * b * kRowY, kRowY);
+        float* x = Ts + (r0 + b + 16 * mt + gq) * kRowL + r0 + 8 * nt + 2 * tg;
+        *reinterpret_cast<float2*>(x) = make_float2(-d[0], -d[1]);
+        *reinterpret_cast<float2*>(x + 8 * kRowL) = make_float2(-d[2], -d[3]);
     }
     __syncthreads();
 }
@@ -587,8 +650,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     __syncthreads();
     invert_doubling_stage<8>(Ls, Ts, Yb, tid);
-    invert_doubling_stage<16>(Ls, Ts, Yb, tid);
-    invert_doubling_stage<32>(Ls, Ts, Yb, tid);
+    invert_doubling_stage_tc<16>(Ls, Ts, Yb, tid);
+    invert_doubling_stage_tc<32>(Ls, Ts, Yb, tid);
 
     // ---- W = T diag(beta g) K (warps 0-3) and U' = T diag(beta) V (warps 4-7) ----
     // Warp w owns rows t of m-tile mt (the two halves take the tiles in opposite orders, so that
