@@ -540,6 +540,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
     }
     for (int e = tid; e < kC * kRowL; e += kPrepThreads) Ts[e] = 0.f;   // upper blocks stay zero
+    // the six 16 x 16 tiles of A' above the diagonal, both pieces: zero (16-byte stores)
+    for (int e = tid; e < 2 * 6 * 32; e += kPrepThreads) {
+        // upper tile u: row block 0, 0, 0, 1, 1, 2 and column block 1, 2, 3, 2, 3, 3 (4 bits each)
+        constexpr int kUpper = 0x123233;
+        const int pc = e / 192, u = (e % 192) / 32, r = (e % 32) / 2, hf = e % 2;
+        const int mi = u < 3 ? 0 : (u < 5 ? 1 : 2);
+        const int ni = (kUpper >> (4 * (5 - u))) & 15;
+        *reinterpret_cast<int4*>(Ap + pc * kC * kRowA + (16 * mi + r) * kRowA + 16 * ni + 8 * hf) =
+            make_int4(0, 0, 0, 0);
+    }
     if (tid < kC) {
         al[tid] = a_in;
         bt[tid] = b_in;
@@ -572,11 +582,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     if (tid < kC) bg[tid] = bt[tid] * g[tid];
 
     // K K^T and Q K^T on the tensor cores: mma.sync m16n8k16 with bf16 operands (exact products,
-    // fp32 sums).  Warp w owns rows 16 (w / 2) .. + 15 and columns 32 (w % 2) .. + 31 of both.
+    // fp32 sums).  Only the ten 16 x 16 tiles on or below the diagonal are needed (L is strictly
+    // lower, A' keeps s <= t; the six upper A' tiles were zeroed above).  Warps 0 and 1 take two
+    // tiles of row block 3 each, the others one tile, so that each scheduler's two warps (w and
+    // w + 4) carry three or two tiles.
     {
         const int warp = tid / 32, lane = tid % 32;
         const int gq = lane >> 2, tg = lane & 3;
-        const int m0 = 16 * (warp >> 1), nb = 32 * (warp & 1);
+        // per warp (4 bits each, warp 0 first): row block 3, 3, 2, 2, 2, 1, 1, 0 and first
+        // column block 0, 2, 0, 1, 2, 0, 1, 0
+        constexpr int kMi = 0x33222110, kNi = 0x02012010;
+        const int m0 = 16 * ((kMi >> (4 * (7 - warp))) & 15);
+        const int nb = 16 * ((kNi >> (4 * (7 - warp))) & 15);
+        const int ntiles = warp < 2 ? 2 : 1;
         float kk[4][4] = {}, qk[4][4] = {};
         const int lr = lane & 7, lb = lane >> 3;
 #pragma unroll
@@ -588,6 +606,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             ldsm_x4(qa, qb_s + aoff);
 #pragma unroll
             for (int np = 0; np < 2; ++np) {
+                if (np >= ntiles) break;
                 // B fragments of n-tiles 2 np, 2 np + 1: k rows n0 + lr, columns k0 + 8 (lb % 2)
                 uint32_t kb4[4];
                 ldsm_x4(kb4, kb_s + tsw(nb + 16 * np + 8 * (lb >> 1) + lr, k0 + 8 * (lb & 1), kC));
@@ -601,6 +620,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const float inv_gc = 1.f / g[kC - 1];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
+            if (nt >= 2 * ntiles) break;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int t = m0 + gq + 8 * h;
