@@ -68,6 +68,11 @@ def parse_args():
     p.add_argument("--sweep-processes", type=int, default=1,
                    help="run --sweep in this many fresh processes and report, per case, the "
                         "median of the per-process means")
+    p.add_argument("--fused-steps", type=int, default=100,
+                   help="steps of the fused leg: bf16 act(A B^T + bias) with GELU on the headline "
+                        "step's two shapes (0: skip)")
+    p.add_argument("--fused-act", default="gelu", choices=["none", "relu", "gelu"],
+                   help="activation of the fused leg")
     p.add_argument("--mx-steps", type=int, default=200,
                    help="steps of the block-scaled FP8 leg (8192^3 and MLP shapes; 0: skip)")
     p.add_argument("--mx-variant", type=int, default=0, help="block-scaled variant (0 = auto)")
@@ -511,6 +516,112 @@ def mx_launch(g, w, t, variant, stream):
                         stream.cuda_stream)
     if rc != g.OK:
         raise g.GemmError(rc, g.gemm_f16_last_error())
+
+
+def run_fused_leg(args, g, dev, stream, peak16, uuid):
+    """The fused linear layer, act(A B^T + bias) with bf16 A, B, bias and D and the exact GELU,
+    on the headline step's two shapes (the MLP up-projection with its bias and activation is the
+    case the fused epilogue is for), inputs resident, back-to-back launches timed with CUDA events
+    at the region's two ends, then each shape alone; cuBLAS on the same buffers for context."""
+    import torch
+    from blackwell_tensor_core_fp16_gb300.workloads import WORKLOADS as W, workload_inputs
+    work = []
+    for name in WORKLOADS:
+        w = W[name]
+        A, B = workload_inputs(w)
+        gen = torch.Generator(device="cpu")
+        gen.manual_seed(1000 + w.seed)
+        bias = (0.1 * torch.randn(w.N, generator=gen)).to(torch.bfloat16)
+        Ad, Bd, bd = (t.to(torch.bfloat16).to(dev) for t in (A, B, bias))
+        D = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+        work.append((w, Ad, Bd, bd, D))
+    del A, B
+
+    def launch(item):
+        w, Ad, Bd, bd, D = item
+        rc = g.gemm_f16_nt_fused(Ad.data_ptr(), Bd.data_ptr(), D.data_ptr(), w.M, w.N, w.K,
+                                 g.DTYPES["bf16"], bd.data_ptr(), g.ACTIVATIONS[args.fused_act],
+                                 0, 0, 0, stream.cuda_stream)
+        if rc != g.OK:
+            raise g.GemmError(rc, g.gemm_f16_last_error())
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            for item in work:
+                launch(item)
+    torch.cuda.synchronize()
+    K = args.fused_steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for _ in range(K):
+            for item in work:
+                launch(item)
+        ev[1].record(stream)
+    torch.cuda.synchronize()
+    clk = sampler.stop()
+    g.check_status(stream)
+    total = ev[0].elapsed_time(ev[1])
+    flops = sum(item[0].flops for item in work)
+    per = {}
+    for item in work:
+        w = item[0]
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s0.record(stream)
+            for _ in range(K):
+                launch(item)
+            s1.record(stream)
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(s1) / K
+        per[w.name] = {"M": w.M, "N": w.N, "K": w.K, "ms_per_launch": ms,
+                       "tflops": w.flops / (ms * 1e-3) / 1e12,
+                       "timing": "this shape alone, as many launches, after the timed region"}
+    g.check_status(stream)
+    achieved = K * flops / (total * 1e-3) / 1e12
+    # cuBLAS for context: one cuBLASLt call with its bias + GELU epilogue (its GELU is the tanh
+    # form) where torch offers it, else addmm followed by a separate GELU
+    cublas = None
+    try:
+        if hasattr(torch, "_addmm_activation"):
+            def ref_step():
+                for w, Ad, Bd, bd, D in work:
+                    torch._addmm_activation(bd, Ad, Bd.t(), use_gelu=True, out=D)
+            how = "torch._addmm_activation (cuBLASLt bias + GELU epilogue, tanh GELU)"
+        else:
+            def ref_step():
+                for w, Ad, Bd, bd, D in work:
+                    torch.nn.functional.gelu(torch.addmm(bd, Ad, Bd.t()), out=D)
+            how = "torch.addmm then torch.nn.functional.gelu (two kernels)"
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                ref_step()
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            c0.record(stream)
+            for _ in range(K):
+                ref_step()
+            c1.record(stream)
+        torch.cuda.synchronize()
+        cv = K * flops / (c0.elapsed_time(c1) * 1e-3) / 1e12
+        cublas = {"value": cv, "unit": "TFLOP/s", "steps": K, "call": how,
+                  "ours_over_cublas": achieved / cv}
+    except Exception as e:   # context only
+        cublas = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+    return {"metric": "fused linear layer TFLOP/s: bf16 act(A B^T + bias), bf16 out",
+            "activation": args.fused_act,
+            "value": achieved, "unit": "TFLOP/s", "steps": K, "per_workload": per,
+            "clocks": clk, "cublas_same_step": cublas,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak16,
+                         "unit": "TFLOP/s", "frac": achieved / peak16, "traffic": None,
+                         "peak_source": "measured bf16_tflops (burst): the leg's region is "
+                                        "well under a second"},
+            "gpu_launches": K * len(work) * 2 + max(3, args.warmup) * len(work)}
 
 
 def run_mx_leg(args, g, dev, stream, num_sms, peak16, uuid):
@@ -1296,6 +1407,9 @@ def run_ours(args):
     mx_leg = None
     if args.mx_steps > 0:
         mx_leg = run_mx_leg(args, g, dev, stream, num_sms, peak_burst, uuid)
+    fused_leg = None
+    if args.fused_steps > 0 and not args.only:
+        fused_leg = run_fused_leg(args, g, dev, stream, peak_burst, uuid)
     gdn_leg = run_gdn_leg(args, g, dev, stream, peak_burst, measured_hbm_gbs()) \
         if args.gdn_reps > 0 else None
 
@@ -1354,6 +1468,7 @@ def run_ours(args):
         "per_config": config_leg,
         "sustained": sustained,
         "mx_fp8": mx_leg,
+        "fused_bf16_gelu": fused_leg,
         "gdn_prefill": gdn_leg,
         "clocks": clock_info,
         "wall_s_timed_region": wall_s,

@@ -108,8 +108,10 @@ int gemm_f16_nt_variant(const void* A, const void* B, void* D, int64_t M, int64_
  * variant:    GEMM_F16_VARIANT_AUTO or one of the persistent variants (2, 3, 4).
  * workspace:  as gemm_f16_nt_ws (may be null).
  * The bias and the activation are applied in fp32 to the fp32 sum; the result is then rounded
- * once (round to nearest even) to the output type.  K must be at least 1.  Other rules and
- * return codes as gemm_f16_nt.
+ * once (round to nearest even) to the output type.  GELU is evaluated with a published
+ * Chebyshev fit of erfc (Numerical Recipes, section 6.2), within 2e-7 plus one fp32 rounding
+ * of the exact GELU for |y| <= 10 before that rounding.  K must be at least 1.  Other rules and return codes as
+ * gemm_f16_nt.
  */
 int gemm_f16_nt_fused(const void* A, const void* B, void* D, int64_t M, int64_t N, int64_t K,
                       int dtype, const void* bias, int activation, int variant, void* workspace,

@@ -577,3 +577,32 @@ def test_half_width_tail_rule():
     assert g.gemm_f16_half_tail_tiles(8, 76) == 8           # few tiles: all of them halved
     assert g.gemm_f16_half_tail_tiles(152, 76) == 0         # whole waves
     assert g.gemm_f16_half_tail_tiles(76 + 39, 76) == 0     # 2 x 39 > 76
+
+
+def test_gelu_erfc_fit_accuracy_in_fp32():
+    """The fused epilogue's GELU evaluates erfc with the Chebyshev fit of Numerical Recipes
+    (section 6.2): erfc(z) = t exp(-z^2 + P(t)), t = 1 / (1 + z/2), for z >= 0, and
+    Phi(x) = 1 - erfc(|x|/sqrt2)/2 (x >= 0) or erfc(|x|/sqrt2)/2 (x < 0).  The same steps in
+    float32 stay within 2e-7 (plus one fp32 rounding of the result) of the exact GELU (binary64
+    math.erfc) for |x| <= 10, and within 5e-6 relative for |x| <= 6; a wrong or missing
+    coefficient breaks both."""
+    import math
+    import numpy as np
+    f32 = np.float32
+    coef = [-1.26551223, 1.00002368, 0.37409196, 0.09678418, -0.18628806, 0.27886807,
+            -1.13520398, 1.48851587, -0.82215223, 0.17087277]
+    x = np.concatenate([np.linspace(-10, 10, 40001), np.linspace(-1e-3, 1e-3, 201)]).astype(f32)
+    z = np.abs(x) * f32(0.70710678118654752)
+    t = f32(1) / (f32(0.5) * z + f32(1))
+    p = np.full_like(t, f32(coef[9]))
+    for c in coef[8::-1]:
+        p = p * t + f32(c)
+    e = t * np.exp(-z * z + p)
+    got = x * np.where(x >= 0, f32(1) - f32(0.5) * e, f32(0.5) * e)
+    xd = x.astype(np.float64)
+    ref = np.array([v * 0.5 * math.erfc(-v / math.sqrt(2.0)) for v in xd])
+    err = np.abs(got.astype(np.float64) - ref)
+    bound = 2e-7 + 2.0 ** -23 * np.abs(ref)   # plus one fp32 rounding of the result
+    assert (err <= bound).all(), float((err / bound).max())
+    mid = (np.abs(xd) <= 6) & (ref != 0)
+    assert (err[mid] / np.abs(ref[mid])).max() < 5e-6
