@@ -1026,11 +1026,18 @@ def merge_config_processes(args, first):
     runs = [first]
     cmd = [sys.executable, os.path.abspath(__file__), "--config-only", "--config-ms",
            str(args.config_ms), "--cublas-steps", str(args.cublas_steps)]
+    failed = []
     for _ in range(args.config_processes - 1):
-        out = subprocess.run(cmd, check=True, capture_output=True, text=True).stdout
-        runs.append(json.loads([ln for ln in out.splitlines() if ln.startswith("{")][-1]))
+        try:
+            out = subprocess.run(cmd, check=True, capture_output=True, text=True,
+                                 timeout=600).stdout
+            runs.append(json.loads([ln for ln in out.splitlines() if ln.startswith("{")][-1]))
+        except Exception as e:   # the leg is extra: keep the processes that ran
+            failed.append(f"{type(e).__name__}: {e}"[:200])
     merged = dict(first)
     merged["processes"] = len(runs)
+    if failed:
+        merged["failed_processes"] = failed
     merged["timing"] = (first["timing"] + "; each figure is the median over " + str(len(runs)) +
                         " processes of the per-process means (listed per process)")
     cfgs = {}
