@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import importlib.util
 import io
+import json
 import os
 import socket
 import sys
@@ -204,3 +205,48 @@ def test_traffic_records_follow_their_kernel_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("mx_step", "ncu_traffic_mx.json") == 1010 + 2020
     with pytest.raises(SystemExit):
         bench.record_traffic_mx(log(3, "mx3"))
+
+
+def test_per_config_processes_take_the_median(monkeypatch):
+    """The per_config leg's figures are the median over its processes of the per-process means;
+    a child process that fails leaves the leg with the ones that ran (and says so)."""
+    bench = load_bench()
+
+    def leg(us, graph, cold):
+        c = {"M": 2048, "N": 2048, "K": 2048, "us_per_launch": us, "us_per_launch_graph": graph,
+             "cold_l2_us_per_launch": cold, "cublas_us_per_launch_graph_context": None,
+             "tflops": 2 * 2048 ** 3 / (us * 1e-6) / 1e12, "frac_of_burst": 0.5,
+             "hbm_gbs_algorithmic": 100.0, "hbm_frac": 0.01}
+        return {"timing": "t", "configs": {"square_2048": c}, "gpu_launches": 10}
+
+    children = [leg(14.0, 13.0, 18.0), leg(16.0, 15.0, 20.0)]
+
+    class Done:
+        def __init__(self, out):
+            self.stdout = out
+
+    def fake_run(cmd, **kw):
+        if not children:
+            raise RuntimeError("child failed")
+        return Done("noise\n" + json.dumps(children.pop(0)) + "\n")
+
+    monkeypatch.setattr(bench.subprocess, "run", fake_run)
+
+    class Args:
+        config_ms = 1.0
+        cublas_steps = 0
+        config_processes = 3
+
+    got = bench.merge_config_processes(Args(), leg(12.0, 11.0, 30.0))
+    c = got["configs"]["square_2048"]
+    assert got["processes"] == 3 and "failed_processes" not in got
+    assert c["us_per_launch"] == 14.0 and c["us_per_launch_per_process"] == [12.0, 14.0, 16.0]
+    assert c["us_per_launch_graph"] == 13.0 and c["cold_l2_us_per_launch"] == 20.0
+    assert c["tflops"] == pytest.approx(2 * 2048 ** 3 / 14e-6 / 1e12)
+    assert c["frac_of_burst"] == pytest.approx(0.5 * 12.0 / 14.0)
+    assert got["gpu_launches"] == 30
+    # one child fails: two processes remain, and the failure is reported
+    children[:] = [leg(14.0, 13.0, 18.0)]
+    got = bench.merge_config_processes(Args(), leg(12.0, 11.0, 30.0))
+    assert got["processes"] == 2 and len(got["failed_processes"]) == 1
+    assert got["configs"]["square_2048"]["us_per_launch"] == 13.0
